@@ -1,0 +1,222 @@
+/*
+ * poetx.h -- C ABI of the POET-X layer library for NVIDIA GB300 (sm_103a).
+ *
+ * The library computes one POET-X layer forward and backward:
+ *   - the Cayley-Neumann parameterization (CNP) that turns the stored upper triangle of a
+ *     skew-symmetric Q into each b x b orthogonal block G = I + 2(Q + Q^2 + Q^3) + Q^4
+ *     (POET-X summary page, "Core method" section 4, eq. 9; the gradient is eq. 10),
+ *   - the input-centric chain z = G_P^T (W' (G_R^T x)) with the permutations applied as
+ *     index remaps and merged into the frozen weight W' = Phi_n^T W0 Phi_m
+ *     (same page, sections 1-3, eq. 3),
+ *   - the backward in a "fast" variant that keeps b = W'a and a "mem" variant that
+ *     recomputes it (same page, section 5), with an int8 frozen weight for the mem variant
+ *     (same page, section 6, POET-XQ).
+ * "POET-X summary page" is the summary of arXiv 2603.05500, "POET-X: Memory-efficient LLM
+ * Training by Scaling Orthogonal Transformation".
+ *
+ * Conventions shared by every entry point
+ *   - Row-vector batches, row-major, no padding: an activation is [N, D] with D contiguous.
+ *     W0 and W' are [n_out, m_in] (PyTorch Linear layout).  G_R acts on the m_in side
+ *     (m/b blocks), G_P on the n_out side (n/b blocks); Q = 0 gives y = x W0^T.
+ *   - Packed triangle q of a block: b(b-1)/2 fp32 values of the strict upper triangle in
+ *     row-major order (0,1),(0,2),...,(0,b-1),(1,2),...; Q = U - U^T.
+ *   - Permutations are int32 gather indices: x~[:, i] = x[:, perm[i]], each a permutation
+ *     of 0..D-1 (not checked on the device; an out-of-range index is undefined behaviour).
+ *   - Every pointer is a DEVICE pointer unless stated otherwise, owned by the caller, and
+ *     must be 16-byte aligned.  The library never allocates device memory: scratch space
+ *     is passed in as (ws, ws_bytes), sized by the matching *_workspace_bytes() call.
+ *   - Calls are asynchronous on the given stream (NULL = legacy default stream).  Argument
+ *     errors are returned synchronously before anything is launched.  Errors seen on the
+ *     device (a bounded wait that expired) are recorded in a device error word and returned
+ *     by poetx_get_device_error().  Results are deterministic: equal inputs give bitwise
+ *     equal outputs.
+ *   - N = 0 (no tokens) is valid and launches nothing except, where a gradient is produced,
+ *     the zeroing of that gradient.
+ */
+#ifndef POETX_H
+#define POETX_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  POETX_OK = 0,
+  POETX_ERR_ARG = 1,         /* NULL where a pointer is required, negative size, bad enum */
+  POETX_ERR_SHAPE = 2,       /* b does not divide m or n, b outside the supported set */
+  POETX_ERR_DTYPE = 3,       /* unsupported dtype combination */
+  POETX_ERR_ALIGN = 4,       /* pointer not 16-byte aligned */
+  POETX_ERR_WORKSPACE = 5,   /* ws_bytes smaller than the *_workspace_bytes() answer */
+  POETX_ERR_UNSUPPORTED = 6, /* Neumann order other than 3, int8 weight with the fast variant */
+  POETX_ERR_TIMEOUT = 7,     /* a bounded wait inside a kernel expired (device error word) */
+  POETX_ERR_CUDA = 8         /* a CUDA runtime call failed (launch, attribute, tensor map) */
+} poetx_status;
+
+typedef enum { POETX_F32 = 0, POETX_BF16 = 1, POETX_I8 = 2 } poetx_dtype;
+typedef enum { POETX_FAST = 0, POETX_MEM = 1 } poetx_variant;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* poetx_status_str(poetx_status st);
+
+/* Synchronizes the stream, reads and clears the device error word.  POETX_OK if no kernel
+ * recorded an error since the last call; POETX_ERR_TIMEOUT if a bounded wait expired. */
+poetx_status poetx_get_device_error(cudaStream_t stream);
+
+/* Self-test of the bounded-wait machinery: launches one block that waits on a shared-memory
+ * barrier nothing arrives on, with a limit of timeout_us microseconds; the kernel records
+ * POETX_ERR_TIMEOUT in the device error word and returns.  No fault, no hang. */
+poetx_status poetx_selftest_timeout(unsigned int timeout_us, cudaStream_t stream);
+
+/* Diagnostic switch for the bf16 products: engine 0 (default) runs them on the tcgen05
+ * tensor cores where the GPU and the shape allow, engine 1 forces the CUDA-core kernels
+ * (fp32 accumulation, same rounding of the stored results).  Process-wide. */
+poetx_status poetx_set_gemm_engine(int engine);
+
+/* ----------------------------------------------------------------------------------------
+ * Cayley-Neumann parameterization (POET-X summary page, "Core method" section 4)
+ * ------------------------------------------------------------------------------------- */
+
+/* Bytes of scratch for poetx_cnp_fwd (phase 0) or poetx_cnp_bwd (phase 1) over nblk
+ * blocks of size b.  Returns 0 for invalid sizes. */
+size_t poetx_cnp_workspace_bytes(int nblk, int b, int phase);
+
+/* Forward CNP, eq. 9, in fp32: for every block j, G_j = I + 2(Q_j + Q_j^2 + Q_j^3) + Q_j^4.
+ *   q       [nblk, b(b-1)/2] fp32 packed triangles (input)
+ *   order   Neumann order; only 3 is accepted (POETX_ERR_UNSUPPORTED otherwise)
+ *   G_f32   [nblk, b, b] fp32 output, row-major (nullable)
+ *   G_bf16  [nblk, b, b] bf16 output (round-to-nearest-even of the fp32 G), row-major
+ *           (nullable)
+ *   Gt_bf16 [nblk, b, b] bf16 output holding each G_j transposed (nullable)
+ *   ws      scratch of poetx_cnp_workspace_bytes(nblk, b, 0) bytes
+ * 2 <= b <= 1024.  At least one output must be non-NULL. */
+poetx_status poetx_cnp_fwd(const float* q, int nblk, int b, int order, float* G_f32,
+                           void* G_bf16, void* Gt_bf16, void* ws, size_t ws_bytes,
+                           cudaStream_t stream);
+
+/* Backward CNP (eq. 10 is named on the page, not printed; derived by the chain rule):
+ *   dG      [splits, nblk, b, b] fp32 partial gradients dL/dG; the gradient is their sum,
+ *           taken in a fixed order (splits >= 1)
+ *   dq      [nblk, b(b-1)/2] fp32 output dL/dq; with accumulate != 0 the result is added
+ *           to the existing contents, else they are overwritten
+ *   ws      scratch of poetx_cnp_workspace_bytes(nblk, b, 1) bytes */
+poetx_status poetx_cnp_bwd(const float* q, const float* dG, int splits, int nblk, int b,
+                           int order, float* dq, int accumulate, void* ws, size_t ws_bytes,
+                           cudaStream_t stream);
+
+/* Step S1 on its own: Q_f32 [nblk, b, b] = unpacked skew blocks of q. */
+poetx_status poetx_triu_unpack(const float* q, int nblk, int b, float* Q_f32,
+                               cudaStream_t stream);
+
+/* Gradient of S1 on its own: dq[k] (+)= Qbar[i,j] - Qbar[j,i] for the k-th pair (i<j). */
+poetx_status poetx_triu_grad_pack(const float* Qbar, int nblk, int b, float* dq,
+                                  int accumulate, cudaStream_t stream);
+
+/* ----------------------------------------------------------------------------------------
+ * Permutations as index remaps (POET-X summary page, "Core method" section 2)
+ * ------------------------------------------------------------------------------------- */
+
+/* Y[t, i] = X[t, perm[i]] for t < N, i < D.  dt: POETX_F32, POETX_BF16 or POETX_I8.
+ * X and Y must not overlap.  D * sizeof(dt) must be a multiple of 16. */
+poetx_status poetx_perm_gather(poetx_dtype dt, const void* X, int N, int D,
+                               const int32_t* perm, void* Y, cudaStream_t stream);
+
+/* Y[t, perm[i]] = X[t, i] (the inverse remap).  Same rules as poetx_perm_gather. */
+poetx_status poetx_perm_scatter(poetx_dtype dt, const void* X, int N, int D,
+                                const int32_t* perm, void* Y, cudaStream_t stream);
+
+/* Merge of the two permutations into the frozen weight, once per draw of the permutations:
+ *   Wp[r, c] = W0[perm_n[r], perm_m[c]]          W0, Wp: [n, m] of dtype dt
+ *   scale_p[r] = scale[perm_n[r]]                when dt == POETX_I8 (scale, scale_p: [n] fp32)
+ * Bit-exact data movement. */
+poetx_status poetx_merge_perm(const void* W0, const float* scale, poetx_dtype dt, int n, int m,
+                              const int32_t* perm_n, const int32_t* perm_m, void* Wp,
+                              float* scale_p, cudaStream_t stream);
+
+/* Per-output-row symmetric int8 quantisation of an fp32 weight (POET-XQ storage; the page
+ * says only "low-bit W", the scheme is this library's reading):
+ *   scale[r] = max_c |W[r,c]| / 127 in fp32 (1 for an all-zero row),
+ *   Wq[r,c]  = clamp(round_half_even(W[r,c] / scale[r]), -127, 127), quotient in fp32. */
+poetx_status poetx_quantize_rows_int8(const float* W, int n, int m, int8_t* Wq, float* scale,
+                                      cudaStream_t stream);
+
+/* ----------------------------------------------------------------------------------------
+ * Batched block-diagonal products (POET-X summary page, "Core method" section 3)
+ * ------------------------------------------------------------------------------------- */
+
+/* Y[:, jb:(j+1)b] = X[:, jb:(j+1)b] . op(G_j) for j < nblk, op = identity (trans == 0) or
+ * transpose (trans != 0); optional column scale: Y[:, c] *= col_scale[c] (nullable).
+ *   dt      POETX_BF16 (X, G, Y bf16; fp32 accumulation; Y rounded to nearest even)
+ *           or POETX_F32 (all fp32)
+ *   X, Y    [N, nblk*b];  G [nblk, b, b] row-major
+ * bf16 requires b in {64, 128, 256, 512}. */
+poetx_status poetx_blockdiag_mm(poetx_dtype dt, const void* X, int N, int nblk, int b,
+                                const void* G, int trans, const float* col_scale, void* Y,
+                                cudaStream_t stream);
+
+/* Weight gradient of Y = X . blkdiag(G): dG[s, j] = X_j^T dY_j summed over the tokens of
+ * split s.  Tokens are cut into `splits` contiguous ranges of chunk = 64*ceil(N/(64*splits))
+ * tokens (the last ones may be short or empty, giving zero partials).
+ *   X, dY   [N, nblk*b] of dtype dt;  dG [splits, nblk, b, b] fp32 output */
+poetx_status poetx_blockdiag_wgrad(poetx_dtype dt, const void* X, const void* dY, int N,
+                                   int nblk, int b, int splits, float* dG,
+                                   cudaStream_t stream);
+
+/* The frozen-weight contraction (POET-X summary page, "Core method" section 1, b = W'a):
+ *   trans == 0:  C[N, n] = A[N, m] . W^T      (forward; int8: C[:, r] *= w_scale[r])
+ *   trans != 0:  C[N, m] = A[N, n] . W        (backward; int8: A must already carry the
+ *                                              per-row scale, i.e. A = dB . diag(w_scale))
+ *   act     POETX_BF16 or POETX_F32 (A and C);  wdt: POETX_BF16, POETX_F32 or POETX_I8
+ *   W       [n, m] row-major;  w_scale [n] fp32 (required when wdt == POETX_I8, else NULL) */
+poetx_status poetx_wprime_gemm(poetx_dtype act, poetx_dtype wdt, const void* A, int N, int m,
+                               int n, const void* W, const float* w_scale, int trans, void* C,
+                               cudaStream_t stream);
+
+/* ----------------------------------------------------------------------------------------
+ * The whole layer (POET-X summary page, "Core method" sections 1-6)
+ * ------------------------------------------------------------------------------------- */
+typedef struct poetx_layer {
+  int m;                   /* in-features (x has m columns) */
+  int n;                   /* out-features (y has n columns) */
+  int b;                   /* block size: b | m, b | n; bf16: b in {64,128,256,512} */
+  int order;               /* Neumann order; must be 3 */
+  poetx_dtype act;         /* POETX_F32 or POETX_BF16: x, y, dy, dx */
+  poetx_dtype wdt;         /* POETX_F32 (with act F32), POETX_BF16, or POETX_I8 (act BF16,
+                              variant MEM) */
+  poetx_variant variant;   /* POETX_FAST keeps B = A W'^T between fwd and bwd; POETX_MEM
+                              recomputes it */
+  const int32_t* perm_m;   /* [m] */
+  const int32_t* perm_n;   /* [n] */
+  const void* Wp;          /* merged frozen weight [n, m] of dtype wdt (poetx_merge_perm) */
+  const float* w_scale;    /* [n] per-row scale of Wp when wdt == POETX_I8, else NULL */
+  const float* q_R;        /* [m/b, b(b-1)/2] */
+  const float* q_P;        /* [n/b, b(b-1)/2] */
+} poetx_layer;
+
+/* Scratch bytes for poetx_layer_fwd (phase 0) or poetx_layer_bwd (phase 1) at N tokens;
+ * 0 if the descriptor is invalid. */
+size_t poetx_layer_workspace_bytes(const poetx_layer* L, int N, int phase);
+
+/* Bytes the caller keeps from poetx_layer_fwd to poetx_layer_bwd ("saved"): the bf16 (or
+ * fp32) blocks G_R, G_P and the fp32 Q_R^2, Q_P^2 (O((m+n) b), independent of N), plus,
+ * for POETX_FAST only, B = A W'^T ([N, n] of dtype act). */
+size_t poetx_layer_saved_bytes(const poetx_layer* L, int N);
+
+/* Forward: y [N, n] = layer(x [N, m]).  Runs both CNPs, writes `saved` for the backward. */
+poetx_status poetx_layer_fwd(const poetx_layer* L, const void* x, int N, void* y, void* saved,
+                             void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Backward from dy [N, n]: dx [N, m], dq_R [m/b, b(b-1)/2], dq_P [n/b, b(b-1)/2] (fp32;
+ * accumulate != 0 adds to them).  `saved` must come from poetx_layer_fwd with the same L,
+ * x and N; the mem variant recomputes B from x. */
+poetx_status poetx_layer_bwd(const poetx_layer* L, const void* x, const void* dy, int N,
+                             const void* saved, void* dx, float* dq_R, float* dq_P,
+                             int accumulate, void* ws, size_t ws_bytes, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* POETX_H */

@@ -1,0 +1,91 @@
+// Status strings, the per-device error word and the bounded-wait self test.
+#include <mutex>
+
+#include "common.cuh"
+
+namespace poetx {
+
+// One error word per device; kernels receive its address as a parameter and record the
+// first error with an atomic compare-and-swap.
+static __device__ int g_error_word;
+
+static std::mutex g_mu;
+static int* g_err_ptr[64];
+static int g_sms[64];
+
+int* device_error_word() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_err_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return nullptr;
+    g_err_ptr[dev] = static_cast<int*>(p);
+  }
+  return g_err_ptr[dev];
+}
+
+int sm_count() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_sms[dev]) {
+    int v = 0;
+    cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+    g_sms[dev] = v > 0 ? v : 148;
+  }
+  return g_sms[dev];
+}
+
+// Waits on a shared-memory barrier that nothing arrives on, for at most limit_ns, then
+// records the timeout and returns.
+__global__ void selftest_timeout_kernel(int* err, unsigned long long limit_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_wait_bounded(&bar, 0, err, limit_ns);
+  __syncthreads();
+}
+
+}  // namespace poetx
+
+using namespace poetx;
+
+extern "C" const char* poetx_status_str(poetx_status st) {
+  switch (st) {
+    case POETX_OK: return "POETX_OK";
+    case POETX_ERR_ARG: return "POETX_ERR_ARG: invalid argument";
+    case POETX_ERR_SHAPE: return "POETX_ERR_SHAPE: unsupported or inconsistent shape";
+    case POETX_ERR_DTYPE: return "POETX_ERR_DTYPE: unsupported dtype";
+    case POETX_ERR_ALIGN: return "POETX_ERR_ALIGN: pointer not 16-byte aligned";
+    case POETX_ERR_WORKSPACE: return "POETX_ERR_WORKSPACE: workspace too small";
+    case POETX_ERR_UNSUPPORTED: return "POETX_ERR_UNSUPPORTED: unsupported option";
+    case POETX_ERR_TIMEOUT: return "POETX_ERR_TIMEOUT: a bounded device wait expired";
+    case POETX_ERR_CUDA: return "POETX_ERR_CUDA: CUDA runtime error";
+  }
+  return "POETX_UNKNOWN_STATUS";
+}
+
+extern "C" poetx_status poetx_get_device_error(cudaStream_t stream) {
+  int* w = device_error_word();
+  if (!w) return POETX_ERR_CUDA;
+  int host = 0;
+  POETX_CUDA_TRY(cudaStreamSynchronize(stream));
+  POETX_CUDA_TRY(cudaMemcpy(&host, w, sizeof(int), cudaMemcpyDeviceToHost));
+  if (host != 0) {
+    const int zero = 0;
+    POETX_CUDA_TRY(cudaMemcpy(w, &zero, sizeof(int), cudaMemcpyHostToDevice));
+  }
+  return static_cast<poetx_status>(host);
+}
+
+extern "C" poetx_status poetx_selftest_timeout(unsigned int timeout_us, cudaStream_t stream) {
+  int* w = device_error_word();
+  if (!w) return POETX_ERR_CUDA;
+  selftest_timeout_kernel<<<1, 32, 0, stream>>>(w, 1000ull * timeout_us);
+  POETX_CUDA_TRY(cudaGetLastError());
+  return POETX_OK;
+}

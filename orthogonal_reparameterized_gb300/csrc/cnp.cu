@@ -1,0 +1,287 @@
+// Cayley-Neumann parameterization (CNP), forward and backward, in fp32 on the CUDA cores.
+//
+// POET-X summary page ("POET-X: Memory-efficient LLM Training by Scaling Orthogonal
+// Transformation"), "Core method" section 4: G = (I + Q)(I + Q + Q^2 + Q^3), rewritten in
+// eq. 9 as G = I + 2(Q + Q^2 + Q^2 Q) + Q^2 Q^2, so that forward and backward need only Q
+// and Q^2; Q is skew-symmetric and only its upper triangle is stored.
+//
+// Every product here is a batched b x b fp32 GEMM (one batch entry per block) whose
+// operands are linear combinations of at most two b x b arrays, staged tile by tile in
+// shared memory, and whose epilogue adds linear combinations of b x b arrays and of I:
+//
+//   forward   Q2 = Q Q                                     (symmetric: upper tiles only)
+//             G  = Q2 (2Q + Q2) + I + 2Q + 2Q2             = I + 2(Q+Q^2+Q^3) + Q^4
+//   backward  X  = sum of the dG partials (fixed order)
+//             M1 = X P + P X                 with P = Q^T = -Q
+//             Qbar = (2X + M1) Q2 + (Q2 - 2Q) M1 + 2X + 2M1
+//             dq_ij = Qbar_ij - Qbar_ji
+//
+// The backward is the adjoint of eq. 9 (eq. 10 on the page is named but not printed):
+// with c = (2, 2, 2, 1) the adjoint of sum_k c_k Q^k at dG = X is
+// Qbar = sum_k c_k sum_{s+t=k-1} P^s X P^t, which factors as
+// (XS + SX) T + S^2 (XP + PX) with S = I + P, T = I + P^2 = I + Q2, S^2 = I - 2Q + Q2;
+// expanding the products gives the expression above.  Work per block: forward 3 b^3 FMA
+// (Q2 half by symmetry, then one full product), backward 5 b^3 FMA.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace poetx {
+
+namespace {
+
+struct Operand {
+  const float* p1;
+  float c1;
+  const float* p2;  // nullable
+  float c2;
+};
+
+struct CnpGemm {
+  int b;
+  int nseg;
+  Operand A[2], B[2];
+  const float* E1;  // epilogue terms (nullable)
+  float e1;
+  const float* E2;
+  float e2;
+  float eI;
+  int mirror;  // result is symmetric: compute tiles ti <= tj only and mirror them
+  float* out_f32;
+  __nv_bfloat16* out_bf16;
+  __nv_bfloat16* out_bf16_t;
+};
+
+constexpr int TK = 16;
+
+__device__ __forceinline__ float op_load(const Operand& o, long long idx) {
+  float v = o.c1 * o.p1[idx];
+  if (o.p2) v = fmaf(o.c2, o.p2[idx], v);
+  return v;
+}
+
+template <int T>
+__global__ void __launch_bounds__((T / 4) * (T / 4)) cnp_gemm_kernel(CnpGemm g) {
+  constexpr int NT = (T / 4) * (T / 4);
+  constexpr int TPR = T / 4;  // threads per row of the thread grid
+  __shared__ float As[TK][T + 4];
+  __shared__ float Bs[TK][T + 4];
+  const int ti = blockIdx.y, tj = blockIdx.x;
+  if (g.mirror && ti > tj) return;
+  const int b = g.b;
+  const long long base = (long long)blockIdx.z * b * b;
+  const int i0 = ti * T, j0 = tj * T;
+  const int tid = threadIdx.x;
+  const int tx = tid % TPR, ty = tid / TPR;
+
+  float acc[4][4] = {};
+  for (int seg = 0; seg < g.nseg; ++seg) {
+    const Operand oa = g.A[seg], ob = g.B[seg];
+    for (int k0 = 0; k0 < b; k0 += TK) {
+#pragma unroll
+      for (int r = 0; r < (T * TK) / NT; ++r) {
+        const int e = tid + r * NT;
+        const int ii = e / TK, kk = e % TK;
+        const int gi = i0 + ii, gk = k0 + kk;
+        As[kk][ii] = (gi < b && gk < b) ? op_load(oa, base + (long long)gi * b + gk) : 0.f;
+      }
+#pragma unroll
+      for (int r = 0; r < (T * TK) / NT; ++r) {
+        const int e = tid + r * NT;
+        const int kk = e / T, jj = e % T;
+        const int gj = j0 + jj, gk = k0 + kk;
+        Bs[kk][jj] = (gj < b && gk < b) ? op_load(ob, base + (long long)gk * b + gj) : 0.f;
+      }
+      __syncthreads();
+#pragma unroll
+      for (int kk = 0; kk < TK; ++kk) {
+        const float4 a4 = *reinterpret_cast<const float4*>(&As[kk][ty * 4]);
+        const float4 b4 = *reinterpret_cast<const float4*>(&Bs[kk][tx * 4]);
+        const float a[4] = {a4.x, a4.y, a4.z, a4.w};
+        const float c[4] = {b4.x, b4.y, b4.z, b4.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+#pragma unroll
+          for (int v = 0; v < 4; ++v) acc[u][v] = fmaf(a[u], c[v], acc[u][v]);
+      }
+      __syncthreads();
+    }
+  }
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const int i = i0 + ty * 4 + u;
+    if (i >= b) continue;
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+      const int j = j0 + tx * 4 + v;
+      if (j >= b) continue;
+      const long long idx = base + (long long)i * b + j;
+      float r = acc[u][v];
+      if (g.E1) r = fmaf(g.e1, g.E1[idx], r);
+      if (g.E2) r = fmaf(g.e2, g.E2[idx], r);
+      if (i == j) r += g.eI;
+      const long long tidx = base + (long long)j * b + i;
+      if (g.out_f32) {
+        g.out_f32[idx] = r;
+        if (g.mirror && ti != tj) g.out_f32[tidx] = r;
+      }
+      if (g.out_bf16) g.out_bf16[idx] = __float2bfloat16_rn(r);
+      if (g.out_bf16_t) g.out_bf16_t[tidx] = __float2bfloat16_rn(r);
+    }
+  }
+}
+
+poetx_status launch_cnp_gemm(const CnpGemm& g, int nblk, cudaStream_t s) {
+  if (g.b >= 64) {
+    dim3 grid(ceil_div(g.b, 64), ceil_div(g.b, 64), nblk);
+    cnp_gemm_kernel<64><<<grid, 256, 0, s>>>(g);
+  } else {
+    dim3 grid(ceil_div(g.b, 32), ceil_div(g.b, 32), nblk);
+    cnp_gemm_kernel<32><<<grid, 64, 0, s>>>(g);
+  }
+  POETX_CUDA_TRY(cudaGetLastError());
+  return POETX_OK;
+}
+
+Operand op1(const float* p, float c) { return Operand{p, c, nullptr, 0.f}; }
+Operand op2(const float* p, float c, const float* q, float d) { return Operand{p, c, q, d}; }
+
+// X = sum_s dG[s] in the order s = 0, 1, ..., S-1.
+__global__ void sum_partials_kernel(const float* __restrict__ dG, int S, long long n,
+                                    float* __restrict__ X) {
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
+       i += (long long)gridDim.x * blockDim.x) {
+    float a = dG[i];
+    for (int s = 1; s < S; ++s) a += dG[(long long)s * n + i];
+    X[i] = a;
+  }
+}
+
+size_t blk_bytes(int nblk, int b) { return align_up((size_t)nblk * b * b * sizeof(float), 256); }
+
+}  // namespace
+
+size_t cnp_fwd_scratch_bytes(int nblk, int b) { return 2 * blk_bytes(nblk, b); }
+size_t cnp_bwd_scratch_bytes(int nblk, int b) { return 5 * blk_bytes(nblk, b); }
+
+poetx_status cnp_forward(const float* q, int nblk, int b, float* Qs, float* Q2, float* G_f32,
+                         void* G_bf16, void* Gt_bf16, cudaStream_t s) {
+  if (nblk == 0) return POETX_OK;
+  POETX_TRY(launch_triu_unpack(q, nblk, b, Qs, s));
+  CnpGemm g{};
+  g.b = b;
+  g.nseg = 1;
+  g.A[0] = op1(Qs, 1.f);
+  g.B[0] = op1(Qs, 1.f);
+  g.mirror = 1;
+  g.out_f32 = Q2;
+  POETX_TRY(launch_cnp_gemm(g, nblk, s));
+  CnpGemm h{};
+  h.b = b;
+  h.nseg = 1;
+  h.A[0] = op1(Q2, 1.f);
+  h.B[0] = op2(Qs, 2.f, Q2, 1.f);
+  h.E1 = Qs;
+  h.e1 = 2.f;
+  h.E2 = Q2;
+  h.e2 = 2.f;
+  h.eI = 1.f;
+  h.out_f32 = G_f32;
+  h.out_bf16 = static_cast<__nv_bfloat16*>(G_bf16);
+  h.out_bf16_t = static_cast<__nv_bfloat16*>(Gt_bf16);
+  return launch_cnp_gemm(h, nblk, s);
+}
+
+poetx_status cnp_backward(const float* q, const float* Q2in, const float* dG, int splits, int nblk,
+                          int b, float* dq, int accumulate, void* scratch, cudaStream_t s) {
+  if (nblk == 0) return POETX_OK;
+  char* w = static_cast<char*>(scratch);
+  const size_t bb = blk_bytes(nblk, b);
+  float* Qs = reinterpret_cast<float*>(w);
+  float* Q2 = reinterpret_cast<float*>(w + bb);
+  float* X = reinterpret_cast<float*>(w + 2 * bb);
+  float* M1 = reinterpret_cast<float*>(w + 3 * bb);
+  float* Qbar = reinterpret_cast<float*>(w + 4 * bb);
+  POETX_TRY(launch_triu_unpack(q, nblk, b, Qs, s));
+  if (!Q2in) {
+    CnpGemm g{};
+    g.b = b;
+    g.nseg = 1;
+    g.A[0] = op1(Qs, 1.f);
+    g.B[0] = op1(Qs, 1.f);
+    g.mirror = 1;
+    g.out_f32 = Q2;
+    POETX_TRY(launch_cnp_gemm(g, nblk, s));
+    Q2in = Q2;
+  }
+  const float* Xp = dG;
+  if (splits > 1) {
+    const long long n = (long long)nblk * b * b;
+    const int grid = (int)((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096);
+    sum_partials_kernel<<<grid, 256, 0, s>>>(dG, splits, n, X);
+    POETX_CUDA_TRY(cudaGetLastError());
+    Xp = X;
+  }
+  // M1 = X P + P X, P = -Q
+  CnpGemm m{};
+  m.b = b;
+  m.nseg = 2;
+  m.A[0] = op1(Xp, 1.f);
+  m.B[0] = op1(Qs, -1.f);
+  m.A[1] = op1(Qs, -1.f);
+  m.B[1] = op1(Xp, 1.f);
+  m.out_f32 = M1;
+  POETX_TRY(launch_cnp_gemm(m, nblk, s));
+  // Qbar = (2X + M1) Q2 + (Q2 - 2Q) M1 + 2X + 2M1
+  CnpGemm r{};
+  r.b = b;
+  r.nseg = 2;
+  r.A[0] = op2(Xp, 2.f, M1, 1.f);
+  r.B[0] = op1(Q2in, 1.f);
+  r.A[1] = op2(Q2in, 1.f, Qs, -2.f);
+  r.B[1] = op1(M1, 1.f);
+  r.E1 = Xp;
+  r.e1 = 2.f;
+  r.E2 = M1;
+  r.e2 = 2.f;
+  r.out_f32 = Qbar;
+  POETX_TRY(launch_cnp_gemm(r, nblk, s));
+  return launch_triu_grad_pack(Qbar, nblk, b, dq, accumulate, s);
+}
+
+}  // namespace poetx
+
+using namespace poetx;
+
+extern "C" size_t poetx_cnp_workspace_bytes(int nblk, int b, int phase) {
+  if (nblk < 0 || b < 2 || b > 1024) return 0;
+  return phase == 0 ? cnp_fwd_scratch_bytes(nblk, b) : cnp_bwd_scratch_bytes(nblk, b);
+}
+
+extern "C" poetx_status poetx_cnp_fwd(const float* q, int nblk, int b, int order, float* G_f32,
+                                      void* G_bf16, void* Gt_bf16, void* ws, size_t ws_bytes,
+                                      cudaStream_t stream) {
+  if (nblk < 0) return POETX_ERR_ARG;
+  if (b < 2 || b > 1024) return POETX_ERR_SHAPE;
+  if (order != 3) return POETX_ERR_UNSUPPORTED;
+  if (nblk == 0) return POETX_OK;
+  if (!q || (!G_f32 && !G_bf16 && !Gt_bf16)) return POETX_ERR_ARG;
+  if (!ws) return POETX_ERR_ARG;
+  if (ws_bytes < cnp_fwd_scratch_bytes(nblk, b)) return POETX_ERR_WORKSPACE;
+  if (!aligned16(ws) || !aligned16(q)) return POETX_ERR_ALIGN;
+  float* Qs = static_cast<float*>(ws);
+  float* Q2 = reinterpret_cast<float*>(static_cast<char*>(ws) + cnp_fwd_scratch_bytes(nblk, b) / 2);
+  return cnp_forward(q, nblk, b, Qs, Q2, G_f32, G_bf16, Gt_bf16, stream);
+}
+
+extern "C" poetx_status poetx_cnp_bwd(const float* q, const float* dG, int splits, int nblk, int b,
+                                      int order, float* dq, int accumulate, void* ws,
+                                      size_t ws_bytes, cudaStream_t stream) {
+  if (nblk < 0 || splits < 1) return POETX_ERR_ARG;
+  if (b < 2 || b > 1024) return POETX_ERR_SHAPE;
+  if (order != 3) return POETX_ERR_UNSUPPORTED;
+  if (nblk == 0) return POETX_OK;
+  if (!q || !dG || !dq || !ws) return POETX_ERR_ARG;
+  if (ws_bytes < cnp_bwd_scratch_bytes(nblk, b)) return POETX_ERR_WORKSPACE;
+  if (!aligned16(ws) || !aligned16(dG)) return POETX_ERR_ALIGN;
+  return cnp_backward(q, nullptr, dG, splits, nblk, b, dq, accumulate, ws, stream);
+}

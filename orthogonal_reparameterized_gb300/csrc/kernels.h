@@ -1,0 +1,68 @@
+// Internal host-side launchers shared between the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/poetx.h"
+
+namespace poetx {
+
+// ---- index.cu
+poetx_status launch_triu_unpack(const float* q, int nblk, int b, float* Q, cudaStream_t s);
+poetx_status launch_triu_grad_pack(const float* Qbar, int nblk, int b, float* dq, int accumulate,
+                                   cudaStream_t s);
+poetx_status launch_perm_rows(size_t esize, bool scatter, const void* X, long long N, int D,
+                              const int32_t* perm, void* Y, const int32_t* src_rows,
+                              const float* scale, float* scale_out, cudaStream_t s);
+poetx_status launch_quantize(const float* W, int n, int m, int8_t* Wq, float* scale,
+                             cudaStream_t s);
+
+// ---- simt_gemm.cu: generic strided batched GEMM on the CUDA cores (fp32 accumulation).
+// C[z][i][j] = colscale[j] * sum_k A(z,i,k) B(z,k,j), element (i,k) of batch z of A at
+// A[z*sab + i*sam + k*sak] (likewise B, C).  Batch index z = blockIdx.z / ksplit; the K range
+// of split s is [s*kchunk, min(K, (s+1)*kchunk)) and its output goes to C + s*scs.
+struct SimtGemm {
+  int M, N, K;
+  int batch;
+  const void* A;
+  long long sam, sak, sab;
+  const void* B;
+  long long sbk, sbn, sbb;
+  void* C;
+  long long scm, scn, scb;
+  const float* colscale;  // nullable, indexed by j + z*colscale_bstride
+  long long colscale_bstride;
+  int ksplit;
+  int kchunk;
+  long long scs;
+};
+poetx_status launch_simt_gemm(poetx_dtype ta, poetx_dtype tb, poetx_dtype tc, const SimtGemm& g,
+                              cudaStream_t s);
+
+// ---- cnp.cu
+size_t cnp_fwd_scratch_bytes(int nblk, int b);
+size_t cnp_bwd_scratch_bytes(int nblk, int b);
+// Forward CNP with caller-provided fp32 scratch Qs [nblk,b,b] and Q2 [nblk,b,b] (Q2 is an
+// output too: Q^2 of every block).
+poetx_status cnp_forward(const float* q, int nblk, int b, float* Qs, float* Q2, float* G_f32,
+                         void* G_bf16, void* Gt_bf16, cudaStream_t s);
+// Backward CNP.  Q2 may be a precomputed Q^2 (from cnp_forward) or NULL to recompute it
+// into the scratch.  scratch holds cnp_bwd_scratch_bytes(nblk, b) bytes.
+poetx_status cnp_backward(const float* q, const float* Q2, const float* dG, int splits, int nblk,
+                          int b, float* dq, int accumulate, void* scratch, cudaStream_t s);
+
+// ---- umma_gemm.cu: tcgen05 / TMA tensor-core GEMMs (bf16 in, fp32 accumulate)
+bool umma_supported();
+// Y = X . op(G) per block (bf16), op = identity (trans=0) or transpose; optional col scale.
+poetx_status umma_blockdiag(const void* X, long long N, int nblk, int b, const void* G, int trans,
+                            const float* col_scale, void* Y, cudaStream_t s);
+// C[N,n] = A[N,m] W^T (trans=0) or C[N,m] = A[N,n] W (trans=1), W [n,m] bf16.
+poetx_status umma_wprime(const void* A, long long N, int m, int n, const void* W,
+                         const float* w_scale, int trans, void* C, cudaStream_t s);
+// dG[s, j] = X_j^T dY_j over the tokens of split s (fp32 partials).
+poetx_status umma_wgrad(const void* X, const void* dY, long long N, int nblk, int b, int splits,
+                        float* dG, cudaStream_t s);
+
+}  // namespace poetx

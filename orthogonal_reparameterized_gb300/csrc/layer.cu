@@ -1,0 +1,339 @@
+// The POET-X layer forward and backward, and the step-level entry points of its products.
+//
+// POET-X summary page ("POET-X: Memory-efficient LLM Training by Scaling Orthogonal
+// Transformation"), "Core method":
+//   section 1 (eq. 3)  input-centric chain a = G_R^T x, b = W' a, z = G_P^T b, here in
+//                      row-vector form  x~ = x[:, pi_m];  A = x~ blkdiag(G_R);  B = A W'^T;
+//                      z~ = B blkdiag(G_P);  y[:, pi_n] = z~
+//   section 2          permutations as index remaps, merged into W' beforehand
+//   section 3          block-diagonal products as batched per-block GEMMs
+//   section 4          CNP forward/backward (cnp.cu)
+//   section 5          "fast" keeps B for the backward, "mem" recomputes it
+//   section 6          POET-XQ: int8 W' dequantised inside the contraction (mem only)
+// Backward (chain rule of the forward):  dz~ = dy[:, pi_n];  dG_P = B^T dz~ (per block);
+//   dB = dz~ blkdiag(G_P)^T;  dA = dB W';  dG_R = x~^T dA (per block);
+//   dx~ = dA blkdiag(G_R)^T;  dx[:, pi_m] = dx~;  dq = CNP backward of dG.
+// Host-side orchestration only: every step runs in this library's kernels on the caller's
+// stream; nothing is allocated.
+#include <atomic>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace poetx {
+
+static std::atomic<int> g_engine{0};  // 0: tensor cores where supported, 1: CUDA cores only
+
+static bool use_umma() { return g_engine.load() == 0 && umma_supported(); }
+
+static int wgrad_splits(long long N, int nblk, int b) {
+  const long long tiles = (long long)nblk * ((b + 127) / 128) * (b > 256 ? b / 256 : 1);
+  long long s = (2LL * sm_count() + tiles - 1) / tiles;
+  long long smax = N / 256;
+  if (smax < 1) smax = 1;
+  if (s > smax) s = smax;
+  if (s < 1) s = 1;
+  return (int)s;
+}
+
+static int wgrad_chunk(long long N, int splits) {
+  long long c = 64 * ((N + 64LL * splits - 1) / (64LL * splits));
+  return (int)(c < 64 ? 64 : c);
+}
+
+// ---------------------------------------------------------------- step implementations
+poetx_status blockdiag_impl(poetx_dtype dt, const void* X, long long N, int nblk, int b,
+                            const void* G, int trans, const float* col_scale, void* Y,
+                            cudaStream_t s) {
+  if (N == 0 || nblk == 0) return POETX_OK;
+  if (dt == POETX_BF16 && use_umma() && b % 64 == 0 && b <= 512)
+    return umma_blockdiag(X, N, nblk, b, G, trans, col_scale, Y, s);
+  const long long D = (long long)nblk * b;
+  SimtGemm g{};
+  g.M = (int)N; g.N = b; g.K = b; g.batch = nblk;
+  g.A = X; g.sam = D; g.sak = 1; g.sab = b;
+  g.B = G; g.sbk = trans ? 1 : b; g.sbn = trans ? b : 1; g.sbb = (long long)b * b;
+  g.C = Y; g.scm = D; g.scn = 1; g.scb = b;
+  g.colscale = col_scale; g.colscale_bstride = b;
+  g.ksplit = 1; g.kchunk = b;
+  return launch_simt_gemm(dt, dt, dt, g, s);
+}
+
+poetx_status wgrad_impl(poetx_dtype dt, const void* X, const void* dY, long long N, int nblk,
+                        int b, int splits, float* dG, cudaStream_t s) {
+  if (nblk == 0) return POETX_OK;
+  if (dt == POETX_BF16 && use_umma() && b % 64 == 0 && b <= 512)
+    return umma_wgrad(X, dY, N, nblk, b, splits, dG, s);
+  if (N == 0) {
+    POETX_CUDA_TRY(cudaMemsetAsync(dG, 0, (size_t)splits * nblk * b * b * sizeof(float), s));
+    return POETX_OK;
+  }
+  const long long D = (long long)nblk * b;
+  SimtGemm g{};
+  g.M = b; g.N = b; g.K = (int)N; g.batch = nblk;
+  g.A = X; g.sam = 1; g.sak = D; g.sab = b;
+  g.B = dY; g.sbk = D; g.sbn = 1; g.sbb = b;
+  g.C = dG; g.scm = b; g.scn = 1; g.scb = (long long)b * b;
+  g.ksplit = splits; g.kchunk = wgrad_chunk(N, splits);
+  g.scs = (long long)nblk * b * b;
+  // splits beyond the last token get an empty K range and write zeros
+  return launch_simt_gemm(dt, dt, POETX_F32, g, s);
+}
+
+poetx_status wprime_impl(poetx_dtype act, poetx_dtype wdt, const void* A, long long N, int m,
+                         int n, const void* W, const float* w_scale, int trans, void* C,
+                         cudaStream_t s) {
+  if (N == 0) return POETX_OK;
+  if (act == POETX_BF16 && wdt == POETX_BF16 && use_umma() && m % 256 == 0 && n % 256 == 0)
+    return umma_wprime(A, N, m, n, W, nullptr, trans, C, s);
+  SimtGemm g{};
+  g.M = (int)N; g.batch = 1; g.A = A; g.B = W; g.C = C;
+  g.ksplit = 1;
+  if (!trans) {
+    g.N = n; g.K = m;
+    g.sam = m; g.sak = 1;
+    g.sbk = 1; g.sbn = m;
+    g.scm = n; g.scn = 1;
+    g.colscale = wdt == POETX_I8 ? w_scale : nullptr;
+  } else {
+    g.N = m; g.K = n;
+    g.sam = n; g.sak = 1;
+    g.sbk = m; g.sbn = 1;
+    g.scm = m; g.scn = 1;
+  }
+  g.kchunk = g.K;
+  return launch_simt_gemm(act, wdt, act, g, s);
+}
+
+// ---------------------------------------------------------------- layer plumbing
+struct Plan {
+  // saved
+  size_t GR, GP, Q2R, Q2P, Bsv, saved_total;
+  // forward workspace
+  size_t f_Qs, f_xt, f_A, f_B, f_zt, fwd_total;
+  // backward workspace
+  size_t b_cnp, b_xt, b_dzt, b_A, b_B, b_dB, b_dA, b_dxt, b_dGP, b_dGR, bwd_total;
+  int splitsR, splitsP;
+};
+
+static poetx_status validate(const poetx_layer* L) {
+  if (!L) return POETX_ERR_ARG;
+  if (L->m <= 0 || L->n <= 0 || L->b <= 0) return POETX_ERR_ARG;
+  if (L->order != 3) return POETX_ERR_UNSUPPORTED;
+  if (L->m % L->b || L->n % L->b) return POETX_ERR_SHAPE;
+  if (L->act == POETX_F32) {
+    if (L->wdt != POETX_F32) return POETX_ERR_DTYPE;
+    if (L->b < 2 || L->b > 1024 || L->m % 4 || L->n % 4) return POETX_ERR_SHAPE;
+  } else if (L->act == POETX_BF16) {
+    if (L->wdt != POETX_BF16 && L->wdt != POETX_I8) return POETX_ERR_DTYPE;
+    if (L->b != 64 && L->b != 128 && L->b != 256 && L->b != 512) return POETX_ERR_SHAPE;
+    if (L->wdt == POETX_I8 && L->variant != POETX_MEM) return POETX_ERR_UNSUPPORTED;
+    if (L->wdt == POETX_I8 && !L->w_scale) return POETX_ERR_ARG;
+  } else {
+    return POETX_ERR_DTYPE;
+  }
+  if (L->variant != POETX_FAST && L->variant != POETX_MEM) return POETX_ERR_ARG;
+  if (!L->perm_m || !L->perm_n || !L->Wp || !L->q_R || !L->q_P) return POETX_ERR_ARG;
+  if (!aligned16(L->Wp)) return POETX_ERR_ALIGN;
+  return POETX_OK;
+}
+
+static Plan make_plan(const poetx_layer* L, long long N) {
+  Plan p{};
+  const size_t as = dtype_size(L->act);
+  const size_t gs = L->act == POETX_F32 ? 4 : 2;
+  const size_t m = L->m, n = L->n, b = L->b;
+  size_t o = 0;
+  auto take = [&](size_t bytes) { size_t r = o; o += align_up(bytes, 256); return r; };
+  p.GR = take(m * b * gs);
+  p.GP = take(n * b * gs);
+  p.Q2R = take(m * b * 4);
+  p.Q2P = take(n * b * 4);
+  p.Bsv = L->variant == POETX_FAST ? take((size_t)N * n * as) : 0;
+  p.saved_total = o;
+
+  o = 0;
+  p.f_Qs = take((m > n ? m : n) * b * 4);
+  p.f_xt = take((size_t)N * m * as);
+  p.f_A = take((size_t)N * m * as);
+  p.f_B = L->variant == POETX_MEM ? take((size_t)N * n * as) : 0;
+  p.f_zt = take((size_t)N * n * as);
+  p.fwd_total = o;
+
+  p.splitsR = wgrad_splits(N, L->m / L->b, L->b);
+  p.splitsP = wgrad_splits(N, L->n / L->b, L->b);
+  o = 0;
+  p.b_cnp = take(cnp_bwd_scratch_bytes((int)((m > n ? m : n) / b), (int)b));
+  p.b_xt = take((size_t)N * m * as);
+  p.b_dzt = take((size_t)N * n * as);
+  p.b_A = L->variant == POETX_MEM ? take((size_t)N * m * as) : 0;
+  p.b_B = L->variant == POETX_MEM ? take((size_t)N * n * as) : 0;
+  p.b_dB = take((size_t)N * n * as);
+  p.b_dA = take((size_t)N * m * as);
+  p.b_dxt = take((size_t)N * m * as);
+  p.b_dGP = take((size_t)p.splitsP * n * b * 4);
+  p.b_dGR = take((size_t)p.splitsR * m * b * 4);
+  p.bwd_total = o;
+  return p;
+}
+
+template <typename T = void>
+static T* at(void* base, size_t off) {
+  return reinterpret_cast<T*>(static_cast<char*>(base) + off);
+}
+template <typename T = void>
+static const T* at(const void* base, size_t off) {
+  return reinterpret_cast<const T*>(static_cast<const char*>(base) + off);
+}
+
+}  // namespace poetx
+
+using namespace poetx;
+
+extern "C" poetx_status poetx_set_gemm_engine(int engine) {
+  if (engine != 0 && engine != 1) return POETX_ERR_ARG;
+  g_engine.store(engine);
+  return POETX_OK;
+}
+
+extern "C" size_t poetx_layer_workspace_bytes(const poetx_layer* L, int N, int phase) {
+  if (validate(L) != POETX_OK || N < 0) return 0;
+  const Plan p = make_plan(L, N);
+  return phase == 0 ? p.fwd_total : p.bwd_total;
+}
+
+extern "C" size_t poetx_layer_saved_bytes(const poetx_layer* L, int N) {
+  if (validate(L) != POETX_OK || N < 0) return 0;
+  return make_plan(L, N).saved_total;
+}
+
+extern "C" poetx_status poetx_layer_fwd(const poetx_layer* L, const void* x, int N, void* y,
+                                        void* saved, void* ws, size_t ws_bytes,
+                                        cudaStream_t stream) {
+  POETX_TRY(validate(L));
+  if (N < 0) return POETX_ERR_ARG;
+  if (!saved || !ws || (N > 0 && (!x || !y))) return POETX_ERR_ARG;
+  if (!aligned16(saved) || !aligned16(ws) || (N > 0 && (!aligned16(x) || !aligned16(y))))
+    return POETX_ERR_ALIGN;
+  const Plan p = make_plan(L, N);
+  if (ws_bytes < p.fwd_total) return POETX_ERR_WORKSPACE;
+  const int b = L->b, m = L->m, n = L->n;
+  const poetx_dtype act = L->act;
+  const bool f32 = act == POETX_F32;
+  const size_t as = dtype_size(act);
+  // S1-S2: both CNPs; G in the activation precision and Q^2 kept for the backward
+  POETX_TRY(cnp_forward(L->q_R, m / b, b, at<float>(ws, p.f_Qs), at<float>(saved, p.Q2R),
+                        f32 ? at<float>(saved, p.GR) : nullptr, f32 ? nullptr : at(saved, p.GR),
+                        nullptr, stream));
+  POETX_TRY(cnp_forward(L->q_P, n / b, b, at<float>(ws, p.f_Qs), at<float>(saved, p.Q2P),
+                        f32 ? at<float>(saved, p.GP) : nullptr, f32 ? nullptr : at(saved, p.GP),
+                        nullptr, stream));
+  if (N == 0) return POETX_OK;
+  void* xt = at(ws, p.f_xt);
+  void* A = at(ws, p.f_A);
+  void* B = L->variant == POETX_FAST ? at(saved, p.Bsv) : at(ws, p.f_B);
+  void* zt = at(ws, p.f_zt);
+  POETX_TRY(launch_perm_rows(as, false, x, N, m, L->perm_m, xt, nullptr, nullptr, nullptr, stream));
+  POETX_TRY(blockdiag_impl(act, xt, N, m / b, b, at(saved, p.GR), 0, nullptr, A, stream));
+  POETX_TRY(wprime_impl(act, L->wdt, A, N, m, n, L->Wp, L->w_scale, 0, B, stream));
+  POETX_TRY(blockdiag_impl(act, B, N, n / b, b, at(saved, p.GP), 0, nullptr, zt, stream));
+  return launch_perm_rows(as, true, zt, N, n, L->perm_n, y, nullptr, nullptr, nullptr, stream);
+}
+
+extern "C" poetx_status poetx_layer_bwd(const poetx_layer* L, const void* x, const void* dy, int N,
+                                        const void* saved, void* dx, float* dq_R, float* dq_P,
+                                        int accumulate, void* ws, size_t ws_bytes,
+                                        cudaStream_t stream) {
+  POETX_TRY(validate(L));
+  if (N < 0) return POETX_ERR_ARG;
+  if (!saved || !ws || !dq_R || !dq_P || (N > 0 && (!x || !dy || !dx))) return POETX_ERR_ARG;
+  if (!aligned16(saved) || !aligned16(ws) ||
+      (N > 0 && (!aligned16(x) || !aligned16(dy) || !aligned16(dx))))
+    return POETX_ERR_ALIGN;
+  const Plan p = make_plan(L, N);
+  if (ws_bytes < p.bwd_total) return POETX_ERR_WORKSPACE;
+  const int b = L->b, m = L->m, n = L->n;
+  const poetx_dtype act = L->act;
+  const size_t as = dtype_size(act);
+  void* xt = at(ws, p.b_xt);
+  void* dzt = at(ws, p.b_dzt);
+  void* dB = at(ws, p.b_dB);
+  void* dA = at(ws, p.b_dA);
+  void* dxt = at(ws, p.b_dxt);
+  float* dGP = at<float>(ws, p.b_dGP);
+  float* dGR = at<float>(ws, p.b_dGR);
+  const void* GR = at(saved, p.GR);
+  const void* GP = at(saved, p.GP);
+  if (N > 0) {
+    POETX_TRY(launch_perm_rows(as, false, x, N, m, L->perm_m, xt, nullptr, nullptr, nullptr, stream));
+    POETX_TRY(launch_perm_rows(as, false, dy, N, n, L->perm_n, dzt, nullptr, nullptr, nullptr, stream));
+  }
+  const void* B;
+  if (L->variant == POETX_MEM) {  // recompute B = (x~ blkdiag(G_R)) W'^T
+    void* A = at(ws, p.b_A);
+    void* Bw = at(ws, p.b_B);
+    POETX_TRY(blockdiag_impl(act, xt, N, m / b, b, GR, 0, nullptr, A, stream));
+    POETX_TRY(wprime_impl(act, L->wdt, A, N, m, n, L->Wp, L->w_scale, 0, Bw, stream));
+    B = Bw;
+  } else {
+    B = at(saved, p.Bsv);
+  }
+  POETX_TRY(wgrad_impl(act, B, dzt, N, n / b, b, p.splitsP, dGP, stream));
+  // int8 weight: dA = dB diag(s) W_q, the row scale is folded into dB's columns
+  POETX_TRY(blockdiag_impl(act, dzt, N, n / b, b, GP, 1,
+                           L->wdt == POETX_I8 ? L->w_scale : nullptr, dB, stream));
+  POETX_TRY(wprime_impl(act, L->wdt, dB, N, m, n, L->Wp, L->w_scale, 1, dA, stream));
+  POETX_TRY(wgrad_impl(act, xt, dA, N, m / b, b, p.splitsR, dGR, stream));
+  POETX_TRY(blockdiag_impl(act, dA, N, m / b, b, GR, 1, nullptr, dxt, stream));
+  if (N > 0)
+    POETX_TRY(launch_perm_rows(as, true, dxt, N, m, L->perm_m, dx, nullptr, nullptr, nullptr, stream));
+  void* cnp_ws = at(ws, p.b_cnp);
+  POETX_TRY(cnp_backward(L->q_P, at<float>(saved, p.Q2P), dGP, p.splitsP, n / b, b, dq_P,
+                         accumulate, cnp_ws, stream));
+  return cnp_backward(L->q_R, at<float>(saved, p.Q2R), dGR, p.splitsR, m / b, b, dq_R, accumulate,
+                      cnp_ws, stream);
+}
+
+// ---------------------------------------------------------------- step entry points
+static poetx_status check_act(poetx_dtype dt, int b) {
+  if (dt == POETX_BF16) return (b == 64 || b == 128 || b == 256 || b == 512) ? POETX_OK : POETX_ERR_SHAPE;
+  if (dt == POETX_F32) return (b >= 1 && b <= 1024) ? POETX_OK : POETX_ERR_SHAPE;
+  return POETX_ERR_DTYPE;
+}
+
+extern "C" poetx_status poetx_blockdiag_mm(poetx_dtype dt, const void* X, int N, int nblk, int b,
+                                           const void* G, int trans, const float* col_scale,
+                                           void* Y, cudaStream_t stream) {
+  POETX_TRY(check_act(dt, b));
+  if (N < 0 || nblk < 0) return POETX_ERR_ARG;
+  if (N == 0 || nblk == 0) return POETX_OK;
+  if (!X || !G || !Y) return POETX_ERR_ARG;
+  if (!aligned16(X) || !aligned16(G) || !aligned16(Y)) return POETX_ERR_ALIGN;
+  return blockdiag_impl(dt, X, N, nblk, b, G, trans, col_scale, Y, stream);
+}
+
+extern "C" poetx_status poetx_blockdiag_wgrad(poetx_dtype dt, const void* X, const void* dY, int N,
+                                              int nblk, int b, int splits, float* dG,
+                                              cudaStream_t stream) {
+  POETX_TRY(check_act(dt, b));
+  if (N < 0 || nblk < 0 || splits < 1) return POETX_ERR_ARG;
+  if (nblk == 0) return POETX_OK;
+  if (!dG || (N > 0 && (!X || !dY))) return POETX_ERR_ARG;
+  if (!aligned16(dG) || (N > 0 && (!aligned16(X) || !aligned16(dY)))) return POETX_ERR_ALIGN;
+  return wgrad_impl(dt, X, dY, N, nblk, b, splits, dG, stream);
+}
+
+extern "C" poetx_status poetx_wprime_gemm(poetx_dtype act, poetx_dtype wdt, const void* A, int N,
+                                          int m, int n, const void* W, const float* w_scale,
+                                          int trans, void* C, cudaStream_t stream) {
+  if (act == POETX_F32 && wdt != POETX_F32) return POETX_ERR_DTYPE;
+  if (act == POETX_BF16 && wdt != POETX_BF16 && wdt != POETX_I8) return POETX_ERR_DTYPE;
+  if (act != POETX_F32 && act != POETX_BF16) return POETX_ERR_DTYPE;
+  if (N < 0 || m <= 0 || n <= 0) return POETX_ERR_ARG;
+  if (wdt == POETX_I8 && !w_scale) return POETX_ERR_ARG;
+  if (N == 0) return POETX_OK;
+  if (!A || !W || !C) return POETX_ERR_ARG;
+  if (!aligned16(A) || !aligned16(W) || !aligned16(C)) return POETX_ERR_ALIGN;
+  if ((m * dtype_size(act)) % 16 || (n * dtype_size(act)) % 16) return POETX_ERR_SHAPE;
+  return wprime_impl(act, wdt, A, N, m, n, W, w_scale, trans, C, stream);
+}

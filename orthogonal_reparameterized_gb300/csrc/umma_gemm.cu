@@ -1,0 +1,422 @@
+// Tensor-core GEMM engine for sm_103a: tcgen05.mma (bf16 x bf16 -> fp32 in TMEM) fed by TMA
+// with 128-byte-swizzled shared-memory tiles, an mbarrier pipeline and a TMEM -> register
+// epilogue.  It carries the bf16 products of the POET-X layer:
+//
+//   block-diagonal multiplies  Y_j = X_j G_j or X_j G_j^T per block j       (steps S4, S6,
+//                              S10, S12; POET-X summary page, "Core method" section 3)
+//   frozen-weight contraction  B = A W'^T (forward) and dA = dB W' (backward)  (S5, S11, S9;
+//                              same page, section 1)
+//   block weight gradients     dG_j = X_j^T dY_j over a token range (S10, S12)
+//
+// One CTA computes one 128 x BN output tile over its K range.  Warp 0 issues the TMA loads,
+// one thread of warp 1 issues the MMAs (4 x K=16 per 64-wide K block) and owns the TMEM
+// allocation, warps 2-5 read the accumulator back (tcgen05.ld 32x32b: warp w reads lanes
+// 32*(w%4)..+31 = output rows) and store it.  Operands may be K-major (rows of the tile are
+// contiguous along K) or MN-major (contiguous along M/N, e.g. the token-major activations
+// of a weight gradient); both use the canonical 128-byte swizzle layouts of tcgen05.
+// Every mbarrier wait is bounded; on expiry the kernel records POETX_ERR_TIMEOUT, drains
+// its own copies, frees its TMEM and returns.
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace poetx {
+
+namespace {
+
+enum Mode : int { MODE_PLAIN = 0, MODE_BLOCKDIAG = 1, MODE_WGRAD = 2 };
+
+struct UmmaParams {
+  int mode;
+  int M;         // valid output rows of the whole problem (tokens, or b for WGRAD)
+  int num_kb;    // 64-wide K blocks per CTA (PLAIN, BLOCKDIAG)
+  int b;         // block size (BLOCKDIAG, WGRAD)
+  int nblk;      // blocks (WGRAD)
+  int splits;    // token splits (WGRAD)
+  int kchunk;    // tokens per split, multiple of 64 (WGRAD)
+  long long ntok;  // tokens (WGRAD)
+  void* C;
+  long long ldc;
+  const float* colscale;
+  int* err;
+  unsigned long long limit_ns;
+};
+
+constexpr int BM = 128;
+constexpr int BK = 64;
+
+__host__ __device__ constexpr uint32_t make_idesc(int M, int N, bool a_mn, bool b_mn) {
+  return (1u << 4)                        // accumulator: f32
+         | (1u << 7)                      // A: bf16
+         | (1u << 10)                     // B: bf16
+         | ((a_mn ? 1u : 0u) << 15)       // A major: 0 = K, 1 = MN
+         | ((b_mn ? 1u : 0u) << 16)       // B major
+         | ((uint32_t)(N >> 3) << 17)     // N / 8
+         | ((uint32_t)(M >> 4) << 24);    // M / 16
+}
+
+// Shared-memory matrix descriptor: start address, leading / stride byte offsets (16-byte
+// units), descriptor version 1 (tcgen05), 128-byte swizzle.
+__device__ __forceinline__ uint64_t make_sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
+// K-major tile: rows of 128 bytes (64 bf16 along K), 8-row groups 1024 bytes apart; the
+// k-th K=16 slice starts 32 bytes further.  MN-major tile: boxes of 64 K-rows x 64 MN
+// elements (8 KB) side by side along MN (LBO = 8 KB), 8 K-row groups 1024 bytes apart; the
+// k-th K=16 slice starts 16 rows (2048 bytes) further.
+template <bool MN>
+__device__ __forceinline__ uint64_t tile_desc(uint32_t base, int k) {
+  return MN ? make_sdesc(base + k * 2048, 8192, 1024) : make_sdesc(base + k * 32, 16, 1024);
+}
+
+template <int BN, int STAGES, bool A_MN, bool B_MN, bool OUT_F32>
+__global__ void __launch_bounds__(192, 1)
+    umma_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
+                     const __grid_constant__ CUtensorMap tmB, const UmmaParams p) {
+  constexpr uint32_t A_BYTES = BM * BK * 2;
+  constexpr uint32_t B_BYTES = BN * BK * 2;
+  constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+  constexpr uint32_t TMEM_COLS = BN < 32 ? 32 : BN;
+  constexpr uint32_t IDESC = make_idesc(BM, BN, A_MN, B_MN);
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint64_t* empty = full + STAGES;
+  uint64_t* accum = empty + STAGES;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accum + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int mt = blockIdx.x, nt = blockIdx.y;
+
+  // ---- tile coordinates (TMA coordinates are {inner, outer} = {column, row})
+  int num_kb = p.num_kb;
+  int a_c0 = 0, a_c1 = 0, b_c0 = 0, b_c1 = 0;  // bases; K offsets are added per K block
+  long long out_row0 = (long long)mt * BM, out_col0 = (long long)nt * BN;
+  int split = 0, blk = 0;
+  if (p.mode == MODE_PLAIN) {
+    a_c0 = 0; a_c1 = mt * BM;                               // A K-major
+    if (!B_MN) { b_c0 = 0; b_c1 = nt * BN; }                // B K-major: W [n][m]
+    else { b_c0 = nt * BN; b_c1 = 0; }                      // B MN-major: W [K=n][MN=m]
+  } else if (p.mode == MODE_BLOCKDIAG) {
+    blk = blockIdx.z;
+    a_c0 = blk * p.b; a_c1 = mt * BM;
+    if (!B_MN) { b_c0 = 0; b_c1 = blk * p.b + nt * BN; }    // G_j rows = output cols
+    else { b_c0 = nt * BN; b_c1 = blk * p.b; }              // G_j rows = K
+    out_col0 = (long long)blk * p.b + nt * BN;
+  } else {  // MODE_WGRAD: A = X_j (MN-major), B = dY_j (MN-major), K = tokens
+    blk = blockIdx.z / p.splits;
+    split = blockIdx.z % p.splits;
+    const long long t0 = (long long)split * p.kchunk;
+    long long tcount = p.ntok - t0;
+    if (tcount > p.kchunk) tcount = p.kchunk;
+    num_kb = tcount > 0 ? (int)((tcount + BK - 1) / BK) : 0;
+    a_c0 = blk * p.b + mt * BM; a_c1 = (int)t0;
+    b_c0 = blk * p.b + nt * BN; b_c1 = (int)t0;
+  }
+
+  if (warp == 0 && lane == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(accum, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const uint32_t smem_base = smem_u32(smem);
+
+  if (warp == 0 && lane == 0) {
+    // ------------------------------------------------------------ TMA producer
+    int issued = 0;
+    for (int kb = 0; kb < num_kb; ++kb) {
+      const int s = kb % STAGES;
+      const uint32_t ph = (kb / STAGES) & 1;
+      if (*abort_flag || !mbar_wait_bounded(&empty[s], ph ^ 1, p.err, p.limit_ns)) {
+        *abort_flag = 1;
+        break;
+      }
+      mbar_arrive_expect_tx(&full[s], STAGE_BYTES);
+      uint8_t* sa = smem + s * STAGE_BYTES;
+      uint8_t* sb = sa + A_BYTES;
+      const int k = kb * BK;
+      if (!A_MN) {
+        tma_load_2d(sa, &tmA, &full[s], a_c0 + k, a_c1);
+      } else {
+#pragma unroll
+        for (int i = 0; i < BM / 64; ++i) tma_load_2d(sa + i * 8192, &tmA, &full[s], a_c0 + 64 * i, a_c1 + k);
+      }
+      if (!B_MN) {
+        tma_load_2d(sb, &tmB, &full[s], b_c0 + k, b_c1);
+      } else {
+#pragma unroll
+        for (int i = 0; i < BN / 64; ++i) tma_load_2d(sb + i * 8192, &tmB, &full[s], b_c0 + 64 * i, b_c1 + k);
+      }
+      ++issued;
+    }
+    // Drain: wait for the last load issued into every stage (already complete in the normal
+    // path), so that no copy is in flight when the CTA exits.
+    for (int kb = issued - 1; kb >= 0 && kb >= issued - STAGES; --kb)
+      mbar_wait_bounded(&full[kb % STAGES], (kb / STAGES) & 1, p.err, p.limit_ns);
+  } else if (warp == 1 && lane == 0) {
+    // ------------------------------------------------------------ MMA issuer
+    bool committed = false;
+    for (int kb = 0; kb < num_kb; ++kb) {
+      const int s = kb % STAGES;
+      const uint32_t ph = (kb / STAGES) & 1;
+      if (*abort_flag || !mbar_wait_bounded(&full[s], ph, p.err, p.limit_ns)) {
+        *abort_flag = 1;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t a_base = smem_base + s * STAGE_BYTES;
+      const uint32_t b_base = a_base + A_BYTES;
+#pragma unroll
+      for (int k = 0; k < BK / 16; ++k)
+        umma_bf16(tmem_base, tile_desc<A_MN>(a_base, k), tile_desc<B_MN>(b_base, k), IDESC,
+                  (kb | k) != 0);
+      umma_commit(&empty[s]);
+    }
+    if (num_kb > 0) {
+      umma_commit(accum);
+      committed = true;
+    }
+    // TMEM is freed after the final barrier: make sure every MMA has completed first.
+    if (committed) mbar_wait_bounded(accum, 0, p.err, p.limit_ns);
+  } else if (warp >= 2) {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;
+    const int row = q * 32 + lane;
+    const long long grow = out_row0 + row;
+    bool have = num_kb > 0;
+    if (have) {
+      const bool ok = mbar_wait_bounded(accum, 0, p.err, p.limit_ns);
+      if (!ok) *abort_flag = 1;
+      have = __all_sync(0xffffffffu, ok);  // tcgen05.ld below must be warp-uniform
+      tc_fence_after();
+    }
+    const bool valid = grow < p.M;
+#pragma unroll 1
+    for (int c0 = 0; c0 < BN; c0 += 32) {
+      uint32_t r[32];
+      if (have) {
+        tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)c0, r);
+        tmem_ld_wait();
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) r[i] = 0u;
+      }
+      if (!valid) continue;
+      if (OUT_F32) {
+        float* dst = static_cast<float*>(p.C) +
+                     (((long long)split * p.nblk + blk) * p.b + grow) * p.b + out_col0 + c0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          reinterpret_cast<float4*>(dst)[i] =
+              make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
+                          __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
+      } else {
+        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.C) + grow * p.ldc + out_col0 + c0;
+        float v[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+        if (p.colscale) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] *= __ldg(p.colscale + out_col0 + c0 + i);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          uint4 w;
+          w.x = pack_bf16x2(v[8 * i + 0], v[8 * i + 1]);
+          w.y = pack_bf16x2(v[8 * i + 2], v[8 * i + 3]);
+          w.z = pack_bf16x2(v[8 * i + 4], v[8 * i + 5]);
+          w.w = pack_bf16x2(v[8 * i + 6], v[8 * i + 7]);
+          reinterpret_cast<uint4*>(dst)[i] = w;
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 2-D bf16 tensor [outer][inner] with row pitch `pitch_elems`, box {box_inner, box_outer},
+// 128-byte swizzle, zero fill out of bounds.
+bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint64_t pitch_elems,
+              uint32_t box_inner, uint32_t box_outer) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {pitch_elems * 2};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int BN, int STAGES, bool A_MN, bool B_MN, bool OUT_F32>
+poetx_status launch(const CUtensorMap& ta, const CUtensorMap& tb, const UmmaParams& p, dim3 grid,
+                    cudaStream_t s) {
+  auto k = umma_gemm_kernel<BN, STAGES, A_MN, B_MN, OUT_F32>;
+  constexpr int smem = STAGES * (BM * BK * 2 + BN * BK * 2) + 1024 + 256;
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [&] {
+    attr_err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  });
+  POETX_CUDA_TRY(attr_err);
+  if (grid.x == 0 || grid.y == 0 || grid.z == 0) return POETX_OK;
+  k<<<grid, 192, smem, s>>>(ta, tb, p);
+  POETX_CUDA_TRY(cudaGetLastError());
+  return POETX_OK;
+}
+
+UmmaParams base_params() {
+  UmmaParams p{};
+  p.err = device_error_word();
+  p.limit_ns = kWaitLimitNs;
+  return p;
+}
+
+}  // namespace
+
+bool umma_supported() {
+  int dev = 0, major = 0, minor = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  return major == 10 && minor == 3 && encode_fn() != nullptr;
+}
+
+poetx_status umma_blockdiag(const void* X, long long N, int nblk, int b, const void* G, int trans,
+                            const float* col_scale, void* Y, cudaStream_t s) {
+  if (N == 0 || nblk == 0) return POETX_OK;
+  const int D = nblk * b;
+  const int BN = b < 256 ? b : 256;
+  CUtensorMap ta, tb;
+  if (!make_map(&ta, X, D, N, D, 64, 128)) return POETX_ERR_CUDA;
+  if (trans) {
+    if (!make_map(&tb, G, b, (uint64_t)nblk * b, b, 64, BN)) return POETX_ERR_CUDA;
+  } else {
+    if (!make_map(&tb, G, b, (uint64_t)nblk * b, b, 64, 64)) return POETX_ERR_CUDA;
+  }
+  UmmaParams p = base_params();
+  p.mode = MODE_BLOCKDIAG;
+  p.M = (int)N;
+  p.num_kb = b / 64;
+  p.b = b;
+  p.C = Y;
+  p.ldc = D;
+  p.colscale = col_scale;
+  dim3 grid((unsigned)((N + BM - 1) / BM), b / BN, nblk);
+  if (trans) {
+    if (BN == 64) return launch<64, 4, false, false, false>(ta, tb, p, grid, s);
+    if (BN == 128) return launch<128, 3, false, false, false>(ta, tb, p, grid, s);
+    return launch<256, 2, false, false, false>(ta, tb, p, grid, s);
+  }
+  if (BN == 64) return launch<64, 4, false, true, false>(ta, tb, p, grid, s);
+  if (BN == 128) return launch<128, 3, false, true, false>(ta, tb, p, grid, s);
+  return launch<256, 2, false, true, false>(ta, tb, p, grid, s);
+}
+
+poetx_status umma_wprime(const void* A, long long N, int m, int n, const void* W,
+                         const float* w_scale, int trans, void* C, cudaStream_t s) {
+  if (N == 0) return POETX_OK;
+  CUtensorMap ta, tb;
+  UmmaParams p = base_params();
+  p.mode = MODE_PLAIN;
+  p.M = (int)N;
+  p.colscale = w_scale;
+  p.C = C;
+  if (!trans) {  // C[N,n] = A[N,m] W^T
+    if (!make_map(&ta, A, m, N, m, 64, 128)) return POETX_ERR_CUDA;
+    if (!make_map(&tb, W, m, n, m, 64, 256)) return POETX_ERR_CUDA;
+    p.num_kb = m / 64;
+    p.ldc = n;
+    dim3 grid((unsigned)((N + BM - 1) / BM), n / 256, 1);
+    return launch<256, 4, false, false, false>(ta, tb, p, grid, s);
+  }
+  // C[N,m] = A[N,n] W: B operand (output col c, K index r) = W[r][c], MN-major
+  if (!make_map(&ta, A, n, N, n, 64, 128)) return POETX_ERR_CUDA;
+  if (!make_map(&tb, W, m, n, m, 64, 64)) return POETX_ERR_CUDA;
+  p.num_kb = n / 64;
+  p.ldc = m;
+  dim3 grid((unsigned)((N + BM - 1) / BM), m / 256, 1);
+  return launch<256, 4, false, true, false>(ta, tb, p, grid, s);
+}
+
+poetx_status umma_wgrad(const void* X, const void* dY, long long N, int nblk, int b, int splits,
+                        float* dG, cudaStream_t s) {
+  if (nblk == 0) return POETX_OK;
+  if (N == 0) {  // no tokens: every partial is zero
+    POETX_CUDA_TRY(cudaMemsetAsync(dG, 0, (size_t)splits * nblk * b * b * sizeof(float), s));
+    return POETX_OK;
+  }
+  const int D = nblk * b;
+  const int BN = b < 256 ? b : 256;
+  CUtensorMap ta, tb;
+  if (!make_map(&ta, X, D, N, D, 64, 64)) return POETX_ERR_CUDA;
+  if (!make_map(&tb, dY, D, N, D, 64, 64)) return POETX_ERR_CUDA;
+  UmmaParams p = base_params();
+  p.mode = MODE_WGRAD;
+  p.M = b;
+  p.b = b;
+  p.nblk = nblk;
+  p.splits = splits;
+  p.kchunk = (int)(64 * ((N + 64LL * splits - 1) / (64LL * splits)));
+  if (p.kchunk < 64) p.kchunk = 64;
+  p.ntok = N;
+  p.C = dG;
+  dim3 grid((b + BM - 1) / BM, b / BN, nblk * splits);
+  if (BN == 64) return launch<64, 4, true, true, true>(ta, tb, p, grid, s);
+  if (BN == 128) return launch<128, 3, true, true, true>(ta, tb, p, grid, s);
+  return launch<256, 2, true, true, true>(ta, tb, p, grid, s);
+}
+
+}  // namespace poetx

@@ -1,0 +1,112 @@
+"""CPU-only checks of the C ABI: the library builds and loads, exports every function the
+header declares, and rejects bad arguments on the host before launching anything."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "poetx.h")
+
+
+@pytest.fixture(scope="module")
+def P():
+    from orthogonal_reparameterized_gb300 import build
+    build.build()
+    import orthogonal_reparameterized_gb300.poetx as P
+    P.lib()
+    return P
+
+
+def _declared():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(poetx_\w+)\s*\(", src)))
+
+
+def test_header_declares_the_boundary():
+    names = _declared()
+    for must in ("poetx_cnp_fwd", "poetx_cnp_bwd", "poetx_layer_fwd", "poetx_layer_bwd",
+                 "poetx_merge_perm"):
+        assert must in names
+
+
+def test_every_declared_symbol_is_exported(P):
+    out = subprocess.run(["nm", "-D", "--defined-only", P.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r" T (poetx_\w+)", out))
+    missing = [n for n in _declared() if n not in exported]
+    assert not missing, missing
+    lib = P.lib()
+    for n in _declared():
+        assert getattr(lib, n) is not None
+
+
+def test_binding_covers_every_symbol(P):
+    for n in _declared():
+        assert n in P._SIGS, n
+
+
+def test_status_strings(P):
+    for st in range(9):
+        assert P.status_str(st).startswith("POETX_")
+    assert "UNKNOWN" in P.status_str(99)
+
+
+def _desc(P, **kw):
+    d = dict(m=256, n=512, b=64, act=P.BF16, wdt=P.BF16, variant=P.FAST, order=3)
+    d.update(kw)
+    fake = ctypes.c_void_p(4096)  # never dereferenced: only host-side logic runs
+    return P.LayerDesc(d["m"], d["n"], d["b"], d["order"], d["act"], d["wdt"], d["variant"],
+                       fake, fake, fake, fake if d["wdt"] == P.I8 else None, fake, fake)
+
+
+def test_layer_sizes_host_logic(P):
+    L = _desc(P)
+    N = 1000
+    fast = P.poetx_layer_saved_bytes(L, N)
+    mem = P.poetx_layer_saved_bytes(_desc(P, variant=P.MEM), N)
+    assert fast - mem >= N * 512 * 2
+    assert mem >= (256 + 512) * 64 * (2 + 4)
+    assert P.poetx_layer_workspace_bytes(L, N, 0) > N * (256 + 512) * 2
+    assert P.poetx_layer_workspace_bytes(L, N, 1) > P.poetx_layer_workspace_bytes(L, N, 0)
+    # invalid descriptors report 0 bytes
+    assert P.poetx_layer_workspace_bytes(_desc(P, b=100), N, 0) == 0        # b not supported
+    assert P.poetx_layer_workspace_bytes(_desc(P, m=320, b=128), N, 0) == 0  # b does not divide m
+    assert P.poetx_layer_workspace_bytes(_desc(P, order=4), N, 0) == 0
+    assert P.poetx_layer_workspace_bytes(_desc(P, wdt=P.I8), N, 0) == 0      # int8 needs mem
+    assert P.poetx_layer_workspace_bytes(_desc(P, wdt=P.I8, variant=P.MEM), N, 0) > 0
+    assert P.poetx_layer_workspace_bytes(_desc(P, act=P.F32, wdt=P.BF16), N, 0) == 0
+    assert P.poetx_layer_workspace_bytes(_desc(P, act=P.F32, wdt=P.F32, b=32), N, 0) > 0
+
+
+def test_argument_errors_before_launch(P):
+    lib = P.lib()
+    fake = ctypes.c_void_p(4096)
+    L = _desc(P, order=2)
+    assert lib.poetx_layer_fwd(ctypes.byref(L), fake, 4, fake, fake, fake, 1 << 30, None) == 6
+    L = _desc(P)
+    assert lib.poetx_layer_fwd(ctypes.byref(L), fake, 4, None, fake, fake, 1 << 30, None) == 1
+    assert lib.poetx_layer_fwd(ctypes.byref(L), fake, 4, fake, fake, fake, 16, None) == 5
+    mis = ctypes.c_void_p(4100)
+    assert lib.poetx_layer_fwd(ctypes.byref(L), mis, 4, fake, fake, fake, 1 << 30, None) == 4
+    assert lib.poetx_cnp_fwd(fake, 4, 64, 2, fake, None, None, fake, 1 << 30, None) == 6
+    assert lib.poetx_cnp_fwd(fake, 4, 1, 3, fake, None, None, fake, 1 << 30, None) == 2
+    assert lib.poetx_cnp_fwd(fake, 4, 64, 3, None, None, None, fake, 1 << 30, None) == 1
+    assert lib.poetx_cnp_fwd(fake, 4, 64, 3, fake, None, None, fake, 8, None) == 5
+    assert lib.poetx_cnp_fwd(fake, 0, 64, 3, fake, None, None, fake, 8, None) == 0  # empty
+    assert lib.poetx_cnp_bwd(fake, fake, 0, 4, 64, 3, fake, 0, fake, 1 << 30, None) == 1
+    assert lib.poetx_perm_gather(P.BF16, fake, 0, 64, fake, fake, None) == 0     # N = 0
+    assert lib.poetx_perm_gather(7, fake, 4, 64, fake, fake, None) == 3
+    assert lib.poetx_perm_gather(P.BF16, mis, 4, 64, fake, fake, None) == 4
+    assert lib.poetx_blockdiag_mm(P.BF16, fake, 4, 2, 100, fake, 0, None, fake, None) == 2
+    assert lib.poetx_blockdiag_wgrad(P.BF16, fake, fake, 4, 2, 64, 0, fake, None) == 1
+    assert lib.poetx_wprime_gemm(P.F32, P.BF16, fake, 4, 64, 64, fake, None, 0, fake, None) == 3
+    assert lib.poetx_wprime_gemm(P.BF16, P.I8, fake, 4, 64, 64, fake, None, 0, fake, None) == 1
+    assert lib.poetx_merge_perm(fake, None, P.I8, 4, 64, fake, fake, fake, None, None) == 1
+    assert lib.poetx_set_gemm_engine(5) == 1
+    assert lib.poetx_cnp_workspace_bytes(4, 64, 0) == 2 * 4 * 64 * 64 * 4
+    assert lib.poetx_cnp_workspace_bytes(4, 1, 0) == 0

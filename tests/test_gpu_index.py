@@ -1,0 +1,93 @@
+"""Bit-exact parity of the index / data-movement kernels with the oracle: packed triangle
+unpack and gradient pack, permutation gather/scatter, the merge into W', the quantiser."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from gpu_util import DEV, P, dev, host  # noqa: F401
+
+pytestmark = pytest.mark.gpu
+RNG = np.random.default_rng(2024)
+
+
+@pytest.mark.parametrize("nblk,b", [(3, 2), (2, 5), (4, 32), (3, 100), (2, 256), (1, 512)])
+def test_triu_unpack_bit_exact(P, nblk, b):
+    q = RNG.standard_normal((nblk, b * (b - 1) // 2)).astype(np.float32)
+    Q = torch.empty(nblk, b, b, device=DEV)
+    P.poetx_triu_unpack(dev(q, torch.float32), b, Q)
+    np.testing.assert_array_equal(host(Q), O.triu_unpack(q.astype(np.float64), b))
+
+
+@pytest.mark.parametrize("nblk,b", [(3, 2), (2, 7), (4, 64), (2, 300)])
+@pytest.mark.parametrize("acc", [False, True])
+def test_triu_grad_pack_bit_exact(P, nblk, b, acc):
+    X = RNG.standard_normal((nblk, b, b)).astype(np.float32)
+    d0 = RNG.standard_normal((nblk, b * (b - 1) // 2)).astype(np.float32)
+    dq = dev(d0, torch.float32)
+    P.poetx_triu_grad_pack(dev(X, torch.float32), dq, accumulate=acc)
+    # fp32 subtraction (and addition) are correctly rounded on both sides
+    ref = O.triu_grad_pack(X.astype(np.float64)).astype(np.float32)
+    if acc:
+        ref = (d0 + ref).astype(np.float32)
+    np.testing.assert_array_equal(host(dq).astype(np.float32), ref)
+
+
+def _perms(D):
+    return {"random": RNG.permutation(D), "identity": np.arange(D),
+            "reversal": np.arange(D)[::-1].copy(),
+            "swap": np.r_[1, 0, np.arange(2, D)]}
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32, torch.int8])
+@pytest.mark.parametrize("N,D", [(1, 64), (37, 256), (300, 2048), (5, 14336)])
+def test_perm_gather_scatter_bit_exact(P, dtype, N, D):
+    if dtype == torch.int8:
+        X = torch.randint(-128, 127, (N, D), dtype=torch.int8, device=DEV)
+    else:
+        X = torch.randn(N, D, device=DEV).to(dtype)
+    for name, p in _perms(D).items():
+        pt = dev(p, torch.int32)
+        Y = torch.empty_like(X)
+        P.poetx_perm_gather(X, pt, Y)
+        ref = O.perm_gather(host(X), p)
+        np.testing.assert_array_equal(host(Y), ref, err_msg=name)
+        Z = torch.empty_like(X)
+        P.poetx_perm_scatter(Y, pt, Z)
+        np.testing.assert_array_equal(host(Z), O.perm_scatter(ref, p), err_msg=name)
+        np.testing.assert_array_equal(host(Z), host(X), err_msg=name)
+
+
+def test_perm_empty(P):
+    X = torch.empty(0, 64, dtype=torch.bfloat16, device=DEV)
+    P.poetx_perm_gather(X, dev(np.arange(64), torch.int32), torch.empty_like(X))
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32, torch.int8])
+@pytest.mark.parametrize("n,m", [(64, 128), (512, 2048), (13824, 5120)])
+def test_merge_perm_bit_exact(P, dtype, n, m):
+    pn, pm = RNG.permutation(n), RNG.permutation(m)
+    if dtype == torch.int8:
+        W = torch.randint(-127, 128, (n, m), dtype=torch.int8, device=DEV)
+        s = torch.rand(n, device=DEV)
+        sp = torch.empty_like(s)
+    else:
+        W = torch.randn(n, m, device=DEV).to(dtype)
+        s = sp = None
+    Wp = torch.empty_like(W)
+    P.poetx_merge_perm(W, dev(pn, torch.int32), dev(pm, torch.int32), Wp, s, sp)
+    np.testing.assert_array_equal(host(Wp), O.merge_perm(host(W), pn, pm))
+    if s is not None:
+        np.testing.assert_array_equal(host(sp), host(s)[pn])
+
+
+@pytest.mark.parametrize("n,m", [(7, 33), (64, 4096), (13824, 5120)])
+def test_quantize_bit_exact(P, n, m):
+    W = (RNG.standard_normal((n, m)) / np.sqrt(m)).astype(np.float32)
+    W[n // 2] = 0.0
+    Wq = torch.empty(n, m, dtype=torch.int8, device=DEV)
+    s = torch.empty(n, device=DEV)
+    P.poetx_quantize_rows_int8(dev(W, torch.float32), Wq, s)
+    rq, rs = O.quantize_rows_int8(W)
+    np.testing.assert_array_equal(host(Wq), rq)
+    np.testing.assert_array_equal(s.cpu().numpy(), rs)

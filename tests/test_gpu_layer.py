@@ -1,0 +1,186 @@
+"""Parity of the whole POET-X layer (both CNPs, forward, backward; fast and mem variants)
+with the fp64 oracle on identical seeded inputs: 1e-5 for the fp32 layer, 2e-2 for bf16
+(relative Frobenius error of y, dx, dq_R and dq_P)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from gpu_util import DEV, P, TOL_BF16_LAYER, TOL_F32, dev, host  # noqa: F401
+from orthogonal_reparameterized_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+TDT = {"f32": torch.float32, "bf16": torch.bfloat16}
+
+
+def run_layer(P, inp, b, act, wdt, variant, dy=None, q_zero=False, accumulate_init=None):
+    """Runs fwd + bwd through the C ABI; returns host arrays and the effective W0 that the
+    oracle must use (the GPU quantiser's own output for int8 weights)."""
+    m, n = inp["W0"].shape[1], inp["W0"].shape[0]
+    adt = TDT[act]
+    x = dev(inp["x"], adt)
+    dyt = dev(inp["dy"] if dy is None else dy, adt)
+    pm = dev(inp["perm_m"], torch.int32)
+    pn = dev(inp["perm_n"], torch.int32)
+    qR = dev(inp["q_R"] * (0 if q_zero else 1), torch.float32)
+    qP = dev(inp["q_P"] * (0 if q_zero else 1), torch.float32)
+    w_scale = None
+    if wdt == "i8":
+        W32 = dev(inp["W0"], torch.float32)
+        Wq = torch.empty(n, m, dtype=torch.int8, device=DEV)
+        s = torch.empty(n, device=DEV)
+        P.poetx_quantize_rows_int8(W32, Wq, s)
+        Wp = torch.empty_like(Wq)
+        w_scale = torch.empty_like(s)
+        P.poetx_merge_perm(Wq, pn, pm, Wp, s, w_scale)
+        W_eff = O.dequantize_rows(host(Wq), host(s))
+        wcode = P.I8
+    else:
+        W0 = dev(inp["W0"], TDT[wdt])
+        Wp = torch.empty_like(W0)
+        P.poetx_merge_perm(W0, pn, pm, Wp)
+        W_eff = inp["W0"]
+        wcode = P.F32 if wdt == "f32" else P.BF16
+    acode = P.F32 if act == "f32" else P.BF16
+    vcode = P.FAST if variant == "fast" else P.MEM
+    N = x.shape[0]
+    L = P.make_layer(m, n, b, acode, wcode, vcode, pm, pn, Wp, qR, qP, w_scale)
+    saved = P.workspace(P.poetx_layer_saved_bytes(L, N), DEV)
+    wsf = P.workspace(P.poetx_layer_workspace_bytes(L, N, 0), DEV)
+    wsb = P.workspace(P.poetx_layer_workspace_bytes(L, N, 1), DEV)
+    y = torch.empty(N, n, dtype=adt, device=DEV)
+    dx = torch.empty(N, m, dtype=adt, device=DEV)
+    if accumulate_init is not None:
+        dqR = dev(accumulate_init[0], torch.float32)
+        dqP = dev(accumulate_init[1], torch.float32)
+    else:
+        dqR = torch.full_like(qR, float("nan"))
+        dqP = torch.full_like(qP, float("nan"))
+    P.poetx_layer_fwd(L, x, y, saved, wsf)
+    P.poetx_layer_bwd(L, x, dyt, saved, dx, dqR, dqP, wsb, accumulate=accumulate_init is not None)
+    torch.cuda.synchronize()
+    assert P.poetx_get_device_error() == 0
+    return {"y": host(y), "dx": host(dx), "dq_R": host(dqR), "dq_P": host(dqP), "W_eff": W_eff}
+
+
+def check(got, ref, tol, keys=("y", "dx", "dq_R", "dq_P")):
+    errs = {k: O.rel_fro(got[k], ref[k]) for k in keys}
+    assert max(errs.values()) <= tol, errs
+    return errs
+
+
+def oracle_for(inp, got, b, q_zero=False, dy=None):
+    s = 0 if q_zero else 1
+    return O.poetx_layer(inp["x"], inp["dy"] if dy is None else dy, got["W_eff"], inp["perm_m"],
+                         inp["perm_n"], inp["q_R"] * s, inp["q_P"] * s, b)
+
+
+@pytest.mark.parametrize("variant", ["fast", "mem"])
+def test_layer_fp32_256_b32(P, variant):
+    wl = inputs.WORKLOADS["fp32_256_b32"]
+    inp = inputs.layer_inputs(wl, wl.layers[0])
+    got = run_layer(P, inp, wl.b, "f32", "f32", variant)
+    check(got, oracle_for(inp, got, wl.b), TOL_F32)
+
+
+@pytest.mark.parametrize("m,n,b,N", [(256, 512, 64, 200), (512, 256, 128, 77), (512, 512, 256, 130),
+                                     (1024, 512, 512, 300)])
+@pytest.mark.parametrize("variant", ["fast", "mem"])
+def test_layer_bf16_small(P, m, n, b, N, variant):
+    inp = inputs.small_layer_inputs(31 + b, m, n, b, N, act="bf16", wdt="bf16")
+    got = run_layer(P, inp, b, "bf16", "bf16", variant)
+    check(got, oracle_for(inp, got, b), TOL_BF16_LAYER)
+
+
+def test_layer_int8_small(P):
+    inp = inputs.small_layer_inputs(41, 512, 768, 256, 150, act="bf16", wdt="i8")
+    got = run_layer(P, inp, 256, "bf16", "i8", "mem")
+    check(got, oracle_for(inp, got, 256), TOL_BF16_LAYER)
+
+
+def test_layer_zero_q_is_plain_linear(P):
+    inp = inputs.small_layer_inputs(43, 256, 512, 64, 100, act="bf16", wdt="bf16")
+    got = run_layer(P, inp, 64, "bf16", "bf16", "fast", q_zero=True)
+    assert O.rel_fro(got["y"], inp["x"] @ inp["W0"].T) <= TOL_BF16_LAYER
+    assert O.rel_fro(got["dx"], inp["dy"] @ inp["W0"]) <= TOL_BF16_LAYER
+
+
+def test_fast_and_mem_bitwise_equal_and_deterministic(P):
+    inp = inputs.small_layer_inputs(47, 512, 512, 128, 333, act="bf16", wdt="bf16")
+    a = run_layer(P, inp, 128, "bf16", "bf16", "fast")
+    b2 = run_layer(P, inp, 128, "bf16", "bf16", "mem")
+    c = run_layer(P, inp, 128, "bf16", "bf16", "fast")
+    for k in ("y", "dx", "dq_R", "dq_P"):
+        np.testing.assert_array_equal(a[k], b2[k], err_msg=k)
+        np.testing.assert_array_equal(a[k], c[k], err_msg=k)
+
+
+def test_layer_accumulate_and_empty(P):
+    inp = inputs.small_layer_inputs(53, 256, 256, 64, 0, act="bf16", wdt="bf16")
+    init = (np.full(inp["q_R"].shape, 0.5), np.full(inp["q_P"].shape, -1.0))
+    got = run_layer(P, inp, 64, "bf16", "bf16", "fast", accumulate_init=init)
+    np.testing.assert_array_equal(got["dq_R"], init[0])   # N = 0 adds exact zeros
+    np.testing.assert_array_equal(got["dq_P"], init[1])
+    inp = inputs.small_layer_inputs(54, 256, 256, 64, 90, act="bf16", wdt="bf16")
+    base = run_layer(P, inp, 64, "bf16", "bf16", "fast")
+    acc = run_layer(P, inp, 64, "bf16", "bf16", "fast", accumulate_init=init)
+    np.testing.assert_allclose(acc["dq_R"], base["dq_R"] + 0.5, rtol=1e-6, atol=1e-6)
+    np.testing.assert_allclose(acc["dq_P"], base["dq_P"] - 1.0, rtol=1e-6, atol=1e-6)
+
+
+@pytest.mark.parametrize("variant", ["fast", "mem"])
+def test_layer_llama1b_2048_full(P, variant):
+    wl = inputs.WORKLOADS["llama1b_2048"]
+    inp = inputs.layer_inputs(wl, wl.layers[0])
+    got = run_layer(P, inp, wl.b, "bf16", "bf16", variant)
+    check(got, oracle_for(inp, got, wl.b), TOL_BF16_LAYER)
+
+
+@pytest.mark.parametrize("b", [64, 128, 256, 512])
+def test_layer_sweep_4096_full(P, b):
+    wl = inputs.WORKLOADS[f"sweep_4096_b{b}"]
+    inp = inputs.layer_inputs(wl, wl.layers[0])
+    got = run_layer(P, inp, b, "bf16", "bf16", "fast")
+    check(got, oracle_for(inp, got, b), TOL_BF16_LAYER)
+
+
+def _masked_full_size(P, wl, layer, variant, n_sample=256, n_rows=48):
+    """Full token count in the benchmark's launch configuration, with the upstream gradient
+    zero outside a random token subset S: then dq (a sum over tokens) equals the oracle's
+    dq over S alone, and y / dx are checked on sampled rows (both are row-independent)."""
+    inp = inputs.layer_inputs(wl, layer)
+    N = inp["x"].shape[0]
+    r = np.random.default_rng(layer.m * 7 + layer.n)
+    S = np.sort(r.choice(N, n_sample, replace=False))
+    dy = np.zeros_like(inp["dy"])
+    dy[S] = inp["dy"][S]
+    got = run_layer(P, inp, wl.b, "bf16", wl.wdt, variant, dy=dy)
+    sub = {k: inp[k] for k in inp}
+    sub["x"], sub["dy"] = inp["x"][S], inp["dy"][S]
+    ref = O.poetx_layer(sub["x"], sub["dy"], got["W_eff"], inp["perm_m"], inp["perm_n"],
+                        inp["q_R"], inp["q_P"], wl.b)
+    rows = np.sort(r.choice(N, n_rows, replace=False))
+    y_ref = O.layer_forward_rows(inp["x"][rows], ref["Wp"], inp["perm_m"], inp["perm_n"],
+                                 ref["G_R"], ref["G_P"])
+    errs = {"y": O.rel_fro(got["y"][rows], y_ref),
+            "dx": O.rel_fro(got["dx"][S], ref["dx"]),
+            "dq_R": O.rel_fro(got["dq_R"], ref["dq_R"]),
+            "dq_P": O.rel_fro(got["dq_P"], ref["dq_P"])}
+    outside = np.setdiff1d(np.arange(N), S)[:64]
+    assert not np.any(got["dx"][outside]), "dx must vanish where dy does"
+    assert max(errs.values()) <= TOL_BF16_LAYER, errs
+
+
+@pytest.mark.parametrize("layer", ["q", "gate", "down"])
+def test_layer_llama8b_block_full_size(P, layer):
+    wl = inputs.WORKLOADS["llama8b_block"]
+    L = [l for l in wl.layers if l.name == layer][0]
+    _masked_full_size(P, wl, L, "fast")
+
+
+@pytest.mark.parametrize("layer", ["up", "down"])
+def test_layer_llama13b_mlp_int8_full_size(P, layer):
+    wl = inputs.WORKLOADS["llama13b_mlp_int8"]
+    L = [l for l in wl.layers if l.name == layer][0]
+    _masked_full_size(P, wl, L, "mem")
