@@ -1,0 +1,467 @@
+#!/usr/bin/env python3
+"""Benchmark of the POET-X layer step on GB300.
+
+A step is one pass of the whole hot path on one batch: both Cayley-Neumann forwards, the
+layer forward, the layer backward and both Cayley-Neumann backwards (poetx_layer_fwd +
+poetx_layer_bwd through the C ABI), on the Llama-1B-shaped layer (m = n = 2048, b = 256,
+N = 4096 bf16 tokens), fast variant.  Prints one JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME] [--variant fast|mem]
+
+N > 1 runs under torchrun: one replica per GPU on its own tokens (weak scaling, no
+collective on the data path; the timing is the max over ranks).  --impl reference times
+the fp64 CPU oracle on the host cores on a bounded sample of the same workload.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "POET-X layer fwd+bwd tokens/s; CNP blocks/s; % of BF16 TC peak / HBM BW"
+L2_FLUSH_BYTES = 512 << 20  # larger than the 129 MB L2
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="llama1b_2048")
+    ap.add_argument("--variant", default="fast", choices=["fast", "mem"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"),
+                "sm_max_mhz": d.get("sm_max_mhz", 2070.0), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "sm_max_mhz": 2070.0, "source": "fallback"}
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.rows = []
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), [c.strip() for c in line.split(",")]))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        inside = [r for t, r in self.rows if t0 <= t <= t1]
+        note = "samples inside the timed region"
+        if not inside:  # timed region shorter than the sampling period: nearest samples
+            inside = [r for t, r in self.rows if t0 - 1.0 <= t <= t1 + 1.0]
+            note = "samples within 1 s of the timed region (region shorter than the period)"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "note": "no samples"}
+        sm = [float(r[1]) for r in inside if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in inside if r[2].replace(".", "").isdigit()]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in inside:
+            for k, nm in enumerate(names):
+                if len(r) > 5 + k and r[5 + k].lower().startswith("active"):
+                    reasons.add(nm)
+        pw = [float(r[3]) for r in inside if r[3].replace(".", "").isdigit()]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "power_w_max": max(pw) if pw else None, "samples": len(inside), "note": note}
+
+
+# ------------------------------------------------------------------ CPU oracle
+CPU_SNIPPET = r"""
+import json, os, sys, time
+sys.path.insert(0, %(root)r)
+import numpy as np
+import oracle as O
+from orthogonal_reparameterized_gb300 import inputs
+wl = inputs.WORKLOADS[%(wl)r]
+layer = wl.layers[0]
+inp = inputs.layer_inputs(wl, layer, N=%(ntok)d)
+W = inp["W0"]
+if wl.wdt == "i8":
+    Wq, s = O.quantize_rows_int8(W)
+    W = O.dequantize_rows(Wq, s)
+O.poetx_layer(inp["x"][:8], inp["dy"][:8], W, inp["perm_m"], inp["perm_n"], inp["q_R"],
+              inp["q_P"], wl.b)
+times = []
+t_end = time.perf_counter() + %(budget)f
+while True:
+    t0 = time.perf_counter()
+    O.poetx_layer(inp["x"], inp["dy"], W, inp["perm_m"], inp["perm_n"], inp["q_R"], inp["q_P"],
+                  wl.b)
+    times.append(time.perf_counter() - t0)
+    if len(times) >= %(reps)d or time.perf_counter() > t_end:
+        break
+print(json.dumps({"times": times}))
+"""
+
+
+def run_oracle_sample(wl_name, ntok, reps, budget_s):
+    cores = os.cpu_count() or 1
+    env = dict(os.environ)
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[k] = str(cores)
+    code = CPU_SNIPPET % {"root": ROOT, "wl": wl_name, "ntok": ntok, "reps": reps,
+                          "budget": budget_s}
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env,
+                       timeout=900)
+    if r.returncode != 0:
+        raise RuntimeError("oracle sample failed: " + r.stderr[-2000:])
+    times = json.loads(r.stdout.strip().splitlines()[-1])["times"]
+    return times, cores
+
+
+def cpu_baseline(wl, ntok=512):
+    times, cores = run_oracle_sample(wl.name, ntok, reps=50, budget_s=15.0)
+    t = statistics.median(times)
+    return {"value": ntok / t, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"fp64 numpy oracle, full step (CNP fwd x2, layer fwd+bwd, CNP bwd x2) of "
+                      f"the {wl.name} layer on {ntok} of its {wl.N} tokens, median of "
+                      f"{len(times)} runs"}
+
+
+# ------------------------------------------------------------------ reference arm
+def reference_arm(args, rank, world):
+    from orthogonal_reparameterized_gb300 import inputs
+    if rank != 0:
+        return
+    wl = inputs.WORKLOADS[args.workload]
+    ntok = 256
+    total = max(1, args.steps) + max(0, args.warmup)
+    times, cores = run_oracle_sample(wl.name, ntok, reps=total, budget_s=180.0)
+    timed = times[args.warmup:] if len(times) > args.warmup else times
+    t = statistics.mean(timed)
+    val = ntok / t
+    out = {"impl": "reference", "metric": METRIC, "value": val, "unit": "tokens/s",
+           "n_gpus": args.gpus, "steps": len(timed), "warmup": min(args.warmup, len(times)),
+           "ms_per_step": t * 1e3, "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "config": {"workload": wl.name, "m": wl.layers[0].m, "n": wl.layers[0].n, "b": wl.b,
+                      "tokens_per_step": ntok, "variant": args.variant},
+           "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                            "sample": f"{ntok} tokens of the {wl.name} layer per step"},
+           "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    if len(timed) < args.steps:
+        out["note"] = f"time budget reached after {len(times)} oracle steps"
+    print(json.dumps(out))
+
+
+# ------------------------------------------------------------------ our arm
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    local = int(os.environ.get("LOCAL_RANK", 0))
+    if args.impl == "reference":
+        reference_arm(args, rank, world)
+        return
+
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    from orthogonal_reparameterized_gb300 import inputs
+    import orthogonal_reparameterized_gb300.poetx as P
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    P.lib()
+
+    wl = inputs.WORKLOADS[args.workload]
+    layer = wl.layers[0]
+    m, n, b, N = layer.m, layer.n, wl.b, wl.N
+    bf = torch.bfloat16 if wl.act == "bf16" else torch.float32
+    inp = inputs.layer_inputs(wl, layer)
+    t = lambda a, dt: torch.tensor(a, dtype=dt, device=dev)
+    x = t(inp["x"], bf)
+    dy = t(inp["dy"], bf)
+    pm = t(inp["perm_m"], torch.int32)
+    pn = t(inp["perm_n"], torch.int32)
+    qR = t(inp["q_R"], torch.float32)
+    qP = t(inp["q_P"], torch.float32)
+    w_scale = None
+    if wl.wdt == "i8":
+        W32 = t(inp["W0"], torch.float32)
+        Wq = torch.empty(n, m, dtype=torch.int8, device=dev)
+        s = torch.empty(n, device=dev)
+        P.poetx_quantize_rows_int8(W32, Wq, s)
+        Wp = torch.empty_like(Wq)
+        w_scale = torch.empty_like(s)
+        P.poetx_merge_perm(Wq, pn, pm, Wp, s, w_scale)
+        wcode = P.I8
+    else:
+        W0 = t(inp["W0"], bf)
+        Wp = torch.empty_like(W0)
+        P.poetx_merge_perm(W0, pn, pm, Wp)
+        wcode = P.BF16 if wl.wdt == "bf16" else P.F32
+    acode = P.BF16 if wl.act == "bf16" else P.F32
+    esz = 2 if wl.act == "bf16" else 4
+
+    def make(variant):
+        L = P.make_layer(m, n, b, acode, wcode, P.FAST if variant == "fast" else P.MEM, pm, pn,
+                         Wp, qR, qP, w_scale)
+        bufs = dict(L=L, saved=P.workspace(P.poetx_layer_saved_bytes(L, N), dev),
+                    wsf=P.workspace(P.poetx_layer_workspace_bytes(L, N, 0), dev),
+                    wsb=P.workspace(P.poetx_layer_workspace_bytes(L, N, 1), dev),
+                    y=torch.empty(N, n, dtype=bf, device=dev),
+                    dx=torch.empty(N, m, dtype=bf, device=dev),
+                    dqR=torch.empty_like(qR), dqP=torch.empty_like(qP))
+        return bufs
+
+    def step(B, xx=None, dyy=None):
+        xx = x if xx is None else xx
+        dyy = dy if dyy is None else dyy
+        P.poetx_layer_fwd(B["L"], xx, B["y"], B["saved"], B["wsf"])
+        P.poetx_layer_bwd(B["L"], xx, dyy, B["saved"], B["dx"], B["dqR"], B["dqP"], B["wsb"])
+
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def timed_steps(B, K, W):
+        for _ in range(W):
+            step(B)
+        torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(K)]
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        c0 = P.poetx_launch_count()
+        w0 = time.time()
+        for e0, e1 in evs:
+            flush.zero_()  # untimed L2 flush between steps
+            e0.record()
+            step(B)
+            e1.record()
+        torch.cuda.synchronize()
+        w1 = time.time()
+        if world > 1:
+            dist.barrier()
+        launches = P.poetx_launch_count() - c0
+        ms = [e0.elapsed_time(e1) for e0, e1 in evs]
+        return ms, launches, (w0, w1)
+
+    variant = args.variant if wl.wdt != "i8" else "mem"
+    main_b = make(variant)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    ms, launches, (w0, w1) = timed_steps(main_b, args.steps, max(3, args.warmup))
+    time.sleep(0.3)
+    clocks.stop()
+    ms_step = statistics.mean(ms)
+    if world > 1:
+        tt = torch.tensor([ms_step], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms_step = float(tt.item())
+    value = world * N / (ms_step * 1e-3)
+
+    # the other variant, same protocol, fewer steps
+    other = {}
+    if wl.wdt != "i8":
+        ov = "mem" if variant == "fast" else "fast"
+        ob = make(ov)
+        oms, _, _ = timed_steps(ob, max(50, args.steps // 10), 5)
+        other[ov] = {"tokens_per_s": N / (statistics.mean(oms) * 1e-3),
+                     "ms_per_step": statistics.mean(oms)}
+        del ob
+
+    # per-stage times inside the same layer calls (library stage events), same flushes
+    P.poetx_profile_enable(True)
+    P.poetx_profile_collect()
+    stage_ms = {}
+    prof_steps = 20
+    for _ in range(prof_steps):
+        flush.zero_()
+        torch.cuda.synchronize()
+        P.poetx_profile_collect()
+        step(main_b)
+        for name, t_ms in P.poetx_profile_collect():
+            stage_ms.setdefault(name, []).append(t_ms)
+    P.poetx_profile_enable(False)
+    stages = {k: {"launches_per_step": len(v) / prof_steps, "ms_per_step": sum(v) / prof_steps,
+                  "ms_per_launch": sum(v) / len(v)} for k, v in stage_ms.items()}
+
+    pk = peaks()
+    w_launch_ms = stages.get("wprime_gemm", {}).get("ms_per_launch")
+    flops = 2.0 * N * m * n
+    achieved = flops / (w_launch_ms * 1e-3) / 1e12 if w_launch_ms else None
+    traffic = None
+    prof_json = os.path.join(ROOT, "profiles", f"wprime_gemm_{wl.name}.json")
+    if os.path.exists(prof_json):
+        try:
+            pj = json.load(open(prof_json))
+            import hashlib
+            src = open(os.path.join(ROOT, "orthogonal_reparameterized_gb300", "csrc",
+                                    "umma_gemm.cu"), "rb").read()
+            if pj.get("kernel_source_sha256") == hashlib.sha256(src).hexdigest():
+                traffic = pj.get("dram_bytes_per_launch")
+        except (OSError, ValueError, KeyError):
+            traffic = None
+    roofline = {"kernel": "wprime_gemm (tcgen05 W' contraction, fwd B = A W'^T and bwd "
+                          "dA = dB W', 2 N m n flops per launch)",
+                "bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": (achieved / pk["bf16_tflops"]) if achieved else None,
+                "traffic": traffic,
+                "peak_source": f"{pk['source']} dense bf16 burst (MEASURED_PEAKS.json)"}
+
+    # HBM-bound stages against the measured copy bandwidth: every launch of these reads one
+    # [N, D] activation and writes one (D = m = n for the benchmarked square layers)
+    hbm = {}
+    for name in ("perm_gather", "perm_scatter", "blockdiag_mm"):
+        if name in stages and m == n:
+            by = 2.0 * N * m * esz
+            gbs = by / (stages[name]["ms_per_launch"] * 1e-3) / 1e9
+            hbm[name] = {"algorithmic_bytes_per_launch": by, "achieved_gbs": gbs,
+                         "frac_of_hbm": gbs / pk["hbm_gbs"]}
+
+    # CNP blocks/s (standalone, both sides' blocks)
+    nblk = (m + n) // b
+    qcat = torch.cat([qR, qP], 0).contiguous()
+    Gb = torch.empty(nblk, b, b, dtype=torch.bfloat16, device=dev)
+    dG = torch.randn(1, nblk, b, b, device=dev)
+    dq = torch.empty_like(qcat)
+    wsc = P.workspace(max(P.poetx_cnp_workspace_bytes(nblk, b, 0),
+                          P.poetx_cnp_workspace_bytes(nblk, b, 1)), dev)
+    for _ in range(5):
+        P.poetx_cnp_fwd(qcat, b, G_bf16=Gb, ws=wsc)
+        P.poetx_cnp_bwd(qcat, dG, b, dq, ws=wsc)
+    cf, cb = [], []
+    for _ in range(50):
+        flush.zero_()
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        e[0].record()
+        P.poetx_cnp_fwd(qcat, b, G_bf16=Gb, ws=wsc)
+        e[1].record()
+        P.poetx_cnp_bwd(qcat, dG, b, dq, ws=wsc)
+        e[2].record()
+        torch.cuda.synchronize()
+        cf.append(e[0].elapsed_time(e[1]))
+        cb.append(e[1].elapsed_time(e[2]))
+    fwd_ms, bwd_ms = statistics.median(cf), statistics.median(cb)
+    ffma_peak = 152 * 128 * 2 * pk["sm_max_mhz"] * 1e6 / 1e12  # TFLOP/s, FP32 FFMA
+    cnp = {"blocks": nblk, "b": b, "fwd_blocks_per_s": nblk / (fwd_ms * 1e-3),
+           "bwd_blocks_per_s": nblk / (bwd_ms * 1e-3),
+           "fwd_bwd_blocks_per_s": nblk / ((fwd_ms + bwd_ms) * 1e-3),
+           "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
+           "roofline": {"bound": "alu", "unit": "TFLOP/s",
+                        "fwd_achieved": 3 * b ** 3 * 2 * nblk / (fwd_ms * 1e-3) / 1e12,
+                        "bwd_achieved": 8 * b ** 3 * 2 * nblk / (bwd_ms * 1e-3) / 1e12,
+                        "peak": ffma_peak,
+                        "peak_source": "152 SMs x 128 FP32 lanes x 2 flop x max SM clock"}}
+    del dG, Gb, wsc
+
+    # end to end through the C ABI with host buffers (pinned), copies inside the timed region
+    hx = x.cpu().pin_memory()
+    hdy = dy.cpu().pin_memory()
+    hy = torch.empty(N, n, dtype=bf).pin_memory()
+    hdx = torch.empty(N, m, dtype=bf).pin_memory()
+    hqR = torch.empty(qR.shape).pin_memory()
+    hqP = torch.empty(qP.shape).pin_memory()
+    dx_in = torch.empty_like(x)
+    ddy_in = torch.empty_like(dy)
+    e2e_ms = []
+    for i in range(max(3, args.warmup // 4) + 50):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        dx_in.copy_(hx, non_blocking=True)
+        ddy_in.copy_(hdy, non_blocking=True)
+        step(main_b, dx_in, ddy_in)
+        hy.copy_(main_b["y"], non_blocking=True)
+        hdx.copy_(main_b["dx"], non_blocking=True)
+        hqR.copy_(main_b["dqR"], non_blocking=True)
+        hqP.copy_(main_b["dqP"], non_blocking=True)
+        e1.record()
+        torch.cuda.synchronize()
+        if i >= max(3, args.warmup // 4):
+            e2e_ms.append(e0.elapsed_time(e1))
+    e2e_t = statistics.mean(e2e_ms)
+    h2d = (x.numel() + dy.numel()) * esz
+    d2h = (N * n + N * m) * esz + (qR.numel() + qP.numel()) * 4
+    if world > 1:
+        tt = torch.tensor([e2e_t], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_t = float(tt.item())
+    assert P.poetx_get_device_error() == 0, "device error word set"
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        try:
+            cpu = cpu_baseline(wl)
+        except Exception as ex:  # reported, not fatal
+            cpu = {"error": str(ex)[:300]}
+
+    if rank == 0:
+        out = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": wl.act, "data": "synthetic (seeded Philox inputs, shapes and "
+                                     "distributions of the workload)",
+            "config": {"workload": wl.name, "m": m, "n": n, "b": b, "tokens_per_gpu": N,
+                       "variant": variant, "wdt": wl.wdt,
+                       "parallelism": f"replicas x{world} (token-sharded, no collective)",
+                       "l2": "flushed between timed steps (512 MiB memset outside the events)"},
+            "variants": {variant: {"tokens_per_s": N / (ms_step * 1e-3), "ms_per_step": ms_step},
+                         **other},
+            "cnp": cnp, "stages": stages, "hbm_stages": hbm, "roofline": roofline,
+            "cpu_baseline": cpu,
+            "e2e": {"value": world * N / (e2e_t * 1e-3), "unit": "tokens/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "ms_per_step": e2e_t},
+            "gpu_launches": launches, "gpu_launches_per_step": launches / max(1, args.steps),
+            "clocks": clocks.summary(w0, w1),
+        }
+        print(json.dumps(out))
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

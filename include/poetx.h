@@ -76,6 +76,19 @@ poetx_status poetx_selftest_timeout(unsigned int timeout_us, cudaStream_t stream
  * (fp32 accumulation, same rounding of the stored results).  Process-wide. */
 poetx_status poetx_set_gemm_engine(int engine);
 
+/* Number of kernels this library has launched in the process so far (host counter). */
+unsigned long long poetx_launch_count(void);
+
+/* Diagnostic per-stage timing.  While enabled (on != 0), every kernel launch of the library
+ * records a CUDA event on its stream, and poetx_layer_fwd / poetx_layer_bwd record a
+ * reference event when they start.  poetx_profile_collect synchronizes those events and
+ * writes, for each launch since the last collect, its stage id and the milliseconds since
+ * the previous event (host arrays of `cap` entries, nullable); it returns the number of
+ * launches timed and forgets them.  Stage ids are named by poetx_stage_name. */
+poetx_status poetx_profile_enable(int on);
+int poetx_profile_collect(int* stage, float* ms, int cap);
+const char* poetx_stage_name(int stage);
+
 /* ----------------------------------------------------------------------------------------
  * Cayley-Neumann parameterization (POET-X summary page, "Core method" section 4)
  * ------------------------------------------------------------------------------------- */

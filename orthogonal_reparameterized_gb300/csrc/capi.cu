@@ -1,5 +1,7 @@
 // Status strings, the per-device error word and the bounded-wait self test.
+#include <atomic>
 #include <mutex>
+#include <vector>
 
 #include "common.cuh"
 
@@ -36,6 +38,43 @@ int sm_count() {
   }
   return g_sms[dev];
 }
+
+static std::atomic<unsigned long long> g_launches{0};
+static std::atomic<int> g_prof_on{0};
+static std::mutex g_prof_mu;
+struct ProfRec {
+  int stage;  // -1: reference mark
+  cudaEvent_t ev;
+};
+static std::vector<ProfRec> g_prof;
+static std::vector<cudaEvent_t> g_prof_pool;
+
+static void prof_record(cudaStream_t s, int stage) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  cudaEvent_t ev = nullptr;
+  if (!g_prof_pool.empty()) {
+    ev = g_prof_pool.back();
+    g_prof_pool.pop_back();
+  } else if (cudaEventCreate(&ev) != cudaSuccess) {
+    return;
+  }
+  cudaEventRecord(ev, s);
+  g_prof.push_back({stage, ev});
+}
+
+void after_launch(cudaStream_t s, int stage) {
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  if (g_prof_on.load(std::memory_order_relaxed)) prof_record(s, stage);
+}
+
+void prof_begin(cudaStream_t s) {
+  if (g_prof_on.load(std::memory_order_relaxed)) prof_record(s, -1);
+}
+
+static const char* kStageNames[ST_COUNT] = {
+    "triu_unpack", "cnp_q2", "cnp_g", "cnp_sum_partials", "cnp_m1", "cnp_qbar", "triu_grad_pack",
+    "perm_gather", "perm_scatter", "blockdiag_mm", "wprime_gemm", "blockdiag_wgrad",
+    "quantize_rows_int8", "merge_perm"};
 
 // Waits on a shared-memory barrier that nothing arrives on, for at most limit_ns, then
 // records the timeout and returns.
@@ -88,4 +127,35 @@ extern "C" poetx_status poetx_selftest_timeout(unsigned int timeout_us, cudaStre
   selftest_timeout_kernel<<<1, 32, 0, stream>>>(w, 1000ull * timeout_us);
   POETX_CUDA_TRY(cudaGetLastError());
   return POETX_OK;
+}
+
+extern "C" unsigned long long poetx_launch_count(void) { return g_launches.load(); }
+
+extern "C" poetx_status poetx_profile_enable(int on) {
+  g_prof_on.store(on ? 1 : 0);
+  return POETX_OK;
+}
+
+extern "C" const char* poetx_stage_name(int stage) {
+  return (stage >= 0 && stage < ST_COUNT) ? kStageNames[stage] : "unknown";
+}
+
+extern "C" int poetx_profile_collect(int* stage, float* ms, int cap) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  int n = 0;
+  cudaEvent_t prev = nullptr;
+  for (const ProfRec& r : g_prof) {
+    cudaEventSynchronize(r.ev);
+    if (r.stage >= 0 && prev && n < cap) {
+      float t = 0.f;
+      cudaEventElapsedTime(&t, prev, r.ev);
+      if (stage) stage[n] = r.stage;
+      if (ms) ms[n] = t;
+      ++n;
+    }
+    prev = r.ev;
+  }
+  for (const ProfRec& r : g_prof) g_prof_pool.push_back(r.ev);
+  g_prof.clear();
+  return n;
 }

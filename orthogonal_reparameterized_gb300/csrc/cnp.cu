@@ -130,7 +130,7 @@ __global__ void __launch_bounds__((T / 4) * (T / 4)) cnp_gemm_kernel(CnpGemm g) 
   }
 }
 
-poetx_status launch_cnp_gemm(const CnpGemm& g, int nblk, cudaStream_t s) {
+poetx_status launch_cnp_gemm(const CnpGemm& g, int nblk, int stage, cudaStream_t s) {
   if (g.b >= 64) {
     dim3 grid(ceil_div(g.b, 64), ceil_div(g.b, 64), nblk);
     cnp_gemm_kernel<64><<<grid, 256, 0, s>>>(g);
@@ -139,6 +139,7 @@ poetx_status launch_cnp_gemm(const CnpGemm& g, int nblk, cudaStream_t s) {
     cnp_gemm_kernel<32><<<grid, 64, 0, s>>>(g);
   }
   POETX_CUDA_TRY(cudaGetLastError());
+  after_launch(s, stage);
   return POETX_OK;
 }
 
@@ -174,7 +175,7 @@ poetx_status cnp_forward(const float* q, int nblk, int b, float* Qs, float* Q2, 
   g.B[0] = op1(Qs, 1.f);
   g.mirror = 1;
   g.out_f32 = Q2;
-  POETX_TRY(launch_cnp_gemm(g, nblk, s));
+  POETX_TRY(launch_cnp_gemm(g, nblk, ST_CNP_Q2, s));
   CnpGemm h{};
   h.b = b;
   h.nseg = 1;
@@ -188,7 +189,7 @@ poetx_status cnp_forward(const float* q, int nblk, int b, float* Qs, float* Q2, 
   h.out_f32 = G_f32;
   h.out_bf16 = static_cast<__nv_bfloat16*>(G_bf16);
   h.out_bf16_t = static_cast<__nv_bfloat16*>(Gt_bf16);
-  return launch_cnp_gemm(h, nblk, s);
+  return launch_cnp_gemm(h, nblk, ST_CNP_G, s);
 }
 
 poetx_status cnp_backward(const float* q, const float* Q2in, const float* dG, int splits, int nblk,
@@ -210,7 +211,7 @@ poetx_status cnp_backward(const float* q, const float* Q2in, const float* dG, in
     g.B[0] = op1(Qs, 1.f);
     g.mirror = 1;
     g.out_f32 = Q2;
-    POETX_TRY(launch_cnp_gemm(g, nblk, s));
+    POETX_TRY(launch_cnp_gemm(g, nblk, ST_CNP_Q2, s));
     Q2in = Q2;
   }
   const float* Xp = dG;
@@ -219,6 +220,7 @@ poetx_status cnp_backward(const float* q, const float* Q2in, const float* dG, in
     const int grid = (int)((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096);
     sum_partials_kernel<<<grid, 256, 0, s>>>(dG, splits, n, X);
     POETX_CUDA_TRY(cudaGetLastError());
+    after_launch(s, ST_CNP_SUM);
     Xp = X;
   }
   // M1 = X P + P X, P = -Q
@@ -230,7 +232,7 @@ poetx_status cnp_backward(const float* q, const float* Q2in, const float* dG, in
   m.A[1] = op1(Qs, -1.f);
   m.B[1] = op1(Xp, 1.f);
   m.out_f32 = M1;
-  POETX_TRY(launch_cnp_gemm(m, nblk, s));
+  POETX_TRY(launch_cnp_gemm(m, nblk, ST_CNP_M1, s));
   // Qbar = (2X + M1) Q2 + (Q2 - 2Q) M1 + 2X + 2M1
   CnpGemm r{};
   r.b = b;
@@ -244,7 +246,7 @@ poetx_status cnp_backward(const float* q, const float* Q2in, const float* dG, in
   r.E2 = M1;
   r.e2 = 2.f;
   r.out_f32 = Qbar;
-  POETX_TRY(launch_cnp_gemm(r, nblk, s));
+  POETX_TRY(launch_cnp_gemm(r, nblk, ST_CNP_QBAR, s));
   return launch_triu_grad_pack(Qbar, nblk, b, dq, accumulate, s);
 }
 

@@ -43,6 +43,18 @@ inline size_t dtype_size(poetx_dtype dt) {
 // Number of SMs of the current device (cached per device).
 int sm_count();
 
+// Stages of the hot path, for the launch counter and the optional per-stage event timing.
+enum Stage : int {
+  ST_TRIU_UNPACK = 0, ST_CNP_Q2, ST_CNP_G, ST_CNP_SUM, ST_CNP_M1, ST_CNP_QBAR, ST_TRIU_PACK,
+  ST_PERM_GATHER, ST_PERM_SCATTER, ST_BLOCKDIAG, ST_WPRIME, ST_WGRAD, ST_QUANTIZE, ST_MERGE,
+  ST_COUNT
+};
+// Called after every kernel launch of the library: counts it and, when stage timing is on,
+// records an event on the launching stream.
+void after_launch(cudaStream_t s, int stage);
+// Records the reference event that the first stage of a call is timed from.
+void prof_begin(cudaStream_t s);
+
 // ------------------------------------------------------------------------------------
 // device helpers
 // ------------------------------------------------------------------------------------

@@ -50,6 +50,7 @@ poetx_status launch_triu_unpack(const float* q, int nblk, int b, float* Q, cudaS
   dim3 grid(1, b, nblk);
   triu_unpack_kernel<<<grid, threads, 0, s>>>(q, b, Q);
   POETX_CUDA_TRY(cudaGetLastError());
+  after_launch(s, ST_TRIU_UNPACK);
   return POETX_OK;
 }
 
@@ -60,6 +61,7 @@ poetx_status launch_triu_grad_pack(const float* Qbar, int nblk, int b, float* dq
   dim3 grid(1, b - 1, nblk);
   triu_grad_pack_kernel<<<grid, threads, 0, s>>>(Qbar, b, dq, accumulate);
   POETX_CUDA_TRY(cudaGetLastError());
+  after_launch(s, ST_TRIU_PACK);
   return POETX_OK;
 }
 
@@ -135,6 +137,7 @@ static poetx_status launch_perm_rows_t(const void* X, long long N, int D, const 
   k<<<grid, 256, smem, s>>>(static_cast<const uint8_t*>(X), N, D, perm, static_cast<uint8_t*>(Y),
                            src_rows, scale, scale_out);
   POETX_CUDA_TRY(cudaGetLastError());
+  after_launch(s, src_rows ? ST_MERGE : (SCATTER ? ST_PERM_SCATTER : ST_PERM_GATHER));
   return POETX_OK;
 }
 
@@ -189,6 +192,7 @@ poetx_status launch_quantize(const float* W, int n, int m, int8_t* Wq, float* sc
   if (n == 0) return POETX_OK;
   quantize_rows_kernel<<<n, 256, 0, s>>>(W, m, Wq, scale);
   POETX_CUDA_TRY(cudaGetLastError());
+  after_launch(s, ST_QUANTIZE);
   return POETX_OK;
 }
 

@@ -37,6 +37,7 @@ struct SimtGemm {
   int ksplit;
   int kchunk;
   long long scs;
+  int stage;  // Stage of the hot path this product serves (launch accounting)
 };
 poetx_status launch_simt_gemm(poetx_dtype ta, poetx_dtype tb, poetx_dtype tc, const SimtGemm& g,
                               cudaStream_t s);

@@ -56,6 +56,7 @@ poetx_status blockdiag_impl(poetx_dtype dt, const void* X, long long N, int nblk
   g.C = Y; g.scm = D; g.scn = 1; g.scb = b;
   g.colscale = col_scale; g.colscale_bstride = b;
   g.ksplit = 1; g.kchunk = b;
+  g.stage = ST_BLOCKDIAG;
   return launch_simt_gemm(dt, dt, dt, g, s);
 }
 
@@ -76,6 +77,7 @@ poetx_status wgrad_impl(poetx_dtype dt, const void* X, const void* dY, long long
   g.C = dG; g.scm = b; g.scn = 1; g.scb = (long long)b * b;
   g.ksplit = splits; g.kchunk = wgrad_chunk(N, splits);
   g.scs = (long long)nblk * b * b;
+  g.stage = ST_WGRAD;
   // splits beyond the last token get an empty K range and write zeros
   return launch_simt_gemm(dt, dt, POETX_F32, g, s);
 }
@@ -102,6 +104,7 @@ poetx_status wprime_impl(poetx_dtype act, poetx_dtype wdt, const void* A, long l
     g.scm = m; g.scn = 1;
   }
   g.kchunk = g.K;
+  g.stage = ST_WPRIME;
   return launch_simt_gemm(act, wdt, act, g, s);
 }
 
@@ -221,6 +224,7 @@ extern "C" poetx_status poetx_layer_fwd(const poetx_layer* L, const void* x, int
   const poetx_dtype act = L->act;
   const bool f32 = act == POETX_F32;
   const size_t as = dtype_size(act);
+  prof_begin(stream);
   // S1-S2: both CNPs; G in the activation precision and Q^2 kept for the backward
   POETX_TRY(cnp_forward(L->q_R, m / b, b, at<float>(ws, p.f_Qs), at<float>(saved, p.Q2R),
                         f32 ? at<float>(saved, p.GR) : nullptr, f32 ? nullptr : at(saved, p.GR),
@@ -255,6 +259,7 @@ extern "C" poetx_status poetx_layer_bwd(const poetx_layer* L, const void* x, con
   const int b = L->b, m = L->m, n = L->n;
   const poetx_dtype act = L->act;
   const size_t as = dtype_size(act);
+  prof_begin(stream);
   void* xt = at(ws, p.b_xt);
   void* dzt = at(ws, p.b_dzt);
   void* dB = at(ws, p.b_dB);

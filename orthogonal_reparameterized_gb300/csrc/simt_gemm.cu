@@ -85,6 +85,7 @@ poetx_status launch_t(const SimtGemm& g, cudaStream_t s) {
   if (grid.y > 65535 || grid.z > 65535) return POETX_ERR_SHAPE;
   simt_gemm_kernel<TA, TB, TC><<<grid, THREADS, 0, s>>>(g);
   POETX_CUDA_TRY(cudaGetLastError());
+  after_launch(s, g.stage);
   return POETX_OK;
 }
 

@@ -303,6 +303,7 @@ bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, u
 template <int BN, int STAGES, bool A_MN, bool B_MN, bool OUT_F32>
 poetx_status launch(const CUtensorMap& ta, const CUtensorMap& tb, const UmmaParams& p, dim3 grid,
                     cudaStream_t s) {
+  const int stage = p.mode == MODE_PLAIN ? ST_WPRIME : (p.mode == MODE_BLOCKDIAG ? ST_BLOCKDIAG : ST_WGRAD);
   auto k = umma_gemm_kernel<BN, STAGES, A_MN, B_MN, OUT_F32>;
   constexpr int smem = STAGES * (BM * BK * 2 + BN * BK * 2) + 1024 + 256;
   static std::once_flag once;
@@ -314,6 +315,7 @@ poetx_status launch(const CUtensorMap& ta, const CUtensorMap& tb, const UmmaPara
   if (grid.x == 0 || grid.y == 0 || grid.z == 0) return POETX_OK;
   k<<<grid, 192, smem, s>>>(ta, tb, p);
   POETX_CUDA_TRY(cudaGetLastError());
+  after_launch(s, stage);
   return POETX_OK;
 }
 

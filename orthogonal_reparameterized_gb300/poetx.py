@@ -42,6 +42,10 @@ _SIGS = {
     "poetx_get_device_error": (_i, [_vp]),
     "poetx_selftest_timeout": (_i, [ctypes.c_uint, _vp]),
     "poetx_set_gemm_engine": (_i, [_i]),
+    "poetx_launch_count": (ctypes.c_ulonglong, []),
+    "poetx_profile_enable": (_i, [_i]),
+    "poetx_profile_collect": (_i, [ctypes.POINTER(_i), ctypes.POINTER(_f), _i]),
+    "poetx_stage_name": (ctypes.c_char_p, [_i]),
     "poetx_cnp_workspace_bytes": (_sz, [_i, _i, _i]),
     "poetx_cnp_fwd": (_i, [_vp, _i, _i, _i, _vp, _vp, _vp, _vp, _sz, _vp]),
     "poetx_cnp_bwd": (_i, [_vp, _vp, _i, _i, _i, _i, _vp, _i, _vp, _sz, _vp]),
@@ -113,6 +117,22 @@ def poetx_selftest_timeout(timeout_us: int, stream=None):
 
 def poetx_set_gemm_engine(engine: int):
     _check("poetx_set_gemm_engine", lib().poetx_set_gemm_engine(engine))
+
+
+def poetx_launch_count() -> int:
+    return lib().poetx_launch_count()
+
+
+def poetx_profile_enable(on: bool):
+    _check("poetx_profile_enable", lib().poetx_profile_enable(int(bool(on))))
+
+
+def poetx_profile_collect(cap: int = 4096):
+    """[(stage name, milliseconds)] for every launch timed since the last collect."""
+    st = (_i * cap)()
+    ms = (_f * cap)()
+    n = lib().poetx_profile_collect(st, ms, cap)
+    return [(lib().poetx_stage_name(st[k]).decode(), float(ms[k])) for k in range(n)]
 
 
 def dtype_code(t: torch.Tensor) -> int:
