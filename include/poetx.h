@@ -120,6 +120,27 @@ poetx_status poetx_cnp_bwd(const float* q, const float* dG, int splits, int nblk
                            int order, float* dq, int accumulate, void* ws, size_t ws_bytes,
                            cudaStream_t stream);
 
+/* Largest nblk * b * b accepted by poetx_cnp_fwd_noalloc: 2 Mi elements (for example 32
+ * blocks of 256 or 8 blocks of 512).  Its fixed scratch holds twice that many floats. */
+#define POETX_CNP_NOALLOC_MAX_ELEMS (2 * 1024 * 1024)
+
+/* poetx_cnp_fwd for callers that cannot allocate device memory: a plugin or extension inside
+ * a host application that owns every device allocation and lends it none, or a code path
+ * where a cudaMalloc (which may synchronize the whole device) is not acceptable after
+ * set-up.  No counterpart in the paper: it computes exactly what poetx_cnp_fwd computes, with
+ * the same kernels, and takes the same arguments minus the workspace.
+ *   Scratch: a fixed 16 MiB fp32 array in the library's device image; every GPU that loads
+ *   the library holds it until the process exits.  The first call on a device looks up the
+ *   array's device address (cudaGetSymbolAddress, with that device current); make that first
+ *   call before any stream capture.  All calls on a device share the array and it keeps the
+ *   last call's contents: calls that overlap on the GPU (on streams not ordered with each
+ *   other) race and give wrong results, so order them.  Nothing in it needs to start at zero:
+ *   every element read is first written by the same call.
+ *   Errors: nblk * b * b > POETX_CNP_NOALLOC_MAX_ELEMS returns POETX_ERR_WORKSPACE before
+ *   anything is launched; the other checks are those of poetx_cnp_fwd.  Allocates nothing. */
+poetx_status poetx_cnp_fwd_noalloc(const float* q, int nblk, int b, int order, float* G_f32,
+                                   void* G_bf16, void* Gt_bf16, cudaStream_t stream);
+
 /* Step S1 on its own: Q_f32 [nblk, b, b] = unpacked skew blocks of q. */
 poetx_status poetx_triu_unpack(const float* q, int nblk, int b, float* Q_f32,
                                cudaStream_t stream);

@@ -49,6 +49,7 @@ _SIGS = {
     "poetx_cnp_workspace_bytes": (_sz, [_i, _i, _i]),
     "poetx_cnp_fwd": (_i, [_vp, _i, _i, _i, _vp, _vp, _vp, _vp, _sz, _vp]),
     "poetx_cnp_bwd": (_i, [_vp, _vp, _i, _i, _i, _i, _vp, _i, _vp, _sz, _vp]),
+    "poetx_cnp_fwd_noalloc": (_i, [_vp, _i, _i, _i, _vp, _vp, _vp, _vp]),
     "poetx_triu_unpack": (_i, [_vp, _i, _i, _vp, _vp]),
     "poetx_triu_grad_pack": (_i, [_vp, _i, _i, _vp, _i, _vp]),
     "poetx_perm_gather": (_i, [_i, _vp, _i, _i, _vp, _vp, _vp]),
@@ -155,6 +156,17 @@ def poetx_cnp_fwd(q, b, G_f32=None, G_bf16=None, Gt_bf16=None, ws=None, order=3,
     _check("poetx_cnp_fwd", lib().poetx_cnp_fwd(_p(q), nblk, b, order, _p(G_f32), _p(G_bf16),
                                                 _p(Gt_bf16), _p(ws), ws.numel(),
                                                 _stream(stream)))
+
+
+CNP_NOALLOC_MAX_ELEMS = 2 * 1024 * 1024
+
+
+def poetx_cnp_fwd_noalloc(q, b, G_f32=None, G_bf16=None, Gt_bf16=None, order=3, stream=None):
+    """poetx_cnp_fwd without a workspace: its scratch is a fixed array inside the library
+    (for callers that cannot allocate device memory; see include/poetx.h)."""
+    _check("poetx_cnp_fwd_noalloc", lib().poetx_cnp_fwd_noalloc(_p(q), q.shape[0], b, order,
+                                                                _p(G_f32), _p(G_bf16),
+                                                                _p(Gt_bf16), _stream(stream)))
 
 
 def poetx_cnp_bwd(q, dG, b, dq, accumulate=False, ws=None, order=3, stream=None):
