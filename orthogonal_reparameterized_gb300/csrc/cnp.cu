@@ -22,6 +22,7 @@
 // (XS + SX) T + S^2 (XP + PX) with S = I + P, T = I + P^2 = I + Q2, S^2 = I - 2Q + Q2;
 // expanding the products gives the expression above.  Work per block: forward 3 b^3 FMA
 // (Q2 half by symmetry, then one full product), backward 5 b^3 FMA.
+#include "cnp_umma.h"
 #include "common.cuh"
 #include "kernels.h"
 
@@ -29,27 +30,8 @@ namespace poetx {
 
 namespace {
 
-struct Operand {
-  const float* p1;
-  float c1;
-  const float* p2;  // nullable
-  float c2;
-};
-
-struct CnpGemm {
-  int b;
-  int nseg;
-  Operand A[2], B[2];
-  const float* E1;  // epilogue terms (nullable)
-  float e1;
-  const float* E2;
-  float e2;
-  float eI;
-  int mirror;  // result is symmetric: compute tiles ti <= tj only and mirror them
-  float* out_f32;
-  __nv_bfloat16* out_bf16;
-  __nv_bfloat16* out_bf16_t;
-};
+using Operand = CnpTerm;
+using CnpGemm = CnpProduct;
 
 constexpr int TK = 16;
 
@@ -131,6 +113,12 @@ __global__ void __launch_bounds__((T / 4) * (T / 4)) cnp_gemm_kernel(CnpGemm g) 
 }
 
 poetx_status launch_cnp_gemm(const CnpGemm& g, int nblk, int stage, cudaStream_t s) {
+  if (nblk == 0) return POETX_OK;
+  if (use_tensor_cores() && cnp_umma_ok(g.b)) {
+    POETX_TRY(cnp_umma_product(g, nblk, s));
+    after_launch(s, stage);
+    return POETX_OK;
+  }
   if (g.b >= 64) {
     dim3 grid(ceil_div(g.b, 64), ceil_div(g.b, 64), nblk);
     cnp_gemm_kernel<64><<<grid, 256, 0, s>>>(g);
@@ -146,13 +134,23 @@ poetx_status launch_cnp_gemm(const CnpGemm& g, int nblk, int stage, cudaStream_t
 Operand op1(const float* p, float c) { return Operand{p, c, nullptr, 0.f}; }
 Operand op2(const float* p, float c, const float* q, float d) { return Operand{p, c, q, d}; }
 
-// X = sum_s dG[s] in the order s = 0, 1, ..., S-1.
-__global__ void sum_partials_kernel(const float* __restrict__ dG, int S, long long n,
+// X[j] = sum_s dG_side[s][j'] in the order s = 0, 1, ..., S_side - 1, for the blocks of
+// both sides (j' = j for side 0, j - n0 for side 1).
+__global__ void sum_partials_kernel(const float* __restrict__ dG0, int S0, long long n0e,
+                                    const float* __restrict__ dG1, int S1, long long n1e,
                                     float* __restrict__ X) {
+  const long long n = n0e + n1e;
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
        i += (long long)gridDim.x * blockDim.x) {
-    float a = dG[i];
-    for (int s = 1; s < S; ++s) a += dG[(long long)s * n + i];
+    float a;
+    if (i < n0e) {
+      a = dG0[i];
+      for (int s = 1; s < S0; ++s) a += dG0[(long long)s * n0e + i];
+    } else {
+      const long long k = i - n0e;
+      a = dG1[k];
+      for (int s = 1; s < S1; ++s) a += dG1[(long long)s * n1e + k];
+    }
     X[i] = a;
   }
 }
@@ -164,10 +162,12 @@ size_t blk_bytes(int nblk, int b) { return align_up((size_t)nblk * b * b * sizeo
 size_t cnp_fwd_scratch_bytes(int nblk, int b) { return 2 * blk_bytes(nblk, b); }
 size_t cnp_bwd_scratch_bytes(int nblk, int b) { return 5 * blk_bytes(nblk, b); }
 
-poetx_status cnp_forward(const float* q, int nblk, int b, float* Qs, float* Q2, float* G_f32,
-                         void* G_bf16, void* Gt_bf16, cudaStream_t s) {
+poetx_status cnp_forward_sides(const CnpSides& q, int b, float* Qs, float* Q2, float* G_f32,
+                               void* G_bf16, void* Gt_bf16, cudaStream_t s) {
+  const int nblk = q.n[0] + q.n[1];
   if (nblk == 0) return POETX_OK;
-  POETX_TRY(launch_triu_unpack(q, nblk, b, Qs, s));
+  POETX_TRY(launch_triu_unpack2(q.q[0], q.n[0], q.q[1], q.n[1], b, Qs, s));
+  // Q2 = Q Q (symmetric)
   CnpGemm g{};
   g.b = b;
   g.nseg = 1;
@@ -176,6 +176,7 @@ poetx_status cnp_forward(const float* q, int nblk, int b, float* Qs, float* Q2, 
   g.mirror = 1;
   g.out_f32 = Q2;
   POETX_TRY(launch_cnp_gemm(g, nblk, ST_CNP_Q2, s));
+  // G = Q2 (2Q + Q2) + I + 2Q + 2Q2
   CnpGemm h{};
   h.b = b;
   h.nseg = 1;
@@ -192,8 +193,16 @@ poetx_status cnp_forward(const float* q, int nblk, int b, float* Qs, float* Q2, 
   return launch_cnp_gemm(h, nblk, ST_CNP_G, s);
 }
 
-poetx_status cnp_backward(const float* q, const float* Q2in, const float* dG, int splits, int nblk,
-                          int b, float* dq, int accumulate, void* scratch, cudaStream_t s) {
+poetx_status cnp_forward(const float* q, int nblk, int b, float* Qs, float* Q2, float* G_f32,
+                         void* G_bf16, void* Gt_bf16, cudaStream_t s) {
+  CnpSides sides{{q, nullptr}, {nblk, 0}};
+  return cnp_forward_sides(sides, b, Qs, Q2, G_f32, G_bf16, Gt_bf16, s);
+}
+
+poetx_status cnp_backward_sides(const CnpSides& q, const float* Q2in, const float* const dG[2],
+                                const int splits[2], int b, float* const dq[2], int accumulate,
+                                void* scratch, cudaStream_t s) {
+  const int nblk = q.n[0] + q.n[1];
   if (nblk == 0) return POETX_OK;
   char* w = static_cast<char*>(scratch);
   const size_t bb = blk_bytes(nblk, b);
@@ -202,7 +211,7 @@ poetx_status cnp_backward(const float* q, const float* Q2in, const float* dG, in
   float* X = reinterpret_cast<float*>(w + 2 * bb);
   float* M1 = reinterpret_cast<float*>(w + 3 * bb);
   float* Qbar = reinterpret_cast<float*>(w + 4 * bb);
-  POETX_TRY(launch_triu_unpack(q, nblk, b, Qs, s));
+  POETX_TRY(launch_triu_unpack2(q.q[0], q.n[0], q.q[1], q.n[1], b, Qs, s));
   if (!Q2in) {
     CnpGemm g{};
     g.b = b;
@@ -214,40 +223,40 @@ poetx_status cnp_backward(const float* q, const float* Q2in, const float* dG, in
     POETX_TRY(launch_cnp_gemm(g, nblk, ST_CNP_Q2, s));
     Q2in = Q2;
   }
-  const float* Xp = dG;
-  if (splits > 1) {
-    const long long n = (long long)nblk * b * b;
+  // X = sum of the partials, both sides, fixed order
+  {
+    const long long n0e = (long long)q.n[0] * b * b, n1e = (long long)q.n[1] * b * b;
+    const long long n = n0e + n1e;
     const int grid = (int)((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096);
-    sum_partials_kernel<<<grid, 256, 0, s>>>(dG, splits, n, X);
+    sum_partials_kernel<<<grid, 256, 0, s>>>(dG[0], splits[0], n0e, dG[1], splits[1], n1e, X);
     POETX_CUDA_TRY(cudaGetLastError());
     after_launch(s, ST_CNP_SUM);
-    Xp = X;
   }
   // M1 = X P + P X, P = -Q
   CnpGemm m{};
   m.b = b;
   m.nseg = 2;
-  m.A[0] = op1(Xp, 1.f);
+  m.A[0] = op1(X, 1.f);
   m.B[0] = op1(Qs, -1.f);
   m.A[1] = op1(Qs, -1.f);
-  m.B[1] = op1(Xp, 1.f);
+  m.B[1] = op1(X, 1.f);
   m.out_f32 = M1;
   POETX_TRY(launch_cnp_gemm(m, nblk, ST_CNP_M1, s));
   // Qbar = (2X + M1) Q2 + (Q2 - 2Q) M1 + 2X + 2M1
   CnpGemm r{};
   r.b = b;
   r.nseg = 2;
-  r.A[0] = op2(Xp, 2.f, M1, 1.f);
+  r.A[0] = op2(X, 2.f, M1, 1.f);
   r.B[0] = op1(Q2in, 1.f);
   r.A[1] = op2(Q2in, 1.f, Qs, -2.f);
   r.B[1] = op1(M1, 1.f);
-  r.E1 = Xp;
+  r.E1 = X;
   r.e1 = 2.f;
   r.E2 = M1;
   r.e2 = 2.f;
   r.out_f32 = Qbar;
   POETX_TRY(launch_cnp_gemm(r, nblk, ST_CNP_QBAR, s));
-  return launch_triu_grad_pack(Qbar, nblk, b, dq, accumulate, s);
+  return launch_triu_grad_pack2(Qbar, q.n[0], q.n[1], b, dq[0], dq[1], accumulate, s);
 }
 
 }  // namespace poetx
@@ -285,5 +294,9 @@ extern "C" poetx_status poetx_cnp_bwd(const float* q, const float* dG, int split
   if (!q || !dG || !dq || !ws) return POETX_ERR_ARG;
   if (ws_bytes < cnp_bwd_scratch_bytes(nblk, b)) return POETX_ERR_WORKSPACE;
   if (!aligned16(ws) || !aligned16(dG)) return POETX_ERR_ALIGN;
-  return cnp_backward(q, nullptr, dG, splits, nblk, b, dq, accumulate, ws, stream);
+  CnpSides sides{{q, nullptr}, {nblk, 0}};
+  const float* const dGs[2] = {dG, nullptr};
+  const int sp[2] = {splits, 1};
+  float* const dqs[2] = {dq, nullptr};
+  return cnp_backward_sides(sides, nullptr, dGs, sp, b, dqs, accumulate, ws, stream);
 }

@@ -1,0 +1,434 @@
+// Tensor-core products of the Cayley-Neumann parameterization: fp32 accuracy from tcgen05
+// kind::tf32 by the 3-term split a*b ~ hi(a)hi(b) + hi(a)lo(b) + lo(a)hi(b), where
+// hi(v) = v with its 13 low mantissa bits cleared (exactly representable in tf32) and
+// lo(v) = v - hi(v) (exact in fp32); the dropped lo*lo term is below 2^-20 |a||b|.
+//
+// Each CNP product (POET-X summary page, "Core method" section 4, eq. 9 and its gradient)
+// is C_j = sum_seg opA_seg(j) . opB_seg(j) + epilogue, for every block j, where each operand
+// is a linear combination of at most two b x b fp32 arrays (Q, Q^2, X, M1).  The pipeline
+// of one CTA (one 128 x BN output tile of one block):
+//   warp 0     TMA: the raw fp32 tiles of every source array of the current K block
+//   warps 2-5  form v = c0*src0 + c1*src1 in shared memory and split it in place into
+//              hi(v) and lo(v) (same swizzled offsets, so the layout is kept)
+//   warp 1     three tcgen05.mma kind::tf32 per K=8 step into one fp32 TMEM accumulator
+//   warps 2-5  epilogue: TMEM -> registers, add the epilogue terms, store fp32 / bf16 / bf16^T
+// A tiles are K-major (row-major arrays), B tiles MN-major; 128-byte swizzle throughout.
+// Every wait is bounded (POETX_ERR_TIMEOUT on expiry, then drain, free TMEM, return).
+#include <mutex>
+
+#include "cnp_umma.h"
+#include "common.cuh"
+#include "kernels.h"
+
+namespace poetx {
+
+namespace {
+
+constexpr int BM = 128;
+constexpr int BK = 32;      // fp32 elements per 128-byte row
+constexpr int NMAPS = 4;
+
+struct CnpMaps {
+  CUtensorMap m[NMAPS];
+};
+
+struct TSrc {
+  int map;   // index into CnpMaps, -1 = absent
+  float coef;
+};
+struct TOp {
+  TSrc s[2];
+};
+
+struct CnpUParams {
+  int b;
+  int nseg;
+  int kb_per_seg;
+  TOp A[2], B[2];
+  const float* E1;
+  float e1;
+  const float* E2;
+  float e2;
+  float eI;
+  float* out_f32;
+  __nv_bfloat16* out_bf16;
+  __nv_bfloat16* out_bf16_t;
+  int* err;
+  unsigned long long limit_ns;
+};
+
+__host__ __device__ constexpr uint32_t tf32_idesc(int M, int N) {
+  return (1u << 4)                      // accumulator f32
+         | (2u << 7)                    // A: tf32
+         | (2u << 10)                   // B: tf32
+         | (0u << 15)                   // A K-major
+         | (1u << 16)                   // B MN-major
+         | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
+__device__ __forceinline__ void umma_tf32(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void fence_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// v = c0*x + c1*y, then x <- hi(v), y <- lo(v).
+__device__ __forceinline__ void combine_split(float4* x, float4* y, float c0, float c1, bool two) {
+  float4 a = *x;
+  float4 b = two ? *y : make_float4(0.f, 0.f, 0.f, 0.f);
+  float v[4] = {c0 * a.x, c0 * a.y, c0 * a.z, c0 * a.w};
+  if (two) {
+    v[0] = fmaf(c1, b.x, v[0]);
+    v[1] = fmaf(c1, b.y, v[1]);
+    v[2] = fmaf(c1, b.z, v[2]);
+    v[3] = fmaf(c1, b.w, v[3]);
+  }
+  float hi[4], lo[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    hi[i] = __uint_as_float(__float_as_uint(v[i]) & 0xFFFFE000u);
+    lo[i] = v[i] - hi[i];
+  }
+  *x = make_float4(hi[0], hi[1], hi[2], hi[3]);
+  *y = make_float4(lo[0], lo[1], lo[2], lo[3]);
+}
+
+template <int BN, int STAGES>
+__global__ void __launch_bounds__(192, 1)
+    cnp_umma_kernel(const __grid_constant__ CnpMaps maps, const CnpUParams p) {
+  constexpr uint32_t A_BYTES = BM * BK * 4;   // 16 KB per buffer
+  constexpr uint32_t B_BYTES = BN * BK * 4;   // BN * 128 bytes per buffer
+  constexpr uint32_t STAGE_BYTES = 2 * A_BYTES + 2 * B_BYTES;
+  constexpr uint32_t TMEM_COLS = BN < 32 ? 32 : BN;
+  constexpr uint32_t IDESC = tf32_idesc(BM, BN);
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint64_t* conv = full + STAGES;
+  uint64_t* empty = conv + STAGES;
+  uint64_t* accum = empty + STAGES;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accum + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int mt = blockIdx.x, nt = blockIdx.y, blk = blockIdx.z;
+  const int b = p.b;
+  const int num_kb = p.nseg * p.kb_per_seg;
+  const int row0 = blk * b;  // first row of this block in the [nblk*b, b] views
+
+  if (warp == 0 && lane == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&conv[s], 4);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(accum, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const uint32_t smem_base = smem_u32(smem);
+
+  if (warp == 0 && lane == 0) {
+    // ---------------------------------------------------------------- TMA producer
+    int issued = 0;
+    for (int kb = 0; kb < num_kb; ++kb) {
+      const int s = kb % STAGES;
+      const uint32_t ph = (kb / STAGES) & 1;
+      if (*abort_flag || !mbar_wait_bounded(&empty[s], ph ^ 1, p.err, p.limit_ns)) {
+        *abort_flag = 1;
+        break;
+      }
+      const int seg = kb / p.kb_per_seg;
+      const int k0 = (kb % p.kb_per_seg) * BK;
+      const TOp& A = p.A[seg];
+      const TOp& B = p.B[seg];
+      uint32_t bytes = 0;
+      for (int i = 0; i < 2; ++i) {
+        if (A.s[i].map >= 0) bytes += A_BYTES;
+        if (B.s[i].map >= 0) bytes += B_BYTES;
+      }
+      mbar_arrive_expect_tx(&full[s], bytes);
+      uint8_t* st = smem + s * STAGE_BYTES;
+      for (int i = 0; i < 2; ++i) {
+        if (A.s[i].map >= 0) {
+          const CUtensorMap* m = &maps.m[A.s[i].map];
+#pragma unroll
+          for (int r = 0; r < BM / 32; ++r)
+            tma_load_2d(st + i * A_BYTES + r * 4096, m, &full[s], k0, row0 + mt * BM + 32 * r);
+        }
+        if (B.s[i].map >= 0) {
+          const CUtensorMap* m = &maps.m[B.s[i].map];
+#pragma unroll
+          for (int c = 0; c < BN / 32; ++c)
+            tma_load_2d(st + 2 * A_BYTES + i * B_BYTES + c * 4096, m, &full[s],
+                        nt * BN + 32 * c, row0 + k0);
+        }
+      }
+      ++issued;
+    }
+    for (int kb = issued - 1; kb >= 0 && kb >= issued - STAGES; --kb)
+      mbar_wait_bounded(&full[kb % STAGES], (kb / STAGES) & 1, p.err, p.limit_ns);
+  } else if (warp == 1 && lane == 0) {
+    // ---------------------------------------------------------------- MMA issuer
+    for (int kb = 0; kb < num_kb; ++kb) {
+      const int s = kb % STAGES;
+      const uint32_t ph = (kb / STAGES) & 1;
+      if (*abort_flag || !mbar_wait_bounded(&conv[s], ph, p.err, p.limit_ns)) {
+        *abort_flag = 1;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t a_hi = smem_base + s * STAGE_BYTES;
+      const uint32_t a_lo = a_hi + A_BYTES;
+      const uint32_t b_hi = a_hi + 2 * A_BYTES;
+      const uint32_t b_lo = b_hi + B_BYTES;
+#pragma unroll
+      for (int k = 0; k < BK / 8; ++k) {
+        const uint64_t ah = sdesc(a_hi + k * 32, 16, 1024), al = sdesc(a_lo + k * 32, 16, 1024);
+        const uint64_t bh = sdesc(b_hi + k * 1024, 4096, 1024);
+        const uint64_t bl = sdesc(b_lo + k * 1024, 4096, 1024);
+        umma_tf32(tmem_base, ah, bh, IDESC, (kb | k) != 0);
+        umma_tf32(tmem_base, ah, bl, IDESC, 1);
+        umma_tf32(tmem_base, al, bh, IDESC, 1);
+      }
+      umma_commit(&empty[s]);
+    }
+    if (num_kb > 0) {
+      umma_commit(accum);
+      mbar_wait_bounded(accum, 0, p.err, p.limit_ns);
+    }
+  } else if (warp >= 2) {
+    // ---------------------------------------------------------------- converter
+    const int ct = threadIdx.x - 64;  // 0..127
+    for (int kb = 0; kb < num_kb; ++kb) {
+      const int s = kb % STAGES;
+      const uint32_t ph = (kb / STAGES) & 1;
+      const bool ok = !*abort_flag && mbar_wait_bounded(&full[s], ph, p.err, p.limit_ns);
+      if (!__all_sync(0xffffffffu, ok)) {
+        *abort_flag = 1;
+        break;
+      }
+      const int seg = kb / p.kb_per_seg;
+      const TOp& A = p.A[seg];
+      const TOp& B = p.B[seg];
+      uint8_t* st = smem + s * STAGE_BYTES;
+      float4* a0 = reinterpret_cast<float4*>(st);
+      float4* a1 = reinterpret_cast<float4*>(st + A_BYTES);
+      const bool a_two = A.s[1].map >= 0;
+#pragma unroll 4
+      for (int e = ct; e < (int)(A_BYTES / 16); e += 128)
+        combine_split(a0 + e, a1 + e, A.s[0].coef, A.s[1].coef, a_two);
+      float4* b0 = reinterpret_cast<float4*>(st + 2 * A_BYTES);
+      float4* b1 = reinterpret_cast<float4*>(st + 2 * A_BYTES + B_BYTES);
+      const bool b_two = B.s[1].map >= 0;
+#pragma unroll 4
+      for (int e = ct; e < (int)(B_BYTES / 16); e += 128)
+        combine_split(b0 + e, b1 + e, B.s[0].coef, B.s[1].coef, b_two);
+      fence_async_smem();  // generic-proxy writes -> visible to the tensor cores
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&conv[s]);
+    }
+    // ---------------------------------------------------------------- epilogue
+    const int q = warp & 3;
+    const int r = q * 32 + lane;
+    const int i = mt * BM + r;
+    bool have = num_kb > 0 && !*abort_flag;
+    if (have) {
+      const bool ok = mbar_wait_bounded(accum, 0, p.err, p.limit_ns);
+      have = __all_sync(0xffffffffu, ok);
+      tc_fence_after();
+    }
+    const long long base = (long long)blk * b * b;
+#pragma unroll 1
+    for (int c0 = 0; c0 < BN; c0 += 32) {
+      uint32_t v[32];
+      if (have) {
+        tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)c0, v);
+        tmem_ld_wait();
+      } else {
+#pragma unroll
+        for (int t = 0; t < 32; ++t) v[t] = 0u;
+      }
+      if (i >= b) continue;
+      const int j0 = nt * BN + c0;
+      const long long idx0 = base + (long long)i * b + j0;
+      float o[32];
+#pragma unroll
+      for (int t = 0; t < 32; ++t) o[t] = __uint_as_float(v[t]);
+      if (p.E1) {
+        const float4* e = reinterpret_cast<const float4*>(p.E1 + idx0);
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+          const float4 w = __ldg(e + t);
+          o[4 * t] = fmaf(p.e1, w.x, o[4 * t]);
+          o[4 * t + 1] = fmaf(p.e1, w.y, o[4 * t + 1]);
+          o[4 * t + 2] = fmaf(p.e1, w.z, o[4 * t + 2]);
+          o[4 * t + 3] = fmaf(p.e1, w.w, o[4 * t + 3]);
+        }
+      }
+      if (p.E2) {
+        const float4* e = reinterpret_cast<const float4*>(p.E2 + idx0);
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+          const float4 w = __ldg(e + t);
+          o[4 * t] = fmaf(p.e2, w.x, o[4 * t]);
+          o[4 * t + 1] = fmaf(p.e2, w.y, o[4 * t + 1]);
+          o[4 * t + 2] = fmaf(p.e2, w.z, o[4 * t + 2]);
+          o[4 * t + 3] = fmaf(p.e2, w.w, o[4 * t + 3]);
+        }
+      }
+#pragma unroll
+      for (int t = 0; t < 32; ++t)
+        if (j0 + t == i) o[t] += p.eI;
+      if (p.out_f32) {
+        float4* d = reinterpret_cast<float4*>(p.out_f32 + idx0);
+#pragma unroll
+        for (int t = 0; t < 8; ++t) d[t] = make_float4(o[4 * t], o[4 * t + 1], o[4 * t + 2], o[4 * t + 3]);
+      }
+      if (p.out_bf16) {
+        uint4* d = reinterpret_cast<uint4*>(p.out_bf16 + idx0);
+#pragma unroll
+        for (int t = 0; t < 4; ++t)
+          d[t] = make_uint4(pack_bf16x2(o[8 * t], o[8 * t + 1]), pack_bf16x2(o[8 * t + 2], o[8 * t + 3]),
+                            pack_bf16x2(o[8 * t + 4], o[8 * t + 5]), pack_bf16x2(o[8 * t + 6], o[8 * t + 7]));
+      }
+      if (p.out_bf16_t) {
+#pragma unroll
+        for (int t = 0; t < 32; ++t)
+          p.out_bf16_t[base + (long long)(j0 + t) * b + i] = __float2bfloat16_rn(o[t]);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+// [nblk*b rows][b cols] fp32 view with 32 x 32 boxes, 128-byte swizzle.
+bool make_blk_map(CUtensorMap* m, const float* ptr, int nblk, int b) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)b, (cuuint64_t)nblk * b};
+  cuuint64_t strides[1] = {(cuuint64_t)b * 4};
+  cuuint32_t box[2] = {32, 32};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(ptr), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int BN, int STAGES>
+poetx_status launch_t(const CnpMaps& maps, const CnpUParams& p, int nblk, cudaStream_t s) {
+  auto k = cnp_umma_kernel<BN, STAGES>;
+  constexpr int smem = STAGES * (2 * BM * BK * 4 + 2 * BN * BK * 4) + 1024 + 256;
+  static std::once_flag once;
+  static cudaError_t attr = cudaSuccess;
+  std::call_once(once, [&] {
+    attr = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  });
+  POETX_CUDA_TRY(attr);
+  dim3 grid((p.b + BM - 1) / BM, p.b / BN, nblk);
+  k<<<grid, 192, smem, s>>>(maps, p);
+  POETX_CUDA_TRY(cudaGetLastError());
+  return POETX_OK;
+}
+
+}  // namespace
+
+bool cnp_umma_ok(int b) {
+  return b >= 32 && b <= 1024 && b % 32 == 0 && umma_supported();
+}
+
+poetx_status cnp_umma_product(const CnpProduct& g, int nblk, cudaStream_t s) {
+  if (nblk == 0) return POETX_OK;
+  CnpMaps maps;
+  const float* ptrs[NMAPS] = {};
+  int nmaps = 0;
+  auto map_of = [&](const float* ptr) -> int {
+    if (!ptr) return -1;
+    for (int i = 0; i < nmaps; ++i)
+      if (ptrs[i] == ptr) return i;
+    if (nmaps == NMAPS) return -2;
+    if (!make_blk_map(&maps.m[nmaps], ptr, nblk, g.b)) return -3;
+    ptrs[nmaps] = ptr;
+    return nmaps++;
+  };
+  CnpUParams p{};
+  p.b = g.b;
+  p.nseg = g.nseg;
+  p.kb_per_seg = g.b / BK;
+  for (int sg = 0; sg < g.nseg; ++sg) {
+    const CnpTerm* ts[2] = {&g.A[sg], &g.B[sg]};
+    TOp* os[2] = {&p.A[sg], &p.B[sg]};
+    for (int w = 0; w < 2; ++w) {
+      for (int i = 0; i < 2; ++i) {
+        const float* ptr = i == 0 ? ts[w]->p1 : ts[w]->p2;
+        const int mi = map_of(ptr);
+        if (mi < -1) return mi == -2 ? POETX_ERR_UNSUPPORTED : POETX_ERR_CUDA;
+        os[w]->s[i].map = mi;
+        os[w]->s[i].coef = i == 0 ? ts[w]->c1 : ts[w]->c2;
+      }
+    }
+  }
+  p.E1 = g.E1; p.e1 = g.e1; p.E2 = g.E2; p.e2 = g.e2; p.eI = g.eI;
+  p.out_f32 = g.out_f32;
+  p.out_bf16 = g.out_bf16;
+  p.out_bf16_t = g.out_bf16_t;
+  p.err = device_error_word();
+  p.limit_ns = kWaitLimitNs;
+  if (g.b % 64 == 0) return launch_t<64, 2>(maps, p, nblk, s);
+  return launch_t<32, 2>(maps, p, nblk, s);
+}
+
+}  // namespace poetx

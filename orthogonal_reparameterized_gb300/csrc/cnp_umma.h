@@ -1,0 +1,35 @@
+// One batched CNP product: C_j = sum over segments of opA_seg(j) . opB_seg(j), plus
+// epilogue terms, for every block j of a [nblk, b, b] fp32 stack (see cnp.cu).
+#pragma once
+
+#include "common.cuh"
+
+namespace poetx {
+
+// c1 * p1 + c2 * p2 (p2 nullable), elementwise over [nblk, b, b] fp32 arrays.
+struct CnpTerm {
+  const float* p1;
+  float c1;
+  const float* p2;
+  float c2;
+};
+
+struct CnpProduct {
+  int b;
+  int nseg;               // 1 or 2
+  CnpTerm A[2], B[2];
+  const float* E1;        // epilogue: out = acc + e1 E1 + e2 E2 + eI I (E1, E2 nullable)
+  float e1;
+  const float* E2;
+  float e2;
+  float eI;
+  int mirror;             // result known symmetric (the CUDA-core kernel computes half)
+  float* out_f32;         // outputs, nullable
+  __nv_bfloat16* out_bf16;
+  __nv_bfloat16* out_bf16_t;
+};
+
+bool cnp_umma_ok(int b);
+poetx_status cnp_umma_product(const CnpProduct& g, int nblk, cudaStream_t s);
+
+}  // namespace poetx

@@ -17,11 +17,14 @@ __device__ __forceinline__ long long tri_index(int i, int j, int b) {
   return (long long)i * (b - 1) - (long long)i * (i - 1) / 2 + (j - i - 1);
 }
 
-__global__ void triu_unpack_kernel(const float* __restrict__ q, int b, float* __restrict__ Q) {
+// Blocks [0, n0) come from q0, blocks [n0, gridDim.z) from q1 (the R and P sides of a layer
+// are unpacked by one launch).
+__global__ void triu_unpack_kernel(const float* __restrict__ q0, int n0, const float* __restrict__ q1,
+                                   int b, float* __restrict__ Q) {
   const int blk = blockIdx.z;
   const int i = blockIdx.y;
   const long long tri = (long long)b * (b - 1) / 2;
-  const float* qb = q + blk * tri;
+  const float* qb = blk < n0 ? q0 + blk * tri : q1 + (blk - n0) * tri;
   float* row = Q + ((long long)blk * b + i) * b;
   for (int j = blockIdx.x * blockDim.x + threadIdx.x; j < b; j += gridDim.x * blockDim.x) {
     float v = 0.f;
@@ -31,38 +34,49 @@ __global__ void triu_unpack_kernel(const float* __restrict__ q, int b, float* __
   }
 }
 
-__global__ void triu_grad_pack_kernel(const float* __restrict__ Qbar, int b, float* __restrict__ dq,
-                                      int accumulate) {
+__global__ void triu_grad_pack_kernel(const float* __restrict__ Qbar, int b, float* __restrict__ dq0,
+                                      int n0, float* __restrict__ dq1, int accumulate) {
   const int blk = blockIdx.z;
   const int i = blockIdx.y;
   const long long tri = (long long)b * (b - 1) / 2;
   const float* Qb = Qbar + (long long)blk * b * b;
+  float* dqb = blk < n0 ? dq0 + blk * tri : dq1 + (blk - n0) * tri;
   for (int j = i + 1 + blockIdx.x * blockDim.x + threadIdx.x; j < b; j += gridDim.x * blockDim.x) {
     const float v = Qb[(long long)i * b + j] - Qb[(long long)j * b + i];
-    float* dst = dq + blk * tri + tri_index(i, j, b);
+    float* dst = dqb + tri_index(i, j, b);
     *dst = accumulate ? *dst + v : v;
   }
 }
 
-poetx_status launch_triu_unpack(const float* q, int nblk, int b, float* Q, cudaStream_t s) {
-  if (nblk == 0) return POETX_OK;
+poetx_status launch_triu_unpack2(const float* q0, int n0, const float* q1, int n1, int b, float* Q,
+                                 cudaStream_t s) {
+  if (n0 + n1 == 0) return POETX_OK;
   const int threads = b < 256 ? ((b + 31) / 32) * 32 : 256;
-  dim3 grid(1, b, nblk);
-  triu_unpack_kernel<<<grid, threads, 0, s>>>(q, b, Q);
+  dim3 grid(1, b, n0 + n1);
+  triu_unpack_kernel<<<grid, threads, 0, s>>>(q0, n0, q1, b, Q);
   POETX_CUDA_TRY(cudaGetLastError());
   after_launch(s, ST_TRIU_UNPACK);
   return POETX_OK;
 }
 
-poetx_status launch_triu_grad_pack(const float* Qbar, int nblk, int b, float* dq, int accumulate,
-                                   cudaStream_t s) {
-  if (nblk == 0 || b < 2) return POETX_OK;
+poetx_status launch_triu_unpack(const float* q, int nblk, int b, float* Q, cudaStream_t s) {
+  return launch_triu_unpack2(q, nblk, nullptr, 0, b, Q, s);
+}
+
+poetx_status launch_triu_grad_pack2(const float* Qbar, int n0, int n1, int b, float* dq0, float* dq1,
+                                    int accumulate, cudaStream_t s) {
+  if (n0 + n1 == 0 || b < 2) return POETX_OK;
   const int threads = b < 256 ? ((b + 31) / 32) * 32 : 256;
-  dim3 grid(1, b - 1, nblk);
-  triu_grad_pack_kernel<<<grid, threads, 0, s>>>(Qbar, b, dq, accumulate);
+  dim3 grid(1, b - 1, n0 + n1);
+  triu_grad_pack_kernel<<<grid, threads, 0, s>>>(Qbar, b, dq0, n0, dq1, accumulate);
   POETX_CUDA_TRY(cudaGetLastError());
   after_launch(s, ST_TRIU_PACK);
   return POETX_OK;
+}
+
+poetx_status launch_triu_grad_pack(const float* Qbar, int nblk, int b, float* dq, int accumulate,
+                                   cudaStream_t s) {
+  return launch_triu_grad_pack2(Qbar, nblk, 0, b, dq, nullptr, accumulate, s);
 }
 
 // ---------------------------------------------------------------- row permutations

@@ -11,6 +11,11 @@ namespace poetx {
 
 // ---- index.cu
 poetx_status launch_triu_unpack(const float* q, int nblk, int b, float* Q, cudaStream_t s);
+// Two-sided: blocks [0, n0) from q0, [n0, n0 + n1) from q1.
+poetx_status launch_triu_unpack2(const float* q0, int n0, const float* q1, int n1, int b, float* Q,
+                                 cudaStream_t s);
+poetx_status launch_triu_grad_pack2(const float* Qbar, int n0, int n1, int b, float* dq0, float* dq1,
+                                    int accumulate, cudaStream_t s);
 poetx_status launch_triu_grad_pack(const float* Qbar, int nblk, int b, float* dq, int accumulate,
                                    cudaStream_t s);
 poetx_status launch_perm_rows(size_t esize, bool scatter, const void* X, long long N, int D,
@@ -43,16 +48,29 @@ poetx_status launch_simt_gemm(poetx_dtype ta, poetx_dtype tb, poetx_dtype tc, co
                               cudaStream_t s);
 
 // ---- cnp.cu
+// The blocks of one CNP call may come from two sides (the R and P factors of a layer):
+// blocks [0, n[0]) belong to side 0, [n[0], n[0] + n[1]) to side 1.  Every block array
+// (Q, Q^2, G, X, ...) is one contiguous [n[0] + n[1], b, b] stack.
+struct CnpSides {
+  const float* q[2];   // packed triangles of each side
+  int n[2];            // blocks of each side (n[1] may be 0)
+};
 size_t cnp_fwd_scratch_bytes(int nblk, int b);
 size_t cnp_bwd_scratch_bytes(int nblk, int b);
-// Forward CNP with caller-provided fp32 scratch Qs [nblk,b,b] and Q2 [nblk,b,b] (Q2 is an
-// output too: Q^2 of every block).
+// Forward CNP with caller-provided fp32 scratch Qs and the Q^2 output (both [nblk, b, b]).
 poetx_status cnp_forward(const float* q, int nblk, int b, float* Qs, float* Q2, float* G_f32,
                          void* G_bf16, void* Gt_bf16, cudaStream_t s);
-// Backward CNP.  Q2 may be a precomputed Q^2 (from cnp_forward) or NULL to recompute it
-// into the scratch.  scratch holds cnp_bwd_scratch_bytes(nblk, b) bytes.
-poetx_status cnp_backward(const float* q, const float* Q2, const float* dG, int splits, int nblk,
-                          int b, float* dq, int accumulate, void* scratch, cudaStream_t s);
+poetx_status cnp_forward_sides(const CnpSides& q, int b, float* Qs, float* Q2, float* G_f32,
+                               void* G_bf16, void* Gt_bf16, cudaStream_t s);
+// Backward CNP.  Q2 may be a precomputed Q^2 stack or NULL to recompute it into the scratch;
+// dG[side] is [splits[side], n[side], b, b]; dq[side] receives that side's gradient.
+// scratch holds cnp_bwd_scratch_bytes(n[0] + n[1], b) bytes.
+poetx_status cnp_backward_sides(const CnpSides& q, const float* Q2, const float* const dG[2],
+                                const int splits[2], int b, float* const dq[2], int accumulate,
+                                void* scratch, cudaStream_t s);
+
+// ---- layer.cu: engine switch (tensor cores unless disabled by poetx_set_gemm_engine)
+bool use_tensor_cores();
 
 // ---- umma_gemm.cu: tcgen05 / TMA tensor-core GEMMs (bf16 in, fp32 accumulate)
 bool umma_supported();

@@ -26,6 +26,8 @@ static std::atomic<int> g_engine{0};  // 0: tensor cores where supported, 1: CUD
 
 static bool use_umma() { return g_engine.load() == 0 && umma_supported(); }
 
+bool use_tensor_cores() { return g_engine.load() == 0; }
+
 static int wgrad_splits(long long N, int nblk, int b) {
   const long long tiles = (long long)nblk * ((b + 127) / 128) * (b > 256 ? b / 256 : 1);
   long long s = (2LL * sm_count() + tiles - 1) / tiles;
@@ -148,15 +150,16 @@ static Plan make_plan(const poetx_layer* L, long long N) {
   const size_t m = L->m, n = L->n, b = L->b;
   size_t o = 0;
   auto take = [&](size_t bytes) { size_t r = o; o += align_up(bytes, 256); return r; };
-  p.GR = take(m * b * gs);
-  p.GP = take(n * b * gs);
-  p.Q2R = take(m * b * 4);
-  p.Q2P = take(n * b * 4);
+  // G_R and G_P (and Q_R^2, Q_P^2) are adjacent stacks so that one CNP launch covers both
+  p.GR = take((m + n) * b * gs);
+  p.GP = p.GR + m * b * gs;
+  p.Q2R = take((m + n) * b * 4);
+  p.Q2P = p.Q2R + m * b * 4;
   p.Bsv = L->variant == POETX_FAST ? take((size_t)N * n * as) : 0;
   p.saved_total = o;
 
   o = 0;
-  p.f_Qs = take((m > n ? m : n) * b * 4);
+  p.f_Qs = take((m + n) * b * 4);
   p.f_xt = take((size_t)N * m * as);
   p.f_A = take((size_t)N * m * as);
   p.f_B = L->variant == POETX_MEM ? take((size_t)N * n * as) : 0;
@@ -166,7 +169,7 @@ static Plan make_plan(const poetx_layer* L, long long N) {
   p.splitsR = wgrad_splits(N, L->m / L->b, L->b);
   p.splitsP = wgrad_splits(N, L->n / L->b, L->b);
   o = 0;
-  p.b_cnp = take(cnp_bwd_scratch_bytes((int)((m > n ? m : n) / b), (int)b));
+  p.b_cnp = take(cnp_bwd_scratch_bytes((int)((m + n) / b), (int)b));
   p.b_xt = take((size_t)N * m * as);
   p.b_dzt = take((size_t)N * n * as);
   p.b_A = L->variant == POETX_MEM ? take((size_t)N * m * as) : 0;
@@ -225,13 +228,12 @@ extern "C" poetx_status poetx_layer_fwd(const poetx_layer* L, const void* x, int
   const bool f32 = act == POETX_F32;
   const size_t as = dtype_size(act);
   prof_begin(stream);
-  // S1-S2: both CNPs; G in the activation precision and Q^2 kept for the backward
-  POETX_TRY(cnp_forward(L->q_R, m / b, b, at<float>(ws, p.f_Qs), at<float>(saved, p.Q2R),
-                        f32 ? at<float>(saved, p.GR) : nullptr, f32 ? nullptr : at(saved, p.GR),
-                        nullptr, stream));
-  POETX_TRY(cnp_forward(L->q_P, n / b, b, at<float>(ws, p.f_Qs), at<float>(saved, p.Q2P),
-                        f32 ? at<float>(saved, p.GP) : nullptr, f32 ? nullptr : at(saved, p.GP),
-                        nullptr, stream));
+  // S1-S2: both CNPs in one pass over the m/b + n/b blocks; G in the activation precision
+  // and Q^2 kept for the backward
+  const CnpSides sides{{L->q_R, L->q_P}, {m / b, n / b}};
+  POETX_TRY(cnp_forward_sides(sides, b, at<float>(ws, p.f_Qs), at<float>(saved, p.Q2R),
+                              f32 ? at<float>(saved, p.GR) : nullptr,
+                              f32 ? nullptr : at(saved, p.GR), nullptr, stream));
   if (N == 0) return POETX_OK;
   void* xt = at(ws, p.f_xt);
   void* A = at(ws, p.f_A);
@@ -292,11 +294,12 @@ extern "C" poetx_status poetx_layer_bwd(const poetx_layer* L, const void* x, con
   POETX_TRY(blockdiag_impl(act, dA, N, m / b, b, GR, 1, nullptr, dxt, stream));
   if (N > 0)
     POETX_TRY(launch_perm_rows(as, true, dxt, N, m, L->perm_m, dx, nullptr, nullptr, nullptr, stream));
-  void* cnp_ws = at(ws, p.b_cnp);
-  POETX_TRY(cnp_backward(L->q_P, at<float>(saved, p.Q2P), dGP, p.splitsP, n / b, b, dq_P,
-                         accumulate, cnp_ws, stream));
-  return cnp_backward(L->q_R, at<float>(saved, p.Q2R), dGR, p.splitsR, m / b, b, dq_R, accumulate,
-                      cnp_ws, stream);
+  const CnpSides sides{{L->q_R, L->q_P}, {m / b, n / b}};
+  const float* const dGs[2] = {dGR, dGP};
+  const int splits[2] = {p.splitsR, p.splitsP};
+  float* const dqs[2] = {dq_R, dq_P};
+  return cnp_backward_sides(sides, at<float>(saved, p.Q2R), dGs, splits, b, dqs, accumulate,
+                            at(ws, p.b_cnp), stream);
 }
 
 // ---------------------------------------------------------------- step entry points

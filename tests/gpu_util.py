@@ -34,3 +34,11 @@ def P():
     P.lib()
     torch.cuda.set_device(0)
     return P
+
+
+@pytest.fixture(params=[0, 1], ids=["tcgen05", "cudacore"])
+def engine(request, P):
+    """Runs a test once with the tensor-core kernels and once with the CUDA-core ones."""
+    P.poetx_set_gemm_engine(request.param)
+    yield request.param
+    P.poetx_set_gemm_engine(0)

@@ -6,7 +6,7 @@ import torch
 
 import oracle as O
 from conftest import read_golden, read_golden_kv  # noqa: F401
-from gpu_util import DEV, P, TOL_F32, dev, host  # noqa: F401
+from gpu_util import DEV, P, TOL_F32, dev, engine, host  # noqa: F401
 from orthogonal_reparameterized_gb300 import inputs
 
 pytestmark = pytest.mark.gpu
@@ -24,7 +24,7 @@ def _fwd(P, q, b):
 @pytest.mark.parametrize("nblk,b,std", [(5, 2, 0.3), (3, 3, 0.3), (4, 5, 0.2), (8, 32, 0.01),
                                         (6, 64, 0.02), (3, 100, 0.02), (4, 128, 0.02),
                                         (3, 256, 0.02), (2, 512, 0.02), (2, 256, 0.2)])
-def test_cnp_fwd_parity(P, nblk, b, std):
+def test_cnp_fwd_parity(P, engine, nblk, b, std):
     q = inputs.cnp_inputs(11, nblk, b, std)
     G, Gb, Gt = _fwd(P, q, b)
     ref = O.cnp_forward(q, b)
@@ -42,7 +42,7 @@ def test_cnp_fwd_golden_b2(P):
         np.testing.assert_allclose(host(G)[j], [[r[1], r[2]], [r[3], r[4]]], rtol=2e-7, atol=1e-6)
 
 
-def test_cnp_fwd_zero_is_identity(P):
+def test_cnp_fwd_zero_is_identity(P, engine):
     for b in (2, 64, 256):
         G, _, _ = _fwd(P, np.zeros((3, b * (b - 1) // 2)), b)
         np.testing.assert_array_equal(host(G), np.broadcast_to(np.eye(b), (3, b, b)))
@@ -52,7 +52,7 @@ def test_cnp_fwd_zero_is_identity(P):
                                                (6, 64, 4, 0.02), (3, 100, 2, 0.02),
                                                (4, 128, 1, 0.02), (3, 256, 5, 0.02),
                                                (2, 512, 2, 0.02)])
-def test_cnp_bwd_parity(P, nblk, b, splits, std):
+def test_cnp_bwd_parity(P, engine, nblk, b, splits, std):
     q = inputs.cnp_inputs(12, nblk, b, std)
     dG = inputs.dG_inputs(13, splits, nblk, b)
     dq = torch.empty(nblk, b * (b - 1) // 2, device=DEV)
@@ -82,7 +82,7 @@ def test_cnp_bwd_zero_q(P):
 
 
 @pytest.mark.parametrize("b", [64, 128, 256, 512])
-def test_cnp_sweep_full_size(P, b):
+def test_cnp_sweep_full_size(P, engine, b):
     """The 4096 x 4096 layer of the block-size sweep: 4096/b blocks on each side."""
     nblk = 2 * 4096 // b
     q = inputs.cnp_inputs(20260308, nblk, b, 0.02)
@@ -94,7 +94,7 @@ def test_cnp_sweep_full_size(P, b):
     assert O.rel_fro(host(dq), O.cnp_backward(q, dG, b), per_block=True) <= TOL_F32
 
 
-def test_cnp_deterministic(P):
+def test_cnp_deterministic(P, engine):
     b, nblk = 256, 4
     q = dev(inputs.cnp_inputs(15, nblk, b, 0.02), torch.float32)
     dG = dev(inputs.dG_inputs(15, 3, nblk, b), torch.float32)

@@ -6,17 +6,10 @@ import pytest
 import torch
 
 import oracle as O
-from gpu_util import DEV, P, TOL_BF16_STEP, TOL_F32, dev, host  # noqa: F401
+from gpu_util import DEV, P, TOL_BF16_STEP, TOL_F32, dev, engine, host  # noqa: F401
 
 pytestmark = pytest.mark.gpu
 RNG = np.random.default_rng(99)
-
-
-@pytest.fixture(params=[0, 1], ids=["tcgen05", "cudacore"])
-def engine(request, P):
-    P.poetx_set_gemm_engine(request.param)
-    yield request.param
-    P.poetx_set_gemm_engine(0)
 
 
 def _bf(a):
