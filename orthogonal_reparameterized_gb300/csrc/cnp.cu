@@ -7,7 +7,10 @@
 //
 // Every product here is a batched b x b fp32 GEMM (one batch entry per block) whose
 // operands are linear combinations of at most two b x b arrays, staged tile by tile in
-// shared memory, and whose epilogue adds linear combinations of b x b arrays and of I:
+// shared memory, and whose epilogue adds linear combinations of b x b arrays and of I.  The
+// second operand is always given transposed (Q^T = -Q, (Q^2)^T = Q^2, and transposed copies
+// X^T, M1^T are written by the kernels that produce X and M1).  On GB300 the products run on
+// the tensor cores (cnp_umma.cu, 3-term tf32 split), else on the CUDA cores below:
 //
 //   forward   Q2 = Q Q                                     (symmetric: upper tiles only)
 //             G  = Q2 (2Q + Q2) + I + 2Q + 2Q2             = I + 2(Q+Q^2+Q^3) + Q^4
@@ -67,11 +70,11 @@ __global__ void __launch_bounds__((T / 4) * (T / 4)) cnp_gemm_kernel(CnpGemm g) 
         As[kk][ii] = (gi < b && gk < b) ? op_load(oa, base + (long long)gi * b + gk) : 0.f;
       }
 #pragma unroll
-      for (int r = 0; r < (T * TK) / NT; ++r) {
+      for (int r = 0; r < (T * TK) / NT; ++r) {  // B from its transpose: B[k][j] = Bt[j][k]
         const int e = tid + r * NT;
-        const int kk = e / T, jj = e % T;
+        const int jj = e / TK, kk = e % TK;
         const int gj = j0 + jj, gk = k0 + kk;
-        Bs[kk][jj] = (gj < b && gk < b) ? op_load(ob, base + (long long)gk * b + gj) : 0.f;
+        Bs[kk][jj] = (gj < b && gk < b) ? op_load(ob, base + (long long)gj * b + gk) : 0.f;
       }
       __syncthreads();
 #pragma unroll
@@ -106,6 +109,7 @@ __global__ void __launch_bounds__((T / 4) * (T / 4)) cnp_gemm_kernel(CnpGemm g) 
         g.out_f32[idx] = r;
         if (g.mirror && ti != tj) g.out_f32[tidx] = r;
       }
+      if (g.out_f32_t) g.out_f32_t[tidx] = r;
       if (g.out_bf16) g.out_bf16[idx] = __float2bfloat16_rn(r);
       if (g.out_bf16_t) g.out_bf16_t[tidx] = __float2bfloat16_rn(r);
     }
@@ -134,24 +138,34 @@ poetx_status launch_cnp_gemm(const CnpGemm& g, int nblk, int stage, cudaStream_t
 Operand op1(const float* p, float c) { return Operand{p, c, nullptr, 0.f}; }
 Operand op2(const float* p, float c, const float* q, float d) { return Operand{p, c, q, d}; }
 
-// X[j] = sum_s dG_side[s][j'] in the order s = 0, 1, ..., S_side - 1, for the blocks of
-// both sides (j' = j for side 0, j - n0 for side 1).
-__global__ void sum_partials_kernel(const float* __restrict__ dG0, int S0, long long n0e,
-                                    const float* __restrict__ dG1, int S1, long long n1e,
-                                    float* __restrict__ X) {
-  const long long n = n0e + n1e;
-  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
-       i += (long long)gridDim.x * blockDim.x) {
-    float a;
-    if (i < n0e) {
-      a = dG0[i];
-      for (int s = 1; s < S0; ++s) a += dG0[(long long)s * n0e + i];
-    } else {
-      const long long k = i - n0e;
-      a = dG1[k];
-      for (int s = 1; s < S1; ++s) a += dG1[(long long)s * n1e + k];
+// X[j] = sum_s dG_side[s][j'] in the order s = 0, 1, ..., S_side - 1 (j' = j for side 0,
+// j - n0 for side 1), and Xt[j] = X[j]^T, one 32 x 32 tile per CTA (transpose through
+// shared memory so that both stores are coalesced).
+__global__ void sum_partials_kernel(const float* __restrict__ dG0, int S0, int n0,
+                                    const float* __restrict__ dG1, int S1, int n1, int b,
+                                    float* __restrict__ X, float* __restrict__ Xt) {
+  __shared__ float tile[32][33];
+  const int j = blockIdx.z;
+  const float* src = j < n0 ? dG0 + (long long)j * b * b : dG1 + (long long)(j - n0) * b * b;
+  const int S = j < n0 ? S0 : S1;
+  const long long sstride = (long long)(j < n0 ? n0 : n1) * b * b;
+  const int r0 = blockIdx.y * 32, c0 = blockIdx.x * 32;
+  const long long base = (long long)j * b * b;
+  for (int rr = threadIdx.y; rr < 32; rr += 8) {
+    const int r = r0 + rr, c = c0 + threadIdx.x;
+    float a = 0.f;
+    if (r < b && c < b) {
+      const long long off = (long long)r * b + c;
+      a = src[off];
+      for (int s2 = 1; s2 < S; ++s2) a += src[s2 * sstride + off];
+      X[base + off] = a;
     }
-    X[i] = a;
+    tile[rr][threadIdx.x] = a;
+  }
+  __syncthreads();
+  for (int cc = threadIdx.y; cc < 32; cc += 8) {
+    const int c = c0 + cc, r = r0 + threadIdx.x;
+    if (r < b && c < b) Xt[base + (long long)c * b + r] = tile[threadIdx.x][cc];
   }
 }
 
@@ -160,28 +174,28 @@ size_t blk_bytes(int nblk, int b) { return align_up((size_t)nblk * b * b * sizeo
 }  // namespace
 
 size_t cnp_fwd_scratch_bytes(int nblk, int b) { return 2 * blk_bytes(nblk, b); }
-size_t cnp_bwd_scratch_bytes(int nblk, int b) { return 5 * blk_bytes(nblk, b); }
+size_t cnp_bwd_scratch_bytes(int nblk, int b) { return 7 * blk_bytes(nblk, b); }
 
 poetx_status cnp_forward_sides(const CnpSides& q, int b, float* Qs, float* Q2, float* G_f32,
                                void* G_bf16, void* Gt_bf16, cudaStream_t s) {
   const int nblk = q.n[0] + q.n[1];
   if (nblk == 0) return POETX_OK;
   POETX_TRY(launch_triu_unpack2(q.q[0], q.n[0], q.q[1], q.n[1], b, Qs, s));
-  // Q2 = Q Q (symmetric)
+  // Q2 = Q Q (symmetric); B^T = Q^T = -Q
   CnpGemm g{};
   g.b = b;
   g.nseg = 1;
   g.A[0] = op1(Qs, 1.f);
-  g.B[0] = op1(Qs, 1.f);
+  g.B[0] = op1(Qs, -1.f);
   g.mirror = 1;
   g.out_f32 = Q2;
   POETX_TRY(launch_cnp_gemm(g, nblk, ST_CNP_Q2, s));
-  // G = Q2 (2Q + Q2) + I + 2Q + 2Q2
+  // G = Q2 (2Q + Q2) + I + 2Q + 2Q2; B^T = (2Q + Q2)^T = -2Q + Q2
   CnpGemm h{};
   h.b = b;
   h.nseg = 1;
   h.A[0] = op1(Q2, 1.f);
-  h.B[0] = op2(Qs, 2.f, Q2, 1.f);
+  h.B[0] = op2(Qs, -2.f, Q2, 1.f);
   h.E1 = Qs;
   h.e1 = 2.f;
   h.E2 = Q2;
@@ -209,47 +223,49 @@ poetx_status cnp_backward_sides(const CnpSides& q, const float* Q2in, const floa
   float* Qs = reinterpret_cast<float*>(w);
   float* Q2 = reinterpret_cast<float*>(w + bb);
   float* X = reinterpret_cast<float*>(w + 2 * bb);
-  float* M1 = reinterpret_cast<float*>(w + 3 * bb);
-  float* Qbar = reinterpret_cast<float*>(w + 4 * bb);
+  float* Xt = reinterpret_cast<float*>(w + 3 * bb);
+  float* M1 = reinterpret_cast<float*>(w + 4 * bb);
+  float* M1t = reinterpret_cast<float*>(w + 5 * bb);
+  float* Qbar = reinterpret_cast<float*>(w + 6 * bb);
   POETX_TRY(launch_triu_unpack2(q.q[0], q.n[0], q.q[1], q.n[1], b, Qs, s));
   if (!Q2in) {
     CnpGemm g{};
     g.b = b;
     g.nseg = 1;
     g.A[0] = op1(Qs, 1.f);
-    g.B[0] = op1(Qs, 1.f);
+    g.B[0] = op1(Qs, -1.f);
     g.mirror = 1;
     g.out_f32 = Q2;
     POETX_TRY(launch_cnp_gemm(g, nblk, ST_CNP_Q2, s));
     Q2in = Q2;
   }
-  // X = sum of the partials, both sides, fixed order
+  // X = sum of the partials (both sides, fixed order) and its transpose Xt
   {
-    const long long n0e = (long long)q.n[0] * b * b, n1e = (long long)q.n[1] * b * b;
-    const long long n = n0e + n1e;
-    const int grid = (int)((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096);
-    sum_partials_kernel<<<grid, 256, 0, s>>>(dG[0], splits[0], n0e, dG[1], splits[1], n1e, X);
+    dim3 grid(ceil_div(b, 32), ceil_div(b, 32), nblk);
+    sum_partials_kernel<<<grid, dim3(32, 8), 0, s>>>(dG[0], splits[0], q.n[0], dG[1], splits[1],
+                                                     q.n[1], b, X, Xt);
     POETX_CUDA_TRY(cudaGetLastError());
     after_launch(s, ST_CNP_SUM);
   }
-  // M1 = X P + P X, P = -Q
+  // M1 = X P + P X with P = -Q (B^T terms: P^T = Q, X^T = Xt); M1^T kept for the next product
   CnpGemm m{};
   m.b = b;
   m.nseg = 2;
   m.A[0] = op1(X, 1.f);
-  m.B[0] = op1(Qs, -1.f);
+  m.B[0] = op1(Qs, 1.f);
   m.A[1] = op1(Qs, -1.f);
-  m.B[1] = op1(X, 1.f);
+  m.B[1] = op1(Xt, 1.f);
   m.out_f32 = M1;
+  m.out_f32_t = M1t;
   POETX_TRY(launch_cnp_gemm(m, nblk, ST_CNP_M1, s));
-  // Qbar = (2X + M1) Q2 + (Q2 - 2Q) M1 + 2X + 2M1
+  // Qbar = (2X + M1) Q2 + (Q2 - 2Q) M1 + 2X + 2M1 (B^T terms: Q2^T = Q2, M1^T = M1t)
   CnpGemm r{};
   r.b = b;
   r.nseg = 2;
   r.A[0] = op2(X, 2.f, M1, 1.f);
   r.B[0] = op1(Q2in, 1.f);
   r.A[1] = op2(Q2in, 1.f, Qs, -2.f);
-  r.B[1] = op1(M1, 1.f);
+  r.B[1] = op1(M1t, 1.f);
   r.E1 = X;
   r.e1 = 2.f;
   r.E2 = M1;

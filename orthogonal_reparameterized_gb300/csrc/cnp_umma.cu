@@ -12,7 +12,8 @@
 //              hi(v) and lo(v) (same swizzled offsets, so the layout is kept)
 //   warp 1     three tcgen05.mma kind::tf32 per K=8 step into one fp32 TMEM accumulator
 //   warps 2-5  epilogue: TMEM -> registers, add the epilogue terms, store fp32 / bf16 / bf16^T
-// A tiles are K-major (row-major arrays), B tiles MN-major; 128-byte swizzle throughout.
+// Both operand tiles are K-major (kind::tf32 takes no MN-major operand): A tiles are rows of
+// A, B tiles rows of B^T (the B terms of a product are given transposed); 128-byte swizzle.
 // Every wait is bounded (POETX_ERR_TIMEOUT on expiry, then drain, free TMEM, return).
 #include <mutex>
 
@@ -51,6 +52,7 @@ struct CnpUParams {
   float e2;
   float eI;
   float* out_f32;
+  float* out_f32_t;
   __nv_bfloat16* out_bf16;
   __nv_bfloat16* out_bf16_t;
   int* err;
@@ -62,7 +64,7 @@ __host__ __device__ constexpr uint32_t tf32_idesc(int M, int N) {
          | (2u << 7)                    // A: tf32
          | (2u << 10)                   // B: tf32
          | (0u << 15)                   // A K-major
-         | (1u << 16)                   // B MN-major
+         | (0u << 16)                   // B K-major (kind::tf32 takes K-major operands only)
          | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
@@ -184,12 +186,12 @@ __global__ void __launch_bounds__(192, 1)
           for (int r = 0; r < BM / 32; ++r)
             tma_load_2d(st + i * A_BYTES + r * 4096, m, &full[s], k0, row0 + mt * BM + 32 * r);
         }
-        if (B.s[i].map >= 0) {
+        if (B.s[i].map >= 0) {  // rows nt*BN.. of B^T, columns k0..k0+31
           const CUtensorMap* m = &maps.m[B.s[i].map];
 #pragma unroll
           for (int c = 0; c < BN / 32; ++c)
-            tma_load_2d(st + 2 * A_BYTES + i * B_BYTES + c * 4096, m, &full[s],
-                        nt * BN + 32 * c, row0 + k0);
+            tma_load_2d(st + 2 * A_BYTES + i * B_BYTES + c * 4096, m, &full[s], k0,
+                        row0 + nt * BN + 32 * c);
         }
       }
       ++issued;
@@ -213,8 +215,7 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
       for (int k = 0; k < BK / 8; ++k) {
         const uint64_t ah = sdesc(a_hi + k * 32, 16, 1024), al = sdesc(a_lo + k * 32, 16, 1024);
-        const uint64_t bh = sdesc(b_hi + k * 1024, 4096, 1024);
-        const uint64_t bl = sdesc(b_lo + k * 1024, 4096, 1024);
+        const uint64_t bh = sdesc(b_hi + k * 32, 16, 1024), bl = sdesc(b_lo + k * 32, 16, 1024);
         umma_tf32(tmem_base, ah, bh, IDESC, (kb | k) != 0);
         umma_tf32(tmem_base, ah, bl, IDESC, 1);
         umma_tf32(tmem_base, al, bh, IDESC, 1);
@@ -312,6 +313,10 @@ __global__ void __launch_bounds__(192, 1)
         float4* d = reinterpret_cast<float4*>(p.out_f32 + idx0);
 #pragma unroll
         for (int t = 0; t < 8; ++t) d[t] = make_float4(o[4 * t], o[4 * t + 1], o[4 * t + 2], o[4 * t + 3]);
+      }
+      if (p.out_f32_t) {  // lanes hold consecutive rows i: each store is coalesced
+#pragma unroll
+        for (int t = 0; t < 32; ++t) p.out_f32_t[base + (long long)(j0 + t) * b + i] = o[t];
       }
       if (p.out_bf16) {
         uint4* d = reinterpret_cast<uint4*>(p.out_bf16 + idx0);
@@ -423,6 +428,7 @@ poetx_status cnp_umma_product(const CnpProduct& g, int nblk, cudaStream_t s) {
   }
   p.E1 = g.E1; p.e1 = g.e1; p.E2 = g.E2; p.e2 = g.e2; p.eI = g.eI;
   p.out_f32 = g.out_f32;
+  p.out_f32_t = g.out_f32_t;
   p.out_bf16 = g.out_bf16;
   p.out_bf16_t = g.out_bf16_t;
   p.err = device_error_word();

@@ -1,5 +1,9 @@
 // One batched CNP product: C_j = sum over segments of opA_seg(j) . opB_seg(j), plus
 // epilogue terms, for every block j of a [nblk, b, b] fp32 stack (see cnp.cu).
+// A terms give A row-major; B terms give B TRANSPOSED (row n of the term = column n of B),
+// so that both operands reach the tensor cores K-major (kind::tf32 takes no MN-major
+// operand): a symmetric or skew source is its own transpose up to sign, a general one needs
+// a transposed copy (written by the kernel that produced it).
 #pragma once
 
 #include "common.cuh"
@@ -25,6 +29,7 @@ struct CnpProduct {
   float eI;
   int mirror;             // result known symmetric (the CUDA-core kernel computes half)
   float* out_f32;         // outputs, nullable
+  float* out_f32_t;       // fp32 output transposed
   __nv_bfloat16* out_bf16;
   __nv_bfloat16* out_bf16_t;
 };
