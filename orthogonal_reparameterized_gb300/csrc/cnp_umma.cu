@@ -27,7 +27,7 @@ namespace {
 
 constexpr int BM = 128;
 constexpr int BK = 32;      // fp32 elements per 128-byte row
-constexpr int NMAPS = 4;
+constexpr int NMAPS = 6;  // distinct source arrays of one product (Q-bar uses 5)
 
 struct CnpMaps {
   CUtensorMap m[NMAPS];
