@@ -1,7 +1,10 @@
 // Tensor-core products of the Cayley-Neumann parameterization: fp32 accuracy from tcgen05
 // kind::tf32 by the 3-term split a*b ~ hi(a)hi(b) + hi(a)lo(b) + lo(a)hi(b), where
-// hi(v) = v with its 13 low mantissa bits cleared (exactly representable in tf32) and
-// lo(v) = v - hi(v) (exact in fp32); the dropped lo*lo term is below 2^-20 |a||b|.
+// hi(v) = v rounded to the nearest tf32 value (13 low mantissa bits cleared) and
+// lo(v) = v - hi(v) (exact in fp32); the dropped lo*lo term is below 2^-22 |a||b|.  The
+// tensor-core fp32 accumulation is kept short: every 32-wide K block goes into a fresh TMEM
+// accumulator (two, used alternately) that the converter warps add into fp32 registers with
+// IEEE adds ("promotion"), so the accumulated rounding does not grow with b.
 //
 // Each CNP product (POET-X summary page, "Core method" section 4, eq. 9 and its gradient)
 // is C_j = sum_seg opA_seg(j) . opB_seg(j) + epilogue, for every block j, where each operand
@@ -10,8 +13,9 @@
 //   warp 0     TMA: the raw fp32 tiles of every source array of the current K block
 //   warps 2-5  form v = c0*src0 + c1*src1 in shared memory and split it in place into
 //              hi(v) and lo(v) (same swizzled offsets, so the layout is kept)
-//   warp 1     three tcgen05.mma kind::tf32 per K=8 step into one fp32 TMEM accumulator
-//   warps 2-5  epilogue: TMEM -> registers, add the epilogue terms, store fp32 / bf16 / bf16^T
+//   warp 1     three tcgen05.mma kind::tf32 per K=8 step into the K block's TMEM accumulator
+//   warps 2-5  promote each K block's accumulator into registers; at the end add the
+//              epilogue terms and store fp32 / fp32^T / bf16 / bf16^T
 // Both operand tiles are K-major (kind::tf32 takes no MN-major operand): A tiles are rows of
 // A, B tiles rows of B^T (the B terms of a product are given transposed); 128-byte swizzle.
 // Every wait is bounded (POETX_ERR_TIMEOUT on expiry, then drain, free TMEM, return).
@@ -106,7 +110,7 @@ __device__ __forceinline__ void combine_split(float4* x, float4* y, float c0, fl
   float hi[4], lo[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    hi[i] = __uint_as_float(__float_as_uint(v[i]) & 0xFFFFE000u);
+    hi[i] = __uint_as_float((__float_as_uint(v[i]) + 0x1000u) & 0xFFFFE000u);
     lo[i] = v[i] - hi[i];
   }
   *x = make_float4(hi[0], hi[1], hi[2], hi[3]);
@@ -119,7 +123,7 @@ __global__ void __launch_bounds__(192, 1)
   constexpr uint32_t A_BYTES = BM * BK * 4;   // 16 KB per buffer
   constexpr uint32_t B_BYTES = BN * BK * 4;   // BN * 128 bytes per buffer
   constexpr uint32_t STAGE_BYTES = 2 * A_BYTES + 2 * B_BYTES;
-  constexpr uint32_t TMEM_COLS = BN < 32 ? 32 : BN;
+  constexpr uint32_t TMEM_COLS = 2 * BN;  // two accumulators, used by alternate K blocks
   constexpr uint32_t IDESC = tf32_idesc(BM, BN);
 
   extern __shared__ uint8_t smem_raw[];
@@ -128,8 +132,9 @@ __global__ void __launch_bounds__(192, 1)
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
   uint64_t* conv = full + STAGES;
   uint64_t* empty = conv + STAGES;
-  uint64_t* accum = empty + STAGES;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accum + 1);
+  uint64_t* tfull = empty + STAGES;   // [2] accumulator a holds a finished K block
+  uint64_t* tempty = tfull + 2;       // [2] accumulator a has been read back
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -144,7 +149,10 @@ __global__ void __launch_bounds__(192, 1)
       mbar_init(&conv[s], 4);
       mbar_init(&empty[s], 1);
     }
-    mbar_init(accum, 1);
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 4);
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -200,14 +208,19 @@ __global__ void __launch_bounds__(192, 1)
       mbar_wait_bounded(&full[kb % STAGES], (kb / STAGES) & 1, p.err, p.limit_ns);
   } else if (warp == 1 && lane == 0) {
     // ---------------------------------------------------------------- MMA issuer
+    int done = 0;
     for (int kb = 0; kb < num_kb; ++kb) {
       const int s = kb % STAGES;
       const uint32_t ph = (kb / STAGES) & 1;
-      if (*abort_flag || !mbar_wait_bounded(&conv[s], ph, p.err, p.limit_ns)) {
+      const int a = kb & 1;
+      const uint32_t pa = (kb >> 1) & 1;
+      if (*abort_flag || !mbar_wait_bounded(&conv[s], ph, p.err, p.limit_ns) ||
+          !mbar_wait_bounded(&tempty[a], pa ^ 1, p.err, p.limit_ns)) {
         *abort_flag = 1;
         break;
       }
       tc_fence_after();
+      const uint32_t d = tmem_base + (uint32_t)(a * BN);
       const uint32_t a_hi = smem_base + s * STAGE_BYTES;
       const uint32_t a_lo = a_hi + A_BYTES;
       const uint32_t b_hi = a_hi + 2 * A_BYTES;
@@ -216,25 +229,55 @@ __global__ void __launch_bounds__(192, 1)
       for (int k = 0; k < BK / 8; ++k) {
         const uint64_t ah = sdesc(a_hi + k * 32, 16, 1024), al = sdesc(a_lo + k * 32, 16, 1024);
         const uint64_t bh = sdesc(b_hi + k * 32, 16, 1024), bl = sdesc(b_lo + k * 32, 16, 1024);
-        umma_tf32(tmem_base, ah, bh, IDESC, (kb | k) != 0);
-        umma_tf32(tmem_base, ah, bl, IDESC, 1);
-        umma_tf32(tmem_base, al, bh, IDESC, 1);
+        umma_tf32(d, ah, bh, IDESC, k != 0);
+        umma_tf32(d, ah, bl, IDESC, 1);
+        umma_tf32(d, al, bh, IDESC, 1);
       }
       umma_commit(&empty[s]);
+      umma_commit(&tfull[a]);
+      ++done;
     }
-    if (num_kb > 0) {
-      umma_commit(accum);
-      mbar_wait_bounded(accum, 0, p.err, p.limit_ns);
-    }
+    // TMEM is freed after the final barrier: wait until the last MMAs have completed.
+    if (done > 0) mbar_wait_bounded(&tfull[(done - 1) & 1], ((done - 1) >> 1) & 1, p.err, p.limit_ns);
   } else if (warp >= 2) {
-    // ---------------------------------------------------------------- converter
+    // ---------------------------------------------------------------- converter + promotion
     const int ct = threadIdx.x - 64;  // 0..127
-    for (int kb = 0; kb < num_kb; ++kb) {
+    const int q = warp & 3;           // TMEM lane quarter of this warp
+    const int r = q * 32 + lane;
+    const int i = mt * BM + r;
+    float acc[BN];
+#pragma unroll
+    for (int t = 0; t < BN; ++t) acc[t] = 0.f;
+    bool ok_all = true;
+    // Adds the accumulator of K block kk to the registers and hands the accumulator back.
+    auto promote = [&](int kk) {
+      const int a = kk & 1;
+      const bool ok = ok_all && mbar_wait_bounded(&tfull[a], (kk >> 1) & 1, p.err, p.limit_ns);
+      ok_all = __all_sync(0xffffffffu, ok);
+      if (!ok_all) {
+        *abort_flag = 1;
+        return;
+      }
+      tc_fence_after();
+#pragma unroll
+      for (int c0 = 0; c0 < BN; c0 += 32) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(a * BN + c0), v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int t = 0; t < 32; ++t) acc[c0 + t] += __uint_as_float(v[t]);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[a]);
+    };
+    for (int kb = 0; kb < num_kb && ok_all; ++kb) {
       const int s = kb % STAGES;
       const uint32_t ph = (kb / STAGES) & 1;
       const bool ok = !*abort_flag && mbar_wait_bounded(&full[s], ph, p.err, p.limit_ns);
       if (!__all_sync(0xffffffffu, ok)) {
         *abort_flag = 1;
+        ok_all = false;
         break;
       }
       const int seg = kb / p.kb_per_seg;
@@ -256,79 +299,65 @@ __global__ void __launch_bounds__(192, 1)
       fence_async_smem();  // generic-proxy writes -> visible to the tensor cores
       __syncwarp();
       if (lane == 0) mbar_arrive(&conv[s]);
+      if (kb >= 1) promote(kb - 1);
     }
+    if (ok_all && num_kb > 0) promote(num_kb - 1);
     // ---------------------------------------------------------------- epilogue
-    const int q = warp & 3;
-    const int r = q * 32 + lane;
-    const int i = mt * BM + r;
-    bool have = num_kb > 0 && !*abort_flag;
-    if (have) {
-      const bool ok = mbar_wait_bounded(accum, 0, p.err, p.limit_ns);
-      have = __all_sync(0xffffffffu, ok);
-      tc_fence_after();
-    }
     const long long base = (long long)blk * b * b;
-#pragma unroll 1
-    for (int c0 = 0; c0 < BN; c0 += 32) {
-      uint32_t v[32];
-      if (have) {
-        tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)c0, v);
-        tmem_ld_wait();
-      } else {
+    if (i < b) {
 #pragma unroll
-        for (int t = 0; t < 32; ++t) v[t] = 0u;
-      }
-      if (i >= b) continue;
-      const int j0 = nt * BN + c0;
-      const long long idx0 = base + (long long)i * b + j0;
-      float o[32];
+      for (int c0 = 0; c0 < BN; c0 += 32) {
+        const int j0 = nt * BN + c0;
+        const long long idx0 = base + (long long)i * b + j0;
+        float o[32];
 #pragma unroll
-      for (int t = 0; t < 32; ++t) o[t] = __uint_as_float(v[t]);
-      if (p.E1) {
-        const float4* e = reinterpret_cast<const float4*>(p.E1 + idx0);
+        for (int t = 0; t < 32; ++t) o[t] = acc[c0 + t];
+        if (p.E1) {
+          const float4* e = reinterpret_cast<const float4*>(p.E1 + idx0);
 #pragma unroll
-        for (int t = 0; t < 8; ++t) {
-          const float4 w = __ldg(e + t);
-          o[4 * t] = fmaf(p.e1, w.x, o[4 * t]);
-          o[4 * t + 1] = fmaf(p.e1, w.y, o[4 * t + 1]);
-          o[4 * t + 2] = fmaf(p.e1, w.z, o[4 * t + 2]);
-          o[4 * t + 3] = fmaf(p.e1, w.w, o[4 * t + 3]);
+          for (int t = 0; t < 8; ++t) {
+            const float4 w = __ldg(e + t);
+            o[4 * t] = fmaf(p.e1, w.x, o[4 * t]);
+            o[4 * t + 1] = fmaf(p.e1, w.y, o[4 * t + 1]);
+            o[4 * t + 2] = fmaf(p.e1, w.z, o[4 * t + 2]);
+            o[4 * t + 3] = fmaf(p.e1, w.w, o[4 * t + 3]);
+          }
         }
-      }
-      if (p.E2) {
-        const float4* e = reinterpret_cast<const float4*>(p.E2 + idx0);
+        if (p.E2) {
+          const float4* e = reinterpret_cast<const float4*>(p.E2 + idx0);
 #pragma unroll
-        for (int t = 0; t < 8; ++t) {
-          const float4 w = __ldg(e + t);
-          o[4 * t] = fmaf(p.e2, w.x, o[4 * t]);
-          o[4 * t + 1] = fmaf(p.e2, w.y, o[4 * t + 1]);
-          o[4 * t + 2] = fmaf(p.e2, w.z, o[4 * t + 2]);
-          o[4 * t + 3] = fmaf(p.e2, w.w, o[4 * t + 3]);
+          for (int t = 0; t < 8; ++t) {
+            const float4 w = __ldg(e + t);
+            o[4 * t] = fmaf(p.e2, w.x, o[4 * t]);
+            o[4 * t + 1] = fmaf(p.e2, w.y, o[4 * t + 1]);
+            o[4 * t + 2] = fmaf(p.e2, w.z, o[4 * t + 2]);
+            o[4 * t + 3] = fmaf(p.e2, w.w, o[4 * t + 3]);
+          }
         }
-      }
-#pragma unroll
-      for (int t = 0; t < 32; ++t)
-        if (j0 + t == i) o[t] += p.eI;
-      if (p.out_f32) {
-        float4* d = reinterpret_cast<float4*>(p.out_f32 + idx0);
-#pragma unroll
-        for (int t = 0; t < 8; ++t) d[t] = make_float4(o[4 * t], o[4 * t + 1], o[4 * t + 2], o[4 * t + 3]);
-      }
-      if (p.out_f32_t) {  // lanes hold consecutive rows i: each store is coalesced
-#pragma unroll
-        for (int t = 0; t < 32; ++t) p.out_f32_t[base + (long long)(j0 + t) * b + i] = o[t];
-      }
-      if (p.out_bf16) {
-        uint4* d = reinterpret_cast<uint4*>(p.out_bf16 + idx0);
-#pragma unroll
-        for (int t = 0; t < 4; ++t)
-          d[t] = make_uint4(pack_bf16x2(o[8 * t], o[8 * t + 1]), pack_bf16x2(o[8 * t + 2], o[8 * t + 3]),
-                            pack_bf16x2(o[8 * t + 4], o[8 * t + 5]), pack_bf16x2(o[8 * t + 6], o[8 * t + 7]));
-      }
-      if (p.out_bf16_t) {
 #pragma unroll
         for (int t = 0; t < 32; ++t)
-          p.out_bf16_t[base + (long long)(j0 + t) * b + i] = __float2bfloat16_rn(o[t]);
+          if (j0 + t == i) o[t] += p.eI;
+        if (p.out_f32) {
+          float4* d = reinterpret_cast<float4*>(p.out_f32 + idx0);
+#pragma unroll
+          for (int t = 0; t < 8; ++t) d[t] = make_float4(o[4 * t], o[4 * t + 1], o[4 * t + 2], o[4 * t + 3]);
+        }
+        if (p.out_f32_t) {  // lanes hold consecutive rows i: each store is coalesced
+#pragma unroll
+          for (int t = 0; t < 32; ++t) p.out_f32_t[base + (long long)(j0 + t) * b + i] = o[t];
+        }
+        if (p.out_bf16) {
+          uint4* d = reinterpret_cast<uint4*>(p.out_bf16 + idx0);
+#pragma unroll
+          for (int t = 0; t < 4; ++t)
+            d[t] = make_uint4(pack_bf16x2(o[8 * t], o[8 * t + 1]), pack_bf16x2(o[8 * t + 2], o[8 * t + 3]),
+                              pack_bf16x2(o[8 * t + 4], o[8 * t + 5]), pack_bf16x2(o[8 * t + 6], o[8 * t + 7]));
+        }
+        if (p.out_bf16_t) {
+#pragma unroll
+          for (int t = 0; t < 32; ++t)
+            p.out_bf16_t[base + (long long)(j0 + t) * b + i] = __float2bfloat16_rn(o[t]);
+        }
       }
     }
   }
