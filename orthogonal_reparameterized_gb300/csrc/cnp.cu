@@ -157,7 +157,8 @@ __global__ void sum_partials_kernel(const float* __restrict__ dG0, int S0, int n
     if (r < b && c < b) {
       const long long off = (long long)r * b + c;
       a = src[off];
-      for (int s2 = 1; s2 < S; ++s2) a += src[s2 * sstride + off];
+#pragma unroll 8
+      for (int s2 = 1; s2 < S; ++s2) a += src[s2 * sstride + off];  // fixed order
       X[base + off] = a;
     }
     tile[rr][threadIdx.x] = a;
@@ -213,21 +214,25 @@ poetx_status cnp_forward(const float* q, int nblk, int b, float* Qs, float* Q2, 
   return cnp_forward_sides(sides, b, Qs, Q2, G_f32, G_bf16, Gt_bf16, s);
 }
 
-poetx_status cnp_backward_sides(const CnpSides& q, const float* Q2in, const float* const dG[2],
-                                const int splits[2], int b, float* const dq[2], int accumulate,
-                                void* scratch, cudaStream_t s) {
+poetx_status cnp_backward_sides(const CnpSides& q, const float* Qin, const float* Q2in,
+                                const float* const dG[2], const int splits[2], int b,
+                                float* const dq[2], int accumulate, void* scratch, cudaStream_t s) {
   const int nblk = q.n[0] + q.n[1];
   if (nblk == 0) return POETX_OK;
   char* w = static_cast<char*>(scratch);
   const size_t bb = blk_bytes(nblk, b);
-  float* Qs = reinterpret_cast<float*>(w);
+  float* Qw = reinterpret_cast<float*>(w);
   float* Q2 = reinterpret_cast<float*>(w + bb);
   float* X = reinterpret_cast<float*>(w + 2 * bb);
   float* Xt = reinterpret_cast<float*>(w + 3 * bb);
   float* M1 = reinterpret_cast<float*>(w + 4 * bb);
   float* M1t = reinterpret_cast<float*>(w + 5 * bb);
   float* Qbar = reinterpret_cast<float*>(w + 6 * bb);
-  POETX_TRY(launch_triu_unpack2(q.q[0], q.n[0], q.q[1], q.n[1], b, Qs, s));
+  const float* Qs = Qin;
+  if (!Qs) {
+    POETX_TRY(launch_triu_unpack2(q.q[0], q.n[0], q.q[1], q.n[1], b, Qw, s));
+    Qs = Qw;
+  }
   if (!Q2in) {
     CnpGemm g{};
     g.b = b;
@@ -314,5 +319,5 @@ extern "C" poetx_status poetx_cnp_bwd(const float* q, const float* dG, int split
   const float* const dGs[2] = {dG, nullptr};
   const int sp[2] = {splits, 1};
   float* const dqs[2] = {dq, nullptr};
-  return cnp_backward_sides(sides, nullptr, dGs, sp, b, dqs, accumulate, ws, stream);
+  return cnp_backward_sides(sides, nullptr, nullptr, dGs, sp, b, dqs, accumulate, ws, stream);
 }

@@ -18,19 +18,41 @@ __device__ __forceinline__ long long tri_index(int i, int j, int b) {
 }
 
 // Blocks [0, n0) come from q0, blocks [n0, gridDim.z) from q1 (the R and P sides of a layer
-// are unpacked by one launch).
+// are unpacked by one launch).  One CTA per 32 x 32 tile (I, J) with I <= J of a block: it
+// reads the packed entries of the tile's upper part (consecutive j are consecutive in q),
+// writes Q[I][J] and, through shared memory, the mirrored tile Q[J][I] = -Q[I][J]^T, both
+// with coalesced rows.
 __global__ void triu_unpack_kernel(const float* __restrict__ q0, int n0, const float* __restrict__ q1,
                                    int b, float* __restrict__ Q) {
+  __shared__ float tile[32][33];
   const int blk = blockIdx.z;
-  const int i = blockIdx.y;
+  const int nt = (b + 31) / 32;
+  // decode the linear upper-tile index blockIdx.x -> (I, J), I <= J
+  int t = blockIdx.x, I = 0;
+  while (t >= nt - I) {
+    t -= nt - I;
+    ++I;
+  }
+  const int J = I + t;
   const long long tri = (long long)b * (b - 1) / 2;
   const float* qb = blk < n0 ? q0 + blk * tri : q1 + (blk - n0) * tri;
-  float* row = Q + ((long long)blk * b + i) * b;
-  for (int j = blockIdx.x * blockDim.x + threadIdx.x; j < b; j += gridDim.x * blockDim.x) {
+  float* Qb = Q + (long long)blk * b * b;
+  const int tx = threadIdx.x, ty = threadIdx.y;  // 32 x 8
+  for (int r = ty; r < 32; r += 8) {
+    const int i = I * 32 + r, j = J * 32 + tx;
     float v = 0.f;
-    if (i < j) v = qb[tri_index(i, j, b)];
-    else if (i > j) v = -qb[tri_index(j, i, b)];
-    row[j] = v;
+    if (i < b && j < b) {
+      if (i < j) v = qb[tri_index(i, j, b)];
+      else if (i > j) v = -qb[tri_index(j, i, b)];
+      Qb[(long long)i * b + j] = v;
+    }
+    tile[r][tx] = v;
+  }
+  if (I == J) return;  // the diagonal tile wrote both of its triangles already
+  __syncthreads();
+  for (int c = ty; c < 32; c += 8) {
+    const int i = J * 32 + c, j = I * 32 + tx;  // Q[i][j] = -Q[j][i]
+    if (i < b && j < b) Qb[(long long)i * b + j] = -tile[tx][c];
   }
 }
 
@@ -51,9 +73,9 @@ __global__ void triu_grad_pack_kernel(const float* __restrict__ Qbar, int b, flo
 poetx_status launch_triu_unpack2(const float* q0, int n0, const float* q1, int n1, int b, float* Q,
                                  cudaStream_t s) {
   if (n0 + n1 == 0) return POETX_OK;
-  const int threads = b < 256 ? ((b + 31) / 32) * 32 : 256;
-  dim3 grid(1, b, n0 + n1);
-  triu_unpack_kernel<<<grid, threads, 0, s>>>(q0, n0, q1, b, Q);
+  const int nt = (b + 31) / 32;
+  dim3 grid(nt * (nt + 1) / 2, 1, n0 + n1);
+  triu_unpack_kernel<<<grid, dim3(32, 8), 0, s>>>(q0, n0, q1, b, Q);
   POETX_CUDA_TRY(cudaGetLastError());
   after_launch(s, ST_TRIU_UNPACK);
   return POETX_OK;
@@ -80,10 +102,14 @@ poetx_status launch_triu_grad_pack(const float* Qbar, int nblk, int b, float* dq
 }
 
 // ---------------------------------------------------------------- row permutations
-// One CTA per row at a time (grid-stride over rows).  The row is staged in shared memory:
-// gather reads it coalesced and writes out[i] = row[perm[i]] as 16-byte vectors; scatter
-// reads 16-byte vectors, writes row[perm[i]] = in[i] into shared memory, then stores the
-// row coalesced.  `src_rows` (nullable) remaps the source row (used by the merge).
+// Persistent CTAs walk the rows (r = blockIdx.x, + gridDim.x, ...).  Each CTA first stages
+// the gather index of the whole row in shared memory: perm itself for a gather, its inverse
+// (idx[perm[i]] = i) for a scatter, so both become out[i] = row[idx[i]].  Rows arrive in a
+// ring of NBUF shared-memory buffers by one-dimensional TMA bulk copies issued by thread 0
+// (NBUF rows ahead), and every thread writes 16-byte vectors of the output row, so loads and
+// stores are both fully coalesced.  `src_rows` (nullable) remaps the source row (the merge
+// W'[r, :] = W0[perm_n[r], perm_m]).  Waits are bounded; on expiry the kernel records
+// POETX_ERR_TIMEOUT, drains the copies it issued and returns.
 template <int E>
 struct VecT;
 template <>
@@ -93,66 +119,152 @@ struct VecT<2> { using T = uint16_t; };
 template <>
 struct VecT<4> { using T = uint32_t; };
 
-template <int E, bool SCATTER>
+__device__ __forceinline__ void bulk_load(void* smem_dst, const void* src, uint32_t bytes,
+                                          uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(smem_dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// V consecutive gather indices, read from shared memory with one aligned vector load per
+// 16 bytes (8-byte loads when the V indices take 8 bytes).
+template <typename IdxT, int V>
+struct IdxVec {
+  IdxT i[V];
+};
+template <typename IdxT, int V>
+__device__ __forceinline__ IdxVec<IdxT, V> load_idx(const IdxT* p) {
+  constexpr int IB = V * (int)sizeof(IdxT);
+  IdxVec<IdxT, V> r;
+  if constexpr (IB == 8) {
+    union { uint2 u; IdxT i[V]; } x;
+    x.u = *reinterpret_cast<const uint2*>(p);
+#pragma unroll
+    for (int e = 0; e < V; ++e) r.i[e] = x.i[e];
+  } else {
+    static_assert(IB % 16 == 0, "index vector must be 8 or a multiple of 16 bytes");
+    union { uint4 u[IB / 16]; IdxT i[V]; } x;
+#pragma unroll
+    for (int w = 0; w < IB / 16; ++w) x.u[w] = reinterpret_cast<const uint4*>(p)[w];
+#pragma unroll
+    for (int e = 0; e < V; ++e) r.i[e] = x.i[e];
+  }
+  return r;
+}
+
+template <int E, bool SCATTER, typename IdxT>
 __global__ void __launch_bounds__(256) perm_rows_kernel(const uint8_t* __restrict__ X, long long N,
                                                         int D, const int32_t* __restrict__ perm,
                                                         uint8_t* __restrict__ Y,
                                                         const int32_t* __restrict__ src_rows,
                                                         const float* __restrict__ scale,
-                                                        float* __restrict__ scale_out) {
+                                                        float* __restrict__ scale_out, int nbuf,
+                                                        int* err, unsigned long long limit_ns) {
   using T = typename VecT<E>::T;
   constexpr int V = 16 / E;  // elements per 16-byte vector
-  extern __shared__ __align__(16) uint8_t smem_raw[];
-  T* buf = reinterpret_cast<T*>(smem_raw);
-  const int nvec = D / V;
-  const size_t row_bytes = (size_t)D * E;
-  for (long long r = blockIdx.x; r < N; r += gridDim.x) {
-    const long long src = src_rows ? (long long)src_rows[r] : r;
-    const uint4* in = reinterpret_cast<const uint4*>(X + src * row_bytes);
-    uint4* out = reinterpret_cast<uint4*>(Y + r * row_bytes);
-    if (scale_out && threadIdx.x == 0) scale_out[r] = scale[src];
-    if (!SCATTER) {
-      uint4* b4 = reinterpret_cast<uint4*>(buf);
-      for (int v = threadIdx.x; v < nvec; v += blockDim.x) b4[v] = __ldg(in + v);
-      __syncthreads();
-      for (int v = threadIdx.x; v < nvec; v += blockDim.x) {
-        union { uint4 u; T e[V]; } pk;
-#pragma unroll
-        for (int e = 0; e < V; ++e) pk.e[e] = buf[__ldg(perm + v * V + e)];
-        out[v] = pk.u;
-      }
-      __syncthreads();
-    } else {
-      for (int v = threadIdx.x; v < nvec; v += blockDim.x) {
-        union { uint4 u; T e[V]; } pk;
-        pk.u = __ldg(in + v);
-#pragma unroll
-        for (int e = 0; e < V; ++e) buf[__ldg(perm + v * V + e)] = pk.e[e];
-      }
-      __syncthreads();
-      const uint4* b4 = reinterpret_cast<const uint4*>(buf);
-      for (int v = threadIdx.x; v < nvec; v += blockDim.x) out[v] = b4[v];
-      __syncthreads();
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  const uint32_t row_bytes = (uint32_t)D * E;
+  const uint32_t idx_bytes = ((uint32_t)D * sizeof(IdxT) + 127u) & ~127u;
+  IdxT* idx = reinterpret_cast<IdxT*>(smem_raw);
+  uint8_t* ring = smem_raw + idx_bytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(ring + (size_t)nbuf * row_bytes);
+  const long long first = blockIdx.x;
+  const long long stride = gridDim.x;
+  const long long nrows = first < N ? (N - 1 - first) / stride + 1 : 0;  // rows of this CTA
+
+  if (threadIdx.x == 0) {
+    for (int k = 0; k < nbuf; ++k) mbar_init(&full[k], 1);
+    fence_mbar_init();
+  }
+  for (int i = threadIdx.x; i < D; i += blockDim.x) {
+    const int pi = __ldg(perm + i);
+    if (SCATTER) idx[pi] = (IdxT)i;
+    else idx[i] = (IdxT)pi;
+  }
+  __syncthreads();
+  auto src_of = [&](long long it) -> const uint8_t* {
+    const long long r = first + it * stride;
+    const long long sr = src_rows ? (long long)__ldg(src_rows + r) : r;
+    return X + sr * row_bytes;
+  };
+  if (threadIdx.x == 0) {
+    for (int k = 0; k < nbuf && k < nrows; ++k) {
+      mbar_arrive_expect_tx(&full[k], row_bytes);
+      bulk_load(ring + (size_t)k * row_bytes, src_of(k), row_bytes, &full[k]);
     }
+  }
+  const int nvec = D / V;
+  bool ok = true;
+  long long it = 0;
+  for (; it < nrows; ++it) {
+    const int k = (int)(it % nbuf);
+    const uint32_t ph = (uint32_t)((it / nbuf) & 1);
+    const bool got = mbar_wait_bounded(&full[k], ph, err, limit_ns);
+    if (!__syncthreads_and(got)) {
+      ok = false;
+      break;
+    }
+    const long long r = first + it * stride;
+    const T* row = reinterpret_cast<const T*>(ring + (size_t)k * row_bytes);
+    uint4* out = reinterpret_cast<uint4*>(Y + r * row_bytes);
+    for (int v = threadIdx.x; v < nvec; v += blockDim.x) {
+      const IdxVec<IdxT, V> ix = load_idx<IdxT, V>(idx + (size_t)v * V);
+      union { uint4 u; T e[V]; } pk;
+#pragma unroll
+      for (int e = 0; e < V; ++e) pk.e[e] = row[ix.i[e]];
+      out[v] = pk.u;
+    }
+    if (scale_out && threadIdx.x == 0) scale_out[r] = scale[src_rows ? src_rows[r] : r];
+    __syncthreads();  // every thread is done with buffer k
+    if (threadIdx.x == 0 && it + nbuf < nrows) {
+      mbar_arrive_expect_tx(&full[k], row_bytes);
+      bulk_load(ring + (size_t)k * row_bytes, src_of(it + nbuf), row_bytes, &full[k]);
+    }
+  }
+  if (!ok && threadIdx.x == 0) {
+    // drain the copies still in flight before the shared memory goes away
+    for (long long j = it; j < nrows && j < it + nbuf; ++j)
+      mbar_wait_bounded(&full[j % nbuf], (uint32_t)((j / nbuf) & 1), err, limit_ns);
   }
 }
 
-template <int E, bool SCATTER>
+template <int E, bool SCATTER, typename IdxT>
 static poetx_status launch_perm_rows_t(const void* X, long long N, int D, const int32_t* perm,
                                        void* Y, const int32_t* src_rows, const float* scale,
                                        float* scale_out, cudaStream_t s) {
-  const size_t smem = (size_t)D * E;
-  auto k = perm_rows_kernel<E, SCATTER>;
-  if (smem > 48 * 1024) POETX_CUDA_TRY(cudaFuncSetAttribute(
-      k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
-  const int per_sm = smem > 0 ? (int)((200 * 1024) / smem) : 8;
-  const long long want = (long long)sm_count() * (per_sm < 1 ? 1 : (per_sm > 8 ? 8 : per_sm));
+  const size_t row_bytes = (size_t)D * E;
+  const size_t idx_bytes = ((size_t)D * sizeof(IdxT) + 127) & ~(size_t)127;
+  // ring of rows: aim at ~64 KB of rows in flight per CTA, 2..8 buffers, <= 200 KB in total
+  int nbuf = (int)((64 * 1024) / row_bytes);
+  nbuf = nbuf < 2 ? 2 : (nbuf > 8 ? 8 : nbuf);
+  while (nbuf > 2 && idx_bytes + nbuf * row_bytes + 128 > 200 * 1024) --nbuf;
+  const size_t smem = idx_bytes + nbuf * row_bytes + 8 * (size_t)nbuf;
+  if (smem > 227 * 1024) return POETX_ERR_SHAPE;
+  auto k = perm_rows_kernel<E, SCATTER, IdxT>;
+  POETX_CUDA_TRY(cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+  int per_sm = (int)((220 * 1024) / (smem + 1024));
+  per_sm = per_sm < 1 ? 1 : (per_sm > 8 ? 8 : per_sm);
+  const long long want = (long long)sm_count() * per_sm;
   const int grid = (int)(N < want ? N : want);
   k<<<grid, 256, smem, s>>>(static_cast<const uint8_t*>(X), N, D, perm, static_cast<uint8_t*>(Y),
-                           src_rows, scale, scale_out);
+                           src_rows, scale, scale_out, nbuf, device_error_word(), kWaitLimitNs);
   POETX_CUDA_TRY(cudaGetLastError());
   after_launch(s, src_rows ? ST_MERGE : (SCATTER ? ST_PERM_SCATTER : ST_PERM_GATHER));
   return POETX_OK;
+}
+
+template <int E>
+static poetx_status launch_perm_rows_e(bool scatter, const void* X, long long N, int D,
+                                       const int32_t* perm, void* Y, const int32_t* src_rows,
+                                       const float* scale, float* scale_out, cudaStream_t s) {
+  if (D <= 65535) {
+    return scatter ? launch_perm_rows_t<E, true, uint16_t>(X, N, D, perm, Y, src_rows, scale, scale_out, s)
+                   : launch_perm_rows_t<E, false, uint16_t>(X, N, D, perm, Y, src_rows, scale, scale_out, s);
+  }
+  return scatter ? launch_perm_rows_t<E, true, uint32_t>(X, N, D, perm, Y, src_rows, scale, scale_out, s)
+                 : launch_perm_rows_t<E, false, uint32_t>(X, N, D, perm, Y, src_rows, scale, scale_out, s);
 }
 
 poetx_status launch_perm_rows(size_t esize, bool scatter, const void* X, long long N, int D,
@@ -160,16 +272,9 @@ poetx_status launch_perm_rows(size_t esize, bool scatter, const void* X, long lo
                               const float* scale, float* scale_out, cudaStream_t s) {
   if (N == 0 || D == 0) return POETX_OK;
   if (((size_t)D * esize) % 16 != 0) return POETX_ERR_SHAPE;
-  if ((size_t)D * esize > 200 * 1024) return POETX_ERR_SHAPE;
-  if (esize == 1)
-    return scatter ? launch_perm_rows_t<1, true>(X, N, D, perm, Y, src_rows, scale, scale_out, s)
-                   : launch_perm_rows_t<1, false>(X, N, D, perm, Y, src_rows, scale, scale_out, s);
-  if (esize == 2)
-    return scatter ? launch_perm_rows_t<2, true>(X, N, D, perm, Y, src_rows, scale, scale_out, s)
-                   : launch_perm_rows_t<2, false>(X, N, D, perm, Y, src_rows, scale, scale_out, s);
-  if (esize == 4)
-    return scatter ? launch_perm_rows_t<4, true>(X, N, D, perm, Y, src_rows, scale, scale_out, s)
-                   : launch_perm_rows_t<4, false>(X, N, D, perm, Y, src_rows, scale, scale_out, s);
+  if (esize == 1) return launch_perm_rows_e<1>(scatter, X, N, D, perm, Y, src_rows, scale, scale_out, s);
+  if (esize == 2) return launch_perm_rows_e<2>(scatter, X, N, D, perm, Y, src_rows, scale, scale_out, s);
+  if (esize == 4) return launch_perm_rows_e<4>(scatter, X, N, D, perm, Y, src_rows, scale, scale_out, s);
   return POETX_ERR_DTYPE;
 }
 

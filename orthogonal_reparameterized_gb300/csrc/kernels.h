@@ -62,12 +62,13 @@ poetx_status cnp_forward(const float* q, int nblk, int b, float* Qs, float* Q2, 
                          void* G_bf16, void* Gt_bf16, cudaStream_t s);
 poetx_status cnp_forward_sides(const CnpSides& q, int b, float* Qs, float* Q2, float* G_f32,
                                void* G_bf16, void* Gt_bf16, cudaStream_t s);
-// Backward CNP.  Q2 may be a precomputed Q^2 stack or NULL to recompute it into the scratch;
-// dG[side] is [splits[side], n[side], b, b]; dq[side] receives that side's gradient.
-// scratch holds cnp_bwd_scratch_bytes(n[0] + n[1], b) bytes.
-poetx_status cnp_backward_sides(const CnpSides& q, const float* Q2, const float* const dG[2],
-                                const int splits[2], int b, float* const dq[2], int accumulate,
-                                void* scratch, cudaStream_t s);
+// Backward CNP.  Q and Q2 may be the stacks kept from the forward, or NULL to recompute
+// them into the scratch; dG[side] is [splits[side], n[side], b, b]; dq[side] receives that
+// side's gradient.  scratch holds cnp_bwd_scratch_bytes(n[0] + n[1], b) bytes.
+poetx_status cnp_backward_sides(const CnpSides& q, const float* Q, const float* Q2,
+                                const float* const dG[2], const int splits[2], int b,
+                                float* const dq[2], int accumulate, void* scratch,
+                                cudaStream_t s);
 
 // ---- layer.cu: engine switch (tensor cores unless disabled by poetx_set_gemm_engine)
 bool use_tensor_cores();

@@ -30,7 +30,7 @@ bool use_tensor_cores() { return g_engine.load() == 0; }
 
 static int wgrad_splits(long long N, int nblk, int b) {
   const long long tiles = (long long)nblk * ((b + 127) / 128) * (b > 256 ? b / 256 : 1);
-  long long s = (2LL * sm_count() + tiles - 1) / tiles;
+  long long s = ((long long)sm_count() + tiles - 1) / tiles;
   long long smax = N / 256;
   if (smax < 1) smax = 1;
   if (s > smax) s = smax;
@@ -113,9 +113,9 @@ poetx_status wprime_impl(poetx_dtype act, poetx_dtype wdt, const void* A, long l
 // ---------------------------------------------------------------- layer plumbing
 struct Plan {
   // saved
-  size_t GR, GP, Q2R, Q2P, Bsv, saved_total;
+  size_t GR, GP, Q2R, Q2P, Qs, Bsv, saved_total;
   // forward workspace
-  size_t f_Qs, f_xt, f_A, f_B, f_zt, fwd_total;
+  size_t f_xt, f_A, f_B, f_zt, fwd_total;
   // backward workspace
   size_t b_cnp, b_xt, b_dzt, b_A, b_B, b_dB, b_dA, b_dxt, b_dGP, b_dGR, bwd_total;
   int splitsR, splitsP;
@@ -155,11 +155,11 @@ static Plan make_plan(const poetx_layer* L, long long N) {
   p.GP = p.GR + m * b * gs;
   p.Q2R = take((m + n) * b * 4);
   p.Q2P = p.Q2R + m * b * 4;
+  p.Qs = take((m + n) * b * 4);
   p.Bsv = L->variant == POETX_FAST ? take((size_t)N * n * as) : 0;
   p.saved_total = o;
 
   o = 0;
-  p.f_Qs = take((m + n) * b * 4);
   p.f_xt = take((size_t)N * m * as);
   p.f_A = take((size_t)N * m * as);
   p.f_B = L->variant == POETX_MEM ? take((size_t)N * n * as) : 0;
@@ -231,7 +231,7 @@ extern "C" poetx_status poetx_layer_fwd(const poetx_layer* L, const void* x, int
   // S1-S2: both CNPs in one pass over the m/b + n/b blocks; G in the activation precision
   // and Q^2 kept for the backward
   const CnpSides sides{{L->q_R, L->q_P}, {m / b, n / b}};
-  POETX_TRY(cnp_forward_sides(sides, b, at<float>(ws, p.f_Qs), at<float>(saved, p.Q2R),
+  POETX_TRY(cnp_forward_sides(sides, b, at<float>(saved, p.Qs), at<float>(saved, p.Q2R),
                               f32 ? at<float>(saved, p.GR) : nullptr,
                               f32 ? nullptr : at(saved, p.GR), nullptr, stream));
   if (N == 0) return POETX_OK;
@@ -298,8 +298,8 @@ extern "C" poetx_status poetx_layer_bwd(const poetx_layer* L, const void* x, con
   const float* const dGs[2] = {dGR, dGP};
   const int splits[2] = {p.splitsR, p.splitsP};
   float* const dqs[2] = {dq_R, dq_P};
-  return cnp_backward_sides(sides, at<float>(saved, p.Q2R), dGs, splits, b, dqs, accumulate,
-                            at(ws, p.b_cnp), stream);
+  return cnp_backward_sides(sides, at<float>(saved, p.Qs), at<float>(saved, p.Q2R), dGs, splits,
+                            b, dqs, accumulate, at(ws, p.b_cnp), stream);
 }
 
 // ---------------------------------------------------------------- step entry points
