@@ -174,9 +174,19 @@ __global__ void __launch_bounds__(256) perm_rows_kernel(const uint8_t* __restric
   const long long stride = gridDim.x;
   const long long nrows = first < N ? (N - 1 - first) / stride + 1 : 0;  // rows of this CTA
 
+  auto src_of = [&](long long it) -> const uint8_t* {
+    const long long r = first + it * stride;
+    const long long sr = src_rows ? (long long)__ldg(src_rows + r) : r;
+    return X + sr * row_bytes;
+  };
+  // start the first row copies, then stage the index while they are in flight
   if (threadIdx.x == 0) {
     for (int k = 0; k < nbuf; ++k) mbar_init(&full[k], 1);
     fence_mbar_init();
+    for (int k = 0; k < nbuf && k < nrows; ++k) {
+      mbar_arrive_expect_tx(&full[k], row_bytes);
+      bulk_load(ring + (size_t)k * row_bytes, src_of(k), row_bytes, &full[k]);
+    }
   }
   for (int i = threadIdx.x; i < D; i += blockDim.x) {
     const int pi = __ldg(perm + i);
@@ -184,17 +194,6 @@ __global__ void __launch_bounds__(256) perm_rows_kernel(const uint8_t* __restric
     else idx[i] = (IdxT)pi;
   }
   __syncthreads();
-  auto src_of = [&](long long it) -> const uint8_t* {
-    const long long r = first + it * stride;
-    const long long sr = src_rows ? (long long)__ldg(src_rows + r) : r;
-    return X + sr * row_bytes;
-  };
-  if (threadIdx.x == 0) {
-    for (int k = 0; k < nbuf && k < nrows; ++k) {
-      mbar_arrive_expect_tx(&full[k], row_bytes);
-      bulk_load(ring + (size_t)k * row_bytes, src_of(k), row_bytes, &full[k]);
-    }
-  }
   const int nvec = D / V;
   bool ok = true;
   long long it = 0;
@@ -244,8 +243,9 @@ static poetx_status launch_perm_rows_t(const void* X, long long N, int D, const 
   if (smem > 227 * 1024) return POETX_ERR_SHAPE;
   auto k = perm_rows_kernel<E, SCATTER, IdxT>;
   POETX_CUDA_TRY(cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+  // two CTAs per SM at most: each stages the whole index once, so it should own many rows
   int per_sm = (int)((220 * 1024) / (smem + 1024));
-  per_sm = per_sm < 1 ? 1 : (per_sm > 8 ? 8 : per_sm);
+  per_sm = per_sm < 1 ? 1 : (per_sm > 2 ? 2 : per_sm);
   const long long want = (long long)sm_count() * per_sm;
   const int grid = (int)(N < want ? N : want);
   k<<<grid, 256, smem, s>>>(static_cast<const uint8_t*>(X), N, D, perm, static_cast<uint8_t*>(Y),

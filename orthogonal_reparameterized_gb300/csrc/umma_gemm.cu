@@ -8,10 +8,12 @@
 //                              same page, section 1)
 //   block weight gradients     dG_j = X_j^T dY_j over a token range (S10, S12)
 //
-// One CTA computes one 128 x BN output tile over its K range.  Warp 0 issues the TMA loads,
-// one thread of warp 1 issues the MMAs (4 x K=16 per 64-wide K block) and owns the TMEM
-// allocation, warps 2-5 read the accumulator back (tcgen05.ld 32x32b: warp w reads lanes
-// 32*(w%4)..+31 = output rows) and store it.  Operands may be K-major (rows of the tile are
+// Persistent CTAs walk the 128 x BN output tiles (tile t = blockIdx.x, + gridDim.x, ...; the
+// M index varies fastest so that concurrent CTAs share the B operand in L2).  Warp 0 issues
+// the TMA loads into a STAGES-deep ring, one thread of warp 1 issues the MMAs (4 x K=16 per
+// 64-wide K block) into one of two TMEM accumulators (alternate tiles), and warps 2-5 read
+// the other accumulator back (tcgen05.ld 32x32b: warp w reads lanes 32*(w%4)..+31 = output
+// rows) and store it, so the epilogue of one tile overlaps the loads and MMAs of the next.  Operands may be K-major (rows of the tile are
 // contiguous along K) or MN-major (contiguous along M/N, e.g. the token-major activations
 // of a weight gradient); both use the canonical 128-byte swizzle layouts of tcgen05.
 // Every mbarrier wait is bounded; on expiry the kernel records POETX_ERR_TIMEOUT, drains
@@ -29,6 +31,8 @@ enum Mode : int { MODE_PLAIN = 0, MODE_BLOCKDIAG = 1, MODE_WGRAD = 2 };
 
 struct UmmaParams {
   int mode;
+  int tiles_m, tiles_n, num_tiles;  // tile t: mt = t % tiles_m, nt = (t / tiles_m) % tiles_n,
+                                    // z = t / (tiles_m * tiles_n) (block, or block*splits+split)
   int M;         // valid output rows of the whole problem (tokens, or b for WGRAD)
   int num_kb;    // 64-wide K blocks per CTA (PLAIN, BLOCKDIAG)
   int b;         // block size (BLOCKDIAG, WGRAD)
@@ -77,6 +81,49 @@ __device__ __forceinline__ uint64_t tile_desc(uint32_t base, int k) {
   return MN ? make_sdesc(base + k * 2048, 8192, 1024) : make_sdesc(base + k * 32, 16, 1024);
 }
 
+// Coordinates of one output tile (TMA coordinates are {inner, outer} = {column, row}).
+struct TileCoords {
+  int num_kb;
+  int a_c0, a_c1, b_c0, b_c1;
+  long long out_row0, out_col0;
+  int split, blk;
+};
+
+template <int BN, bool B_MN>
+__device__ __forceinline__ TileCoords tile_coords(const UmmaParams& p, int t) {
+  TileCoords c;
+  const int mt = t % p.tiles_m;
+  const int rest = t / p.tiles_m;
+  const int nt = rest % p.tiles_n;
+  const int z = rest / p.tiles_n;
+  c.num_kb = p.num_kb;
+  c.out_row0 = (long long)mt * BM;
+  c.out_col0 = (long long)nt * BN;
+  c.split = 0;
+  c.blk = 0;
+  if (p.mode == MODE_PLAIN) {
+    c.a_c0 = 0; c.a_c1 = mt * BM;                               // A K-major
+    if (!B_MN) { c.b_c0 = 0; c.b_c1 = nt * BN; }                // B K-major: W [n][m]
+    else { c.b_c0 = nt * BN; c.b_c1 = 0; }                      // B MN-major: W [K=n][MN=m]
+  } else if (p.mode == MODE_BLOCKDIAG) {
+    c.blk = z;
+    c.a_c0 = z * p.b; c.a_c1 = mt * BM;
+    if (!B_MN) { c.b_c0 = 0; c.b_c1 = z * p.b + nt * BN; }      // G_j rows = output cols
+    else { c.b_c0 = nt * BN; c.b_c1 = z * p.b; }                // G_j rows = K
+    c.out_col0 = (long long)z * p.b + nt * BN;
+  } else {  // MODE_WGRAD: A = X_j (MN-major), B = dY_j (MN-major), K = tokens of the split
+    c.blk = z / p.splits;
+    c.split = z % p.splits;
+    const long long t0 = (long long)c.split * p.kchunk;
+    long long tcount = p.ntok - t0;
+    if (tcount > p.kchunk) tcount = p.kchunk;
+    c.num_kb = tcount > 0 ? (int)((tcount + BK - 1) / BK) : 0;
+    c.a_c0 = c.blk * p.b + mt * BM; c.a_c1 = (int)t0;
+    c.b_c0 = c.blk * p.b + nt * BN; c.b_c1 = (int)t0;
+  }
+  return c;
+}
+
 template <int BN, int STAGES, bool A_MN, bool B_MN, bool OUT_F32>
 __global__ void __launch_bounds__(192, 1)
     umma_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
@@ -84,7 +131,7 @@ __global__ void __launch_bounds__(192, 1)
   constexpr uint32_t A_BYTES = BM * BK * 2;
   constexpr uint32_t B_BYTES = BN * BK * 2;
   constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
-  constexpr uint32_t TMEM_COLS = BN < 32 ? 32 : BN;
+  constexpr uint32_t TMEM_COLS = 2 * BN;  // two accumulators
   constexpr uint32_t IDESC = make_idesc(BM, BN, A_MN, B_MN);
 
   extern __shared__ uint8_t smem_raw[];
@@ -92,45 +139,22 @@ __global__ void __launch_bounds__(192, 1)
                                              ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
   uint64_t* empty = full + STAGES;
-  uint64_t* accum = empty + STAGES;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accum + 1);
+  uint64_t* tfull = empty + STAGES;  // [2]
+  uint64_t* tempty = tfull + 2;      // [2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int mt = blockIdx.x, nt = blockIdx.y;
-
-  // ---- tile coordinates (TMA coordinates are {inner, outer} = {column, row})
-  int num_kb = p.num_kb;
-  int a_c0 = 0, a_c1 = 0, b_c0 = 0, b_c1 = 0;  // bases; K offsets are added per K block
-  long long out_row0 = (long long)mt * BM, out_col0 = (long long)nt * BN;
-  int split = 0, blk = 0;
-  if (p.mode == MODE_PLAIN) {
-    a_c0 = 0; a_c1 = mt * BM;                               // A K-major
-    if (!B_MN) { b_c0 = 0; b_c1 = nt * BN; }                // B K-major: W [n][m]
-    else { b_c0 = nt * BN; b_c1 = 0; }                      // B MN-major: W [K=n][MN=m]
-  } else if (p.mode == MODE_BLOCKDIAG) {
-    blk = blockIdx.z;
-    a_c0 = blk * p.b; a_c1 = mt * BM;
-    if (!B_MN) { b_c0 = 0; b_c1 = blk * p.b + nt * BN; }    // G_j rows = output cols
-    else { b_c0 = nt * BN; b_c1 = blk * p.b; }              // G_j rows = K
-    out_col0 = (long long)blk * p.b + nt * BN;
-  } else {  // MODE_WGRAD: A = X_j (MN-major), B = dY_j (MN-major), K = tokens
-    blk = blockIdx.z / p.splits;
-    split = blockIdx.z % p.splits;
-    const long long t0 = (long long)split * p.kchunk;
-    long long tcount = p.ntok - t0;
-    if (tcount > p.kchunk) tcount = p.kchunk;
-    num_kb = tcount > 0 ? (int)((tcount + BK - 1) / BK) : 0;
-    a_c0 = blk * p.b + mt * BM; a_c1 = (int)t0;
-    b_c0 = blk * p.b + nt * BN; b_c1 = (int)t0;
-  }
 
   if (warp == 0 && lane == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    mbar_init(accum, 1);
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 4);
+    }
     *abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
@@ -148,112 +172,138 @@ __global__ void __launch_bounds__(192, 1)
 
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------ TMA producer
-    int issued = 0;
-    for (int kb = 0; kb < num_kb; ++kb) {
-      const int s = kb % STAGES;
-      const uint32_t ph = (kb / STAGES) & 1;
-      if (*abort_flag || !mbar_wait_bounded(&empty[s], ph ^ 1, p.err, p.limit_ns)) {
-        *abort_flag = 1;
-        break;
-      }
-      mbar_arrive_expect_tx(&full[s], STAGE_BYTES);
-      uint8_t* sa = smem + s * STAGE_BYTES;
-      uint8_t* sb = sa + A_BYTES;
-      const int k = kb * BK;
-      if (!A_MN) {
-        tma_load_2d(sa, &tmA, &full[s], a_c0 + k, a_c1);
-      } else {
+    long long g = 0;  // k blocks issued by this CTA (ring position)
+    bool ok = true;
+    for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+      const TileCoords c = tile_coords<BN, B_MN>(p, t);
+      for (int kb = 0; kb < c.num_kb; ++kb, ++g) {
+        const int s = (int)(g % STAGES);
+        const uint32_t ph = (uint32_t)((g / STAGES) & 1);
+        if (*abort_flag || !mbar_wait_bounded(&empty[s], ph ^ 1, p.err, p.limit_ns)) {
+          *abort_flag = 1;
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&full[s], STAGE_BYTES);
+        uint8_t* sa = smem + s * STAGE_BYTES;
+        uint8_t* sb = sa + A_BYTES;
+        const int k = kb * BK;
+        if (!A_MN) {
+          tma_load_2d(sa, &tmA, &full[s], c.a_c0 + k, c.a_c1);
+        } else {
 #pragma unroll
-        for (int i = 0; i < BM / 64; ++i) tma_load_2d(sa + i * 8192, &tmA, &full[s], a_c0 + 64 * i, a_c1 + k);
-      }
-      if (!B_MN) {
-        tma_load_2d(sb, &tmB, &full[s], b_c0 + k, b_c1);
-      } else {
+          for (int i = 0; i < BM / 64; ++i)
+            tma_load_2d(sa + i * 8192, &tmA, &full[s], c.a_c0 + 64 * i, c.a_c1 + k);
+        }
+        if (!B_MN) {
+          tma_load_2d(sb, &tmB, &full[s], c.b_c0 + k, c.b_c1);
+        } else {
 #pragma unroll
-        for (int i = 0; i < BN / 64; ++i) tma_load_2d(sb + i * 8192, &tmB, &full[s], b_c0 + 64 * i, b_c1 + k);
+          for (int i = 0; i < BN / 64; ++i)
+            tma_load_2d(sb + i * 8192, &tmB, &full[s], c.b_c0 + 64 * i, c.b_c1 + k);
+        }
       }
-      ++issued;
     }
     // Drain: wait for the last load issued into every stage (already complete in the normal
     // path), so that no copy is in flight when the CTA exits.
-    for (int kb = issued - 1; kb >= 0 && kb >= issued - STAGES; --kb)
-      mbar_wait_bounded(&full[kb % STAGES], (kb / STAGES) & 1, p.err, p.limit_ns);
+    for (long long j = g - 1; j >= 0 && j >= g - STAGES; --j)
+      mbar_wait_bounded(&full[j % STAGES], (uint32_t)((j / STAGES) & 1), p.err, p.limit_ns);
   } else if (warp == 1 && lane == 0) {
     // ------------------------------------------------------------ MMA issuer
-    bool committed = false;
-    for (int kb = 0; kb < num_kb; ++kb) {
-      const int s = kb % STAGES;
-      const uint32_t ph = (kb / STAGES) & 1;
-      if (*abort_flag || !mbar_wait_bounded(&full[s], ph, p.err, p.limit_ns)) {
+    long long g = 0;
+    int it = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x, ++it) {
+      const TileCoords c = tile_coords<BN, B_MN>(p, t);
+      const int a = it & 1;
+      if (*abort_flag || !mbar_wait_bounded(&tempty[a], ((it >> 1) & 1) ^ 1, p.err, p.limit_ns)) {
         *abort_flag = 1;
         break;
       }
       tc_fence_after();
-      const uint32_t a_base = smem_base + s * STAGE_BYTES;
-      const uint32_t b_base = a_base + A_BYTES;
+      const uint32_t d = tmem_base + (uint32_t)(a * BN);
+      for (int kb = 0; kb < c.num_kb; ++kb, ++g) {
+        const int s = (int)(g % STAGES);
+        const uint32_t ph = (uint32_t)((g / STAGES) & 1);
+        if (*abort_flag || !mbar_wait_bounded(&full[s], ph, p.err, p.limit_ns)) {
+          *abort_flag = 1;
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t a_base = smem_base + s * STAGE_BYTES;
+        const uint32_t b_base = a_base + A_BYTES;
 #pragma unroll
-      for (int k = 0; k < BK / 16; ++k)
-        umma_bf16(tmem_base, tile_desc<A_MN>(a_base, k), tile_desc<B_MN>(b_base, k), IDESC,
-                  (kb | k) != 0);
-      umma_commit(&empty[s]);
+        for (int k = 0; k < BK / 16; ++k)
+          umma_bf16(d, tile_desc<A_MN>(a_base, k), tile_desc<B_MN>(b_base, k), IDESC,
+                    (kb | k) != 0);
+        umma_commit(&empty[s]);
+      }
+      umma_commit(&tfull[a]);  // also when the tile had no K block (empty token split)
     }
-    if (num_kb > 0) {
-      umma_commit(accum);
-      committed = true;
+    // TMEM is freed after the final barrier: wait until the last MMAs have completed.
+    if (it > 0) {
+      const int last = it - 1;
+      mbar_wait_bounded(&tfull[last & 1], (last >> 1) & 1, p.err, p.limit_ns);
     }
-    // TMEM is freed after the final barrier: make sure every MMA has completed first.
-    if (committed) mbar_wait_bounded(accum, 0, p.err, p.limit_ns);
   } else if (warp >= 2) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;
     const int row = q * 32 + lane;
-    const long long grow = out_row0 + row;
-    bool have = num_kb > 0;
-    if (have) {
-      const bool ok = mbar_wait_bounded(accum, 0, p.err, p.limit_ns);
-      if (!ok) *abort_flag = 1;
-      have = __all_sync(0xffffffffu, ok);  // tcgen05.ld below must be warp-uniform
+    int it = 0;
+    for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++it) {
+      const TileCoords c = tile_coords<BN, B_MN>(p, t);
+      const int a = it & 1;
+      const bool ok = !*abort_flag && mbar_wait_bounded(&tfull[a], (it >> 1) & 1, p.err, p.limit_ns);
+      if (!__all_sync(0xffffffffu, ok)) {
+        *abort_flag = 1;
+        break;
+      }
       tc_fence_after();
-    }
-    const bool valid = grow < p.M;
+      const long long grow = c.out_row0 + row;
+      const bool valid = grow < p.M;
 #pragma unroll 1
-    for (int c0 = 0; c0 < BN; c0 += 32) {
-      uint32_t r[32];
-      if (have) {
-        tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)c0, r);
-        tmem_ld_wait();
-      } else {
+      for (int c0 = 0; c0 < BN; c0 += 32) {
+        uint32_t r[32];
+        if (c.num_kb > 0) {
+          tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(a * BN + c0), r);
+          tmem_ld_wait();
+        } else {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) r[i] = 0u;
-      }
-      if (!valid) continue;
-      if (OUT_F32) {
-        float* dst = static_cast<float*>(p.C) +
-                     (((long long)split * p.nblk + blk) * p.b + grow) * p.b + out_col0 + c0;
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-          reinterpret_cast<float4*>(dst)[i] =
-              make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
-                          __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
-      } else {
-        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.C) + grow * p.ldc + out_col0 + c0;
-        float v[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-        if (p.colscale) {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] *= __ldg(p.colscale + out_col0 + c0 + i);
+          for (int i = 0; i < 32; ++i) r[i] = 0u;
         }
+        if (!valid) continue;
+        if (OUT_F32) {
+          float* dst = static_cast<float*>(p.C) +
+                       (((long long)c.split * p.nblk + c.blk) * p.b + grow) * p.b + c.out_col0 + c0;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          uint4 w;
-          w.x = pack_bf16x2(v[8 * i + 0], v[8 * i + 1]);
-          w.y = pack_bf16x2(v[8 * i + 2], v[8 * i + 3]);
-          w.z = pack_bf16x2(v[8 * i + 4], v[8 * i + 5]);
-          w.w = pack_bf16x2(v[8 * i + 6], v[8 * i + 7]);
-          reinterpret_cast<uint4*>(dst)[i] = w;
+          for (int i = 0; i < 8; ++i)
+            reinterpret_cast<float4*>(dst)[i] =
+                make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
+                            __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
+        } else {
+          __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.C) + grow * p.ldc + c.out_col0 + c0;
+          float v[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+          if (p.colscale) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] *= __ldg(p.colscale + c.out_col0 + c0 + i);
+          }
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            uint4 w;
+            w.x = pack_bf16x2(v[8 * i + 0], v[8 * i + 1]);
+            w.y = pack_bf16x2(v[8 * i + 2], v[8 * i + 3]);
+            w.z = pack_bf16x2(v[8 * i + 4], v[8 * i + 5]);
+            w.w = pack_bf16x2(v[8 * i + 6], v[8 * i + 7]);
+            reinterpret_cast<uint4*>(dst)[i] = w;
+          }
         }
       }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[a]);
     }
   }
   tc_fence_before();
@@ -301,18 +351,31 @@ bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, u
 }
 
 template <int BN, int STAGES, bool A_MN, bool B_MN, bool OUT_F32>
-poetx_status launch(const CUtensorMap& ta, const CUtensorMap& tb, const UmmaParams& p, dim3 grid,
-                    cudaStream_t s) {
+poetx_status launch(const CUtensorMap& ta, const CUtensorMap& tb, UmmaParams p, int tiles_m,
+                    int tiles_n, int tiles_z, cudaStream_t s) {
   const int stage = p.mode == MODE_PLAIN ? ST_WPRIME : (p.mode == MODE_BLOCKDIAG ? ST_BLOCKDIAG : ST_WGRAD);
   auto k = umma_gemm_kernel<BN, STAGES, A_MN, B_MN, OUT_F32>;
   constexpr int smem = STAGES * (BM * BK * 2 + BN * BK * 2) + 1024 + 256;
+  // TMEM holds 512 columns per SM: 2 x BN columns per CTA bound the CTAs per SM, and the
+  // shared memory of every configuration is sized so that no more than that many fit.
+  constexpr int per_sm = 512 / (2 * BN) < 2 ? 512 / (2 * BN) : 2;
+  static_assert(per_sm >= 1, "accumulators exceed TMEM");
+  static_assert((size_t)smem * (per_sm + 1) > 228 * 1024 || per_sm == 2,
+                "shared memory must keep the CTAs per SM within TMEM");
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [&] {
     attr_err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   });
   POETX_CUDA_TRY(attr_err);
-  if (grid.x == 0 || grid.y == 0 || grid.z == 0) return POETX_OK;
+  const long long tiles = (long long)tiles_m * tiles_n * tiles_z;
+  if (tiles == 0) return POETX_OK;
+  if (tiles > 0x7fffffffLL) return POETX_ERR_SHAPE;
+  p.tiles_m = tiles_m;
+  p.tiles_n = tiles_n;
+  p.num_tiles = (int)tiles;
+  const long long want = (long long)sm_count() * per_sm;
+  const int grid = (int)(tiles < want ? tiles : want);
   k<<<grid, 192, smem, s>>>(ta, tb, p);
   POETX_CUDA_TRY(cudaGetLastError());
   after_launch(s, stage);
@@ -356,15 +419,15 @@ poetx_status umma_blockdiag(const void* X, long long N, int nblk, int b, const v
   p.C = Y;
   p.ldc = D;
   p.colscale = col_scale;
-  dim3 grid((unsigned)((N + BM - 1) / BM), b / BN, nblk);
+  const int tm = (int)((N + BM - 1) / BM), tn = b / BN;
   if (trans) {
-    if (BN == 64) return launch<64, 4, false, false, false>(ta, tb, p, grid, s);
-    if (BN == 128) return launch<128, 3, false, false, false>(ta, tb, p, grid, s);
-    return launch<256, 2, false, false, false>(ta, tb, p, grid, s);
+    if (BN == 64) return launch<64, 4, false, false, false>(ta, tb, p, tm, tn, nblk, s);
+    if (BN == 128) return launch<128, 3, false, false, false>(ta, tb, p, tm, tn, nblk, s);
+    return launch<256, 4, false, false, false>(ta, tb, p, tm, tn, nblk, s);
   }
-  if (BN == 64) return launch<64, 4, false, true, false>(ta, tb, p, grid, s);
-  if (BN == 128) return launch<128, 3, false, true, false>(ta, tb, p, grid, s);
-  return launch<256, 2, false, true, false>(ta, tb, p, grid, s);
+  if (BN == 64) return launch<64, 4, false, true, false>(ta, tb, p, tm, tn, nblk, s);
+  if (BN == 128) return launch<128, 3, false, true, false>(ta, tb, p, tm, tn, nblk, s);
+  return launch<256, 4, false, true, false>(ta, tb, p, tm, tn, nblk, s);
 }
 
 poetx_status umma_wprime(const void* A, long long N, int m, int n, const void* W,
@@ -381,16 +444,14 @@ poetx_status umma_wprime(const void* A, long long N, int m, int n, const void* W
     if (!make_map(&tb, W, m, n, m, 64, 256)) return POETX_ERR_CUDA;
     p.num_kb = m / 64;
     p.ldc = n;
-    dim3 grid((unsigned)((N + BM - 1) / BM), n / 256, 1);
-    return launch<256, 4, false, false, false>(ta, tb, p, grid, s);
+    return launch<256, 4, false, false, false>(ta, tb, p, (int)((N + BM - 1) / BM), n / 256, 1, s);
   }
   // C[N,m] = A[N,n] W: B operand (output col c, K index r) = W[r][c], MN-major
   if (!make_map(&ta, A, n, N, n, 64, 128)) return POETX_ERR_CUDA;
   if (!make_map(&tb, W, m, n, m, 64, 64)) return POETX_ERR_CUDA;
   p.num_kb = n / 64;
   p.ldc = m;
-  dim3 grid((unsigned)((N + BM - 1) / BM), m / 256, 1);
-  return launch<256, 4, false, true, false>(ta, tb, p, grid, s);
+  return launch<256, 4, false, true, false>(ta, tb, p, (int)((N + BM - 1) / BM), m / 256, 1, s);
 }
 
 poetx_status umma_wgrad(const void* X, const void* dY, long long N, int nblk, int b, int splits,
@@ -415,10 +476,10 @@ poetx_status umma_wgrad(const void* X, const void* dY, long long N, int nblk, in
   if (p.kchunk < 64) p.kchunk = 64;
   p.ntok = N;
   p.C = dG;
-  dim3 grid((b + BM - 1) / BM, b / BN, nblk * splits);
-  if (BN == 64) return launch<64, 4, true, true, true>(ta, tb, p, grid, s);
-  if (BN == 128) return launch<128, 3, true, true, true>(ta, tb, p, grid, s);
-  return launch<256, 2, true, true, true>(ta, tb, p, grid, s);
+  const int tm = (b + BM - 1) / BM, tn = b / BN;
+  if (BN == 64) return launch<64, 4, true, true, true>(ta, tb, p, tm, tn, nblk * splits, s);
+  if (BN == 128) return launch<128, 3, true, true, true>(ta, tb, p, tm, tn, nblk * splits, s);
+  return launch<256, 4, true, true, true>(ta, tb, p, tm, tn, nblk * splits, s);
 }
 
 }  // namespace poetx
