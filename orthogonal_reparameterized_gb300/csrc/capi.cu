@@ -12,31 +12,40 @@ namespace poetx {
 static __device__ int g_error_word;
 
 static std::mutex g_mu;
-static int* g_err_ptr[64];
-static int g_sms[64];
+static std::atomic<int*> g_err_ptr[64];
+static std::atomic<int> g_sms[64];
+
+static int current_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -1;
+  return dev;
+}
 
 int* device_error_word() {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  const int dev = current_device();
+  if (dev < 0) return nullptr;
+  int* p = g_err_ptr[dev].load(std::memory_order_acquire);
+  if (p) return p;
   std::lock_guard<std::mutex> lk(g_mu);
-  if (!g_err_ptr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return nullptr;
-    g_err_ptr[dev] = static_cast<int*>(p);
+  p = g_err_ptr[dev].load(std::memory_order_acquire);
+  if (!p) {
+    void* v = nullptr;
+    if (cudaGetSymbolAddress(&v, g_error_word) != cudaSuccess) return nullptr;
+    p = static_cast<int*>(v);
+    g_err_ptr[dev].store(p, std::memory_order_release);
   }
-  return g_err_ptr[dev];
+  return p;
 }
 
 int sm_count() {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
-  std::lock_guard<std::mutex> lk(g_mu);
-  if (!g_sms[dev]) {
-    int v = 0;
-    cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
-    g_sms[dev] = v > 0 ? v : 148;
-  }
-  return g_sms[dev];
+  const int dev = current_device();
+  if (dev < 0) return 148;
+  int v = g_sms[dev].load(std::memory_order_relaxed);
+  if (v) return v;
+  cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+  if (v <= 0) v = 148;
+  g_sms[dev].store(v, std::memory_order_relaxed);
+  return v;
 }
 
 static std::atomic<unsigned long long> g_launches{0};

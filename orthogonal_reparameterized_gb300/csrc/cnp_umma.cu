@@ -389,17 +389,40 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// [nblk*b rows][b cols] fp32 view with 32 x 32 boxes, 128-byte swizzle.
+// [nblk*b rows][b cols] fp32 view with 32 x 32 boxes, 128-byte swizzle (per-thread cache of
+// encoded maps keyed by pointer and shape).
 bool make_blk_map(CUtensorMap* m, const float* ptr, int nblk, int b) {
+  struct Entry {
+    const float* ptr;
+    int nblk, b, dev;
+    CUtensorMap map;
+  };
+  constexpr int kEntries = 32;
+  thread_local Entry cache[kEntries];
+  thread_local int next = 0;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  for (int i = 0; i < kEntries; ++i) {
+    const Entry& e = cache[i];
+    if (e.ptr == ptr && ptr && e.nblk == nblk && e.b == b && e.dev == dev) {
+      *m = e.map;
+      return true;
+    }
+  }
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {(cuuint64_t)b, (cuuint64_t)nblk * b};
   cuuint64_t strides[1] = {(cuuint64_t)b * 4};
   cuuint32_t box[2] = {32, 32};
   cuuint32_t es[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(ptr), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  if (fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(ptr), dims, strides, box, es,
+         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  Entry& e = cache[next];
+  next = (next + 1) % kEntries;
+  e.ptr = ptr; e.nblk = nblk; e.b = b; e.dev = dev; e.map = *m;
+  return true;
 }
 
 template <int BN, int STAGES>

@@ -6,6 +6,8 @@
 // POET-X summary page ("POET-X: Memory-efficient LLM Training by Scaling Orthogonal
 // Transformation"), "Core method" section 2 (permutations as index remaps; merge of the
 // two permutations into W once per inner loop) and section 4 (upper-triangle storage).
+#include <mutex>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -242,7 +244,12 @@ static poetx_status launch_perm_rows_t(const void* X, long long N, int D, const 
   const size_t smem = idx_bytes + nbuf * row_bytes + 8 * (size_t)nbuf;
   if (smem > 227 * 1024) return POETX_ERR_SHAPE;
   auto k = perm_rows_kernel<E, SCATTER, IdxT>;
-  POETX_CUDA_TRY(cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+  static std::once_flag once;  // the opt-in limit is set once, to the largest size used
+  static cudaError_t attr = cudaSuccess;
+  std::call_once(once, [&] {
+    attr = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+  });
+  POETX_CUDA_TRY(attr);
   // two CTAs per SM at most: each stages the whole index once, so it should own many rows
   int per_sm = (int)((220 * 1024) / (smem + 1024));
   per_sm = per_sm < 1 ? 1 : (per_sm > 2 ? 2 : per_sm);

@@ -18,6 +18,7 @@
 // of a weight gradient); both use the canonical 128-byte swizzle layouts of tcgen05.
 // Every mbarrier wait is bounded; on expiry the kernel records POETX_ERR_TIMEOUT, drains
 // its own copies, frees its TMEM and returns.
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
@@ -336,18 +337,45 @@ EncodeTiledFn encode_fn() {
 }
 
 // 2-D bf16 tensor [outer][inner] with row pitch `pitch_elems`, box {box_inner, box_outer},
-// 128-byte swizzle, zero fill out of bounds.
+// 128-byte swizzle, zero fill out of bounds.  Encoded maps are kept in a small per-thread
+// cache keyed by every argument, since training loops pass the same buffers every step.
 bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint64_t pitch_elems,
               uint32_t box_inner, uint32_t box_outer) {
+  struct Entry {
+    const void* ptr;
+    uint64_t inner, outer, pitch;
+    uint32_t bi, bo;
+    int dev;
+    CUtensorMap map;
+  };
+  constexpr int kEntries = 64;
+  thread_local Entry cache[kEntries];
+  thread_local int next = 0;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  for (int i = 0; i < kEntries; ++i) {
+    const Entry& e = cache[i];
+    if (e.ptr == ptr && ptr && e.inner == inner && e.outer == outer && e.pitch == pitch_elems &&
+        e.bi == box_inner && e.bo == box_outer && e.dev == dev) {
+      *m = e.map;
+      return true;
+    }
+  }
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {inner, outer};
   cuuint64_t strides[1] = {pitch_elems * 2};
   cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t es[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  if (fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
+         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  Entry& e = cache[next];
+  next = (next + 1) % kEntries;
+  e.ptr = ptr; e.inner = inner; e.outer = outer; e.pitch = pitch_elems;
+  e.bi = box_inner; e.bo = box_outer; e.dev = dev; e.map = *m;
+  return true;
 }
 
 template <int BN, int STAGES, bool A_MN, bool B_MN, bool OUT_F32>
@@ -392,11 +420,19 @@ UmmaParams base_params() {
 }  // namespace
 
 bool umma_supported() {
-  int dev = 0, major = 0, minor = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return false;
-  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
-  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
-  return major == 10 && minor == 3 && encode_fn() != nullptr;
+  // sm_103 and a driver entry point for tensor maps; cached per device
+  static std::atomic<int> cached[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+  int v = cached[dev].load(std::memory_order_relaxed);
+  if (!v) {
+    int major = 0, minor = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    v = (major == 10 && minor == 3 && encode_fn() != nullptr) ? 1 : 2;
+    cached[dev].store(v, std::memory_order_relaxed);
+  }
+  return v == 1;
 }
 
 poetx_status umma_blockdiag(const void* X, long long N, int nblk, int b, const void* G, int trans,
