@@ -182,14 +182,17 @@ poetx_status poetx_quantize_rows_int8(const float* W, int n, int m, int8_t* Wq, 
  * ------------------------------------------------------------------------------------- */
 
 /* Y[:, jb:(j+1)b] = X[:, jb:(j+1)b] . op(G_j) for j < nblk, op = identity (trans == 0) or
- * transpose (trans != 0); optional column scale: Y[:, c] *= col_scale[c] (nullable).
+ * transpose (trans != 0); optional column scale: column c is multiplied by col_scale[c]
+ * (nullable); optional output permutation: column c of the product is stored at column
+ * out_perm[c] of Y (nullable; the output remap of the POET-X summary page, "Core method"
+ * section 2, fused into the product; Y must not alias X then).
  *   dt      POETX_BF16 (X, G, Y bf16; fp32 accumulation; Y rounded to nearest even)
  *           or POETX_F32 (all fp32)
  *   X, Y    [N, nblk*b];  G [nblk, b, b] row-major
  * bf16 requires b in {64, 128, 256, 512}. */
 poetx_status poetx_blockdiag_mm(poetx_dtype dt, const void* X, int N, int nblk, int b,
-                                const void* G, int trans, const float* col_scale, void* Y,
-                                cudaStream_t stream);
+                                const void* G, int trans, const float* col_scale,
+                                const int32_t* out_perm, void* Y, cudaStream_t stream);
 
 /* Weight gradient of Y = X . blkdiag(G): dG[s, j] = X_j^T dY_j summed over the tokens of
  * split s.  Tokens are cut into `splits` contiguous ranges of chunk = 64*ceil(N/(64*splits))

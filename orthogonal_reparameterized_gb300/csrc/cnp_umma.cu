@@ -117,9 +117,16 @@ __device__ __forceinline__ void combine_split(float4* x, float4* y, float c0, fl
   *y = make_float4(lo[0], lo[1], lo[2], lo[3]);
 }
 
+// Converter / promotion warps: 4 * BN / 32, two per TMEM lane quarter for BN = 64, each
+// owning 32 accumulator columns.
+template <int BN>
+constexpr int conv_warps() { return BN / 8; }
+
 template <int BN, int STAGES>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(64 + 32 * conv_warps<BN>(), 2)
     cnp_umma_kernel(const __grid_constant__ CnpMaps maps, const CnpUParams p) {
+  constexpr int NCW = conv_warps<BN>();
+  constexpr int NCT = 32 * NCW;  // converter threads
   constexpr uint32_t A_BYTES = BM * BK * 4;   // 16 KB per buffer
   constexpr uint32_t B_BYTES = BN * BK * 4;   // BN * 128 bytes per buffer
   constexpr uint32_t STAGE_BYTES = 2 * A_BYTES + 2 * B_BYTES;
@@ -146,12 +153,12 @@ __global__ void __launch_bounds__(192, 1)
   if (warp == 0 && lane == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&conv[s], 4);
+      mbar_init(&conv[s], NCW);
       mbar_init(&empty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], 4);
+      mbar_init(&tempty[a], NCW);
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -241,13 +248,14 @@ __global__ void __launch_bounds__(192, 1)
     if (done > 0) mbar_wait_bounded(&tfull[(done - 1) & 1], ((done - 1) >> 1) & 1, p.err, p.limit_ns);
   } else if (warp >= 2) {
     // ---------------------------------------------------------------- converter + promotion
-    const int ct = threadIdx.x - 64;  // 0..127
+    const int ct = threadIdx.x - 64;  // 0..NCT-1
     const int q = warp & 3;           // TMEM lane quarter of this warp
+    const int h = (warp - 2) >> 2;    // which 32 accumulator columns this warp owns
     const int r = q * 32 + lane;
     const int i = mt * BM + r;
-    float acc[BN];
+    float acc[32];
 #pragma unroll
-    for (int t = 0; t < BN; ++t) acc[t] = 0.f;
+    for (int t = 0; t < 32; ++t) acc[t] = 0.f;
     bool ok_all = true;
     // Adds the accumulator of K block kk to the registers and hands the accumulator back.
     auto promote = [&](int kk) {
@@ -259,13 +267,12 @@ __global__ void __launch_bounds__(192, 1)
         return;
       }
       tc_fence_after();
-#pragma unroll
-      for (int c0 = 0; c0 < BN; c0 += 32) {
+      {
         uint32_t v[32];
-        tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(a * BN + c0), v);
+        tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(a * BN + h * 32), v);
         tmem_ld_wait();
 #pragma unroll
-        for (int t = 0; t < 32; ++t) acc[c0 + t] += __uint_as_float(v[t]);
+        for (int t = 0; t < 32; ++t) acc[t] += __uint_as_float(v[t]);
       }
       tc_fence_before();
       __syncwarp();
@@ -288,13 +295,13 @@ __global__ void __launch_bounds__(192, 1)
       float4* a1 = reinterpret_cast<float4*>(st + A_BYTES);
       const bool a_two = A.s[1].map >= 0;
 #pragma unroll 4
-      for (int e = ct; e < (int)(A_BYTES / 16); e += 128)
+      for (int e = ct; e < (int)(A_BYTES / 16); e += NCT)
         combine_split(a0 + e, a1 + e, A.s[0].coef, A.s[1].coef, a_two);
       float4* b0 = reinterpret_cast<float4*>(st + 2 * A_BYTES);
       float4* b1 = reinterpret_cast<float4*>(st + 2 * A_BYTES + B_BYTES);
       const bool b_two = B.s[1].map >= 0;
 #pragma unroll 4
-      for (int e = ct; e < (int)(B_BYTES / 16); e += 128)
+      for (int e = ct; e < (int)(B_BYTES / 16); e += NCT)
         combine_split(b0 + e, b1 + e, B.s[0].coef, B.s[1].coef, b_two);
       fence_async_smem();  // generic-proxy writes -> visible to the tensor cores
       __syncwarp();
@@ -305,13 +312,12 @@ __global__ void __launch_bounds__(192, 1)
     // ---------------------------------------------------------------- epilogue
     const long long base = (long long)blk * b * b;
     if (i < b) {
-#pragma unroll
-      for (int c0 = 0; c0 < BN; c0 += 32) {
-        const int j0 = nt * BN + c0;
+      {
+        const int j0 = nt * BN + h * 32;
         const long long idx0 = base + (long long)i * b + j0;
         float o[32];
 #pragma unroll
-        for (int t = 0; t < 32; ++t) o[t] = acc[c0 + t];
+        for (int t = 0; t < 32; ++t) o[t] = acc[t];
         if (p.E1) {
           const float4* e = reinterpret_cast<const float4*>(p.E1 + idx0);
 #pragma unroll
@@ -436,7 +442,7 @@ poetx_status launch_t(const CnpMaps& maps, const CnpUParams& p, int nblk, cudaSt
   });
   POETX_CUDA_TRY(attr);
   dim3 grid((p.b + BM - 1) / BM, p.b / BN, nblk);
-  k<<<grid, 192, smem, s>>>(maps, p);
+  k<<<grid, 64 + 32 * conv_warps<BN>(), smem, s>>>(maps, p);
   POETX_CUDA_TRY(cudaGetLastError());
   return POETX_OK;
 }

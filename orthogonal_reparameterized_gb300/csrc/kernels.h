@@ -39,6 +39,7 @@ struct SimtGemm {
   long long scm, scn, scb;
   const float* colscale;  // nullable, indexed by j + z*colscale_bstride
   long long colscale_bstride;
+  const int32_t* colperm;  // nullable: column j of batch z is stored at colperm[j + z*bstride]
   int ksplit;
   int kchunk;
   long long scs;
@@ -75,9 +76,11 @@ bool use_tensor_cores();
 
 // ---- umma_gemm.cu: tcgen05 / TMA tensor-core GEMMs (bf16 in, fp32 accumulate)
 bool umma_supported();
-// Y = X . op(G) per block (bf16), op = identity (trans=0) or transpose; optional col scale.
+// Y = X . op(G) per block (bf16), op = identity (trans=0) or transpose; optional column
+// scale; optional output permutation (column c of the product is stored at out_perm[c]).
 poetx_status umma_blockdiag(const void* X, long long N, int nblk, int b, const void* G, int trans,
-                            const float* col_scale, void* Y, cudaStream_t s);
+                            const float* col_scale, const int32_t* out_perm, void* Y,
+                            cudaStream_t s);
 // C[N,n] = A[N,m] W^T (trans=0) or C[N,m] = A[N,n] W (trans=1), W [n,m] bf16.
 poetx_status umma_wprime(const void* A, long long N, int m, int n, const void* W,
                          const float* w_scale, int trans, void* C, cudaStream_t s);

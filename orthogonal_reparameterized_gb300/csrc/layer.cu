@@ -45,11 +45,11 @@ static int wgrad_chunk(long long N, int splits) {
 
 // ---------------------------------------------------------------- step implementations
 poetx_status blockdiag_impl(poetx_dtype dt, const void* X, long long N, int nblk, int b,
-                            const void* G, int trans, const float* col_scale, void* Y,
-                            cudaStream_t s) {
+                            const void* G, int trans, const float* col_scale,
+                            const int32_t* out_perm, void* Y, cudaStream_t s) {
   if (N == 0 || nblk == 0) return POETX_OK;
   if (dt == POETX_BF16 && use_umma() && b % 64 == 0 && b <= 512)
-    return umma_blockdiag(X, N, nblk, b, G, trans, col_scale, Y, s);
+    return umma_blockdiag(X, N, nblk, b, G, trans, col_scale, out_perm, Y, s);
   const long long D = (long long)nblk * b;
   SimtGemm g{};
   g.M = (int)N; g.N = b; g.K = b; g.batch = nblk;
@@ -57,6 +57,7 @@ poetx_status blockdiag_impl(poetx_dtype dt, const void* X, long long N, int nblk
   g.B = G; g.sbk = trans ? 1 : b; g.sbn = trans ? b : 1; g.sbb = (long long)b * b;
   g.C = Y; g.scm = D; g.scn = 1; g.scb = b;
   g.colscale = col_scale; g.colscale_bstride = b;
+  g.colperm = out_perm;
   g.ksplit = 1; g.kchunk = b;
   g.stage = ST_BLOCKDIAG;
   return launch_simt_gemm(dt, dt, dt, g, s);
@@ -115,9 +116,9 @@ struct Plan {
   // saved
   size_t GR, GP, Q2R, Q2P, Qs, Bsv, saved_total;
   // forward workspace
-  size_t f_xt, f_A, f_B, f_zt, fwd_total;
+  size_t f_xt, f_A, f_B, fwd_total;
   // backward workspace
-  size_t b_cnp, b_xt, b_dzt, b_A, b_B, b_dB, b_dA, b_dxt, b_dGP, b_dGR, bwd_total;
+  size_t b_cnp, b_xt, b_dzt, b_A, b_B, b_dB, b_dA, b_dGP, b_dGR, bwd_total;
   int splitsR, splitsP;
 };
 
@@ -163,7 +164,6 @@ static Plan make_plan(const poetx_layer* L, long long N) {
   p.f_xt = take((size_t)N * m * as);
   p.f_A = take((size_t)N * m * as);
   p.f_B = L->variant == POETX_MEM ? take((size_t)N * n * as) : 0;
-  p.f_zt = take((size_t)N * n * as);
   p.fwd_total = o;
 
   p.splitsR = wgrad_splits(N, L->m / L->b, L->b);
@@ -176,7 +176,6 @@ static Plan make_plan(const poetx_layer* L, long long N) {
   p.b_B = L->variant == POETX_MEM ? take((size_t)N * n * as) : 0;
   p.b_dB = take((size_t)N * n * as);
   p.b_dA = take((size_t)N * m * as);
-  p.b_dxt = take((size_t)N * m * as);
   p.b_dGP = take((size_t)p.splitsP * n * b * 4);
   p.b_dGR = take((size_t)p.splitsR * m * b * 4);
   p.bwd_total = o;
@@ -238,12 +237,11 @@ extern "C" poetx_status poetx_layer_fwd(const poetx_layer* L, const void* x, int
   void* xt = at(ws, p.f_xt);
   void* A = at(ws, p.f_A);
   void* B = L->variant == POETX_FAST ? at(saved, p.Bsv) : at(ws, p.f_B);
-  void* zt = at(ws, p.f_zt);
   POETX_TRY(launch_perm_rows(as, false, x, N, m, L->perm_m, xt, nullptr, nullptr, nullptr, stream));
-  POETX_TRY(blockdiag_impl(act, xt, N, m / b, b, at(saved, p.GR), 0, nullptr, A, stream));
+  POETX_TRY(blockdiag_impl(act, xt, N, m / b, b, at(saved, p.GR), 0, nullptr, nullptr, A, stream));
   POETX_TRY(wprime_impl(act, L->wdt, A, N, m, n, L->Wp, L->w_scale, 0, B, stream));
-  POETX_TRY(blockdiag_impl(act, B, N, n / b, b, at(saved, p.GP), 0, nullptr, zt, stream));
-  return launch_perm_rows(as, true, zt, N, n, L->perm_n, y, nullptr, nullptr, nullptr, stream);
+  // S6 + S7: z~ = B blkdiag(G_P), stored straight into y through the permutation
+  return blockdiag_impl(act, B, N, n / b, b, at(saved, p.GP), 0, nullptr, L->perm_n, y, stream);
 }
 
 extern "C" poetx_status poetx_layer_bwd(const poetx_layer* L, const void* x, const void* dy, int N,
@@ -266,7 +264,6 @@ extern "C" poetx_status poetx_layer_bwd(const poetx_layer* L, const void* x, con
   void* dzt = at(ws, p.b_dzt);
   void* dB = at(ws, p.b_dB);
   void* dA = at(ws, p.b_dA);
-  void* dxt = at(ws, p.b_dxt);
   float* dGP = at<float>(ws, p.b_dGP);
   float* dGR = at<float>(ws, p.b_dGR);
   const void* GR = at(saved, p.GR);
@@ -279,7 +276,7 @@ extern "C" poetx_status poetx_layer_bwd(const poetx_layer* L, const void* x, con
   if (L->variant == POETX_MEM) {  // recompute B = (x~ blkdiag(G_R)) W'^T
     void* A = at(ws, p.b_A);
     void* Bw = at(ws, p.b_B);
-    POETX_TRY(blockdiag_impl(act, xt, N, m / b, b, GR, 0, nullptr, A, stream));
+    POETX_TRY(blockdiag_impl(act, xt, N, m / b, b, GR, 0, nullptr, nullptr, A, stream));
     POETX_TRY(wprime_impl(act, L->wdt, A, N, m, n, L->Wp, L->w_scale, 0, Bw, stream));
     B = Bw;
   } else {
@@ -288,12 +285,11 @@ extern "C" poetx_status poetx_layer_bwd(const poetx_layer* L, const void* x, con
   POETX_TRY(wgrad_impl(act, B, dzt, N, n / b, b, p.splitsP, dGP, stream));
   // int8 weight: dA = dB diag(s) W_q, the row scale is folded into dB's columns
   POETX_TRY(blockdiag_impl(act, dzt, N, n / b, b, GP, 1,
-                           L->wdt == POETX_I8 ? L->w_scale : nullptr, dB, stream));
+                           L->wdt == POETX_I8 ? L->w_scale : nullptr, nullptr, dB, stream));
   POETX_TRY(wprime_impl(act, L->wdt, dB, N, m, n, L->Wp, L->w_scale, 1, dA, stream));
   POETX_TRY(wgrad_impl(act, xt, dA, N, m / b, b, p.splitsR, dGR, stream));
-  POETX_TRY(blockdiag_impl(act, dA, N, m / b, b, GR, 1, nullptr, dxt, stream));
-  if (N > 0)
-    POETX_TRY(launch_perm_rows(as, true, dxt, N, m, L->perm_m, dx, nullptr, nullptr, nullptr, stream));
+  // S12 + S13: dx~ = dA blkdiag(G_R)^T, stored straight into dx through the permutation
+  POETX_TRY(blockdiag_impl(act, dA, N, m / b, b, GR, 1, nullptr, L->perm_m, dx, stream));
   const CnpSides sides{{L->q_R, L->q_P}, {m / b, n / b}};
   const float* const dGs[2] = {dGR, dGP};
   const int splits[2] = {p.splitsR, p.splitsP};
@@ -311,13 +307,14 @@ static poetx_status check_act(poetx_dtype dt, int b) {
 
 extern "C" poetx_status poetx_blockdiag_mm(poetx_dtype dt, const void* X, int N, int nblk, int b,
                                            const void* G, int trans, const float* col_scale,
-                                           void* Y, cudaStream_t stream) {
+                                           const int32_t* out_perm, void* Y, cudaStream_t stream) {
   POETX_TRY(check_act(dt, b));
   if (N < 0 || nblk < 0) return POETX_ERR_ARG;
   if (N == 0 || nblk == 0) return POETX_OK;
   if (!X || !G || !Y) return POETX_ERR_ARG;
   if (!aligned16(X) || !aligned16(G) || !aligned16(Y)) return POETX_ERR_ALIGN;
-  return blockdiag_impl(dt, X, N, nblk, b, G, trans, col_scale, Y, stream);
+  if (out_perm && X == Y) return POETX_ERR_ARG;
+  return blockdiag_impl(dt, X, N, nblk, b, G, trans, col_scale, out_perm, Y, stream);
 }
 
 extern "C" poetx_status poetx_blockdiag_wgrad(poetx_dtype dt, const void* X, const void* dY, int N,

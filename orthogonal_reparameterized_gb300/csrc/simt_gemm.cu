@@ -74,7 +74,13 @@ __global__ void __launch_bounds__(THREADS) simt_gemm_kernel(SimtGemm g) {
       if (gj >= g.N) continue;
       float r = acc[u][v];
       if (g.colscale) r *= g.colscale[gj + (long long)z * g.colscale_bstride];
-      C[(long long)gi * g.scm + (long long)gj * g.scn] = from_f32<TC>(r);
+      if (g.colperm) {  // output permutation: batch offset is part of the permuted index
+        const long long dc = g.colperm[gj + (long long)z * g.colscale_bstride];
+        static_cast<TC*>(g.C)[(long long)split * g.scs + (long long)gi * g.scm + dc * g.scn] =
+            from_f32<TC>(r);
+      } else {
+        C[(long long)gi * g.scm + (long long)gj * g.scn] = from_f32<TC>(r);
+      }
     }
   }
 }

@@ -44,6 +44,7 @@ struct UmmaParams {
   void* C;
   long long ldc;
   const float* colscale;
+  const int32_t* out_perm;  // BLOCKDIAG: output column c is stored at column out_perm[c]
   int* err;
   unsigned long long limit_ns;
 };
@@ -291,14 +292,27 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] *= __ldg(p.colscale + c.out_col0 + c0 + i);
           }
+          if (p.out_perm) {  // fused output permutation: scattered 2-byte stores
+            __nv_bfloat16* rowp = static_cast<__nv_bfloat16*>(p.C) + grow * p.ldc;
+            const int4* pp = reinterpret_cast<const int4*>(p.out_perm + c.out_col0 + c0);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            uint4 w;
-            w.x = pack_bf16x2(v[8 * i + 0], v[8 * i + 1]);
-            w.y = pack_bf16x2(v[8 * i + 2], v[8 * i + 3]);
-            w.z = pack_bf16x2(v[8 * i + 4], v[8 * i + 5]);
-            w.w = pack_bf16x2(v[8 * i + 6], v[8 * i + 7]);
-            reinterpret_cast<uint4*>(dst)[i] = w;
+            for (int i = 0; i < 8; ++i) {
+              const int4 d4 = __ldg(pp + i);
+              rowp[d4.x] = __float2bfloat16_rn(v[4 * i]);
+              rowp[d4.y] = __float2bfloat16_rn(v[4 * i + 1]);
+              rowp[d4.z] = __float2bfloat16_rn(v[4 * i + 2]);
+              rowp[d4.w] = __float2bfloat16_rn(v[4 * i + 3]);
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              uint4 w;
+              w.x = pack_bf16x2(v[8 * i + 0], v[8 * i + 1]);
+              w.y = pack_bf16x2(v[8 * i + 2], v[8 * i + 3]);
+              w.z = pack_bf16x2(v[8 * i + 4], v[8 * i + 5]);
+              w.w = pack_bf16x2(v[8 * i + 6], v[8 * i + 7]);
+              reinterpret_cast<uint4*>(dst)[i] = w;
+            }
           }
         }
       }
@@ -436,7 +450,8 @@ bool umma_supported() {
 }
 
 poetx_status umma_blockdiag(const void* X, long long N, int nblk, int b, const void* G, int trans,
-                            const float* col_scale, void* Y, cudaStream_t s) {
+                            const float* col_scale, const int32_t* out_perm, void* Y,
+                            cudaStream_t s) {
   if (N == 0 || nblk == 0) return POETX_OK;
   const int D = nblk * b;
   const int BN = b < 256 ? b : 256;
@@ -455,6 +470,7 @@ poetx_status umma_blockdiag(const void* X, long long N, int nblk, int b, const v
   p.C = Y;
   p.ldc = D;
   p.colscale = col_scale;
+  p.out_perm = out_perm;
   const int tm = (int)((N + BM - 1) / BM), tn = b / BN;
   if (trans) {
     if (BN == 64) return launch<64, 4, false, false, false>(ta, tb, p, tm, tn, nblk, s);

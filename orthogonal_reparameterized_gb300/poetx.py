@@ -56,7 +56,7 @@ _SIGS = {
     "poetx_perm_scatter": (_i, [_i, _vp, _i, _i, _vp, _vp, _vp]),
     "poetx_merge_perm": (_i, [_vp, _vp, _i, _i, _i, _vp, _vp, _vp, _vp, _vp]),
     "poetx_quantize_rows_int8": (_i, [_vp, _i, _i, _vp, _vp, _vp]),
-    "poetx_blockdiag_mm": (_i, [_i, _vp, _i, _i, _i, _vp, _i, _vp, _vp, _vp]),
+    "poetx_blockdiag_mm": (_i, [_i, _vp, _i, _i, _i, _vp, _i, _vp, _vp, _vp, _vp]),
     "poetx_blockdiag_wgrad": (_i, [_i, _vp, _vp, _i, _i, _i, _i, _vp, _vp]),
     "poetx_wprime_gemm": (_i, [_i, _i, _vp, _i, _i, _i, _vp, _vp, _i, _vp, _vp]),
     "poetx_layer_workspace_bytes": (_sz, [ctypes.POINTER(LayerDesc), _i, _i]),
@@ -218,12 +218,12 @@ def poetx_quantize_rows_int8(W, Wq, scale, stream=None):
 
 
 # ---------------------------------------------------------------- products
-def poetx_blockdiag_mm(X, G, Y, trans=False, col_scale=None, stream=None):
+def poetx_blockdiag_mm(X, G, Y, trans=False, col_scale=None, out_perm=None, stream=None):
     N = X.shape[0]
     nblk, b, _ = G.shape
     _check("poetx_blockdiag_mm", lib().poetx_blockdiag_mm(dtype_code(X), _p(X), N, nblk, b, _p(G),
-                                                          int(bool(trans)), _p(col_scale), _p(Y),
-                                                          _stream(stream)))
+                                                          int(bool(trans)), _p(col_scale),
+                                                          _p(out_perm), _p(Y), _stream(stream)))
 
 
 def poetx_blockdiag_wgrad(X, dY, b, dG, stream=None):

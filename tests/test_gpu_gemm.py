@@ -43,6 +43,25 @@ def test_blockdiag_bf16_colscale(P, engine):
     assert O.rel_fro(host(Y), ref) <= TOL_BF16_STEP
 
 
+@pytest.mark.parametrize("N,nblk,b", [(300, 4, 64), (517, 2, 256), (200, 2, 512)])
+@pytest.mark.parametrize("trans", [False, True])
+def test_blockdiag_bf16_out_perm(P, engine, N, nblk, b, trans):
+    """Product stored through a column permutation: bit-identical to the product followed
+    by the standalone scatter."""
+    X = _rand_bf16((N, nblk * b)).to(DEV)
+    G = _rand_bf16((nblk, b, b), 1 / np.sqrt(b)).to(DEV)
+    perm = torch.tensor(RNG.permutation(nblk * b), dtype=torch.int32, device=DEV)
+    Y = torch.empty_like(X)
+    P.poetx_blockdiag_mm(X, G, Y, trans=trans, out_perm=perm)
+    Z = torch.empty_like(X)
+    P.poetx_blockdiag_mm(X, G, Z, trans=trans)
+    ref = torch.empty_like(X)
+    P.poetx_perm_scatter(Z, perm, ref)
+    np.testing.assert_array_equal(host(Y), host(ref))
+    assert O.rel_fro(host(Y), O.perm_scatter(O.blockdiag_mm(host(X), host(G), trans),
+                                             host(perm))) <= TOL_BF16_STEP
+
+
 @pytest.mark.parametrize("N,nblk,b,splits", [(300, 4, 64, 3), (1000, 2, 128, 4),
                                              (517, 2, 256, 2), (256, 1, 512, 1),
                                              (100, 2, 256, 4), (0, 2, 64, 2)])
