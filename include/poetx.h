@@ -86,6 +86,10 @@ unsigned long long poetx_launch_count(void);
  * the previous event (host arrays of `cap` entries, nullable); it returns the number of
  * launches timed and forgets them.  Stage ids are named by poetx_stage_name. */
 poetx_status poetx_profile_enable(int on);
+/* Diagnostic phase trace: with a device buffer set (NULL turns it off), the tensor-core GEMM
+ * kernels write %globaltimer stamps (ns) of their phases, 32 unsigned 64-bit slots per CTA,
+ * CTA-major, into it (slots beyond `bytes` are dropped).  Each launch overwrites it. */
+poetx_status poetx_set_trace_buffer(void* buf, size_t bytes);
 int poetx_profile_collect(int* stage, float* ms, int cap);
 const char* poetx_stage_name(int stage);
 

@@ -168,3 +168,18 @@ extern "C" int poetx_profile_collect(int* stage, float* ms, int cap) {
   g_prof.clear();
   return n;
 }
+
+static std::atomic<unsigned long long*> g_trace{nullptr};
+static std::atomic<size_t> g_trace_slots{0};
+
+unsigned long long* poetx::trace_buffer(size_t* slots) {
+  *slots = g_trace_slots.load();
+  return g_trace.load();
+}
+
+extern "C" poetx_status poetx_set_trace_buffer(void* buf, size_t bytes) {
+  if (buf && !aligned16(buf)) return POETX_ERR_ALIGN;
+  g_trace_slots.store(buf ? bytes / 8 : 0);
+  g_trace.store(static_cast<unsigned long long*>(buf));
+  return POETX_OK;
+}

@@ -123,7 +123,7 @@ template <int BN>
 constexpr int conv_warps() { return BN / 8; }
 
 template <int BN, int STAGES>
-__global__ void __launch_bounds__(64 + 32 * conv_warps<BN>(), 2)
+__global__ void __launch_bounds__(64 + 32 * conv_warps<BN>(), 1)
     cnp_umma_kernel(const __grid_constant__ CnpMaps maps, const CnpUParams p) {
   constexpr int NCW = conv_warps<BN>();
   constexpr int NCT = 32 * NCW;  // converter threads
@@ -491,8 +491,8 @@ poetx_status cnp_umma_product(const CnpProduct& g, int nblk, cudaStream_t s) {
   p.out_bf16_t = g.out_bf16_t;
   p.err = device_error_word();
   p.limit_ns = kWaitLimitNs;
-  if (g.b % 64 == 0) return launch_t<64, 2>(maps, p, nblk, s);
-  return launch_t<32, 2>(maps, p, nblk, s);
+  if (g.b % 64 == 0) return launch_t<64, 4>(maps, p, nblk, s);
+  return launch_t<32, 4>(maps, p, nblk, s);
 }
 
 }  // namespace poetx

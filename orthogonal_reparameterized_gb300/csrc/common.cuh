@@ -54,6 +54,10 @@ enum Stage : int {
 void after_launch(cudaStream_t s, int stage);
 // Records the reference event that the first stage of a call is timed from.
 void prof_begin(cudaStream_t s);
+// Diagnostic trace buffer (device, nullable): the tensor-core kernels record %globaltimer
+// stamps of their phases into it, kTraceSlots 64-bit slots per CTA.
+unsigned long long* trace_buffer(size_t* slots);
+constexpr int kTraceSlots = 32;
 
 // ------------------------------------------------------------------------------------
 // device helpers
@@ -62,6 +66,13 @@ __device__ __forceinline__ unsigned long long global_ns() {
   unsigned long long t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
+}
+
+__device__ __forceinline__ void trace_stamp(unsigned long long* tr, size_t cap, int slot) {
+  if (tr) {
+    const size_t i = (size_t)blockIdx.x * kTraceSlots + slot;
+    if (i < cap) tr[i] = global_ns();
+  }
 }
 
 __device__ __forceinline__ void record_error(int* err, int code) {

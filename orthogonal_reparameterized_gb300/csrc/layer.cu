@@ -116,9 +116,9 @@ struct Plan {
   // saved
   size_t GR, GP, Q2R, Q2P, Qs, Bsv, saved_total;
   // forward workspace
-  size_t f_xt, f_A, f_B, fwd_total;
+  size_t f_xt, f_A, f_B, f_zt, fwd_total;
   // backward workspace
-  size_t b_cnp, b_xt, b_dzt, b_A, b_B, b_dB, b_dA, b_dGP, b_dGR, bwd_total;
+  size_t b_cnp, b_xt, b_dzt, b_A, b_B, b_dB, b_dA, b_dxt, b_dGP, b_dGR, bwd_total;
   int splitsR, splitsP;
 };
 
@@ -164,6 +164,7 @@ static Plan make_plan(const poetx_layer* L, long long N) {
   p.f_xt = take((size_t)N * m * as);
   p.f_A = take((size_t)N * m * as);
   p.f_B = L->variant == POETX_MEM ? take((size_t)N * n * as) : 0;
+  p.f_zt = take((size_t)N * n * as);
   p.fwd_total = o;
 
   p.splitsR = wgrad_splits(N, L->m / L->b, L->b);
@@ -176,6 +177,7 @@ static Plan make_plan(const poetx_layer* L, long long N) {
   p.b_B = L->variant == POETX_MEM ? take((size_t)N * n * as) : 0;
   p.b_dB = take((size_t)N * n * as);
   p.b_dA = take((size_t)N * m * as);
+  p.b_dxt = take((size_t)N * m * as);
   p.b_dGP = take((size_t)p.splitsP * n * b * 4);
   p.b_dGR = take((size_t)p.splitsR * m * b * 4);
   p.bwd_total = o;
@@ -240,8 +242,11 @@ extern "C" poetx_status poetx_layer_fwd(const poetx_layer* L, const void* x, int
   POETX_TRY(launch_perm_rows(as, false, x, N, m, L->perm_m, xt, nullptr, nullptr, nullptr, stream));
   POETX_TRY(blockdiag_impl(act, xt, N, m / b, b, at(saved, p.GR), 0, nullptr, nullptr, A, stream));
   POETX_TRY(wprime_impl(act, L->wdt, A, N, m, n, L->Wp, L->w_scale, 0, B, stream));
-  // S6 + S7: z~ = B blkdiag(G_P), stored straight into y through the permutation
-  return blockdiag_impl(act, B, N, n / b, b, at(saved, p.GP), 0, nullptr, L->perm_n, y, stream);
+  // S6 + S7.  (Storing z~ through the permutation inside the product is supported, but its
+  // 2-byte scattered stores are slower than this coalesced scatter pass.)
+  void* zt = at(ws, p.f_zt);
+  POETX_TRY(blockdiag_impl(act, B, N, n / b, b, at(saved, p.GP), 0, nullptr, nullptr, zt, stream));
+  return launch_perm_rows(as, true, zt, N, n, L->perm_n, y, nullptr, nullptr, nullptr, stream);
 }
 
 extern "C" poetx_status poetx_layer_bwd(const poetx_layer* L, const void* x, const void* dy, int N,
@@ -288,8 +293,11 @@ extern "C" poetx_status poetx_layer_bwd(const poetx_layer* L, const void* x, con
                            L->wdt == POETX_I8 ? L->w_scale : nullptr, nullptr, dB, stream));
   POETX_TRY(wprime_impl(act, L->wdt, dB, N, m, n, L->Wp, L->w_scale, 1, dA, stream));
   POETX_TRY(wgrad_impl(act, xt, dA, N, m / b, b, p.splitsR, dGR, stream));
-  // S12 + S13: dx~ = dA blkdiag(G_R)^T, stored straight into dx through the permutation
-  POETX_TRY(blockdiag_impl(act, dA, N, m / b, b, GR, 1, nullptr, L->perm_m, dx, stream));
+  // S12 + S13
+  void* dxt = at(ws, p.b_dxt);
+  POETX_TRY(blockdiag_impl(act, dA, N, m / b, b, GR, 1, nullptr, nullptr, dxt, stream));
+  if (N > 0)
+    POETX_TRY(launch_perm_rows(as, true, dxt, N, m, L->perm_m, dx, nullptr, nullptr, nullptr, stream));
   const CnpSides sides{{L->q_R, L->q_P}, {m / b, n / b}};
   const float* const dGs[2] = {dGR, dGP};
   const int splits[2] = {p.splitsR, p.splitsP};

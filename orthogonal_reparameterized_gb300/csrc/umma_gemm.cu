@@ -45,6 +45,8 @@ struct UmmaParams {
   long long ldc;
   const float* colscale;
   const int32_t* out_perm;  // BLOCKDIAG: output column c is stored at column out_perm[c]
+  unsigned long long* trace;  // diagnostic phase stamps (nullable)
+  size_t trace_cap;
   int* err;
   unsigned long long limit_ns;
 };
@@ -147,6 +149,7 @@ __global__ void __launch_bounds__(192, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) trace_stamp(p.trace, p.trace_cap, 0);  // slot 0: CTA start
 
   if (warp == 0 && lane == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -171,6 +174,7 @@ __global__ void __launch_bounds__(192, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const uint32_t smem_base = smem_u32(smem);
+  if (threadIdx.x == 0) trace_stamp(p.trace, p.trace_cap, 1);  // slot 1: set-up done
 
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -187,6 +191,7 @@ __global__ void __launch_bounds__(192, 1)
           break;
         }
         mbar_arrive_expect_tx(&full[s], STAGE_BYTES);
+        if (g == 0) trace_stamp(p.trace, p.trace_cap, 2);  // slot 2: first TMA issued
         uint8_t* sa = smem + s * STAGE_BYTES;
         uint8_t* sb = sa + A_BYTES;
         const int k = kb * BK;
@@ -233,6 +238,7 @@ __global__ void __launch_bounds__(192, 1)
           break;
         }
         tc_fence_after();
+        if (g == 0) trace_stamp(p.trace, p.trace_cap, 3);  // slot 3: first stage landed
         const uint32_t a_base = smem_base + s * STAGE_BYTES;
         const uint32_t b_base = a_base + A_BYTES;
 #pragma unroll
@@ -262,6 +268,7 @@ __global__ void __launch_bounds__(192, 1)
         break;
       }
       tc_fence_after();
+      if (warp == 2 && lane == 0 && it < 12) trace_stamp(p.trace, p.trace_cap, 5 + 2 * it);  // acc ready
       const long long grow = c.out_row0 + row;
       const bool valid = grow < p.M;
 #pragma unroll 1
@@ -319,10 +326,13 @@ __global__ void __launch_bounds__(192, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty[a]);
+      if (warp == 2 && lane == 0 && it < 12) trace_stamp(p.trace, p.trace_cap, 4 + 2 * it);  // tile stored
     }
   }
+  if (warp == 2 && lane == 0) trace_stamp(p.trace, p.trace_cap, 30);  // epilogue loop done
   tc_fence_before();
   __syncthreads();
+  if (threadIdx.x == 0) trace_stamp(p.trace, p.trace_cap, 31);  // slot 31: exit
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
@@ -426,6 +436,7 @@ poetx_status launch(const CUtensorMap& ta, const CUtensorMap& tb, UmmaParams p, 
 
 UmmaParams base_params() {
   UmmaParams p{};
+  p.trace = trace_buffer(&p.trace_cap);
   p.err = device_error_word();
   p.limit_ns = kWaitLimitNs;
   return p;

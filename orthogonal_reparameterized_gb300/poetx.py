@@ -44,6 +44,7 @@ _SIGS = {
     "poetx_set_gemm_engine": (_i, [_i]),
     "poetx_launch_count": (ctypes.c_ulonglong, []),
     "poetx_profile_enable": (_i, [_i]),
+    "poetx_set_trace_buffer": (_i, [_vp, _sz]),
     "poetx_profile_collect": (_i, [ctypes.POINTER(_i), ctypes.POINTER(_f), _i]),
     "poetx_stage_name": (ctypes.c_char_p, [_i]),
     "poetx_cnp_workspace_bytes": (_sz, [_i, _i, _i]),
@@ -126,6 +127,11 @@ def poetx_launch_count() -> int:
 
 def poetx_profile_enable(on: bool):
     _check("poetx_profile_enable", lib().poetx_profile_enable(int(bool(on))))
+
+
+def poetx_set_trace_buffer(buf=None):
+    _check("poetx_set_trace_buffer",
+           lib().poetx_set_trace_buffer(_p(buf), 0 if buf is None else buf.numel() * buf.element_size()))
 
 
 def poetx_profile_collect(cap: int = 4096):

@@ -71,7 +71,7 @@ def test_layer_sizes_host_logic(P):
     mem = P.poetx_layer_saved_bytes(_desc(P, variant=P.MEM), N)
     assert fast - mem >= N * 512 * 2
     assert mem >= (256 + 512) * 64 * (2 + 4)
-    assert P.poetx_layer_workspace_bytes(L, N, 0) >= 2 * N * 256 * 2  # x~ and A
+    assert P.poetx_layer_workspace_bytes(L, N, 0) >= N * (2 * 256 + 512) * 2  # x~, A, z~
     assert P.poetx_layer_workspace_bytes(L, N, 1) > P.poetx_layer_workspace_bytes(L, N, 0)
     # invalid descriptors report 0 bytes
     assert P.poetx_layer_workspace_bytes(_desc(P, b=100), N, 0) == 0        # b not supported
