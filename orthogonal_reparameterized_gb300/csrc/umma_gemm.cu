@@ -128,8 +128,12 @@ __device__ __forceinline__ TileCoords tile_coords(const UmmaParams& p, int t) {
   return c;
 }
 
+// 8 epilogue warps (2..9): two per TMEM lane quarter, each storing half of the BN columns.
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 64 + 32 * kEpiWarps;
+
 template <int BN, int STAGES, bool A_MN, bool B_MN, bool OUT_F32>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(kThreads, 1)
     umma_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmB, const UmmaParams p) {
   constexpr uint32_t A_BYTES = BM * BK * 2;
@@ -158,7 +162,7 @@ __global__ void __launch_bounds__(192, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], 4);
+      mbar_init(&tempty[a], kEpiWarps);
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -256,7 +260,8 @@ __global__ void __launch_bounds__(192, 1)
     }
   } else if (warp >= 2) {
     // ------------------------------------------------------------ epilogue
-    const int q = warp & 3;
+    const int q = warp & 3;                   // TMEM lane quarter = output rows
+    const int cbeg = ((warp - 2) >> 2) * (BN / 2);  // this warp's half of the columns
     const int row = q * 32 + lane;
     int it = 0;
     for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++it) {
@@ -272,7 +277,7 @@ __global__ void __launch_bounds__(192, 1)
       const long long grow = c.out_row0 + row;
       const bool valid = grow < p.M;
 #pragma unroll 1
-      for (int c0 = 0; c0 < BN; c0 += 32) {
+      for (int c0 = cbeg; c0 < cbeg + BN / 2; c0 += 32) {
         uint32_t r[32];
         if (c.num_kb > 0) {
           tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(a * BN + c0), r);
@@ -410,10 +415,11 @@ poetx_status launch(const CUtensorMap& ta, const CUtensorMap& tb, UmmaParams p, 
   constexpr int smem = STAGES * (BM * BK * 2 + BN * BK * 2) + 1024 + 256;
   // TMEM holds 512 columns per SM: 2 x BN columns per CTA bound the CTAs per SM, and the
   // shared memory of every configuration is sized so that no more than that many fit.
-  constexpr int per_sm = 512 / (2 * BN) < 2 ? 512 / (2 * BN) : 2;
-  static_assert(per_sm >= 1, "accumulators exceed TMEM");
-  static_assert((size_t)smem * (per_sm + 1) > 228 * 1024 || per_sm == 2,
-                "shared memory must keep the CTAs per SM within TMEM");
+  // CTAs per SM: bounded by TMEM (2 x BN columns each, 512 per SM) and shared memory.
+  constexpr int by_tmem = 512 / (2 * BN);
+  constexpr int by_smem = (int)((227 * 1024) / (smem + 1024));
+  constexpr int per_sm = by_tmem < by_smem ? by_tmem : by_smem;
+  static_assert(per_sm >= 1, "configuration exceeds TMEM or shared memory");
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [&] {
@@ -428,7 +434,7 @@ poetx_status launch(const CUtensorMap& ta, const CUtensorMap& tb, UmmaParams p, 
   p.num_tiles = (int)tiles;
   const long long want = (long long)sm_count() * per_sm;
   const int grid = (int)(tiles < want ? tiles : want);
-  k<<<grid, 192, smem, s>>>(ta, tb, p);
+  k<<<grid, kThreads, smem, s>>>(ta, tb, p);
   POETX_CUDA_TRY(cudaGetLastError());
   after_launch(s, stage);
   return POETX_OK;
@@ -465,7 +471,7 @@ poetx_status umma_blockdiag(const void* X, long long N, int nblk, int b, const v
                             cudaStream_t s) {
   if (N == 0 || nblk == 0) return POETX_OK;
   const int D = nblk * b;
-  const int BN = b < 256 ? b : 256;
+  const int BN = b < 128 ? b : 128;  // narrow tiles, deep ring: this product is HBM bound
   CUtensorMap ta, tb;
   if (!make_map(&ta, X, D, N, D, 64, 128)) return POETX_ERR_CUDA;
   if (trans) {
@@ -484,13 +490,11 @@ poetx_status umma_blockdiag(const void* X, long long N, int nblk, int b, const v
   p.out_perm = out_perm;
   const int tm = (int)((N + BM - 1) / BM), tn = b / BN;
   if (trans) {
-    if (BN == 64) return launch<64, 4, false, false, false>(ta, tb, p, tm, tn, nblk, s);
-    if (BN == 128) return launch<128, 3, false, false, false>(ta, tb, p, tm, tn, nblk, s);
-    return launch<256, 4, false, false, false>(ta, tb, p, tm, tn, nblk, s);
+    if (BN == 64) return launch<64, 8, false, false, false>(ta, tb, p, tm, tn, nblk, s);
+    return launch<128, 6, false, false, false>(ta, tb, p, tm, tn, nblk, s);
   }
-  if (BN == 64) return launch<64, 4, false, true, false>(ta, tb, p, tm, tn, nblk, s);
-  if (BN == 128) return launch<128, 3, false, true, false>(ta, tb, p, tm, tn, nblk, s);
-  return launch<256, 4, false, true, false>(ta, tb, p, tm, tn, nblk, s);
+  if (BN == 64) return launch<64, 8, false, true, false>(ta, tb, p, tm, tn, nblk, s);
+  return launch<128, 6, false, true, false>(ta, tb, p, tm, tn, nblk, s);
 }
 
 poetx_status umma_wprime(const void* A, long long N, int m, int n, const void* W,
