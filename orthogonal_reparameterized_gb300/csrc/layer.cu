@@ -29,8 +29,9 @@ static bool use_umma() { return g_engine.load() == 0 && umma_supported(); }
 bool use_tensor_cores() { return g_engine.load() == 0; }
 
 static int wgrad_splits(long long N, int nblk, int b) {
+  // one wave: tiles x splits <= SMs (a partial second wave costs a whole extra tile time)
   const long long tiles = (long long)nblk * ((b + 127) / 128) * (b > 256 ? b / 256 : 1);
-  long long s = ((long long)sm_count() + tiles - 1) / tiles;
+  long long s = (long long)sm_count() / tiles;
   long long smax = N / 256;
   if (smax < 1) smax = 1;
   if (s > smax) s = smax;

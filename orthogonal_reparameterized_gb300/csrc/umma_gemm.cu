@@ -19,6 +19,7 @@
 // Every mbarrier wait is bounded; on expiry the kernel records POETX_ERR_TIMEOUT, drains
 // its own copies, frees its TMEM and returns.
 #include <atomic>
+#include <cstdlib>
 #include <mutex>
 
 #include "common.cuh"
@@ -34,6 +35,7 @@ struct UmmaParams {
   int mode;
   int tiles_m, tiles_n, num_tiles;  // tile t: mt = t % tiles_m, nt = (t / tiles_m) % tiles_n,
                                     // z = t / (tiles_m * tiles_n) (block, or block*splits+split)
+  int order;                        // 1: z fastest, then nt, then mt
   int M;         // valid output rows of the whole problem (tokens, or b for WGRAD)
   int num_kb;    // 64-wide K blocks per CTA (PLAIN, BLOCKDIAG)
   int b;         // block size (BLOCKDIAG, WGRAD)
@@ -96,10 +98,19 @@ struct TileCoords {
 template <int BN, bool B_MN>
 __device__ __forceinline__ TileCoords tile_coords(const UmmaParams& p, int t) {
   TileCoords c;
-  const int mt = t % p.tiles_m;
-  const int rest = t / p.tiles_m;
-  const int nt = rest % p.tiles_n;
-  const int z = rest / p.tiles_n;
+  int mt, nt, z;
+  if (p.order == 0) {
+    mt = t % p.tiles_m;
+    const int rest = t / p.tiles_m;
+    nt = rest % p.tiles_n;
+    z = rest / p.tiles_n;
+  } else {
+    const int tz = p.num_tiles / (p.tiles_m * p.tiles_n);
+    z = t % tz;
+    const int rest = t / tz;
+    nt = rest % p.tiles_n;
+    mt = rest / p.tiles_n;
+  }
   c.num_kb = p.num_kb;
   c.out_row0 = (long long)mt * BM;
   c.out_col0 = (long long)nt * BN;
@@ -145,7 +156,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  // per epilogue warp: 32 rows x 64 columns staging buffer (rows padded by 16 bytes), so
+  // that the global stores cover whole row segments instead of 16 bytes of 32 rows each
+  constexpr uint32_t ESZ = OUT_F32 ? 4 : 2;
+  constexpr uint32_t STG_PITCH = 64 * ESZ + 16;
+  uint8_t* staging = smem + STAGES * STAGE_BYTES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(staging + kEpiWarps * 32 * STG_PITCH);
   uint64_t* empty = full + STAGES;
   uint64_t* tfull = empty + STAGES;  // [2]
   uint64_t* tempty = tfull + 2;      // [2]
@@ -274,59 +290,75 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
       if (warp == 2 && lane == 0 && it < 12) trace_stamp(p.trace, p.trace_cap, 5 + 2 * it);  // acc ready
-      const long long grow = c.out_row0 + row;
-      const bool valid = grow < p.M;
+      uint8_t* stg = staging + (warp - 2) * 32 * STG_PITCH;
+      const long long row0 = c.out_row0 + q * 32;  // first output row of this warp
 #pragma unroll 1
-      for (int c0 = cbeg; c0 < cbeg + BN / 2; c0 += 32) {
-        uint32_t r[32];
+      for (int c0 = cbeg; c0 < cbeg + BN / 2; c0 += 64) {
+        // two 32-column TMEM loads, one wait
+        uint32_t r[64];
         if (c.num_kb > 0) {
-          tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(a * BN + c0), r);
+          const uint32_t ta = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(a * BN + c0);
+          tmem_ld_32x32b_x32(ta, *reinterpret_cast<uint32_t(*)[32]>(r));
+          if (BN / 2 >= 64) tmem_ld_32x32b_x32(ta + 32, *reinterpret_cast<uint32_t(*)[32]>(r + 32));
           tmem_ld_wait();
         } else {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) r[i] = 0u;
+          for (int i = 0; i < 64; ++i) r[i] = 0u;
         }
-        if (!valid) continue;
+        const int ncol = BN / 2 >= 64 ? 64 : BN / 2;  // columns in this pass
+        // lane = row: write its values into the staging rows
         if (OUT_F32) {
-          float* dst = static_cast<float*>(p.C) +
-                       (((long long)c.split * p.nblk + c.blk) * p.b + grow) * p.b + c.out_col0 + c0;
+          float4* dst = reinterpret_cast<float4*>(stg + lane * STG_PITCH);
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            reinterpret_cast<float4*>(dst)[i] =
-                make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
-                            __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
+          for (int i = 0; i < 16; ++i)
+            if (4 * i < ncol)
+              dst[i] = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
+                                   __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
         } else {
-          __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.C) + grow * p.ldc + c.out_col0 + c0;
-          float v[32];
+          float v[64];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+          for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
           if (p.colscale) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] *= __ldg(p.colscale + c.out_col0 + c0 + i);
+            for (int i = 0; i < 64; ++i)
+              if (i < ncol) v[i] *= __ldg(p.colscale + c.out_col0 + c0 + i);
           }
-          if (p.out_perm) {  // fused output permutation: scattered 2-byte stores
+          uint4* dst = reinterpret_cast<uint4*>(stg + lane * STG_PITCH);
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            if (8 * i < ncol)
+              dst[i] = make_uint4(pack_bf16x2(v[8 * i], v[8 * i + 1]), pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
+                                  pack_bf16x2(v[8 * i + 4], v[8 * i + 5]), pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
+        }
+        __syncwarp();
+        // lanes cover whole row segments: (ncol * ESZ / 16) lanes per row
+        const int per_row = ncol * (int)ESZ / 16;
+        const int rows_per_pass = 32 / per_row;
+        const int pr = lane / per_row, pc = lane % per_row;
+        for (int rr = pr; rr < 32; rr += rows_per_pass) {
+          const long long grow = row0 + rr;
+          if (grow >= p.M) continue;
+          const uint4 val = *reinterpret_cast<const uint4*>(stg + rr * STG_PITCH + pc * 16);
+          uint8_t* gdst;
+          if (OUT_F32)
+            gdst = reinterpret_cast<uint8_t*>(static_cast<float*>(p.C) +
+                   (((long long)c.split * p.nblk + c.blk) * p.b + grow) * p.b + c.out_col0 + c0);
+          else if (p.out_perm)
+            gdst = nullptr;
+          else
+            gdst = reinterpret_cast<uint8_t*>(static_cast<__nv_bfloat16*>(p.C) + grow * p.ldc +
+                                              c.out_col0 + c0);
+          if (gdst) {
+            *reinterpret_cast<uint4*>(gdst + pc * 16) = val;
+          } else {  // fused output permutation: scattered 2-byte stores
             __nv_bfloat16* rowp = static_cast<__nv_bfloat16*>(p.C) + grow * p.ldc;
-            const int4* pp = reinterpret_cast<const int4*>(p.out_perm + c.out_col0 + c0);
+            const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&val);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const int4 d4 = __ldg(pp + i);
-              rowp[d4.x] = __float2bfloat16_rn(v[4 * i]);
-              rowp[d4.y] = __float2bfloat16_rn(v[4 * i + 1]);
-              rowp[d4.z] = __float2bfloat16_rn(v[4 * i + 2]);
-              rowp[d4.w] = __float2bfloat16_rn(v[4 * i + 3]);
-            }
-          } else {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              uint4 w;
-              w.x = pack_bf16x2(v[8 * i + 0], v[8 * i + 1]);
-              w.y = pack_bf16x2(v[8 * i + 2], v[8 * i + 3]);
-              w.z = pack_bf16x2(v[8 * i + 4], v[8 * i + 5]);
-              w.w = pack_bf16x2(v[8 * i + 6], v[8 * i + 7]);
-              reinterpret_cast<uint4*>(dst)[i] = w;
-            }
+            for (int i = 0; i < 8; ++i)
+              rowp[__ldg(p.out_perm + c.out_col0 + c0 + pc * 8 + i)] = e[i];
           }
         }
+        __syncwarp();
       }
       tc_fence_before();
       __syncwarp();
@@ -412,13 +444,15 @@ poetx_status launch(const CUtensorMap& ta, const CUtensorMap& tb, UmmaParams p, 
                     int tiles_n, int tiles_z, cudaStream_t s) {
   const int stage = p.mode == MODE_PLAIN ? ST_WPRIME : (p.mode == MODE_BLOCKDIAG ? ST_BLOCKDIAG : ST_WGRAD);
   auto k = umma_gemm_kernel<BN, STAGES, A_MN, B_MN, OUT_F32>;
-  constexpr int smem = STAGES * (BM * BK * 2 + BN * BK * 2) + 1024 + 256;
+  constexpr int smem = STAGES * (BM * BK * 2 + BN * BK * 2) +
+                       kEpiWarps * 32 * (64 * (OUT_F32 ? 4 : 2) + 16) + 1024 + 256;
   // TMEM holds 512 columns per SM: 2 x BN columns per CTA bound the CTAs per SM, and the
   // shared memory of every configuration is sized so that no more than that many fit.
   // CTAs per SM: bounded by TMEM (2 x BN columns each, 512 per SM) and shared memory.
   constexpr int by_tmem = 512 / (2 * BN);
   constexpr int by_smem = (int)((227 * 1024) / (smem + 1024));
   constexpr int per_sm = by_tmem < by_smem ? by_tmem : by_smem;
+  static_assert(smem <= 227 * 1024, "shared memory per CTA exceeds the sm_103 limit");
   static_assert(per_sm >= 1, "configuration exceeds TMEM or shared memory");
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
@@ -442,6 +476,11 @@ poetx_status launch(const CUtensorMap& ta, const CUtensorMap& tb, UmmaParams p, 
 
 UmmaParams base_params() {
   UmmaParams p{};
+  static const int order_env = [] {
+    const char* e = getenv("POETX_TILE_ORDER");
+    return e ? atoi(e) : 0;
+  }();
+  p.order = order_env;
   p.trace = trace_buffer(&p.trace_cap);
   p.err = device_error_word();
   p.limit_ns = kWaitLimitNs;
@@ -490,11 +529,11 @@ poetx_status umma_blockdiag(const void* X, long long N, int nblk, int b, const v
   p.out_perm = out_perm;
   const int tm = (int)((N + BM - 1) / BM), tn = b / BN;
   if (trans) {
-    if (BN == 64) return launch<64, 8, false, false, false>(ta, tb, p, tm, tn, nblk, s);
-    return launch<128, 6, false, false, false>(ta, tb, p, tm, tn, nblk, s);
+    if (BN == 64) return launch<64, 7, false, false, false>(ta, tb, p, tm, tn, nblk, s);
+    return launch<128, 5, false, false, false>(ta, tb, p, tm, tn, nblk, s);
   }
-  if (BN == 64) return launch<64, 8, false, true, false>(ta, tb, p, tm, tn, nblk, s);
-  return launch<128, 6, false, true, false>(ta, tb, p, tm, tn, nblk, s);
+  if (BN == 64) return launch<64, 7, false, true, false>(ta, tb, p, tm, tn, nblk, s);
+  return launch<128, 5, false, true, false>(ta, tb, p, tm, tn, nblk, s);
 }
 
 poetx_status umma_wprime(const void* A, long long N, int m, int n, const void* W,
@@ -511,14 +550,14 @@ poetx_status umma_wprime(const void* A, long long N, int m, int n, const void* W
     if (!make_map(&tb, W, m, n, m, 64, 256)) return POETX_ERR_CUDA;
     p.num_kb = m / 64;
     p.ldc = n;
-    return launch<256, 4, false, false, false>(ta, tb, p, (int)((N + BM - 1) / BM), n / 256, 1, s);
+    return launch<256, 3, false, false, false>(ta, tb, p, (int)((N + BM - 1) / BM), n / 256, 1, s);
   }
   // C[N,m] = A[N,n] W: B operand (output col c, K index r) = W[r][c], MN-major
   if (!make_map(&ta, A, n, N, n, 64, 128)) return POETX_ERR_CUDA;
   if (!make_map(&tb, W, m, n, m, 64, 64)) return POETX_ERR_CUDA;
   p.num_kb = n / 64;
   p.ldc = m;
-  return launch<256, 4, false, true, false>(ta, tb, p, (int)((N + BM - 1) / BM), m / 256, 1, s);
+  return launch<256, 3, false, true, false>(ta, tb, p, (int)((N + BM - 1) / BM), m / 256, 1, s);
 }
 
 poetx_status umma_wgrad(const void* X, const void* dY, long long N, int nblk, int b, int splits,
@@ -546,7 +585,7 @@ poetx_status umma_wgrad(const void* X, const void* dY, long long N, int nblk, in
   const int tm = (b + BM - 1) / BM, tn = b / BN;
   if (BN == 64) return launch<64, 4, true, true, true>(ta, tb, p, tm, tn, nblk * splits, s);
   if (BN == 128) return launch<128, 3, true, true, true>(ta, tb, p, tm, tn, nblk * splits, s);
-  return launch<256, 4, true, true, true>(ta, tb, p, tm, tn, nblk * splits, s);
+  return launch<256, 3, true, true, true>(ta, tb, p, tm, tn, nblk * splits, s);
 }
 
 }  // namespace poetx
