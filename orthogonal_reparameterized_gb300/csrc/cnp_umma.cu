@@ -59,6 +59,8 @@ struct CnpUParams {
   float* out_f32_t;
   __nv_bfloat16* out_bf16;
   __nv_bfloat16* out_bf16_t;
+  unsigned long long* trace;  // diagnostic phase stamps (nullable)
+  size_t trace_cap;
   int* err;
   unsigned long long limit_ns;
 };
@@ -146,6 +148,15 @@ __global__ void __launch_bounds__(64 + 32 * conv_warps<BN>(), 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int mt = blockIdx.x, nt = blockIdx.y, blk = blockIdx.z;
+  // trace slots are indexed by the linear CTA id
+  const unsigned long long lin = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
+  auto stamp = [&](int slot) {
+    if (p.trace) {
+      const size_t i = lin * kTraceSlots + slot;
+      if (i < p.trace_cap) p.trace[i] = global_ns();
+    }
+  };
+  if (threadIdx.x == 0) stamp(0);
   const int b = p.b;
   const int num_kb = p.nseg * p.kb_per_seg;
   const int row0 = blk * b;  // first row of this block in the [nblk*b, b] views
@@ -172,6 +183,7 @@ __global__ void __launch_bounds__(64 + 32 * conv_warps<BN>(), 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const uint32_t smem_base = smem_u32(smem);
+  if (threadIdx.x == 0) stamp(1);
 
   if (warp == 0 && lane == 0) {
     // ---------------------------------------------------------------- TMA producer
@@ -193,6 +205,7 @@ __global__ void __launch_bounds__(64 + 32 * conv_warps<BN>(), 1)
         if (B.s[i].map >= 0) bytes += B_BYTES;
       }
       mbar_arrive_expect_tx(&full[s], bytes);
+      if (kb < 8) stamp(2 + kb);  // slots 2..9: K block issued
       uint8_t* st = smem + s * STAGE_BYTES;
       for (int i = 0; i < 2; ++i) {
         if (A.s[i].map >= 0) {
@@ -306,10 +319,13 @@ __global__ void __launch_bounds__(64 + 32 * conv_warps<BN>(), 1)
       fence_async_smem();  // generic-proxy writes -> visible to the tensor cores
       __syncwarp();
       if (lane == 0) mbar_arrive(&conv[s]);
+      if (warp == 2 && lane == 0 && kb < 8) stamp(10 + kb);  // slots 10..17: K block converted
       if (kb >= 1) promote(kb - 1);
+      if (warp == 2 && lane == 0 && kb >= 1 && kb < 9) stamp(18 + kb - 1);  // 18..25: promoted
     }
     if (ok_all && num_kb > 0) promote(num_kb - 1);
     // ---------------------------------------------------------------- epilogue
+    if (warp == 2 && lane == 0) stamp(26);  // epilogue start
     const long long base = (long long)blk * b * b;
     if (i < b) {
       {
@@ -369,6 +385,7 @@ __global__ void __launch_bounds__(64 + 32 * conv_warps<BN>(), 1)
   }
   tc_fence_before();
   __syncthreads();
+  if (threadIdx.x == 0) stamp(31);
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
@@ -491,6 +508,7 @@ poetx_status cnp_umma_product(const CnpProduct& g, int nblk, cudaStream_t s) {
   p.out_bf16_t = g.out_bf16_t;
   p.err = device_error_word();
   p.limit_ns = kWaitLimitNs;
+  p.trace = trace_buffer(&p.trace_cap);
   if (g.b % 64 == 0) return launch_t<64, 4>(maps, p, nblk, s);
   return launch_t<32, 4>(maps, p, nblk, s);
 }

@@ -143,6 +143,15 @@ __device__ __forceinline__ TileCoords tile_coords(const UmmaParams& p, int t) {
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 
+// Columns the epilogue stages per pass: 64, or 32 when the operand ring leaves no room.
+template <int BN, int STAGES, bool OUT_F32>
+constexpr int epi_pass_cols() {
+  constexpr int ring = STAGES * (BM * BK * 2 + BN * BK * 2);
+  constexpr int esz = OUT_F32 ? 4 : 2;
+  constexpr int c = (BN / 2 < 64) ? BN / 2 : 64;
+  return ring + kEpiWarps * 32 * (c * esz + 16) + 1280 <= 227 * 1024 ? c : 32;
+}
+
 template <int BN, int STAGES, bool A_MN, bool B_MN, bool OUT_F32>
 __global__ void __launch_bounds__(kThreads, 1)
     umma_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
@@ -159,7 +168,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   // per epilogue warp: 32 rows x 64 columns staging buffer (rows padded by 16 bytes), so
   // that the global stores cover whole row segments instead of 16 bytes of 32 rows each
   constexpr uint32_t ESZ = OUT_F32 ? 4 : 2;
-  constexpr uint32_t STG_PITCH = 64 * ESZ + 16;
+  constexpr int EPC = epi_pass_cols<BN, STAGES, OUT_F32>();  // columns per epilogue pass
+  constexpr uint32_t STG_PITCH = EPC * ESZ + 16;
   uint8_t* staging = smem + STAGES * STAGE_BYTES;
   uint64_t* full = reinterpret_cast<uint64_t*>(staging + kEpiWarps * 32 * STG_PITCH);
   uint64_t* empty = full + STAGES;
@@ -293,19 +303,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint8_t* stg = staging + (warp - 2) * 32 * STG_PITCH;
       const long long row0 = c.out_row0 + q * 32;  // first output row of this warp
 #pragma unroll 1
-      for (int c0 = cbeg; c0 < cbeg + BN / 2; c0 += 64) {
-        // two 32-column TMEM loads, one wait
+      for (int c0 = cbeg; c0 < cbeg + BN / 2; c0 += EPC) {
+        // one or two 32-column TMEM loads, one wait
         uint32_t r[64];
         if (c.num_kb > 0) {
           const uint32_t ta = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(a * BN + c0);
           tmem_ld_32x32b_x32(ta, *reinterpret_cast<uint32_t(*)[32]>(r));
-          if (BN / 2 >= 64) tmem_ld_32x32b_x32(ta + 32, *reinterpret_cast<uint32_t(*)[32]>(r + 32));
+          if (EPC >= 64) tmem_ld_32x32b_x32(ta + 32, *reinterpret_cast<uint32_t(*)[32]>(r + 32));
           tmem_ld_wait();
         } else {
 #pragma unroll
           for (int i = 0; i < 64; ++i) r[i] = 0u;
         }
-        const int ncol = BN / 2 >= 64 ? 64 : BN / 2;  // columns in this pass
+        const int ncol = EPC;  // columns in this pass
         // lane = row: write its values into the staging rows
         if (OUT_F32) {
           float4* dst = reinterpret_cast<float4*>(stg + lane * STG_PITCH);
@@ -445,7 +455,8 @@ poetx_status launch(const CUtensorMap& ta, const CUtensorMap& tb, UmmaParams p, 
   const int stage = p.mode == MODE_PLAIN ? ST_WPRIME : (p.mode == MODE_BLOCKDIAG ? ST_BLOCKDIAG : ST_WGRAD);
   auto k = umma_gemm_kernel<BN, STAGES, A_MN, B_MN, OUT_F32>;
   constexpr int smem = STAGES * (BM * BK * 2 + BN * BK * 2) +
-                       kEpiWarps * 32 * (64 * (OUT_F32 ? 4 : 2) + 16) + 1024 + 256;
+                       kEpiWarps * 32 * (epi_pass_cols<BN, STAGES, OUT_F32>() * (OUT_F32 ? 4 : 2) + 16) +
+                       1024 + 256;
   // TMEM holds 512 columns per SM: 2 x BN columns per CTA bound the CTAs per SM, and the
   // shared memory of every configuration is sized so that no more than that many fit.
   // CTAs per SM: bounded by TMEM (2 x BN columns each, 512 per SM) and shared memory.
@@ -550,14 +561,14 @@ poetx_status umma_wprime(const void* A, long long N, int m, int n, const void* W
     if (!make_map(&tb, W, m, n, m, 64, 256)) return POETX_ERR_CUDA;
     p.num_kb = m / 64;
     p.ldc = n;
-    return launch<256, 3, false, false, false>(ta, tb, p, (int)((N + BM - 1) / BM), n / 256, 1, s);
+    return launch<256, 4, false, false, false>(ta, tb, p, (int)((N + BM - 1) / BM), n / 256, 1, s);
   }
   // C[N,m] = A[N,n] W: B operand (output col c, K index r) = W[r][c], MN-major
   if (!make_map(&ta, A, n, N, n, 64, 128)) return POETX_ERR_CUDA;
   if (!make_map(&tb, W, m, n, m, 64, 64)) return POETX_ERR_CUDA;
   p.num_kb = n / 64;
   p.ldc = m;
-  return launch<256, 3, false, true, false>(ta, tb, p, (int)((N + BM - 1) / BM), m / 256, 1, s);
+  return launch<256, 4, false, true, false>(ta, tb, p, (int)((N + BM - 1) / BM), m / 256, 1, s);
 }
 
 poetx_status umma_wgrad(const void* X, const void* dY, long long N, int nblk, int b, int splits,
