@@ -31,7 +31,7 @@ namespace {
 
 constexpr int BM = 128;
 constexpr int BK = 32;      // fp32 elements per 128-byte row
-constexpr int NMAPS = 6;  // distinct source arrays of one product (Q-bar uses 5)
+constexpr int NMAPS = 8;  // distinct (source array, operand role) pairs of one product
 
 struct CnpMaps {
   CUtensorMap m[NMAPS];
@@ -47,6 +47,7 @@ struct TOp {
 
 struct CnpUParams {
   int b;
+  int nmaps;
   int nseg;
   int kb_per_seg;
   TOp A[2], B[2];
@@ -119,20 +120,23 @@ __device__ __forceinline__ void combine_split(float4* x, float4* y, float c0, fl
   *y = make_float4(lo[0], lo[1], lo[2], lo[3]);
 }
 
-// Converter / promotion warps: 4 * BN / 32, two per TMEM lane quarter for BN = 64, each
-// owning 32 accumulator columns.
-template <int BN>
-constexpr int conv_warps() { return BN / 8; }
+// Warp roles: 0 TMA producer, 1 MMA issuer (and TMEM owner), 2..9 converters (form and
+// split the operands), 10..13 promotion + epilogue (warp 10 + q reads TMEM lane quarter
+// (10 + q) % 4 = q + 2 mod 4).  NACC accumulators let the MMA run ahead of the promotion.
+constexpr int kConvWarps = 8;
+constexpr int kPromWarps = 4;
+constexpr int kThreadsCnp = 32 * (2 + kConvWarps + kPromWarps);
+constexpr int NACC = 4;
 
 template <int BN, int STAGES>
-__global__ void __launch_bounds__(64 + 32 * conv_warps<BN>(), 1)
+__global__ void __launch_bounds__(kThreadsCnp, 1)
     cnp_umma_kernel(const __grid_constant__ CnpMaps maps, const CnpUParams p) {
-  constexpr int NCW = conv_warps<BN>();
-  constexpr int NCT = 32 * NCW;  // converter threads
+  constexpr int NCT = 32 * kConvWarps;  // converter threads
   constexpr uint32_t A_BYTES = BM * BK * 4;   // 16 KB per buffer
   constexpr uint32_t B_BYTES = BN * BK * 4;   // BN * 128 bytes per buffer
   constexpr uint32_t STAGE_BYTES = 2 * A_BYTES + 2 * B_BYTES;
-  constexpr uint32_t TMEM_COLS = 2 * BN;  // two accumulators, used by alternate K blocks
+  constexpr uint32_t TMEM_COLS = NACC * BN;
+  static_assert(TMEM_COLS == 128 || TMEM_COLS == 256, "TMEM allocation must be a power of two");
   constexpr uint32_t IDESC = tf32_idesc(BM, BN);
 
   extern __shared__ uint8_t smem_raw[];
@@ -141,14 +145,13 @@ __global__ void __launch_bounds__(64 + 32 * conv_warps<BN>(), 1)
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
   uint64_t* conv = full + STAGES;
   uint64_t* empty = conv + STAGES;
-  uint64_t* tfull = empty + STAGES;   // [2] accumulator a holds a finished K block
-  uint64_t* tempty = tfull + 2;       // [2] accumulator a has been read back
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  uint64_t* tfull = empty + STAGES;   // [NACC] accumulator holds a finished K block
+  uint64_t* tempty = tfull + NACC;    // [NACC] accumulator has been read back
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + NACC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int mt = blockIdx.x, nt = blockIdx.y, blk = blockIdx.z;
-  // trace slots are indexed by the linear CTA id
   const unsigned long long lin = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
   auto stamp = [&](int slot) {
     if (p.trace) {
@@ -164,15 +167,16 @@ __global__ void __launch_bounds__(64 + 32 * conv_warps<BN>(), 1)
   if (warp == 0 && lane == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&conv[s], NCW);
+      mbar_init(&conv[s], kConvWarps);
       mbar_init(&empty[s], 1);
     }
-    for (int a = 0; a < 2; ++a) {
+    for (int a = 0; a < NACC; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], NCW);
+      mbar_init(&tempty[a], kPromWarps);
     }
     *abort_flag = 0;
     fence_mbar_init();
+    for (int i = 0; i < p.nmaps; ++i) tma_prefetch_desc(&maps.m[i]);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, TMEM_COLS);
@@ -208,19 +212,11 @@ __global__ void __launch_bounds__(64 + 32 * conv_warps<BN>(), 1)
       if (kb < 8) stamp(2 + kb);  // slots 2..9: K block issued
       uint8_t* st = smem + s * STAGE_BYTES;
       for (int i = 0; i < 2; ++i) {
-        if (A.s[i].map >= 0) {
-          const CUtensorMap* m = &maps.m[A.s[i].map];
-#pragma unroll
-          for (int r = 0; r < BM / 32; ++r)
-            tma_load_2d(st + i * A_BYTES + r * 4096, m, &full[s], k0, row0 + mt * BM + 32 * r);
-        }
-        if (B.s[i].map >= 0) {  // rows nt*BN.. of B^T, columns k0..k0+31
-          const CUtensorMap* m = &maps.m[B.s[i].map];
-#pragma unroll
-          for (int c = 0; c < BN / 32; ++c)
-            tma_load_2d(st + 2 * A_BYTES + i * B_BYTES + c * 4096, m, &full[s], k0,
-                        row0 + nt * BN + 32 * c);
-        }
+        if (A.s[i].map >= 0)  // rows mt*128.. of A (one 32 x 128 box)
+          tma_load_2d(st + i * A_BYTES, &maps.m[A.s[i].map], &full[s], k0, row0 + mt * BM);
+        if (B.s[i].map >= 0)  // rows nt*BN.. of B^T, columns k0..k0+31 (one 32 x BN box)
+          tma_load_2d(st + 2 * A_BYTES + i * B_BYTES, &maps.m[B.s[i].map], &full[s], k0,
+                      row0 + nt * BN);
       }
       ++issued;
     }
@@ -232,8 +228,8 @@ __global__ void __launch_bounds__(64 + 32 * conv_warps<BN>(), 1)
     for (int kb = 0; kb < num_kb; ++kb) {
       const int s = kb % STAGES;
       const uint32_t ph = (kb / STAGES) & 1;
-      const int a = kb & 1;
-      const uint32_t pa = (kb >> 1) & 1;
+      const int a = kb % NACC;
+      const uint32_t pa = (kb / NACC) & 1;
       if (*abort_flag || !mbar_wait_bounded(&conv[s], ph, p.err, p.limit_ns) ||
           !mbar_wait_bounded(&tempty[a], pa ^ 1, p.err, p.limit_ns)) {
         *abort_flag = 1;
@@ -258,46 +254,17 @@ __global__ void __launch_bounds__(64 + 32 * conv_warps<BN>(), 1)
       ++done;
     }
     // TMEM is freed after the final barrier: wait until the last MMAs have completed.
-    if (done > 0) mbar_wait_bounded(&tfull[(done - 1) & 1], ((done - 1) >> 1) & 1, p.err, p.limit_ns);
-  } else if (warp >= 2) {
-    // ---------------------------------------------------------------- converter + promotion
+    if (done > 0)
+      mbar_wait_bounded(&tfull[(done - 1) % NACC], ((done - 1) / NACC) & 1, p.err, p.limit_ns);
+  } else if (warp >= 2 && warp < 2 + kConvWarps) {
+    // ---------------------------------------------------------------- converters
     const int ct = threadIdx.x - 64;  // 0..NCT-1
-    const int q = warp & 3;           // TMEM lane quarter of this warp
-    const int h = (warp - 2) >> 2;    // which 32 accumulator columns this warp owns
-    const int r = q * 32 + lane;
-    const int i = mt * BM + r;
-    float acc[32];
-#pragma unroll
-    for (int t = 0; t < 32; ++t) acc[t] = 0.f;
-    bool ok_all = true;
-    // Adds the accumulator of K block kk to the registers and hands the accumulator back.
-    auto promote = [&](int kk) {
-      const int a = kk & 1;
-      const bool ok = ok_all && mbar_wait_bounded(&tfull[a], (kk >> 1) & 1, p.err, p.limit_ns);
-      ok_all = __all_sync(0xffffffffu, ok);
-      if (!ok_all) {
-        *abort_flag = 1;
-        return;
-      }
-      tc_fence_after();
-      {
-        uint32_t v[32];
-        tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(a * BN + h * 32), v);
-        tmem_ld_wait();
-#pragma unroll
-        for (int t = 0; t < 32; ++t) acc[t] += __uint_as_float(v[t]);
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty[a]);
-    };
-    for (int kb = 0; kb < num_kb && ok_all; ++kb) {
+    for (int kb = 0; kb < num_kb; ++kb) {
       const int s = kb % STAGES;
       const uint32_t ph = (kb / STAGES) & 1;
       const bool ok = !*abort_flag && mbar_wait_bounded(&full[s], ph, p.err, p.limit_ns);
       if (!__all_sync(0xffffffffu, ok)) {
         *abort_flag = 1;
-        ok_all = false;
         break;
       }
       const int seg = kb / p.kb_per_seg;
@@ -313,27 +280,56 @@ __global__ void __launch_bounds__(64 + 32 * conv_warps<BN>(), 1)
       float4* b0 = reinterpret_cast<float4*>(st + 2 * A_BYTES);
       float4* b1 = reinterpret_cast<float4*>(st + 2 * A_BYTES + B_BYTES);
       const bool b_two = B.s[1].map >= 0;
-#pragma unroll 4
+#pragma unroll 2
       for (int e = ct; e < (int)(B_BYTES / 16); e += NCT)
         combine_split(b0 + e, b1 + e, B.s[0].coef, B.s[1].coef, b_two);
       fence_async_smem();  // generic-proxy writes -> visible to the tensor cores
       __syncwarp();
       if (lane == 0) mbar_arrive(&conv[s]);
       if (warp == 2 && lane == 0 && kb < 8) stamp(10 + kb);  // slots 10..17: K block converted
-      if (kb >= 1) promote(kb - 1);
-      if (warp == 2 && lane == 0 && kb >= 1 && kb < 9) stamp(18 + kb - 1);  // 18..25: promoted
     }
-    if (ok_all && num_kb > 0) promote(num_kb - 1);
-    // ---------------------------------------------------------------- epilogue
-    if (warp == 2 && lane == 0) stamp(26);  // epilogue start
+  } else if (warp >= 2 + kConvWarps) {
+    // ---------------------------------------------------------------- promotion + epilogue
+    const int q = warp & 3;  // TMEM lane quarter
+    const int r = q * 32 + lane;
+    const int i = mt * BM + r;
+    float acc[BN];
+#pragma unroll
+    for (int t = 0; t < BN; ++t) acc[t] = 0.f;
+    bool ok_all = true;
+    for (int kb = 0; kb < num_kb; ++kb) {
+      const int a = kb % NACC;
+      const bool ok = !*abort_flag &&
+                      mbar_wait_bounded(&tfull[a], (kb / NACC) & 1, p.err, p.limit_ns);
+      ok_all = __all_sync(0xffffffffu, ok);
+      if (!ok_all) {
+        *abort_flag = 1;
+        break;
+      }
+      tc_fence_after();
+#pragma unroll
+      for (int c0 = 0; c0 < BN; c0 += 32) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(a * BN + c0), v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int t = 0; t < 32; ++t) acc[c0 + t] += __uint_as_float(v[t]);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[a]);
+      if (warp == 2 + kConvWarps && lane == 0 && kb < 8) stamp(18 + kb);  // 18..25: promoted
+    }
+    if (warp == 2 + kConvWarps && lane == 0) stamp(26);  // epilogue start
     const long long base = (long long)blk * b * b;
-    if (i < b) {
-      {
-        const int j0 = nt * BN + h * 32;
+    if (ok_all && i < b) {
+#pragma unroll
+      for (int c0 = 0; c0 < BN; c0 += 32) {
+        const int j0 = nt * BN + c0;
         const long long idx0 = base + (long long)i * b + j0;
         float o[32];
 #pragma unroll
-        for (int t = 0; t < 32; ++t) o[t] = acc[t];
+        for (int t = 0; t < 32; ++t) o[t] = acc[c0 + t];
         if (p.E1) {
           const float4* e = reinterpret_cast<const float4*>(p.E1 + idx0);
 #pragma unroll
@@ -412,12 +408,12 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// [nblk*b rows][b cols] fp32 view with 32 x 32 boxes, 128-byte swizzle (per-thread cache of
-// encoded maps keyed by pointer and shape).
-bool make_blk_map(CUtensorMap* m, const float* ptr, int nblk, int b) {
+// [nblk*b rows][b cols] fp32 view with {32, box_rows} boxes, 128-byte swizzle (per-thread
+// cache of encoded maps keyed by pointer, shape and box).
+bool make_blk_map(CUtensorMap* m, const float* ptr, int nblk, int b, int box_rows) {
   struct Entry {
     const float* ptr;
-    int nblk, b, dev;
+    int nblk, b, box_rows, dev;
     CUtensorMap map;
   };
   constexpr int kEntries = 32;
@@ -427,7 +423,8 @@ bool make_blk_map(CUtensorMap* m, const float* ptr, int nblk, int b) {
   cudaGetDevice(&dev);
   for (int i = 0; i < kEntries; ++i) {
     const Entry& e = cache[i];
-    if (e.ptr == ptr && ptr && e.nblk == nblk && e.b == b && e.dev == dev) {
+    if (e.ptr == ptr && ptr && e.nblk == nblk && e.b == b && e.box_rows == box_rows &&
+        e.dev == dev) {
       *m = e.map;
       return true;
     }
@@ -436,7 +433,7 @@ bool make_blk_map(CUtensorMap* m, const float* ptr, int nblk, int b) {
   if (!fn) return false;
   cuuint64_t dims[2] = {(cuuint64_t)b, (cuuint64_t)nblk * b};
   cuuint64_t strides[1] = {(cuuint64_t)b * 4};
-  cuuint32_t box[2] = {32, 32};
+  cuuint32_t box[2] = {32, (cuuint32_t)box_rows};
   cuuint32_t es[2] = {1, 1};
   if (fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(ptr), dims, strides, box, es,
          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -444,7 +441,7 @@ bool make_blk_map(CUtensorMap* m, const float* ptr, int nblk, int b) {
     return false;
   Entry& e = cache[next];
   next = (next + 1) % kEntries;
-  e.ptr = ptr; e.nblk = nblk; e.b = b; e.dev = dev; e.map = *m;
+  e.ptr = ptr; e.nblk = nblk; e.b = b; e.box_rows = box_rows; e.dev = dev; e.map = *m;
   return true;
 }
 
@@ -452,6 +449,7 @@ template <int BN, int STAGES>
 poetx_status launch_t(const CnpMaps& maps, const CnpUParams& p, int nblk, cudaStream_t s) {
   auto k = cnp_umma_kernel<BN, STAGES>;
   constexpr int smem = STAGES * (2 * BM * BK * 4 + 2 * BN * BK * 4) + 1024 + 256;
+  static_assert(smem <= 227 * 1024, "shared memory per CTA exceeds the sm_103 limit");
   static std::once_flag once;
   static cudaError_t attr = cudaSuccess;
   std::call_once(once, [&] {
@@ -459,7 +457,7 @@ poetx_status launch_t(const CnpMaps& maps, const CnpUParams& p, int nblk, cudaSt
   });
   POETX_CUDA_TRY(attr);
   dim3 grid((p.b + BM - 1) / BM, p.b / BN, nblk);
-  k<<<grid, 64 + 32 * conv_warps<BN>(), smem, s>>>(maps, p);
+  k<<<grid, kThreadsCnp, smem, s>>>(maps, p);
   POETX_CUDA_TRY(cudaGetLastError());
   return POETX_OK;
 }
@@ -472,20 +470,25 @@ bool cnp_umma_ok(int b) {
 
 poetx_status cnp_umma_product(const CnpProduct& g, int nblk, cudaStream_t s) {
   if (nblk == 0) return POETX_OK;
+  const int BN = g.b % 64 == 0 ? 64 : 32;
   CnpMaps maps;
   const float* ptrs[NMAPS] = {};
+  int roles[NMAPS] = {};
   int nmaps = 0;
-  auto map_of = [&](const float* ptr) -> int {
+  // role 0: A operand (128-row boxes), role 1: transposed B operand (BN-row boxes)
+  auto map_of = [&](const float* ptr, int role) -> int {
     if (!ptr) return -1;
     for (int i = 0; i < nmaps; ++i)
-      if (ptrs[i] == ptr) return i;
+      if (ptrs[i] == ptr && roles[i] == role) return i;
     if (nmaps == NMAPS) return -2;
-    if (!make_blk_map(&maps.m[nmaps], ptr, nblk, g.b)) return -3;
+    if (!make_blk_map(&maps.m[nmaps], ptr, nblk, g.b, role == 0 ? BM : BN)) return -3;
     ptrs[nmaps] = ptr;
+    roles[nmaps] = role;
     return nmaps++;
   };
   CnpUParams p{};
   p.b = g.b;
+  p.nmaps = nmaps;
   p.nseg = g.nseg;
   p.kb_per_seg = g.b / BK;
   for (int sg = 0; sg < g.nseg; ++sg) {
@@ -494,7 +497,7 @@ poetx_status cnp_umma_product(const CnpProduct& g, int nblk, cudaStream_t s) {
     for (int w = 0; w < 2; ++w) {
       for (int i = 0; i < 2; ++i) {
         const float* ptr = i == 0 ? ts[w]->p1 : ts[w]->p2;
-        const int mi = map_of(ptr);
+        const int mi = map_of(ptr, w);
         if (mi < -1) return mi == -2 ? POETX_ERR_UNSUPPORTED : POETX_ERR_CUDA;
         os[w]->s[i].map = mi;
         os[w]->s[i].coef = i == 0 ? ts[w]->c1 : ts[w]->c2;
@@ -509,7 +512,8 @@ poetx_status cnp_umma_product(const CnpProduct& g, int nblk, cudaStream_t s) {
   p.err = device_error_word();
   p.limit_ns = kWaitLimitNs;
   p.trace = trace_buffer(&p.trace_cap);
-  if (g.b % 64 == 0) return launch_t<64, 4>(maps, p, nblk, s);
+  p.nmaps = nmaps;
+  if (BN == 64) return launch_t<64, 4>(maps, p, nblk, s);
   return launch_t<32, 4>(maps, p, nblk, s);
 }
 

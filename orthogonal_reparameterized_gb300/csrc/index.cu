@@ -237,9 +237,10 @@ static poetx_status launch_perm_rows_t(const void* X, long long N, int D, const 
                                        float* scale_out, cudaStream_t s) {
   const size_t row_bytes = (size_t)D * E;
   const size_t idx_bytes = ((size_t)D * sizeof(IdxT) + 127) & ~(size_t)127;
-  // ring of rows: aim at ~64 KB of rows in flight per CTA, 2..8 buffers, <= 200 KB in total
-  int nbuf = (int)((64 * 1024) / row_bytes);
-  nbuf = nbuf < 2 ? 2 : (nbuf > 8 ? 8 : nbuf);
+  // ring of rows: aim at ~96 KB of rows in flight per CTA (two CTAs per SM keep ~190 KB of
+  // loads outstanding, enough to cover the DRAM latency), 2..32 buffers, <= 200 KB in total
+  int nbuf = (int)((96 * 1024) / row_bytes);
+  nbuf = nbuf < 2 ? 2 : (nbuf > 32 ? 32 : nbuf);
   while (nbuf > 2 && idx_bytes + nbuf * row_bytes + 128 > 200 * 1024) --nbuf;
   const size_t smem = idx_bytes + nbuf * row_bytes + 8 * (size_t)nbuf;
   if (smem > 227 * 1024) return POETX_ERR_SHAPE;
