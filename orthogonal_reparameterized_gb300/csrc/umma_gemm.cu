@@ -140,25 +140,32 @@ __device__ __forceinline__ TileCoords tile_coords(const UmmaParams& p, int t) {
 }
 
 // 8 epilogue warps (2..9): two per TMEM lane quarter, each storing half of the BN columns.
+// With an int8 B operand, 4 more warps (10..13) widen its tiles to bf16 in shared memory.
 constexpr int kEpiWarps = 8;
-constexpr int kThreads = 64 + 32 * kEpiWarps;
+constexpr int kConvWarpsI8 = 4;
+template <bool B_I8>
+constexpr int gemm_threads() { return 64 + 32 * kEpiWarps + (B_I8 ? 32 * kConvWarpsI8 : 0); }
+
+// Bytes of one pipeline stage: A (bf16), B (bf16) and, for an int8 B, its raw int8 tile.
+template <int BN, bool B_I8>
+constexpr int stage_bytes() { return BM * BK * 2 + BN * BK * 2 + (B_I8 ? BN * BK : 0); }
 
 // Columns the epilogue stages per pass: 64, or 32 when the operand ring leaves no room.
-template <int BN, int STAGES, bool OUT_F32>
+template <int BN, int STAGES, bool OUT_F32, bool B_I8>
 constexpr int epi_pass_cols() {
-  constexpr int ring = STAGES * (BM * BK * 2 + BN * BK * 2);
+  constexpr int ring = STAGES * stage_bytes<BN, B_I8>();
   constexpr int esz = OUT_F32 ? 4 : 2;
   constexpr int c = (BN / 2 < 64) ? BN / 2 : 64;
   return ring + kEpiWarps * 32 * (c * esz + 16) + 1280 <= 227 * 1024 ? c : 32;
 }
 
-template <int BN, int STAGES, bool A_MN, bool B_MN, bool OUT_F32>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int BN, int STAGES, bool A_MN, bool B_MN, bool OUT_F32, bool B_I8>
+__global__ void __launch_bounds__(gemm_threads<B_I8>(), 1)
     umma_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmB, const UmmaParams p) {
   constexpr uint32_t A_BYTES = BM * BK * 2;
   constexpr uint32_t B_BYTES = BN * BK * 2;
-  constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+  constexpr uint32_t STAGE_BYTES = stage_bytes<BN, B_I8>();  // int8 tile (if any) after B
   constexpr uint32_t TMEM_COLS = 2 * BN;  // two accumulators
   constexpr uint32_t IDESC = make_idesc(BM, BN, A_MN, B_MN);
 
@@ -168,14 +175,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   // per epilogue warp: 32 rows x 64 columns staging buffer (rows padded by 16 bytes), so
   // that the global stores cover whole row segments instead of 16 bytes of 32 rows each
   constexpr uint32_t ESZ = OUT_F32 ? 4 : 2;
-  constexpr int EPC = epi_pass_cols<BN, STAGES, OUT_F32>();  // columns per epilogue pass
+  constexpr int EPC = epi_pass_cols<BN, STAGES, OUT_F32, B_I8>();  // columns per epilogue pass
   constexpr uint32_t STG_PITCH = EPC * ESZ + 16;
   uint8_t* staging = smem + STAGES * STAGE_BYTES;
   uint64_t* full = reinterpret_cast<uint64_t*>(staging + kEpiWarps * 32 * STG_PITCH);
   uint64_t* empty = full + STAGES;
   uint64_t* tfull = empty + STAGES;  // [2]
   uint64_t* tempty = tfull + 2;      // [2]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  uint64_t* conv = tempty + 2;       // [STAGES] int8 B tile widened (B_I8 only)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(conv + STAGES);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -190,6 +198,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&tfull[a], 1);
       mbar_init(&tempty[a], kEpiWarps);
     }
+    for (int s = 0; s < STAGES; ++s) mbar_init(&conv[s], kConvWarpsI8);
     *abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
@@ -220,10 +229,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        mbar_arrive_expect_tx(&full[s], STAGE_BYTES);
+        mbar_arrive_expect_tx(&full[s], B_I8 ? A_BYTES + BN * BK : STAGE_BYTES);
         if (g == 0) trace_stamp(p.trace, p.trace_cap, 2);  // slot 2: first TMA issued
         uint8_t* sa = smem + s * STAGE_BYTES;
-        uint8_t* sb = sa + A_BYTES;
+        uint8_t* sb = B_I8 ? sa + A_BYTES + B_BYTES : sa + A_BYTES;  // int8: raw tile
         const int k = kb * BK;
         if (!A_MN) {
           tma_load_2d(sa, &tmA, &full[s], c.a_c0 + k, c.a_c1);
@@ -235,9 +244,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!B_MN) {
           tma_load_2d(sb, &tmB, &full[s], c.b_c0 + k, c.b_c1);
         } else {
+          constexpr int BOX_BYTES = B_I8 ? 4096 : 8192;  // 64 x 64 elements
 #pragma unroll
           for (int i = 0; i < BN / 64; ++i)
-            tma_load_2d(sb + i * 8192, &tmB, &full[s], c.b_c0 + 64 * i, c.b_c1 + k);
+            tma_load_2d(sb + i * BOX_BYTES, &tmB, &full[s], c.b_c0 + 64 * i, c.b_c1 + k);
         }
       }
     }
@@ -262,7 +272,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int kb = 0; kb < c.num_kb; ++kb, ++g) {
         const int s = (int)(g % STAGES);
         const uint32_t ph = (uint32_t)((g / STAGES) & 1);
-        if (*abort_flag || !mbar_wait_bounded(&full[s], ph, p.err, p.limit_ns)) {
+        // an int8 B tile is usable once the converter warps have widened it
+        if (*abort_flag || !mbar_wait_bounded(B_I8 ? &conv[s] : &full[s], ph, p.err, p.limit_ns)) {
           *abort_flag = 1;
           ok = false;
           break;
@@ -283,6 +294,46 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (it > 0) {
       const int last = it - 1;
       mbar_wait_bounded(&tfull[last & 1], (last >> 1) & 1, p.err, p.limit_ns);
+    }
+  } else if (B_I8 && warp >= 2 + kEpiWarps) {
+    // ------------------------------------------------------------ int8 -> bf16 converters
+    // Raw tile: BN rows of 64 bytes (K-major: rows = N, K contiguous; MN-major: BN/64 boxes
+    // of 64 K rows x 64 MN bytes).  bf16 tile: the same rows at 128-byte pitch with 16-byte
+    // chunk c of row r stored at chunk c ^ (r % 8) (128-byte swizzle, both majors).
+    // |q| <= 127, so the widening is exact.
+    const int ct = threadIdx.x - 32 * (2 + kEpiWarps);
+    long long g = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+      const TileCoords c = tile_coords<BN, B_MN>(p, t);
+      for (int kb = 0; kb < c.num_kb; ++kb, ++g) {
+        const int s = (int)(g % STAGES);
+        const uint32_t ph = (uint32_t)((g / STAGES) & 1);
+        const bool got = !*abort_flag && mbar_wait_bounded(&full[s], ph, p.err, p.limit_ns);
+        if (!__all_sync(0xffffffffu, got)) {
+          *abort_flag = 1;
+          ok = false;
+          break;
+        }
+        uint8_t* st = smem + s * STAGE_BYTES;
+        const uint8_t* raw = st + A_BYTES + B_BYTES;
+        uint8_t* bt = st + A_BYTES;
+#pragma unroll 4
+        for (int e = ct; e < BN * 8; e += 32 * kConvWarpsI8) {
+          const int r = e >> 3, ch = e & 7;
+          const uint2 w = *reinterpret_cast<const uint2*>(raw + r * 64 + ch * 8);
+          const int8_t* q8 = reinterpret_cast<const int8_t*>(&w);
+          uint4 o;
+          o.x = pack_bf16x2((float)q8[0], (float)q8[1]);
+          o.y = pack_bf16x2((float)q8[2], (float)q8[3]);
+          o.z = pack_bf16x2((float)q8[4], (float)q8[5]);
+          o.w = pack_bf16x2((float)q8[6], (float)q8[7]);
+          *reinterpret_cast<uint4*>(bt + r * 128 + ((ch ^ (r & 7)) << 4)) = o;
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&conv[s]);
+      }
     }
   } else if (warp >= 2) {
     // ------------------------------------------------------------ epilogue
@@ -410,13 +461,13 @@ EncodeTiledFn encode_fn() {
 // 2-D bf16 tensor [outer][inner] with row pitch `pitch_elems`, box {box_inner, box_outer},
 // 128-byte swizzle, zero fill out of bounds.  Encoded maps are kept in a small per-thread
 // cache keyed by every argument, since training loops pass the same buffers every step.
-bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint64_t pitch_elems,
-              uint32_t box_inner, uint32_t box_outer) {
+bool make_map_t(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer,
+                uint64_t pitch_elems, uint32_t box_inner, uint32_t box_outer, bool i8) {
   struct Entry {
     const void* ptr;
     uint64_t inner, outer, pitch;
     uint32_t bi, bo;
-    int dev;
+    int dev, i8;
     CUtensorMap map;
   };
   constexpr int kEntries = 64;
@@ -427,7 +478,7 @@ bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, u
   for (int i = 0; i < kEntries; ++i) {
     const Entry& e = cache[i];
     if (e.ptr == ptr && ptr && e.inner == inner && e.outer == outer && e.pitch == pitch_elems &&
-        e.bi == box_inner && e.bo == box_outer && e.dev == dev) {
+        e.bi == box_inner && e.bo == box_outer && e.dev == dev && e.i8 == (int)i8) {
       *m = e.map;
       return true;
     }
@@ -435,30 +486,36 @@ bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, u
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {inner, outer};
-  cuuint64_t strides[1] = {pitch_elems * 2};
+  cuuint64_t strides[1] = {pitch_elems * (i8 ? 1 : 2)};
   cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t es[2] = {1, 1};
-  if (fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
-         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+  if (fn(m, i8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+         const_cast<void*>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+         i8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return false;
   Entry& e = cache[next];
   next = (next + 1) % kEntries;
   e.ptr = ptr; e.inner = inner; e.outer = outer; e.pitch = pitch_elems;
-  e.bi = box_inner; e.bo = box_outer; e.dev = dev; e.map = *m;
+  e.bi = box_inner; e.bo = box_outer; e.dev = dev; e.i8 = (int)i8; e.map = *m;
   return true;
 }
 
-template <int BN, int STAGES, bool A_MN, bool B_MN, bool OUT_F32>
+// 2-D bf16 tensor [outer][inner] with row pitch `pitch_elems`, box {box_inner, box_outer},
+// 128-byte swizzle, zero fill out of bounds (encoded maps are cached per thread).
+bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint64_t pitch_elems,
+              uint32_t box_inner, uint32_t box_outer) {
+  return make_map_t(m, ptr, inner, outer, pitch_elems, box_inner, box_outer, false);
+}
+
+template <int BN, int STAGES, bool A_MN, bool B_MN, bool OUT_F32, bool B_I8 = false>
 poetx_status launch(const CUtensorMap& ta, const CUtensorMap& tb, UmmaParams p, int tiles_m,
                     int tiles_n, int tiles_z, cudaStream_t s) {
   const int stage = p.mode == MODE_PLAIN ? ST_WPRIME : (p.mode == MODE_BLOCKDIAG ? ST_BLOCKDIAG : ST_WGRAD);
-  auto k = umma_gemm_kernel<BN, STAGES, A_MN, B_MN, OUT_F32>;
-  constexpr int smem = STAGES * (BM * BK * 2 + BN * BK * 2) +
-                       kEpiWarps * 32 * (epi_pass_cols<BN, STAGES, OUT_F32>() * (OUT_F32 ? 4 : 2) + 16) +
-                       1024 + 256;
-  // TMEM holds 512 columns per SM: 2 x BN columns per CTA bound the CTAs per SM, and the
-  // shared memory of every configuration is sized so that no more than that many fit.
+  auto k = umma_gemm_kernel<BN, STAGES, A_MN, B_MN, OUT_F32, B_I8>;
+  constexpr int smem = STAGES * stage_bytes<BN, B_I8>() +
+                       kEpiWarps * 32 * (epi_pass_cols<BN, STAGES, OUT_F32, B_I8>() * (OUT_F32 ? 4 : 2) + 16) +
+                       1024 + 512;
   // CTAs per SM: bounded by TMEM (2 x BN columns each, 512 per SM) and shared memory.
   constexpr int by_tmem = 512 / (2 * BN);
   constexpr int by_smem = (int)((227 * 1024) / (smem + 1024));
@@ -479,7 +536,7 @@ poetx_status launch(const CUtensorMap& ta, const CUtensorMap& tb, UmmaParams p, 
   p.num_tiles = (int)tiles;
   const long long want = (long long)sm_count() * per_sm;
   const int grid = (int)(tiles < want ? tiles : want);
-  k<<<grid, kThreads, smem, s>>>(ta, tb, p);
+  k<<<grid, gemm_threads<B_I8>(), smem, s>>>(ta, tb, p);
   POETX_CUDA_TRY(cudaGetLastError());
   after_launch(s, stage);
   return POETX_OK;
@@ -547,28 +604,31 @@ poetx_status umma_blockdiag(const void* X, long long N, int nblk, int b, const v
   return launch<128, 5, false, true, false>(ta, tb, p, tm, tn, nblk, s);
 }
 
-poetx_status umma_wprime(const void* A, long long N, int m, int n, const void* W,
+poetx_status umma_wprime(const void* A, long long N, int m, int n, const void* W, bool w_i8,
                          const float* w_scale, int trans, void* C, cudaStream_t s) {
   if (N == 0) return POETX_OK;
   CUtensorMap ta, tb;
   UmmaParams p = base_params();
   p.mode = MODE_PLAIN;
   p.M = (int)N;
-  p.colscale = w_scale;
+  p.colscale = (w_i8 && !trans) ? w_scale : nullptr;  // int8 forward: C[:, r] *= s_r
   p.C = C;
+  const int tm = (int)((N + BM - 1) / BM);
   if (!trans) {  // C[N,n] = A[N,m] W^T
     if (!make_map(&ta, A, m, N, m, 64, 128)) return POETX_ERR_CUDA;
-    if (!make_map(&tb, W, m, n, m, 64, 256)) return POETX_ERR_CUDA;
+    if (!make_map_t(&tb, W, m, n, m, 64, 256, w_i8)) return POETX_ERR_CUDA;
     p.num_kb = m / 64;
     p.ldc = n;
-    return launch<256, 4, false, false, false>(ta, tb, p, (int)((N + BM - 1) / BM), n / 256, 1, s);
+    if (w_i8) return launch<256, 3, false, false, false, true>(ta, tb, p, tm, n / 256, 1, s);
+    return launch<256, 4, false, false, false>(ta, tb, p, tm, n / 256, 1, s);
   }
   // C[N,m] = A[N,n] W: B operand (output col c, K index r) = W[r][c], MN-major
   if (!make_map(&ta, A, n, N, n, 64, 128)) return POETX_ERR_CUDA;
-  if (!make_map(&tb, W, m, n, m, 64, 64)) return POETX_ERR_CUDA;
+  if (!make_map_t(&tb, W, m, n, m, 64, 64, w_i8)) return POETX_ERR_CUDA;
   p.num_kb = n / 64;
   p.ldc = m;
-  return launch<256, 4, false, true, false>(ta, tb, p, (int)((N + BM - 1) / BM), m / 256, 1, s);
+  if (w_i8) return launch<256, 3, false, true, false, true>(ta, tb, p, tm, m / 256, 1, s);
+  return launch<256, 4, false, true, false>(ta, tb, p, tm, m / 256, 1, s);
 }
 
 poetx_status umma_wgrad(const void* X, const void* dY, long long N, int nblk, int b, int splits,

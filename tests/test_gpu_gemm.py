@@ -96,7 +96,7 @@ def test_wprime_bf16(P, engine, N, m, n, trans):
 
 
 @pytest.mark.parametrize("trans", [False, True])
-def test_wprime_int8(P, trans):
+def test_wprime_int8(P, engine, trans):
     N, m, n = 300, 512, 768
     Wq = torch.randint(-127, 128, (n, m), dtype=torch.int8, device=DEV)
     s = (torch.rand(n, device=DEV) + 0.5) / 127
