@@ -159,6 +159,19 @@ constexpr int epi_pass_cols() {
   return ring + kEpiWarps * 32 * (c * esz + 16) + 1280 <= 227 * 1024 ? c : 32;
 }
 
+// Two signed bytes of w (bytes lo, lo+1) -> two bf16 in one word, exactly and on the full-rate
+// ALU: the byte biased by 128 goes under the exponent of 2^23 (byte_perm), one FADD removes
+// 2^23 + 128, and the upper halves of the two floats are the bf16 values (an integer of
+// magnitude < 256 has at most 8 significant bits).
+__device__ __forceinline__ uint32_t i8x2_to_bf16x2(uint32_t w, int lo) {
+  const uint32_t u = w ^ 0x80808080u;                       // bias: q + 128 as unsigned bytes
+  const uint32_t sel0 = lo == 0 ? 0x7540u : 0x7542u;        // [byte lo, 0, 0, 0x4B]
+  const uint32_t sel1 = lo == 0 ? 0x7541u : 0x7543u;        // [byte lo+1, 0, 0, 0x4B]
+  const float f0 = __uint_as_float(__byte_perm(u, 0x4B000000u, sel0)) - 8388736.0f;
+  const float f1 = __uint_as_float(__byte_perm(u, 0x4B000000u, sel1)) - 8388736.0f;
+  return __byte_perm(__float_as_uint(f0), __float_as_uint(f1), 0x7632u);
+}
+
 template <int BN, int STAGES, bool A_MN, bool B_MN, bool OUT_F32, bool B_I8>
 __global__ void __launch_bounds__(gemm_threads<B_I8>(), 1)
     umma_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
@@ -322,12 +335,11 @@ __global__ void __launch_bounds__(gemm_threads<B_I8>(), 1)
         for (int e = ct; e < BN * 8; e += 32 * kConvWarpsI8) {
           const int r = e >> 3, ch = e & 7;
           const uint2 w = *reinterpret_cast<const uint2*>(raw + r * 64 + ch * 8);
-          const int8_t* q8 = reinterpret_cast<const int8_t*>(&w);
           uint4 o;
-          o.x = pack_bf16x2((float)q8[0], (float)q8[1]);
-          o.y = pack_bf16x2((float)q8[2], (float)q8[3]);
-          o.z = pack_bf16x2((float)q8[4], (float)q8[5]);
-          o.w = pack_bf16x2((float)q8[6], (float)q8[7]);
+          o.x = i8x2_to_bf16x2(w.x, 0);
+          o.y = i8x2_to_bf16x2(w.x, 2);
+          o.z = i8x2_to_bf16x2(w.y, 0);
+          o.w = i8x2_to_bf16x2(w.y, 2);
           *reinterpret_cast<uint4*>(bt + r * 128 + ((ch ^ (r & 7)) << 4)) = o;
         }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
