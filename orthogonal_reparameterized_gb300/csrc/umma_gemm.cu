@@ -141,10 +141,13 @@ __device__ __forceinline__ TileCoords tile_coords(const UmmaParams& p, int t) {
 
 // 8 epilogue warps (2..9): two per TMEM lane quarter, each storing half of the BN columns.
 // With an int8 B operand, 4 more warps (10..13) widen its tiles to bf16 in shared memory.
-constexpr int kEpiWarps = 8;
-constexpr int kConvWarpsI8 = 4;
+// (int8 B: 4 epilogue warps, one per lane quarter, and 8 converter warps instead.)
 template <bool B_I8>
-constexpr int gemm_threads() { return 64 + 32 * kEpiWarps + (B_I8 ? 32 * kConvWarpsI8 : 0); }
+constexpr int epi_warps() { return B_I8 ? 4 : 8; }
+template <bool B_I8>
+constexpr int conv_warps() { return B_I8 ? 8 : 0; }
+template <bool B_I8>
+constexpr int gemm_threads() { return 64 + 32 * (epi_warps<B_I8>() + conv_warps<B_I8>()); }
 
 // Bytes of one pipeline stage: A (bf16), B (bf16) and, for an int8 B, its raw int8 tile.
 template <int BN, bool B_I8>
@@ -155,8 +158,9 @@ template <int BN, int STAGES, bool OUT_F32, bool B_I8>
 constexpr int epi_pass_cols() {
   constexpr int ring = STAGES * stage_bytes<BN, B_I8>();
   constexpr int esz = OUT_F32 ? 4 : 2;
-  constexpr int c = (BN / 2 < 64) ? BN / 2 : 64;
-  return ring + kEpiWarps * 32 * (c * esz + 16) + 1280 <= 227 * 1024 ? c : 32;
+  constexpr int wc = BN / (epi_warps<B_I8>() / 4);
+  constexpr int c = (wc < 64) ? wc : 64;
+  return ring + epi_warps<B_I8>() * 32 * (c * esz + 16) + 1280 <= 227 * 1024 ? c : 32;
 }
 
 // Two signed bytes of w (bytes lo, lo+1) -> two bf16 in one word, exactly and on the full-rate
@@ -190,8 +194,10 @@ __global__ void __launch_bounds__(gemm_threads<B_I8>(), 1)
   constexpr uint32_t ESZ = OUT_F32 ? 4 : 2;
   constexpr int EPC = epi_pass_cols<BN, STAGES, OUT_F32, B_I8>();  // columns per epilogue pass
   constexpr uint32_t STG_PITCH = EPC * ESZ + 16;
-  uint8_t* staging = smem + STAGES * STAGE_BYTES;
-  uint64_t* full = reinterpret_cast<uint64_t*>(staging + kEpiWarps * 32 * STG_PITCH);
+  uint8_t* staging = smem + STAGES * STAGE_BYTES;  // EPIW buffers
+  constexpr int EPIW = epi_warps<B_I8>();
+  constexpr int CONVW = conv_warps<B_I8>();
+  uint64_t* full = reinterpret_cast<uint64_t*>(staging + EPIW * 32 * STG_PITCH);
   uint64_t* empty = full + STAGES;
   uint64_t* tfull = empty + STAGES;  // [2]
   uint64_t* tempty = tfull + 2;      // [2]
@@ -209,9 +215,9 @@ __global__ void __launch_bounds__(gemm_threads<B_I8>(), 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], kEpiWarps);
+      mbar_init(&tempty[a], EPIW);
     }
-    for (int s = 0; s < STAGES; ++s) mbar_init(&conv[s], kConvWarpsI8);
+    for (int s = 0; s < STAGES; ++s) mbar_init(&conv[s], CONVW > 0 ? CONVW : 1);
     *abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
@@ -308,13 +314,13 @@ __global__ void __launch_bounds__(gemm_threads<B_I8>(), 1)
       const int last = it - 1;
       mbar_wait_bounded(&tfull[last & 1], (last >> 1) & 1, p.err, p.limit_ns);
     }
-  } else if (B_I8 && warp >= 2 + kEpiWarps) {
+  } else if (B_I8 && warp >= 2 + EPIW) {
     // ------------------------------------------------------------ int8 -> bf16 converters
     // Raw tile: BN rows of 64 bytes (K-major: rows = N, K contiguous; MN-major: BN/64 boxes
     // of 64 K rows x 64 MN bytes).  bf16 tile: the same rows at 128-byte pitch with 16-byte
     // chunk c of row r stored at chunk c ^ (r % 8) (128-byte swizzle, both majors).
     // |q| <= 127, so the widening is exact.
-    const int ct = threadIdx.x - 32 * (2 + kEpiWarps);
+    const int ct = threadIdx.x - 32 * (2 + EPIW);
     long long g = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
@@ -331,16 +337,22 @@ __global__ void __launch_bounds__(gemm_threads<B_I8>(), 1)
         uint8_t* st = smem + s * STAGE_BYTES;
         const uint8_t* raw = st + A_BYTES + B_BYTES;
         uint8_t* bt = st + A_BYTES;
-#pragma unroll 4
-        for (int e = ct; e < BN * 8; e += 32 * kConvWarpsI8) {
-          const int r = e >> 3, ch = e & 7;
-          const uint2 w = *reinterpret_cast<const uint2*>(raw + r * 64 + ch * 8);
-          uint4 o;
-          o.x = i8x2_to_bf16x2(w.x, 0);
-          o.y = i8x2_to_bf16x2(w.x, 2);
-          o.z = i8x2_to_bf16x2(w.y, 0);
-          o.w = i8x2_to_bf16x2(w.y, 2);
-          *reinterpret_cast<uint4*>(bt + r * 128 + ((ch ^ (r & 7)) << 4)) = o;
+#pragma unroll 2
+        for (int e = ct; e < BN * 4; e += 32 * CONVW) {  // 16 raw bytes = two bf16 chunks
+          const int r = e >> 2, ch = (e & 3) * 2;
+          const uint4 w = *reinterpret_cast<const uint4*>(raw + r * 64 + ch * 8);
+          uint4 o0, o1;
+          o0.x = i8x2_to_bf16x2(w.x, 0);
+          o0.y = i8x2_to_bf16x2(w.x, 2);
+          o0.z = i8x2_to_bf16x2(w.y, 0);
+          o0.w = i8x2_to_bf16x2(w.y, 2);
+          o1.x = i8x2_to_bf16x2(w.z, 0);
+          o1.y = i8x2_to_bf16x2(w.z, 2);
+          o1.z = i8x2_to_bf16x2(w.w, 0);
+          o1.w = i8x2_to_bf16x2(w.w, 2);
+          uint8_t* rowp = bt + r * 128;
+          *reinterpret_cast<uint4*>(rowp + ((ch ^ (r & 7)) << 4)) = o0;
+          *reinterpret_cast<uint4*>(rowp + (((ch + 1) ^ (r & 7)) << 4)) = o1;
         }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
@@ -350,7 +362,8 @@ __global__ void __launch_bounds__(gemm_threads<B_I8>(), 1)
   } else if (warp >= 2) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;                   // TMEM lane quarter = output rows
-    const int cbeg = ((warp - 2) >> 2) * (BN / 2);  // this warp's half of the columns
+    constexpr int WCOLS = BN / (EPIW / 4);    // columns handled by this warp
+    const int cbeg = ((warp - 2) >> 2) * WCOLS;
     const int row = q * 32 + lane;
     int it = 0;
     for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++it) {
@@ -366,7 +379,7 @@ __global__ void __launch_bounds__(gemm_threads<B_I8>(), 1)
       uint8_t* stg = staging + (warp - 2) * 32 * STG_PITCH;
       const long long row0 = c.out_row0 + q * 32;  // first output row of this warp
 #pragma unroll 1
-      for (int c0 = cbeg; c0 < cbeg + BN / 2; c0 += EPC) {
+      for (int c0 = cbeg; c0 < cbeg + WCOLS; c0 += EPC) {
         // one or two 32-column TMEM loads, one wait
         uint32_t r[64];
         if (c.num_kb > 0) {
@@ -526,7 +539,7 @@ poetx_status launch(const CUtensorMap& ta, const CUtensorMap& tb, UmmaParams p, 
   const int stage = p.mode == MODE_PLAIN ? ST_WPRIME : (p.mode == MODE_BLOCKDIAG ? ST_BLOCKDIAG : ST_WGRAD);
   auto k = umma_gemm_kernel<BN, STAGES, A_MN, B_MN, OUT_F32, B_I8>;
   constexpr int smem = STAGES * stage_bytes<BN, B_I8>() +
-                       kEpiWarps * 32 * (epi_pass_cols<BN, STAGES, OUT_F32, B_I8>() * (OUT_F32 ? 4 : 2) + 16) +
+                       epi_warps<B_I8>() * 32 * (epi_pass_cols<BN, STAGES, OUT_F32, B_I8>() * (OUT_F32 ? 4 : 2) + 16) +
                        1024 + 512;
   // CTAs per SM: bounded by TMEM (2 x BN columns each, 512 per SM) and shared memory.
   constexpr int by_tmem = 512 / (2 * BN);
