@@ -149,14 +149,19 @@ constexpr int conv_warps() { return B_I8 ? 8 : 0; }
 template <bool B_I8>
 constexpr int gemm_threads() { return 64 + 32 * (epi_warps<B_I8>() + conv_warps<B_I8>()); }
 
-// Bytes of one pipeline stage: A (bf16), B (bf16) and, for an int8 B, its raw int8 tile.
-template <int BN, bool B_I8>
-constexpr int stage_bytes() { return BM * BK * 2 + BN * BK * 2 + (B_I8 ? BN * BK : 0); }
+// Bytes of one pipeline stage: A (bf16), B (bf16; absent when B is resident) and, for an
+// int8 B, its raw int8 tile.  RES > 0: B is a resident panel of RES 64-wide K blocks.
+template <int BN, bool B_I8, int RES>
+constexpr int stage_bytes() {
+  return BM * BK * 2 + (RES > 0 ? 0 : BN * BK * 2) + (B_I8 ? BN * BK : 0);
+}
+template <int BN, int RES>
+constexpr int res_bytes() { return RES * BN * BK * 2; }
 
 // Columns the epilogue stages per pass: 64, or 32 when the operand ring leaves no room.
-template <int BN, int STAGES, bool OUT_F32, bool B_I8>
+template <int BN, int STAGES, bool OUT_F32, bool B_I8, int RES>
 constexpr int epi_pass_cols() {
-  constexpr int ring = STAGES * stage_bytes<BN, B_I8>();
+  constexpr int ring = STAGES * stage_bytes<BN, B_I8, RES>() + res_bytes<BN, RES>();
   constexpr int esz = OUT_F32 ? 4 : 2;
   constexpr int wc = BN / (epi_warps<B_I8>() / 4);
   constexpr int c = (wc < 64) ? wc : 64;
@@ -176,13 +181,17 @@ __device__ __forceinline__ uint32_t i8x2_to_bf16x2(uint32_t w, int lo) {
   return __byte_perm(__float_as_uint(f0), __float_as_uint(f1), 0x7632u);
 }
 
-template <int BN, int STAGES, bool A_MN, bool B_MN, bool OUT_F32, bool B_I8>
+// RES > 0 (block-diagonal products): each CTA walks a contiguous range of tiles and keeps the
+// B panel of the current (block, column tile) resident in shared memory, so that the ring
+// carries only the streamed A tiles; the panel is reloaded when the range crosses into the
+// next block (guarded by its own full / empty barriers).
+template <int BN, int STAGES, bool A_MN, bool B_MN, bool OUT_F32, bool B_I8, int RES>
 __global__ void __launch_bounds__(gemm_threads<B_I8>(), 1)
     umma_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmB, const UmmaParams p) {
   constexpr uint32_t A_BYTES = BM * BK * 2;
   constexpr uint32_t B_BYTES = BN * BK * 2;
-  constexpr uint32_t STAGE_BYTES = stage_bytes<BN, B_I8>();  // int8 tile (if any) after B
+  constexpr uint32_t STAGE_BYTES = stage_bytes<BN, B_I8, RES>();  // int8 tile (if any) after B
   constexpr uint32_t TMEM_COLS = 2 * BN;  // two accumulators
   constexpr uint32_t IDESC = make_idesc(BM, BN, A_MN, B_MN);
 
@@ -192,9 +201,10 @@ __global__ void __launch_bounds__(gemm_threads<B_I8>(), 1)
   // per epilogue warp: 32 rows x 64 columns staging buffer (rows padded by 16 bytes), so
   // that the global stores cover whole row segments instead of 16 bytes of 32 rows each
   constexpr uint32_t ESZ = OUT_F32 ? 4 : 2;
-  constexpr int EPC = epi_pass_cols<BN, STAGES, OUT_F32, B_I8>();  // columns per epilogue pass
+  constexpr int EPC = epi_pass_cols<BN, STAGES, OUT_F32, B_I8, RES>();  // columns per epilogue pass
   constexpr uint32_t STG_PITCH = EPC * ESZ + 16;
-  uint8_t* staging = smem + STAGES * STAGE_BYTES;  // EPIW buffers
+  uint8_t* resb = smem + STAGES * STAGE_BYTES;            // resident B panel (RES > 0)
+  uint8_t* staging = resb + res_bytes<BN, RES>();         // EPIW buffers
   constexpr int EPIW = epi_warps<B_I8>();
   constexpr int CONVW = conv_warps<B_I8>();
   uint64_t* full = reinterpret_cast<uint64_t*>(staging + EPIW * 32 * STG_PITCH);
@@ -202,7 +212,9 @@ __global__ void __launch_bounds__(gemm_threads<B_I8>(), 1)
   uint64_t* tfull = empty + STAGES;  // [2]
   uint64_t* tempty = tfull + 2;      // [2]
   uint64_t* conv = tempty + 2;       // [STAGES] int8 B tile widened (B_I8 only)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(conv + STAGES);
+  uint64_t* rfull = conv + STAGES;   // resident B panel loaded (RES > 0)
+  uint64_t* rempty = rfull + 1;      // resident B panel no longer read by MMAs (RES > 0)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(rempty + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -218,6 +230,8 @@ __global__ void __launch_bounds__(gemm_threads<B_I8>(), 1)
       mbar_init(&tempty[a], EPIW);
     }
     for (int s = 0; s < STAGES; ++s) mbar_init(&conv[s], CONVW > 0 ? CONVW : 1);
+    mbar_init(rfull, 1);
+    mbar_init(rempty, 1);
     *abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
@@ -233,13 +247,45 @@ __global__ void __launch_bounds__(gemm_threads<B_I8>(), 1)
   const uint32_t tmem_base = *tmem_slot;
   const uint32_t smem_base = smem_u32(smem);
   if (threadIdx.x == 0) trace_stamp(p.trace, p.trace_cap, 1);  // slot 1: set-up done
+  // tiles of this CTA: strided (t = blockIdx.x, + gridDim.x, ...) or, with a resident B
+  // panel, one contiguous range
+  const int t_first = RES > 0 ? (int)((long long)blockIdx.x * p.num_tiles / gridDim.x) : (int)blockIdx.x;
+  const int t_end = RES > 0 ? (int)((long long)(blockIdx.x + 1) * p.num_tiles / gridDim.x) : p.num_tiles;
+  const int t_step = RES > 0 ? 1 : (int)gridDim.x;
+  auto panel_key = [](const TileCoords& c) -> long long {
+    return ((long long)c.b_c0 << 32) | (unsigned)c.b_c1;
+  };
 
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------ TMA producer
     long long g = 0;  // k blocks issued by this CTA (ring position)
     bool ok = true;
-    for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+    long long cur_key = -1;
+    int npanels = 0;
+    for (int t = t_first; t < t_end && ok; t += t_step) {
       const TileCoords c = tile_coords<BN, B_MN>(p, t);
+      if (RES > 0 && panel_key(c) != cur_key) {
+        // the previous panel must be free (all MMAs that read it completed) before reloading
+        if (npanels > 0 &&
+            (*abort_flag || !mbar_wait_bounded(rempty, (npanels - 1) & 1, p.err, p.limit_ns))) {
+          *abort_flag = 1;
+          break;
+        }
+        mbar_arrive_expect_tx(rfull, RES * B_BYTES);
+#pragma unroll 1
+        for (int kb = 0; kb < RES; ++kb) {
+          uint8_t* dst = resb + kb * B_BYTES;
+          if (!B_MN) {
+            tma_load_2d(dst, &tmB, rfull, c.b_c0 + kb * BK, c.b_c1);
+          } else {
+#pragma unroll
+            for (int i = 0; i < BN / 64; ++i)
+              tma_load_2d(dst + i * 8192, &tmB, rfull, c.b_c0 + 64 * i, c.b_c1 + kb * BK);
+          }
+        }
+        cur_key = panel_key(c);
+        ++npanels;
+      }
       for (int kb = 0; kb < c.num_kb; ++kb, ++g) {
         const int s = (int)(g % STAGES);
         const uint32_t ph = (uint32_t)((g / STAGES) & 1);
@@ -248,7 +294,7 @@ __global__ void __launch_bounds__(gemm_threads<B_I8>(), 1)
           ok = false;
           break;
         }
-        mbar_arrive_expect_tx(&full[s], B_I8 ? A_BYTES + BN * BK : STAGE_BYTES);
+        mbar_arrive_expect_tx(&full[s], B_I8 ? A_BYTES + BN * BK : (RES > 0 ? A_BYTES : STAGE_BYTES));
         if (g == 0) trace_stamp(p.trace, p.trace_cap, 2);  // slot 2: first TMA issued
         uint8_t* sa = smem + s * STAGE_BYTES;
         uint8_t* sb = B_I8 ? sa + A_BYTES + B_BYTES : sa + A_BYTES;  // int8: raw tile
@@ -260,16 +306,20 @@ __global__ void __launch_bounds__(gemm_threads<B_I8>(), 1)
           for (int i = 0; i < BM / 64; ++i)
             tma_load_2d(sa + i * 8192, &tmA, &full[s], c.a_c0 + 64 * i, c.a_c1 + k);
         }
-        if (!B_MN) {
-          tma_load_2d(sb, &tmB, &full[s], c.b_c0 + k, c.b_c1);
-        } else {
-          constexpr int BOX_BYTES = B_I8 ? 4096 : 8192;  // 64 x 64 elements
+        if (RES == 0) {
+          if (!B_MN) {
+            tma_load_2d(sb, &tmB, &full[s], c.b_c0 + k, c.b_c1);
+          } else {
+            constexpr int BOX_BYTES = B_I8 ? 4096 : 8192;  // 64 x 64 elements
 #pragma unroll
-          for (int i = 0; i < BN / 64; ++i)
-            tma_load_2d(sb + i * BOX_BYTES, &tmB, &full[s], c.b_c0 + 64 * i, c.b_c1 + k);
+            for (int i = 0; i < BN / 64; ++i)
+              tma_load_2d(sb + i * BOX_BYTES, &tmB, &full[s], c.b_c0 + 64 * i, c.b_c1 + k);
+          }
         }
       }
     }
+    // a resident panel still loading must land before the CTA may exit
+    if (RES > 0 && npanels > 0) mbar_wait_bounded(rfull, (npanels - 1) & 1, p.err, p.limit_ns);
     // Drain: wait for the last load issued into every stage (already complete in the normal
     // path), so that no copy is in flight when the CTA exits.
     for (long long j = g - 1; j >= 0 && j >= g - STAGES; --j)
@@ -279,12 +329,23 @@ __global__ void __launch_bounds__(gemm_threads<B_I8>(), 1)
     long long g = 0;
     int it = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x, ++it) {
+    long long cur_key = -1;
+    int npanels = 0;
+    for (int t = t_first; t < t_end && ok; t += t_step, ++it) {
       const TileCoords c = tile_coords<BN, B_MN>(p, t);
       const int a = it & 1;
       if (*abort_flag || !mbar_wait_bounded(&tempty[a], ((it >> 1) & 1) ^ 1, p.err, p.limit_ns)) {
         *abort_flag = 1;
         break;
+      }
+      if (RES > 0 && panel_key(c) != cur_key) {
+        if (npanels > 0) umma_commit(rempty);  // the old panel is free once these MMAs finish
+        if (*abort_flag || !mbar_wait_bounded(rfull, npanels & 1, p.err, p.limit_ns)) {
+          *abort_flag = 1;
+          break;
+        }
+        cur_key = panel_key(c);
+        ++npanels;
       }
       tc_fence_after();
       const uint32_t d = tmem_base + (uint32_t)(a * BN);
@@ -300,7 +361,7 @@ __global__ void __launch_bounds__(gemm_threads<B_I8>(), 1)
         tc_fence_after();
         if (g == 0) trace_stamp(p.trace, p.trace_cap, 3);  // slot 3: first stage landed
         const uint32_t a_base = smem_base + s * STAGE_BYTES;
-        const uint32_t b_base = a_base + A_BYTES;
+        const uint32_t b_base = RES > 0 ? smem_u32(resb) + kb * B_BYTES : a_base + A_BYTES;
 #pragma unroll
         for (int k = 0; k < BK / 16; ++k)
           umma_bf16(d, tile_desc<A_MN>(a_base, k), tile_desc<B_MN>(b_base, k), IDESC,
@@ -323,7 +384,7 @@ __global__ void __launch_bounds__(gemm_threads<B_I8>(), 1)
     const int ct = threadIdx.x - 32 * (2 + EPIW);
     long long g = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+    for (int t = t_first; t < t_end && ok; t += t_step) {
       const TileCoords c = tile_coords<BN, B_MN>(p, t);
       for (int kb = 0; kb < c.num_kb; ++kb, ++g) {
         const int s = (int)(g % STAGES);
@@ -366,7 +427,7 @@ __global__ void __launch_bounds__(gemm_threads<B_I8>(), 1)
     const int cbeg = ((warp - 2) >> 2) * WCOLS;
     const int row = q * 32 + lane;
     int it = 0;
-    for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++it) {
+    for (int t = t_first; t < t_end; t += t_step, ++it) {
       const TileCoords c = tile_coords<BN, B_MN>(p, t);
       const int a = it & 1;
       const bool ok = !*abort_flag && mbar_wait_bounded(&tfull[a], (it >> 1) & 1, p.err, p.limit_ns);
@@ -533,13 +594,14 @@ bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, u
   return make_map_t(m, ptr, inner, outer, pitch_elems, box_inner, box_outer, false);
 }
 
-template <int BN, int STAGES, bool A_MN, bool B_MN, bool OUT_F32, bool B_I8 = false>
+template <int BN, int STAGES, bool A_MN, bool B_MN, bool OUT_F32, bool B_I8 = false, int RES = 0>
 poetx_status launch(const CUtensorMap& ta, const CUtensorMap& tb, UmmaParams p, int tiles_m,
                     int tiles_n, int tiles_z, cudaStream_t s) {
   const int stage = p.mode == MODE_PLAIN ? ST_WPRIME : (p.mode == MODE_BLOCKDIAG ? ST_BLOCKDIAG : ST_WGRAD);
-  auto k = umma_gemm_kernel<BN, STAGES, A_MN, B_MN, OUT_F32, B_I8>;
-  constexpr int smem = STAGES * stage_bytes<BN, B_I8>() +
-                       epi_warps<B_I8>() * 32 * (epi_pass_cols<BN, STAGES, OUT_F32, B_I8>() * (OUT_F32 ? 4 : 2) + 16) +
+  auto k = umma_gemm_kernel<BN, STAGES, A_MN, B_MN, OUT_F32, B_I8, RES>;
+  constexpr int smem = STAGES * stage_bytes<BN, B_I8, RES>() + res_bytes<BN, RES>() +
+                       epi_warps<B_I8>() * 32 *
+                           (epi_pass_cols<BN, STAGES, OUT_F32, B_I8, RES>() * (OUT_F32 ? 4 : 2) + 16) +
                        1024 + 512;
   // CTAs per SM: bounded by TMEM (2 x BN columns each, 512 per SM) and shared memory.
   constexpr int by_tmem = 512 / (2 * BN);
@@ -621,12 +683,21 @@ poetx_status umma_blockdiag(const void* X, long long N, int nblk, int b, const v
   p.colscale = col_scale;
   p.out_perm = out_perm;
   const int tm = (int)((N + BM - 1) / BM), tn = b / BN;
+  // resident G panel of b/64 K blocks; the ring carries only the activation tiles
   if (trans) {
-    if (BN == 64) return launch<64, 7, false, false, false>(ta, tb, p, tm, tn, nblk, s);
-    return launch<128, 5, false, false, false>(ta, tb, p, tm, tn, nblk, s);
+    switch (b) {
+      case 64: return launch<64, 10, false, false, false, false, 1>(ta, tb, p, tm, tn, nblk, s);
+      case 128: return launch<128, 10, false, false, false, false, 2>(ta, tb, p, tm, tn, nblk, s);
+      case 256: return launch<128, 8, false, false, false, false, 4>(ta, tb, p, tm, tn, nblk, s);
+      default: return launch<128, 4, false, false, false, false, 8>(ta, tb, p, tm, tn, nblk, s);
+    }
   }
-  if (BN == 64) return launch<64, 7, false, true, false>(ta, tb, p, tm, tn, nblk, s);
-  return launch<128, 5, false, true, false>(ta, tb, p, tm, tn, nblk, s);
+  switch (b) {
+    case 64: return launch<64, 10, false, true, false, false, 1>(ta, tb, p, tm, tn, nblk, s);
+    case 128: return launch<128, 10, false, true, false, false, 2>(ta, tb, p, tm, tn, nblk, s);
+    case 256: return launch<128, 8, false, true, false, false, 4>(ta, tb, p, tm, tn, nblk, s);
+    default: return launch<128, 4, false, true, false, false, 8>(ta, tb, p, tm, tn, nblk, s);
+  }
 }
 
 poetx_status umma_wprime(const void* A, long long N, int m, int n, const void* W, bool w_i8,
