@@ -46,6 +46,8 @@ __device__ __forceinline__ float op_load(const Operand& o, long long idx) {
 
 template <int T>
 __global__ void __launch_bounds__((T / 4) * (T / 4)) cnp_gemm_kernel(CnpGemm g) {
+  pdl_trigger();
+  pdl_wait();
   constexpr int NT = (T / 4) * (T / 4);
   constexpr int TPR = T / 4;  // threads per row of the thread grid
   __shared__ float As[TK][T + 4];
@@ -125,10 +127,10 @@ poetx_status launch_cnp_gemm(const CnpGemm& g, int nblk, int stage, cudaStream_t
   }
   if (g.b >= 64) {
     dim3 grid(ceil_div(g.b, 64), ceil_div(g.b, 64), nblk);
-    cnp_gemm_kernel<64><<<grid, 256, 0, s>>>(g);
+    POETX_CUDA_TRY(launch_pdl(cnp_gemm_kernel<64>, grid, dim3(256), 0, s, g));
   } else {
     dim3 grid(ceil_div(g.b, 32), ceil_div(g.b, 32), nblk);
-    cnp_gemm_kernel<32><<<grid, 64, 0, s>>>(g);
+    POETX_CUDA_TRY(launch_pdl(cnp_gemm_kernel<32>, grid, dim3(64), 0, s, g));
   }
   POETX_CUDA_TRY(cudaGetLastError());
   after_launch(s, stage);
@@ -144,6 +146,8 @@ Operand op2(const float* p, float c, const float* q, float d) { return Operand{p
 __global__ void sum_partials_kernel(const float* __restrict__ dG0, int S0, int n0,
                                     const float* __restrict__ dG1, int S1, int n1, int b,
                                     float* __restrict__ X, float* __restrict__ Xt) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ float tile[32][33];
   const int j = blockIdx.z;
   const float* src = j < n0 ? dG0 + (long long)j * b * b : dG1 + (long long)(j - n0) * b * b;
@@ -247,8 +251,8 @@ poetx_status cnp_backward_sides(const CnpSides& q, const float* Qin, const float
   // X = sum of the partials (both sides, fixed order) and its transpose Xt
   {
     dim3 grid(ceil_div(b, 32), ceil_div(b, 32), nblk);
-    sum_partials_kernel<<<grid, dim3(32, 8), 0, s>>>(dG[0], splits[0], q.n[0], dG[1], splits[1],
-                                                     q.n[1], b, X, Xt);
+    POETX_CUDA_TRY(launch_pdl(sum_partials_kernel, grid, dim3(32, 8), 0, s, dG[0], splits[0],
+                              q.n[0], dG[1], splits[1], q.n[1], b, X, Xt));
     POETX_CUDA_TRY(cudaGetLastError());
     after_launch(s, ST_CNP_SUM);
   }

@@ -160,6 +160,7 @@ __global__ void __launch_bounds__(kThreadsCnp, 1)
     }
   };
   if (threadIdx.x == 0) stamp(0);
+  pdl_trigger();
   const int b = p.b;
   const int num_kb = p.nseg * p.kb_per_seg;
   const int row0 = blk * b;  // first row of this block in the [nblk*b, b] views
@@ -187,6 +188,7 @@ __global__ void __launch_bounds__(kThreadsCnp, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const uint32_t smem_base = smem_u32(smem);
+  pdl_wait();  // the previous kernel's outputs are visible from here on
   if (threadIdx.x == 0) stamp(1);
 
   if (warp == 0 && lane == 0) {
@@ -267,6 +269,7 @@ __global__ void __launch_bounds__(kThreadsCnp, 1)
         *abort_flag = 1;
         break;
       }
+      if (warp == 2 && lane == 0 && kb < 4) stamp(27 + kb);  // slots 27..30: K block landed
       const int seg = kb / p.kb_per_seg;
       const TOp& A = p.A[seg];
       const TOp& B = p.B[seg];
@@ -457,7 +460,7 @@ poetx_status launch_t(const CnpMaps& maps, const CnpUParams& p, int nblk, cudaSt
   });
   POETX_CUDA_TRY(attr);
   dim3 grid((p.b + BM - 1) / BM, p.b / BN, nblk);
-  k<<<grid, kThreadsCnp, smem, s>>>(maps, p);
+  POETX_CUDA_TRY(launch_pdl(k, grid, dim3(kThreadsCnp), smem, s, maps, p));
   POETX_CUDA_TRY(cudaGetLastError());
   return POETX_OK;
 }

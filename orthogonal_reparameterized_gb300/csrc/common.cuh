@@ -8,6 +8,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/poetx.h"
 
 #define POETX_CUDA_TRY(expr)                                    \
@@ -43,6 +45,25 @@ inline size_t dtype_size(poetx_dtype dt) {
 // Number of SMs of the current device (cached per device).
 int sm_count();
 
+// Launch with programmatic dependent launch allowed: the kernel may start (and run its
+// prologue) while the previous kernel on the stream is finishing; every kernel of this
+// library calls pdl_wait() before it touches global memory, so results are unchanged.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t s, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 // Stages of the hot path, for the launch counter and the optional per-stage event timing.
 enum Stage : int {
   ST_TRIU_UNPACK = 0, ST_CNP_Q2, ST_CNP_G, ST_CNP_SUM, ST_CNP_M1, ST_CNP_QBAR, ST_TRIU_PACK,
@@ -62,6 +83,13 @@ constexpr int kTraceSlots = 32;
 // ------------------------------------------------------------------------------------
 // device helpers
 // ------------------------------------------------------------------------------------
+// Programmatic dependent launch: let the next kernel on the stream start launching, and
+// wait until the previous one has completed and its writes are visible.
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ unsigned long long global_ns() {
   unsigned long long t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

@@ -26,6 +26,8 @@ __device__ __forceinline__ long long tri_index(int i, int j, int b) {
 // with coalesced rows.
 __global__ void triu_unpack_kernel(const float* __restrict__ q0, int n0, const float* __restrict__ q1,
                                    int b, float* __restrict__ Q) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ float tile[32][33];
   const int blk = blockIdx.z;
   const int nt = (b + 31) / 32;
@@ -60,6 +62,8 @@ __global__ void triu_unpack_kernel(const float* __restrict__ q0, int n0, const f
 
 __global__ void triu_grad_pack_kernel(const float* __restrict__ Qbar, int b, float* __restrict__ dq0,
                                       int n0, float* __restrict__ dq1, int accumulate) {
+  pdl_trigger();
+  pdl_wait();
   const int blk = blockIdx.z;
   const int i = blockIdx.y;
   const long long tri = (long long)b * (b - 1) / 2;
@@ -77,7 +81,7 @@ poetx_status launch_triu_unpack2(const float* q0, int n0, const float* q1, int n
   if (n0 + n1 == 0) return POETX_OK;
   const int nt = (b + 31) / 32;
   dim3 grid(nt * (nt + 1) / 2, 1, n0 + n1);
-  triu_unpack_kernel<<<grid, dim3(32, 8), 0, s>>>(q0, n0, q1, b, Q);
+  POETX_CUDA_TRY(launch_pdl(triu_unpack_kernel, grid, dim3(32, 8), 0, s, q0, n0, q1, b, Q));
   POETX_CUDA_TRY(cudaGetLastError());
   after_launch(s, ST_TRIU_UNPACK);
   return POETX_OK;
@@ -92,7 +96,8 @@ poetx_status launch_triu_grad_pack2(const float* Qbar, int n0, int n1, int b, fl
   if (n0 + n1 == 0 || b < 2) return POETX_OK;
   const int threads = b < 256 ? ((b + 31) / 32) * 32 : 256;
   dim3 grid(1, b - 1, n0 + n1);
-  triu_grad_pack_kernel<<<grid, threads, 0, s>>>(Qbar, b, dq0, n0, dq1, accumulate);
+  POETX_CUDA_TRY(launch_pdl(triu_grad_pack_kernel, grid, dim3(threads), 0, s, Qbar, b, dq0, n0,
+                            dq1, accumulate));
   POETX_CUDA_TRY(cudaGetLastError());
   after_launch(s, ST_TRIU_PACK);
   return POETX_OK;
@@ -181,6 +186,8 @@ __global__ void __launch_bounds__(256) perm_rows_kernel(const uint8_t* __restric
     const long long sr = src_rows ? (long long)__ldg(src_rows + r) : r;
     return X + sr * row_bytes;
   };
+  pdl_trigger();
+  pdl_wait();
   // start the first row copies, then stage the index while they are in flight
   if (threadIdx.x == 0) {
     for (int k = 0; k < nbuf; ++k) mbar_init(&full[k], 1);
@@ -256,8 +263,9 @@ static poetx_status launch_perm_rows_t(const void* X, long long N, int D, const 
   per_sm = per_sm < 1 ? 1 : (per_sm > 2 ? 2 : per_sm);
   const long long want = (long long)sm_count() * per_sm;
   const int grid = (int)(N < want ? N : want);
-  k<<<grid, 256, smem, s>>>(static_cast<const uint8_t*>(X), N, D, perm, static_cast<uint8_t*>(Y),
-                           src_rows, scale, scale_out, nbuf, device_error_word(), kWaitLimitNs);
+  POETX_CUDA_TRY(launch_pdl(k, dim3(grid), dim3(256), smem, s, static_cast<const uint8_t*>(X), N, D,
+                            perm, static_cast<uint8_t*>(Y), src_rows, scale, scale_out, nbuf,
+                            device_error_word(), kWaitLimitNs));
   POETX_CUDA_TRY(cudaGetLastError());
   after_launch(s, src_rows ? ST_MERGE : (SCATTER ? ST_PERM_SCATTER : ST_PERM_GATHER));
   return POETX_OK;
@@ -290,6 +298,8 @@ poetx_status launch_perm_rows(size_t esize, bool scatter, const void* X, long lo
 __global__ void __launch_bounds__(256) quantize_rows_kernel(const float* __restrict__ W, int m,
                                                             int8_t* __restrict__ Wq,
                                                             float* __restrict__ scale) {
+  pdl_trigger();
+  pdl_wait();
   const long long r = blockIdx.x;
   const float* row = W + r * m;
   float amax = 0.f;
@@ -317,7 +327,7 @@ __global__ void __launch_bounds__(256) quantize_rows_kernel(const float* __restr
 poetx_status launch_quantize(const float* W, int n, int m, int8_t* Wq, float* scale,
                              cudaStream_t s) {
   if (n == 0) return POETX_OK;
-  quantize_rows_kernel<<<n, 256, 0, s>>>(W, m, Wq, scale);
+  POETX_CUDA_TRY(launch_pdl(quantize_rows_kernel, dim3(n), dim3(256), 0, s, W, m, Wq, scale));
   POETX_CUDA_TRY(cudaGetLastError());
   after_launch(s, ST_QUANTIZE);
   return POETX_OK;

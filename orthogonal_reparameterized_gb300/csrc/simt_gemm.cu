@@ -12,6 +12,8 @@ constexpr int TM = 64, TN = 64, TK = 16, THREADS = 256;
 
 template <typename TA, typename TB, typename TC>
 __global__ void __launch_bounds__(THREADS) simt_gemm_kernel(SimtGemm g) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ float As[TK][TM + 4];
   __shared__ float Bs[TK][TN + 4];
   const int tid = threadIdx.x;
@@ -89,7 +91,7 @@ template <typename TA, typename TB, typename TC>
 poetx_status launch_t(const SimtGemm& g, cudaStream_t s) {
   dim3 grid(ceil_div(g.N, TN), ceil_div(g.M, TM), g.batch * g.ksplit);
   if (grid.y > 65535 || grid.z > 65535) return POETX_ERR_SHAPE;
-  simt_gemm_kernel<TA, TB, TC><<<grid, THREADS, 0, s>>>(g);
+  POETX_CUDA_TRY(launch_pdl(simt_gemm_kernel<TA, TB, TC>, grid, dim3(THREADS), 0, s, g));
   POETX_CUDA_TRY(cudaGetLastError());
   after_launch(s, g.stage);
   return POETX_OK;

@@ -219,6 +219,7 @@ __global__ void __launch_bounds__(gemm_threads<B_I8>(), 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) trace_stamp(p.trace, p.trace_cap, 0);  // slot 0: CTA start
+  pdl_trigger();
 
   if (warp == 0 && lane == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -246,6 +247,7 @@ __global__ void __launch_bounds__(gemm_threads<B_I8>(), 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const uint32_t smem_base = smem_u32(smem);
+  pdl_wait();  // the previous kernel's outputs are visible from here on
   if (threadIdx.x == 0) trace_stamp(p.trace, p.trace_cap, 1);  // slot 1: set-up done
   // tiles of this CTA: strided (t = blockIdx.x, + gridDim.x, ...) or, with a resident B
   // panel, one contiguous range
@@ -623,7 +625,7 @@ poetx_status launch(const CUtensorMap& ta, const CUtensorMap& tb, UmmaParams p, 
   p.num_tiles = (int)tiles;
   const long long want = (long long)sm_count() * per_sm;
   const int grid = (int)(tiles < want ? tiles : want);
-  k<<<grid, gemm_threads<B_I8>(), smem, s>>>(ta, tb, p);
+  POETX_CUDA_TRY(launch_pdl(k, dim3(grid), dim3(gemm_threads<B_I8>()), smem, s, ta, tb, p));
   POETX_CUDA_TRY(cudaGetLastError());
   after_launch(s, stage);
   return POETX_OK;
