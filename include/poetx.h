@@ -243,7 +243,8 @@ size_t poetx_layer_workspace_bytes(const poetx_layer* L, int N, int phase);
 
 /* Bytes the caller keeps from poetx_layer_fwd to poetx_layer_bwd ("saved"): the bf16 (or
  * fp32) blocks G_R, G_P and the fp32 Q_R, Q_P, Q_R^2, Q_P^2 (O((m+n) b), independent of N),
- * plus, for POETX_FAST only, B = A W'^T ([N, n] of dtype act). */
+ * plus, for POETX_FAST only, what default autograd keeps: B = A W'^T ([N, n]) and the
+ * permuted input x~ ([N, m]), both of dtype act.  POETX_MEM keeps nothing of size N. */
 size_t poetx_layer_saved_bytes(const poetx_layer* L, int N);
 
 /* Forward: y [N, n] = layer(x [N, m]).  Runs both CNPs, writes `saved` for the backward. */

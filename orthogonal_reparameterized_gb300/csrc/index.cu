@@ -109,13 +109,14 @@ poetx_status launch_triu_grad_pack(const float* Qbar, int nblk, int b, float* dq
 }
 
 // ---------------------------------------------------------------- row permutations
-// Persistent CTAs walk the rows (r = blockIdx.x, + gridDim.x, ...).  Each CTA first stages
-// the gather index of the whole row in shared memory: perm itself for a gather, its inverse
-// (idx[perm[i]] = i) for a scatter, so both become out[i] = row[idx[i]].  Rows arrive in a
-// ring of NBUF shared-memory buffers by one-dimensional TMA bulk copies issued by thread 0
-// (NBUF rows ahead), and every thread writes 16-byte vectors of the output row, so loads and
-// stores are both fully coalesced.  `src_rows` (nullable) remaps the source row (the merge
-// W'[r, :] = W0[perm_n[r], perm_m]).  Waits are bounded; on expiry the kernel records
+// Every row is permuted on its own: out[i] = row[idx[i]], with idx = perm for a gather and
+// its inverse (idx[perm[i]] = i) for a scatter, staged once per CTA in shared memory.  The
+// CTA's eight warps form 8/G independent groups of G warps (G = 1 when rows are short): a
+// group owns the rows r = group, + groups in the grid, ..., streams them into its own ring of
+// S row buffers by one-dimensional TMA bulk copies (S rows ahead) and writes 16-byte vectors
+// of each output row, so loads and stores are fully coalesced and no barrier wider than the
+// group ever stalls the other groups.  `src_rows` (nullable) remaps the source row (the
+// merge W'[r, :] = W0[perm_n[r], perm_m]).  Waits are bounded; on expiry the kernel records
 // POETX_ERR_TIMEOUT, drains the copies it issued and returns.
 template <int E>
 struct VecT;
@@ -161,81 +162,182 @@ __device__ __forceinline__ IdxVec<IdxT, V> load_idx(const IdxT* p) {
   return r;
 }
 
+// Barrier over one group of G warps (G = 1: the warp itself); named barriers 1..8.
+__device__ __forceinline__ void group_sync(int g, int G) {
+  if (G == 1) {
+    __syncwarp();
+  } else {
+    asm volatile("bar.sync %0, %1;" ::"r"(1 + g), "r"(G * 32) : "memory");
+  }
+}
+// True when `v` holds on every thread of the group.
+__device__ __forceinline__ bool group_all(bool v, int g, int G) {
+  if (G == 1) return __all_sync(0xffffffffu, v);
+  uint32_t r;
+  asm volatile(
+      "{ .reg .pred p, q; setp.ne.u32 q, %1, 0; bar.red.and.pred p, %2, %3, q; selp.u32 %0, 1, 0, p; }"
+      : "=r"(r)
+      : "r"((uint32_t)v), "r"(1 + g), "r"(G * 32)
+      : "memory");
+  return r != 0;
+}
+
+constexpr int kPermWarps = 8;  // consumer warps; one more warp issues the row copies
+
 template <int E, bool SCATTER, typename IdxT>
-__global__ void __launch_bounds__(256) perm_rows_kernel(const uint8_t* __restrict__ X, long long N,
-                                                        int D, const int32_t* __restrict__ perm,
-                                                        uint8_t* __restrict__ Y,
-                                                        const int32_t* __restrict__ src_rows,
-                                                        const float* __restrict__ scale,
-                                                        float* __restrict__ scale_out, int nbuf,
-                                                        int* err, unsigned long long limit_ns) {
+__global__ void __launch_bounds__((kPermWarps + 1) * 32) perm_rows_kernel(
+    const uint8_t* __restrict__ X, long long N, int D, const int32_t* __restrict__ perm,
+    uint8_t* __restrict__ Y, const int32_t* __restrict__ src_rows, const float* __restrict__ scale,
+    float* __restrict__ scale_out, int G, int S, int* err, unsigned long long limit_ns,
+    unsigned long long* trace, size_t trace_cap) {
   using T = typename VecT<E>::T;
   constexpr int V = 16 / E;  // elements per 16-byte vector
   extern __shared__ __align__(128) uint8_t smem_raw[];
   const uint32_t row_bytes = (uint32_t)D * E;
   const uint32_t idx_bytes = ((uint32_t)D * sizeof(IdxT) + 127u) & ~127u;
+  const int ngrp = kPermWarps / G;
   IdxT* idx = reinterpret_cast<IdxT*>(smem_raw);
-  uint8_t* ring = smem_raw + idx_bytes;
-  uint64_t* full = reinterpret_cast<uint64_t*>(ring + (size_t)nbuf * row_bytes);
-  const long long first = blockIdx.x;
-  const long long stride = gridDim.x;
-  const long long nrows = first < N ? (N - 1 - first) / stride + 1 : 0;  // rows of this CTA
-
-  auto src_of = [&](long long it) -> const uint8_t* {
-    const long long r = first + it * stride;
-    const long long sr = src_rows ? (long long)__ldg(src_rows + r) : r;
-    return X + sr * row_bytes;
+  uint8_t* ring = smem_raw + idx_bytes;  // [ngrp][S] rows
+  uint64_t* full = reinterpret_cast<uint64_t*>(ring + (size_t)ngrp * S * row_bytes);
+  uint64_t* empty = full + ngrp * S;
+  const int warp = threadIdx.x >> 5;
+  // group gr of this CTA owns rows first + gr + it * stride, it < rows_of(gr); rows per group
+  // fit 32 bits (N < 2^31), so the loops below count in 32 bits and never divide
+  const long long first = (long long)blockIdx.x * ngrp;
+  const long long stride = (long long)gridDim.x * ngrp;
+  auto rows_of = [&](int gr) -> int {
+    const long long f = first + gr;
+    return f < N ? (int)((N - 1 - f) / stride + 1) : 0;
   };
+  if (threadIdx.x == 0) trace_stamp(trace, trace_cap, 0);  // slot 0: CTA start
   pdl_trigger();
-  pdl_wait();
-  // start the first row copies, then stage the index while they are in flight
-  if (threadIdx.x == 0) {
-    for (int k = 0; k < nbuf; ++k) mbar_init(&full[k], 1);
-    fence_mbar_init();
-    for (int k = 0; k < nbuf && k < nrows; ++k) {
-      mbar_arrive_expect_tx(&full[k], row_bytes);
-      bulk_load(ring + (size_t)k * row_bytes, src_of(k), row_bytes, &full[k]);
+  if (warp == kPermWarps && (threadIdx.x & 31) == 0) {
+    for (int k = 0; k < ngrp * S; ++k) {
+      mbar_init(&full[k], 1);
+      mbar_init(&empty[k], 1);
     }
-  }
-  for (int i = threadIdx.x; i < D; i += blockDim.x) {
-    const int pi = __ldg(perm + i);
-    if (SCATTER) idx[pi] = (IdxT)i;
-    else idx[i] = (IdxT)pi;
+    fence_mbar_init();
   }
   __syncthreads();
-  const int nvec = D / V;
-  bool ok = true;
-  long long it = 0;
-  for (; it < nrows; ++it) {
-    const int k = (int)(it % nbuf);
-    const uint32_t ph = (uint32_t)((it / nbuf) & 1);
-    const bool got = mbar_wait_bounded(&full[k], ph, err, limit_ns);
-    if (!__syncthreads_and(got)) {
-      ok = false;
-      break;
-    }
-    const long long r = first + it * stride;
-    const T* row = reinterpret_cast<const T*>(ring + (size_t)k * row_bytes);
-    uint4* out = reinterpret_cast<uint4*>(Y + r * row_bytes);
-    for (int v = threadIdx.x; v < nvec; v += blockDim.x) {
-      const IdxVec<IdxT, V> ix = load_idx<IdxT, V>(idx + (size_t)v * V);
-      union { uint4 u; T e[V]; } pk;
+  pdl_wait();
+  if (threadIdx.x == 0) trace_stamp(trace, trace_cap, 1);  // slot 1: predecessor done
+
+  if (warp == kPermWarps) {
+    // producer: one thread streams every group's rows, round robin over the groups so the
+    // first rows of all groups land first; a slot is refilled once its group released it
+    if ((threadIdx.x & 31) == 0) {
+      int nr[kPermWarps], issued[kPermWarps];
+      int most = 0;
 #pragma unroll
-      for (int e = 0; e < V; ++e) pk.e[e] = row[ix.i[e]];
-      out[v] = pk.u;
+      for (int gr = 0; gr < kPermWarps; ++gr) {
+        nr[gr] = gr < ngrp ? rows_of(gr) : 0;
+        issued[gr] = 0;
+        most = nr[gr] > most ? nr[gr] : most;
+      }
+      bool ok = true;
+      int k = 0, round = 0;
+      for (int it = 0; ok && it < most; ++it) {
+#pragma unroll
+        for (int gr = 0; gr < kPermWarps; ++gr) {
+          if (!ok || it >= nr[gr]) continue;
+          const int slot = gr * S + k;
+          if (round > 0 && !mbar_wait_bounded(&empty[slot], (uint32_t)((round - 1) & 1), err, limit_ns)) {
+            ok = false;
+            continue;
+          }
+          const long long r = first + gr + (long long)it * stride;
+          const long long sr = src_rows ? (long long)__ldg(src_rows + r) : r;
+          mbar_arrive_expect_tx(&full[slot], row_bytes);
+          bulk_load(ring + (size_t)slot * row_bytes, X + sr * row_bytes, row_bytes, &full[slot]);
+          issued[gr] = it + 1;
+        }
+        if (it == 0) trace_stamp(trace, trace_cap, 2);  // slot 2: first row of every group issued
+        if (++k == S) {
+          k = 0;
+          ++round;
+        }
+      }
+      if (!ok) {
+        // drain: the last S rows issued to each group may still be in flight
+#pragma unroll
+        for (int gr = 0; gr < kPermWarps; ++gr)
+          for (int j = issued[gr] - S < 0 ? 0 : issued[gr] - S; j < issued[gr]; ++j)
+            mbar_wait_bounded(&full[gr * S + j % S], (uint32_t)((j / S) & 1), err, limit_ns);
+      }
     }
-    if (scale_out && threadIdx.x == 0) scale_out[r] = scale[src_rows ? src_rows[r] : r];
-    __syncthreads();  // every thread is done with buffer k
-    if (threadIdx.x == 0 && it + nbuf < nrows) {
-      mbar_arrive_expect_tx(&full[k], row_bytes);
-      bulk_load(ring + (size_t)k * row_bytes, src_of(it + nbuf), row_bytes, &full[k]);
+  } else {
+    // consumers: stage the index, then each group of G warps permutes its own rows
+    const int g = warp / G;
+    const int tig = threadIdx.x - g * G * 32;
+    for (int i = threadIdx.x; i < D; i += kPermWarps * 32) {
+      const int pi = __ldg(perm + i);
+      if (SCATTER) idx[pi] = (IdxT)i;
+      else idx[i] = (IdxT)pi;
+    }
+    asm volatile("bar.sync %0, %1;" ::"r"(kPermWarps + 1), "r"(kPermWarps * 32) : "memory");
+    if (threadIdx.x == 0) trace_stamp(trace, trace_cap, 3);  // slot 3: index staged
+    const int nrows = rows_of(g);
+    const int nvec = D / V;
+    const int gthreads = G * 32;
+    int k = 0;
+    uint32_t ph = 0;
+    for (int it = 0; it < nrows; ++it) {
+      const int slot = g * S + k;
+      const bool got = mbar_wait_bounded(&full[slot], ph, err, limit_ns);
+      if (!group_all(got, g, G)) break;
+      if (threadIdx.x == 0 && it < 13) trace_stamp(trace, trace_cap, 4 + 2 * it);  // landed
+      const long long r = first + g + (long long)it * stride;
+      const T* row = reinterpret_cast<const T*>(ring + (size_t)slot * row_bytes);
+      uint4* out = reinterpret_cast<uint4*>(Y + r * row_bytes);
+#pragma unroll 4
+      for (int v = tig; v < nvec; v += gthreads) {
+        const IdxVec<IdxT, V> ix = load_idx<IdxT, V>(idx + (size_t)v * V);
+        union { uint4 u; T e[V]; } pk;
+#pragma unroll
+        for (int e = 0; e < V; ++e) pk.e[e] = row[ix.i[e]];
+        out[v] = pk.u;
+      }
+      if (scale_out && tig == 0) scale_out[r] = scale[src_rows ? src_rows[r] : r];
+      group_sync(g, G);  // every thread of the group is done with buffer k
+      if (threadIdx.x == 0 && it < 13) trace_stamp(trace, trace_cap, 5 + 2 * it);  // row done
+      if (tig == 0) mbar_arrive(&empty[slot]);
+      if (++k == S) {
+        k = 0;
+        ph ^= 1u;
+      }
     }
   }
-  if (!ok && threadIdx.x == 0) {
-    // drain the copies still in flight before the shared memory goes away
-    for (long long j = it; j < nrows && j < it + nbuf; ++j)
-      mbar_wait_bounded(&full[j % nbuf], (uint32_t)((j / nbuf) & 1), err, limit_ns);
+  if (trace) {
+    __syncthreads();
+    if (threadIdx.x == 0) trace_stamp(trace, trace_cap, 31);  // slot 31: every row done
   }
+}
+
+// Group size and ring depth for rows of `row_bytes`: the narrowest groups of two warps or
+// more whose rings (two rows at least) fit ~110 KB with the index, so that two CTAs share an
+// SM; one CTA of a single group per SM for rows too long for that.  Returns false when not
+// even that fits.  (Measured on 2048-wide bf16 rows: two-warp groups match one-warp groups at
+// 4096 rows and stream ~10 % faster from 8192 rows up; wider groups are slower.)
+static bool perm_shape(size_t row_bytes, size_t idx_bytes, int* G, int* S, size_t* smem) {
+  const size_t budget2 = 110 * 1024, budget1 = 220 * 1024;
+  for (int g = 2; g <= kPermWarps; g *= 2) {
+    const size_t ngrp = kPermWarps / g;
+    if (idx_bytes + ngrp * 2 * (row_bytes + 16) <= budget2) {
+      int s = (int)((budget2 - idx_bytes) / (ngrp * (row_bytes + 16)));
+      s = s > 8 ? 8 : s;
+      *G = g;
+      *S = s;
+      *smem = idx_bytes + ngrp * s * (row_bytes + 16);
+      return true;
+    }
+  }
+  if (idx_bytes + row_bytes + 16 > budget1) return false;
+  int s = (int)((budget1 - idx_bytes) / (row_bytes + 16));
+  s = s > 8 ? 8 : s;
+  *G = kPermWarps;
+  *S = s;
+  *smem = idx_bytes + s * (row_bytes + 16);
+  return true;
 }
 
 template <int E, bool SCATTER, typename IdxT>
@@ -244,13 +346,9 @@ static poetx_status launch_perm_rows_t(const void* X, long long N, int D, const 
                                        float* scale_out, cudaStream_t s) {
   const size_t row_bytes = (size_t)D * E;
   const size_t idx_bytes = ((size_t)D * sizeof(IdxT) + 127) & ~(size_t)127;
-  // ring of rows: aim at ~96 KB of rows in flight per CTA (two CTAs per SM keep ~190 KB of
-  // loads outstanding, enough to cover the DRAM latency), 2..32 buffers, <= 200 KB in total
-  int nbuf = (int)((96 * 1024) / row_bytes);
-  nbuf = nbuf < 2 ? 2 : (nbuf > 32 ? 32 : nbuf);
-  while (nbuf > 2 && idx_bytes + nbuf * row_bytes + 128 > 200 * 1024) --nbuf;
-  const size_t smem = idx_bytes + nbuf * row_bytes + 8 * (size_t)nbuf;
-  if (smem > 227 * 1024) return POETX_ERR_SHAPE;
+  int G = 0, S = 0;
+  size_t smem = 0;
+  if (!perm_shape(row_bytes, idx_bytes, &G, &S, &smem)) return POETX_ERR_SHAPE;
   auto k = perm_rows_kernel<E, SCATTER, IdxT>;
   static std::once_flag once;  // the opt-in limit is set once, to the largest size used
   static cudaError_t attr = cudaSuccess;
@@ -258,14 +356,17 @@ static poetx_status launch_perm_rows_t(const void* X, long long N, int D, const 
     attr = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
   });
   POETX_CUDA_TRY(attr);
-  // two CTAs per SM at most: each stages the whole index once, so it should own many rows
-  int per_sm = (int)((220 * 1024) / (smem + 1024));
-  per_sm = per_sm < 1 ? 1 : (per_sm > 2 ? 2 : per_sm);
+  const int ngrp = kPermWarps / G;
+  size_t tr_cap = 0;
+  unsigned long long* tr = trace_buffer(&tr_cap);
+  const int per_sm = smem <= 110 * 1024 ? 2 : 1;
   const long long want = (long long)sm_count() * per_sm;
-  const int grid = (int)(N < want ? N : want);
-  POETX_CUDA_TRY(launch_pdl(k, dim3(grid), dim3(256), smem, s, static_cast<const uint8_t*>(X), N, D,
-                            perm, static_cast<uint8_t*>(Y), src_rows, scale, scale_out, nbuf,
-                            device_error_word(), kWaitLimitNs));
+  const long long need = (N + ngrp - 1) / ngrp;
+  const int grid = (int)(need < want ? need : want);
+  POETX_CUDA_TRY(launch_pdl(k, dim3(grid), dim3((kPermWarps + 1) * 32), smem, s,
+                            static_cast<const uint8_t*>(X), N, D, perm, static_cast<uint8_t*>(Y),
+                            src_rows, scale, scale_out, G, S, device_error_word(), kWaitLimitNs,
+                            tr, tr_cap));
   POETX_CUDA_TRY(cudaGetLastError());
   after_launch(s, src_rows ? ST_MERGE : (SCATTER ? ST_PERM_SCATTER : ST_PERM_GATHER));
   return POETX_OK;

@@ -116,7 +116,7 @@ poetx_status wprime_impl(poetx_dtype act, poetx_dtype wdt, const void* A, long l
 // ---------------------------------------------------------------- layer plumbing
 struct Plan {
   // saved
-  size_t GR, GP, Q2R, Q2P, Qs, Bsv, saved_total;
+  size_t GR, GP, Q2R, Q2P, Qs, Bsv, Xsv, saved_total;
   // forward workspace
   size_t f_xt, f_A, f_B, f_zt, fwd_total;
   // backward workspace
@@ -160,10 +160,11 @@ static Plan make_plan(const poetx_layer* L, long long N) {
   p.Q2P = p.Q2R + m * b * 4;
   p.Qs = take((m + n) * b * 4);
   p.Bsv = L->variant == POETX_FAST ? take((size_t)N * n * as) : 0;
+  p.Xsv = L->variant == POETX_FAST ? take((size_t)N * m * as) : 0;
   p.saved_total = o;
 
   o = 0;
-  p.f_xt = take((size_t)N * m * as);
+  p.f_xt = L->variant == POETX_MEM ? take((size_t)N * m * as) : 0;
   p.f_A = take((size_t)N * m * as);
   p.f_B = L->variant == POETX_MEM ? take((size_t)N * n * as) : 0;
   p.f_zt = take((size_t)N * n * as);
@@ -173,7 +174,7 @@ static Plan make_plan(const poetx_layer* L, long long N) {
   p.splitsP = wgrad_splits(N, L->n / L->b, L->b);
   o = 0;
   p.b_cnp = take(cnp_bwd_scratch_bytes((int)((m + n) / b), (int)b));
-  p.b_xt = take((size_t)N * m * as);
+  p.b_xt = L->variant == POETX_MEM ? take((size_t)N * m * as) : 0;
   p.b_dzt = take((size_t)N * n * as);
   p.b_A = L->variant == POETX_MEM ? take((size_t)N * m * as) : 0;
   p.b_B = L->variant == POETX_MEM ? take((size_t)N * n * as) : 0;
@@ -238,7 +239,8 @@ extern "C" poetx_status poetx_layer_fwd(const poetx_layer* L, const void* x, int
                               f32 ? at<float>(saved, p.GR) : nullptr,
                               f32 ? nullptr : at(saved, p.GR), nullptr, stream));
   if (N == 0) return POETX_OK;
-  void* xt = at(ws, p.f_xt);
+  // fast keeps x~ and B for the backward (what default autograd keeps), mem keeps neither
+  void* xt = L->variant == POETX_FAST ? at(saved, p.Xsv) : at(ws, p.f_xt);
   void* A = at(ws, p.f_A);
   void* B = L->variant == POETX_FAST ? at(saved, p.Bsv) : at(ws, p.f_B);
   POETX_TRY(launch_perm_rows(as, false, x, N, m, L->perm_m, xt, nullptr, nullptr, nullptr, stream));
@@ -267,7 +269,8 @@ extern "C" poetx_status poetx_layer_bwd(const poetx_layer* L, const void* x, con
   const poetx_dtype act = L->act;
   const size_t as = dtype_size(act);
   prof_begin(stream);
-  void* xt = at(ws, p.b_xt);
+  const bool fast = L->variant == POETX_FAST;
+  const void* xt = fast ? at(saved, p.Xsv) : at(ws, p.b_xt);
   void* dzt = at(ws, p.b_dzt);
   void* dB = at(ws, p.b_dB);
   void* dA = at(ws, p.b_dA);
@@ -276,7 +279,9 @@ extern "C" poetx_status poetx_layer_bwd(const poetx_layer* L, const void* x, con
   const void* GR = at(saved, p.GR);
   const void* GP = at(saved, p.GP);
   if (N > 0) {
-    POETX_TRY(launch_perm_rows(as, false, x, N, m, L->perm_m, xt, nullptr, nullptr, nullptr, stream));
+    if (!fast)  // mem: x~ is recomputed
+      POETX_TRY(launch_perm_rows(as, false, x, N, m, L->perm_m, at(ws, p.b_xt), nullptr, nullptr,
+                                 nullptr, stream));
     POETX_TRY(launch_perm_rows(as, false, dy, N, n, L->perm_n, dzt, nullptr, nullptr, nullptr, stream));
   }
   const void* B;

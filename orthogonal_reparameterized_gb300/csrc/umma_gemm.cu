@@ -35,7 +35,6 @@ struct UmmaParams {
   int mode;
   int tiles_m, tiles_n, num_tiles;  // tile t: mt = t % tiles_m, nt = (t / tiles_m) % tiles_n,
                                     // z = t / (tiles_m * tiles_n) (block, or block*splits+split)
-  int order;                        // 1: z fastest, then nt, then mt
   int M;         // valid output rows of the whole problem (tokens, or b for WGRAD)
   int num_kb;    // 64-wide K blocks per CTA (PLAIN, BLOCKDIAG)
   int b;         // block size (BLOCKDIAG, WGRAD)
@@ -98,19 +97,10 @@ struct TileCoords {
 template <int BN, bool B_MN>
 __device__ __forceinline__ TileCoords tile_coords(const UmmaParams& p, int t) {
   TileCoords c;
-  int mt, nt, z;
-  if (p.order == 0) {
-    mt = t % p.tiles_m;
-    const int rest = t / p.tiles_m;
-    nt = rest % p.tiles_n;
-    z = rest / p.tiles_n;
-  } else {
-    const int tz = p.num_tiles / (p.tiles_m * p.tiles_n);
-    z = t % tz;
-    const int rest = t / tz;
-    nt = rest % p.tiles_n;
-    mt = rest / p.tiles_n;
-  }
+  const int mt = t % p.tiles_m;
+  const int rest = t / p.tiles_m;
+  const int nt = rest % p.tiles_n;
+  const int z = rest / p.tiles_n;
   c.num_kb = p.num_kb;
   c.out_row0 = (long long)mt * BM;
   c.out_col0 = (long long)nt * BN;
@@ -633,11 +623,6 @@ poetx_status launch(const CUtensorMap& ta, const CUtensorMap& tb, UmmaParams p, 
 
 UmmaParams base_params() {
   UmmaParams p{};
-  static const int order_env = [] {
-    const char* e = getenv("POETX_TILE_ORDER");
-    return e ? atoi(e) : 0;
-  }();
-  p.order = order_env;
   p.trace = trace_buffer(&p.trace_cap);
   p.err = device_error_word();
   p.limit_ns = kWaitLimitNs;

@@ -40,7 +40,11 @@ def _perms(D):
 
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32, torch.int8])
-@pytest.mark.parametrize("N,D", [(1, 64), (37, 256), (300, 2048), (5, 14336)])
+# shapes reach every ring layout of the kernel: one-warp groups with deep rings that wrap many
+# times (20000 x 256), two-warp groups (4096 wide), whole-CTA groups (14336), and rows so
+# long that one CTA fills an SM (32768)
+@pytest.mark.parametrize("N,D", [(1, 64), (37, 256), (300, 2048), (20000, 256), (64, 4096),
+                                 (5, 14336), (3, 32768)])
 def test_perm_gather_scatter_bit_exact(P, dtype, N, D):
     if dtype == torch.int8:
         X = torch.randint(-128, 127, (N, D), dtype=torch.int8, device=DEV)
