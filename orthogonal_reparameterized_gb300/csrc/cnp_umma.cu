@@ -3,22 +3,26 @@
 // hi(v) = v rounded to the nearest tf32 value (13 low mantissa bits cleared) and
 // lo(v) = v - hi(v) (exact in fp32); the dropped lo*lo term is below 2^-22 |a||b|.  The
 // tensor-core fp32 accumulation is kept short: every 32-wide K block goes into a fresh TMEM
-// accumulator (two, used alternately) that the converter warps add into fp32 registers with
-// IEEE adds ("promotion"), so the accumulated rounding does not grow with b.
+// accumulator (NACC of them, used in turn) that the promotion warps add into a running sum
+// with IEEE fp32 adds ("promotion"), so the accumulated rounding does not grow with b.
 //
 // Each CNP product (POET-X summary page, "Core method" section 4, eq. 9 and its gradient)
 // is C_j = sum_seg opA_seg(j) . opB_seg(j) + epilogue, for every block j, where each operand
-// is a linear combination of at most two b x b fp32 arrays (Q, Q^2, X, M1).  The pipeline
-// of one CTA (one 128 x BN output tile of one block):
-//   warp 0     TMA: the raw fp32 tiles of every source array of the current K block
-//   warps 2-5  form v = c0*src0 + c1*src1 in shared memory and split it in place into
-//              hi(v) and lo(v) (same swizzled offsets, so the layout is kept)
-//   warp 1     three tcgen05.mma kind::tf32 per K=8 step into the K block's TMEM accumulator
-//   warps 2-5  promote each K block's accumulator into registers; at the end add the
-//              epilogue terms and store fp32 / fp32^T / bf16 / bf16^T
+// is a linear combination of at most two b x b fp32 arrays (Q, Q^2, X, M1).  One CTA makes
+// one 128 x BN output tile of one block:
+//   warp 0      TMA: the raw fp32 tiles of every source array of the current K block
+//   warps 2-9   form v = c0*src0 + c1*src1 and split it into hi(v), lo(v): the A operand
+//               straight into tensor memory (where the MMA reads it), the B operand in place
+//               in shared memory (same swizzled offsets, so the layout is kept)
+//   warp 1      three tcgen05.mma kind::tf32 per K=8 step into the K block's accumulator
+//   warps 10-13 promotion: add each K block's accumulator into the running sum (in TMEM)
+//   all warps   epilogue: out = sum + e1 E1 + e2 E2 + eI I through a shared-memory tile,
+//               stored as fp32 / fp32^T / bf16 / bf16^T with coalesced 16-byte accesses
 // Both operand tiles are K-major (kind::tf32 takes no MN-major operand): A tiles are rows of
 // A, B tiles rows of B^T (the B terms of a product are given transposed); 128-byte swizzle.
-// Every wait is bounded (POETX_ERR_TIMEOUT on expiry, then drain, free TMEM, return).
+// Keeping A out of shared memory halves the shared-memory traffic of a K block, which is
+// what bounds this kernel.  Every wait is bounded (POETX_ERR_TIMEOUT on expiry, then drain,
+// free TMEM, return).
 #include <mutex>
 
 #include "cnp_umma.h"
@@ -31,7 +35,7 @@ namespace {
 
 constexpr int BM = 128;
 constexpr int BK = 32;      // fp32 elements per 128-byte row
-constexpr int NMAPS = 8;  // distinct (source array, operand role) pairs of one product
+constexpr int NMAPS = 8;    // distinct (source array, operand role) pairs of one product
 
 struct CnpMaps {
   CUtensorMap m[NMAPS];
@@ -85,14 +89,23 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t
   return d;
 }
 
-__device__ __forceinline__ void umma_tf32(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                          uint32_t idesc, uint32_t accumulate) {
+// A operand in tensor memory (M rows = lanes, one tf32 element per 32-bit column), B in
+// shared memory.
+__device__ __forceinline__ void umma_tf32_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                             uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
+}
+
+// tf32 split of v: hi = v rounded to the nearest tf32 value, lo = v - hi (exact).
+__device__ __forceinline__ void split_tf32(float v, uint32_t& hi, uint32_t& lo) {
+  const float h = __uint_as_float((__float_as_uint(v) + 0x1000u) & 0xFFFFE000u);
+  hi = __float_as_uint(h);
+  lo = __float_as_uint(v - h);
 }
 
 __device__ __forceinline__ void fence_async_smem() {
@@ -120,29 +133,62 @@ __device__ __forceinline__ void combine_split(float4* x, float4* y, float c0, fl
   *y = make_float4(lo[0], lo[1], lo[2], lo[3]);
 }
 
-// Warp roles: 0 TMA producer, 1 MMA issuer (and TMEM owner), 2..9 converters (form and
-// split the operands), 10..13 promotion + epilogue (warp 10 + q reads TMEM lane quarter
-// (10 + q) % 4 = q + 2 mod 4).  NACC accumulators let the MMA run ahead of the promotion.
-constexpr int kConvWarps = 8;
+// Warp roles: 0 TMA producer, 1 MMA issuer (and TMEM owner), 2..9 converters, 10..13
+// promotion.  Converter warp w forms and splits the A operand of its TMEM lane quarter w % 4
+// (rows 32 (w % 4) .. +31, K columns 16 ((w - 2) / 4) .. +15) and writes hi and lo into
+// tensor memory; the B operand is formed and split in shared memory by all converters.
+// Promotion warp w adds each K block's accumulator of its lane quarter into the running sum,
+// kept in TMEM as well so that it holds no accumulator registers.  TMEM columns: NACC
+// accumulators of BN, the running sum (BN), then STAGES A slots of 64 (hi 32 + lo 32).
+constexpr int NACC = 4;
+constexpr int kConvWarps = 8;  // two per TMEM lane quarter
 constexpr int kPromWarps = 4;
 constexpr int kThreadsCnp = 32 * (2 + kConvWarps + kPromWarps);
-constexpr int NACC = 4;
 
-template <int BN, int STAGES>
+// cp.async (global -> shared, no registers held while in flight; bypasses L1).
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem)), "l"(gmem)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
+template <int BN>
+__host__ __device__ constexpr int cnp_stages() { return BN >= 64 ? 3 : 4; }
+// dynamic shared memory: the operand ring, the two epilogue-term tiles, 1 KB of alignment
+// slack and the barriers
+template <int BN>
+__host__ __device__ constexpr int cnp_smem() {
+  return cnp_stages<BN>() * (2 * BM * BK * 4 + 2 * BN * BK * 4) + 2 * BM * BN * 4 + 1024 + 256;
+}
+
+template <int BN>
 __global__ void __launch_bounds__(kThreadsCnp, 1)
     cnp_umma_kernel(const __grid_constant__ CnpMaps maps, const CnpUParams p) {
-  constexpr int NCT = 32 * kConvWarps;  // converter threads
+  constexpr int STAGES = cnp_stages<BN>();
+  constexpr int CW = BN;                      // running-sum columns per promotion thread
+  constexpr int NCT = 32 * kConvWarps;        // converter threads
   constexpr uint32_t A_BYTES = BM * BK * 4;   // 16 KB per buffer
   constexpr uint32_t B_BYTES = BN * BK * 4;   // BN * 128 bytes per buffer
   constexpr uint32_t STAGE_BYTES = 2 * A_BYTES + 2 * B_BYTES;
-  constexpr uint32_t TMEM_COLS = NACC * BN;
-  static_assert(TMEM_COLS == 128 || TMEM_COLS == 256, "TMEM allocation must be a power of two");
+  constexpr uint32_t RING_BYTES = STAGES * STAGE_BYTES;
+  constexpr uint32_t SUM_COL = NACC * BN;     // running sum
+  constexpr uint32_t A_COL = NACC * BN + BN;  // A slots: A_COL + 64 s (+32 for lo)
+  constexpr uint32_t TMEM_COLS = A_COL + 64 * STAGES <= 256 ? 256 : 512;
+  constexpr int G4 = BN / 4;                  // float4 groups per tile row
+  constexpr int LD = BN + 4;                  // staged tile pitch (16-byte rows)
+  constexpr int TILE = BM * BN;               // floats of one epilogue-term tile
+  static_assert(A_COL + 64 * STAGES <= TMEM_COLS, "accumulators, sum and A slots fit TMEM");
+  static_assert(RING_BYTES >= (uint32_t)BM * LD * 4, "the staged tile fits the ring");
   constexpr uint32_t IDESC = tf32_idesc(BM, BN);
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  float* const tile = reinterpret_cast<float*>(smem);                // epilogue (ring idle)
+  float* const etile = reinterpret_cast<float*>(smem + RING_BYTES);  // [2][BM][BN] E1, E2
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + RING_BYTES + 2 * TILE * 4);
   uint64_t* conv = full + STAGES;
   uint64_t* empty = conv + STAGES;
   uint64_t* tfull = empty + STAGES;   // [NACC] accumulator holds a finished K block
@@ -164,6 +210,9 @@ __global__ void __launch_bounds__(kThreadsCnp, 1)
   const int b = p.b;
   const int num_kb = p.nseg * p.kb_per_seg;
   const int row0 = blk * b;  // first row of this block in the [nblk*b, b] views
+  const long long base = (long long)blk * b * b;
+  const int i0 = mt * BM, j0 = nt * BN;
+  const int rows = b - i0 < BM ? b - i0 : BM;  // valid rows of the tile; b % 32 == 0
 
   if (warp == 0 && lane == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -191,9 +240,10 @@ __global__ void __launch_bounds__(kThreadsCnp, 1)
   pdl_wait();  // the previous kernel's outputs are visible from here on
   if (threadIdx.x == 0) stamp(1);
 
+  int tma_issued = 0;  // TMA thread: K blocks issued
+  int mma_last = -1;   // MMA thread: last K block issued
   if (warp == 0 && lane == 0) {
     // ---------------------------------------------------------------- TMA producer
-    int issued = 0;
     for (int kb = 0; kb < num_kb; ++kb) {
       const int s = kb % STAGES;
       const uint32_t ph = (kb / STAGES) & 1;
@@ -215,18 +265,15 @@ __global__ void __launch_bounds__(kThreadsCnp, 1)
       uint8_t* st = smem + s * STAGE_BYTES;
       for (int i = 0; i < 2; ++i) {
         if (A.s[i].map >= 0)  // rows mt*128.. of A (one 32 x 128 box)
-          tma_load_2d(st + i * A_BYTES, &maps.m[A.s[i].map], &full[s], k0, row0 + mt * BM);
+          tma_load_2d(st + i * A_BYTES, &maps.m[A.s[i].map], &full[s], k0, row0 + i0);
         if (B.s[i].map >= 0)  // rows nt*BN.. of B^T, columns k0..k0+31 (one 32 x BN box)
           tma_load_2d(st + 2 * A_BYTES + i * B_BYTES, &maps.m[B.s[i].map], &full[s], k0,
-                      row0 + nt * BN);
+                      row0 + j0);
       }
-      ++issued;
+      ++tma_issued;
     }
-    for (int kb = issued - 1; kb >= 0 && kb >= issued - STAGES; --kb)
-      mbar_wait_bounded(&full[kb % STAGES], (kb / STAGES) & 1, p.err, p.limit_ns);
   } else if (warp == 1 && lane == 0) {
     // ---------------------------------------------------------------- MMA issuer
-    int done = 0;
     for (int kb = 0; kb < num_kb; ++kb) {
       const int s = kb % STAGES;
       const uint32_t ph = (kb / STAGES) & 1;
@@ -239,28 +286,27 @@ __global__ void __launch_bounds__(kThreadsCnp, 1)
       }
       tc_fence_after();
       const uint32_t d = tmem_base + (uint32_t)(a * BN);
-      const uint32_t a_hi = smem_base + s * STAGE_BYTES;
-      const uint32_t a_lo = a_hi + A_BYTES;
-      const uint32_t b_hi = a_hi + 2 * A_BYTES;
+      const uint32_t a_hi = tmem_base + A_COL + 64u * (uint32_t)s;
+      const uint32_t a_lo = a_hi + 32;
+      const uint32_t b_hi = smem_base + s * STAGE_BYTES + 2 * A_BYTES;
       const uint32_t b_lo = b_hi + B_BYTES;
 #pragma unroll
-      for (int k = 0; k < BK / 8; ++k) {
-        const uint64_t ah = sdesc(a_hi + k * 32, 16, 1024), al = sdesc(a_lo + k * 32, 16, 1024);
+      for (int k = 0; k < BK / 8; ++k) {  // K = 8 per MMA: 8 TMEM columns of A
         const uint64_t bh = sdesc(b_hi + k * 32, 16, 1024), bl = sdesc(b_lo + k * 32, 16, 1024);
-        umma_tf32(d, ah, bh, IDESC, k != 0);
-        umma_tf32(d, ah, bl, IDESC, 1);
-        umma_tf32(d, al, bh, IDESC, 1);
+        umma_tf32_ta(d, a_hi + 8 * k, bh, IDESC, k != 0);
+        umma_tf32_ta(d, a_hi + 8 * k, bl, IDESC, 1);
+        umma_tf32_ta(d, a_lo + 8 * k, bh, IDESC, 1);
       }
       umma_commit(&empty[s]);
       umma_commit(&tfull[a]);
-      ++done;
+      mma_last = kb;
     }
-    // TMEM is freed after the final barrier: wait until the last MMAs have completed.
-    if (done > 0)
-      mbar_wait_bounded(&tfull[(done - 1) % NACC], ((done - 1) / NACC) & 1, p.err, p.limit_ns);
   } else if (warp >= 2 && warp < 2 + kConvWarps) {
     // ---------------------------------------------------------------- converters
     const int ct = threadIdx.x - 64;  // 0..NCT-1
+    const int qa = warp & 3, ha = (warp - 2) >> 2;
+    const int ra = qa * 32 + lane;    // A row of this thread
+    const uint32_t a_lane = tmem_base + ((uint32_t)(qa * 32) << 16);
     for (int kb = 0; kb < num_kb; ++kb) {
       const int s = kb % STAGES;
       const uint32_t ph = (kb / STAGES) & 1;
@@ -269,36 +315,68 @@ __global__ void __launch_bounds__(kThreadsCnp, 1)
         *abort_flag = 1;
         break;
       }
-      if (warp == 2 && lane == 0 && kb < 4) stamp(27 + kb);  // slots 27..30: K block landed
       const int seg = kb / p.kb_per_seg;
       const TOp& A = p.A[seg];
       const TOp& B = p.B[seg];
       uint8_t* st = smem + s * STAGE_BYTES;
-      float4* a0 = reinterpret_cast<float4*>(st);
-      float4* a1 = reinterpret_cast<float4*>(st + A_BYTES);
-      const bool a_two = A.s[1].map >= 0;
-#pragma unroll 4
-      for (int e = ct; e < (int)(A_BYTES / 16); e += NCT)
-        combine_split(a0 + e, a1 + e, A.s[0].coef, A.s[1].coef, a_two);
+      {
+        // A: row ra, K columns 16 ha .. 16 ha + 15 = 16-byte chunks 4 ha .. 4 ha + 3 of the
+        // 128-byte row (128-byte swizzle: chunk c of row r sits at chunk c ^ (r % 8))
+        const bool two = A.s[1].map >= 0;
+        const float c0 = A.s[0].coef, c1 = A.s[1].coef;
+        uint32_t hi[16], lo[16];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const int off = ra * 128 + (((4 * ha + t) ^ (ra & 7)) << 4);
+          const float4 x = *reinterpret_cast<const float4*>(st + off);
+          float4 v = make_float4(c0 * x.x, c0 * x.y, c0 * x.z, c0 * x.w);
+          if (two) {
+            const float4 y = *reinterpret_cast<const float4*>(st + A_BYTES + off);
+            v.x = fmaf(c1, y.x, v.x);
+            v.y = fmaf(c1, y.y, v.y);
+            v.z = fmaf(c1, y.z, v.z);
+            v.w = fmaf(c1, y.w, v.w);
+          }
+          split_tf32(v.x, hi[4 * t], lo[4 * t]);
+          split_tf32(v.y, hi[4 * t + 1], lo[4 * t + 1]);
+          split_tf32(v.z, hi[4 * t + 2], lo[4 * t + 2]);
+          split_tf32(v.w, hi[4 * t + 3], lo[4 * t + 3]);
+        }
+        const uint32_t col = A_COL + 64u * (uint32_t)s + 16u * (uint32_t)ha;
+        tmem_st_32x32b_x16(a_lane + col, hi);
+        tmem_st_32x32b_x16(a_lane + col + 32, lo);
+      }
       float4* b0 = reinterpret_cast<float4*>(st + 2 * A_BYTES);
       float4* b1 = reinterpret_cast<float4*>(st + 2 * A_BYTES + B_BYTES);
       const bool b_two = B.s[1].map >= 0;
-#pragma unroll 2
+#pragma unroll 4
       for (int e = ct; e < (int)(B_BYTES / 16); e += NCT)
         combine_split(b0 + e, b1 + e, B.s[0].coef, B.s[1].coef, b_two);
-      fence_async_smem();  // generic-proxy writes -> visible to the tensor cores
+      tmem_st_wait();      // A in TMEM complete
+      fence_async_smem();  // B in shared memory -> visible to the tensor cores
+      tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&conv[s]);
-      if (warp == 2 && lane == 0 && kb < 8) stamp(10 + kb);  // slots 10..17: K block converted
+      if (warp == 2 && lane == 0 && kb < 8) stamp(10 + kb);  // slots 10..17: converted
     }
   } else if (warp >= 2 + kConvWarps) {
-    // ---------------------------------------------------------------- promotion + epilogue
-    const int q = warp & 3;  // TMEM lane quarter
-    const int r = q * 32 + lane;
-    const int i = mt * BM + r;
-    float acc[BN];
-#pragma unroll
-    for (int t = 0; t < BN; ++t) acc[t] = 0.f;
+    // ---------------------------------------------------------------- promotion
+    // (whole warps only: lanes 1..31 of warps 0 and 1 take no role and go on to the
+    // epilogue)
+    const int pw = warp - (2 + kConvWarps);
+    const int q = warp & 3;           // TMEM lane quarter of this warp
+    const int r = q * 32 + lane;      // tile row of this thread
+    const uint32_t lane_base = tmem_base + ((uint32_t)(q * 32) << 16);
+    // the epilogue terms are inputs of this launch: fetch their tiles now, to land while the
+    // K loop runs
+    for (int e = 0; e < 2; ++e) {
+      const float* E = e == 0 ? p.E1 : p.E2;
+      if (!E) continue;
+      for (int g = pw * 32 + lane; g < rows * G4; g += kPromWarps * 32) {
+        const int rr = g / G4, c = 4 * (g % G4);
+        cp_async16(etile + e * TILE + rr * BN + c, E + base + (long long)(i0 + rr) * b + j0 + c);
+      }
+    }
     bool ok_all = true;
     for (int kb = 0; kb < num_kb; ++kb) {
       const int a = kb % NACC;
@@ -311,77 +389,107 @@ __global__ void __launch_bounds__(kThreadsCnp, 1)
       }
       tc_fence_after();
 #pragma unroll
-      for (int c0 = 0; c0 < BN; c0 += 32) {
-        uint32_t v[32];
-        tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(a * BN + c0), v);
+      for (int c0 = 0; c0 < CW; c0 += 16) {
+        uint32_t v[16], w[16];
+        tmem_ld_32x32b_x16(lane_base + (uint32_t)(a * BN + c0), v);
+        if (kb > 0) tmem_ld_32x32b_x16(lane_base + (uint32_t)(SUM_COL + c0), w);
         tmem_ld_wait();
+        if (kb > 0) {
 #pragma unroll
-        for (int t = 0; t < 32; ++t) acc[c0 + t] += __uint_as_float(v[t]);
+          for (int t = 0; t < 16; ++t)
+            v[t] = __float_as_uint(__uint_as_float(w[t]) + __uint_as_float(v[t]));
+        }
+        tmem_st_32x32b_x16(lane_base + (uint32_t)(SUM_COL + c0), v);
       }
+      tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty[a]);
-      if (warp == 2 + kConvWarps && lane == 0 && kb < 8) stamp(18 + kb);  // 18..25: promoted
+      if (pw == 0 && lane == 0 && kb < 8) stamp(18 + kb);  // slots 18..25: promoted
     }
-    if (warp == 2 + kConvWarps && lane == 0) stamp(26);  // epilogue start
-    const long long base = (long long)blk * b * b;
-    if (ok_all && i < b) {
+    // the sum goes to a shared-memory tile (the ring is idle: every MMA has completed)
+    if (ok_all && num_kb > 0) {
+      tc_fence_after();
 #pragma unroll
-      for (int c0 = 0; c0 < BN; c0 += 32) {
-        const int j0 = nt * BN + c0;
-        const long long idx0 = base + (long long)i * b + j0;
-        float o[32];
+      for (int c0 = 0; c0 < CW; c0 += 16) {
+        uint32_t v[16];
+        tmem_ld_32x32b_x16(lane_base + (uint32_t)(SUM_COL + c0), v);
+        tmem_ld_wait();
 #pragma unroll
-        for (int t = 0; t < 32; ++t) o[t] = acc[c0 + t];
-        if (p.E1) {
-          const float4* e = reinterpret_cast<const float4*>(p.E1 + idx0);
+        for (int t = 0; t < 16; t += 4)
+          *reinterpret_cast<float4*>(tile + r * LD + c0 + t) =
+              make_float4(__uint_as_float(v[t]), __uint_as_float(v[t + 1]),
+                          __uint_as_float(v[t + 2]), __uint_as_float(v[t + 3]));
+      }
+    }
+    cp_async_wait_all();
+    if (!ok_all) *abort_flag = 1;
+  }
+
+  // ------------------------------------------------------------------ epilogue (all warps)
+  // out = sum + e1 E1 + e2 E2 + eI I; every global store is coalesced and 8 or 16 bytes wide
+  const bool live = __syncthreads_or(*abort_flag) == 0;
+  if (threadIdx.x == 0) stamp(26);  // slot 26: tile staged
+  const int ng = rows * G4;
+  if (live) {
+    for (int g = threadIdx.x; g < ng; g += kThreadsCnp) {
+      const int rr = g / G4, c = 4 * (g % G4);
+      const int i = i0 + rr, j = j0 + c;
+      float4* tp = reinterpret_cast<float4*>(tile + rr * LD + c);
+      float4 o = *tp;
+      if (p.E1) {
+        const float4 w = *reinterpret_cast<const float4*>(etile + rr * BN + c);
+        o.x = fmaf(p.e1, w.x, o.x);
+        o.y = fmaf(p.e1, w.y, o.y);
+        o.z = fmaf(p.e1, w.z, o.z);
+        o.w = fmaf(p.e1, w.w, o.w);
+      }
+      if (p.E2) {
+        const float4 w = *reinterpret_cast<const float4*>(etile + TILE + rr * BN + c);
+        o.x = fmaf(p.e2, w.x, o.x);
+        o.y = fmaf(p.e2, w.y, o.y);
+        o.z = fmaf(p.e2, w.z, o.z);
+        o.w = fmaf(p.e2, w.w, o.w);
+      }
+      if (i == j) o.x += p.eI;
+      if (i == j + 1) o.y += p.eI;
+      if (i == j + 2) o.z += p.eI;
+      if (i == j + 3) o.w += p.eI;
+      *tp = o;
+      const long long idx = base + (long long)i * b + j;
+      if (p.out_f32) *reinterpret_cast<float4*>(p.out_f32 + idx) = o;
+      if (p.out_bf16)
+        *reinterpret_cast<uint2*>(p.out_bf16 + idx) =
+            make_uint2(pack_bf16x2(o.x, o.y), pack_bf16x2(o.z, o.w));
+    }
+  }
+  if (p.out_f32_t || p.out_bf16_t) {
+    __syncthreads();
+    if (live) {
+      // transposed outputs: consecutive threads take consecutive rows (rows % 32 == 0), so
+      // each of the four stores of a float4 group is coalesced
+      for (int g = threadIdx.x; g < ng; g += kThreadsCnp) {
+        const int rr = g % rows, c = 4 * (g / rows);
+        const float4 v = *reinterpret_cast<const float4*>(tile + rr * LD + c);
+        const float o[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-          for (int t = 0; t < 8; ++t) {
-            const float4 w = __ldg(e + t);
-            o[4 * t] = fmaf(p.e1, w.x, o[4 * t]);
-            o[4 * t + 1] = fmaf(p.e1, w.y, o[4 * t + 1]);
-            o[4 * t + 2] = fmaf(p.e1, w.z, o[4 * t + 2]);
-            o[4 * t + 3] = fmaf(p.e1, w.w, o[4 * t + 3]);
-          }
-        }
-        if (p.E2) {
-          const float4* e = reinterpret_cast<const float4*>(p.E2 + idx0);
-#pragma unroll
-          for (int t = 0; t < 8; ++t) {
-            const float4 w = __ldg(e + t);
-            o[4 * t] = fmaf(p.e2, w.x, o[4 * t]);
-            o[4 * t + 1] = fmaf(p.e2, w.y, o[4 * t + 1]);
-            o[4 * t + 2] = fmaf(p.e2, w.z, o[4 * t + 2]);
-            o[4 * t + 3] = fmaf(p.e2, w.w, o[4 * t + 3]);
-          }
-        }
-#pragma unroll
-        for (int t = 0; t < 32; ++t)
-          if (j0 + t == i) o[t] += p.eI;
-        if (p.out_f32) {
-          float4* d = reinterpret_cast<float4*>(p.out_f32 + idx0);
-#pragma unroll
-          for (int t = 0; t < 8; ++t) d[t] = make_float4(o[4 * t], o[4 * t + 1], o[4 * t + 2], o[4 * t + 3]);
-        }
-        if (p.out_f32_t) {  // lanes hold consecutive rows i: each store is coalesced
-#pragma unroll
-          for (int t = 0; t < 32; ++t) p.out_f32_t[base + (long long)(j0 + t) * b + i] = o[t];
-        }
-        if (p.out_bf16) {
-          uint4* d = reinterpret_cast<uint4*>(p.out_bf16 + idx0);
-#pragma unroll
-          for (int t = 0; t < 4; ++t)
-            d[t] = make_uint4(pack_bf16x2(o[8 * t], o[8 * t + 1]), pack_bf16x2(o[8 * t + 2], o[8 * t + 3]),
-                              pack_bf16x2(o[8 * t + 4], o[8 * t + 5]), pack_bf16x2(o[8 * t + 6], o[8 * t + 7]));
-        }
-        if (p.out_bf16_t) {
-#pragma unroll
-          for (int t = 0; t < 32; ++t)
-            p.out_bf16_t[base + (long long)(j0 + t) * b + i] = __float2bfloat16_rn(o[t]);
+        for (int k = 0; k < 4; ++k) {
+          const long long tidx = base + (long long)(j0 + c + k) * b + (i0 + rr);
+          if (p.out_f32_t) p.out_f32_t[tidx] = o[k];
+          if (p.out_bf16_t) p.out_bf16_t[tidx] = __float2bfloat16_rn(o[k]);
         }
       }
     }
   }
+
+  // ------------------------------------------------------------------ teardown
+  if (warp == 0 && lane == 0 && *abort_flag) {
+    // drain: the last STAGES K blocks issued may still be landing
+    for (int g = tma_issued - 1; g >= 0 && g >= tma_issued - STAGES; --g)
+      mbar_wait_bounded(&full[g % STAGES], (g / STAGES) & 1, p.err, p.limit_ns);
+  }
+  if (warp == 1 && lane == 0 && mma_last >= 0)  // TMEM is freed below: the MMAs must be done
+    mbar_wait_bounded(&tfull[mma_last % NACC], (mma_last / NACC) & 1, p.err, p.limit_ns);
   tc_fence_before();
   __syncthreads();
   if (threadIdx.x == 0) stamp(31);
@@ -448,10 +556,10 @@ bool make_blk_map(CUtensorMap* m, const float* ptr, int nblk, int b, int box_row
   return true;
 }
 
-template <int BN, int STAGES>
+template <int BN>
 poetx_status launch_t(const CnpMaps& maps, const CnpUParams& p, int nblk, cudaStream_t s) {
-  auto k = cnp_umma_kernel<BN, STAGES>;
-  constexpr int smem = STAGES * (2 * BM * BK * 4 + 2 * BN * BK * 4) + 1024 + 256;
+  auto k = cnp_umma_kernel<BN>;
+  constexpr int smem = cnp_smem<BN>();
   static_assert(smem <= 227 * 1024, "shared memory per CTA exceeds the sm_103 limit");
   static std::once_flag once;
   static cudaError_t attr = cudaSuccess;
@@ -491,7 +599,6 @@ poetx_status cnp_umma_product(const CnpProduct& g, int nblk, cudaStream_t s) {
   };
   CnpUParams p{};
   p.b = g.b;
-  p.nmaps = nmaps;
   p.nseg = g.nseg;
   p.kb_per_seg = g.b / BK;
   for (int sg = 0; sg < g.nseg; ++sg) {
@@ -516,8 +623,8 @@ poetx_status cnp_umma_product(const CnpProduct& g, int nblk, cudaStream_t s) {
   p.limit_ns = kWaitLimitNs;
   p.trace = trace_buffer(&p.trace_cap);
   p.nmaps = nmaps;
-  if (BN == 64) return launch_t<64, 4>(maps, p, nblk, s);
-  return launch_t<32, 4>(maps, p, nblk, s);
+  if (BN == 64) return launch_t<64>(maps, p, nblk, s);
+  return launch_t<32>(maps, p, nblk, s);
 }
 
 }  // namespace poetx
