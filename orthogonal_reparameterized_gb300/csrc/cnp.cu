@@ -25,6 +25,8 @@
 // (XS + SX) T + S^2 (XP + PX) with S = I + P, T = I + P^2 = I + Q2, S^2 = I - 2Q + Q2;
 // expanding the products gives the expression above.  Work per block: forward 3 b^3 FMA
 // (Q2 half by symmetry, then one full product), backward 5 b^3 FMA.
+#include <mutex>
+
 #include "cnp_umma.h"
 #include "common.cuh"
 #include "kernels.h"
@@ -174,6 +176,79 @@ __global__ void sum_partials_kernel(const float* __restrict__ dG0, int S0, int n
   }
 }
 
+// The same sum for b % 64 == 0, one 32 x 64 tile per CTA: the partial tiles land in shared
+// memory by 16-byte cp.async, kSumChunk partials at a time, so that all loads of a chunk are
+// in flight together and no register waits on them; each thread then adds its two float4
+// groups in the order s = 0, 1, ... (the same sums, bit for bit, as the kernel above).
+constexpr int kSumR = 32, kSumC = 64, kSumChunk = 5;
+constexpr size_t kSumSmem = (size_t)(kSumChunk * kSumR * kSumC + kSumC * (kSumR + 1)) * 4;
+
+__global__ void __launch_bounds__(256) sum_partials_vec_kernel(const float* __restrict__ dG0,
+                                                                int S0, int n0,
+                                                                const float* __restrict__ dG1,
+                                                                int S1, int n1, int b,
+                                                                float* __restrict__ X,
+                                                                float* __restrict__ Xt) {
+  pdl_trigger();
+  pdl_wait();
+  extern __shared__ __align__(16) float ssm[];
+  float* T = ssm + kSumChunk * kSumR * kSumC;  // [kSumC][kSumR + 1] transposed tile
+  const int j = blockIdx.z;
+  const float* src = j < n0 ? dG0 + (long long)j * b * b : dG1 + (long long)(j - n0) * b * b;
+  const int S = j < n0 ? S0 : S1;
+  const long long sstride = (long long)(j < n0 ? n0 : n1) * b * b;
+  const int r0 = blockIdx.y * kSumR, c0 = blockIdx.x * kSumC;
+  const long long base = (long long)j * b * b;
+  constexpr int G = kSumR * kSumC / 4;  // float4 groups of the tile (2 per thread)
+  const int tid = threadIdx.x;
+  float4 acc[2];
+  for (int s0 = 0; s0 < S; s0 += kSumChunk) {
+    const int ns = S - s0 < kSumChunk ? S - s0 : kSumChunk;
+    for (int t = 0; t < ns; ++t)
+      for (int g = tid; g < G; g += 256) {
+        const int rr = g / (kSumC / 4), c = 4 * (g % (kSumC / 4));
+        const float* gsrc = src + (long long)(s0 + t) * sstride + (long long)(r0 + rr) * b + c0 + c;
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(
+                         ssm + (t * kSumR + rr) * kSumC + c)),
+                     "l"(gsrc)
+                     : "memory");
+      }
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    __syncthreads();
+    for (int t = 0; t < ns; ++t)
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int g = tid + 256 * u;
+        const int rr = g / (kSumC / 4), c = 4 * (g % (kSumC / 4));
+        const float4 v = *reinterpret_cast<const float4*>(ssm + (t * kSumR + rr) * kSumC + c);
+        if (s0 + t == 0) {
+          acc[u] = v;
+        } else {
+          acc[u].x += v.x;
+          acc[u].y += v.y;
+          acc[u].z += v.z;
+          acc[u].w += v.w;
+        }
+      }
+    __syncthreads();  // the next chunk overwrites the partial tiles
+  }
+#pragma unroll
+  for (int u = 0; u < 2; ++u) {
+    const int g = tid + 256 * u;
+    const int rr = g / (kSumC / 4), c = 4 * (g % (kSumC / 4));
+    *reinterpret_cast<float4*>(X + base + (long long)(r0 + rr) * b + c0 + c) = acc[u];
+    T[(c + 0) * (kSumR + 1) + rr] = acc[u].x;
+    T[(c + 1) * (kSumR + 1) + rr] = acc[u].y;
+    T[(c + 2) * (kSumR + 1) + rr] = acc[u].z;
+    T[(c + 3) * (kSumR + 1) + rr] = acc[u].w;
+  }
+  __syncthreads();
+  for (int e = tid; e < kSumC * kSumR; e += 256) {
+    const int cc = e / kSumR, rr = e % kSumR;
+    Xt[base + (long long)(c0 + cc) * b + r0 + rr] = T[cc * (kSumR + 1) + rr];
+  }
+}
+
 size_t blk_bytes(int nblk, int b) { return align_up((size_t)nblk * b * b * sizeof(float), 256); }
 
 }  // namespace
@@ -249,7 +324,20 @@ poetx_status cnp_backward_sides(const CnpSides& q, const float* Qin, const float
     Q2in = Q2;
   }
   // X = sum of the partials (both sides, fixed order) and its transpose Xt
-  {
+  if (b % kSumC == 0 && aligned16(dG[0]) && (!dG[1] || aligned16(dG[1]))) {
+    static std::once_flag once;
+    static cudaError_t attr = cudaSuccess;
+    std::call_once(once, [] {
+      attr = cudaFuncSetAttribute(sum_partials_vec_kernel,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSumSmem);
+    });
+    POETX_CUDA_TRY(attr);
+    dim3 grid(b / kSumC, b / kSumR, nblk);
+    POETX_CUDA_TRY(launch_pdl(sum_partials_vec_kernel, grid, dim3(256), kSumSmem, s, dG[0],
+                              splits[0], q.n[0], dG[1], splits[1], q.n[1], b, X, Xt));
+    POETX_CUDA_TRY(cudaGetLastError());
+    after_launch(s, ST_CNP_SUM);
+  } else {
     dim3 grid(ceil_div(b, 32), ceil_div(b, 32), nblk);
     POETX_CUDA_TRY(launch_pdl(sum_partials_kernel, grid, dim3(32, 8), 0, s, dG[0], splits[0],
                               q.n[0], dG[1], splits[1], q.n[1], b, X, Xt));

@@ -60,19 +60,39 @@ __global__ void triu_unpack_kernel(const float* __restrict__ q0, int n0, const f
   }
 }
 
+// dq_ij (+)= Qbar_ij - Qbar_ji for i < j.  One CTA per 32 x 32 tile (I, J), I <= J, of a
+// block: the mirrored tile Qbar[J][I] is read with coalesced rows into shared memory and
+// read back transposed, so both reads of Qbar are coalesced; the writes of a row i of the
+// tile are consecutive entries of the packed triangle.
 __global__ void triu_grad_pack_kernel(const float* __restrict__ Qbar, int b, float* __restrict__ dq0,
                                       int n0, float* __restrict__ dq1, int accumulate) {
   pdl_trigger();
   pdl_wait();
+  __shared__ float tile[32][33];
   const int blk = blockIdx.z;
-  const int i = blockIdx.y;
+  const int nt = (b + 31) / 32;
+  int t = blockIdx.x, I = 0;
+  while (t >= nt - I) {
+    t -= nt - I;
+    ++I;
+  }
+  const int J = I + t;
   const long long tri = (long long)b * (b - 1) / 2;
   const float* Qb = Qbar + (long long)blk * b * b;
   float* dqb = blk < n0 ? dq0 + blk * tri : dq1 + (blk - n0) * tri;
-  for (int j = i + 1 + blockIdx.x * blockDim.x + threadIdx.x; j < b; j += gridDim.x * blockDim.x) {
-    const float v = Qb[(long long)i * b + j] - Qb[(long long)j * b + i];
-    float* dst = dqb + tri_index(i, j, b);
-    *dst = accumulate ? *dst + v : v;
+  const int tx = threadIdx.x, ty = threadIdx.y;  // 32 x 8
+  for (int r = ty; r < 32; r += 8) {  // tile[r][c] = Qbar[J*32 + r][I*32 + c]
+    const int j = J * 32 + r, i = I * 32 + tx;
+    tile[r][tx] = (j < b && i < b) ? Qb[(long long)j * b + i] : 0.f;
+  }
+  __syncthreads();
+  for (int r = ty; r < 32; r += 8) {
+    const int i = I * 32 + r, j = J * 32 + tx;
+    if (i < j && j < b) {
+      const float v = Qb[(long long)i * b + j] - tile[tx][r];
+      float* dst = dqb + tri_index(i, j, b);
+      *dst = accumulate ? *dst + v : v;
+    }
   }
 }
 
@@ -94,9 +114,9 @@ poetx_status launch_triu_unpack(const float* q, int nblk, int b, float* Q, cudaS
 poetx_status launch_triu_grad_pack2(const float* Qbar, int n0, int n1, int b, float* dq0, float* dq1,
                                     int accumulate, cudaStream_t s) {
   if (n0 + n1 == 0 || b < 2) return POETX_OK;
-  const int threads = b < 256 ? ((b + 31) / 32) * 32 : 256;
-  dim3 grid(1, b - 1, n0 + n1);
-  POETX_CUDA_TRY(launch_pdl(triu_grad_pack_kernel, grid, dim3(threads), 0, s, Qbar, b, dq0, n0,
+  const int nt = (b + 31) / 32;
+  dim3 grid(nt * (nt + 1) / 2, 1, n0 + n1);
+  POETX_CUDA_TRY(launch_pdl(triu_grad_pack_kernel, grid, dim3(32, 8), 0, s, Qbar, b, dq0, n0,
                             dq1, accumulate));
   POETX_CUDA_TRY(cudaGetLastError());
   after_launch(s, ST_TRIU_PACK);

@@ -46,6 +46,8 @@ struct UmmaParams {
   long long ldc;
   const float* colscale;
   const int32_t* out_perm;  // BLOCKDIAG: output column c is stored at column out_perm[c]
+  const uint8_t* bpre;      // nullable: B operand (a weight, not written by the previous
+  unsigned long long bpre_bytes;  // kernel) to prefetch into L2 while that kernel drains
   unsigned long long* trace;  // diagnostic phase stamps (nullable)
   size_t trace_cap;
   int* err;
@@ -231,6 +233,21 @@ __global__ void __launch_bounds__(gemm_threads<B_I8>(), 1)
   if (warp == 1) {
     tmem_alloc(tmem_slot, TMEM_COLS);
     tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0 && p.bpre) {
+    // this CTA's share of the weight operand into L2 (a prefetch returns no data, so it is
+    // safe before the wait even if the bytes were still being written)
+    const unsigned long long share =
+        ((p.bpre_bytes + gridDim.x - 1) / gridDim.x + 4095) & ~4095ull;
+    const unsigned long long lo = (unsigned long long)blockIdx.x * share;
+    for (unsigned long long off = lo; off < lo + share && off < p.bpre_bytes; off += 32768) {
+      unsigned long long n = p.bpre_bytes - off;
+      n = n < 32768 ? n : 32768;
+      if (off + n > lo + share) n = lo + share - off;
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p.bpre + off),
+                   "r"((uint32_t)(n & ~15ull))
+                   : "memory");
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -669,6 +686,8 @@ poetx_status umma_blockdiag(const void* X, long long N, int nblk, int b, const v
   p.ldc = D;
   p.colscale = col_scale;
   p.out_perm = out_perm;
+  p.bpre = static_cast<const uint8_t*>(G);
+  p.bpre_bytes = (unsigned long long)nblk * b * b * 2;
   const int tm = (int)((N + BM - 1) / BM), tn = b / BN;
   // resident G panel of b/64 K blocks; the ring carries only the activation tiles
   if (trans) {
@@ -696,6 +715,8 @@ poetx_status umma_wprime(const void* A, long long N, int m, int n, const void* W
   p.M = (int)N;
   p.colscale = (w_i8 && !trans) ? w_scale : nullptr;  // int8 forward: C[:, r] *= s_r
   p.C = C;
+  p.bpre = static_cast<const uint8_t*>(W);
+  p.bpre_bytes = (unsigned long long)m * n * (w_i8 ? 1 : 2);
   const int tm = (int)((N + BM - 1) / BM);
   if (!trans) {  // C[N,n] = A[N,m] W^T
     if (!make_map(&ta, A, m, N, m, 64, 128)) return POETX_ERR_CUDA;
