@@ -86,9 +86,12 @@ unsigned long long poetx_launch_count(void);
  * the previous event (host arrays of `cap` entries, nullable); it returns the number of
  * launches timed and forgets them.  Stage ids are named by poetx_stage_name. */
 poetx_status poetx_profile_enable(int on);
-/* Diagnostic phase trace: with a device buffer set (NULL turns it off), the tensor-core GEMM
- * kernels write %globaltimer stamps (ns) of their phases, 32 unsigned 64-bit slots per CTA,
- * CTA-major, into it (slots beyond `bytes` are dropped).  Each launch overwrites it. */
+/* Diagnostic phase trace: with a device buffer set (NULL turns it off), the library's kernels
+ * write %globaltimer stamps (ns) of their phases into it, 32 unsigned 64-bit slots per CTA,
+ * CTA-major.  The k-th launch after the buffer was set writes region k of 1024 x 32 slots
+ * (slot 0: CTA start, slot 31: CTA end); launches beyond `bytes` write nothing.  The regions
+ * are fixed when a launch is recorded, so a captured CUDA graph writes the same regions on
+ * every replay. */
 poetx_status poetx_set_trace_buffer(void* buf, size_t bytes);
 int poetx_profile_collect(int* stage, float* ms, int cap);
 const char* poetx_stage_name(int stage);

@@ -171,15 +171,31 @@ extern "C" int poetx_profile_collect(int* stage, float* ms, int cap) {
 
 static std::atomic<unsigned long long*> g_trace{nullptr};
 static std::atomic<size_t> g_trace_slots{0};
+static std::atomic<size_t> g_trace_next{0};  // region of the next launch
 
+// Each launch gets its own region of kTraceRegionCtas CTAs (the k-th launch since the buffer
+// was set writes region k), so that the launches of a captured graph keep separate stamps.
 unsigned long long* poetx::trace_buffer(size_t* slots) {
-  *slots = g_trace_slots.load();
-  return g_trace.load();
+  unsigned long long* base = g_trace.load();
+  const size_t total = g_trace_slots.load();
+  constexpr size_t region = (size_t)kTraceRegionCtas * kTraceSlots;
+  if (!base) {
+    *slots = 0;
+    return nullptr;
+  }
+  const size_t k = g_trace_next.fetch_add(1);
+  if ((k + 1) * region > total) {
+    *slots = 0;
+    return nullptr;
+  }
+  *slots = region;
+  return base + k * region;
 }
 
 extern "C" poetx_status poetx_set_trace_buffer(void* buf, size_t bytes) {
   if (buf && !aligned16(buf)) return POETX_ERR_ALIGN;
   g_trace_slots.store(buf ? bytes / 8 : 0);
+  g_trace_next.store(0);
   g_trace.store(static_cast<unsigned long long*>(buf));
   return POETX_OK;
 }

@@ -188,7 +188,10 @@ __global__ void __launch_bounds__(256) sum_partials_vec_kernel(const float* __re
                                                                 const float* __restrict__ dG1,
                                                                 int S1, int n1, int b,
                                                                 float* __restrict__ X,
-                                                                float* __restrict__ Xt) {
+                                                                float* __restrict__ Xt,
+                                                                unsigned long long* tr,
+                                                                size_t tr_cap) {
+  if (threadIdx.x == 0) trace_stamp3(tr, tr_cap, 0);
   pdl_trigger();
   pdl_wait();
   extern __shared__ __align__(16) float ssm[];
@@ -246,6 +249,10 @@ __global__ void __launch_bounds__(256) sum_partials_vec_kernel(const float* __re
   for (int e = tid; e < kSumC * kSumR; e += 256) {
     const int cc = e / kSumR, rr = e % kSumR;
     Xt[base + (long long)(c0 + cc) * b + r0 + rr] = T[cc * (kSumR + 1) + rr];
+  }
+  if (tr) {
+    __syncthreads();
+    if (threadIdx.x == 0) trace_stamp3(tr, tr_cap, 31);
   }
 }
 
@@ -333,8 +340,10 @@ poetx_status cnp_backward_sides(const CnpSides& q, const float* Qin, const float
     });
     POETX_CUDA_TRY(attr);
     dim3 grid(b / kSumC, b / kSumR, nblk);
+    size_t tr_cap = 0;
+    unsigned long long* tr = trace_buffer(&tr_cap);
     POETX_CUDA_TRY(launch_pdl(sum_partials_vec_kernel, grid, dim3(256), kSumSmem, s, dG[0],
-                              splits[0], q.n[0], dG[1], splits[1], q.n[1], b, X, Xt));
+                              splits[0], q.n[0], dG[1], splits[1], q.n[1], b, X, Xt, tr, tr_cap));
     POETX_CUDA_TRY(cudaGetLastError());
     after_launch(s, ST_CNP_SUM);
   } else {

@@ -79,6 +79,7 @@ void prof_begin(cudaStream_t s);
 // stamps of their phases into it, kTraceSlots 64-bit slots per CTA.
 unsigned long long* trace_buffer(size_t* slots);
 constexpr int kTraceSlots = 32;
+constexpr int kTraceRegionCtas = 1024;  // CTAs of one launch's region of the trace buffer
 
 // ------------------------------------------------------------------------------------
 // device helpers
@@ -96,6 +97,14 @@ __device__ __forceinline__ unsigned long long global_ns() {
   return t;
 }
 
+// Stamp by the CTA's linear index over a 3-D grid.
+__device__ __forceinline__ void trace_stamp3(unsigned long long* tr, size_t cap, int slot) {
+  if (tr) {
+    const size_t lin = blockIdx.x + (size_t)gridDim.x * (blockIdx.y + (size_t)gridDim.y * blockIdx.z);
+    const size_t i = lin * kTraceSlots + slot;
+    if (i < cap) tr[i] = global_ns();
+  }
+}
 __device__ __forceinline__ void trace_stamp(unsigned long long* tr, size_t cap, int slot) {
   if (tr) {
     const size_t i = (size_t)blockIdx.x * kTraceSlots + slot;

@@ -25,7 +25,9 @@ __device__ __forceinline__ long long tri_index(int i, int j, int b) {
 // writes Q[I][J] and, through shared memory, the mirrored tile Q[J][I] = -Q[I][J]^T, both
 // with coalesced rows.
 __global__ void triu_unpack_kernel(const float* __restrict__ q0, int n0, const float* __restrict__ q1,
-                                   int b, float* __restrict__ Q) {
+                                   int b, float* __restrict__ Q, unsigned long long* tr,
+                                   size_t tr_cap) {
+  if (threadIdx.x == 0 && threadIdx.y == 0) trace_stamp3(tr, tr_cap, 0);
   pdl_trigger();
   pdl_wait();
   __shared__ float tile[32][33];
@@ -52,11 +54,16 @@ __global__ void triu_unpack_kernel(const float* __restrict__ q0, int n0, const f
     }
     tile[r][tx] = v;
   }
-  if (I == J) return;  // the diagonal tile wrote both of its triangles already
-  __syncthreads();
-  for (int c = ty; c < 32; c += 8) {
-    const int i = J * 32 + c, j = I * 32 + tx;  // Q[i][j] = -Q[j][i]
-    if (i < b && j < b) Qb[(long long)i * b + j] = -tile[tx][c];
+  if (I != J) {  // the diagonal tile wrote both of its triangles already
+    __syncthreads();
+    for (int c = ty; c < 32; c += 8) {
+      const int i = J * 32 + c, j = I * 32 + tx;  // Q[i][j] = -Q[j][i]
+      if (i < b && j < b) Qb[(long long)i * b + j] = -tile[tx][c];
+    }
+  }
+  if (tr) {
+    __syncthreads();
+    if (threadIdx.x == 0 && threadIdx.y == 0) trace_stamp3(tr, tr_cap, 31);
   }
 }
 
@@ -65,7 +72,9 @@ __global__ void triu_unpack_kernel(const float* __restrict__ q0, int n0, const f
 // read back transposed, so both reads of Qbar are coalesced; the writes of a row i of the
 // tile are consecutive entries of the packed triangle.
 __global__ void triu_grad_pack_kernel(const float* __restrict__ Qbar, int b, float* __restrict__ dq0,
-                                      int n0, float* __restrict__ dq1, int accumulate) {
+                                      int n0, float* __restrict__ dq1, int accumulate,
+                                      unsigned long long* tr, size_t tr_cap) {
+  if (threadIdx.x == 0 && threadIdx.y == 0) trace_stamp3(tr, tr_cap, 0);
   pdl_trigger();
   pdl_wait();
   __shared__ float tile[32][33];
@@ -94,6 +103,10 @@ __global__ void triu_grad_pack_kernel(const float* __restrict__ Qbar, int b, flo
       *dst = accumulate ? *dst + v : v;
     }
   }
+  if (tr) {
+    __syncthreads();
+    if (threadIdx.x == 0 && threadIdx.y == 0) trace_stamp3(tr, tr_cap, 31);
+  }
 }
 
 poetx_status launch_triu_unpack2(const float* q0, int n0, const float* q1, int n1, int b, float* Q,
@@ -101,7 +114,10 @@ poetx_status launch_triu_unpack2(const float* q0, int n0, const float* q1, int n
   if (n0 + n1 == 0) return POETX_OK;
   const int nt = (b + 31) / 32;
   dim3 grid(nt * (nt + 1) / 2, 1, n0 + n1);
-  POETX_CUDA_TRY(launch_pdl(triu_unpack_kernel, grid, dim3(32, 8), 0, s, q0, n0, q1, b, Q));
+  size_t tr_cap = 0;
+  unsigned long long* tr = trace_buffer(&tr_cap);
+  POETX_CUDA_TRY(launch_pdl(triu_unpack_kernel, grid, dim3(32, 8), 0, s, q0, n0, q1, b, Q, tr,
+                            tr_cap));
   POETX_CUDA_TRY(cudaGetLastError());
   after_launch(s, ST_TRIU_UNPACK);
   return POETX_OK;
@@ -116,8 +132,10 @@ poetx_status launch_triu_grad_pack2(const float* Qbar, int n0, int n1, int b, fl
   if (n0 + n1 == 0 || b < 2) return POETX_OK;
   const int nt = (b + 31) / 32;
   dim3 grid(nt * (nt + 1) / 2, 1, n0 + n1);
+  size_t tr_cap = 0;
+  unsigned long long* tr = trace_buffer(&tr_cap);
   POETX_CUDA_TRY(launch_pdl(triu_grad_pack_kernel, grid, dim3(32, 8), 0, s, Qbar, b, dq0, n0,
-                            dq1, accumulate));
+                            dq1, accumulate, tr, tr_cap));
   POETX_CUDA_TRY(cudaGetLastError());
   after_launch(s, ST_TRIU_PACK);
   return POETX_OK;
