@@ -15,7 +15,7 @@
 //               straight into tensor memory (where the MMA reads it), the B operand in place
 //               in shared memory (same swizzled offsets, so the layout is kept)
 //   warp 1      three tcgen05.mma kind::tf32 per K=8 step into the K block's accumulator
-//   warps 10-13 promotion: add each K block's accumulator into the running sum (in TMEM)
+//   warps 10..  promotion: add each K block's accumulator into the running sum (in TMEM)
 //   all warps   epilogue: out = sum + e1 E1 + e2 E2 + eI I through a shared-memory tile,
 //               stored as fp32 / fp32^T / bf16 / bf16^T with coalesced 16-byte accesses
 // Both operand tiles are K-major (kind::tf32 takes no MN-major operand): A tiles are rows of
@@ -133,17 +133,25 @@ __device__ __forceinline__ void combine_split(float4* x, float4* y, float c0, fl
   *y = make_float4(lo[0], lo[1], lo[2], lo[3]);
 }
 
-// Warp roles: 0 TMA producer, 1 MMA issuer (and TMEM owner), 2..9 converters, 10..13
-// promotion.  Converter warp w forms and splits the A operand of its TMEM lane quarter w % 4
+// Warp roles: 0 TMA producer, 1 MMA issuer (and TMEM owner), 2..9 converters, 10.. promotion.  Converter warp w forms and splits the A operand of its TMEM lane quarter w % 4
 // (rows 32 (w % 4) .. +31, K columns 16 ((w - 2) / 4) .. +15) and writes hi and lo into
 // tensor memory; the B operand is formed and split in shared memory by all converters.
-// Promotion warp w adds each K block's accumulator of its lane quarter into the running sum,
-// kept in TMEM as well so that it holds no accumulator registers.  TMEM columns: NACC
+// Promotion warp w adds each K block's accumulator of its lane quarter w % 4 (and column
+// slice) into the running sum, kept in TMEM as well so that it holds no accumulator registers.  TMEM columns: NACC
 // accumulators of BN, the running sum (BN), then STAGES A slots of 64 (hi 32 + lo 32).
-constexpr int NACC = 4;
 constexpr int kConvWarps = 8;  // two per TMEM lane quarter
-constexpr int kPromWarps = 4;
-constexpr int kThreadsCnp = 32 * (2 + kConvWarps + kPromWarps);
+// Tiles of 32 or 64 columns: 4 promotion warps, 4 TMEM accumulators, the epilogue-term tiles
+// prefetched into their own shared memory during the K loop.  Tiles of 128 columns (blocks of
+// 256 and up when 64-wide tiles would need more than one wave of CTAs): 8 promotion warps
+// (two per lane quarter, 64 columns each), one accumulator (the accumulators, the running sum
+// and the A slots must fit the 512 TMEM columns), epilogue-term tiles fetched into the idle
+// ring after the K loop.
+__host__ __device__ constexpr int prom_warps(int bn) { return bn >= 128 ? 8 : 4; }
+__host__ __device__ constexpr int cnp_nacc(int bn) { return bn >= 128 ? 1 : 4; }
+__host__ __device__ constexpr bool e_in_ring(int bn) { return bn >= 128; }
+__host__ __device__ constexpr int cnp_threads(int bn) {
+  return 32 * (2 + kConvWarps + prom_warps(bn));
+}
 
 // cp.async (global -> shared, no registers held while in flight; bypasses L1).
 __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
@@ -158,21 +166,33 @@ template <int BN>
 __host__ __device__ constexpr int cnp_stages() { return BN >= 64 ? 3 : 4; }
 // dynamic shared memory: the operand ring, the two epilogue-term tiles, 1 KB of alignment
 // slack and the barriers
+// bytes of the region the ring occupies during the K loop and the epilogue's tiles after it
+template <int BN>
+__host__ __device__ constexpr int cnp_ring_bytes() {
+  return cnp_stages<BN>() * (2 * BM * BK * 4 + 2 * BN * BK * 4) >
+                 (BM * (BN + 4) + (e_in_ring(BN) ? 2 * BM * BN : 0)) * 4
+             ? cnp_stages<BN>() * (2 * BM * BK * 4 + 2 * BN * BK * 4)
+             : (BM * (BN + 4) + (e_in_ring(BN) ? 2 * BM * BN : 0)) * 4;
+}
 template <int BN>
 __host__ __device__ constexpr int cnp_smem() {
-  return cnp_stages<BN>() * (2 * BM * BK * 4 + 2 * BN * BK * 4) + 2 * BM * BN * 4 + 1024 + 256;
+  return cnp_ring_bytes<BN>() + (e_in_ring(BN) ? 0 : 2 * BM * BN * 4) + 1024 + 256;
 }
 
 template <int BN>
-__global__ void __launch_bounds__(kThreadsCnp, 1)
+__global__ void __launch_bounds__(cnp_threads(BN), 1)
     cnp_umma_kernel(const __grid_constant__ CnpMaps maps, const CnpUParams p) {
   constexpr int STAGES = cnp_stages<BN>();
-  constexpr int CW = BN;                      // running-sum columns per promotion thread
+  constexpr int NACC = cnp_nacc(BN);
+  constexpr int kPromWarps = prom_warps(BN);
+  constexpr int kThreadsCnp = cnp_threads(BN);
+  constexpr bool E_RING = e_in_ring(BN);
+  constexpr int CW = BN * 4 / kPromWarps;     // running-sum columns per promotion thread
   constexpr int NCT = 32 * kConvWarps;        // converter threads
   constexpr uint32_t A_BYTES = BM * BK * 4;   // 16 KB per buffer
   constexpr uint32_t B_BYTES = BN * BK * 4;   // BN * 128 bytes per buffer
   constexpr uint32_t STAGE_BYTES = 2 * A_BYTES + 2 * B_BYTES;
-  constexpr uint32_t RING_BYTES = STAGES * STAGE_BYTES;
+  constexpr uint32_t RING_BYTES = cnp_ring_bytes<BN>();  // >= STAGES * STAGE_BYTES
   constexpr uint32_t SUM_COL = NACC * BN;     // running sum
   constexpr uint32_t A_COL = NACC * BN + BN;  // A slots: A_COL + 64 s (+32 for lo)
   constexpr uint32_t TMEM_COLS = A_COL + 64 * STAGES <= 256 ? 256 : 512;
@@ -180,15 +200,17 @@ __global__ void __launch_bounds__(kThreadsCnp, 1)
   constexpr int LD = BN + 4;                  // staged tile pitch (16-byte rows)
   constexpr int TILE = BM * BN;               // floats of one epilogue-term tile
   static_assert(A_COL + 64 * STAGES <= TMEM_COLS, "accumulators, sum and A slots fit TMEM");
-  static_assert(RING_BYTES >= (uint32_t)BM * LD * 4, "the staged tile fits the ring");
+  static_assert(RING_BYTES >= (uint32_t)(BM * LD + (E_RING ? 2 * TILE : 0)) * 4,
+                "the staged tile (and the epilogue-term tiles) fit the ring");
   constexpr uint32_t IDESC = tf32_idesc(BM, BN);
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  float* const tile = reinterpret_cast<float*>(smem);                // epilogue (ring idle)
-  float* const etile = reinterpret_cast<float*>(smem + RING_BYTES);  // [2][BM][BN] E1, E2
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + RING_BYTES + 2 * TILE * 4);
+  float* const tile = reinterpret_cast<float*>(smem);  // epilogue (ring idle)
+  float* const etile = E_RING ? tile + BM * LD           // [2][BM][BN] E1, E2
+                              : reinterpret_cast<float*>(smem + RING_BYTES);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + RING_BYTES + (E_RING ? 0 : 2 * TILE * 4));
   uint64_t* conv = full + STAGES;
   uint64_t* empty = conv + STAGES;
   uint64_t* tfull = empty + STAGES;   // [NACC] accumulator holds a finished K block
@@ -365,18 +387,22 @@ __global__ void __launch_bounds__(kThreadsCnp, 1)
     // epilogue)
     const int pw = warp - (2 + kConvWarps);
     const int q = warp & 3;           // TMEM lane quarter of this warp
+    const int h = pw >> 2;            // column slice of this warp
     const int r = q * 32 + lane;      // tile row of this thread
-    const uint32_t lane_base = tmem_base + ((uint32_t)(q * 32) << 16);
-    // the epilogue terms are inputs of this launch: fetch their tiles now, to land while the
-    // K loop runs
-    for (int e = 0; e < 2; ++e) {
-      const float* E = e == 0 ? p.E1 : p.E2;
-      if (!E) continue;
-      for (int g = pw * 32 + lane; g < rows * G4; g += kPromWarps * 32) {
-        const int rr = g / G4, c = 4 * (g % G4);
-        cp_async16(etile + e * TILE + rr * BN + c, E + base + (long long)(i0 + rr) * b + j0 + c);
+    const uint32_t lane_base = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(h * CW);
+    // the epilogue terms are inputs of this launch: fetch their tiles (now, to land while
+    // the K loop runs, or into the ring once it is idle)
+    auto fetch_e = [&]() {
+      for (int e = 0; e < 2; ++e) {
+        const float* E = e == 0 ? p.E1 : p.E2;
+        if (!E) continue;
+        for (int g = pw * 32 + lane; g < rows * G4; g += kPromWarps * 32) {
+          const int rr = g / G4, c = 4 * (g % G4);
+          cp_async16(etile + e * TILE + rr * BN + c, E + base + (long long)(i0 + rr) * b + j0 + c);
+        }
       }
-    }
+    };
+    if (!E_RING) fetch_e();
     bool ok_all = true;
     for (int kb = 0; kb < num_kb; ++kb) {
       const int a = kb % NACC;
@@ -389,17 +415,25 @@ __global__ void __launch_bounds__(kThreadsCnp, 1)
       }
       tc_fence_after();
 #pragma unroll
-      for (int c0 = 0; c0 < CW; c0 += 16) {
-        uint32_t v[16], w[16];
-        tmem_ld_32x32b_x16(lane_base + (uint32_t)(a * BN + c0), v);
-        if (kb > 0) tmem_ld_32x32b_x16(lane_base + (uint32_t)(SUM_COL + c0), w);
-        tmem_ld_wait();
-        if (kb > 0) {
+      for (int c0 = 0; c0 < CW; c0 += 32) {  // two 16-column chunks per load round trip
+        uint32_t v[2][16], w[2][16];
 #pragma unroll
-          for (int t = 0; t < 16; ++t)
-            v[t] = __float_as_uint(__uint_as_float(w[t]) + __uint_as_float(v[t]));
+        for (int u = 0; u < 2; ++u) {
+          if (c0 + 16 * u >= CW) continue;
+          tmem_ld_32x32b_x16(lane_base + (uint32_t)(a * BN + c0 + 16 * u), v[u]);
+          if (kb > 0) tmem_ld_32x32b_x16(lane_base + (uint32_t)(SUM_COL + c0 + 16 * u), w[u]);
         }
-        tmem_st_32x32b_x16(lane_base + (uint32_t)(SUM_COL + c0), v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          if (c0 + 16 * u >= CW) continue;
+          if (kb > 0) {
+#pragma unroll
+            for (int t = 0; t < 16; ++t)
+              v[u][t] = __float_as_uint(__uint_as_float(w[u][t]) + __uint_as_float(v[u][t]));
+          }
+          tmem_st_32x32b_x16(lane_base + (uint32_t)(SUM_COL + c0 + 16 * u), v[u]);
+        }
       }
       tmem_st_wait();
       tc_fence_before();
@@ -407,7 +441,8 @@ __global__ void __launch_bounds__(kThreadsCnp, 1)
       if (lane == 0) mbar_arrive(&tempty[a]);
       if (pw == 0 && lane == 0 && kb < 8) stamp(18 + kb);  // slots 18..25: promoted
     }
-    // the sum goes to a shared-memory tile (the ring is idle: every MMA has completed)
+    // every MMA has completed, so the ring is idle: the sum goes to a shared-memory tile
+    if (E_RING && ok_all) fetch_e();
     if (ok_all && num_kb > 0) {
       tc_fence_after();
 #pragma unroll
@@ -417,7 +452,7 @@ __global__ void __launch_bounds__(kThreadsCnp, 1)
         tmem_ld_wait();
 #pragma unroll
         for (int t = 0; t < 16; t += 4)
-          *reinterpret_cast<float4*>(tile + r * LD + c0 + t) =
+          *reinterpret_cast<float4*>(tile + r * LD + h * CW + c0 + t) =
               make_float4(__uint_as_float(v[t]), __uint_as_float(v[t + 1]),
                           __uint_as_float(v[t + 2]), __uint_as_float(v[t + 3]));
       }
@@ -568,7 +603,7 @@ poetx_status launch_t(const CnpMaps& maps, const CnpUParams& p, int nblk, cudaSt
   });
   POETX_CUDA_TRY(attr);
   dim3 grid((p.b + BM - 1) / BM, p.b / BN, nblk);
-  POETX_CUDA_TRY(launch_pdl(k, grid, dim3(kThreadsCnp), smem, s, maps, p));
+  POETX_CUDA_TRY(launch_pdl(k, grid, dim3(cnp_threads(BN)), smem, s, maps, p));
   POETX_CUDA_TRY(cudaGetLastError());
   return POETX_OK;
 }
@@ -581,7 +616,10 @@ bool cnp_umma_ok(int b) {
 
 poetx_status cnp_umma_product(const CnpProduct& g, int nblk, cudaStream_t s) {
   if (nblk == 0) return POETX_OK;
-  const int BN = g.b % 64 == 0 ? 64 : 32;
+  // 128-wide tiles once 64-wide ones would take more than one wave of CTAs (one per SM)
+  const long long tiles64 = (long long)((g.b + BM - 1) / BM) * (g.b / 64) * nblk;
+  const int BN = (g.b % 128 == 0 && g.b >= 256 && tiles64 > sm_count()) ? 128
+                 : (g.b % 64 == 0 ? 64 : 32);
   CnpMaps maps;
   const float* ptrs[NMAPS] = {};
   int roles[NMAPS] = {};
@@ -623,6 +661,7 @@ poetx_status cnp_umma_product(const CnpProduct& g, int nblk, cudaStream_t s) {
   p.limit_ns = kWaitLimitNs;
   p.trace = trace_buffer(&p.trace_cap);
   p.nmaps = nmaps;
+  if (BN == 128) return launch_t<128>(maps, p, nblk, s);
   if (BN == 64) return launch_t<64>(maps, p, nblk, s);
   return launch_t<32>(maps, p, nblk, s);
 }
