@@ -38,6 +38,9 @@ def parse():
     ap.add_argument("--workload", default="llama1b_2048")
     ap.add_argument("--variant", default="fast", choices=["fast", "mem"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--all-layers", action="store_true",
+                    help="also time every layer of a multi-layer workload (the Llama-8B "
+                         "block's 7 linears, the 13B MLP's up and down) and report their sum")
     return ap.parse_args()
 
 
@@ -311,6 +314,8 @@ def main():
     clocks.stop()
     launches = kernels_per_step * args.steps
     ms_step = statistics.mean(ms)
+    qs = statistics.quantiles(ms, n=10) if len(ms) >= 10 else [min(ms)] * 9
+    ms_pct = {"p10": qs[0], "p50": statistics.median(ms), "p90": qs[8]}
     if world > 1:
         tt = torch.tensor([ms_step], device=dev)
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
@@ -416,6 +421,97 @@ def main():
                         "peak_source": "152 SMs x 128 FP32 lanes x 2 flop x max SM clock"}}
     del dG, Gb, wsc
 
+    # amortised set-up stages, timed on their own (merge once per permutation draw, the int8
+    # quantiser once per weight): every launch reads and writes the whole weight
+    def median_us(fn, reps=20):
+        for _ in range(3):
+            fn()
+        ts = []
+        for _ in range(reps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1) * 1e3)
+        return statistics.median(ts)
+    setup = {}
+    W0s = torch.randn(n, m, device=dev).to(bf)
+    Wps = torch.empty_like(W0s)
+    us = median_us(lambda: P.poetx_merge_perm(W0s, pn, pm, Wps))
+    by = 2.0 * n * m * esz
+    setup["merge_perm"] = {"us": us, "bytes": by, "gbs": by / (us * 1e-6) / 1e9,
+                           "frac_of_hbm": by / (us * 1e-6) / 1e9 / pk["hbm_gbs"]}
+    W32s = torch.randn(n, m, device=dev)
+    Wqs = torch.empty(n, m, dtype=torch.int8, device=dev)
+    ss = torch.empty(n, device=dev)
+    us = median_us(lambda: P.poetx_quantize_rows_int8(W32s, Wqs, ss))
+    by = 5.0 * n * m
+    setup["quantize_rows_int8"] = {"us": us, "bytes": by, "gbs": by / (us * 1e-6) / 1e9,
+                                   "frac_of_hbm": by / (us * 1e-6) / 1e9 / pk["hbm_gbs"]}
+    del W0s, Wps, W32s, Wqs, ss
+
+    # every layer of a multi-layer workload (on request): the metric of such a workload is
+    # N / (sum of the layers' step times)
+    block = None
+    if args.all_layers and len(wl.layers) > 1:
+        per = []
+        for li, ly in enumerate(wl.layers):
+            li_inp = inputs.layer_inputs(wl, ly)
+            lx = t(li_inp["x"], bf)
+            ldy = t(li_inp["dy"], bf)
+            lpm = t(li_inp["perm_m"], torch.int32)
+            lpn = t(li_inp["perm_n"], torch.int32)
+            lqR = t(li_inp["q_R"], torch.float32)
+            lqP = t(li_inp["q_P"], torch.float32)
+            lsc = None
+            if wl.wdt == "i8":
+                lW32 = t(li_inp["W0"], torch.float32)
+                lWq = torch.empty(ly.n, ly.m, dtype=torch.int8, device=dev)
+                ls = torch.empty(ly.n, device=dev)
+                P.poetx_quantize_rows_int8(lW32, lWq, ls)
+                lWp = torch.empty_like(lWq)
+                lsc = torch.empty_like(ls)
+                P.poetx_merge_perm(lWq, lpn, lpm, lWp, ls, lsc)
+                del lW32
+            else:
+                lW0 = t(li_inp["W0"], bf)
+                lWp = torch.empty_like(lW0)
+                P.poetx_merge_perm(lW0, lpn, lpm, lWp)
+                del lW0
+            LL = P.make_layer(ly.m, ly.n, b, acode, wcode, P.FAST if variant == "fast" else P.MEM,
+                              lpm, lpn, lWp, lqR, lqP, lsc)
+            LB = dict(L=LL, saved=P.workspace(P.poetx_layer_saved_bytes(LL, N), dev),
+                      wsf=P.workspace(P.poetx_layer_workspace_bytes(LL, N, 0), dev),
+                      wsb=P.workspace(P.poetx_layer_workspace_bytes(LL, N, 1), dev),
+                      y=torch.empty(N, ly.n, dtype=bf, device=dev),
+                      dx=torch.empty(N, ly.m, dtype=bf, device=dev),
+                      dqR=torch.empty_like(lqR), dqP=torch.empty_like(lqP))
+
+            def lstep(B=LB, xx=lx, dyy=ldy):
+                P.poetx_layer_fwd(B["L"], xx, B["y"], B["saved"], B["wsf"])
+                P.poetx_layer_bwd(B["L"], xx, dyy, B["saved"], B["dx"], B["dqR"], B["dqP"],
+                                  B["wsb"])
+            side = torch.cuda.Stream(device=dev)
+            side.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(side):
+                for _ in range(3):
+                    lstep()
+            torch.cuda.current_stream().wait_stream(side)
+            torch.cuda.synchronize()
+            lg = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(lg):
+                lstep()
+            torch.cuda.synchronize()
+            lms, _ = timed_steps(None, max(20, args.steps // 20), 5, lg)
+            per.append({"m": ly.m, "n": ly.n, "ms_per_step": statistics.mean(lms)})
+            del LB, lg, lx, ldy, lWp
+            torch.cuda.empty_cache()
+        tot = sum(pl["ms_per_step"] for pl in per)
+        block = {"layers": per, "ms_per_step": tot, "tokens_per_s": N / (tot * 1e-3),
+                 "metric": "N / sum of the layers' fwd+bwd step times"}
+
     # end to end through the C ABI with host buffers (pinned), copies inside the timed region
     hx = x.cpu().pin_memory()
     hdy = dy.cpu().pin_memory()
@@ -468,12 +564,14 @@ def main():
                        "variant": variant, "wdt": wl.wdt,
                        "parallelism": f"replicas x{world} (token-sharded, no collective)",
                        "l2": "flushed between timed steps (512 MiB memset outside the events)"},
-            "variants": {variant: {"tokens_per_s": N / (ms_step * 1e-3), "ms_per_step": ms_step},
+            "variants": {variant: {"tokens_per_s": N / (ms_step * 1e-3), "ms_per_step": ms_step,
+                                   "ms_percentiles": ms_pct},
                          **other},
             "eager": eager,
             "timing": "CUDA-graph replay of the step's C-ABI calls (captured once); 'eager' is "
                       "the same step launched from the host each time",
             "cnp": cnp, "stages": stages, "hbm_stages": hbm, "roofline": roofline,
+            "setup": setup, **({"block": block} if block else {}),
             "cpu_baseline": cpu,
             "e2e": {"value": world * N / (e2e_t * 1e-3), "unit": "tokens/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,

@@ -81,11 +81,15 @@ bool umma_supported();
 poetx_status umma_blockdiag(const void* X, long long N, int nblk, int b, const void* G, int trans,
                             const float* col_scale, const int32_t* out_perm, void* Y,
                             cudaStream_t s);
-// C[N,n] = A[N,m] W^T (trans=0) or C[N,m] = A[N,n] W (trans=1), W [n,m] bf16 or int8
-// (int8: widened to bf16 in shared memory; the forward multiplies column r by w_scale[r],
-// the backward expects A to carry the scale already).
-poetx_status umma_wprime(const void* A, long long N, int m, int n, const void* W, bool w_i8,
-                         const float* w_scale, int trans, void* C, cudaStream_t s);
+// C[N,n] = A[N,m] W^T (trans=0) or C[N,m] = A[N,n] W (trans=1), W [n,m] bf16.
+poetx_status umma_wprime(const void* A, long long N, int m, int n, const void* W, int trans,
+                         void* C, cudaStream_t s);
+// The same contraction with an int8 W, run transposed so that the widened weight is the
+// tensor-memory A operand (K and the output features must be multiples of 64 and 128); the
+// forward multiplies output column r by w_scale[r], the backward expects A to carry the
+// scale already.
+poetx_status umma_wprime_i8(const void* A, long long N, int m, int n, const void* Wq,
+                            const float* w_scale, int trans, void* C, cudaStream_t s);
 // dG[s, j] = X_j^T dY_j over the tokens of split s (fp32 partials).
 poetx_status umma_wgrad(const void* X, const void* dY, long long N, int nblk, int b, int splits,
                         float* dG, cudaStream_t s);

@@ -90,9 +90,10 @@ poetx_status wprime_impl(poetx_dtype act, poetx_dtype wdt, const void* A, long l
                          int n, const void* W, const float* w_scale, int trans, void* C,
                          cudaStream_t s) {
   if (N == 0) return POETX_OK;
-  if (act == POETX_BF16 && (wdt == POETX_BF16 || wdt == POETX_I8) && use_umma() &&
-      m % 256 == 0 && n % 256 == 0)
-    return umma_wprime(A, N, m, n, W, wdt == POETX_I8, w_scale, trans, C, s);
+  if (act == POETX_BF16 && wdt == POETX_I8 && use_umma() && m % 256 == 0 && n % 256 == 0)
+    return umma_wprime_i8(A, N, m, n, W, w_scale, trans, C, s);
+  if (act == POETX_BF16 && wdt == POETX_BF16 && use_umma() && m % 256 == 0 && n % 256 == 0)
+    return umma_wprime(A, N, m, n, W, trans, C, s);
   SimtGemm g{};
   g.M = (int)N; g.batch = 1; g.A = A; g.B = W; g.C = C;
   g.ksplit = 1;

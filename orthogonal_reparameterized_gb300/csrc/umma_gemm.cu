@@ -11,11 +11,13 @@
 // Persistent CTAs walk the 128 x BN output tiles (tile t = blockIdx.x, + gridDim.x, ...; the
 // M index varies fastest so that concurrent CTAs share the B operand in L2).  Warp 0 issues
 // the TMA loads into a STAGES-deep ring, one thread of warp 1 issues the MMAs (4 x K=16 per
-// 64-wide K block) into one of two TMEM accumulators (alternate tiles), and warps 2-5 read
+// 64-wide K block) into one of two TMEM accumulators (alternate tiles), and warps 2-9 read
 // the other accumulator back (tcgen05.ld 32x32b: warp w reads lanes 32*(w%4)..+31 = output
-// rows) and store it, so the epilogue of one tile overlaps the loads and MMAs of the next.  Operands may be K-major (rows of the tile are
-// contiguous along K) or MN-major (contiguous along M/N, e.g. the token-major activations
-// of a weight gradient); both use the canonical 128-byte swizzle layouts of tcgen05.
+// rows) and store it, so the epilogue of one tile overlaps the loads and MMAs of the next.
+// Operands may be K-major (rows of the tile are contiguous along K) or MN-major (contiguous
+// along M/N, e.g. the token-major activations of a weight gradient); both use the canonical
+// 128-byte swizzle layouts of tcgen05.  With an int8 W' the frozen-weight contraction runs
+// in its own kernel (below), transposed.
 // Every mbarrier wait is bounded; on expiry the kernel records POETX_ERR_TIMEOUT, drains
 // its own copies, frees its TMEM and returns.
 #include <atomic>
@@ -132,32 +134,26 @@ __device__ __forceinline__ TileCoords tile_coords(const UmmaParams& p, int t) {
 }
 
 // 8 epilogue warps (2..9): two per TMEM lane quarter, each storing half of the BN columns.
-// With an int8 B operand, 4 more warps (10..13) widen its tiles to bf16 in shared memory.
-// (int8 B: 4 epilogue warps, one per lane quarter, and 8 converter warps instead.)
-template <bool B_I8>
-constexpr int epi_warps() { return B_I8 ? 4 : 8; }
-template <bool B_I8>
-constexpr int conv_warps() { return B_I8 ? 8 : 0; }
-template <bool B_I8>
-constexpr int gemm_threads() { return 64 + 32 * (epi_warps<B_I8>() + conv_warps<B_I8>()); }
+constexpr int kEpiWarps = 8;
+constexpr int kGemmThreads = 64 + 32 * kEpiWarps;
 
-// Bytes of one pipeline stage: A (bf16), B (bf16; absent when B is resident) and, for an
-// int8 B, its raw int8 tile.  RES > 0: B is a resident panel of RES 64-wide K blocks.
-template <int BN, bool B_I8, int RES>
+// Bytes of one pipeline stage: A (bf16) and B (bf16; absent when B is resident).  RES > 0:
+// B is a resident panel of RES 64-wide K blocks.
+template <int BN, int RES>
 constexpr int stage_bytes() {
-  return BM * BK * 2 + (RES > 0 ? 0 : BN * BK * 2) + (B_I8 ? BN * BK : 0);
+  return BM * BK * 2 + (RES > 0 ? 0 : BN * BK * 2);
 }
 template <int BN, int RES>
 constexpr int res_bytes() { return RES * BN * BK * 2; }
 
 // Columns the epilogue stages per pass: 64, or 32 when the operand ring leaves no room.
-template <int BN, int STAGES, bool OUT_F32, bool B_I8, int RES>
+template <int BN, int STAGES, bool OUT_F32, int RES>
 constexpr int epi_pass_cols() {
-  constexpr int ring = STAGES * stage_bytes<BN, B_I8, RES>() + res_bytes<BN, RES>();
+  constexpr int ring = STAGES * stage_bytes<BN, RES>() + res_bytes<BN, RES>();
   constexpr int esz = OUT_F32 ? 4 : 2;
-  constexpr int wc = BN / (epi_warps<B_I8>() / 4);
+  constexpr int wc = BN / (kEpiWarps / 4);
   constexpr int c = (wc < 64) ? wc : 64;
-  return ring + epi_warps<B_I8>() * 32 * (c * esz + 16) + 1280 <= 227 * 1024 ? c : 32;
+  return ring + kEpiWarps * 32 * (c * esz + 16) + 1280 <= 227 * 1024 ? c : 32;
 }
 
 // Two signed bytes of w (bytes lo, lo+1) -> two bf16 in one word, exactly and on the full-rate
@@ -177,13 +173,13 @@ __device__ __forceinline__ uint32_t i8x2_to_bf16x2(uint32_t w, int lo) {
 // B panel of the current (block, column tile) resident in shared memory, so that the ring
 // carries only the streamed A tiles; the panel is reloaded when the range crosses into the
 // next block (guarded by its own full / empty barriers).
-template <int BN, int STAGES, bool A_MN, bool B_MN, bool OUT_F32, bool B_I8, int RES>
-__global__ void __launch_bounds__(gemm_threads<B_I8>(), 1)
+template <int BN, int STAGES, bool A_MN, bool B_MN, bool OUT_F32, int RES>
+__global__ void __launch_bounds__(kGemmThreads, 1)
     umma_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmB, const UmmaParams p) {
   constexpr uint32_t A_BYTES = BM * BK * 2;
   constexpr uint32_t B_BYTES = BN * BK * 2;
-  constexpr uint32_t STAGE_BYTES = stage_bytes<BN, B_I8, RES>();  // int8 tile (if any) after B
+  constexpr uint32_t STAGE_BYTES = stage_bytes<BN, RES>();
   constexpr uint32_t TMEM_COLS = 2 * BN;  // two accumulators
   constexpr uint32_t IDESC = make_idesc(BM, BN, A_MN, B_MN);
 
@@ -193,18 +189,16 @@ __global__ void __launch_bounds__(gemm_threads<B_I8>(), 1)
   // per epilogue warp: 32 rows x 64 columns staging buffer (rows padded by 16 bytes), so
   // that the global stores cover whole row segments instead of 16 bytes of 32 rows each
   constexpr uint32_t ESZ = OUT_F32 ? 4 : 2;
-  constexpr int EPC = epi_pass_cols<BN, STAGES, OUT_F32, B_I8, RES>();  // columns per epilogue pass
+  constexpr int EPC = epi_pass_cols<BN, STAGES, OUT_F32, RES>();  // columns per epilogue pass
   constexpr uint32_t STG_PITCH = EPC * ESZ + 16;
   uint8_t* resb = smem + STAGES * STAGE_BYTES;            // resident B panel (RES > 0)
   uint8_t* staging = resb + res_bytes<BN, RES>();         // EPIW buffers
-  constexpr int EPIW = epi_warps<B_I8>();
-  constexpr int CONVW = conv_warps<B_I8>();
+  constexpr int EPIW = kEpiWarps;
   uint64_t* full = reinterpret_cast<uint64_t*>(staging + EPIW * 32 * STG_PITCH);
   uint64_t* empty = full + STAGES;
   uint64_t* tfull = empty + STAGES;  // [2]
   uint64_t* tempty = tfull + 2;      // [2]
-  uint64_t* conv = tempty + 2;       // [STAGES] int8 B tile widened (B_I8 only)
-  uint64_t* rfull = conv + STAGES;   // resident B panel loaded (RES > 0)
+  uint64_t* rfull = tempty + 2;      // resident B panel loaded (RES > 0)
   uint64_t* rempty = rfull + 1;      // resident B panel no longer read by MMAs (RES > 0)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(rempty + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -222,7 +216,6 @@ __global__ void __launch_bounds__(gemm_threads<B_I8>(), 1)
       mbar_init(&tfull[a], 1);
       mbar_init(&tempty[a], EPIW);
     }
-    for (int s = 0; s < STAGES; ++s) mbar_init(&conv[s], CONVW > 0 ? CONVW : 1);
     mbar_init(rfull, 1);
     mbar_init(rempty, 1);
     *abort_flag = 0;
@@ -303,10 +296,10 @@ __global__ void __launch_bounds__(gemm_threads<B_I8>(), 1)
           ok = false;
           break;
         }
-        mbar_arrive_expect_tx(&full[s], B_I8 ? A_BYTES + BN * BK : (RES > 0 ? A_BYTES : STAGE_BYTES));
+        mbar_arrive_expect_tx(&full[s], RES > 0 ? A_BYTES : STAGE_BYTES);
         if (g == 0) trace_stamp(p.trace, p.trace_cap, 2);  // slot 2: first TMA issued
         uint8_t* sa = smem + s * STAGE_BYTES;
-        uint8_t* sb = B_I8 ? sa + A_BYTES + B_BYTES : sa + A_BYTES;  // int8: raw tile
+        uint8_t* sb = sa + A_BYTES;
         const int k = kb * BK;
         if (!A_MN) {
           tma_load_2d(sa, &tmA, &full[s], c.a_c0 + k, c.a_c1);
@@ -319,7 +312,7 @@ __global__ void __launch_bounds__(gemm_threads<B_I8>(), 1)
           if (!B_MN) {
             tma_load_2d(sb, &tmB, &full[s], c.b_c0 + k, c.b_c1);
           } else {
-            constexpr int BOX_BYTES = B_I8 ? 4096 : 8192;  // 64 x 64 elements
+            constexpr int BOX_BYTES = 8192;  // 64 x 64 elements
 #pragma unroll
             for (int i = 0; i < BN / 64; ++i)
               tma_load_2d(sb + i * BOX_BYTES, &tmB, &full[s], c.b_c0 + 64 * i, c.b_c1 + k);
@@ -361,8 +354,7 @@ __global__ void __launch_bounds__(gemm_threads<B_I8>(), 1)
       for (int kb = 0; kb < c.num_kb; ++kb, ++g) {
         const int s = (int)(g % STAGES);
         const uint32_t ph = (uint32_t)((g / STAGES) & 1);
-        // an int8 B tile is usable once the converter warps have widened it
-        if (*abort_flag || !mbar_wait_bounded(B_I8 ? &conv[s] : &full[s], ph, p.err, p.limit_ns)) {
+        if (*abort_flag || !mbar_wait_bounded(&full[s], ph, p.err, p.limit_ns)) {
           *abort_flag = 1;
           ok = false;
           break;
@@ -383,51 +375,6 @@ __global__ void __launch_bounds__(gemm_threads<B_I8>(), 1)
     if (it > 0) {
       const int last = it - 1;
       mbar_wait_bounded(&tfull[last & 1], (last >> 1) & 1, p.err, p.limit_ns);
-    }
-  } else if (B_I8 && warp >= 2 + EPIW) {
-    // ------------------------------------------------------------ int8 -> bf16 converters
-    // Raw tile: BN rows of 64 bytes (K-major: rows = N, K contiguous; MN-major: BN/64 boxes
-    // of 64 K rows x 64 MN bytes).  bf16 tile: the same rows at 128-byte pitch with 16-byte
-    // chunk c of row r stored at chunk c ^ (r % 8) (128-byte swizzle, both majors).
-    // |q| <= 127, so the widening is exact.
-    const int ct = threadIdx.x - 32 * (2 + EPIW);
-    long long g = 0;
-    bool ok = true;
-    for (int t = t_first; t < t_end && ok; t += t_step) {
-      const TileCoords c = tile_coords<BN, B_MN>(p, t);
-      for (int kb = 0; kb < c.num_kb; ++kb, ++g) {
-        const int s = (int)(g % STAGES);
-        const uint32_t ph = (uint32_t)((g / STAGES) & 1);
-        const bool got = !*abort_flag && mbar_wait_bounded(&full[s], ph, p.err, p.limit_ns);
-        if (!__all_sync(0xffffffffu, got)) {
-          *abort_flag = 1;
-          ok = false;
-          break;
-        }
-        uint8_t* st = smem + s * STAGE_BYTES;
-        const uint8_t* raw = st + A_BYTES + B_BYTES;
-        uint8_t* bt = st + A_BYTES;
-#pragma unroll 2
-        for (int e = ct; e < BN * 4; e += 32 * CONVW) {  // 16 raw bytes = two bf16 chunks
-          const int r = e >> 2, ch = (e & 3) * 2;
-          const uint4 w = *reinterpret_cast<const uint4*>(raw + r * 64 + ch * 8);
-          uint4 o0, o1;
-          o0.x = i8x2_to_bf16x2(w.x, 0);
-          o0.y = i8x2_to_bf16x2(w.x, 2);
-          o0.z = i8x2_to_bf16x2(w.y, 0);
-          o0.w = i8x2_to_bf16x2(w.y, 2);
-          o1.x = i8x2_to_bf16x2(w.z, 0);
-          o1.y = i8x2_to_bf16x2(w.z, 2);
-          o1.z = i8x2_to_bf16x2(w.w, 0);
-          o1.w = i8x2_to_bf16x2(w.w, 2);
-          uint8_t* rowp = bt + r * 128;
-          *reinterpret_cast<uint4*>(rowp + ((ch ^ (r & 7)) << 4)) = o0;
-          *reinterpret_cast<uint4*>(rowp + (((ch + 1) ^ (r & 7)) << 4)) = o1;
-        }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&conv[s]);
-      }
     }
   } else if (warp >= 2) {
     // ------------------------------------------------------------ epilogue
@@ -533,6 +480,294 @@ __global__ void __launch_bounds__(gemm_threads<B_I8>(), 1)
   }
 }
 
+
+// ---------------------------------------------------------------- int8 W' contraction
+// With an int8 W' the contraction runs transposed: D[f, t] = sum_k W(f, k) act[t, k] for
+// output feature f and token t, so that the widened weight is the A operand, which tcgen05
+// reads from tensor memory: converter warps widen the raw int8 tile (exactly, byte-permute
+// construction) straight into TMEM, and shared memory carries only the raw weight tile and
+// the bf16 activation tile (the B operand).  Forward: W(f, k) = Wq[f][k], out[t][f] =
+// s_f D[f, t]; backward: W(f, k) = Wq[k][f] (the activation was scaled by s beforehand),
+// out[t][f] = D[f, t].  Tiles: 128 features x I8T tokens, K blocks of 64; a 4-deep shared-
+// memory ring, two TMEM accumulators (the epilogue of a tile overlaps the next) and a ring
+// of 4 A slots of 32 TMEM columns with its own "slot free" barriers.  The widening (about
+// 1 us per K block per converter group, measured) bounds the kernel, not the MMAs: deeper
+// rings did not help.
+//   warp 0      TMA: raw weight tile (fwd: 128 rows x 64 bytes; bwd: 64 rows x 128 bytes)
+//               and the activation tile (I8T rows x 64 bf16, 128-byte swizzle)
+//   warp 1      MMA issuer: 4 tcgen05.mma kind::f16 (K = 16) per K block, A from TMEM
+//   warps 2-9   converters, two groups of four taking alternate K blocks: warp w widens
+//               the 64 K values of lane quarter w % 4 (rows 32 (w % 4) .. +31)
+//   warps 10-13 epilogue: lane quarter w % 4, all I8T tokens, through a transposing tile
+constexpr int I8T = 192;         // tokens per tile
+constexpr int I8_STAGES = 4;      // shared-memory ring (raw weight + activation tiles)
+constexpr int I8_ASLOTS = 4;      // TMEM ring of widened weight tiles
+constexpr int I8_CONVW = 8;
+constexpr int I8_EPIW = 4;
+constexpr int I8_THREADS = 32 * (2 + I8_CONVW + I8_EPIW);
+constexpr uint32_t I8_W_BYTES = 128 * 64;          // raw weight tile
+constexpr uint32_t I8_X_BYTES = I8T * BK * 2;      // activation tile
+constexpr uint32_t I8_STAGE = I8_X_BYTES + I8_W_BYTES;
+constexpr int I8_STG_PITCH = 80;                   // 32 features x 2 bytes + 16 (conflict-free)
+constexpr int I8_SMEM = I8_STAGES * I8_STAGE + I8_EPIW * 32 * I8_STG_PITCH + 1024 + 512;
+
+struct I8Params {
+  int tiles_f, tiles_t, num_tiles;  // tile t: ft = t % tiles_f, tt = t / tiles_f
+  int num_kb;
+  long long ntok;                   // tokens
+  int nfeat;                        // output features
+  int trans;                        // 0: forward, 1: backward (weight read transposed)
+  const float* scale;               // forward: s_f (nullable)
+  __nv_bfloat16* C;                 // [ntok][nfeat]
+  unsigned long long* trace;
+  size_t trace_cap;
+  int* err;
+  unsigned long long limit_ns;
+};
+
+__device__ __forceinline__ void umma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                             uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__global__ void __launch_bounds__(I8_THREADS, 1)
+    umma_i8_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                   const I8Params p) {
+  constexpr uint32_t ACC_COLS = I8T;           // one accumulator
+  constexpr uint32_t A_COL = 2 * ACC_COLS;     // A slots: A_COL + 32 j
+  constexpr uint32_t TMEM_COLS = 512;
+  static_assert(A_COL + 32 * I8_ASLOTS <= TMEM_COLS, "accumulators and A slots fit TMEM");
+  constexpr uint32_t IDESC = make_idesc(BM, I8T, false, false);
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint8_t* staging = smem + I8_STAGES * I8_STAGE;
+  uint64_t* full = reinterpret_cast<uint64_t*>(staging + I8_EPIW * 32 * I8_STG_PITCH);
+  uint64_t* empty = full + I8_STAGES;
+  uint64_t* conv = empty + I8_STAGES;   // [I8_ASLOTS] slot holds the widened tile of a block
+  uint64_t* afree = conv + I8_ASLOTS;   // [I8_ASLOTS] slot no longer read by MMAs
+  uint64_t* tfull = afree + I8_ASLOTS;  // [2]
+  uint64_t* tempty = tfull + 2;         // [2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) trace_stamp(p.trace, p.trace_cap, 0);
+  pdl_trigger();
+  if (warp == 0 && lane == 0) {
+    for (int s = 0; s < I8_STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int j = 0; j < I8_ASLOTS; ++j) {
+      mbar_init(&conv[j], I8_CONVW / 2);  // one converter group per K block
+      mbar_init(&afree[j], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], I8_EPIW);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tmW);
+    tma_prefetch_desc(&tmX);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const uint32_t smem_base = smem_u32(smem);
+  pdl_wait();
+  if (threadIdx.x == 0) trace_stamp(p.trace, p.trace_cap, 1);
+
+  if (warp == 0 && lane == 0) {
+    // ---------------------------------------------------------------- TMA producer
+    long long g = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+      const int f0 = (t % p.tiles_f) * BM, t0 = (t / p.tiles_f) * I8T;
+      for (int kb = 0; kb < p.num_kb; ++kb, ++g) {
+        const int s = (int)(g % I8_STAGES);
+        const uint32_t ph = (uint32_t)((g / I8_STAGES) & 1);
+        if (*abort_flag || !mbar_wait_bounded(&empty[s], ph ^ 1, p.err, p.limit_ns)) {
+          *abort_flag = 1;
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&full[s], I8_STAGE);
+        if (g < 8) trace_stamp(p.trace, p.trace_cap, 2 + (int)g);  // slots 2..9: K block issued
+        uint8_t* sx = smem + s * I8_STAGE;
+        uint8_t* sw = sx + I8_X_BYTES;
+        tma_load_2d(sx, &tmX, &full[s], kb * BK, t0);  // tokens t0.., K columns kb*64..
+        if (!p.trans)
+          tma_load_2d(sw, &tmW, &full[s], kb * BK, f0);  // rows f0.. of Wq, K bytes kb*64..
+        else
+          tma_load_2d(sw, &tmW, &full[s], f0, kb * BK);  // rows kb*64.. of Wq, bytes f0..
+      }
+    }
+    for (long long j = g - 1; j >= 0 && j >= g - I8_STAGES; --j)
+      mbar_wait_bounded(&full[j % I8_STAGES], (uint32_t)((j / I8_STAGES) & 1), p.err, p.limit_ns);
+  } else if (warp == 1 && lane == 0) {
+    // ---------------------------------------------------------------- MMA issuer
+    long long g = 0;
+    int it = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x, ++it) {
+      const int a = it & 1;
+      if (*abort_flag || !mbar_wait_bounded(&tempty[a], ((it >> 1) & 1) ^ 1, p.err, p.limit_ns)) {
+        *abort_flag = 1;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t d = tmem_base + (uint32_t)(a * ACC_COLS);
+      for (int kb = 0; kb < p.num_kb; ++kb, ++g) {
+        const int s = (int)(g % I8_STAGES);
+        const int j = (int)(g % I8_ASLOTS);
+        if (*abort_flag ||
+            !mbar_wait_bounded(&conv[j], (uint32_t)((g / I8_ASLOTS) & 1), p.err, p.limit_ns)) {
+          *abort_flag = 1;
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (g < 8) trace_stamp(p.trace, p.trace_cap, 18 + (int)g);  // slots 18..25: MMAs issued
+        const uint32_t xa = smem_base + s * I8_STAGE;
+        const uint32_t wa = tmem_base + A_COL + 32u * (uint32_t)j;
+#pragma unroll
+        for (int k = 0; k < BK / 16; ++k)  // K = 16 per MMA: 8 TMEM columns of A
+          umma_bf16_ta(d, wa + 8 * k, tile_desc<false>(xa, k), IDESC, (kb | k) != 0);
+        umma_commit(&empty[s]);
+        if (I8_ASLOTS < I8_STAGES) umma_commit(&afree[j]);
+      }
+      umma_commit(&tfull[a]);
+    }
+    if (it > 0) {
+      const int last = it - 1;
+      mbar_wait_bounded(&tfull[last & 1], (last >> 1) & 1, p.err, p.limit_ns);
+    }
+  } else if (warp >= 2 && warp < 2 + I8_CONVW) {
+    // ---------------------------------------------------------------- converters
+    // group cg = (w - 2) / 4 takes the K blocks g with g % 2 == cg; warp w widens row
+    // f = 32 (w % 4) + lane of the A operand: 64 int8 values -> 32 bf16 pairs -> TMEM slot
+    // g % I8_ASLOTS (|q| <= 127: exact)
+    const int q = warp & 3, cg = (warp - 2) >> 2;
+    const int f = q * 32 + lane;
+    const uint32_t lane_base = tmem_base + ((uint32_t)(q * 32) << 16);
+    long long g = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+      for (int kb = 0; kb < p.num_kb; ++kb, ++g) {
+        if ((int)(g & 1) != cg) continue;
+        const int s = (int)(g % I8_STAGES);
+        const int j = (int)(g % I8_ASLOTS);
+        bool got = !*abort_flag &&
+                   mbar_wait_bounded(&full[s], (uint32_t)((g / I8_STAGES) & 1), p.err, p.limit_ns);
+        // the slot's previous tile must have been read by its MMAs (implied by the ring when
+        // it is no deeper than the slots: the stage was refilled only after those MMAs)
+        if (I8_ASLOTS < I8_STAGES && got && g >= I8_ASLOTS)
+          got = mbar_wait_bounded(&afree[j], (uint32_t)(((g / I8_ASLOTS) - 1) & 1), p.err,
+                                  p.limit_ns);
+        if (!__all_sync(0xffffffffu, got)) {
+          *abort_flag = 1;
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint8_t* raw = smem + s * I8_STAGE + I8_X_BYTES;
+        uint32_t w[32];
+        if (!p.trans) {  // row f: 64 contiguous bytes
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const uint4 x = *reinterpret_cast<const uint4*>(raw + f * 64 + 16 * c);
+            const uint32_t bt[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              w[8 * c + 2 * i] = i8x2_to_bf16x2(bt[i], 0);
+              w[8 * c + 2 * i + 1] = i8x2_to_bf16x2(bt[i], 2);
+            }
+          }
+        } else {  // column f of 64 rows of 128 bytes
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const uint32_t lo = raw[(2 * i) * 128 + f];
+            const uint32_t hi = raw[(2 * i + 1) * 128 + f];
+            w[i] = i8x2_to_bf16x2(lo | (hi << 8), 0);
+          }
+        }
+        const uint32_t col = A_COL + 32u * (uint32_t)j;
+        tmem_st_32x32b_x16(lane_base + col, *reinterpret_cast<const uint32_t(*)[16]>(w));
+        tmem_st_32x32b_x16(lane_base + col + 16, *reinterpret_cast<const uint32_t(*)[16]>(w + 16));
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&conv[j]);
+        if (q == 2 && lane == 0 && g < 8) trace_stamp(p.trace, p.trace_cap, 10 + (int)g);  // converted
+      }
+    }
+  } else if (warp >= 2 + I8_CONVW) {
+    // ---------------------------------------------------------------- epilogue
+    // lane = feature f of quarter q; per 32-token chunk: TMEM -> scaled bf16 -> transposing
+    // tile [token][feature] -> each lane stores one token row of 32 features (64 bytes)
+    const int q = warp & 3;
+    uint8_t* stg = staging + (warp - 2 - I8_CONVW) * 32 * I8_STG_PITCH;
+    int it = 0;
+    for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++it) {
+      const int f0 = (t % p.tiles_f) * BM + q * 32;
+      const long long t0 = (long long)(t / p.tiles_f) * I8T;
+      const int a = it & 1;
+      const bool ok = !*abort_flag && mbar_wait_bounded(&tfull[a], (it >> 1) & 1, p.err, p.limit_ns);
+      if (!__all_sync(0xffffffffu, ok)) {
+        *abort_flag = 1;
+        break;
+      }
+      tc_fence_after();
+      const float sc = (p.scale && f0 + lane < p.nfeat) ? __ldg(p.scale + f0 + lane) : 1.f;
+#pragma unroll 1
+      for (int c0 = 0; c0 < I8T; c0 += 32) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(a * ACC_COLS + c0), r);
+        tmem_ld_wait();
+        // lane f: token j of the chunk at row j, column f of the tile
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          *reinterpret_cast<__nv_bfloat16*>(stg + j * I8_STG_PITCH + lane * 2) =
+              __float2bfloat16_rn(__uint_as_float(r[j]) * sc);
+        __syncwarp();
+        const long long tok = t0 + c0 + lane;
+        if (tok < p.ntok) {
+          const uint4* src = reinterpret_cast<const uint4*>(stg + lane * I8_STG_PITCH);
+          uint4* dst = reinterpret_cast<uint4*>(p.C + tok * p.nfeat + f0);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) dst[i] = src[i];
+        }
+        __syncwarp();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[a]);
+      if (q == 2 && lane == 0 && it < 4) trace_stamp(p.trace, p.trace_cap, 26 + it);  // tile stored
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x == 0) trace_stamp(p.trace, p.trace_cap, 31);
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
 // ---------------------------------------------------------------- host side
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -603,14 +838,14 @@ bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, u
   return make_map_t(m, ptr, inner, outer, pitch_elems, box_inner, box_outer, false);
 }
 
-template <int BN, int STAGES, bool A_MN, bool B_MN, bool OUT_F32, bool B_I8 = false, int RES = 0>
+template <int BN, int STAGES, bool A_MN, bool B_MN, bool OUT_F32, int RES = 0>
 poetx_status launch(const CUtensorMap& ta, const CUtensorMap& tb, UmmaParams p, int tiles_m,
                     int tiles_n, int tiles_z, cudaStream_t s) {
   const int stage = p.mode == MODE_PLAIN ? ST_WPRIME : (p.mode == MODE_BLOCKDIAG ? ST_BLOCKDIAG : ST_WGRAD);
-  auto k = umma_gemm_kernel<BN, STAGES, A_MN, B_MN, OUT_F32, B_I8, RES>;
-  constexpr int smem = STAGES * stage_bytes<BN, B_I8, RES>() + res_bytes<BN, RES>() +
-                       epi_warps<B_I8>() * 32 *
-                           (epi_pass_cols<BN, STAGES, OUT_F32, B_I8, RES>() * (OUT_F32 ? 4 : 2) + 16) +
+  auto k = umma_gemm_kernel<BN, STAGES, A_MN, B_MN, OUT_F32, RES>;
+  constexpr int smem = STAGES * stage_bytes<BN, RES>() + res_bytes<BN, RES>() +
+                       kEpiWarps * 32 *
+                           (epi_pass_cols<BN, STAGES, OUT_F32, RES>() * (OUT_F32 ? 4 : 2) + 16) +
                        1024 + 512;
   // CTAs per SM: bounded by TMEM (2 x BN columns each, 512 per SM) and shared memory.
   constexpr int by_tmem = 512 / (2 * BN);
@@ -632,7 +867,7 @@ poetx_status launch(const CUtensorMap& ta, const CUtensorMap& tb, UmmaParams p, 
   p.num_tiles = (int)tiles;
   const long long want = (long long)sm_count() * per_sm;
   const int grid = (int)(tiles < want ? tiles : want);
-  POETX_CUDA_TRY(launch_pdl(k, dim3(grid), dim3(gemm_threads<B_I8>()), smem, s, ta, tb, p));
+  POETX_CUDA_TRY(launch_pdl(k, dim3(grid), dim3(kGemmThreads), smem, s, ta, tb, p));
   POETX_CUDA_TRY(cudaGetLastError());
   after_launch(s, stage);
   return POETX_OK;
@@ -692,47 +927,87 @@ poetx_status umma_blockdiag(const void* X, long long N, int nblk, int b, const v
   // resident G panel of b/64 K blocks; the ring carries only the activation tiles
   if (trans) {
     switch (b) {
-      case 64: return launch<64, 10, false, false, false, false, 1>(ta, tb, p, tm, tn, nblk, s);
-      case 128: return launch<128, 10, false, false, false, false, 2>(ta, tb, p, tm, tn, nblk, s);
-      case 256: return launch<128, 8, false, false, false, false, 4>(ta, tb, p, tm, tn, nblk, s);
-      default: return launch<128, 4, false, false, false, false, 8>(ta, tb, p, tm, tn, nblk, s);
+      case 64: return launch<64, 10, false, false, false, 1>(ta, tb, p, tm, tn, nblk, s);
+      case 128: return launch<128, 10, false, false, false, 2>(ta, tb, p, tm, tn, nblk, s);
+      case 256: return launch<128, 8, false, false, false, 4>(ta, tb, p, tm, tn, nblk, s);
+      default: return launch<128, 4, false, false, false, 8>(ta, tb, p, tm, tn, nblk, s);
     }
   }
   switch (b) {
-    case 64: return launch<64, 10, false, true, false, false, 1>(ta, tb, p, tm, tn, nblk, s);
-    case 128: return launch<128, 10, false, true, false, false, 2>(ta, tb, p, tm, tn, nblk, s);
-    case 256: return launch<128, 8, false, true, false, false, 4>(ta, tb, p, tm, tn, nblk, s);
-    default: return launch<128, 4, false, true, false, false, 8>(ta, tb, p, tm, tn, nblk, s);
+    case 64: return launch<64, 10, false, true, false, 1>(ta, tb, p, tm, tn, nblk, s);
+    case 128: return launch<128, 10, false, true, false, 2>(ta, tb, p, tm, tn, nblk, s);
+    case 256: return launch<128, 8, false, true, false, 4>(ta, tb, p, tm, tn, nblk, s);
+    default: return launch<128, 4, false, true, false, 8>(ta, tb, p, tm, tn, nblk, s);
   }
 }
 
-poetx_status umma_wprime(const void* A, long long N, int m, int n, const void* W, bool w_i8,
-                         const float* w_scale, int trans, void* C, cudaStream_t s) {
+poetx_status umma_wprime(const void* A, long long N, int m, int n, const void* W, int trans,
+                         void* C, cudaStream_t s) {
   if (N == 0) return POETX_OK;
   CUtensorMap ta, tb;
   UmmaParams p = base_params();
   p.mode = MODE_PLAIN;
   p.M = (int)N;
-  p.colscale = (w_i8 && !trans) ? w_scale : nullptr;  // int8 forward: C[:, r] *= s_r
   p.C = C;
   p.bpre = static_cast<const uint8_t*>(W);
-  p.bpre_bytes = (unsigned long long)m * n * (w_i8 ? 1 : 2);
+  p.bpre_bytes = (unsigned long long)m * n * 2;
   const int tm = (int)((N + BM - 1) / BM);
   if (!trans) {  // C[N,n] = A[N,m] W^T
     if (!make_map(&ta, A, m, N, m, 64, 128)) return POETX_ERR_CUDA;
-    if (!make_map_t(&tb, W, m, n, m, 64, 256, w_i8)) return POETX_ERR_CUDA;
+    if (!make_map(&tb, W, m, n, m, 64, 256)) return POETX_ERR_CUDA;
     p.num_kb = m / 64;
     p.ldc = n;
-    if (w_i8) return launch<256, 3, false, false, false, true>(ta, tb, p, tm, n / 256, 1, s);
     return launch<256, 4, false, false, false>(ta, tb, p, tm, n / 256, 1, s);
   }
   // C[N,m] = A[N,n] W: B operand (output col c, K index r) = W[r][c], MN-major
   if (!make_map(&ta, A, n, N, n, 64, 128)) return POETX_ERR_CUDA;
-  if (!make_map_t(&tb, W, m, n, m, 64, 64, w_i8)) return POETX_ERR_CUDA;
+  if (!make_map(&tb, W, m, n, m, 64, 64)) return POETX_ERR_CUDA;
   p.num_kb = n / 64;
   p.ldc = m;
-  if (w_i8) return launch<256, 3, false, true, false, true>(ta, tb, p, tm, m / 256, 1, s);
   return launch<256, 4, false, true, false>(ta, tb, p, tm, m / 256, 1, s);
+}
+
+// int8 W' contraction (the transposed kernel above).  Forward (trans = 0): C[N, n] =
+// (A[N, m] Wq^T) diag(s); backward (trans = 1): C[N, m] = A[N, n] Wq, A already scaled by s.
+poetx_status umma_wprime_i8(const void* A, long long N, int m, int n, const void* Wq,
+                            const float* w_scale, int trans, void* C, cudaStream_t s) {
+  if (N == 0) return POETX_OK;
+  const int K = trans ? n : m, F = trans ? m : n;  // contraction length, output features
+  if (K % 64 || F % 128) return POETX_ERR_SHAPE;
+  CUtensorMap tw, tx;
+  if (!make_map(&tx, A, K, N, K, 64, I8T)) return POETX_ERR_CUDA;
+  if (!trans) {
+    if (!make_map_t(&tw, Wq, m, n, m, 64, 128, true)) return POETX_ERR_CUDA;
+  } else {
+    if (!make_map_t(&tw, Wq, m, n, m, 128, 64, true)) return POETX_ERR_CUDA;
+  }
+  I8Params p{};
+  p.tiles_f = F / BM;
+  p.tiles_t = (int)((N + I8T - 1) / I8T);
+  const long long tiles = (long long)p.tiles_f * p.tiles_t;
+  if (tiles > 0x7fffffffLL) return POETX_ERR_SHAPE;
+  p.num_tiles = (int)tiles;
+  p.num_kb = K / 64;
+  p.ntok = N;
+  p.nfeat = F;
+  p.trans = trans;
+  p.scale = trans ? nullptr : w_scale;
+  p.C = static_cast<__nv_bfloat16*>(C);
+  p.trace = trace_buffer(&p.trace_cap);
+  p.err = device_error_word();
+  p.limit_ns = kWaitLimitNs;
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [&] {
+    attr_err = cudaFuncSetAttribute(umma_i8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    I8_SMEM);
+  });
+  POETX_CUDA_TRY(attr_err);
+  const int grid = (int)(tiles < sm_count() ? tiles : sm_count());
+  POETX_CUDA_TRY(launch_pdl(umma_i8_kernel, dim3(grid), dim3(I8_THREADS), I8_SMEM, s, tw, tx, p));
+  POETX_CUDA_TRY(cudaGetLastError());
+  after_launch(s, ST_WPRIME);
+  return POETX_OK;
 }
 
 poetx_status umma_wgrad(const void* X, const void* dY, long long N, int nblk, int b, int splits,
