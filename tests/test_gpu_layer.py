@@ -85,7 +85,9 @@ def test_layer_fp32_256_b32(P, variant):
 
 
 @pytest.mark.parametrize("m,n,b,N", [(256, 512, 64, 200), (512, 256, 128, 77), (512, 512, 256, 130),
-                                     (1024, 512, 512, 300)])
+                                     (1024, 512, 512, 300),
+                                     # fewer W' tiles than SMs, ragged token tail
+                                     (2048, 1024, 256, 1000), (1024, 2048, 256, 520)])
 @pytest.mark.parametrize("variant", ["fast", "mem"])
 def test_layer_bf16_small(P, m, n, b, N, variant):
     inp = inputs.small_layer_inputs(31 + b, m, n, b, N, act="bf16", wdt="bf16")
@@ -184,3 +186,13 @@ def test_layer_llama13b_mlp_int8_full_size(P, layer):
     wl = inputs.WORKLOADS["llama13b_mlp_int8"]
     L = [l for l in wl.layers if l.name == layer][0]
     _masked_full_size(P, wl, L, "mem")
+
+
+def test_layer_bf16_split_tiles_deterministic(P):
+    """Every reduction of the chain (split-K weight gradients, CNP partial sums) adds in a
+    fixed order, so two runs give bit-identical outputs and gradients."""
+    inp = inputs.small_layer_inputs(77, 2048, 1024, 256, 1000, act="bf16", wdt="bf16")
+    a = run_layer(P, inp, 256, "bf16", "bf16", "mem")
+    b = run_layer(P, inp, 256, "bf16", "bf16", "mem")
+    for k in ("y", "dx", "dq_R", "dq_P"):
+        assert np.array_equal(a[k], b[k]), k
