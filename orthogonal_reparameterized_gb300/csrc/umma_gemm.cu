@@ -98,10 +98,12 @@ struct TileCoords {
   int split, blk;
 };
 
-template <int BN, bool B_MN>
-__device__ __forceinline__ TileCoords tile_coords(const UmmaParams& p, int t) {
+// CL = 2 (PLAIN): tile t is a pair of M tiles sharing the B tile; CTA rank r of the cluster
+// takes M tile 2 (t % tiles_m) + r.
+template <int BN, bool B_MN, int CL>
+__device__ __forceinline__ TileCoords tile_coords(const UmmaParams& p, int t, int crank) {
   TileCoords c;
-  const int mt = t % p.tiles_m;
+  const int mt = CL > 1 ? CL * (t % p.tiles_m) + crank : t % p.tiles_m;
   const int rest = t / p.tiles_m;
   const int nt = rest % p.tiles_n;
   const int z = rest / p.tiles_n;
@@ -137,19 +139,19 @@ __device__ __forceinline__ TileCoords tile_coords(const UmmaParams& p, int t) {
 constexpr int kEpiWarps = 8;
 constexpr int kGemmThreads = 64 + 32 * kEpiWarps;
 
-// Bytes of one pipeline stage: A (bf16) and B (bf16; absent when B is resident).  RES > 0:
-// B is a resident panel of RES 64-wide K blocks.
-template <int BN, int RES>
+// Bytes of one pipeline stage: A (bf16) and B (bf16; absent when B is resident; half of it
+// in each CTA of a pair).  RES > 0: B is a resident panel of RES 64-wide K blocks.
+template <int BN, int RES, int CL = 1>
 constexpr int stage_bytes() {
-  return BM * BK * 2 + (RES > 0 ? 0 : BN * BK * 2);
+  return BM * BK * 2 + (RES > 0 ? 0 : BN / CL * BK * 2);
 }
 template <int BN, int RES>
 constexpr int res_bytes() { return RES * BN * BK * 2; }
 
 // Columns the epilogue stages per pass: 64, or 32 when the operand ring leaves no room.
-template <int BN, int STAGES, bool OUT_F32, int RES>
+template <int BN, int STAGES, bool OUT_F32, int RES, int CL = 1>
 constexpr int epi_pass_cols() {
-  constexpr int ring = STAGES * stage_bytes<BN, RES>() + res_bytes<BN, RES>();
+  constexpr int ring = STAGES * stage_bytes<BN, RES, CL>() + res_bytes<BN, RES>();
   constexpr int esz = OUT_F32 ? 4 : 2;
   constexpr int wc = BN / (kEpiWarps / 4);
   constexpr int c = (wc < 64) ? wc : 64;
@@ -173,15 +175,26 @@ __device__ __forceinline__ uint32_t i8x2_to_bf16x2(uint32_t w, int lo) {
 // B panel of the current (block, column tile) resident in shared memory, so that the ring
 // carries only the streamed A tiles; the panel is reloaded when the range crosses into the
 // next block (guarded by its own full / empty barriers).
-template <int BN, int STAGES, bool A_MN, bool B_MN, bool OUT_F32, int RES>
+//
+// CL = 2 (PLAIN only): 2-CTA pairs (cta_group::2).  A cluster of two CTAs computes a
+// 256 x BN tile: each CTA loads its 128 rows of A and its half of the BN rows of B, both
+// signalling the even CTA's "full" barrier, and the even CTA's MMA thread issues M = 256
+// MMAs that read both CTAs' shared memory and write each CTA's 128 accumulator rows into
+// its own TMEM.  Per SM a stage then carries half of B (32 KB instead of 48 KB per K block
+// at BN = 256, so 6 stages fit where 4 did), which is what bounded the single-CTA tiles:
+// shared memory traffic (TMA writes plus MMA reads), not the tensor pipe.  The MMA commits
+// arrive on both CTAs' barriers; both CTAs' epilogue warps release an accumulator on the
+// even CTA's "empty" barrier; neither CTA exits before the other has drained what is aimed
+// at it.
+template <int BN, int STAGES, bool A_MN, bool B_MN, bool OUT_F32, int RES, int CL>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     umma_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmB, const UmmaParams p) {
   constexpr uint32_t A_BYTES = BM * BK * 2;
   constexpr uint32_t B_BYTES = BN * BK * 2;
-  constexpr uint32_t STAGE_BYTES = stage_bytes<BN, RES>();
+  constexpr uint32_t STAGE_BYTES = stage_bytes<BN, RES, CL>();
   constexpr uint32_t TMEM_COLS = 2 * BN;  // two accumulators
-  constexpr uint32_t IDESC = make_idesc(BM, BN, A_MN, B_MN);
+  constexpr uint32_t IDESC = make_idesc(BM * CL, BN, A_MN, B_MN);
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -189,7 +202,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   // per epilogue warp: 32 rows x 64 columns staging buffer (rows padded by 16 bytes), so
   // that the global stores cover whole row segments instead of 16 bytes of 32 rows each
   constexpr uint32_t ESZ = OUT_F32 ? 4 : 2;
-  constexpr int EPC = epi_pass_cols<BN, STAGES, OUT_F32, RES>();  // columns per epilogue pass
+  constexpr int EPC = epi_pass_cols<BN, STAGES, OUT_F32, RES, CL>();  // columns per pass
   constexpr uint32_t STG_PITCH = EPC * ESZ + 16;
   uint8_t* resb = smem + STAGES * STAGE_BYTES;            // resident B panel (RES > 0)
   uint8_t* staging = resb + res_bytes<BN, RES>();         // EPIW buffers
@@ -203,7 +216,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(rempty + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
+  static_assert(CL == 1 || (CL == 2 && RES == 0 && BN % 128 == 0), "pairs: PLAIN tiles only");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int crank = CL > 1 ? (int)cluster_ctarank() : 0;
   if (threadIdx.x == 0) trace_stamp(p.trace, p.trace_cap, 0);  // slot 0: CTA start
   pdl_trigger();
 
@@ -214,7 +229,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], EPIW);
+      mbar_init(&tempty[a], CL * EPIW);  // pairs: both CTAs' epilogue warps
     }
     mbar_init(rfull, 1);
     mbar_init(rempty, 1);
@@ -224,8 +239,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tma_prefetch_desc(&tmB);
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, TMEM_COLS);
-    tmem_relinquish();
+    if (CL > 1) {  // one warp of each CTA of the pair, same columns in both
+      tmem_alloc_pair(tmem_slot, TMEM_COLS);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(tmem_slot, TMEM_COLS);
+      tmem_relinquish();
+    }
   }
   if (warp == 0 && lane == 0 && p.bpre) {
     // this CTA's share of the weight operand into L2 (a prefetch returns no data, so it is
@@ -243,7 +263,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
   }
   tc_fence_before();
-  __syncthreads();
+  if (CL > 1) cluster_sync();  // the peer's barriers exist before anything is aimed at them
+  else __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const uint32_t smem_base = smem_u32(smem);
@@ -251,9 +272,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (threadIdx.x == 0) trace_stamp(p.trace, p.trace_cap, 1);  // slot 1: set-up done
   // tiles of this CTA: strided (t = blockIdx.x, + gridDim.x, ...) or, with a resident B
   // panel, one contiguous range
-  const int t_first = RES > 0 ? (int)((long long)blockIdx.x * p.num_tiles / gridDim.x) : (int)blockIdx.x;
+  const int t_first = RES > 0 ? (int)((long long)blockIdx.x * p.num_tiles / gridDim.x)
+                              : (int)blockIdx.x / CL;
   const int t_end = RES > 0 ? (int)((long long)(blockIdx.x + 1) * p.num_tiles / gridDim.x) : p.num_tiles;
-  const int t_step = RES > 0 ? 1 : (int)gridDim.x;
+  const int t_step = RES > 0 ? 1 : (int)gridDim.x / CL;
   auto panel_key = [](const TileCoords& c) -> long long {
     return ((long long)c.b_c0 << 32) | (unsigned)c.b_c1;
   };
@@ -265,7 +287,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     long long cur_key = -1;
     int npanels = 0;
     for (int t = t_first; t < t_end && ok; t += t_step) {
-      const TileCoords c = tile_coords<BN, B_MN>(p, t);
+      const TileCoords c = tile_coords<BN, B_MN, CL>(p, t, crank);
       if (RES > 0 && panel_key(c) != cur_key) {
         // the previous panel must be free (all MMAs that read it completed) before reloading
         if (npanels > 0 &&
@@ -296,11 +318,26 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           ok = false;
           break;
         }
-        mbar_arrive_expect_tx(&full[s], RES > 0 ? A_BYTES : STAGE_BYTES);
         if (g == 0) trace_stamp(p.trace, p.trace_cap, 2);  // slot 2: first TMA issued
         uint8_t* sa = smem + s * STAGE_BYTES;
         uint8_t* sb = sa + A_BYTES;
         const int k = kb * BK;
+        if (CL > 1) {
+          // this CTA's A rows and half of B, completing on the even CTA's barrier
+          if (crank == 0) mbar_arrive_expect_tx(&full[s], CL * STAGE_BYTES);
+          const uint32_t fb = mapa_shared(&full[s], 0);
+          tma_load_2d_pair(sa, &tmA, fb, c.a_c0 + k, c.a_c1);
+          if (!B_MN) {
+            tma_load_2d_pair(sb, &tmB, fb, c.b_c0 + k, c.b_c1 + crank * (BN / 2));
+          } else {
+#pragma unroll
+            for (int j = 0; j < BN / 128; ++j)
+              tma_load_2d_pair(sb + j * 8192, &tmB, fb, c.b_c0 + 64 * (crank * (BN / 128) + j),
+                               c.b_c1 + k);
+          }
+          continue;
+        }
+        mbar_arrive_expect_tx(&full[s], RES > 0 ? A_BYTES : STAGE_BYTES);
         if (!A_MN) {
           tma_load_2d(sa, &tmA, &full[s], c.a_c0 + k, c.a_c1);
         } else {
@@ -324,9 +361,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (RES > 0 && npanels > 0) mbar_wait_bounded(rfull, (npanels - 1) & 1, p.err, p.limit_ns);
     // Drain: wait for the last load issued into every stage (already complete in the normal
     // path), so that no copy is in flight when the CTA exits.
+    // (Pairs: the loads complete on the even CTA's barriers, so wait instead until the MMAs
+    // have released the last stages, which they do only after reading them.)
     for (long long j = g - 1; j >= 0 && j >= g - STAGES; --j)
-      mbar_wait_bounded(&full[j % STAGES], (uint32_t)((j / STAGES) & 1), p.err, p.limit_ns);
-  } else if (warp == 1 && lane == 0) {
+      mbar_wait_bounded(CL > 1 ? &empty[j % STAGES] : &full[j % STAGES],
+                        (uint32_t)((j / STAGES) & 1), p.err, p.limit_ns);
+  } else if (warp == 1 && lane == 0 && crank == 0) {
     // ------------------------------------------------------------ MMA issuer
     long long g = 0;
     int it = 0;
@@ -334,7 +374,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     long long cur_key = -1;
     int npanels = 0;
     for (int t = t_first; t < t_end && ok; t += t_step, ++it) {
-      const TileCoords c = tile_coords<BN, B_MN>(p, t);
+      const TileCoords c = tile_coords<BN, B_MN, CL>(p, t, crank);
       const int a = it & 1;
       if (*abort_flag || !mbar_wait_bounded(&tempty[a], ((it >> 1) & 1) ^ 1, p.err, p.limit_ns)) {
         *abort_flag = 1;
@@ -365,11 +405,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const uint32_t b_base = RES > 0 ? smem_u32(resb) + kb * B_BYTES : a_base + A_BYTES;
 #pragma unroll
         for (int k = 0; k < BK / 16; ++k)
-          umma_bf16(d, tile_desc<A_MN>(a_base, k), tile_desc<B_MN>(b_base, k), IDESC,
-                    (kb | k) != 0);
-        umma_commit(&empty[s]);
+          if (CL > 1)
+            umma_bf16_pair(d, tile_desc<A_MN>(a_base, k), tile_desc<B_MN>(b_base, k), IDESC,
+                           (kb | k) != 0);
+          else
+            umma_bf16(d, tile_desc<A_MN>(a_base, k), tile_desc<B_MN>(b_base, k), IDESC,
+                      (kb | k) != 0);
+        if (CL > 1) umma_commit_pair(&empty[s]);
+        else umma_commit(&empty[s]);
       }
-      umma_commit(&tfull[a]);  // also when the tile had no K block (empty token split)
+      // also when the tile had no K block (empty token split)
+      if (CL > 1) umma_commit_pair(&tfull[a]);
+      else umma_commit(&tfull[a]);
     }
     // TMEM is freed after the final barrier: wait until the last MMAs have completed.
     if (it > 0) {
@@ -384,7 +431,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int row = q * 32 + lane;
     int it = 0;
     for (int t = t_first; t < t_end; t += t_step, ++it) {
-      const TileCoords c = tile_coords<BN, B_MN>(p, t);
+      const TileCoords c = tile_coords<BN, B_MN, CL>(p, t, crank);
       const int a = it & 1;
       const bool ok = !*abort_flag && mbar_wait_bounded(&tfull[a], (it >> 1) & 1, p.err, p.limit_ns);
       if (!__all_sync(0xffffffffu, ok)) {
@@ -465,18 +512,23 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty[a]);
+      if (lane == 0) {
+        if (CL > 1) mbar_arrive_cluster(mapa_shared(&tempty[a], 0));
+        else mbar_arrive(&tempty[a]);
+      }
       if (warp == 2 && lane == 0 && it < 12) trace_stamp(p.trace, p.trace_cap, 4 + 2 * it);  // tile stored
     }
   }
   if (warp == 2 && lane == 0) trace_stamp(p.trace, p.trace_cap, 30);  // epilogue loop done
   tc_fence_before();
-  __syncthreads();
+  if (CL > 1) cluster_sync();
+  else __syncthreads();
   if (threadIdx.x == 0) trace_stamp(p.trace, p.trace_cap, 31);  // slot 31: exit
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem_base, TMEM_COLS);
+    if (CL > 1) tmem_dealloc_pair(tmem_base, TMEM_COLS);
+    else tmem_dealloc(tmem_base, TMEM_COLS);
   }
 }
 
@@ -838,14 +890,15 @@ bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, u
   return make_map_t(m, ptr, inner, outer, pitch_elems, box_inner, box_outer, false);
 }
 
-template <int BN, int STAGES, bool A_MN, bool B_MN, bool OUT_F32, int RES = 0>
+// CL = 2: tiles_m counts pairs of M tiles (see tile_coords).
+template <int BN, int STAGES, bool A_MN, bool B_MN, bool OUT_F32, int RES = 0, int CL = 1>
 poetx_status launch(const CUtensorMap& ta, const CUtensorMap& tb, UmmaParams p, int tiles_m,
                     int tiles_n, int tiles_z, cudaStream_t s) {
   const int stage = p.mode == MODE_PLAIN ? ST_WPRIME : (p.mode == MODE_BLOCKDIAG ? ST_BLOCKDIAG : ST_WGRAD);
-  auto k = umma_gemm_kernel<BN, STAGES, A_MN, B_MN, OUT_F32, RES>;
-  constexpr int smem = STAGES * stage_bytes<BN, RES>() + res_bytes<BN, RES>() +
+  auto k = umma_gemm_kernel<BN, STAGES, A_MN, B_MN, OUT_F32, RES, CL>;
+  constexpr int smem = STAGES * stage_bytes<BN, RES, CL>() + res_bytes<BN, RES>() +
                        kEpiWarps * 32 *
-                           (epi_pass_cols<BN, STAGES, OUT_F32, RES>() * (OUT_F32 ? 4 : 2) + 16) +
+                           (epi_pass_cols<BN, STAGES, OUT_F32, RES, CL>() * (OUT_F32 ? 4 : 2) + 16) +
                        1024 + 512;
   // CTAs per SM: bounded by TMEM (2 x BN columns each, 512 per SM) and shared memory.
   constexpr int by_tmem = 512 / (2 * BN);
@@ -855,8 +908,24 @@ poetx_status launch(const CUtensorMap& ta, const CUtensorMap& tb, UmmaParams p, 
   static_assert(per_sm >= 1, "configuration exceeds TMEM or shared memory");
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
+  static int max_clusters = 0;  // CL > 1: co-resident clusters of this configuration
   std::call_once(once, [&] {
     attr_err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (attr_err == cudaSuccess && CL > 1) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(CL * sm_count());
+      cfg.blockDim = dim3(kGemmThreads);
+      cfg.dynamicSmemBytes = smem;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = CL;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      attr_err = cudaOccupancyMaxActiveClusters(&max_clusters, k, &cfg);
+      if (attr_err == cudaSuccess && max_clusters < 1) attr_err = cudaErrorInvalidConfiguration;
+    }
   });
   POETX_CUDA_TRY(attr_err);
   const long long tiles = (long long)tiles_m * tiles_n * tiles_z;
@@ -865,9 +934,12 @@ poetx_status launch(const CUtensorMap& ta, const CUtensorMap& tb, UmmaParams p, 
   p.tiles_m = tiles_m;
   p.tiles_n = tiles_n;
   p.num_tiles = (int)tiles;
-  const long long want = (long long)sm_count() * per_sm;
-  const int grid = (int)(tiles < want ? tiles : want);
-  POETX_CUDA_TRY(launch_pdl(k, dim3(grid), dim3(kGemmThreads), smem, s, ta, tb, p));
+  const long long want = CL > 1 ? max_clusters : (long long)sm_count() * per_sm;
+  const int grid = CL * (int)(tiles < want ? tiles : want);
+  if (CL > 1)
+    POETX_CUDA_TRY(launch_pdl_cluster(k, dim3(grid), dim3(kGemmThreads), smem, s, CL, ta, tb, p));
+  else
+    POETX_CUDA_TRY(launch_pdl(k, dim3(grid), dim3(kGemmThreads), smem, s, ta, tb, p));
   POETX_CUDA_TRY(cudaGetLastError());
   after_launch(s, stage);
   return POETX_OK;
@@ -952,19 +1024,21 @@ poetx_status umma_wprime(const void* A, long long N, int m, int n, const void* W
   p.bpre = static_cast<const uint8_t*>(W);
   p.bpre_bytes = (unsigned long long)m * n * 2;
   const int tm = (int)((N + BM - 1) / BM);
+  // 256 x 256 tiles computed by 2-CTA pairs (each CTA: 128 rows of A, 128 rows of W')
+  const int tm2 = (tm + 1) / 2;
   if (!trans) {  // C[N,n] = A[N,m] W^T
     if (!make_map(&ta, A, m, N, m, 64, 128)) return POETX_ERR_CUDA;
-    if (!make_map(&tb, W, m, n, m, 64, 256)) return POETX_ERR_CUDA;
+    if (!make_map(&tb, W, m, n, m, 64, 128)) return POETX_ERR_CUDA;  // half of a 256-row tile
     p.num_kb = m / 64;
     p.ldc = n;
-    return launch<256, 4, false, false, false>(ta, tb, p, tm, n / 256, 1, s);
+    return launch<256, 6, false, false, false, 0, 2>(ta, tb, p, tm2, n / 256, 1, s);
   }
   // C[N,m] = A[N,n] W: B operand (output col c, K index r) = W[r][c], MN-major
   if (!make_map(&ta, A, n, N, n, 64, 128)) return POETX_ERR_CUDA;
   if (!make_map(&tb, W, m, n, m, 64, 64)) return POETX_ERR_CUDA;
   p.num_kb = n / 64;
   p.ldc = m;
-  return launch<256, 4, false, true, false>(ta, tb, p, tm, m / 256, 1, s);
+  return launch<256, 6, false, true, false, 0, 2>(ta, tb, p, tm2, m / 256, 1, s);
 }
 
 // int8 W' contraction (the transposed kernel above).  Forward (trans = 0): C[N, n] =
