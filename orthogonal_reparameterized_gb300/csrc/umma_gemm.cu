@@ -1024,21 +1024,28 @@ poetx_status umma_wprime(const void* A, long long N, int m, int n, const void* W
   p.bpre = static_cast<const uint8_t*>(W);
   p.bpre_bytes = (unsigned long long)m * n * 2;
   const int tm = (int)((N + BM - 1) / BM);
-  // 256 x 256 tiles computed by 2-CTA pairs (each CTA: 128 rows of A, 128 rows of W')
+  // 256 x 256 tiles computed by 2-CTA pairs (each CTA: 128 rows of A, 128 rows of W') when
+  // there are at least two of them per pair of SMs; with fewer, both forms take the same
+  // number of tile rounds and the single-CTA 128 x 256 tiles start faster.
   const int tm2 = (tm + 1) / 2;
+  const long long pair_tiles = (long long)tm2 * ((trans ? m : n) / 256);
+  const bool pairs = pair_tiles >= sm_count();
   if (!trans) {  // C[N,n] = A[N,m] W^T
     if (!make_map(&ta, A, m, N, m, 64, 128)) return POETX_ERR_CUDA;
-    if (!make_map(&tb, W, m, n, m, 64, 128)) return POETX_ERR_CUDA;  // half of a 256-row tile
+    // (pairs: each CTA loads half of a 256-row W' tile)
+    if (!make_map(&tb, W, m, n, m, 64, pairs ? 128 : 256)) return POETX_ERR_CUDA;
     p.num_kb = m / 64;
     p.ldc = n;
-    return launch<256, 6, false, false, false, 0, 2>(ta, tb, p, tm2, n / 256, 1, s);
+    if (pairs) return launch<256, 6, false, false, false, 0, 2>(ta, tb, p, tm2, n / 256, 1, s);
+    return launch<256, 4, false, false, false>(ta, tb, p, tm, n / 256, 1, s);
   }
   // C[N,m] = A[N,n] W: B operand (output col c, K index r) = W[r][c], MN-major
   if (!make_map(&ta, A, n, N, n, 64, 128)) return POETX_ERR_CUDA;
   if (!make_map(&tb, W, m, n, m, 64, 64)) return POETX_ERR_CUDA;
   p.num_kb = n / 64;
   p.ldc = m;
-  return launch<256, 6, false, true, false, 0, 2>(ta, tb, p, tm2, m / 256, 1, s);
+  if (pairs) return launch<256, 6, false, true, false, 0, 2>(ta, tb, p, tm2, m / 256, 1, s);
+  return launch<256, 4, false, true, false>(ta, tb, p, tm, m / 256, 1, s);
 }
 
 // int8 W' contraction (the transposed kernel above).  Forward (trans = 0): C[N, n] =

@@ -84,7 +84,10 @@ def test_wgrad_bf16(P, engine, N, nblk, b, splits):
 
 
 @pytest.mark.parametrize("N,m,n", [(300, 512, 768), (129, 256, 256), (1, 512, 256),
-                                   (640, 1024, 512), (4100, 2048, 1024)])
+                                   (640, 1024, 512), (4100, 2048, 1024),
+                                   # enough 256 x 256 tiles for the 2-CTA pair kernel, in
+                                   # one direction each, odd count of 128-row tiles
+                                   (2600, 1024, 8192), (2600, 8192, 1024)])
 @pytest.mark.parametrize("trans", [False, True])
 def test_wprime_bf16(P, engine, N, m, n, trans):
     W = _rand_bf16((n, m), 1 / np.sqrt(m)).to(DEV)
