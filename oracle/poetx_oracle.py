@@ -15,7 +15,7 @@ section:
   block-diagonal multiply; §4 Cayley-Neumann parameterization, eq. 9/10; §5 fast/mem
   checkpointing; §6 POET-XQ).
 * "POET skill page" -- *Poet Orthogonal LLM Training*, Step 1 (W = R W0 P) and Step 4
-  (merge-then-reinitialize).
+  (merge-then-reinitialize, ``merge_reinit``).
 
 Conventions (readings of the pages, each also listed in the design notes):
 
@@ -260,6 +260,23 @@ def dx_rows(dy_rows, Wp, perm_m, perm_n, G_R, G_P) -> np.ndarray:
     dB = blockdiag_mm(dzt, G_P, transpose=True)
     dA = dB @ np.asarray(Wp, dtype=F64)
     return perm_scatter(blockdiag_mm(dA, G_R, transpose=True), perm_m)
+
+
+# ----------------------------------------------------------------------------------------
+# Merge-then-reinitialize (POET skill page, Step 4: the current R W0 P is written back into
+# W0 and the factors are reset to the identity; the POET-X summary's "inner optimization"
+# loop between merges).  In this library's form the factors are q = 0 after the reset and
+# the permutations are drawn anew and merged again (merge_perm).
+# ----------------------------------------------------------------------------------------
+def merge_reinit(Wp, perm_m, perm_n, q_R, q_P, b: int, order: int = 3) -> np.ndarray:
+    """W0_new [n, m]: the weight with which the layer at q = 0 computes the same linear map
+    as the layer with the merged weight Wp, the permutations and q_R, q_P.  It is that map's
+    matrix, read off as the layer's response to the identity batch (row i of the response
+    is the image of the i-th unit input)."""
+    G_R = cnp_forward(q_R, b, order)
+    G_P = cnp_forward(q_P, b, order)
+    m = np.asarray(Wp).shape[1]
+    return layer_forward(np.eye(m, dtype=F64), Wp, perm_m, perm_n, G_R, G_P)["y"].T
 
 
 # ----------------------------------------------------------------------------------------

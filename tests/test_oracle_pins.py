@@ -327,6 +327,75 @@ def test_spectrum_preserved_with_orthogonal_blocks():
     np.testing.assert_allclose(s1, s0, rtol=0, atol=1e-13)
 
 
+# ------------------------------------------------------------------ merge-then-reinitialize
+def test_merge_reinit_zero_q_returns_w0():
+    """With the factors at the identity the merge writes back exactly the frozen weight."""
+    m, n, b = 12, 8, 4
+    L = _layer(m, n, b, 1)
+    Wp = O.merge_perm(L["W0"], L["perm_n"], L["perm_m"])
+    W0n = O.merge_reinit(Wp, L["perm_m"], L["perm_n"], 0 * L["q_R"], 0 * L["q_P"], b)
+    np.testing.assert_allclose(W0n, L["W0"], rtol=0, atol=1e-15)
+
+
+def test_merge_reinit_closed_form_b2():
+    """b = 2, identity permutations: Q = [[0, t], [-t, 0]] gives Q^2 = -t^2 I, so
+    G = (I + Q)(I + Q + Q^2 + Q^3) = (1 - t^2) [[1 - t^2, 2t], [-2t, 1 - t^2]] (by hand), and
+    the merged weight is G_P^T W0 G_R^T (POET skill page, Step 1 and Step 4)."""
+    def G2(t):
+        return (1 - t * t) * np.array([[1 - t * t, 2 * t], [-2 * t, 1 - t * t]])
+    W0 = np.array([[0.5, -1.25], [2.0, 0.75]])
+    tR, tP = 0.3, -0.2
+    W0n = O.merge_reinit(W0, np.array([0, 1]), np.array([0, 1]), np.array([[tR]]),
+                         np.array([[tP]]), 2)
+    np.testing.assert_allclose(W0n, G2(tP).T @ W0 @ G2(tR).T, rtol=0, atol=1e-15)
+
+
+@pytest.mark.parametrize("m,n,b", [(8, 8, 4), (12, 8, 4), (16, 32, 8)])
+def test_merge_reinit_equals_dense_R_W0_P(m, n, b):
+    """W0_new = R W0 P with R = Psi_n^T D_P^T Psi_n and P = Psi_m^T D_R^T Psi_m built as dense
+    matrices (POET skill page, Step 1: W = R W0 P; Step 4 writes it back into W0)."""
+    L = _layer(m, n, b, 1)
+    Wp = O.merge_perm(L["W0"], L["perm_n"], L["perm_m"])
+    W0n = O.merge_reinit(Wp, L["perm_m"], L["perm_n"], L["q_R"], L["q_P"], b)
+    Psi_m = np.eye(m)[L["perm_m"]]
+    Psi_n = np.eye(n)[L["perm_n"]]
+    R = Psi_n.T @ _blkdiag(O.cnp_forward(L["q_P"], b)).T @ Psi_n
+    P = Psi_m.T @ _blkdiag(O.cnp_forward(L["q_R"], b)).T @ Psi_m
+    np.testing.assert_allclose(W0n, R @ L["W0"] @ P, rtol=0, atol=1e-13)
+
+
+def test_merge_reinit_preserves_the_layer_with_new_permutations():
+    """After the merge, q = 0 and freshly drawn permutations, the layer computes the same
+    outputs and input gradients as before (the purpose of the step)."""
+    m, n, b, N = 16, 24, 4, 7
+    L = _layer(m, n, b, N, seed=3)
+    Wp = O.merge_perm(L["W0"], L["perm_n"], L["perm_m"])
+    before = O.poetx_layer(L["x"], L["dy"], L["W0"], L["perm_m"], L["perm_n"], L["q_R"],
+                           L["q_P"], b)
+    W0n = O.merge_reinit(Wp, L["perm_m"], L["perm_n"], L["q_R"], L["q_P"], b)
+    r = np.random.default_rng(9)
+    pm2, pn2 = r.permutation(m), r.permutation(n)
+    after = O.poetx_layer(L["x"], L["dy"], W0n, pm2, pn2, 0 * L["q_R"], 0 * L["q_P"], b)
+    np.testing.assert_allclose(after["y"], before["y"], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(after["dx"], before["dx"], rtol=0, atol=1e-12)
+
+
+def test_merge_reinit_singular_values_within_cnp_bound():
+    """G is a polynomial in the skew Q, so it is normal with singular values 1 - lambda^4
+    for the eigenvalues +-i lambda of Q (|1 + i l| |1 + i l - l^2 - i l^3| = (1 + l^2)
+    (1 - l^2)).  Hence sigma_k(W0_new) / sigma_k(W0) lies in [(1 - lR^4)(1 - lP^4), 1]
+    with lR, lP the largest |eigenvalue| over the blocks of each side."""
+    m, n, b = 16, 12, 4
+    L = _layer(m, n, b, 1, seed=5, qstd=0.15)
+    Wp = O.merge_perm(L["W0"], L["perm_n"], L["perm_m"])
+    W0n = O.merge_reinit(Wp, L["perm_m"], L["perm_n"], L["q_R"], L["q_P"], b)
+    lam = lambda q: max(np.abs(np.linalg.eigvals(Qj)).max() for Qj in O.triu_unpack(q, b))
+    lo = (1 - lam(L["q_R"]) ** 4) * (1 - lam(L["q_P"]) ** 4)
+    assert lo < 1 - 1e-6  # the bound is not trivial here
+    ratio = np.linalg.svd(W0n, compute_uv=False) / np.linalg.svd(L["W0"], compute_uv=False)
+    assert np.all(ratio <= 1 + 1e-12) and np.all(ratio >= lo - 1e-12), (ratio, lo)
+
+
 @pytest.mark.parametrize("m,n,b,N", [(8, 8, 4, 3), (12, 8, 4, 2)])
 def test_layer_backward_finite_differences(m, n, b, N):
     L = _layer(m, n, b, N, seed=3, qstd=0.3)
