@@ -451,6 +451,16 @@ def main():
     setup["quantize_rows_int8"] = {"us": us, "bytes": by, "gbs": by / (us * 1e-6) / 1e9,
                                    "frac_of_hbm": by / (us * 1e-6) / 1e9 / pk["hbm_gbs"]}
     del W0s, Wps, W32s, Wqs, ss
+    # merge-then-reinitialize of the benchmarked layer: W0_new = R W0 P in fp32 (two batched
+    # block products of 2 n m b flops each on the CUDA cores, the CNP and two index passes)
+    W0n = torch.empty(n, m, device=dev)
+    mws = P.workspace(P.poetx_merge_reinit_workspace_bytes(main_b["L"]), dev)
+    us = median_us(lambda: P.poetx_merge_reinit(main_b["L"], W0n, mws))
+    fl = 4.0 * n * m * b
+    setup["merge_reinit"] = {"us": us, "flops": fl, "tflops_fp32": fl / (us * 1e-6) / 1e12,
+                             "note": "fp32 FFMA products (CUDA cores) + CNP + permutation "
+                                     "inverse and gather; runs once per many steps"}
+    del W0n, mws
 
     # every layer of a multi-layer workload (on request): the metric of such a workload is
     # N / (sum of the layers' step times)

@@ -261,6 +261,24 @@ poetx_status poetx_layer_bwd(const poetx_layer* L, const void* x, const void* dy
                              const void* saved, void* dx, float* dq_R, float* dq_P,
                              int accumulate, void* ws, size_t ws_bytes, cudaStream_t stream);
 
+/* Merge-then-reinitialize (POET skill page, Step 4 "Merge-Then-Reinitialize Optimization":
+ * the current R W0 P is written back into W0 and the factors are reset to the identity).
+ * Writes the weight that, with q_R = q_P = 0, makes the layer compute the map it computes
+ * now:
+ *   W0_new = Pi_n blkdiag(G_P)^T W' blkdiag(G_R)^T Pi_m^T,
+ *   i.e.  W0_new[perm_n[r], perm_m[c]] = (blkdiag(G_P)^T W' blkdiag(G_R)^T)[r, c],
+ * with G_R, G_P the CNP (order L->order) of the layer's current q_R, q_P and W' = L->Wp
+ * (times L->w_scale per row for an int8 layer).  W0_new: [n, m] fp32, device, 16-byte
+ * aligned, in the original (unpermuted) coordinates of W0.  fp32 arithmetic throughout.
+ * The reinitialisation is then the caller's: set q_R and q_P to zero, draw new
+ * permutations, and merge them into W0_new with poetx_merge_perm (an int8 layer first
+ * re-quantises W0_new with poetx_quantize_rows_int8).  ws: at least
+ * poetx_merge_reinit_workspace_bytes(L) bytes (0 for an invalid descriptor).  Errors as for
+ * poetx_layer_fwd. */
+size_t poetx_merge_reinit_workspace_bytes(const poetx_layer* L);
+poetx_status poetx_merge_reinit(const poetx_layer* L, float* W0_new, void* ws, size_t ws_bytes,
+                                cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

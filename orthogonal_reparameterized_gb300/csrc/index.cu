@@ -472,6 +472,67 @@ poetx_status launch_quantize(const float* W, int n, int m, int8_t* Wq, float* sc
   return POETX_OK;
 }
 
+// ---------------------------------------------------------------- merge helpers
+// inv[perm[i]] = i, for the two permutations of a layer at once (perm_a of length na, then
+// perm_b of length nb, into inv_a / inv_b).
+__global__ void __launch_bounds__(256) invert_perm_kernel(const int32_t* __restrict__ perm_a,
+                                                          int na, int32_t* __restrict__ inv_a,
+                                                          const int32_t* __restrict__ perm_b,
+                                                          int nb, int32_t* __restrict__ inv_b) {
+  pdl_trigger();
+  pdl_wait();
+  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < na) {
+    inv_a[perm_a[i]] = (int32_t)i;
+  } else if (i < (long long)na + nb) {
+    const int k = (int)(i - na);
+    inv_b[perm_b[k]] = k;
+  }
+}
+
+poetx_status launch_invert_perms(const int32_t* perm_a, int na, int32_t* inv_a,
+                                 const int32_t* perm_b, int nb, int32_t* inv_b, cudaStream_t s) {
+  const long long n = (long long)na + nb;
+  if (n == 0) return POETX_OK;
+  POETX_CUDA_TRY(launch_pdl(invert_perm_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0,
+                            s, perm_a, na, inv_a, perm_b, nb, inv_b));
+  POETX_CUDA_TRY(cudaGetLastError());
+  after_launch(s, ST_MERGE_REINIT);
+  return POETX_OK;
+}
+
+// W[r][c] = scale[r] * Wq[r][c] in fp32 (m a multiple of 4: four codes per thread).
+__global__ void __launch_bounds__(256) dequant_rows_kernel(const int8_t* __restrict__ Wq,
+                                                           const float* __restrict__ scale,
+                                                           int n, int m, float* __restrict__ W) {
+  pdl_trigger();
+  pdl_wait();
+  const long long quads = (long long)n * (m / 4);
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < quads;
+       i += (long long)gridDim.x * blockDim.x) {
+    const long long r = i / (m / 4);
+    const char4 q = reinterpret_cast<const char4*>(Wq)[i];
+    const float sr = scale[r];
+    reinterpret_cast<float4*>(W)[i] =
+        make_float4(sr * (float)q.x, sr * (float)q.y, sr * (float)q.z, sr * (float)q.w);
+  }
+}
+
+poetx_status launch_dequant_rows(const int8_t* Wq, const float* scale, int n, int m, float* W,
+                                 cudaStream_t s) {
+  if (n == 0 || m == 0) return POETX_OK;
+  if (m % 4) return POETX_ERR_SHAPE;
+  const long long quads = (long long)n * (m / 4);
+  long long blocks = (quads + 255) / 256;
+  const long long cap = (long long)sm_count() * 8;
+  if (blocks > cap) blocks = cap;
+  POETX_CUDA_TRY(launch_pdl(dequant_rows_kernel, dim3((unsigned)blocks), dim3(256), 0, s, Wq,
+                            scale, n, m, W));
+  POETX_CUDA_TRY(cudaGetLastError());
+  after_launch(s, ST_MERGE_REINIT);
+  return POETX_OK;
+}
+
 }  // namespace poetx
 
 using namespace poetx;

@@ -23,6 +23,12 @@ poetx_status launch_perm_rows(size_t esize, bool scatter, const void* X, long lo
                               const float* scale, float* scale_out, cudaStream_t s);
 poetx_status launch_quantize(const float* W, int n, int m, int8_t* Wq, float* scale,
                              cudaStream_t s);
+// inv_a[perm_a[i]] = i (i < na) and inv_b[perm_b[k]] = k (k < nb), one launch.
+poetx_status launch_invert_perms(const int32_t* perm_a, int na, int32_t* inv_a,
+                                 const int32_t* perm_b, int nb, int32_t* inv_b, cudaStream_t s);
+// W[r][c] = scale[r] * Wq[r][c] (fp32 out, m % 4 == 0).
+poetx_status launch_dequant_rows(const int8_t* Wq, const float* scale, int n, int m, float* W,
+                                 cudaStream_t s);
 
 // ---- simt_gemm.cu: generic strided batched GEMM on the CUDA cores (fp32 accumulation).
 // C[z][i][j] = colscale[j] * sum_k A(z,i,k) B(z,k,j), element (i,k) of batch z of A at

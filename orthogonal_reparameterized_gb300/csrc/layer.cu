@@ -188,6 +188,32 @@ static Plan make_plan(const poetx_layer* L, long long N) {
   return p;
 }
 
+// ---------------------------------------------------------------- merge-then-reinitialize
+// W0_new = Pi_n blkdiag(G_P)^T W' blkdiag(G_R)^T Pi_m^T: T = W' blkdiag(G_R)^T (the blocks of
+// the columns), M = blkdiag(G_P)^T T (the blocks of the rows), then both permutations undone
+// by one gather, W0_new[k, l] = M[inv_n[k], inv_m[l]].  fp32 throughout (CUDA cores): the
+// merge runs once per many steps and its error would stay in W0.
+struct MergePlan {
+  size_t Qs, Q2, G, Wf, T, M, inv_m, inv_n, total;
+};
+
+static MergePlan merge_plan(const poetx_layer* L) {
+  MergePlan p{};
+  const size_t m = L->m, n = L->n, b = L->b;
+  size_t o = 0;
+  auto take = [&](size_t bytes) { size_t r = o; o += align_up(bytes, 256); return r; };
+  p.Qs = take((m + n) * b * 4);
+  p.Q2 = take((m + n) * b * 4);
+  p.G = take((m + n) * b * 4);
+  p.Wf = L->wdt == POETX_I8 ? take(n * m * 4) : 0;
+  p.T = take(n * m * 4);
+  p.M = take(n * m * 4);
+  p.inv_m = take(m * 4);
+  p.inv_n = take(n * 4);
+  p.total = o;
+  return p;
+}
+
 template <typename T = void>
 static T* at(void* base, size_t off) {
   return reinterpret_cast<T*>(static_cast<char*>(base) + off);
@@ -211,6 +237,60 @@ extern "C" size_t poetx_layer_workspace_bytes(const poetx_layer* L, int N, int p
   if (validate(L) != POETX_OK || N < 0) return 0;
   const Plan p = make_plan(L, N);
   return phase == 0 ? p.fwd_total : p.bwd_total;
+}
+
+extern "C" size_t poetx_merge_reinit_workspace_bytes(const poetx_layer* L) {
+  if (validate(L) != POETX_OK) return 0;
+  return merge_plan(L).total;
+}
+
+extern "C" poetx_status poetx_merge_reinit(const poetx_layer* L, float* W0_new, void* ws,
+                                           size_t ws_bytes, cudaStream_t stream) {
+  POETX_TRY(validate(L));
+  if (!W0_new || !ws) return POETX_ERR_ARG;
+  if (!aligned16(W0_new) || !aligned16(ws)) return POETX_ERR_ALIGN;
+  const MergePlan p = merge_plan(L);
+  if (ws_bytes < p.total) return POETX_ERR_WORKSPACE;
+  const int b = L->b, m = L->m, n = L->n;
+  // G_R (blocks [0, m/b)) and G_P (blocks [m/b, (m+n)/b)) in fp32
+  const CnpSides sides{{L->q_R, L->q_P}, {m / b, n / b}};
+  float* G = at<float>(ws, p.G);
+  POETX_TRY(cnp_forward_sides(sides, b, at<float>(ws, p.Qs), at<float>(ws, p.Q2), G, nullptr,
+                              nullptr, stream));
+  const float* GR = G;
+  const float* GP = G + (size_t)m * b;
+  const void* Wsrc = L->Wp;
+  poetx_dtype wt = L->wdt;
+  if (L->wdt == POETX_I8) {
+    POETX_TRY(launch_dequant_rows(static_cast<const int8_t*>(L->Wp), L->w_scale, n, m,
+                                  at<float>(ws, p.Wf), stream));
+    Wsrc = at<float>(ws, p.Wf);
+    wt = POETX_F32;
+  }
+  float* T = at<float>(ws, p.T);
+  float* M = at<float>(ws, p.M);
+  SimtGemm g{};
+  // T[:, jb:(j+1)b] = W'[:, jb:(j+1)b] G_R,j^T
+  g.M = n; g.N = b; g.K = b; g.batch = m / b;
+  g.A = Wsrc; g.sam = m; g.sak = 1; g.sab = b;
+  g.B = GR; g.sbk = 1; g.sbn = b; g.sbb = (long long)b * b;
+  g.C = T; g.scm = m; g.scn = 1; g.scb = b;
+  g.ksplit = 1; g.kchunk = b;
+  g.stage = ST_MERGE_REINIT;
+  POETX_TRY(launch_simt_gemm(wt, POETX_F32, POETX_F32, g, stream));
+  // M[jb:(j+1)b, :] = G_P,j^T T[jb:(j+1)b, :]
+  g = SimtGemm{};
+  g.M = b; g.N = m; g.K = b; g.batch = n / b;
+  g.A = GP; g.sam = 1; g.sak = b; g.sab = (long long)b * b;
+  g.B = T; g.sbk = m; g.sbn = 1; g.sbb = (long long)b * m;
+  g.C = M; g.scm = m; g.scn = 1; g.scb = (long long)b * m;
+  g.ksplit = 1; g.kchunk = b;
+  g.stage = ST_MERGE_REINIT;
+  POETX_TRY(launch_simt_gemm(POETX_F32, POETX_F32, POETX_F32, g, stream));
+  int32_t* inv_m = at<int32_t>(ws, p.inv_m);
+  int32_t* inv_n = at<int32_t>(ws, p.inv_n);
+  POETX_TRY(launch_invert_perms(L->perm_m, m, inv_m, L->perm_n, n, inv_n, stream));
+  return launch_perm_rows(4, false, M, n, m, inv_m, W0_new, inv_n, nullptr, nullptr, stream);
 }
 
 extern "C" size_t poetx_layer_saved_bytes(const poetx_layer* L, int N) {

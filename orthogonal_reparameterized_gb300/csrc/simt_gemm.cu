@@ -109,6 +109,7 @@ poetx_status launch_simt_gemm(poetx_dtype ta, poetx_dtype tb, poetx_dtype tc, co
   if (ta == POETX_F32 && tb == POETX_F32 && tc == POETX_F32) return launch_t<float, float, float>(g, s);
   if (ta == POETX_BF16 && tb == POETX_BF16 && tc == POETX_BF16) return launch_t<bf, bf, bf>(g, s);
   if (ta == POETX_BF16 && tb == POETX_BF16 && tc == POETX_F32) return launch_t<bf, bf, float>(g, s);
+  if (ta == POETX_BF16 && tb == POETX_F32 && tc == POETX_F32) return launch_t<bf, float, float>(g, s);
   if (ta == POETX_BF16 && tb == POETX_I8 && tc == POETX_BF16) return launch_t<bf, int8_t, bf>(g, s);
   return POETX_ERR_DTYPE;
 }

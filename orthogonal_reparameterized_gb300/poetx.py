@@ -65,6 +65,8 @@ _SIGS = {
     "poetx_layer_fwd": (_i, [ctypes.POINTER(LayerDesc), _vp, _i, _vp, _vp, _vp, _sz, _vp]),
     "poetx_layer_bwd": (_i, [ctypes.POINTER(LayerDesc), _vp, _vp, _i, _vp, _vp, _vp, _vp, _i,
                              _vp, _sz, _vp]),
+    "poetx_merge_reinit_workspace_bytes": (_sz, [ctypes.POINTER(LayerDesc)]),
+    "poetx_merge_reinit": (_i, [ctypes.POINTER(LayerDesc), _vp, _vp, _sz, _vp]),
 }
 
 _lib: Optional[ctypes.CDLL] = None
@@ -277,3 +279,14 @@ def poetx_layer_bwd(L: LayerDesc, x, dy, saved, dx, dq_R, dq_P, ws, accumulate=F
                                                     _p(dx), _p(dq_R), _p(dq_P),
                                                     int(bool(accumulate)), _p(ws), ws.numel(),
                                                     _stream(stream)))
+
+
+def poetx_merge_reinit_workspace_bytes(L: LayerDesc) -> int:
+    return lib().poetx_merge_reinit_workspace_bytes(ctypes.byref(L))
+
+
+def poetx_merge_reinit(L: LayerDesc, W0_new, ws, stream=None):
+    """W0_new [n, m] fp32 <- the layer's current map as a plain weight (q reset is the
+    caller's)."""
+    _check("poetx_merge_reinit", lib().poetx_merge_reinit(ctypes.byref(L), _p(W0_new), _p(ws),
+                                                          ws.numel(), _stream(stream)))

@@ -84,6 +84,22 @@ def test_layer_sizes_host_logic(P):
     assert P.poetx_layer_workspace_bytes(_desc(P, act=P.F32, wdt=P.F32, b=32), N, 0) > 0
 
 
+def test_merge_reinit_workspace_host_logic(P):
+    L = _desc(P)
+    need = P.poetx_merge_reinit_workspace_bytes(L)
+    assert need >= (256 + 512) * 64 * 4 * 3 + 2 * 256 * 512 * 4  # G, Q, Q^2; T, M
+    assert P.poetx_merge_reinit_workspace_bytes(_desc(P, wdt=P.I8, variant=P.MEM)) >= \
+        need + 256 * 512 * 4                                      # the dequantised W'
+    assert P.poetx_merge_reinit_workspace_bytes(_desc(P, b=100)) == 0
+    lib = P.lib()
+    fake = ctypes.c_void_p(4096)
+    assert lib.poetx_merge_reinit(ctypes.byref(L), fake, fake, 16, None) == 5
+    assert lib.poetx_merge_reinit(ctypes.byref(L), ctypes.c_void_p(4100), fake, 1 << 30,
+                                  None) == 4
+    assert lib.poetx_merge_reinit(ctypes.byref(_desc(P, order=2)), fake, fake, 1 << 30,
+                                  None) == 6
+
+
 def test_argument_errors_before_launch(P):
     lib = P.lib()
     fake = ctypes.c_void_p(4096)
