@@ -280,6 +280,26 @@ def merge_reinit(Wp, perm_m, perm_n, q_R, q_P, b: int, order: int = 3) -> np.nda
 
 
 # ----------------------------------------------------------------------------------------
+# Optimizer step on the packed triangles.  The POET-X summary ("Core method" §4) counts the
+# optimizer state per stored parameter, b(b-1)/2 per block, and ("Practical guidance" 3)
+# scales the learning rate by gamma = 0.5 for POET-XQ; it names no optimizer.  Our reading:
+# Adam (Kingma & Ba, Algorithm 1) with decoupled weight decay (AdamW), elementwise on q;
+# gamma is folded into lr by the caller.
+# ----------------------------------------------------------------------------------------
+def adam_step(q, g, m, v, t: int, lr: float, beta1: float = 0.9, beta2: float = 0.999,
+              eps: float = 1e-8, weight_decay: float = 0.0):
+    """One step at step count t >= 1.  Returns (q_new, m_new, v_new)."""
+    q = np.asarray(q, dtype=F64)
+    g = np.asarray(g, dtype=F64)
+    m_new = beta1 * np.asarray(m, dtype=F64) + (1.0 - beta1) * g
+    v_new = beta2 * np.asarray(v, dtype=F64) + (1.0 - beta2) * g * g
+    m_hat = m_new / (1.0 - beta1 ** t)
+    v_hat = v_new / (1.0 - beta2 ** t)
+    q_new = q - lr * (m_hat / (np.sqrt(v_hat) + eps) + weight_decay * q)
+    return q_new, m_new, v_new
+
+
+# ----------------------------------------------------------------------------------------
 # Error metric used by every parity test: relative Frobenius error, optionally the max over
 # the leading (block) axis.
 # ----------------------------------------------------------------------------------------

@@ -396,6 +396,41 @@ def test_merge_reinit_singular_values_within_cnp_bound():
     assert np.all(ratio <= 1 + 1e-12) and np.all(ratio >= lo - 1e-12), (ratio, lo)
 
 
+# ------------------------------------------------------------------ optimizer on triu(q)
+def test_adam_first_step_closed_form():
+    """t = 1 from zero state: m_hat = g and v_hat = g^2 exactly, so the step is
+    -lr g / (|g| + eps) (Kingma & Ba, Algorithm 1); |g| near eps separates eps outside the
+    square root from eps inside it."""
+    g = np.array([3.0, -2e-8, 1e-8, -0.5, 0.0])
+    q = np.array([0.1, 0.2, -0.3, 0.4, 0.5])
+    z = np.zeros_like(g)
+    qn, m, v = O.adam_step(q, g, z, z, 1, lr=0.01, eps=1e-8)
+    np.testing.assert_allclose(qn, q - 0.01 * g / (np.abs(g) + 1e-8), rtol=0, atol=1e-16)
+    np.testing.assert_allclose(m, 0.1 * g, rtol=1e-15, atol=0)
+    np.testing.assert_allclose(v, 0.001 * g * g, rtol=1e-12, atol=0)
+
+
+def test_adam_constant_gradient_is_bias_free():
+    """With a constant gradient the bias corrections make m_hat = g and v_hat = g^2 at every
+    step, so T steps move q by exactly T lr g / (|g| + eps)."""
+    g = np.array([0.7, -1.3, 2e-3])
+    q = np.array([1.0, -1.0, 0.25])
+    m = v = np.zeros_like(g)
+    qt = q.copy()
+    for t in range(1, 8):
+        qt, m, v = O.adam_step(qt, g, m, v, t, lr=1e-3, beta1=0.8, beta2=0.95, eps=1e-6)
+    np.testing.assert_allclose(qt, q - 7 * 1e-3 * g / (np.abs(g) + 1e-6), rtol=0, atol=1e-14)
+
+
+def test_adam_weight_decay_alone_and_zero_gradient():
+    q = np.array([0.5, -2.0])
+    z = np.zeros_like(q)
+    qn, m, v = O.adam_step(q, z, z, z, 3, lr=0.1, weight_decay=0.01)
+    np.testing.assert_allclose(qn, q * (1 - 0.1 * 0.01), rtol=0, atol=1e-16)
+    qn, _, _ = O.adam_step(q, z, z, z, 3, lr=0.1)
+    np.testing.assert_array_equal(qn, q)
+
+
 @pytest.mark.parametrize("m,n,b,N", [(8, 8, 4, 3), (12, 8, 4, 2)])
 def test_layer_backward_finite_differences(m, n, b, N):
     L = _layer(m, n, b, N, seed=3, qstd=0.3)
