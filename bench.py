@@ -461,6 +461,18 @@ def main():
                              "note": "fp32 FFMA products (CUDA cores) + CNP + permutation "
                                      "inverse and gather; runs once per many steps"}
     del W0n, mws
+    # the optimizer step on the layer's packed triangles (after the backward of every step;
+    # reads q, dq, m, v and writes q, m, v: 28 bytes per parameter)
+    npar = qR.numel() + qP.numel()
+    oq = torch.zeros(npar, device=dev)
+    og, om, ov = torch.randn_like(oq), torch.zeros_like(oq), torch.zeros_like(oq)
+    us = median_us(lambda: P.poetx_adam_triu(oq, og, om, ov, 1, 1e-3))
+    by = 28.0 * npar
+    setup["adam_triu"] = {"us": us, "params": npar, "bytes": by,
+                          "gbs": by / (us * 1e-6) / 1e9,
+                          "frac_of_hbm": by / (us * 1e-6) / 1e9 / pk["hbm_gbs"],
+                          "note": "per training step, not part of the timed layer step"}
+    del oq, og, om, ov
 
     # every layer of a multi-layer workload (on request): the metric of such a workload is
     # N / (sum of the layers' step times)

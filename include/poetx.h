@@ -279,6 +279,25 @@ size_t poetx_merge_reinit_workspace_bytes(const poetx_layer* L);
 poetx_status poetx_merge_reinit(const poetx_layer* L, float* W0_new, void* ws, size_t ws_bytes,
                                 cudaStream_t stream);
 
+/* ----------------------------------------------------------------------------------------
+ * Optimizer step on the packed triangles (POET-X summary page, "Core method" section 4:
+ * optimizer state per stored parameter, b(b-1)/2 per block; "Practical guidance" 3: the
+ * POET-XQ learning-rate factor gamma).  The pages name no optimizer: this is Adam (Kingma &
+ * Ba, Algorithm 1) with decoupled weight decay, the library's reading:
+ *   m <- beta1 m + (1 - beta1) g,  v <- beta2 v + (1 - beta2) g^2,
+ *   q <- q - lr (m / (1 - beta1^step) / (sqrt(v / (1 - beta2^step)) + eps) + weight_decay q)
+ * elementwise over `count` fp32 values (q, dq = g, m, v: device, 16-byte aligned, updated in
+ * place except dq; m and v start at zero).  Use it after the data-parallel sum of dq; fold
+ * gamma into lr for POET-XQ.  step >= 1 (the caller counts), 0 <= beta < 1; otherwise
+ * POETX_ERR_ARG before any launch.
+ * ------------------------------------------------------------------------------------- */
+typedef struct poetx_adam {
+  float lr, beta1, beta2, eps, weight_decay;
+  int step;
+} poetx_adam;
+poetx_status poetx_adam_triu(float* q, const float* dq, float* m, float* v, long long count,
+                             const poetx_adam* hp, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

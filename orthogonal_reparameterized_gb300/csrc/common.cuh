@@ -89,7 +89,7 @@ inline cudaError_t launch_pdl_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 
 enum Stage : int {
   ST_TRIU_UNPACK = 0, ST_CNP_Q2, ST_CNP_G, ST_CNP_SUM, ST_CNP_M1, ST_CNP_QBAR, ST_TRIU_PACK,
   ST_PERM_GATHER, ST_PERM_SCATTER, ST_BLOCKDIAG, ST_WPRIME, ST_WGRAD, ST_QUANTIZE, ST_MERGE,
-  ST_MERGE_REINIT,
+  ST_MERGE_REINIT, ST_OPTIM,
   ST_COUNT
 };
 // Called after every kernel launch of the library: counts it and, when stage timing is on,

@@ -37,6 +37,12 @@ class LayerDesc(ctypes.Structure):
                 ("w_scale", _vp), ("q_R", _vp), ("q_P", _vp)]
 
 
+class AdamDesc(ctypes.Structure):
+    """Mirror of ``poetx_adam``."""
+    _fields_ = [("lr", _f), ("beta1", _f), ("beta2", _f), ("eps", _f), ("weight_decay", _f),
+                ("step", _i)]
+
+
 _SIGS = {
     "poetx_status_str": (ctypes.c_char_p, [_i]),
     "poetx_get_device_error": (_i, [_vp]),
@@ -67,6 +73,8 @@ _SIGS = {
                              _vp, _sz, _vp]),
     "poetx_merge_reinit_workspace_bytes": (_sz, [ctypes.POINTER(LayerDesc)]),
     "poetx_merge_reinit": (_i, [ctypes.POINTER(LayerDesc), _vp, _vp, _sz, _vp]),
+    "poetx_adam_triu": (_i, [_vp, _vp, _vp, _vp, ctypes.c_longlong, ctypes.POINTER(AdamDesc),
+                             _vp]),
 }
 
 _lib: Optional[ctypes.CDLL] = None
@@ -290,3 +298,11 @@ def poetx_merge_reinit(L: LayerDesc, W0_new, ws, stream=None):
     caller's)."""
     _check("poetx_merge_reinit", lib().poetx_merge_reinit(ctypes.byref(L), _p(W0_new), _p(ws),
                                                           ws.numel(), _stream(stream)))
+
+
+def poetx_adam_triu(q, dq, m, v, step: int, lr: float, beta1: float = 0.9, beta2: float = 0.999,
+                    eps: float = 1e-8, weight_decay: float = 0.0, stream=None):
+    """In-place Adam step on the packed triangles q (m, v: state, zero at step 1)."""
+    hp = AdamDesc(lr, beta1, beta2, eps, weight_decay, step)
+    _check("poetx_adam_triu", lib().poetx_adam_triu(_p(q), _p(dq), _p(m), _p(v), q.numel(),
+                                                    ctypes.byref(hp), _stream(stream)))

@@ -100,6 +100,20 @@ def test_merge_reinit_workspace_host_logic(P):
                                   None) == 6
 
 
+def test_adam_argument_errors(P):
+    lib = P.lib()
+    fake = ctypes.c_void_p(4096)
+    hp = P.AdamDesc(1e-3, 0.9, 0.999, 1e-8, 0.0, 0)          # step 0
+    assert lib.poetx_adam_triu(fake, fake, fake, fake, 8, ctypes.byref(hp), None) == 1
+    hp.step = 1
+    assert lib.poetx_adam_triu(fake, fake, fake, fake, 0, ctypes.byref(hp), None) == 0
+    assert lib.poetx_adam_triu(ctypes.c_void_p(4100), fake, fake, fake, 8, ctypes.byref(hp),
+                               None) == 4
+    hp.beta2 = 1.0
+    assert lib.poetx_adam_triu(fake, fake, fake, fake, 8, ctypes.byref(hp), None) == 1
+    assert lib.poetx_adam_triu(fake, fake, fake, fake, 8, None, None) == 1
+
+
 def test_argument_errors_before_launch(P):
     lib = P.lib()
     fake = ctypes.c_void_p(4096)
