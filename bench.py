@@ -215,6 +215,14 @@ def main():
         dist.init_process_group("nccl", device_id=dev)
     P.lib()
 
+    def check_err(section):
+        """Fail loudly, naming the section, if a kernel recorded an error (a bounded wait
+        that expired): no number is reported from such a run."""
+        st = P.poetx_get_device_error()
+        if st != 0:
+            raise RuntimeError(f"device error after {section}: {P.status_str(st)} "
+                               f"(wait site {P.poetx_timeout_site()})")
+
     wl = inputs.WORKLOADS[args.workload]
     layer = wl.layers[0]
     m, n, b, N = layer.m, layer.n, wl.b, wl.N
@@ -321,10 +329,12 @@ def main():
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         ms_step = float(tt.item())
     value = world * N / (ms_step * 1e-3)
+    check_err("graph-replayed steps")
     # the same step issued eagerly (host launches through the C ABI), same protocol
     ems, _ = timed_steps(main_b, max(50, args.steps // 10), 5)
     eager = {"tokens_per_s": N / (statistics.mean(ems) * 1e-3), "ms_per_step": statistics.mean(ems)}
 
+    check_err("eager steps")
     # the other variant, same protocol, fewer steps
     other = {}
     if wl.wdt != "i8":
@@ -336,6 +346,7 @@ def main():
                      "ms_per_step": statistics.mean(oms)}
         del ob, og
 
+    check_err("the other variant")
     # per-stage times inside the same layer calls (library stage events), same flushes
     P.poetx_profile_enable(True)
     P.poetx_profile_collect()
@@ -385,6 +396,7 @@ def main():
             hbm[name] = {"algorithmic_bytes_per_launch": by, "achieved_gbs": gbs,
                          "frac_of_hbm": gbs / pk["hbm_gbs"]}
 
+    check_err("per-stage timing")
     # CNP blocks/s (standalone, both sides' blocks)
     nblk = (m + n) // b
     qcat = torch.cat([qR, qP], 0).contiguous()
@@ -421,6 +433,7 @@ def main():
                         "peak_source": "152 SMs x 128 FP32 lanes x 2 flop x max SM clock"}}
     del dG, Gb, wsc
 
+    check_err("CNP timing")
     # amortised set-up stages, timed on their own (merge once per permutation draw, the int8
     # quantiser once per weight): every launch reads and writes the whole weight
     def median_us(fn, reps=20):
@@ -451,6 +464,7 @@ def main():
     setup["quantize_rows_int8"] = {"us": us, "bytes": by, "gbs": by / (us * 1e-6) / 1e9,
                                    "frac_of_hbm": by / (us * 1e-6) / 1e9 / pk["hbm_gbs"]}
     del W0s, Wps, W32s, Wqs, ss
+    check_err("merge/quantise timing")
     # merge-then-reinitialize of the benchmarked layer: W0_new = R W0 P in fp32 (two batched
     # block products of 2 n m b flops each on the CUDA cores, the CNP and two index passes)
     W0n = torch.empty(n, m, device=dev)
@@ -461,6 +475,7 @@ def main():
                              "note": "fp32 FFMA products (CUDA cores) + CNP + permutation "
                                      "inverse and gather; runs once per many steps"}
     del W0n, mws
+    check_err("merge_reinit timing")
     # the optimizer step on the layer's packed triangles (after the backward of every step;
     # reads q, dq, m, v and writes q, m, v: 28 bytes per parameter)
     npar = qR.numel() + qP.numel()
@@ -474,6 +489,7 @@ def main():
                           "note": "per training step, not part of the timed layer step"}
     del oq, og, om, ov
 
+    check_err("adam timing")
     # every layer of a multi-layer workload (on request): the metric of such a workload is
     # N / (sum of the layers' step times)
     block = None
@@ -534,6 +550,7 @@ def main():
         block = {"layers": per, "ms_per_step": tot, "tokens_per_s": N / (tot * 1e-3),
                  "metric": "N / sum of the layers' fwd+bwd step times"}
 
+    check_err("per-layer timing")
     # end to end through the C ABI with host buffers (pinned), copies inside the timed region
     hx = x.cpu().pin_memory()
     hdy = dy.cpu().pin_memory()

@@ -66,6 +66,12 @@ const char* poetx_status_str(poetx_status st);
  * recorded an error since the last call; POETX_ERR_TIMEOUT if a bounded wait expired. */
 poetx_status poetx_get_device_error(cudaStream_t stream);
 
+/* Where the first expired bounded wait seen by poetx_get_device_error happened: a site id,
+ * (source file id) x 10000 + (source line) of the waiting call (file ids: 1 the tensor-core
+ * GEMM engine, 2 the CNP products, 3 the index kernels, 4 the self-test), or 0 if none was
+ * recorded.  Host-only (no synchronisation); for diagnosis. */
+int poetx_timeout_site(void);
+
 /* Self-test of the bounded-wait machinery: launches one block that waits on a shared-memory
  * barrier nothing arrives on, with a limit of timeout_us microseconds; the kernel records
  * POETX_ERR_TIMEOUT in the device error word and returns.  No fault, no hang. */

@@ -7,13 +7,18 @@
 
 namespace poetx {
 
-// One error word per device; kernels receive its address as a parameter and record the
-// first error with an atomic compare-and-swap.
-static __device__ int g_error_word;
+// Site id of this file's bounded waits (file id x 10000 + source line), recorded with
+// the first timeout.
+constexpr int kSite = 4 * 10000;
+
+// Two error words per device (the first error status, the site of the first expired wait);
+// kernels receive their address as a parameter and record with atomic compare-and-swaps.
+static __device__ int g_error_word[2];
 
 static std::mutex g_mu;
 static std::atomic<int*> g_err_ptr[64];
 static std::atomic<int> g_sms[64];
+static std::atomic<int> g_last_site{0};
 
 static int current_device() {
   int dev = 0;
@@ -94,7 +99,7 @@ __global__ void selftest_timeout_kernel(int* err, unsigned long long limit_ns) {
     fence_mbar_init();
   }
   __syncthreads();
-  if (threadIdx.x == 0) mbar_wait_bounded(&bar, 0, err, limit_ns);
+  if (threadIdx.x == 0) mbar_wait_bounded(&bar, 0, err, limit_ns, kSite + __LINE__);
   __syncthreads();
 }
 
@@ -120,14 +125,15 @@ extern "C" const char* poetx_status_str(poetx_status st) {
 extern "C" poetx_status poetx_get_device_error(cudaStream_t stream) {
   int* w = device_error_word();
   if (!w) return POETX_ERR_CUDA;
-  int host = 0;
+  int host[2] = {0, 0};
   POETX_CUDA_TRY(cudaStreamSynchronize(stream));
-  POETX_CUDA_TRY(cudaMemcpy(&host, w, sizeof(int), cudaMemcpyDeviceToHost));
-  if (host != 0) {
-    const int zero = 0;
-    POETX_CUDA_TRY(cudaMemcpy(w, &zero, sizeof(int), cudaMemcpyHostToDevice));
+  POETX_CUDA_TRY(cudaMemcpy(host, w, sizeof(host), cudaMemcpyDeviceToHost));
+  if (host[0] != 0 || host[1] != 0) {
+    const int zero[2] = {0, 0};
+    POETX_CUDA_TRY(cudaMemcpy(w, zero, sizeof(zero), cudaMemcpyHostToDevice));
+    g_last_site.store(host[1]);
   }
-  return static_cast<poetx_status>(host);
+  return static_cast<poetx_status>(host[0]);
 }
 
 extern "C" poetx_status poetx_selftest_timeout(unsigned int timeout_us, cudaStream_t stream) {
@@ -137,6 +143,8 @@ extern "C" poetx_status poetx_selftest_timeout(unsigned int timeout_us, cudaStre
   POETX_CUDA_TRY(cudaGetLastError());
   return POETX_OK;
 }
+
+extern "C" int poetx_timeout_site(void) { return g_last_site.load(); }
 
 extern "C" unsigned long long poetx_launch_count(void) { return g_launches.load(); }
 

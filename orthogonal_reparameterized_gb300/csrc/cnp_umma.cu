@@ -31,6 +31,10 @@
 
 namespace poetx {
 
+// Site id of this file's bounded waits (file id x 10000 + source line), recorded with
+// the first timeout.
+constexpr int kSite = 2 * 10000;
+
 namespace {
 
 constexpr int BM = 128;
@@ -269,7 +273,7 @@ __global__ void __launch_bounds__(cnp_threads(BN), 1)
     for (int kb = 0; kb < num_kb; ++kb) {
       const int s = kb % STAGES;
       const uint32_t ph = (kb / STAGES) & 1;
-      if (*abort_flag || !mbar_wait_bounded(&empty[s], ph ^ 1, p.err, p.limit_ns)) {
+      if (*abort_flag || !mbar_wait_bounded(&empty[s], ph ^ 1, p.err, p.limit_ns, kSite + __LINE__)) {
         *abort_flag = 1;
         break;
       }
@@ -301,8 +305,8 @@ __global__ void __launch_bounds__(cnp_threads(BN), 1)
       const uint32_t ph = (kb / STAGES) & 1;
       const int a = kb % NACC;
       const uint32_t pa = (kb / NACC) & 1;
-      if (*abort_flag || !mbar_wait_bounded(&conv[s], ph, p.err, p.limit_ns) ||
-          !mbar_wait_bounded(&tempty[a], pa ^ 1, p.err, p.limit_ns)) {
+      if (*abort_flag || !mbar_wait_bounded(&conv[s], ph, p.err, p.limit_ns, kSite + __LINE__) ||
+          !mbar_wait_bounded(&tempty[a], pa ^ 1, p.err, p.limit_ns, kSite + __LINE__)) {
         *abort_flag = 1;
         break;
       }
@@ -332,7 +336,7 @@ __global__ void __launch_bounds__(cnp_threads(BN), 1)
     for (int kb = 0; kb < num_kb; ++kb) {
       const int s = kb % STAGES;
       const uint32_t ph = (kb / STAGES) & 1;
-      const bool ok = !*abort_flag && mbar_wait_bounded(&full[s], ph, p.err, p.limit_ns);
+      const bool ok = !*abort_flag && mbar_wait_bounded(&full[s], ph, p.err, p.limit_ns, kSite + __LINE__);
       if (!__all_sync(0xffffffffu, ok)) {
         *abort_flag = 1;
         break;
@@ -407,7 +411,7 @@ __global__ void __launch_bounds__(cnp_threads(BN), 1)
     for (int kb = 0; kb < num_kb; ++kb) {
       const int a = kb % NACC;
       const bool ok = !*abort_flag &&
-                      mbar_wait_bounded(&tfull[a], (kb / NACC) & 1, p.err, p.limit_ns);
+                      mbar_wait_bounded(&tfull[a], (kb / NACC) & 1, p.err, p.limit_ns, kSite + __LINE__);
       ok_all = __all_sync(0xffffffffu, ok);
       if (!ok_all) {
         *abort_flag = 1;
@@ -521,10 +525,10 @@ __global__ void __launch_bounds__(cnp_threads(BN), 1)
   if (warp == 0 && lane == 0 && *abort_flag) {
     // drain: the last STAGES K blocks issued may still be landing
     for (int g = tma_issued - 1; g >= 0 && g >= tma_issued - STAGES; --g)
-      mbar_wait_bounded(&full[g % STAGES], (g / STAGES) & 1, p.err, p.limit_ns);
+      mbar_wait_bounded(&full[g % STAGES], (g / STAGES) & 1, p.err, p.limit_ns, kSite + __LINE__);
   }
   if (warp == 1 && lane == 0 && mma_last >= 0)  // TMEM is freed below: the MMAs must be done
-    mbar_wait_bounded(&tfull[mma_last % NACC], (mma_last / NACC) & 1, p.err, p.limit_ns);
+    mbar_wait_bounded(&tfull[mma_last % NACC], (mma_last / NACC) & 1, p.err, p.limit_ns, kSite + __LINE__);
   tc_fence_before();
   __syncthreads();
   if (threadIdx.x == 0) stamp(31);

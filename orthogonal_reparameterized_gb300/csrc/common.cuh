@@ -30,6 +30,8 @@ namespace poetx {
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
 
 // Address of this device's error word (lazily resolved once per device; host side).
+// The device's error words: [0] the first error status, [1] the site of the first
+// expired wait (see mbar_wait_bounded).
 int* device_error_word();
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -193,15 +195,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 // Wait for the phase with the given parity to complete, for at most limit_ns.  Returns
-// false (and records POETX_ERR_TIMEOUT) if the limit expired.
+// false (and records POETX_ERR_TIMEOUT in err[0], and the waiting site's id in err[1] if
+// it is the first timeout) if the limit expired.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, int* err,
-                                                  unsigned long long limit_ns) {
+                                                  unsigned long long limit_ns, int site) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_ns();
   while (true) {
     for (int i = 0; i < 64; ++i)
       if (mbar_try_wait(bar, parity)) return true;
     if (global_ns() - t0 > limit_ns) {
+      if (err && atomicCAS(err + 1, 0, site) == 0) __threadfence();
       record_error(err, POETX_ERR_TIMEOUT);
       return false;
     }

@@ -13,6 +13,10 @@
 
 namespace poetx {
 
+// Site id of this file's bounded waits (file id x 10000 + source line), recorded with
+// the first timeout.
+constexpr int kSite = 3 * 10000;
+
 // ---------------------------------------------------------------- packed triangle
 // Offset of pair (i, j), i < j, in the row-major strict upper triangle of a b x b block.
 __device__ __forceinline__ long long tri_index(int i, int j, int b) {
@@ -279,7 +283,7 @@ __global__ void __launch_bounds__((kPermWarps + 1) * 32) perm_rows_kernel(
         for (int gr = 0; gr < kPermWarps; ++gr) {
           if (!ok || it >= nr[gr]) continue;
           const int slot = gr * S + k;
-          if (round > 0 && !mbar_wait_bounded(&empty[slot], (uint32_t)((round - 1) & 1), err, limit_ns)) {
+          if (round > 0 && !mbar_wait_bounded(&empty[slot], (uint32_t)((round - 1) & 1), err, limit_ns, kSite + __LINE__)) {
             ok = false;
             continue;
           }
@@ -300,7 +304,7 @@ __global__ void __launch_bounds__((kPermWarps + 1) * 32) perm_rows_kernel(
 #pragma unroll
         for (int gr = 0; gr < kPermWarps; ++gr)
           for (int j = issued[gr] - S < 0 ? 0 : issued[gr] - S; j < issued[gr]; ++j)
-            mbar_wait_bounded(&full[gr * S + j % S], (uint32_t)((j / S) & 1), err, limit_ns);
+            mbar_wait_bounded(&full[gr * S + j % S], (uint32_t)((j / S) & 1), err, limit_ns, kSite + __LINE__);
       }
     }
   } else {
@@ -321,7 +325,7 @@ __global__ void __launch_bounds__((kPermWarps + 1) * 32) perm_rows_kernel(
     uint32_t ph = 0;
     for (int it = 0; it < nrows; ++it) {
       const int slot = g * S + k;
-      const bool got = mbar_wait_bounded(&full[slot], ph, err, limit_ns);
+      const bool got = mbar_wait_bounded(&full[slot], ph, err, limit_ns, kSite + __LINE__);
       if (!group_all(got, g, G)) break;
       if (threadIdx.x == 0 && it < 13) trace_stamp(trace, trace_cap, 4 + 2 * it);  // landed
       const long long r = first + g + (long long)it * stride;

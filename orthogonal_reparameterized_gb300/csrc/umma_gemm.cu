@@ -29,6 +29,10 @@
 
 namespace poetx {
 
+// Site id of this file's bounded waits (file id x 10000 + source line), recorded with
+// the first timeout.
+constexpr int kSite = 1 * 10000;
+
 namespace {
 
 enum Mode : int { MODE_PLAIN = 0, MODE_BLOCKDIAG = 1, MODE_WGRAD = 2 };
@@ -291,7 +295,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       if (RES > 0 && panel_key(c) != cur_key) {
         // the previous panel must be free (all MMAs that read it completed) before reloading
         if (npanels > 0 &&
-            (*abort_flag || !mbar_wait_bounded(rempty, (npanels - 1) & 1, p.err, p.limit_ns))) {
+            (*abort_flag || !mbar_wait_bounded(rempty, (npanels - 1) & 1, p.err, p.limit_ns, kSite + __LINE__))) {
           *abort_flag = 1;
           break;
         }
@@ -313,7 +317,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       for (int kb = 0; kb < c.num_kb; ++kb, ++g) {
         const int s = (int)(g % STAGES);
         const uint32_t ph = (uint32_t)((g / STAGES) & 1);
-        if (*abort_flag || !mbar_wait_bounded(&empty[s], ph ^ 1, p.err, p.limit_ns)) {
+        if (*abort_flag || !mbar_wait_bounded(&empty[s], ph ^ 1, p.err, p.limit_ns, kSite + __LINE__)) {
           *abort_flag = 1;
           ok = false;
           break;
@@ -358,14 +362,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
     }
     // a resident panel still loading must land before the CTA may exit
-    if (RES > 0 && npanels > 0) mbar_wait_bounded(rfull, (npanels - 1) & 1, p.err, p.limit_ns);
+    if (RES > 0 && npanels > 0) mbar_wait_bounded(rfull, (npanels - 1) & 1, p.err, p.limit_ns, kSite + __LINE__);
     // Drain: wait for the last load issued into every stage (already complete in the normal
     // path), so that no copy is in flight when the CTA exits.
     // (Pairs: the loads complete on the even CTA's barriers, so wait instead until the MMAs
     // have released the last stages, which they do only after reading them.)
     for (long long j = g - 1; j >= 0 && j >= g - STAGES; --j)
       mbar_wait_bounded(CL > 1 ? &empty[j % STAGES] : &full[j % STAGES],
-                        (uint32_t)((j / STAGES) & 1), p.err, p.limit_ns);
+                        (uint32_t)((j / STAGES) & 1), p.err, p.limit_ns, kSite + __LINE__);
   } else if (warp == 1 && lane == 0 && crank == 0) {
     // ------------------------------------------------------------ MMA issuer
     long long g = 0;
@@ -376,13 +380,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     for (int t = t_first; t < t_end && ok; t += t_step, ++it) {
       const TileCoords c = tile_coords<BN, B_MN, CL>(p, t, crank);
       const int a = it & 1;
-      if (*abort_flag || !mbar_wait_bounded(&tempty[a], ((it >> 1) & 1) ^ 1, p.err, p.limit_ns)) {
+      if (*abort_flag || !mbar_wait_bounded(&tempty[a], ((it >> 1) & 1) ^ 1, p.err, p.limit_ns, kSite + __LINE__)) {
         *abort_flag = 1;
         break;
       }
       if (RES > 0 && panel_key(c) != cur_key) {
         if (npanels > 0) umma_commit(rempty);  // the old panel is free once these MMAs finish
-        if (*abort_flag || !mbar_wait_bounded(rfull, npanels & 1, p.err, p.limit_ns)) {
+        if (*abort_flag || !mbar_wait_bounded(rfull, npanels & 1, p.err, p.limit_ns, kSite + __LINE__)) {
           *abort_flag = 1;
           break;
         }
@@ -394,7 +398,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       for (int kb = 0; kb < c.num_kb; ++kb, ++g) {
         const int s = (int)(g % STAGES);
         const uint32_t ph = (uint32_t)((g / STAGES) & 1);
-        if (*abort_flag || !mbar_wait_bounded(&full[s], ph, p.err, p.limit_ns)) {
+        if (*abort_flag || !mbar_wait_bounded(&full[s], ph, p.err, p.limit_ns, kSite + __LINE__)) {
           *abort_flag = 1;
           ok = false;
           break;
@@ -421,7 +425,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // TMEM is freed after the final barrier: wait until the last MMAs have completed.
     if (it > 0) {
       const int last = it - 1;
-      mbar_wait_bounded(&tfull[last & 1], (last >> 1) & 1, p.err, p.limit_ns);
+      mbar_wait_bounded(&tfull[last & 1], (last >> 1) & 1, p.err, p.limit_ns, kSite + __LINE__);
     }
   } else if (warp >= 2) {
     // ------------------------------------------------------------ epilogue
@@ -433,7 +437,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     for (int t = t_first; t < t_end; t += t_step, ++it) {
       const TileCoords c = tile_coords<BN, B_MN, CL>(p, t, crank);
       const int a = it & 1;
-      const bool ok = !*abort_flag && mbar_wait_bounded(&tfull[a], (it >> 1) & 1, p.err, p.limit_ns);
+      const bool ok = !*abort_flag && mbar_wait_bounded(&tfull[a], (it >> 1) & 1, p.err, p.limit_ns, kSite + __LINE__);
       if (!__all_sync(0xffffffffu, ok)) {
         *abort_flag = 1;
         break;
@@ -540,21 +544,34 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 // construction) straight into TMEM, and shared memory carries only the raw weight tile and
 // the bf16 activation tile (the B operand).  Forward: W(f, k) = Wq[f][k], out[t][f] =
 // s_f D[f, t]; backward: W(f, k) = Wq[k][f] (the activation was scaled by s beforehand),
-// out[t][f] = D[f, t].  Tiles: 128 features x I8T tokens, K blocks of 64; a 4-deep shared-
-// memory ring, two TMEM accumulators (the epilogue of a tile overlaps the next) and a ring
-// of 4 A slots of 32 TMEM columns with its own "slot free" barriers.  The widening (about
-// 1 us per K block per converter group, measured) bounds the kernel, not the MMAs: deeper
-// rings did not help.
+// out[t][f] = D[f, t].  Tiles: 128 features x I8T = 384 tokens, K blocks of 64; a 3-deep
+// shared-memory ring, one TMEM accumulator of 384 columns and a ring of 4 A slots of 32
+// TMEM columns.  Widening a weight tile takes about as long as the MMAs of 192 tokens
+// (measured), so each widened tile feeds as many tokens as TMEM holds: 384 (two MMAs of
+// N = 192 per K step) instead of 192 with two accumulators, which halves the widening per
+// flop at the price of an epilogue that no longer overlaps the next tile's MMAs.  Tiles are
+// numbered token-fastest, so that the CTAs running at the same time share a few weight
+// tiles (read from DRAM about once) and read the activations from L2.
 //   warp 0      TMA: raw weight tile (fwd: 128 rows x 64 bytes; bwd: 64 rows x 128 bytes)
-//               and the activation tile (I8T rows x 64 bf16, 128-byte swizzle)
-//   warp 1      MMA issuer: 4 tcgen05.mma kind::f16 (K = 16) per K block, A from TMEM
-//   warps 2-9   converters, two groups of four taking alternate K blocks: warp w widens
-//               the 64 K values of lane quarter w % 4 (rows 32 (w % 4) .. +31)
-//   warps 10-13 epilogue: lane quarter w % 4, all I8T tokens, through a transposing tile
-constexpr int I8T = 192;         // tokens per tile
-constexpr int I8_STAGES = 4;      // shared-memory ring (raw weight + activation tiles)
+//               and the activation tile (2 x 192 rows x 64 bf16, 128-byte swizzle)
+//   warp 1      MMA issuer: 2 x 4 tcgen05.mma kind::f16 (K = 16) per K block, A from TMEM
+//   warps 2-13  converters, three groups of four taking every third K block: warp w
+//               widens the 64 K values of lane quarter w % 4 (rows 32 (w % 4) .. +31)
+//   warps 14-17 epilogue: lane quarter w % 4, all I8T tokens, through a transposing tile
+constexpr int I8N = 192;          // tokens per MMA (and per TMA box of the activation tile)
+constexpr int I8_NSUB = 2;        // MMAs per K step sharing the widened weight slot
+constexpr int I8T = I8N * I8_NSUB;  // tokens per tile
+constexpr int I8_STAGES = 3;      // shared-memory ring (raw weight + activation tiles)
 constexpr int I8_ASLOTS = 4;      // TMEM ring of widened weight tiles
-constexpr int I8_CONVW = 8;
+constexpr int I8_CONVG = 3;       // converter groups (four warps each), one per ring stage:
+                                  // a group takes the K blocks g with g % I8_CONVG == its
+                                  // index, so each stage's "full" barrier is waited on by one
+                                  // group only.  (With groups sharing a stage, a group could
+                                  // reach the stage's next-but-one phase while the other
+                                  // group's phase is still in flight, and the parity wait
+                                  // would take the old phase for the new one.)
+constexpr int I8_CONVW = 4 * I8_CONVG;
+static_assert(I8_STAGES % I8_CONVG == 0, "each ring stage belongs to one converter group");
 constexpr int I8_EPIW = 4;
 constexpr int I8_THREADS = 32 * (2 + I8_CONVW + I8_EPIW);
 constexpr uint32_t I8_W_BYTES = 128 * 64;          // raw weight tile
@@ -564,7 +581,7 @@ constexpr int I8_STG_PITCH = 80;                   // 32 features x 2 bytes + 16
 constexpr int I8_SMEM = I8_STAGES * I8_STAGE + I8_EPIW * 32 * I8_STG_PITCH + 1024 + 512;
 
 struct I8Params {
-  int tiles_f, tiles_t, num_tiles;  // tile t: ft = t % tiles_f, tt = t / tiles_f
+  int tiles_f, tiles_t, num_tiles;  // tile t: tt = t % tiles_t, ft = t / tiles_t
   int num_kb;
   long long ntok;                   // tokens
   int nfeat;                        // output features
@@ -590,11 +607,11 @@ __device__ __forceinline__ void umma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, u
 __global__ void __launch_bounds__(I8_THREADS, 1)
     umma_i8_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                    const I8Params p) {
-  constexpr uint32_t ACC_COLS = I8T;           // one accumulator
-  constexpr uint32_t A_COL = 2 * ACC_COLS;     // A slots: A_COL + 32 j
+  constexpr uint32_t ACC_COLS = I8T;           // the accumulator (I8_NSUB x I8N columns)
+  constexpr uint32_t A_COL = ACC_COLS;         // A slots: A_COL + 32 j
   constexpr uint32_t TMEM_COLS = 512;
-  static_assert(A_COL + 32 * I8_ASLOTS <= TMEM_COLS, "accumulators and A slots fit TMEM");
-  constexpr uint32_t IDESC = make_idesc(BM, I8T, false, false);
+  static_assert(A_COL + 32 * I8_ASLOTS <= TMEM_COLS, "accumulator and A slots fit TMEM");
+  constexpr uint32_t IDESC = make_idesc(BM, I8N, false, false);
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -618,13 +635,11 @@ __global__ void __launch_bounds__(I8_THREADS, 1)
       mbar_init(&empty[s], 1);
     }
     for (int j = 0; j < I8_ASLOTS; ++j) {
-      mbar_init(&conv[j], I8_CONVW / 2);  // one converter group per K block
+      mbar_init(&conv[j], 4);  // the four warps of the K block's converter group
       mbar_init(&afree[j], 1);
     }
-    for (int a = 0; a < 2; ++a) {
-      mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], I8_EPIW);
-    }
+    mbar_init(tfull, 1);
+    mbar_init(tempty, I8_EPIW);
     *abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tmW);
@@ -647,20 +662,24 @@ __global__ void __launch_bounds__(I8_THREADS, 1)
     long long g = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
-      const int f0 = (t % p.tiles_f) * BM, t0 = (t / p.tiles_f) * I8T;
+      const int f0 = (t / p.tiles_t) * BM, t0 = (t % p.tiles_t) * I8T;
       for (int kb = 0; kb < p.num_kb; ++kb, ++g) {
         const int s = (int)(g % I8_STAGES);
         const uint32_t ph = (uint32_t)((g / I8_STAGES) & 1);
-        if (*abort_flag || !mbar_wait_bounded(&empty[s], ph ^ 1, p.err, p.limit_ns)) {
+        if (*abort_flag || !mbar_wait_bounded(&empty[s], ph ^ 1, p.err, p.limit_ns, kSite + __LINE__)) {
           *abort_flag = 1;
           ok = false;
           break;
         }
         mbar_arrive_expect_tx(&full[s], I8_STAGE);
-        if (g < 8) trace_stamp(p.trace, p.trace_cap, 2 + (int)g);  // slots 2..9: K block issued
+        // (diagnostic stamps cover 8 K blocks from the middle of the first tile)
+        if (g - p.num_kb / 2 >= 0 && g - p.num_kb / 2 < 8)
+          trace_stamp(p.trace, p.trace_cap, 2 + (int)(g - p.num_kb / 2));  // slots 2..9: issued
         uint8_t* sx = smem + s * I8_STAGE;
         uint8_t* sw = sx + I8_X_BYTES;
-        tma_load_2d(sx, &tmX, &full[s], kb * BK, t0);  // tokens t0.., K columns kb*64..
+#pragma unroll
+        for (int h = 0; h < I8_NSUB; ++h)  // tokens t0 + h I8N.., K columns kb*64..
+          tma_load_2d(sx + h * I8N * 128, &tmX, &full[s], kb * BK, t0 + h * I8N);
         if (!p.trans)
           tma_load_2d(sw, &tmW, &full[s], kb * BK, f0);  // rows f0.. of Wq, K bytes kb*64..
         else
@@ -668,48 +687,49 @@ __global__ void __launch_bounds__(I8_THREADS, 1)
       }
     }
     for (long long j = g - 1; j >= 0 && j >= g - I8_STAGES; --j)
-      mbar_wait_bounded(&full[j % I8_STAGES], (uint32_t)((j / I8_STAGES) & 1), p.err, p.limit_ns);
+      mbar_wait_bounded(&full[j % I8_STAGES], (uint32_t)((j / I8_STAGES) & 1), p.err, p.limit_ns, kSite + __LINE__);
   } else if (warp == 1 && lane == 0) {
     // ---------------------------------------------------------------- MMA issuer
     long long g = 0;
     int it = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x, ++it) {
-      const int a = it & 1;
-      if (*abort_flag || !mbar_wait_bounded(&tempty[a], ((it >> 1) & 1) ^ 1, p.err, p.limit_ns)) {
+      // one accumulator: the epilogue of the previous tile must have drained it
+      if (*abort_flag || !mbar_wait_bounded(tempty, (it & 1) ^ 1, p.err, p.limit_ns, kSite + __LINE__)) {
         *abort_flag = 1;
         break;
       }
       tc_fence_after();
-      const uint32_t d = tmem_base + (uint32_t)(a * ACC_COLS);
+      const uint32_t d = tmem_base;
       for (int kb = 0; kb < p.num_kb; ++kb, ++g) {
         const int s = (int)(g % I8_STAGES);
         const int j = (int)(g % I8_ASLOTS);
         if (*abort_flag ||
-            !mbar_wait_bounded(&conv[j], (uint32_t)((g / I8_ASLOTS) & 1), p.err, p.limit_ns)) {
+            !mbar_wait_bounded(&conv[j], (uint32_t)((g / I8_ASLOTS) & 1), p.err, p.limit_ns, kSite + __LINE__)) {
           *abort_flag = 1;
           ok = false;
           break;
         }
         tc_fence_after();
-        if (g < 8) trace_stamp(p.trace, p.trace_cap, 18 + (int)g);  // slots 18..25: MMAs issued
+        if (g - p.num_kb / 2 >= 0 && g - p.num_kb / 2 < 8)
+          trace_stamp(p.trace, p.trace_cap, 18 + (int)(g - p.num_kb / 2));  // 18..25: MMAs
         const uint32_t xa = smem_base + s * I8_STAGE;
         const uint32_t wa = tmem_base + A_COL + 32u * (uint32_t)j;
 #pragma unroll
         for (int k = 0; k < BK / 16; ++k)  // K = 16 per MMA: 8 TMEM columns of A
-          umma_bf16_ta(d, wa + 8 * k, tile_desc<false>(xa, k), IDESC, (kb | k) != 0);
+#pragma unroll
+          for (int h = 0; h < I8_NSUB; ++h)
+            umma_bf16_ta(d + h * I8N, wa + 8 * k, tile_desc<false>(xa + h * I8N * 128, k), IDESC,
+                         (kb | k) != 0);
         umma_commit(&empty[s]);
         if (I8_ASLOTS < I8_STAGES) umma_commit(&afree[j]);
       }
-      umma_commit(&tfull[a]);
+      umma_commit(tfull);
     }
-    if (it > 0) {
-      const int last = it - 1;
-      mbar_wait_bounded(&tfull[last & 1], (last >> 1) & 1, p.err, p.limit_ns);
-    }
+    if (it > 0) mbar_wait_bounded(tfull, (it - 1) & 1, p.err, p.limit_ns, kSite + __LINE__);
   } else if (warp >= 2 && warp < 2 + I8_CONVW) {
     // ---------------------------------------------------------------- converters
-    // group cg = (w - 2) / 4 takes the K blocks g with g % 2 == cg; warp w widens row
+    // group cg = (w - 2) / 4 takes the K blocks g with g % I8_CONVG == cg; warp w widens row
     // f = 32 (w % 4) + lane of the A operand: 64 int8 values -> 32 bf16 pairs -> TMEM slot
     // g % I8_ASLOTS (|q| <= 127: exact)
     const int q = warp & 3, cg = (warp - 2) >> 2;
@@ -719,16 +739,16 @@ __global__ void __launch_bounds__(I8_THREADS, 1)
     bool ok = true;
     for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
       for (int kb = 0; kb < p.num_kb; ++kb, ++g) {
-        if ((int)(g & 1) != cg) continue;
+        if ((int)(g % I8_CONVG) != cg) continue;
         const int s = (int)(g % I8_STAGES);
         const int j = (int)(g % I8_ASLOTS);
         bool got = !*abort_flag &&
-                   mbar_wait_bounded(&full[s], (uint32_t)((g / I8_STAGES) & 1), p.err, p.limit_ns);
+                   mbar_wait_bounded(&full[s], (uint32_t)((g / I8_STAGES) & 1), p.err, p.limit_ns, kSite + __LINE__);
         // the slot's previous tile must have been read by its MMAs (implied by the ring when
         // it is no deeper than the slots: the stage was refilled only after those MMAs)
         if (I8_ASLOTS < I8_STAGES && got && g >= I8_ASLOTS)
           got = mbar_wait_bounded(&afree[j], (uint32_t)(((g / I8_ASLOTS) - 1) & 1), p.err,
-                                  p.limit_ns);
+                                  p.limit_ns, kSite + __LINE__);
         if (!__all_sync(0xffffffffu, got)) {
           *abort_flag = 1;
           ok = false;
@@ -763,7 +783,8 @@ __global__ void __launch_bounds__(I8_THREADS, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&conv[j]);
-        if (q == 2 && lane == 0 && g < 8) trace_stamp(p.trace, p.trace_cap, 10 + (int)g);  // converted
+        if (q == 2 && lane == 0 && g - p.num_kb / 2 >= 0 && g - p.num_kb / 2 < 8)
+          trace_stamp(p.trace, p.trace_cap, 10 + (int)(g - p.num_kb / 2));  // 10..17: converted
       }
     }
   } else if (warp >= 2 + I8_CONVW) {
@@ -774,10 +795,9 @@ __global__ void __launch_bounds__(I8_THREADS, 1)
     uint8_t* stg = staging + (warp - 2 - I8_CONVW) * 32 * I8_STG_PITCH;
     int it = 0;
     for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++it) {
-      const int f0 = (t % p.tiles_f) * BM + q * 32;
-      const long long t0 = (long long)(t / p.tiles_f) * I8T;
-      const int a = it & 1;
-      const bool ok = !*abort_flag && mbar_wait_bounded(&tfull[a], (it >> 1) & 1, p.err, p.limit_ns);
+      const int f0 = (t / p.tiles_t) * BM + q * 32;
+      const long long t0 = (long long)(t % p.tiles_t) * I8T;
+      const bool ok = !*abort_flag && mbar_wait_bounded(tfull, it & 1, p.err, p.limit_ns, kSite + __LINE__);
       if (!__all_sync(0xffffffffu, ok)) {
         *abort_flag = 1;
         break;
@@ -787,7 +807,7 @@ __global__ void __launch_bounds__(I8_THREADS, 1)
 #pragma unroll 1
       for (int c0 = 0; c0 < I8T; c0 += 32) {
         uint32_t r[32];
-        tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(a * ACC_COLS + c0), r);
+        tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)c0, r);
         tmem_ld_wait();
         // lane f: token j of the chunk at row j, column f of the tile
 #pragma unroll
@@ -806,7 +826,7 @@ __global__ void __launch_bounds__(I8_THREADS, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty[a]);
+      if (lane == 0) mbar_arrive(tempty);
       if (q == 2 && lane == 0 && it < 4) trace_stamp(p.trace, p.trace_cap, 26 + it);  // tile stored
     }
   }
@@ -1056,7 +1076,7 @@ poetx_status umma_wprime_i8(const void* A, long long N, int m, int n, const void
   const int K = trans ? n : m, F = trans ? m : n;  // contraction length, output features
   if (K % 64 || F % 128) return POETX_ERR_SHAPE;
   CUtensorMap tw, tx;
-  if (!make_map(&tx, A, K, N, K, 64, I8T)) return POETX_ERR_CUDA;
+  if (!make_map(&tx, A, K, N, K, 64, I8N)) return POETX_ERR_CUDA;
   if (!trans) {
     if (!make_map_t(&tw, Wq, m, n, m, 64, 128, true)) return POETX_ERR_CUDA;
   } else {

@@ -49,6 +49,7 @@ _SIGS = {
     "poetx_selftest_timeout": (_i, [ctypes.c_uint, _vp]),
     "poetx_set_gemm_engine": (_i, [_i]),
     "poetx_launch_count": (ctypes.c_ulonglong, []),
+    "poetx_timeout_site": (_i, []),
     "poetx_profile_enable": (_i, [_i]),
     "poetx_set_trace_buffer": (_i, [_vp, _sz]),
     "poetx_profile_collect": (_i, [ctypes.POINTER(_i), ctypes.POINTER(_f), _i]),
@@ -306,3 +307,9 @@ def poetx_adam_triu(q, dq, m, v, step: int, lr: float, beta1: float = 0.9, beta2
     hp = AdamDesc(lr, beta1, beta2, eps, weight_decay, step)
     _check("poetx_adam_triu", lib().poetx_adam_triu(_p(q), _p(dq), _p(m), _p(v), q.numel(),
                                                     ctypes.byref(hp), _stream(stream)))
+
+
+def poetx_timeout_site() -> int:
+    """Site id of the first expired bounded wait reported by the last poetx_get_device_error
+    (file id x 10000 + source line), 0 if none."""
+    return lib().poetx_timeout_site()

@@ -13,6 +13,7 @@ def test_bounded_wait_times_out_and_context_survives(P):
     assert P.poetx_get_device_error() == 0
     P.poetx_selftest_timeout(2000)  # 2 ms
     assert P.poetx_get_device_error() == 7  # POETX_ERR_TIMEOUT
+    assert 40000 < P.poetx_timeout_site() < 50000  # the self-test's wait (file id 4)
     assert P.poetx_get_device_error() == 0  # cleared by the read
     X = torch.randn(8, 64, device=DEV).to(torch.bfloat16)
     Y = torch.empty_like(X)
