@@ -99,8 +99,10 @@ def test_wprime_bf16(P, engine, N, m, n, trans):
 
 
 @pytest.mark.parametrize("trans", [False, True])
-def test_wprime_int8(P, engine, trans):
-    N, m, n = 300, 512, 768
+@pytest.mark.parametrize("N,m,n", [(300, 512, 768),
+                                   # several tiles per SM, a ragged last token tile
+                                   (2600, 4096, 2816)])
+def test_wprime_int8(P, engine, trans, N, m, n):
     Wq = torch.randint(-127, 128, (n, m), dtype=torch.int8, device=DEV)
     s = (torch.rand(n, device=DEV) + 0.5) / 127
     A = _rand_bf16((N, n if trans else m)).to(DEV)
