@@ -38,6 +38,8 @@ def parse():
     ap.add_argument("--workload", default="llama1b_2048")
     ap.add_argument("--variant", default="fast", choices=["fast", "mem"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--fusion", default="on", choices=["on", "off"],
+                    help="W' contraction + following block product in one kernel (default on)")
     ap.add_argument("--all-layers", action="store_true",
                     help="also time every layer of a multi-layer workload (the Llama-8B "
                          "block's 7 linears, the 13B MLP's up and down) and report their sum")
@@ -214,6 +216,7 @@ def main():
     if world > 1:
         dist.init_process_group("nccl", device_id=dev)
     P.lib()
+    P.poetx_set_fusion(args.fusion == "on")
 
     def check_err(section):
         """Fail loudly, naming the section, if a kernel recorded an error (a bounded wait
@@ -364,11 +367,16 @@ def main():
                   "ms_per_launch": sum(v) / len(v)} for k, v in stage_ms.items()}
 
     pk = peaks()
-    w_launch_ms = stages.get("wprime_gemm", {}).get("ms_per_launch")
-    flops = 2.0 * N * m * n
+    # the dominant kernel: the W' contraction, or (where the layer fuses them) the W'
+    # contraction with the block-diagonal product after it, whose flops count too
+    fused = "wprime_gemm" not in stages and "wprime_blockdiag_fused" in stages
+    w_launch_ms = stages.get("wprime_blockdiag_fused" if fused else "wprime_gemm",
+                             {}).get("ms_per_launch")
+    flops = 2.0 * N * m * n + (2.0 * N * n * b if fused else 0.0)  # (square layers: n = m)
     achieved = flops / (w_launch_ms * 1e-3) / 1e12 if w_launch_ms else None
     traffic = None
-    prof_json = os.path.join(ROOT, "profiles", f"wprime_gemm_{wl.name}.json")
+    prof_json = os.path.join(ROOT, "profiles", ("wprime_blockdiag_fused" if fused else
+                                                 "wprime_gemm") + f"_{wl.name}.json")
     if os.path.exists(prof_json):
         try:
             pj = json.load(open(prof_json))
@@ -379,7 +387,11 @@ def main():
                 traffic = pj.get("dram_bytes_per_launch")
         except (OSError, ValueError, KeyError):
             traffic = None
-    roofline = {"kernel": "wprime_gemm (tcgen05 W' contraction, fwd B = A W'^T and bwd "
+    roofline = {"kernel": ("wprime_blockdiag_fused (tcgen05 W' contraction with the "
+                           "block-diagonal product after it: fwd z~ = (A W'^T) blkdiag(G_P), "
+                           "bwd dx~ = (dB W') blkdiag(G_R)^T; 2 N m n + 2 N n b flops per "
+                           "launch)") if fused else
+                          "wprime_gemm (tcgen05 W' contraction, fwd B = A W'^T and bwd "
                           "dA = dB W', 2 N m n flops per launch)",
                 "bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops"],
                 "unit": "TFLOP/s", "frac": (achieved / pk["bf16_tflops"]) if achieved else None,
@@ -615,7 +627,7 @@ def main():
             "dtype": wl.act, "data": "synthetic (seeded Philox inputs, shapes and "
                                      "distributions of the workload)",
             "config": {"workload": wl.name, "m": m, "n": n, "b": b, "tokens_per_gpu": N,
-                       "variant": variant, "wdt": wl.wdt,
+                       "variant": variant, "wdt": wl.wdt, "fusion": args.fusion == "on",
                        "parallelism": f"replicas x{world} (token-sharded, no collective)",
                        "l2": "flushed between timed steps (512 MiB memset outside the events)"},
             "variants": {variant: {"tokens_per_s": N / (ms_step * 1e-3), "ms_per_step": ms_step,

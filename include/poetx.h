@@ -82,6 +82,13 @@ poetx_status poetx_selftest_timeout(unsigned int timeout_us, cudaStream_t stream
  * (fp32 accumulation, same rounding of the stored results).  Process-wide. */
 poetx_status poetx_set_gemm_engine(int engine);
 
+/* Diagnostic switch: with on = 1 (the default) the layer runs the W' contraction and the
+ * block-diagonal product that follows it (forward: z~ = (A W'^T) blkdiag(G_P); backward:
+ * dx~ = (dB W') blkdiag(G_R)^T) as one tensor-core kernel where the shape allows (bf16 W',
+ * b = 64, 128 or 256, single-CTA tiles); on = 0 runs them as two kernels.  Same results up to
+ * the order of fp32 accumulation.  Process-wide. */
+poetx_status poetx_set_fusion(int on);
+
 /* Number of kernels this library has launched in the process so far (host counter). */
 unsigned long long poetx_launch_count(void);
 

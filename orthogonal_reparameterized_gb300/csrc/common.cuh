@@ -91,7 +91,7 @@ inline cudaError_t launch_pdl_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 
 enum Stage : int {
   ST_TRIU_UNPACK = 0, ST_CNP_Q2, ST_CNP_G, ST_CNP_SUM, ST_CNP_M1, ST_CNP_QBAR, ST_TRIU_PACK,
   ST_PERM_GATHER, ST_PERM_SCATTER, ST_BLOCKDIAG, ST_WPRIME, ST_WGRAD, ST_QUANTIZE, ST_MERGE,
-  ST_MERGE_REINIT, ST_OPTIM,
+  ST_MERGE_REINIT, ST_OPTIM, ST_WPRIME_FUSED,
   ST_COUNT
 };
 // Called after every kernel launch of the library: counts it and, when stage timing is on,
@@ -233,6 +233,12 @@ __device__ __forceinline__ void tma_load_2d_pair(void* smem_dst, const CUtensorM
 }
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// Shared-memory writes of this thread (generic proxy) made visible to the tensor cores and
+// TMA (async proxy).
+__device__ __forceinline__ void fence_async_shared() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 // ---------------------------------------------------------------- tcgen05

@@ -90,6 +90,15 @@ poetx_status umma_blockdiag(const void* X, long long N, int nblk, int b, const v
 // C[N,n] = A[N,m] W^T (trans=0) or C[N,m] = A[N,n] W (trans=1), W [n,m] bf16.
 poetx_status umma_wprime(const void* A, long long N, int m, int n, const void* W, int trans,
                          void* C, cudaStream_t s);
+// Whether the bf16 contraction runs as 2-CTA pairs (at least as many 256 x 256 tiles as SMs).
+bool umma_wprime_pairs(long long N, int m, int n, int trans);
+// The contraction followed by the block-diagonal product on the same tiles (one launch):
+// C1 = A W^T (trans 0; nullable: not stored) and C2 = C1 blkdiag(G) with G = G_P stacks
+// [n/b, b, b]; or C1 = A W (trans 1) and C2 = C1 blkdiag(G)^T with G = G_R [m/b, b, b].  Taken
+// when umma_wprime_fusable (b = 64, 128 or 256; single-CTA tiles, i.e. not pairs).
+bool umma_wprime_fusable(long long N, int m, int n, int trans, int b);
+poetx_status umma_wprime_fused(const void* A, long long N, int m, int n, const void* W, int trans,
+                               const void* G, int b, void* C1, void* C2, cudaStream_t s);
 // The same contraction with an int8 W, run transposed so that the widened weight is the
 // tensor-memory A operand (K and the output features must be multiples of 64 and 128); the
 // forward multiplies output column r by w_scale[r], the backward expects A to carry the

@@ -23,6 +23,7 @@
 namespace poetx {
 
 static std::atomic<int> g_engine{0};  // 0: tensor cores where supported, 1: CUDA cores only
+static std::atomic<int> g_fuse{1};    // W' contraction + following block product in one kernel
 
 static bool use_umma() { return g_engine.load() == 0 && umma_supported(); }
 
@@ -112,6 +113,13 @@ poetx_status wprime_impl(poetx_dtype act, poetx_dtype wdt, const void* A, long l
   g.kchunk = g.K;
   g.stage = ST_WPRIME;
   return launch_simt_gemm(act, wdt, act, g, s);
+}
+
+// The W' contraction and the block-diagonal product after it in one kernel (bf16 W', the
+// tensor-core engine, shapes the fused kernel takes).
+static bool fused_ok(const poetx_layer* L, long long N, int trans) {
+  return L->act == POETX_BF16 && L->wdt == POETX_BF16 && use_umma() && g_fuse.load() &&
+         umma_wprime_fusable(N, L->m, L->n, trans, L->b);
 }
 
 // ---------------------------------------------------------------- layer plumbing
@@ -227,6 +235,12 @@ static const T* at(const void* base, size_t off) {
 
 using namespace poetx;
 
+extern "C" poetx_status poetx_set_fusion(int on) {
+  if (on != 0 && on != 1) return POETX_ERR_ARG;
+  g_fuse.store(on);
+  return POETX_OK;
+}
+
 extern "C" poetx_status poetx_set_gemm_engine(int engine) {
   if (engine != 0 && engine != 1) return POETX_ERR_ARG;
   g_engine.store(engine);
@@ -326,11 +340,17 @@ extern "C" poetx_status poetx_layer_fwd(const poetx_layer* L, const void* x, int
   void* B = L->variant == POETX_FAST ? at(saved, p.Bsv) : at(ws, p.f_B);
   POETX_TRY(launch_perm_rows(as, false, x, N, m, L->perm_m, xt, nullptr, nullptr, nullptr, stream));
   POETX_TRY(blockdiag_impl(act, xt, N, m / b, b, at(saved, p.GR), 0, nullptr, nullptr, A, stream));
-  POETX_TRY(wprime_impl(act, L->wdt, A, N, m, n, L->Wp, L->w_scale, 0, B, stream));
-  // S6 + S7.  (Storing z~ through the permutation inside the product is supported, but its
-  // 2-byte scattered stores are slower than this coalesced scatter pass.)
   void* zt = at(ws, p.f_zt);
-  POETX_TRY(blockdiag_impl(act, B, N, n / b, b, at(saved, p.GP), 0, nullptr, nullptr, zt, stream));
+  if (fused_ok(L, N, 0)) {
+    // S5 + S6 on the same tiles (mem does not keep B)
+    POETX_TRY(umma_wprime_fused(A, N, m, n, L->Wp, 0, at(saved, p.GP), b,
+                                L->variant == POETX_FAST ? B : nullptr, zt, stream));
+  } else {
+    POETX_TRY(wprime_impl(act, L->wdt, A, N, m, n, L->Wp, L->w_scale, 0, B, stream));
+    POETX_TRY(blockdiag_impl(act, B, N, n / b, b, at(saved, p.GP), 0, nullptr, nullptr, zt, stream));
+  }
+  // S7.  (Storing z~ through the permutation inside the product is supported, but its
+  // 2-byte scattered stores are slower than this coalesced scatter pass.)
   return launch_perm_rows(as, true, zt, N, n, L->perm_n, y, nullptr, nullptr, nullptr, stream);
 }
 
@@ -379,11 +399,17 @@ extern "C" poetx_status poetx_layer_bwd(const poetx_layer* L, const void* x, con
   // int8 weight: dA = dB diag(s) W_q, the row scale is folded into dB's columns
   POETX_TRY(blockdiag_impl(act, dzt, N, n / b, b, GP, 1,
                            L->wdt == POETX_I8 ? L->w_scale : nullptr, nullptr, dB, stream));
-  POETX_TRY(wprime_impl(act, L->wdt, dB, N, m, n, L->Wp, L->w_scale, 1, dA, stream));
-  POETX_TRY(wgrad_impl(act, xt, dA, N, m / b, b, p.splitsR, dGR, stream));
-  // S12 + S13
   void* dxt = at(ws, p.b_dxt);
-  POETX_TRY(blockdiag_impl(act, dA, N, m / b, b, GR, 1, nullptr, nullptr, dxt, stream));
+  if (fused_ok(L, N, 1)) {
+    // S11 + the dx~ half of S12 on the same tiles
+    POETX_TRY(umma_wprime_fused(dB, N, m, n, L->Wp, 1, GR, b, dA, dxt, stream));
+    POETX_TRY(wgrad_impl(act, xt, dA, N, m / b, b, p.splitsR, dGR, stream));
+  } else {
+    POETX_TRY(wprime_impl(act, L->wdt, dB, N, m, n, L->Wp, L->w_scale, 1, dA, stream));
+    POETX_TRY(wgrad_impl(act, xt, dA, N, m / b, b, p.splitsR, dGR, stream));
+    POETX_TRY(blockdiag_impl(act, dA, N, m / b, b, GR, 1, nullptr, nullptr, dxt, stream));
+  }
+  // S13
   if (N > 0)
     POETX_TRY(launch_perm_rows(as, true, dxt, N, m, L->perm_m, dx, nullptr, nullptr, nullptr, stream));
   const CnpSides sides{{L->q_R, L->q_P}, {m / b, n / b}};

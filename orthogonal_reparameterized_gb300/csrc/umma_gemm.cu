@@ -537,6 +537,343 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 }
 
 
+// ---------------------------------------------------------------- fused W' + block product
+// The W' contraction with the block-diagonal product that follows it done on the same tile
+// (POET-X summary page, "Core method" section 1: b = W' a, z = G_P^T b; and the backward's
+// dA = dB W', dx~ = dA G_R^T): a 128 x 256 tile of the first product is complete in TMEM after
+// its K loop; the epilogue rounds it to bf16 into a shared-memory operand tile (and stores it
+// when the caller keeps it), a second round of MMAs multiplies that tile by the G blocks
+// covering its 256 columns (b = 64, 128 or 256 divides 256), and the epilogue stores the
+// result.  This removes one pass over the [N, D] activations.
+//   forward:  C1 = A W'^T (W' K-major), C2[:, jb..] = C1[:, jb..] G_j       (G MN-major)
+//   backward: C1 = A W' (W' MN-major),  C2[:, jb..] = C1[:, jb..] G_j^T     (G K-major)
+// Ring order (one producer, one MMA thread): the K blocks of tile i, then the four G blocks of
+// tile i-1, so that the second product of a tile is issued while the epilogue of the next
+// one is not yet needed and the tensor pipe never waits for the epilogue.  The shared-memory
+// operand tile doubles as each epilogue warp's staging area (every warp owns 32 rows x 128
+// columns of it).
+struct FusedParams {
+  int M;                      // valid token rows
+  int tiles_m, num_tiles;     // tile t: mt = t % tiles_m, nt = t / tiles_m
+  int num_kb;                 // 64-wide K blocks of the first product
+  int b;                      // block size of the second product
+  long long ldc;              // columns of C1 and C2
+  __nv_bfloat16* C1;          // nullable: first product not stored
+  __nv_bfloat16* C2;
+  const uint8_t* bpre;
+  unsigned long long bpre_bytes;
+  unsigned long long* trace;
+  size_t trace_cap;
+  int* err;
+  unsigned long long limit_ns;
+};
+
+constexpr int FZ_BN = 256;
+constexpr int FZ_STAGES = 3;
+constexpr uint32_t FZ_A_BYTES = BM * BK * 2;                 // 16 KB
+constexpr uint32_t FZ_STAGE = FZ_A_BYTES + FZ_BN * BK * 2;   // 48 KB
+constexpr uint32_t FZ_A2_SUB = BM * BK * 2;                  // one 64-column sub-tile: 16 KB
+constexpr uint32_t FZ_A2 = FZ_BN / BK * FZ_A2_SUB;           // 64 KB
+constexpr int FZ_SMEM = FZ_STAGES * FZ_STAGE + FZ_A2 + 1024 + 512;
+static_assert(FZ_SMEM <= 227 * 1024, "fused W' kernel: shared memory");
+
+// byte offset of row r, 16-byte chunk c of a 128 x 64 bf16 K-major tile (128-byte swizzle)
+__device__ __forceinline__ uint32_t sw128_off(int r, int c) {
+  return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
+}
+
+template <bool W_MN, bool G_MN>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    umma_fused_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
+                      const __grid_constant__ CUtensorMap tmG, const FusedParams p) {
+  constexpr uint32_t IDESC1 = make_idesc(BM, FZ_BN, false, W_MN);
+  constexpr uint32_t TMEM_COLS = 2 * FZ_BN;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint8_t* a2 = smem + FZ_STAGES * FZ_STAGE;  // the second product's A operand / staging
+  uint64_t* full = reinterpret_cast<uint64_t*>(a2 + FZ_A2);
+  uint64_t* empty = full + FZ_STAGES;
+  uint64_t* tfull1 = empty + FZ_STAGES;  // [2] first product of the tile in TMEM
+  uint64_t* tfull2 = tfull1 + 2;         // [2] second product in TMEM
+  uint64_t* tempty = tfull2 + 2;         // [2] accumulator drained
+  uint64_t* a2full = tempty + 2;         // operand tile written by every epilogue warp
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(a2full + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) trace_stamp(p.trace, p.trace_cap, 0);
+  pdl_trigger();
+  if (warp == 0 && lane == 0) {
+    for (int s = 0; s < FZ_STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull1[a], 1);
+      mbar_init(&tfull2[a], 1);
+      mbar_init(&tempty[a], kEpiWarps);
+    }
+    mbar_init(a2full, kEpiWarps);
+    *abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmW);
+    tma_prefetch_desc(&tmG);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, TMEM_COLS);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0 && p.bpre) {  // this CTA's share of W' into L2
+    const unsigned long long share =
+        ((p.bpre_bytes + gridDim.x - 1) / gridDim.x + 4095) & ~4095ull;
+    const unsigned long long lo = (unsigned long long)blockIdx.x * share;
+    for (unsigned long long off = lo; off < lo + share && off < p.bpre_bytes; off += 32768) {
+      unsigned long long n = p.bpre_bytes - off;
+      n = n < 32768 ? n : 32768;
+      if (off + n > lo + share) n = lo + share - off;
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p.bpre + off),
+                   "r"((uint32_t)(n & ~15ull))
+                   : "memory");
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const uint32_t smem_base = smem_u32(smem);
+  const uint32_t a2_base = smem_u32(a2);
+  pdl_wait();
+  if (threadIdx.x == 0) trace_stamp(p.trace, p.trace_cap, 1);
+  const int b = p.b;
+  const uint32_t g2_bytes = (uint32_t)b * BK * 2;
+
+  if (warp == 0 && lane == 0) {
+    // ---------------------------------------------------------------- TMA producer
+    long long g = 0;
+    bool ok = true;
+    auto slot = [&](uint32_t bytes, uint8_t*& st) -> bool {
+      const int s = (int)(g % FZ_STAGES);
+      const uint32_t ph = (uint32_t)((g / FZ_STAGES) & 1);
+      if (*abort_flag || !mbar_wait_bounded(&empty[s], ph ^ 1, p.err, p.limit_ns, kSite + __LINE__)) {
+        *abort_flag = 1;
+        return false;
+      }
+      mbar_arrive_expect_tx(&full[s], bytes);
+      st = smem + s * FZ_STAGE;
+      return true;
+    };
+    // the G blocks covering the 256 columns of tile column nt (K of the second product)
+    auto issue_g2 = [&](int nt) -> bool {
+      for (int kb2 = 0; kb2 < FZ_BN / BK; ++kb2, ++g) {
+        uint8_t* st;
+        if (!slot(g2_bytes, st)) return false;
+        const int col = nt * FZ_BN + kb2 * BK;  // first column of the K block
+        const int j = col / b, r0 = col % b;
+        uint8_t* sb = st + FZ_A_BYTES;
+        if (G_MN) {  // rows r0.. of G_j, all b columns: b/64 boxes of 64 x 64
+          for (int i = 0; i < b / 64; ++i)
+            tma_load_2d(sb + i * 8192, &tmG, &full[(int)(g % FZ_STAGES)], 64 * i, j * b + r0);
+        } else {     // all b rows of G_j, columns r0..: one box of 64 x b
+          tma_load_2d(sb, &tmG, &full[(int)(g % FZ_STAGES)], r0, j * b);
+        }
+      }
+      return true;
+    };
+    int prev_nt = -1;
+    for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+      const int mt = t % p.tiles_m, nt = t / p.tiles_m;
+      for (int kb = 0; kb < p.num_kb; ++kb, ++g) {
+        uint8_t* st;
+        if (!slot(FZ_STAGE, st)) {
+          ok = false;
+          break;
+        }
+        if (g == 0) trace_stamp(p.trace, p.trace_cap, 2);
+        uint64_t* fb = &full[(int)(g % FZ_STAGES)];
+        tma_load_2d(st, &tmA, fb, kb * BK, mt * BM);
+        if (!W_MN) {
+          tma_load_2d(st + FZ_A_BYTES, &tmW, fb, kb * BK, nt * FZ_BN);
+        } else {
+#pragma unroll
+          for (int i = 0; i < FZ_BN / 64; ++i)
+            tma_load_2d(st + FZ_A_BYTES + i * 8192, &tmW, fb, nt * FZ_BN + 64 * i, kb * BK);
+        }
+      }
+      if (!ok) break;
+      if (prev_nt >= 0 && !issue_g2(prev_nt)) {
+        ok = false;
+        break;
+      }
+      prev_nt = nt;
+    }
+    if (ok && prev_nt >= 0) issue_g2(prev_nt);
+    for (long long j = g - 1; j >= 0 && j >= g - FZ_STAGES; --j)
+      mbar_wait_bounded(&full[j % FZ_STAGES], (uint32_t)((j / FZ_STAGES) & 1), p.err, p.limit_ns,
+                        kSite + __LINE__);
+  } else if (warp == 1 && lane == 0) {
+    // ---------------------------------------------------------------- MMA issuer
+    long long g = 0;
+    bool ok = true;
+    auto take = [&](int& s) -> bool {
+      s = (int)(g % FZ_STAGES);
+      const uint32_t ph = (uint32_t)((g / FZ_STAGES) & 1);
+      if (*abort_flag || !mbar_wait_bounded(&full[s], ph, p.err, p.limit_ns, kSite + __LINE__)) {
+        *abort_flag = 1;
+        return false;
+      }
+      tc_fence_after();
+      return true;
+    };
+    // second product of the tile with index i (its accumulator holds the first product,
+    // already read out into the operand tile by the epilogue)
+    auto mma2 = [&](int i) -> bool {
+      const int a = i & 1;
+      if (*abort_flag || !mbar_wait_bounded(a2full, (uint32_t)(i & 1), p.err, p.limit_ns, kSite + __LINE__)) {
+        *abort_flag = 1;
+        return false;
+      }
+      tc_fence_after();
+      const uint32_t idesc2 = make_idesc(BM, b, false, G_MN);
+      for (int kb2 = 0; kb2 < FZ_BN / BK; ++kb2, ++g) {
+        int s;
+        if (!take(s)) return false;
+        const int lb = kb2 * BK / b, kk = kb2 * BK % b;  // block within the tile, K offset
+        const uint32_t d = tmem_base + (uint32_t)(a * FZ_BN + lb * b);
+        const uint32_t bb = smem_base + s * FZ_STAGE + FZ_A_BYTES;
+#pragma unroll
+        for (int k = 0; k < BK / 16; ++k)
+          umma_bf16(d, tile_desc<false>(a2_base + kb2 * FZ_A2_SUB, k), tile_desc<G_MN>(bb, k),
+                    idesc2, (kk | k) != 0);
+        umma_commit(&empty[s]);
+      }
+      umma_commit(&tfull2[a]);
+      return true;
+    };
+    int it = 0;
+    for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x, ++it) {
+      const int a = it & 1;
+      if (*abort_flag ||
+          !mbar_wait_bounded(&tempty[a], ((it >> 1) & 1) ^ 1, p.err, p.limit_ns, kSite + __LINE__)) {
+        *abort_flag = 1;
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t d = tmem_base + (uint32_t)(a * FZ_BN);
+      for (int kb = 0; kb < p.num_kb; ++kb, ++g) {
+        int s;
+        if (!take(s)) {
+          ok = false;
+          break;
+        }
+        if (g == 0) trace_stamp(p.trace, p.trace_cap, 3);
+        const uint32_t sa = smem_base + s * FZ_STAGE;
+#pragma unroll
+        for (int k = 0; k < BK / 16; ++k)
+          umma_bf16(d, tile_desc<false>(sa, k), tile_desc<W_MN>(sa + FZ_A_BYTES, k), IDESC1,
+                    (kb | k) != 0);
+        umma_commit(&empty[s]);
+      }
+      if (!ok) break;
+      umma_commit(&tfull1[a]);
+      if (it > 0 && !mma2(it - 1)) {
+        ok = false;
+        break;
+      }
+    }
+    if (ok && it > 0) mma2(it - 1);
+    if (it > 0) mbar_wait_bounded(&tfull2[(it - 1) & 1], ((it - 1) >> 1) & 1, p.err, p.limit_ns,
+                                  kSite + __LINE__);
+  } else if (warp >= 2) {
+    // ---------------------------------------------------------------- epilogue
+    // warp w: rows 32 (w % 4) .. +31 of the tile, columns 128 h .. +127 (h = (w - 2) / 4),
+    // i.e. the operand tile's 64-column sub-tiles 2h and 2h + 1 for those rows
+    const int q = warp & 3, h = (warp - 2) >> 2;
+    const int r = q * 32 + lane;
+    // TMEM (64 columns from column c of accumulator a, this warp's lanes) -> bf16 -> the
+    // operand tile's sub-tile kb2, row r
+    auto to_tile = [&](int a, int kb2) {
+      uint32_t v[64];
+      const uint32_t ta = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(a * FZ_BN + kb2 * BK);
+      tmem_ld_32x32b_x32(ta, *reinterpret_cast<uint32_t(*)[32]>(v));
+      tmem_ld_32x32b_x32(ta + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
+      tmem_ld_wait();
+      uint8_t* sub = a2 + kb2 * FZ_A2_SUB;
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        *reinterpret_cast<uint4*>(sub + sw128_off(r, c)) =
+            make_uint4(pack_bf16x2(__uint_as_float(v[8 * c]), __uint_as_float(v[8 * c + 1])),
+                       pack_bf16x2(__uint_as_float(v[8 * c + 2]), __uint_as_float(v[8 * c + 3])),
+                       pack_bf16x2(__uint_as_float(v[8 * c + 4]), __uint_as_float(v[8 * c + 5])),
+                       pack_bf16x2(__uint_as_float(v[8 * c + 6]), __uint_as_float(v[8 * c + 7])));
+    };
+    // this warp's 32 rows x 128 columns of the operand tile -> global (8 lanes per 128-byte
+    // row segment, 4 rows per pass)
+    auto store = [&](__nv_bfloat16* C, long long row0, long long col0) {
+      const int rr0 = lane >> 3, c = lane & 7;
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int kb2 = 2 * h + u;
+        const uint8_t* sub = a2 + kb2 * FZ_A2_SUB;
+#pragma unroll 2
+        for (int rr = rr0; rr < 32; rr += 4) {
+          const int rt = q * 32 + rr;
+          const long long grow = row0 + rt;
+          if (grow >= p.M) continue;
+          const uint4 val = *reinterpret_cast<const uint4*>(sub + sw128_off(rt, c));
+          *reinterpret_cast<uint4*>(C + grow * p.ldc + col0 + kb2 * BK + c * 8) = val;
+        }
+      }
+    };
+    int it = 0;
+    for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++it) {
+      const int a = it & 1;
+      const long long row0 = (long long)(t % p.tiles_m) * BM;
+      const long long col0 = (long long)(t / p.tiles_m) * FZ_BN;
+      bool ok = !*abort_flag && mbar_wait_bounded(&tfull1[a], (it >> 1) & 1, p.err, p.limit_ns,
+                                                  kSite + __LINE__);
+      if (!__all_sync(0xffffffffu, ok)) {
+        *abort_flag = 1;
+        break;
+      }
+      tc_fence_after();
+      to_tile(a, 2 * h);
+      to_tile(a, 2 * h + 1);
+      fence_async_shared();  // generic writes -> visible to the tensor cores
+      __syncwarp();
+      if (p.C1) store(p.C1, row0, col0);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(a2full);
+      ok = !*abort_flag && mbar_wait_bounded(&tfull2[a], (it >> 1) & 1, p.err, p.limit_ns,
+                                             kSite + __LINE__);
+      if (!__all_sync(0xffffffffu, ok)) {
+        *abort_flag = 1;
+        break;
+      }
+      tc_fence_after();
+      to_tile(a, 2 * h);  // the second product, staged in the same rows and columns
+      to_tile(a, 2 * h + 1);
+      __syncwarp();
+      store(p.C2, row0, col0);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[a]);
+      if (warp == 2 && lane == 0 && it < 12) trace_stamp(p.trace, p.trace_cap, 4 + 2 * it);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x == 0) trace_stamp(p.trace, p.trace_cap, 31);
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
 // ---------------------------------------------------------------- int8 W' contraction
 // With an int8 W' the contraction runs transposed: D[f, t] = sum_k W(f, k) act[t, k] for
 // output feature f and token t, so that the widened weight is the A operand, which tcgen05
@@ -1048,8 +1385,7 @@ poetx_status umma_wprime(const void* A, long long N, int m, int n, const void* W
   // there are at least two of them per pair of SMs; with fewer, both forms take the same
   // number of tile rounds and the single-CTA 128 x 256 tiles start faster.
   const int tm2 = (tm + 1) / 2;
-  const long long pair_tiles = (long long)tm2 * ((trans ? m : n) / 256);
-  const bool pairs = pair_tiles >= sm_count();
+  const bool pairs = umma_wprime_pairs(N, m, n, trans);
   if (!trans) {  // C[N,n] = A[N,m] W^T
     if (!make_map(&ta, A, m, N, m, 64, 128)) return POETX_ERR_CUDA;
     // (pairs: each CTA loads half of a 256-row W' tile)
@@ -1066,6 +1402,65 @@ poetx_status umma_wprime(const void* A, long long N, int m, int n, const void* W
   p.ldc = m;
   if (pairs) return launch<256, 6, false, true, false, 0, 2>(ta, tb, p, tm2, m / 256, 1, s);
   return launch<256, 4, false, true, false>(ta, tb, p, tm, m / 256, 1, s);
+}
+
+bool umma_wprime_pairs(long long N, int m, int n, int trans) {
+  const long long tm2 = ((N + BM - 1) / BM + 1) / 2;
+  return tm2 * ((trans ? m : n) / 256) >= sm_count();
+}
+
+bool umma_wprime_fusable(long long N, int m, int n, int trans, int b) {
+  const int out = trans ? m : n, K = trans ? n : m;
+  return N > 0 && (b == 64 || b == 128 || b == 256) && out % 256 == 0 && K % 64 == 0 &&
+         !umma_wprime_pairs(N, m, n, trans);
+}
+
+poetx_status umma_wprime_fused(const void* A, long long N, int m, int n, const void* W, int trans,
+                               const void* G, int b, void* C1, void* C2, cudaStream_t s) {
+  if (N == 0) return POETX_OK;
+  const int out = trans ? m : n, K = trans ? n : m;
+  if (!(b == 64 || b == 128 || b == 256) || out % 256 || K % 64) return POETX_ERR_SHAPE;
+  CUtensorMap ta, tw, tg;
+  if (!make_map(&ta, A, K, N, K, 64, 128)) return POETX_ERR_CUDA;
+  if (!trans) {
+    if (!make_map(&tw, W, m, n, m, 64, 256)) return POETX_ERR_CUDA;
+    if (!make_map(&tg, G, b, (uint64_t)(out / b) * b, b, 64, 64)) return POETX_ERR_CUDA;
+  } else {
+    if (!make_map(&tw, W, m, n, m, 64, 64)) return POETX_ERR_CUDA;
+    if (!make_map(&tg, G, b, (uint64_t)(out / b) * b, b, 64, b)) return POETX_ERR_CUDA;
+  }
+  FusedParams p{};
+  p.M = (int)N;
+  p.tiles_m = (int)((N + BM - 1) / BM);
+  const long long tiles = (long long)p.tiles_m * (out / FZ_BN);
+  if (tiles > 0x7fffffffLL) return POETX_ERR_SHAPE;
+  p.num_tiles = (int)tiles;
+  p.num_kb = K / 64;
+  p.b = b;
+  p.ldc = out;
+  p.C1 = static_cast<__nv_bfloat16*>(C1);
+  p.C2 = static_cast<__nv_bfloat16*>(C2);
+  p.bpre = static_cast<const uint8_t*>(W);
+  p.bpre_bytes = (unsigned long long)m * n * 2;
+  p.trace = trace_buffer(&p.trace_cap);
+  p.err = device_error_word();
+  p.limit_ns = kWaitLimitNs;
+  auto k = trans ? umma_fused_kernel<true, false> : umma_fused_kernel<false, true>;
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [&] {
+    attr_err = cudaFuncSetAttribute(umma_fused_kernel<false, true>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, FZ_SMEM);
+    if (attr_err == cudaSuccess)
+      attr_err = cudaFuncSetAttribute(umma_fused_kernel<true, false>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize, FZ_SMEM);
+  });
+  POETX_CUDA_TRY(attr_err);
+  const int grid = (int)(tiles < sm_count() ? tiles : sm_count());
+  POETX_CUDA_TRY(launch_pdl(k, dim3(grid), dim3(kGemmThreads), FZ_SMEM, s, ta, tw, tg, p));
+  POETX_CUDA_TRY(cudaGetLastError());
+  after_launch(s, ST_WPRIME_FUSED);
+  return POETX_OK;
 }
 
 // int8 W' contraction (the transposed kernel above).  Forward (trans = 0): C[N, n] =

@@ -48,6 +48,7 @@ _SIGS = {
     "poetx_get_device_error": (_i, [_vp]),
     "poetx_selftest_timeout": (_i, [ctypes.c_uint, _vp]),
     "poetx_set_gemm_engine": (_i, [_i]),
+    "poetx_set_fusion": (_i, [_i]),
     "poetx_launch_count": (ctypes.c_ulonglong, []),
     "poetx_timeout_site": (_i, []),
     "poetx_profile_enable": (_i, [_i]),
@@ -130,6 +131,10 @@ def poetx_selftest_timeout(timeout_us: int, stream=None):
 
 def poetx_set_gemm_engine(engine: int):
     _check("poetx_set_gemm_engine", lib().poetx_set_gemm_engine(engine))
+
+
+def poetx_set_fusion(on: bool):
+    _check("poetx_set_fusion", lib().poetx_set_fusion(1 if on else 0))
 
 
 def poetx_launch_count() -> int:
