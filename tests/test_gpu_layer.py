@@ -196,3 +196,24 @@ def test_layer_bf16_split_tiles_deterministic(P):
     b = run_layer(P, inp, 256, "bf16", "bf16", "mem")
     for k in ("y", "dx", "dq_R", "dq_P"):
         assert np.array_equal(a[k], b[k]), k
+
+
+@pytest.mark.parametrize("m,n,b,N", [(512, 256, 128, 77), (256, 512, 64, 200),
+                                     (2048, 1024, 256, 1000)])
+@pytest.mark.parametrize("variant", ["fast", "mem"])
+def test_layer_fused_and_separate_products_agree(P, m, n, b, N, variant):
+    """The W' contraction fused with the block-diagonal product after it (one kernel) and
+    the two as separate kernels both match the oracle, and each other to within their
+    accumulation-order differences."""
+    inp = inputs.small_layer_inputs(61 + b, m, n, b, N, act="bf16", wdt="bf16")
+    try:
+        P.poetx_set_fusion(False)
+        sep = run_layer(P, inp, b, "bf16", "bf16", variant)
+    finally:
+        P.poetx_set_fusion(True)
+    fus = run_layer(P, inp, b, "bf16", "bf16", variant)
+    ref = oracle_for(inp, fus, b)
+    check(sep, ref, TOL_BF16_LAYER)
+    check(fus, ref, TOL_BF16_LAYER)
+    for k in ("y", "dx", "dq_R", "dq_P"):
+        assert O.rel_fro(fus[k], sep[k]) <= 1e-2, k
