@@ -217,3 +217,27 @@ def test_layer_fused_and_separate_products_agree(P, m, n, b, N, variant):
     check(fus, ref, TOL_BF16_LAYER)
     for k in ("y", "dx", "dq_R", "dq_P"):
         assert O.rel_fro(fus[k], sep[k]) <= 1e-2, k
+
+
+def _random_shapes(count, seed=2026):
+    r = np.random.default_rng(seed)
+    out = []
+    while len(out) < count:
+        b = int(r.choice([64, 128, 256, 512]))
+        m = b * int(r.integers(1, 9))
+        n = b * int(r.integers(1, 9))
+        if max(m, n) > 2048:
+            continue
+        N = int(r.integers(1, 1500))
+        out.append((m, n, b, N, str(r.choice(["fast", "mem"]))))
+    return out
+
+
+@pytest.mark.parametrize("m,n,b,N,variant", _random_shapes(12))
+def test_layer_bf16_random_shapes(P, m, n, b, N, variant):
+    """Seeded random layer shapes (block sizes 64-512, widths that may or may not fill a
+    256-wide W' tile, ragged token counts): whichever kernels the shape selects (fused or
+    separate products, tensor-core or CUDA-core contraction) must match the oracle."""
+    inp = inputs.small_layer_inputs(1000 + m + n + N, m, n, b, N, act="bf16", wdt="bf16")
+    got = run_layer(P, inp, b, "bf16", "bf16", variant)
+    check(got, oracle_for(inp, got, b), TOL_BF16_LAYER)
