@@ -195,6 +195,10 @@ def reference_arm(args, rank, world):
 
 
 # ------------------------------------------------------------------ our arm
+def h2d_bytes_of(*ts):
+    return sum(t.numel() * t.element_size() for t in ts)
+
+
 def main():
     args = parse()
     rank = int(os.environ.get("RANK", 0))
@@ -563,46 +567,48 @@ def main():
                  "metric": "N / sum of the layers' fwd+bwd step times"}
 
     check_err("per-layer timing")
-    # end to end through the C ABI with host buffers (pinned), copies inside the timed region
+    # end to end through the C ABI with host buffers (pinned), copies inside the timed region:
+    # one poetx_layer_step_host call per step, which uploads x and dy, runs the forward and
+    # the backward and downloads y, dx, dq_R and dq_P, the copies on its own copy stream
+    # beside the kernels
     hx = x.cpu().pin_memory()
     hdy = dy.cpu().pin_memory()
     hy = torch.empty(N, n, dtype=bf).pin_memory()
     hdx = torch.empty(N, m, dtype=bf).pin_memory()
     hqR = torch.empty(qR.shape).pin_memory()
     hqP = torch.empty(qP.shape).pin_memory()
-    dx_in = torch.empty_like(x)
-    ddy_in = torch.empty_like(dy)
-    e2e_ms = []
-    # the copies that do not feed the next layer call run on a second stream beside the
-    # compute: dy goes up during the forward, y comes down during the backward
-    cs = torch.cuda.Stream(device=dev)
-    main_s = torch.cuda.current_stream()
     B = main_b
+    step_dev = P.workspace(P.poetx_layer_step_host_bytes(B["L"], N), dev)
+    e2e_ms = []
     for i in range(max(3, args.warmup // 4) + 50):
         flush.zero_()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        ev_dy, ev_y = torch.cuda.Event(), torch.cuda.Event()
         e0.record()
-        cs.wait_stream(main_s)
-        dx_in.copy_(hx, non_blocking=True)
-        with torch.cuda.stream(cs):
-            ddy_in.copy_(hdy, non_blocking=True)
-            ev_dy.record(cs)
-        P.poetx_layer_fwd(B["L"], dx_in, B["y"], B["saved"], B["wsf"])
-        ev_y.record(main_s)
-        with torch.cuda.stream(cs):
-            cs.wait_event(ev_y)
-            hy.copy_(B["y"], non_blocking=True)
-        main_s.wait_event(ev_dy)
-        P.poetx_layer_bwd(B["L"], dx_in, ddy_in, B["saved"], B["dx"], B["dqR"], B["dqP"], B["wsb"])
-        hdx.copy_(B["dx"], non_blocking=True)
-        hqR.copy_(B["dqR"], non_blocking=True)
-        hqP.copy_(B["dqP"], non_blocking=True)
-        main_s.wait_stream(cs)
+        P.poetx_layer_step_host(B["L"], hx, hdy, hy, hdx, hqR, hqP, step_dev)
         e1.record()
         torch.cuda.synchronize()
         if i >= max(3, args.warmup // 4):
             e2e_ms.append(e0.elapsed_time(e1))
+    del step_dev
+    # the host link's own rate, for the e2e figure: pinned copies of the step's sizes alone
+    link = {}
+    hbuf = torch.empty(max(h2d_bytes_of(x, dy), 1), dtype=torch.uint8).pin_memory()
+    dbuf = torch.empty(hbuf.numel(), dtype=torch.uint8, device=dev)
+    for kind in ("h2d", "d2h"):
+        ts = []
+        for i in range(13):
+            c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            c0.record()
+            if kind == "h2d":
+                dbuf.copy_(hbuf, non_blocking=True)
+            else:
+                hbuf.copy_(dbuf, non_blocking=True)
+            c1.record()
+            torch.cuda.synchronize()
+            if i >= 3:
+                ts.append(c0.elapsed_time(c1))
+        link[kind + "_gbs"] = hbuf.numel() / (statistics.median(ts) * 1e-3) / 1e9
+    del hbuf, dbuf
     e2e_t = statistics.mean(e2e_ms)
     h2d = (x.numel() + dy.numel()) * esz
     d2h = (N * n + N * m) * esz + (qR.numel() + qP.numel()) * 4
@@ -642,9 +648,15 @@ def main():
             "e2e": {"value": world * N / (e2e_t * 1e-3), "unit": "tokens/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": e2e_t,
-                    "note": "eager C-ABI calls; x up before the forward, dx and dq down after "
-                            "the backward; dy goes up during the forward and y comes down "
-                            "during the backward on a second stream"},
+                    "link": {**{k: round(v, 1) for k, v in link.items()},
+                             "traffic_gbs": (h2d + d2h) / (e2e_t * 1e-3) / 1e9,
+                             "note": "one pinned copy of the step's upload size alone, each "
+                                     "direction; the step moves h2d + d2h bytes"},
+                    "note": "one poetx_layer_step_host call per step (pinned host buffers): "
+                            "x and dy up, forward, backward, y, dx, dq_R and dq_P down; the "
+                            "library's copy stream overlaps the x upload with the CNP "
+                            "forward, dy's with the forward chain, y's download with the "
+                            "backward and dx's with the CNP backward"},
             "gpu_launches": launches, "gpu_launches_per_step": kernels_per_step,
             "clocks": clocks.summary(w0, w1),
         }

@@ -274,6 +274,28 @@ poetx_status poetx_layer_bwd(const poetx_layer* L, const void* x, const void* dy
                              const void* saved, void* dx, float* dq_R, float* dq_P,
                              int accumulate, void* ws, size_t ws_bytes, cudaStream_t stream);
 
+/* One training step of the layer (forward, then backward from dy) with HOST buffers, the
+ * transfers overlapped with the kernels (the input-centric chain, POET-X summary page, "Core
+ * method" sections 1-5, as poetx_layer_fwd + poetx_layer_bwd with accumulate = 0):
+ *   x [N, m], dy [N, n]: host inputs, read by uploads;
+ *   y [N, n], dx [N, m], dq_R [m/b, b(b-1)/2], dq_P [n/b, b(b-1)/2] (fp32): host outputs,
+ *   written by downloads.
+ * Activations are of dtype L->act.  Host buffers should be page-locked (cudaHostAlloc /
+ * cudaHostRegister): from pageable memory the copies are correct but not overlapped, and
+ * under stream capture they fail (POETX_ERR_CUDA).  dev: device scratch of at least
+ * poetx_layer_step_host_bytes(L, N) bytes (16-byte aligned; 0 for an invalid descriptor),
+ * holding the device copies of the six arrays, the forward's saved state and the workspace;
+ * the library allocates nothing.  The uploads and downloads of x, dy, y and dx run on a
+ * copy stream the library creates once per device; the x upload overlaps the CNP forward,
+ * dy's the forward chain, y's download the backward and dx's the CNP backward.  When the
+ * call's work on `stream` completes, every output is in host memory (synchronise `stream`
+ * before reading them).  Calls from several host threads are serialised while they enqueue.
+ * Errors: those of poetx_layer_fwd / poetx_layer_bwd, checked before any transfer. */
+size_t poetx_layer_step_host_bytes(const poetx_layer* L, int N);
+poetx_status poetx_layer_step_host(const poetx_layer* L, const void* x, const void* dy, int N,
+                                   void* y, void* dx, float* dq_R, float* dq_P, void* dev,
+                                   size_t dev_bytes, cudaStream_t stream);
+
 /* Merge-then-reinitialize (POET skill page, Step 4 "Merge-Then-Reinitialize Optimization":
  * the current R W0 P is written back into W0 and the factors are reset to the identity).
  * Writes the weight that, with q_R = q_P = 0, makes the layer compute the map it computes

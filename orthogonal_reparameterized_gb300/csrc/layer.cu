@@ -16,6 +16,7 @@
 // Host-side orchestration only: every step runs in this library's kernels on the caller's
 // stream; nothing is allocated.
 #include <atomic>
+#include <mutex>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -312,9 +313,19 @@ extern "C" size_t poetx_layer_saved_bytes(const poetx_layer* L, int N) {
   return make_plan(L, N).saved_total;
 }
 
-extern "C" poetx_status poetx_layer_fwd(const poetx_layer* L, const void* x, int N, void* y,
-                                        void* saved, void* ws, size_t ws_bytes,
-                                        cudaStream_t stream) {
+// Events a host-buffer step hands to the layer calls (all nullable): the forward waits for
+// x_ready before its first read of x (the CNP runs before that, beside the upload); the
+// backward waits for dy_ready before its first read of dy and records dx_done once dx is
+// complete (the CNP backward then runs beside the download of dx).
+struct StepHooks {
+  cudaEvent_t x_ready = nullptr;
+  cudaEvent_t dy_ready = nullptr;
+  cudaEvent_t dx_done = nullptr;
+};
+
+static poetx_status layer_fwd_impl(const poetx_layer* L, const void* x, int N, void* y,
+                                   void* saved, void* ws, size_t ws_bytes, cudaStream_t stream,
+                                   const StepHooks& hk) {
   POETX_TRY(validate(L));
   if (N < 0) return POETX_ERR_ARG;
   if (!saved || !ws || (N > 0 && (!x || !y))) return POETX_ERR_ARG;
@@ -338,6 +349,7 @@ extern "C" poetx_status poetx_layer_fwd(const poetx_layer* L, const void* x, int
   void* xt = L->variant == POETX_FAST ? at(saved, p.Xsv) : at(ws, p.f_xt);
   void* A = at(ws, p.f_A);
   void* B = L->variant == POETX_FAST ? at(saved, p.Bsv) : at(ws, p.f_B);
+  if (hk.x_ready) POETX_CUDA_TRY(cudaStreamWaitEvent(stream, hk.x_ready, 0));
   POETX_TRY(launch_perm_rows(as, false, x, N, m, L->perm_m, xt, nullptr, nullptr, nullptr, stream));
   POETX_TRY(blockdiag_impl(act, xt, N, m / b, b, at(saved, p.GR), 0, nullptr, nullptr, A, stream));
   void* zt = at(ws, p.f_zt);
@@ -354,10 +366,16 @@ extern "C" poetx_status poetx_layer_fwd(const poetx_layer* L, const void* x, int
   return launch_perm_rows(as, true, zt, N, n, L->perm_n, y, nullptr, nullptr, nullptr, stream);
 }
 
-extern "C" poetx_status poetx_layer_bwd(const poetx_layer* L, const void* x, const void* dy, int N,
-                                        const void* saved, void* dx, float* dq_R, float* dq_P,
-                                        int accumulate, void* ws, size_t ws_bytes,
+extern "C" poetx_status poetx_layer_fwd(const poetx_layer* L, const void* x, int N, void* y,
+                                        void* saved, void* ws, size_t ws_bytes,
                                         cudaStream_t stream) {
+  return layer_fwd_impl(L, x, N, y, saved, ws, ws_bytes, stream, StepHooks{});
+}
+
+static poetx_status layer_bwd_impl(const poetx_layer* L, const void* x, const void* dy, int N,
+                                   const void* saved, void* dx, float* dq_R, float* dq_P,
+                                   int accumulate, void* ws, size_t ws_bytes, cudaStream_t stream,
+                                   const StepHooks& hk) {
   POETX_TRY(validate(L));
   if (N < 0) return POETX_ERR_ARG;
   if (!saved || !ws || !dq_R || !dq_P || (N > 0 && (!x || !dy || !dx))) return POETX_ERR_ARG;
@@ -383,6 +401,7 @@ extern "C" poetx_status poetx_layer_bwd(const poetx_layer* L, const void* x, con
     if (!fast)  // mem: x~ is recomputed
       POETX_TRY(launch_perm_rows(as, false, x, N, m, L->perm_m, at(ws, p.b_xt), nullptr, nullptr,
                                  nullptr, stream));
+    if (hk.dy_ready) POETX_CUDA_TRY(cudaStreamWaitEvent(stream, hk.dy_ready, 0));
     POETX_TRY(launch_perm_rows(as, false, dy, N, n, L->perm_n, dzt, nullptr, nullptr, nullptr, stream));
   }
   const void* B;
@@ -412,12 +431,138 @@ extern "C" poetx_status poetx_layer_bwd(const poetx_layer* L, const void* x, con
   // S13
   if (N > 0)
     POETX_TRY(launch_perm_rows(as, true, dxt, N, m, L->perm_m, dx, nullptr, nullptr, nullptr, stream));
+  if (hk.dx_done) POETX_CUDA_TRY(cudaEventRecord(hk.dx_done, stream));
   const CnpSides sides{{L->q_R, L->q_P}, {m / b, n / b}};
   const float* const dGs[2] = {dGR, dGP};
   const int splits[2] = {p.splitsR, p.splitsP};
   float* const dqs[2] = {dq_R, dq_P};
   return cnp_backward_sides(sides, at<float>(saved, p.Qs), at<float>(saved, p.Q2R), dGs, splits,
                             b, dqs, accumulate, at(ws, p.b_cnp), stream);
+}
+
+extern "C" poetx_status poetx_layer_bwd(const poetx_layer* L, const void* x, const void* dy, int N,
+                                        const void* saved, void* dx, float* dq_R, float* dq_P,
+                                        int accumulate, void* ws, size_t ws_bytes,
+                                        cudaStream_t stream) {
+  return layer_bwd_impl(L, x, dy, N, saved, dx, dq_R, dq_P, accumulate, ws, ws_bytes, stream,
+                        StepHooks{});
+}
+
+// ---------------------------------------------------------------- host-buffer step
+// One forward + backward with the caller's host buffers: the uploads and downloads run on a
+// copy stream of the library's own, beside the kernels on the caller's stream:
+//   copy stream   x up | dy up |           | y down (after the forward) | dx down |
+//   caller stream CNP fwd | (wait x) fwd chain | (wait dy) bwd chain | CNP bwd | dq down
+// so the CNP forward hides part of the x upload, the dy upload runs under the forward, the
+// y download under the backward and the dx download under the CNP backward.
+struct StepPlan {
+  size_t x, dy, y, dx, dqR, dqP, saved, ws, ws_bytes, total;
+};
+
+static StepPlan step_plan(const poetx_layer* L, long long N) {
+  StepPlan sp{};
+  const Plan p = make_plan(L, N);
+  const size_t as = dtype_size(L->act);
+  const size_t m = L->m, n = L->n, b = L->b;
+  size_t o = 0;
+  auto take = [&](size_t bytes) { size_t r = o; o += align_up(bytes, 256); return r; };
+  sp.x = take(N * m * as);
+  sp.dy = take(N * n * as);
+  sp.y = take(N * n * as);
+  sp.dx = take(N * m * as);
+  sp.dqR = take(m / b * (b * (b - 1) / 2) * 4);
+  sp.dqP = take(n / b * (b * (b - 1) / 2) * 4);
+  sp.saved = take(p.saved_total);
+  sp.ws_bytes = p.fwd_total > p.bwd_total ? p.fwd_total : p.bwd_total;
+  sp.ws = take(sp.ws_bytes);
+  sp.total = o;
+  return sp;
+}
+
+namespace {
+enum { EV_START, EV_X, EV_DY, EV_Y, EV_DX, EV_DONE, EV_COUNT };
+struct CopyCtx {
+  bool ready = false;
+  cudaStream_t cs = nullptr;
+  cudaEvent_t ev[EV_COUNT] = {};
+};
+std::mutex g_step_mu;  // the events are reused: one step is enqueued at a time
+CopyCtx g_copy[64];    // per device
+}  // namespace
+
+extern "C" size_t poetx_layer_step_host_bytes(const poetx_layer* L, int N) {
+  if (validate(L) != POETX_OK || N < 0) return 0;
+  return step_plan(L, N).total;
+}
+
+extern "C" poetx_status poetx_layer_step_host(const poetx_layer* L, const void* x, const void* dy,
+                                              int N, void* y, void* dx, float* dq_R, float* dq_P,
+                                              void* dev, size_t dev_bytes, cudaStream_t stream) {
+  POETX_TRY(validate(L));
+  if (N < 0) return POETX_ERR_ARG;
+  if (!dev || !dq_R || !dq_P || (N > 0 && (!x || !dy || !y || !dx))) return POETX_ERR_ARG;
+  if (!aligned16(dev)) return POETX_ERR_ALIGN;
+  const StepPlan sp = step_plan(L, N);
+  if (dev_bytes < sp.total) return POETX_ERR_WORKSPACE;
+  int d = 0;
+  POETX_CUDA_TRY(cudaGetDevice(&d));
+  if (d < 0 || d >= 64) return POETX_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lk(g_step_mu);
+  CopyCtx& c = g_copy[d];
+  if (!c.ready) {
+    POETX_CUDA_TRY(cudaStreamCreateWithFlags(&c.cs, cudaStreamNonBlocking));
+    for (int i = 0; i < EV_COUNT; ++i)
+      POETX_CUDA_TRY(cudaEventCreateWithFlags(&c.ev[i], cudaEventDisableTiming));
+    c.ready = true;
+  }
+  uint8_t* base = static_cast<uint8_t*>(dev);
+  const size_t as = dtype_size(L->act);
+  const size_t m = L->m, n = L->n, b = L->b;
+  const size_t xb = (size_t)N * m * as, yb = (size_t)N * n * as;
+  const size_t qRb = m / b * (b * (b - 1) / 2) * 4, qPb = n / b * (b * (b - 1) / 2) * 4;
+  // the copy stream starts after the caller's earlier work (which may still use `dev`)
+  POETX_CUDA_TRY(cudaEventRecord(c.ev[EV_START], stream));
+  POETX_CUDA_TRY(cudaStreamWaitEvent(c.cs, c.ev[EV_START], 0));
+  StepHooks fh, bh;
+  poetx_status st = POETX_OK;
+  auto cuda = [&](cudaError_t e) {
+    if (st == POETX_OK && e != cudaSuccess) st = POETX_ERR_CUDA;
+  };
+  if (N > 0) {
+    cuda(cudaMemcpyAsync(base + sp.x, x, xb, cudaMemcpyHostToDevice, c.cs));
+    cuda(cudaEventRecord(c.ev[EV_X], c.cs));
+    cuda(cudaMemcpyAsync(base + sp.dy, dy, yb, cudaMemcpyHostToDevice, c.cs));
+    cuda(cudaEventRecord(c.ev[EV_DY], c.cs));
+    fh.x_ready = c.ev[EV_X];
+    bh.dy_ready = c.ev[EV_DY];
+    bh.dx_done = c.ev[EV_DX];
+  }
+  if (st == POETX_OK)
+    st = layer_fwd_impl(L, base + sp.x, N, base + sp.y, base + sp.saved, base + sp.ws,
+                        sp.ws_bytes, stream, fh);
+  if (st == POETX_OK && N > 0) {
+    cuda(cudaEventRecord(c.ev[EV_Y], stream));
+    cuda(cudaStreamWaitEvent(c.cs, c.ev[EV_Y], 0));
+    cuda(cudaMemcpyAsync(y, base + sp.y, yb, cudaMemcpyDeviceToHost, c.cs));
+  }
+  if (st == POETX_OK)
+    st = layer_bwd_impl(L, base + sp.x, base + sp.dy, N, base + sp.saved, base + sp.dx,
+                        reinterpret_cast<float*>(base + sp.dqR),
+                        reinterpret_cast<float*>(base + sp.dqP), 0, base + sp.ws, sp.ws_bytes,
+                        stream, bh);
+  if (st == POETX_OK && N > 0) {
+    cuda(cudaStreamWaitEvent(c.cs, c.ev[EV_DX], 0));
+    cuda(cudaMemcpyAsync(dx, base + sp.dx, xb, cudaMemcpyDeviceToHost, c.cs));
+  }
+  if (st == POETX_OK) {
+    cuda(cudaMemcpyAsync(dq_R, base + sp.dqR, qRb, cudaMemcpyDeviceToHost, stream));
+    cuda(cudaMemcpyAsync(dq_P, base + sp.dqP, qPb, cudaMemcpyDeviceToHost, stream));
+  }
+  // the caller's stream is done with the step only when the copy stream is
+  const cudaError_t e1 = cudaEventRecord(c.ev[EV_DONE], c.cs);
+  const cudaError_t e2 = e1 == cudaSuccess ? cudaStreamWaitEvent(stream, c.ev[EV_DONE], 0) : e1;
+  cuda(e2);
+  return st;
 }
 
 // ---------------------------------------------------------------- step entry points

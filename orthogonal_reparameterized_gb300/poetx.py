@@ -73,6 +73,9 @@ _SIGS = {
     "poetx_layer_fwd": (_i, [ctypes.POINTER(LayerDesc), _vp, _i, _vp, _vp, _vp, _sz, _vp]),
     "poetx_layer_bwd": (_i, [ctypes.POINTER(LayerDesc), _vp, _vp, _i, _vp, _vp, _vp, _vp, _i,
                              _vp, _sz, _vp]),
+    "poetx_layer_step_host_bytes": (_sz, [ctypes.POINTER(LayerDesc), _i]),
+    "poetx_layer_step_host": (_i, [ctypes.POINTER(LayerDesc), _vp, _vp, _i, _vp, _vp, _vp, _vp,
+                                   _vp, _sz, _vp]),
     "poetx_merge_reinit_workspace_bytes": (_sz, [ctypes.POINTER(LayerDesc)]),
     "poetx_merge_reinit": (_i, [ctypes.POINTER(LayerDesc), _vp, _vp, _sz, _vp]),
     "poetx_adam_triu": (_i, [_vp, _vp, _vp, _vp, ctypes.c_longlong, ctypes.POINTER(AdamDesc),
@@ -293,6 +296,24 @@ def poetx_layer_bwd(L: LayerDesc, x, dy, saved, dx, dq_R, dq_P, ws, accumulate=F
                                                     _p(dx), _p(dq_R), _p(dq_P),
                                                     int(bool(accumulate)), _p(ws), ws.numel(),
                                                     _stream(stream)))
+
+
+def poetx_layer_step_host_bytes(L: LayerDesc, N: int) -> int:
+    return lib().poetx_layer_step_host_bytes(ctypes.byref(L), N)
+
+
+def poetx_layer_step_host(L: LayerDesc, x, dy, y, dx, dq_R, dq_P, dev, stream=None):
+    """Forward + backward with host (CPU, preferably pinned) tensors x, dy in and y, dx,
+    dq_R, dq_P out; dev: device scratch of poetx_layer_step_host_bytes(L, N) bytes.  The
+    outputs are valid once `stream` has been synchronised."""
+    for t in (x, dy, y, dx, dq_R, dq_P):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError("poetx_layer_step_host takes contiguous host tensors")
+    N = x.shape[0]
+    h = lambda t: ctypes.c_void_p(t.data_ptr())
+    _check("poetx_layer_step_host", lib().poetx_layer_step_host(
+        ctypes.byref(L), h(x), h(dy), N, h(y), h(dx), h(dq_R), h(dq_P), _p(dev),
+        dev.numel() * dev.element_size(), _stream(stream)))
 
 
 def poetx_merge_reinit_workspace_bytes(L: LayerDesc) -> int:

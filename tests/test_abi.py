@@ -142,3 +142,29 @@ def test_argument_errors_before_launch(P):
     assert lib.poetx_set_gemm_engine(5) == 1
     assert lib.poetx_cnp_workspace_bytes(4, 64, 0) == 2 * 4 * 64 * 64 * 4
     assert lib.poetx_cnp_workspace_bytes(4, 1, 0) == 0
+
+
+def test_step_host_sizes_and_argument_errors(P):
+    """The host-buffer step: its device scratch covers the six device arrays, the saved state
+    and the larger of the two workspaces; bad arguments are refused before any CUDA call."""
+    L = _desc(P)
+    N = 1000
+    need = P.poetx_layer_step_host_bytes(L, N)
+    arrays = 2 * N * (256 + 512) * 2 + (256 // 64 + 512 // 64) * (64 * 63 // 2) * 4
+    ws = max(P.poetx_layer_workspace_bytes(L, N, 0), P.poetx_layer_workspace_bytes(L, N, 1))
+    assert need >= arrays + P.poetx_layer_saved_bytes(L, N) + ws
+    assert P.poetx_layer_step_host_bytes(_desc(P, b=100), N) == 0
+    assert P.poetx_layer_step_host_bytes(L, -1) == 0
+    lib = P.lib()
+    fake = ctypes.c_void_p(4096)
+    args = [fake] * 6
+    assert lib.poetx_layer_step_host(ctypes.byref(L), *args[:2], 4, *args[2:], fake, 16,
+                                     None) == 5
+    assert lib.poetx_layer_step_host(ctypes.byref(L), *args[:2], 4, *args[2:],
+                                     ctypes.c_void_p(4100), 1 << 40, None) == 4
+    assert lib.poetx_layer_step_host(ctypes.byref(L), None, fake, 4, *args[2:], fake, 1 << 40,
+                                     None) == 1
+    assert lib.poetx_layer_step_host(ctypes.byref(_desc(P, order=2)), *args[:2], 4, *args[2:],
+                                     fake, 1 << 40, None) == 6
+    assert lib.poetx_layer_step_host(ctypes.byref(L), *args[:2], -1, *args[2:], fake, 1 << 40,
+                                     None) == 1

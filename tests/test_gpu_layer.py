@@ -241,3 +241,77 @@ def test_layer_bf16_random_shapes(P, m, n, b, N, variant):
     inp = inputs.small_layer_inputs(1000 + m + n + N, m, n, b, N, act="bf16", wdt="bf16")
     got = run_layer(P, inp, b, "bf16", "bf16", variant)
     check(got, oracle_for(inp, got, b), TOL_BF16_LAYER)
+
+
+def _step_host(P, inp, b, act, wdt, variant, pinned=True):
+    """poetx_layer_step_host with host tensors; the layer descriptor is built as run_layer
+    builds it (same weights, permutations and q)."""
+    m, n = inp["W0"].shape[1], inp["W0"].shape[0]
+    adt = TDT[act]
+    pm = dev(inp["perm_m"], torch.int32)
+    pn = dev(inp["perm_n"], torch.int32)
+    qR = dev(inp["q_R"], torch.float32)
+    qP = dev(inp["q_P"], torch.float32)
+    w_scale = None
+    if wdt == "i8":
+        Wq = torch.empty(n, m, dtype=torch.int8, device=DEV)
+        s = torch.empty(n, device=DEV)
+        P.poetx_quantize_rows_int8(dev(inp["W0"], torch.float32), Wq, s)
+        Wp = torch.empty_like(Wq)
+        w_scale = torch.empty_like(s)
+        P.poetx_merge_perm(Wq, pn, pm, Wp, s, w_scale)
+        wcode = P.I8
+    else:
+        W0 = dev(inp["W0"], TDT[wdt])
+        Wp = torch.empty_like(W0)
+        P.poetx_merge_perm(W0, pn, pm, Wp)
+        wcode = P.F32 if wdt == "f32" else P.BF16
+    acode = P.F32 if act == "f32" else P.BF16
+    L = P.make_layer(m, n, b, acode, wcode, P.FAST if variant == "fast" else P.MEM, pm, pn, Wp,
+                     qR, qP, w_scale)
+    N = inp["x"].shape[0]
+    pin = (lambda t: t.pin_memory()) if pinned else (lambda t: t)
+    hx = pin(torch.tensor(np.asarray(inp["x"]), dtype=adt))    # the same rounding as dev()
+    hdy = pin(torch.tensor(np.asarray(inp["dy"]), dtype=adt))
+    hy = pin(torch.full((N, n), float("nan"), dtype=adt))
+    hdx = pin(torch.full((N, m), float("nan"), dtype=adt))
+    hqR = pin(torch.full(tuple(qR.shape), float("nan")))
+    hqP = pin(torch.full(tuple(qP.shape), float("nan")))
+    devbuf = P.workspace(P.poetx_layer_step_host_bytes(L, N), DEV)
+    s = torch.cuda.current_stream()
+    P.poetx_layer_step_host(L, hx, hdy, hy, hdx, hqR, hqP, devbuf)
+    s.synchronize()
+    assert P.poetx_get_device_error() == 0
+    f = lambda t: t.float().numpy().astype(np.float64)
+    return {"y": f(hy), "dx": f(hdx), "dq_R": f(hqR), "dq_P": f(hqP)}
+
+
+@pytest.mark.parametrize("act,wdt,variant,shape", [
+    ("bf16", "bf16", "fast", (2048, 2048, 256, 1000)),
+    ("bf16", "bf16", "mem", (512, 1024, 128, 333)),
+    ("bf16", "i8", "mem", (512, 768, 256, 150)),
+    ("f32", "f32", "fast", (256, 256, 32, 64)),
+])
+def test_step_host_equals_device_calls(P, act, wdt, variant, shape):
+    """The host-buffer step runs the same kernels as poetx_layer_fwd + poetx_layer_bwd on
+    device buffers: bit-identical outputs, and within the layer tolerance of the oracle."""
+    m, n, b, N = shape
+    inp = inputs.small_layer_inputs(61 + b, m, n, b, N, act=act, wdt=wdt)
+    got = _step_host(P, inp, b, act, wdt, variant)
+    ref_dev = run_layer(P, inp, b, act, wdt, variant)
+    for k in ("y", "dx", "dq_R", "dq_P"):
+        np.testing.assert_array_equal(got[k], ref_dev[k], err_msg=k)
+    got["W_eff"] = ref_dev["W_eff"]
+    check(got, oracle_for(inp, got, b), TOL_F32 if act == "f32" else TOL_BF16_LAYER)
+
+
+def test_step_host_pageable_and_repeated(P):
+    """Pageable host buffers give the same result (without overlap), and repeated calls
+    reuse the copy stream and events."""
+    inp = inputs.small_layer_inputs(71, 512, 512, 128, 200, act="bf16", wdt="bf16")
+    a = _step_host(P, inp, 128, "bf16", "bf16", "fast", pinned=True)
+    b2 = _step_host(P, inp, 128, "bf16", "bf16", "fast", pinned=False)
+    c = _step_host(P, inp, 128, "bf16", "bf16", "fast", pinned=True)
+    for k in ("y", "dx", "dq_R", "dq_P"):
+        np.testing.assert_array_equal(a[k], b2[k], err_msg=k)
+        np.testing.assert_array_equal(a[k], c[k], err_msg=k)
