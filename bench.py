@@ -40,6 +40,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--fusion", default="on", choices=["on", "off"],
                     help="W' contraction + following block product in one kernel (default on)")
+    ap.add_argument("--overlap", default="on", choices=["on", "off"],
+                    help="dx scatter on a side stream beside the CNP backward (library switch)")
     ap.add_argument("--all-layers", action="store_true",
                     help="also time every layer of a multi-layer workload (the Llama-8B "
                          "block's 7 linears, the 13B MLP's up and down) and report their sum")
@@ -221,6 +223,7 @@ def main():
         dist.init_process_group("nccl", device_id=dev)
     P.lib()
     P.poetx_set_fusion(args.fusion == "on")
+    P.poetx_set_overlap(args.overlap == "on")
 
     def check_err(section):
         """Fail loudly, naming the section, if a kernel recorded an error (a bounded wait
@@ -634,6 +637,7 @@ def main():
                                      "distributions of the workload)",
             "config": {"workload": wl.name, "m": m, "n": n, "b": b, "tokens_per_gpu": N,
                        "variant": variant, "wdt": wl.wdt, "fusion": args.fusion == "on",
+                       "overlap": args.overlap == "on",
                        "parallelism": f"replicas x{world} (token-sharded, no collective)",
                        "l2": "flushed between timed steps (512 MiB memset outside the events)"},
             "variants": {variant: {"tokens_per_s": N / (ms_step * 1e-3), "ms_per_step": ms_step,

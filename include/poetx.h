@@ -89,6 +89,15 @@ poetx_status poetx_set_gemm_engine(int engine);
  * the order of fp32 accumulation.  Process-wide. */
 poetx_status poetx_set_fusion(int on);
 
+/* Overlap switch (default 1): poetx_layer_bwd runs the dx scatter beside the G_R weight
+ * gradient and the CNP backward, on a side stream of the library's own (created once per
+ * device) forked from and joined back into the caller's stream, the permutation in a
+ * one-CTA-per-SM shape small enough to share SMs with the CNP products.  Results are
+ * bit-identical either way; 0 runs every kernel on the caller's stream, and so do
+ * per-stage profiling (poetx_profile_enable) and poetx_layer_step_host (whose download of
+ * dx waits for the scatter).  POETX_ERR_ARG unless on is 0 or 1. */
+poetx_status poetx_set_overlap(int on);
+
 /* Number of kernels this library has launched in the process so far (host counter). */
 unsigned long long poetx_launch_count(void);
 

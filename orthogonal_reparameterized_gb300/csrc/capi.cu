@@ -81,6 +81,8 @@ void after_launch(cudaStream_t s, int stage) {
   if (g_prof_on.load(std::memory_order_relaxed)) prof_record(s, stage);
 }
 
+bool prof_enabled() { return g_prof_on.load(std::memory_order_relaxed); }
+
 void prof_begin(cudaStream_t s) {
   if (g_prof_on.load(std::memory_order_relaxed)) prof_record(s, -1);
 }

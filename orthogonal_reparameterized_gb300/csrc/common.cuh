@@ -99,6 +99,8 @@ enum Stage : int {
 void after_launch(cudaStream_t s, int stage);
 // Records the reference event that the first stage of a call is timed from.
 void prof_begin(cudaStream_t s);
+// Whether per-stage profiling is on (its stage events assume one stream per layer call).
+bool prof_enabled();
 // Diagnostic trace buffer (device, nullable): the tensor-core kernels record %globaltimer
 // stamps of their phases into it, kTraceSlots 64-bit slots per CTA.
 unsigned long long* trace_buffer(size_t* slots);

@@ -382,33 +382,63 @@ static bool perm_shape(size_t row_bytes, size_t idx_bytes, int* G, int* S, size_
   return true;
 }
 
+// Co-resident shape: one CTA per SM in the shared memory that a 64-wide CNP product CTA
+// leaves free (of an SM's 228 KB: the product's 214,272 bytes, and 1 KB reserved for each of
+// the two CTAs), so that the permutation runs beside the CNP products instead of after them.
+// All consumer warps form one group; at least two rows in flight.
+constexpr size_t kPermSideSmem = 233472 - 214272 - 2 * 1024;
+static bool perm_shape_side(size_t row_bytes, size_t idx_bytes, int* G, int* S, size_t* smem) {
+  if (idx_bytes + 2 * (row_bytes + 16) > kPermSideSmem) return false;
+  int s = (int)((kPermSideSmem - idx_bytes) / (row_bytes + 16));
+  s = s > 8 ? 8 : s;
+  *G = kPermWarps;
+  *S = s;
+  *smem = idx_bytes + s * (row_bytes + 16);
+  return true;
+}
+
 template <int E, bool SCATTER, typename IdxT>
 static poetx_status launch_perm_rows_t(const void* X, long long N, int D, const int32_t* perm,
                                        void* Y, const int32_t* src_rows, const float* scale,
-                                       float* scale_out, cudaStream_t s) {
+                                       float* scale_out, bool side, cudaStream_t s) {
   const size_t row_bytes = (size_t)D * E;
   const size_t idx_bytes = ((size_t)D * sizeof(IdxT) + 127) & ~(size_t)127;
   int G = 0, S = 0;
   size_t smem = 0;
-  if (!perm_shape(row_bytes, idx_bytes, &G, &S, &smem)) return POETX_ERR_SHAPE;
+  if (!(side ? perm_shape_side : perm_shape)(row_bytes, idx_bytes, &G, &S, &smem))
+    return POETX_ERR_SHAPE;
   auto k = perm_rows_kernel<E, SCATTER, IdxT>;
   static std::once_flag once;  // the opt-in limit is set once, to the largest size used
   static cudaError_t attr = cudaSuccess;
   std::call_once(once, [&] {
     attr = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    // all of the unified L1 as shared memory, as the CNP products take it, so that a
+    // co-resident CTA never holds an SM in a smaller split
+    if (attr == cudaSuccess)
+      attr = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                  (int)cudaSharedmemCarveoutMaxShared);
   });
   POETX_CUDA_TRY(attr);
   const int ngrp = kPermWarps / G;
   size_t tr_cap = 0;
   unsigned long long* tr = trace_buffer(&tr_cap);
-  const int per_sm = smem <= 110 * 1024 ? 2 : 1;
+  const int per_sm = side ? 1 : (smem <= 110 * 1024 ? 2 : 1);
   const long long want = (long long)sm_count() * per_sm;
   const long long need = (N + ngrp - 1) / ngrp;
   const int grid = (int)(need < want ? need : want);
-  POETX_CUDA_TRY(launch_pdl(k, dim3(grid), dim3((kPermWarps + 1) * 32), smem, s,
-                            static_cast<const uint8_t*>(X), N, D, perm, static_cast<uint8_t*>(Y),
-                            src_rows, scale, scale_out, G, S, device_error_word(), kWaitLimitNs,
-                            tr, tr_cap));
+  if (side) {
+    // no early launch: waiting CTAs would hold shared memory on every SM while the kernels
+    // of the other stream still need it
+    k<<<grid, (kPermWarps + 1) * 32, smem, s>>>(static_cast<const uint8_t*>(X), N, D, perm,
+                                                static_cast<uint8_t*>(Y), src_rows, scale,
+                                                scale_out, G, S, device_error_word(),
+                                                kWaitLimitNs, tr, tr_cap);
+  } else {
+    POETX_CUDA_TRY(launch_pdl(k, dim3(grid), dim3((kPermWarps + 1) * 32), smem, s,
+                              static_cast<const uint8_t*>(X), N, D, perm,
+                              static_cast<uint8_t*>(Y), src_rows, scale, scale_out, G, S,
+                              device_error_word(), kWaitLimitNs, tr, tr_cap));
+  }
   POETX_CUDA_TRY(cudaGetLastError());
   after_launch(s, src_rows ? ST_MERGE : (SCATTER ? ST_PERM_SCATTER : ST_PERM_GATHER));
   return POETX_OK;
@@ -417,24 +447,44 @@ static poetx_status launch_perm_rows_t(const void* X, long long N, int D, const 
 template <int E>
 static poetx_status launch_perm_rows_e(bool scatter, const void* X, long long N, int D,
                                        const int32_t* perm, void* Y, const int32_t* src_rows,
-                                       const float* scale, float* scale_out, cudaStream_t s) {
+                                       const float* scale, float* scale_out, bool side,
+                                       cudaStream_t s) {
   if (D <= 65535) {
-    return scatter ? launch_perm_rows_t<E, true, uint16_t>(X, N, D, perm, Y, src_rows, scale, scale_out, s)
-                   : launch_perm_rows_t<E, false, uint16_t>(X, N, D, perm, Y, src_rows, scale, scale_out, s);
+    return scatter ? launch_perm_rows_t<E, true, uint16_t>(X, N, D, perm, Y, src_rows, scale, scale_out, side, s)
+                   : launch_perm_rows_t<E, false, uint16_t>(X, N, D, perm, Y, src_rows, scale, scale_out, side, s);
   }
-  return scatter ? launch_perm_rows_t<E, true, uint32_t>(X, N, D, perm, Y, src_rows, scale, scale_out, s)
-                 : launch_perm_rows_t<E, false, uint32_t>(X, N, D, perm, Y, src_rows, scale, scale_out, s);
+  return scatter ? launch_perm_rows_t<E, true, uint32_t>(X, N, D, perm, Y, src_rows, scale, scale_out, side, s)
+                 : launch_perm_rows_t<E, false, uint32_t>(X, N, D, perm, Y, src_rows, scale, scale_out, side, s);
+}
+
+static poetx_status perm_rows_any(size_t esize, bool scatter, const void* X, long long N, int D,
+                                  const int32_t* perm, void* Y, const int32_t* src_rows,
+                                  const float* scale, float* scale_out, bool side,
+                                  cudaStream_t s) {
+  if (N == 0 || D == 0) return POETX_OK;
+  if (((size_t)D * esize) % 16 != 0) return POETX_ERR_SHAPE;
+  if (esize == 1) return launch_perm_rows_e<1>(scatter, X, N, D, perm, Y, src_rows, scale, scale_out, side, s);
+  if (esize == 2) return launch_perm_rows_e<2>(scatter, X, N, D, perm, Y, src_rows, scale, scale_out, side, s);
+  if (esize == 4) return launch_perm_rows_e<4>(scatter, X, N, D, perm, Y, src_rows, scale, scale_out, side, s);
+  return POETX_ERR_DTYPE;
 }
 
 poetx_status launch_perm_rows(size_t esize, bool scatter, const void* X, long long N, int D,
                               const int32_t* perm, void* Y, const int32_t* src_rows,
                               const float* scale, float* scale_out, cudaStream_t s) {
-  if (N == 0 || D == 0) return POETX_OK;
-  if (((size_t)D * esize) % 16 != 0) return POETX_ERR_SHAPE;
-  if (esize == 1) return launch_perm_rows_e<1>(scatter, X, N, D, perm, Y, src_rows, scale, scale_out, s);
-  if (esize == 2) return launch_perm_rows_e<2>(scatter, X, N, D, perm, Y, src_rows, scale, scale_out, s);
-  if (esize == 4) return launch_perm_rows_e<4>(scatter, X, N, D, perm, Y, src_rows, scale, scale_out, s);
-  return POETX_ERR_DTYPE;
+  return perm_rows_any(esize, scatter, X, N, D, perm, Y, src_rows, scale, scale_out, false, s);
+}
+
+bool perm_side_fits(size_t esize, int D) {
+  const size_t idx = ((size_t)D * (D <= 65535 ? 2 : 4) + 127) & ~(size_t)127;
+  int G = 0, S = 0;
+  size_t smem = 0;
+  return ((size_t)D * esize) % 16 == 0 && perm_shape_side((size_t)D * esize, idx, &G, &S, &smem);
+}
+
+poetx_status launch_perm_rows_side(size_t esize, bool scatter, const void* X, long long N, int D,
+                                   const int32_t* perm, void* Y, cudaStream_t s) {
+  return perm_rows_any(esize, scatter, X, N, D, perm, Y, nullptr, nullptr, nullptr, true, s);
 }
 
 // ---------------------------------------------------------------- int8 quantiser

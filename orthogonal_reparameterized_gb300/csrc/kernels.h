@@ -21,6 +21,11 @@ poetx_status launch_triu_grad_pack(const float* Qbar, int nblk, int b, float* dq
 poetx_status launch_perm_rows(size_t esize, bool scatter, const void* X, long long N, int D,
                               const int32_t* perm, void* Y, const int32_t* src_rows,
                               const float* scale, float* scale_out, cudaStream_t s);
+// The same permutation in the co-resident shape (one small CTA per SM, beside a CNP
+// product); perm_side_fits says whether rows of D elements fit that shape.
+bool perm_side_fits(size_t esize, int D);
+poetx_status launch_perm_rows_side(size_t esize, bool scatter, const void* X, long long N, int D,
+                                   const int32_t* perm, void* Y, cudaStream_t s);
 poetx_status launch_quantize(const float* W, int n, int m, int8_t* Wq, float* scale,
                              cudaStream_t s);
 // inv_a[perm_a[i]] = i (i < na) and inv_b[perm_b[k]] = k (k < nb), one launch.

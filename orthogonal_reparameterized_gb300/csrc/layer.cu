@@ -25,6 +25,7 @@ namespace poetx {
 
 static std::atomic<int> g_engine{0};  // 0: tensor cores where supported, 1: CUDA cores only
 static std::atomic<int> g_fuse{1};    // W' contraction + following block product in one kernel
+static std::atomic<int> g_overlap{1};  // dx scatter beside the CNP backward (side stream)
 
 static bool use_umma() { return g_engine.load() == 0 && umma_supported(); }
 
@@ -313,6 +314,43 @@ extern "C" size_t poetx_layer_saved_bytes(const poetx_layer* L, int N) {
   return make_plan(L, N).saved_total;
 }
 
+// Side stream of the overlapped permutation: the dx scatter runs beside the CNP backward,
+// in the co-resident shape (one small CTA per SM in the shared
+// memory the CNP product CTAs leave), forked from and joined back into the caller's stream
+// by events.
+namespace {
+struct SideCtx {
+  bool ready = false, failed = false;
+  cudaStream_t ss = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+std::mutex g_side_mu;  // the events are reused: one layer call is enqueued at a time
+SideCtx g_side[64];    // per device
+}  // namespace
+
+// The device's side context, created on first use; nullptr when overlap is off or the
+// stream and events cannot be made (the calls then run everything on the caller's stream).
+static SideCtx* side_ctx() {
+  if (!g_overlap.load() || prof_enabled()) return nullptr;  // stage events need one stream
+  int d = 0;
+  if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= 64) return nullptr;
+  SideCtx& c = g_side[d];
+  if (!c.ready && !c.failed) {
+    c.failed = cudaStreamCreateWithFlags(&c.ss, cudaStreamNonBlocking) != cudaSuccess ||
+               cudaEventCreateWithFlags(&c.fork, cudaEventDisableTiming) != cudaSuccess ||
+               cudaEventCreateWithFlags(&c.join, cudaEventDisableTiming) != cudaSuccess;
+    if (c.failed) cudaGetLastError();
+    c.ready = !c.failed;
+  }
+  return c.ready ? &c : nullptr;
+}
+
+extern "C" poetx_status poetx_set_overlap(int on) {
+  if (on != 0 && on != 1) return POETX_ERR_ARG;
+  g_overlap.store(on);
+  return POETX_OK;
+}
+
 // Events a host-buffer step hands to the layer calls (all nullable): the forward waits for
 // x_ready before its first read of x (the CNP runs before that, beside the upload); the
 // backward waits for dy_ready before its first read of dy and records dx_done once dx is
@@ -338,17 +376,19 @@ static poetx_status layer_fwd_impl(const poetx_layer* L, const void* x, int N, v
   const bool f32 = act == POETX_F32;
   const size_t as = dtype_size(act);
   prof_begin(stream);
+  // fast keeps x~ and B for the backward (what default autograd keeps), mem keeps neither
+  void* xt = L->variant == POETX_FAST ? at(saved, p.Xsv) : at(ws, p.f_xt);
+  void* A = at(ws, p.f_A);
+  void* B = L->variant == POETX_FAST ? at(saved, p.Bsv) : at(ws, p.f_B);
   // S1-S2: both CNPs in one pass over the m/b + n/b blocks; G in the activation precision
-  // and Q^2 kept for the backward
+  // and Q^2 kept for the backward.  (Running the x gather beside them on the side stream
+  // was measured: the CNP kernels slowed by about what the gather saved, and the join cost
+  // the programmatic overlap of the next launch; so S3 follows them.)
   const CnpSides sides{{L->q_R, L->q_P}, {m / b, n / b}};
   POETX_TRY(cnp_forward_sides(sides, b, at<float>(saved, p.Qs), at<float>(saved, p.Q2R),
                               f32 ? at<float>(saved, p.GR) : nullptr,
                               f32 ? nullptr : at(saved, p.GR), nullptr, stream));
   if (N == 0) return POETX_OK;
-  // fast keeps x~ and B for the backward (what default autograd keeps), mem keeps neither
-  void* xt = L->variant == POETX_FAST ? at(saved, p.Xsv) : at(ws, p.f_xt);
-  void* A = at(ws, p.f_A);
-  void* B = L->variant == POETX_FAST ? at(saved, p.Bsv) : at(ws, p.f_B);
   if (hk.x_ready) POETX_CUDA_TRY(cudaStreamWaitEvent(stream, hk.x_ready, 0));
   POETX_TRY(launch_perm_rows(as, false, x, N, m, L->perm_m, xt, nullptr, nullptr, nullptr, stream));
   POETX_TRY(blockdiag_impl(act, xt, N, m / b, b, at(saved, p.GR), 0, nullptr, nullptr, A, stream));
@@ -422,22 +462,44 @@ static poetx_status layer_bwd_impl(const poetx_layer* L, const void* x, const vo
   if (fused_ok(L, N, 1)) {
     // S11 + the dx~ half of S12 on the same tiles
     POETX_TRY(umma_wprime_fused(dB, N, m, n, L->Wp, 1, GR, b, dA, dxt, stream));
-    POETX_TRY(wgrad_impl(act, xt, dA, N, m / b, b, p.splitsR, dGR, stream));
   } else {
     POETX_TRY(wprime_impl(act, L->wdt, dB, N, m, n, L->Wp, L->w_scale, 1, dA, stream));
-    POETX_TRY(wgrad_impl(act, xt, dA, N, m / b, b, p.splitsR, dGR, stream));
     POETX_TRY(blockdiag_impl(act, dA, N, m / b, b, GR, 1, nullptr, nullptr, dxt, stream));
   }
-  // S13
-  if (N > 0)
-    POETX_TRY(launch_perm_rows(as, true, dxt, N, m, L->perm_m, dx, nullptr, nullptr, nullptr, stream));
-  if (hk.dx_done) POETX_CUDA_TRY(cudaEventRecord(hk.dx_done, stream));
-  const CnpSides sides{{L->q_R, L->q_P}, {m / b, n / b}};
-  const float* const dGs[2] = {dGR, dGP};
-  const int splits[2] = {p.splitsR, p.splitsP};
-  float* const dqs[2] = {dq_R, dq_P};
-  return cnp_backward_sides(sides, at<float>(saved, p.Qs), at<float>(saved, p.Q2R), dGs, splits,
+  poetx_status st = wgrad_impl(act, xt, dA, N, m / b, b, p.splitsR, dGR, stream);
+  // S13 beside S14 when it can: the dx scatter does not feed the CNP backward.  It is
+  // forked after the G_R weight gradient (a whole-GPU kernel that it would slow down), and
+  // not when a download waits for dx (dx_done): the co-resident scatter is slower than the
+  // whole-GPU one, and dx is then needed as early as possible.
+  std::unique_lock<std::mutex> lk(g_side_mu, std::defer_lock);
+  SideCtx* sc = nullptr;
+  if (st == POETX_OK && N > 0 && !hk.dx_done && perm_side_fits(as, m)) {
+    lk.lock();
+    sc = side_ctx();
+    if (!sc) lk.unlock();
+  }
+  if (sc) {
+    POETX_CUDA_TRY(cudaEventRecord(sc->fork, stream));
+    POETX_CUDA_TRY(cudaStreamWaitEvent(sc->ss, sc->fork, 0));
+    const poetx_status g = launch_perm_rows_side(as, true, dxt, N, m, L->perm_m, dx, sc->ss);
+    POETX_CUDA_TRY(cudaEventRecord(sc->join, sc->ss));
+    POETX_TRY(g);
+  } else if (st == POETX_OK && N > 0) {
+    st = launch_perm_rows(as, true, dxt, N, m, L->perm_m, dx, nullptr, nullptr, nullptr, stream);
+    if (st == POETX_OK && hk.dx_done && cudaEventRecord(hk.dx_done, stream) != cudaSuccess)
+      st = POETX_ERR_CUDA;
+  }
+  if (st == POETX_OK) {
+    const CnpSides sides{{L->q_R, L->q_P}, {m / b, n / b}};
+    const float* const dGs[2] = {dGR, dGP};
+    const int splits[2] = {p.splitsR, p.splitsP};
+    float* const dqs[2] = {dq_R, dq_P};
+    st = cnp_backward_sides(sides, at<float>(saved, p.Qs), at<float>(saved, p.Q2R), dGs, splits,
                             b, dqs, accumulate, at(ws, p.b_cnp), stream);
+  }
+  if (sc && cudaStreamWaitEvent(stream, sc->join, 0) != cudaSuccess && st == POETX_OK)
+    st = POETX_ERR_CUDA;
+  return st;
 }
 
 extern "C" poetx_status poetx_layer_bwd(const poetx_layer* L, const void* x, const void* dy, int N,

@@ -49,6 +49,7 @@ _SIGS = {
     "poetx_selftest_timeout": (_i, [ctypes.c_uint, _vp]),
     "poetx_set_gemm_engine": (_i, [_i]),
     "poetx_set_fusion": (_i, [_i]),
+    "poetx_set_overlap": (_i, [_i]),
     "poetx_launch_count": (ctypes.c_ulonglong, []),
     "poetx_timeout_site": (_i, []),
     "poetx_profile_enable": (_i, [_i]),
@@ -138,6 +139,10 @@ def poetx_set_gemm_engine(engine: int):
 
 def poetx_set_fusion(on: bool):
     _check("poetx_set_fusion", lib().poetx_set_fusion(1 if on else 0))
+
+
+def poetx_set_overlap(on: bool):
+    _check("poetx_set_overlap", lib().poetx_set_overlap(1 if on else 0))
 
 
 def poetx_launch_count() -> int:

@@ -315,3 +315,71 @@ def test_step_host_pageable_and_repeated(P):
     for k in ("y", "dx", "dq_R", "dq_P"):
         np.testing.assert_array_equal(a[k], b2[k], err_msg=k)
         np.testing.assert_array_equal(a[k], c[k], err_msg=k)
+
+
+@pytest.mark.parametrize("act,wdt,variant,shape", [
+    ("bf16", "bf16", "fast", (2048, 2048, 256, 1000)),
+    ("bf16", "bf16", "mem", (1024, 512, 128, 333)),
+    ("bf16", "i8", "mem", (512, 768, 256, 150)),
+    ("f32", "f32", "fast", (256, 256, 32, 64)),
+])
+def test_overlap_on_and_off_bitwise_equal(P, act, wdt, variant, shape):
+    """The dx scatter on the side stream (beside the CNP backward) gives the same bits as
+    the serial order."""
+    m, n, b, N = shape
+    inp = inputs.small_layer_inputs(83 + b, m, n, b, N, act=act, wdt=wdt)
+    try:
+        P.poetx_set_overlap(False)
+        off = run_layer(P, inp, b, act, wdt, variant)
+    finally:
+        P.poetx_set_overlap(True)
+    on = run_layer(P, inp, b, act, wdt, variant)
+    for k in ("y", "dx", "dq_R", "dq_P"):
+        np.testing.assert_array_equal(on[k], off[k], err_msg=k)
+
+
+def test_overlapped_step_in_a_cuda_graph(P):
+    """Forward + backward with the side-stream fork and join captured into a CUDA graph and
+    replayed: the same bits as the eager calls."""
+    m, n, b, N = 2048, 2048, 256, 777
+    inp = inputs.small_layer_inputs(89, m, n, b, N, act="bf16", wdt="bf16")
+    ref = run_layer(P, inp, b, "bf16", "bf16", "fast")
+    x = dev(inp["x"], torch.bfloat16)
+    dyt = dev(inp["dy"], torch.bfloat16)
+    pm = dev(inp["perm_m"], torch.int32)
+    pn = dev(inp["perm_n"], torch.int32)
+    qR = dev(inp["q_R"], torch.float32)
+    qP = dev(inp["q_P"], torch.float32)
+    W0 = dev(inp["W0"], torch.bfloat16)
+    Wp = torch.empty_like(W0)
+    P.poetx_merge_perm(W0, pn, pm, Wp)
+    L = P.make_layer(m, n, b, P.BF16, P.BF16, P.FAST, pm, pn, Wp, qR, qP, None)
+    saved = P.workspace(P.poetx_layer_saved_bytes(L, N), DEV)
+    wsf = P.workspace(P.poetx_layer_workspace_bytes(L, N, 0), DEV)
+    wsb = P.workspace(P.poetx_layer_workspace_bytes(L, N, 1), DEV)
+    y = torch.empty(N, n, dtype=torch.bfloat16, device=DEV)
+    dx = torch.empty(N, m, dtype=torch.bfloat16, device=DEV)
+    dqR = torch.empty_like(qR)
+    dqP = torch.empty_like(qP)
+
+    def step():
+        P.poetx_layer_fwd(L, x, y, saved, wsf)
+        P.poetx_layer_bwd(L, x, dyt, saved, dx, dqR, dqP, wsb)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    for t in (y, dx, dqR, dqP):
+        t.fill_(float("nan"))
+    g.replay()
+    torch.cuda.synchronize()
+    assert P.poetx_get_device_error() == 0
+    got = {"y": host(y), "dx": host(dx), "dq_R": host(dqR), "dq_P": host(dqP)}
+    for k in got:
+        np.testing.assert_array_equal(got[k], ref[k], err_msg=k)
