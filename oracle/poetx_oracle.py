@@ -300,6 +300,124 @@ def adam_step(q, g, m, v, t: int, lr: float, beta1: float = 0.9, beta2: float = 
 
 
 # ----------------------------------------------------------------------------------------
+# Ragged last block.  The POET-X summary ("Core method" §1) splits a side of d features into
+# ceil(d/b) blocks; when b does not divide d the last block has r = d - (ceil(d/b) - 1) b
+# features and its own r x r factor.  Storage (our reading, the pages do not say): q keeps
+# one row of b(b-1)/2 entries per block; the last block's parameters are the entries of the
+# pairs (i, k), i < k < r, at their places in the b-block's row-major order, and the other
+# entries of that row are not parameters (ignored on input, zero gradient).  Written out
+# per block with its own size, without padding.
+# ----------------------------------------------------------------------------------------
+def block_sizes(d: int, b: int):
+    """Sizes of the ceil(d/b) blocks of a side of d features."""
+    nb = -(-d // b)
+    return [min(b, d - j * b) for j in range(nb)]
+
+
+def _skew_of_row(qrow: np.ndarray, b: int, r: int) -> np.ndarray:
+    """The r x r skew block of one packed row (pairs i < k < r of the b-block order)."""
+    Q = np.zeros((r, r), dtype=F64)
+    k = 0
+    for i in range(b):
+        for j in range(i + 1, b):
+            if j < r:
+                Q[i, j] = qrow[k]
+                Q[j, i] = -qrow[k]
+            k += 1
+    return Q
+
+
+def cnp_forward_ragged(q: np.ndarray, b: int, d: int, order: int = 3):
+    """[G_j] for the blocks of a side of d features, G_j = (I + Q_j) N(Q_j) of size b_j."""
+    q = np.asarray(q, dtype=F64)
+    out = []
+    for j, r in enumerate(block_sizes(d, b)):
+        Q = _skew_of_row(q[j], b, r)
+        out.append((np.eye(r) + Q) @ _neumann_factor(Q, order))
+    return out
+
+
+def cnp_backward_ragged(q: np.ndarray, dGs, b: int, d: int, order: int = 3) -> np.ndarray:
+    """dq [ceil(d/b), b(b-1)/2] from the per-block dL/dG_j (sizes b_j); entries that are
+    not parameters of the last block get zero.  Per block this is cnp_backward's chain rule
+    (dL/d(I+Q) = dG N^T, dL/dN = (I+Q)^T dG, the power adjoints), then dq_k = Qbar_ij -
+    Qbar_ji for the parameter pairs."""
+    q = np.asarray(q, dtype=F64)
+    sizes = block_sizes(d, b)
+    out = np.zeros((len(sizes), b * (b - 1) // 2), dtype=F64)
+    for j, r in enumerate(sizes):
+        Q = _skew_of_row(q[j], b, r)
+        I = np.eye(r)
+        A = I + Q
+        Nq = _neumann_factor(Q, order)
+        dG = np.asarray(dGs[j], dtype=F64)
+        dA = dG @ Nq.T
+        dN = A.T @ dG
+        Pt = [I]
+        for _ in range(order):
+            Pt.append(Pt[-1] @ Q.T)
+        Qbar = dA.copy()
+        for p in range(1, order + 1):
+            for s in range(p):
+                Qbar = Qbar + Pt[s] @ dN @ Pt[p - 1 - s]
+        k = 0
+        for i in range(b):
+            for c in range(i + 1, b):
+                if c < r:
+                    out[j, k] = Qbar[i, c] - Qbar[c, i]
+                k += 1
+    return out
+
+
+def blockdiag_mm_ragged(X: np.ndarray, Gs, transpose: bool = False) -> np.ndarray:
+    """Y[:, o_j:o_j+b_j] = X[:, o_j:o_j+b_j] G_j (or G_j^T), o_j = sum of earlier sizes."""
+    X = np.asarray(X, dtype=F64)
+    Y = np.empty_like(X)
+    o = 0
+    for G in Gs:
+        r = G.shape[0]
+        Y[:, o:o + r] = X[:, o:o + r] @ (G.T if transpose else G)
+        o += r
+    assert o == X.shape[1]
+    return Y
+
+
+def blockdiag_wgrad_ragged(X: np.ndarray, dY: np.ndarray, sizes):
+    """[dG_j = X_j^T dY_j] for the column blocks of the given sizes."""
+    X = np.asarray(X, dtype=F64)
+    dY = np.asarray(dY, dtype=F64)
+    out, o = [], 0
+    for r in sizes:
+        out.append(X[:, o:o + r].T @ dY[:, o:o + r])
+        o += r
+    return out
+
+
+def poetx_layer_ragged(x, dy, W0, perm_m, perm_n, q_R, q_P, b: int, order: int = 3):
+    """poetx_layer for any m, n: ceil(m/b) and ceil(n/b) blocks, the last ones ragged.
+    Returns y, dx, dq_R, dq_P (dq rows of b(b-1)/2 with the non-parameters zero)."""
+    x = np.asarray(x, dtype=F64)
+    dy = np.asarray(dy, dtype=F64)
+    m, n = x.shape[1], dy.shape[1]
+    G_R = cnp_forward_ragged(q_R, b, m, order)
+    G_P = cnp_forward_ragged(q_P, b, n, order)
+    Wp = merge_perm(W0, perm_n, perm_m)
+    xt = perm_gather(x, perm_m)
+    A = blockdiag_mm_ragged(xt, G_R)
+    B = A @ Wp.T
+    zt = blockdiag_mm_ragged(B, G_P)
+    y = perm_scatter(zt, perm_n)
+    dzt = perm_gather(dy, perm_n)
+    dG_P = blockdiag_wgrad_ragged(B, dzt, block_sizes(n, b))
+    dB = blockdiag_mm_ragged(dzt, G_P, transpose=True)
+    dA = dB @ Wp
+    dG_R = blockdiag_wgrad_ragged(xt, dA, block_sizes(m, b))
+    dx = perm_scatter(blockdiag_mm_ragged(dA, G_R, transpose=True), perm_m)
+    return {"y": y, "dx": dx, "dq_R": cnp_backward_ragged(q_R, dG_R, b, m, order),
+            "dq_P": cnp_backward_ragged(q_P, dG_P, b, n, order), "G_R": G_R, "G_P": G_P}
+
+
+# ----------------------------------------------------------------------------------------
 # Error metric used by every parity test: relative Frobenius error, optionally the max over
 # the leading (block) axis.
 # ----------------------------------------------------------------------------------------

@@ -497,3 +497,90 @@ def test_rel_fro():
     b[1] *= 1.1
     assert O.rel_fro(a, a) == 0.0
     assert abs(O.rel_fro(b, a, per_block=True) - 0.1) < 1e-12
+
+
+# ------------------------------------------------------------------ ragged last block (N4)
+def _ragged(m, n, b, N, seed, qstd=0.3):
+    r = np.random.default_rng(seed)
+    nR, nP = -(-m // b), -(-n // b)
+    return {"x": r.standard_normal((N, m)), "dy": r.standard_normal((N, n)),
+            "W0": r.standard_normal((n, m)) / np.sqrt(m), "perm_m": r.permutation(m),
+            "perm_n": r.permutation(n),
+            "q_R": r.standard_normal((nR, b * (b - 1) // 2)) * qstd,
+            "q_P": r.standard_normal((nP, b * (b - 1) // 2)) * qstd}
+
+
+def test_block_sizes():
+    assert O.block_sizes(10, 4) == [4, 4, 2]
+    assert O.block_sizes(8, 4) == [4, 4]
+    assert O.block_sizes(9, 4) == [4, 4, 1]
+    assert O.block_sizes(3, 4) == [3]
+
+
+@pytest.mark.parametrize("m,n,b,N", [(10, 7, 4, 3), (9, 6, 4, 2), (6, 13, 5, 2)])
+def test_ragged_layer_finite_differences(m, n, b, N):
+    """Every gradient of L = <dy, y> (x, the parameters of every block including the ragged
+    last ones) against central differences of the ragged forward."""
+    L = _ragged(m, n, b, N, seed=m * 31 + n)
+    r = O.poetx_layer_ragged(L["x"], L["dy"], L["W0"], L["perm_m"], L["perm_n"], L["q_R"],
+                             L["q_P"], b)
+
+    def loss(x, qR, qP):
+        return np.sum(L["dy"] * O.poetx_layer_ragged(x, L["dy"], L["W0"], L["perm_m"],
+                                                     L["perm_n"], qR, qP, b)["y"])
+
+    h = 1e-6
+    base = {"x": L["x"], "qR": L["q_R"], "qP": L["q_P"]}
+    for name, grad in (("qR", r["dq_R"]), ("qP", r["dq_P"]), ("x", r["dx"])):
+        arr = base[name]
+        fd = np.zeros_like(arr)
+        for idx in np.ndindex(arr.shape):
+            p, mm = arr.copy(), arr.copy()
+            p[idx] += h
+            mm[idx] -= h
+            fd[idx] = (loss(**{**base, name: p}) - loss(**{**base, name: mm})) / (2 * h)
+        np.testing.assert_allclose(grad, fd, rtol=1e-6, atol=1e-8)
+
+
+def test_ragged_entries_outside_the_last_block_are_not_parameters():
+    """Changing an entry (i, k) with k >= r of the last block's row changes nothing, and its
+    gradient is zero; for b = 4, r = 2 only the pair (0, 1) is a parameter."""
+    m, n, b, N = 10, 8, 4, 3
+    L = _ragged(m, n, b, N, seed=5)
+    r0 = O.poetx_layer_ragged(L["x"], L["dy"], L["W0"], L["perm_m"], L["perm_n"], L["q_R"],
+                              L["q_P"], b)
+    q2 = L["q_R"].copy()
+    q2[2, 1:] += 0.7          # pairs (0,2), (0,3), (1,2), (1,3), (2,3) of the last block
+    r1 = O.poetx_layer_ragged(L["x"], L["dy"], L["W0"], L["perm_m"], L["perm_n"], q2,
+                              L["q_P"], b)
+    np.testing.assert_array_equal(r0["y"], r1["y"])
+    assert np.all(r0["dq_R"][2, 1:] == 0) and r0["dq_R"][2, 0] != 0
+
+
+def test_ragged_zero_q_is_plain_linear():
+    m, n, b, N = 11, 9, 4, 5
+    L = _ragged(m, n, b, N, seed=7)
+    z = lambda a: 0 * a
+    r = O.poetx_layer_ragged(L["x"], L["dy"], L["W0"], L["perm_m"], L["perm_n"], z(L["q_R"]),
+                             z(L["q_P"]), b)
+    np.testing.assert_allclose(r["y"], L["x"] @ L["W0"].T, rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(r["dx"], L["dy"] @ L["W0"], rtol=1e-13, atol=1e-13)
+
+
+def test_ragged_blocks_have_the_closed_form_defect():
+    """Each block, ragged or not, is the CNP of its own skew block: G^T G = (I - Q^4)^2
+    (Q^4 symmetric), and a block of one feature is the 1 x 1 identity."""
+    b, d = 4, 9
+    q = _rand_q(3, b)
+    Gs = O.cnp_forward_ragged(q, b, d)
+    assert [G.shape[0] for G in Gs] == [4, 4, 1]
+    assert Gs[2].tolist() == [[1.0]]
+    for j, G in enumerate(Gs[:2]):
+        Q = O.triu_unpack(q[j:j + 1], b)[0]
+        Q4 = np.linalg.matrix_power(Q, 4)
+        np.testing.assert_allclose(G.T @ G, (np.eye(b) - Q4) @ (np.eye(b) - Q4), atol=1e-12)
+    Gs2 = O.cnp_forward_ragged(q, b, 7)       # last block of 3: pairs (0,1), (0,2), (1,2)
+    Q3 = np.array([[0, q[1, 0], q[1, 1]], [-q[1, 0], 0, q[1, 3]], [-q[1, 1], -q[1, 3], 0]])
+    Q34 = np.linalg.matrix_power(Q3, 4)
+    np.testing.assert_allclose(Gs2[1].T @ Gs2[1], (np.eye(3) - Q34) @ (np.eye(3) - Q34),
+                               atol=1e-12)
