@@ -199,6 +199,20 @@ poetx_status poetx_merge_perm(const void* W0, const float* scale, poetx_dtype dt
                               const int32_t* perm_n, const int32_t* perm_m, void* Wp,
                               float* scale_p, cudaStream_t stream);
 
+/* The same merge into a zero-padded weight, for layers whose block size does not divide m
+ * or n (a ragged last block, see poetx_layer):
+ *   Wp [n_pad, m_pad]:  Wp[r, c] = W0[perm_n[r], perm_m[c]] for r < n, c < m; 0 elsewhere
+ *   scale_p [n_pad]:    scale[perm_n[r]] for r < n; 0 elsewhere (dt == POETX_I8)
+ * A layer takes n_pad = ceil(n/b) b and m_pad = ceil(m/b) b.  n_pad >= n, m_pad >= m;
+ * m * sizeof(dt) and m_pad * sizeof(dt) multiples of 16 (POETX_ERR_SHAPE otherwise: for
+ * int8, m a multiple of 16); int8
+ * with n_pad > n also needs n % 4 == 0, (n_pad - n) % 4 == 0 and a 16-byte aligned
+ * scale_p.  Bit-exact data movement and zero fill. */
+poetx_status poetx_merge_perm_padded(const void* W0, const float* scale, poetx_dtype dt, int n,
+                                     int m, int n_pad, int m_pad, const int32_t* perm_n,
+                                     const int32_t* perm_m, void* Wp, float* scale_p,
+                                     cudaStream_t stream);
+
 /* Per-output-row symmetric int8 quantisation of an fp32 weight (POET-XQ storage; the page
  * says only "low-bit W", the scheme is this library's reading):
  *   scale[r] = max_c |W[r,c]| / 127 in fp32 (1 for an all-zero row),
@@ -247,7 +261,11 @@ poetx_status poetx_wprime_gemm(poetx_dtype act, poetx_dtype wdt, const void* A, 
 typedef struct poetx_layer {
   int m;                   /* in-features (x has m columns) */
   int n;                   /* out-features (y has n columns) */
-  int b;                   /* block size: b | m, b | n; bf16: b in {64,128,256,512} */
+  int b;                   /* block size; bf16: b in {64,128,256,512}.  ceil(m/b) and ceil(n/b)
+                              blocks per side; when b does not divide m or n the last block
+                              of that side is ragged (r = m - (ceil(m/b) - 1) b features,
+                              its own r x r factor; POET-X summary, "Core method" §1), which
+                              needs b, m and n multiples of 8 */
   int order;               /* Neumann order; must be 3 */
   poetx_dtype act;         /* POETX_F32 or POETX_BF16: x, y, dy, dx */
   poetx_dtype wdt;         /* POETX_F32 (with act F32), POETX_BF16, or POETX_I8 (act BF16,
@@ -256,10 +274,15 @@ typedef struct poetx_layer {
                               recomputes it */
   const int32_t* perm_m;   /* [m] */
   const int32_t* perm_n;   /* [n] */
-  const void* Wp;          /* merged frozen weight [n, m] of dtype wdt (poetx_merge_perm) */
-  const float* w_scale;    /* [n] per-row scale of Wp when wdt == POETX_I8, else NULL */
-  const float* q_R;        /* [m/b, b(b-1)/2] */
-  const float* q_P;        /* [n/b, b(b-1)/2] */
+  const void* Wp;          /* merged frozen weight [n_pad, m_pad] of dtype wdt, n_pad =
+                              ceil(n/b) b, m_pad = ceil(m/b) b (poetx_merge_perm when b
+                              divides both, else poetx_merge_perm_padded) */
+  const float* w_scale;    /* [n_pad] per-row scale of Wp when wdt == POETX_I8, else NULL */
+  const float* q_R;        /* [ceil(m/b), b(b-1)/2]; the ragged last block's parameters are
+                              the pairs (i, k), i < k < r, at their places in the b-block's
+                              row-major order; its other entries are ignored and get zero
+                              gradient */
+  const float* q_P;        /* [ceil(n/b), b(b-1)/2], the same way */
 } poetx_layer;
 
 /* Scratch bytes for poetx_layer_fwd (phase 0) or poetx_layer_bwd (phase 1) at N tokens;

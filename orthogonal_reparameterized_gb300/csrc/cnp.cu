@@ -267,7 +267,8 @@ poetx_status cnp_forward_sides(const CnpSides& q, int b, float* Qs, float* Q2, f
                                void* G_bf16, void* Gt_bf16, cudaStream_t s) {
   const int nblk = q.n[0] + q.n[1];
   if (nblk == 0) return POETX_OK;
-  POETX_TRY(launch_triu_unpack2(q.q[0], q.n[0], q.q[1], q.n[1], b, Qs, s));
+  POETX_TRY(launch_triu_unpack2(q.q[0], q.n[0], q.q[1], q.n[1], b, Qs, s, q.last[0],
+                                  q.last[1]));
   // Q2 = Q Q (symmetric); B^T = Q^T = -Q
   CnpGemm g{};
   g.b = b;
@@ -316,7 +317,8 @@ poetx_status cnp_backward_sides(const CnpSides& q, const float* Qin, const float
   float* Qbar = reinterpret_cast<float*>(w + 6 * bb);
   const float* Qs = Qin;
   if (!Qs) {
-    POETX_TRY(launch_triu_unpack2(q.q[0], q.n[0], q.q[1], q.n[1], b, Qw, s));
+    POETX_TRY(launch_triu_unpack2(q.q[0], q.n[0], q.q[1], q.n[1], b, Qw, s, q.last[0],
+                                  q.last[1]));
     Qs = Qw;
   }
   if (!Q2in) {
@@ -378,7 +380,8 @@ poetx_status cnp_backward_sides(const CnpSides& q, const float* Qin, const float
   r.e2 = 2.f;
   r.out_f32 = Qbar;
   POETX_TRY(launch_cnp_gemm(r, nblk, ST_CNP_QBAR, s));
-  return launch_triu_grad_pack2(Qbar, q.n[0], q.n[1], b, dq[0], dq[1], accumulate, s);
+  return launch_triu_grad_pack2(Qbar, q.n[0], q.n[1], b, dq[0], dq[1], accumulate, s,
+                                q.last[0], q.last[1]);
 }
 
 }  // namespace poetx

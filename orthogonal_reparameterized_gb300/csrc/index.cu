@@ -28,9 +28,15 @@ __device__ __forceinline__ long long tri_index(int i, int j, int b) {
 // reads the packed entries of the tile's upper part (consecutive j are consecutive in q),
 // writes Q[I][J] and, through shared memory, the mirrored tile Q[J][I] = -Q[I][J]^T, both
 // with coalesced rows.
+// r0, r1: features of the last block of each side (b unless that block is ragged): the
+// entries of a ragged block outside its r x r corner are not parameters and are zero in Q.
+__device__ __forceinline__ int block_valid(int blk, int n0, int r0, int r1, int b) {
+  return blk == n0 - 1 ? r0 : (blk == (int)gridDim.z - 1 ? r1 : b);
+}
+
 __global__ void triu_unpack_kernel(const float* __restrict__ q0, int n0, const float* __restrict__ q1,
-                                   int b, float* __restrict__ Q, unsigned long long* tr,
-                                   size_t tr_cap) {
+                                   int b, int r0, int r1, float* __restrict__ Q,
+                                   unsigned long long* tr, size_t tr_cap) {
   if (threadIdx.x == 0 && threadIdx.y == 0) trace_stamp3(tr, tr_cap, 0);
   pdl_trigger();
   pdl_wait();
@@ -47,12 +53,14 @@ __global__ void triu_unpack_kernel(const float* __restrict__ q0, int n0, const f
   const long long tri = (long long)b * (b - 1) / 2;
   const float* qb = blk < n0 ? q0 + blk * tri : q1 + (blk - n0) * tri;
   float* Qb = Q + (long long)blk * b * b;
+  const int rv = block_valid(blk, n0, r0, r1, b);
   const int tx = threadIdx.x, ty = threadIdx.y;  // 32 x 8
   for (int r = ty; r < 32; r += 8) {
     const int i = I * 32 + r, j = J * 32 + tx;
     float v = 0.f;
     if (i < b && j < b) {
-      if (i < j) v = qb[tri_index(i, j, b)];
+      if (i >= rv || j >= rv) v = 0.f;
+      else if (i < j) v = qb[tri_index(i, j, b)];
       else if (i > j) v = -qb[tri_index(j, i, b)];
       Qb[(long long)i * b + j] = v;
     }
@@ -76,8 +84,8 @@ __global__ void triu_unpack_kernel(const float* __restrict__ q0, int n0, const f
 // read back transposed, so both reads of Qbar are coalesced; the writes of a row i of the
 // tile are consecutive entries of the packed triangle.
 __global__ void triu_grad_pack_kernel(const float* __restrict__ Qbar, int b, float* __restrict__ dq0,
-                                      int n0, float* __restrict__ dq1, int accumulate,
-                                      unsigned long long* tr, size_t tr_cap) {
+                                      int n0, float* __restrict__ dq1, int accumulate, int r0,
+                                      int r1, unsigned long long* tr, size_t tr_cap) {
   if (threadIdx.x == 0 && threadIdx.y == 0) trace_stamp3(tr, tr_cap, 0);
   pdl_trigger();
   pdl_wait();
@@ -93,6 +101,7 @@ __global__ void triu_grad_pack_kernel(const float* __restrict__ Qbar, int b, flo
   const long long tri = (long long)b * (b - 1) / 2;
   const float* Qb = Qbar + (long long)blk * b * b;
   float* dqb = blk < n0 ? dq0 + blk * tri : dq1 + (blk - n0) * tri;
+  const int rv = block_valid(blk, n0, r0, r1, b);
   const int tx = threadIdx.x, ty = threadIdx.y;  // 32 x 8
   for (int r = ty; r < 32; r += 8) {  // tile[r][c] = Qbar[J*32 + r][I*32 + c]
     const int j = J * 32 + r, i = I * 32 + tx;
@@ -102,7 +111,7 @@ __global__ void triu_grad_pack_kernel(const float* __restrict__ Qbar, int b, flo
   for (int r = ty; r < 32; r += 8) {
     const int i = I * 32 + r, j = J * 32 + tx;
     if (i < j && j < b) {
-      const float v = Qb[(long long)i * b + j] - tile[tx][r];
+      const float v = j < rv ? Qb[(long long)i * b + j] - tile[tx][r] : 0.f;
       float* dst = dqb + tri_index(i, j, b);
       *dst = accumulate ? *dst + v : v;
     }
@@ -114,14 +123,14 @@ __global__ void triu_grad_pack_kernel(const float* __restrict__ Qbar, int b, flo
 }
 
 poetx_status launch_triu_unpack2(const float* q0, int n0, const float* q1, int n1, int b, float* Q,
-                                 cudaStream_t s) {
+                                 cudaStream_t s, int r0, int r1) {
   if (n0 + n1 == 0) return POETX_OK;
   const int nt = (b + 31) / 32;
   dim3 grid(nt * (nt + 1) / 2, 1, n0 + n1);
   size_t tr_cap = 0;
   unsigned long long* tr = trace_buffer(&tr_cap);
-  POETX_CUDA_TRY(launch_pdl(triu_unpack_kernel, grid, dim3(32, 8), 0, s, q0, n0, q1, b, Q, tr,
-                            tr_cap));
+  POETX_CUDA_TRY(launch_pdl(triu_unpack_kernel, grid, dim3(32, 8), 0, s, q0, n0, q1, b,
+                            r0 > 0 ? r0 : b, r1 > 0 ? r1 : b, Q, tr, tr_cap));
   POETX_CUDA_TRY(cudaGetLastError());
   after_launch(s, ST_TRIU_UNPACK);
   return POETX_OK;
@@ -132,14 +141,14 @@ poetx_status launch_triu_unpack(const float* q, int nblk, int b, float* Q, cudaS
 }
 
 poetx_status launch_triu_grad_pack2(const float* Qbar, int n0, int n1, int b, float* dq0, float* dq1,
-                                    int accumulate, cudaStream_t s) {
+                                    int accumulate, cudaStream_t s, int r0, int r1) {
   if (n0 + n1 == 0 || b < 2) return POETX_OK;
   const int nt = (b + 31) / 32;
   dim3 grid(nt * (nt + 1) / 2, 1, n0 + n1);
   size_t tr_cap = 0;
   unsigned long long* tr = trace_buffer(&tr_cap);
   POETX_CUDA_TRY(launch_pdl(triu_grad_pack_kernel, grid, dim3(32, 8), 0, s, Qbar, b, dq0, n0,
-                            dq1, accumulate, tr, tr_cap));
+                            dq1, accumulate, r0 > 0 ? r0 : b, r1 > 0 ? r1 : b, tr, tr_cap));
   POETX_CUDA_TRY(cudaGetLastError());
   after_launch(s, ST_TRIU_PACK);
   return POETX_OK;
@@ -230,8 +239,8 @@ template <int E, bool SCATTER, typename IdxT>
 __global__ void __launch_bounds__((kPermWarps + 1) * 32) perm_rows_kernel(
     const uint8_t* __restrict__ X, long long N, int D, const int32_t* __restrict__ perm,
     uint8_t* __restrict__ Y, const int32_t* __restrict__ src_rows, const float* __restrict__ scale,
-    float* __restrict__ scale_out, int G, int S, int* err, unsigned long long limit_ns,
-    unsigned long long* trace, size_t trace_cap) {
+    float* __restrict__ scale_out, long long src_pitch, long long dst_pitch, int G, int S,
+    int* err, unsigned long long limit_ns, unsigned long long* trace, size_t trace_cap) {
   using T = typename VecT<E>::T;
   constexpr int V = 16 / E;  // elements per 16-byte vector
   extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -290,7 +299,8 @@ __global__ void __launch_bounds__((kPermWarps + 1) * 32) perm_rows_kernel(
           const long long r = first + gr + (long long)it * stride;
           const long long sr = src_rows ? (long long)__ldg(src_rows + r) : r;
           mbar_arrive_expect_tx(&full[slot], row_bytes);
-          bulk_load(ring + (size_t)slot * row_bytes, X + sr * row_bytes, row_bytes, &full[slot]);
+          bulk_load(ring + (size_t)slot * row_bytes, X + sr * src_pitch * E, row_bytes,
+                    &full[slot]);
           issued[gr] = it + 1;
         }
         if (it == 0) trace_stamp(trace, trace_cap, 2);  // slot 2: first row of every group issued
@@ -320,6 +330,7 @@ __global__ void __launch_bounds__((kPermWarps + 1) * 32) perm_rows_kernel(
     if (threadIdx.x == 0) trace_stamp(trace, trace_cap, 3);  // slot 3: index staged
     const int nrows = rows_of(g);
     const int nvec = D / V;
+    const int nvec_dst = (int)(dst_pitch / V);
     const int gthreads = G * 32;
     int k = 0;
     uint32_t ph = 0;
@@ -330,7 +341,7 @@ __global__ void __launch_bounds__((kPermWarps + 1) * 32) perm_rows_kernel(
       if (threadIdx.x == 0 && it < 13) trace_stamp(trace, trace_cap, 4 + 2 * it);  // landed
       const long long r = first + g + (long long)it * stride;
       const T* row = reinterpret_cast<const T*>(ring + (size_t)slot * row_bytes);
-      uint4* out = reinterpret_cast<uint4*>(Y + r * row_bytes);
+      uint4* out = reinterpret_cast<uint4*>(Y + r * dst_pitch * E);
 #pragma unroll 4
       for (int v = tig; v < nvec; v += gthreads) {
         const IdxVec<IdxT, V> ix = load_idx<IdxT, V>(idx + (size_t)v * V);
@@ -339,6 +350,8 @@ __global__ void __launch_bounds__((kPermWarps + 1) * 32) perm_rows_kernel(
         for (int e = 0; e < V; ++e) pk.e[e] = row[ix.i[e]];
         out[v] = pk.u;
       }
+      // columns D .. dst_pitch - 1 of a padded destination row (ragged last block) are zero
+      for (int v = nvec + tig; v < nvec_dst; v += gthreads) out[v] = make_uint4(0, 0, 0, 0);
       if (scale_out && tig == 0) scale_out[r] = scale[src_rows ? src_rows[r] : r];
       group_sync(g, G);  // every thread of the group is done with buffer k
       if (threadIdx.x == 0 && it < 13) trace_stamp(trace, trace_cap, 5 + 2 * it);  // row done
@@ -400,7 +413,8 @@ static bool perm_shape_side(size_t row_bytes, size_t idx_bytes, int* G, int* S, 
 template <int E, bool SCATTER, typename IdxT>
 static poetx_status launch_perm_rows_t(const void* X, long long N, int D, const int32_t* perm,
                                        void* Y, const int32_t* src_rows, const float* scale,
-                                       float* scale_out, bool side, cudaStream_t s) {
+                                       float* scale_out, long long sp, long long dp, bool side,
+                                       cudaStream_t s) {
   const size_t row_bytes = (size_t)D * E;
   const size_t idx_bytes = ((size_t)D * sizeof(IdxT) + 127) & ~(size_t)127;
   int G = 0, S = 0;
@@ -431,13 +445,13 @@ static poetx_status launch_perm_rows_t(const void* X, long long N, int D, const 
     // of the other stream still need it
     k<<<grid, (kPermWarps + 1) * 32, smem, s>>>(static_cast<const uint8_t*>(X), N, D, perm,
                                                 static_cast<uint8_t*>(Y), src_rows, scale,
-                                                scale_out, G, S, device_error_word(),
+                                                scale_out, sp, dp, G, S, device_error_word(),
                                                 kWaitLimitNs, tr, tr_cap);
   } else {
     POETX_CUDA_TRY(launch_pdl(k, dim3(grid), dim3((kPermWarps + 1) * 32), smem, s,
                               static_cast<const uint8_t*>(X), N, D, perm,
-                              static_cast<uint8_t*>(Y), src_rows, scale, scale_out, G, S,
-                              device_error_word(), kWaitLimitNs, tr, tr_cap));
+                              static_cast<uint8_t*>(Y), src_rows, scale, scale_out, sp, dp, G,
+                              S, device_error_word(), kWaitLimitNs, tr, tr_cap));
   }
   POETX_CUDA_TRY(cudaGetLastError());
   after_launch(s, src_rows ? ST_MERGE : (SCATTER ? ST_PERM_SCATTER : ST_PERM_GATHER));
@@ -447,32 +461,42 @@ static poetx_status launch_perm_rows_t(const void* X, long long N, int D, const 
 template <int E>
 static poetx_status launch_perm_rows_e(bool scatter, const void* X, long long N, int D,
                                        const int32_t* perm, void* Y, const int32_t* src_rows,
-                                       const float* scale, float* scale_out, bool side,
-                                       cudaStream_t s) {
+                                       const float* scale, float* scale_out, long long sp,
+                                       long long dp, bool side, cudaStream_t s) {
   if (D <= 65535) {
-    return scatter ? launch_perm_rows_t<E, true, uint16_t>(X, N, D, perm, Y, src_rows, scale, scale_out, side, s)
-                   : launch_perm_rows_t<E, false, uint16_t>(X, N, D, perm, Y, src_rows, scale, scale_out, side, s);
+    return scatter ? launch_perm_rows_t<E, true, uint16_t>(X, N, D, perm, Y, src_rows, scale, scale_out, sp, dp, side, s)
+                   : launch_perm_rows_t<E, false, uint16_t>(X, N, D, perm, Y, src_rows, scale, scale_out, sp, dp, side, s);
   }
-  return scatter ? launch_perm_rows_t<E, true, uint32_t>(X, N, D, perm, Y, src_rows, scale, scale_out, side, s)
-                 : launch_perm_rows_t<E, false, uint32_t>(X, N, D, perm, Y, src_rows, scale, scale_out, side, s);
+  return scatter ? launch_perm_rows_t<E, true, uint32_t>(X, N, D, perm, Y, src_rows, scale, scale_out, sp, dp, side, s)
+                 : launch_perm_rows_t<E, false, uint32_t>(X, N, D, perm, Y, src_rows, scale, scale_out, sp, dp, side, s);
 }
 
+// sp, dp: source and destination row pitches in elements (0: D).  The D permuted columns
+// of each row go to columns 0 .. D - 1 of the destination row and columns D .. dp - 1 are
+// written with zeros; every pitch is a whole number of 16-byte vectors.
 static poetx_status perm_rows_any(size_t esize, bool scatter, const void* X, long long N, int D,
                                   const int32_t* perm, void* Y, const int32_t* src_rows,
-                                  const float* scale, float* scale_out, bool side,
-                                  cudaStream_t s) {
+                                  const float* scale, float* scale_out, long long sp,
+                                  long long dp, bool side, cudaStream_t s) {
   if (N == 0 || D == 0) return POETX_OK;
-  if (((size_t)D * esize) % 16 != 0) return POETX_ERR_SHAPE;
-  if (esize == 1) return launch_perm_rows_e<1>(scatter, X, N, D, perm, Y, src_rows, scale, scale_out, side, s);
-  if (esize == 2) return launch_perm_rows_e<2>(scatter, X, N, D, perm, Y, src_rows, scale, scale_out, side, s);
-  if (esize == 4) return launch_perm_rows_e<4>(scatter, X, N, D, perm, Y, src_rows, scale, scale_out, side, s);
+  sp = sp ? sp : D;
+  dp = dp ? dp : D;
+  if (sp < D || dp < D) return POETX_ERR_ARG;
+  if (((size_t)D * esize) % 16 != 0 || ((size_t)sp * esize) % 16 != 0 ||
+      ((size_t)dp * esize) % 16 != 0)
+    return POETX_ERR_SHAPE;
+  if (esize == 1) return launch_perm_rows_e<1>(scatter, X, N, D, perm, Y, src_rows, scale, scale_out, sp, dp, side, s);
+  if (esize == 2) return launch_perm_rows_e<2>(scatter, X, N, D, perm, Y, src_rows, scale, scale_out, sp, dp, side, s);
+  if (esize == 4) return launch_perm_rows_e<4>(scatter, X, N, D, perm, Y, src_rows, scale, scale_out, sp, dp, side, s);
   return POETX_ERR_DTYPE;
 }
 
 poetx_status launch_perm_rows(size_t esize, bool scatter, const void* X, long long N, int D,
                               const int32_t* perm, void* Y, const int32_t* src_rows,
-                              const float* scale, float* scale_out, cudaStream_t s) {
-  return perm_rows_any(esize, scatter, X, N, D, perm, Y, src_rows, scale, scale_out, false, s);
+                              const float* scale, float* scale_out, cudaStream_t s,
+                              long long src_pitch, long long dst_pitch) {
+  return perm_rows_any(esize, scatter, X, N, D, perm, Y, src_rows, scale, scale_out, src_pitch,
+                       dst_pitch, false, s);
 }
 
 bool perm_side_fits(size_t esize, int D) {
@@ -483,8 +507,10 @@ bool perm_side_fits(size_t esize, int D) {
 }
 
 poetx_status launch_perm_rows_side(size_t esize, bool scatter, const void* X, long long N, int D,
-                                   const int32_t* perm, void* Y, cudaStream_t s) {
-  return perm_rows_any(esize, scatter, X, N, D, perm, Y, nullptr, nullptr, nullptr, true, s);
+                                   const int32_t* perm, void* Y, cudaStream_t s,
+                                   long long src_pitch, long long dst_pitch) {
+  return perm_rows_any(esize, scatter, X, N, D, perm, Y, nullptr, nullptr, nullptr, src_pitch,
+                       dst_pitch, true, s);
 }
 
 // ---------------------------------------------------------------- int8 quantiser
@@ -626,6 +652,56 @@ extern "C" poetx_status poetx_perm_gather(poetx_dtype dt, const void* X, int N, 
 extern "C" poetx_status poetx_perm_scatter(poetx_dtype dt, const void* X, int N, int D,
                                            const int32_t* perm, void* Y, cudaStream_t stream) {
   return perm_entry(true, dt, X, N, D, perm, Y, stream);
+}
+
+// Zeroes `words` 16-byte words at p (p 16-byte aligned).
+__global__ void zero_fill_kernel(uint4* __restrict__ p, unsigned long long words) {
+  pdl_trigger();
+  pdl_wait();
+  for (unsigned long long i = blockIdx.x * (unsigned long long)blockDim.x + threadIdx.x;
+       i < words; i += (unsigned long long)gridDim.x * blockDim.x)
+    p[i] = make_uint4(0, 0, 0, 0);
+}
+
+static poetx_status launch_zero_fill(void* p, size_t bytes, cudaStream_t s) {
+  const unsigned long long words = bytes / 16;
+  if (words == 0) return POETX_OK;
+  const unsigned long long want = (words + 255) / 256;
+  const int grid = (int)(want < 4ull * sm_count() ? want : 4ull * sm_count());
+  POETX_CUDA_TRY(launch_pdl(zero_fill_kernel, dim3(grid), dim3(256), 0, s,
+                            static_cast<uint4*>(p), words));
+  POETX_CUDA_TRY(cudaGetLastError());
+  after_launch(s, ST_MERGE);
+  return POETX_OK;
+}
+
+extern "C" poetx_status poetx_merge_perm_padded(const void* W0, const float* scale,
+                                                poetx_dtype dt, int n, int m, int n_pad,
+                                                int m_pad, const int32_t* perm_n,
+                                                const int32_t* perm_m, void* Wp,
+                                                float* scale_p, cudaStream_t stream) {
+  const size_t es = dtype_size(dt);
+  if (!es) return POETX_ERR_DTYPE;
+  if (n < 0 || m < 0 || n_pad < n || m_pad < m) return POETX_ERR_ARG;
+  if (n_pad == 0 || m_pad == 0) return POETX_OK;
+  if (!Wp || (n > 0 && m > 0 && (!W0 || !perm_n || !perm_m))) return POETX_ERR_ARG;
+  if (dt == POETX_I8 && (!scale_p || (n > 0 && !scale))) return POETX_ERR_ARG;
+  if ((W0 && !aligned16(W0)) || !aligned16(Wp)) return POETX_ERR_ALIGN;
+  if (((size_t)m * es) % 16 || ((size_t)m_pad * es) % 16) return POETX_ERR_SHAPE;
+  const int live = (n > 0 && m > 0) ? n : 0;  // rows written from W0; the rest are zero
+  if (dt == POETX_I8 && n_pad > live &&
+      (!aligned16(scale_p) || live % 4 || (n_pad - live) % 4))
+    return aligned16(scale_p) ? POETX_ERR_SHAPE : POETX_ERR_ALIGN;
+  if (live > 0)
+    POETX_TRY(launch_perm_rows(es, false, W0, n, m, perm_m, Wp, perm_n,
+                               dt == POETX_I8 ? scale : nullptr,
+                               dt == POETX_I8 ? scale_p : nullptr, stream, m, m_pad));
+  // rows live .. n_pad - 1 (and their scales) are zero
+  POETX_TRY(launch_zero_fill(static_cast<uint8_t*>(Wp) + (size_t)live * m_pad * es,
+                             (size_t)(n_pad - live) * m_pad * es, stream));
+  if (dt == POETX_I8 && n_pad > live)
+    POETX_TRY(launch_zero_fill(scale_p + live, (size_t)(n_pad - live) * 4, stream));
+  return POETX_OK;
 }
 
 extern "C" poetx_status poetx_merge_perm(const void* W0, const float* scale, poetx_dtype dt,

@@ -12,20 +12,27 @@ namespace poetx {
 // ---- index.cu
 poetx_status launch_triu_unpack(const float* q, int nblk, int b, float* Q, cudaStream_t s);
 // Two-sided: blocks [0, n0) from q0, [n0, n0 + n1) from q1.
+// r0, r1: features of the last block of side 0 / side 1 (0: b); entries of a ragged last
+// block outside its r x r corner are zero in Q and get zero gradient.
 poetx_status launch_triu_unpack2(const float* q0, int n0, const float* q1, int n1, int b, float* Q,
-                                 cudaStream_t s);
+                                 cudaStream_t s, int r0 = 0, int r1 = 0);
 poetx_status launch_triu_grad_pack2(const float* Qbar, int n0, int n1, int b, float* dq0, float* dq1,
-                                    int accumulate, cudaStream_t s);
+                                    int accumulate, cudaStream_t s, int r0 = 0, int r1 = 0);
 poetx_status launch_triu_grad_pack(const float* Qbar, int nblk, int b, float* dq, int accumulate,
                                    cudaStream_t s);
+// Y[r][j] = X[src_rows ? src_rows[r] : r][perm[j]] (gather) or Y[r][perm[j]] = X[r][j]
+// (scatter), j < D; src_pitch / dst_pitch: row pitches in elements (0: D), destination
+// columns D .. dst_pitch - 1 zeroed.
 poetx_status launch_perm_rows(size_t esize, bool scatter, const void* X, long long N, int D,
                               const int32_t* perm, void* Y, const int32_t* src_rows,
-                              const float* scale, float* scale_out, cudaStream_t s);
+                              const float* scale, float* scale_out, cudaStream_t s,
+                              long long src_pitch = 0, long long dst_pitch = 0);
 // The same permutation in the co-resident shape (one small CTA per SM, beside a CNP
 // product); perm_side_fits says whether rows of D elements fit that shape.
 bool perm_side_fits(size_t esize, int D);
 poetx_status launch_perm_rows_side(size_t esize, bool scatter, const void* X, long long N, int D,
-                                   const int32_t* perm, void* Y, cudaStream_t s);
+                                   const int32_t* perm, void* Y, cudaStream_t s,
+                                   long long src_pitch = 0, long long dst_pitch = 0);
 poetx_status launch_quantize(const float* W, int n, int m, int8_t* Wq, float* scale,
                              cudaStream_t s);
 // inv_a[perm_a[i]] = i (i < na) and inv_b[perm_b[k]] = k (k < nb), one launch.
@@ -66,6 +73,7 @@ poetx_status launch_simt_gemm(poetx_dtype ta, poetx_dtype tb, poetx_dtype tc, co
 struct CnpSides {
   const float* q[2];   // packed triangles of each side
   int n[2];            // blocks of each side (n[1] may be 0)
+  int last[2] = {0, 0};  // features of each side's last block when ragged (0: b)
 };
 size_t cnp_fwd_scratch_bytes(int nblk, int b);
 size_t cnp_bwd_scratch_bytes(int nblk, int b);

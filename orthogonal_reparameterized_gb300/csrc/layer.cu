@@ -117,11 +117,28 @@ poetx_status wprime_impl(poetx_dtype act, poetx_dtype wdt, const void* A, long l
   return launch_simt_gemm(act, wdt, act, g, s);
 }
 
+// Ragged last block (POET-X summary, "Core method" §1: ceil(d/b) blocks per side).  Inside
+// the layer every side is padded to whole blocks: the activations between the permutations
+// have ceil(d/b) b columns (the gathers write the padding columns as zeros, the scatters read
+// only the first d), the merged weight is [ceil(n/b) b, ceil(m/b) b] with zero padding, and
+// the last block's Q is zero outside its r x r corner, so its G is the r x r factor with the
+// identity beside it: the padding columns stay zero through every product and the results
+// are those of the ragged blocks.
+static int padded(int d, int b) { return (d + b - 1) / b * b; }
+static int last_block(int d, int b) { return d % b; }  // 0: the last block is whole
+
+static CnpSides layer_sides(const poetx_layer* L) {
+  CnpSides sd{{L->q_R, L->q_P}, {padded(L->m, L->b) / L->b, padded(L->n, L->b) / L->b}};
+  sd.last[0] = last_block(L->m, L->b);
+  sd.last[1] = last_block(L->n, L->b);
+  return sd;
+}
+
 // The W' contraction and the block-diagonal product after it in one kernel (bf16 W', the
 // tensor-core engine, shapes the fused kernel takes).
 static bool fused_ok(const poetx_layer* L, long long N, int trans) {
   return L->act == POETX_BF16 && L->wdt == POETX_BF16 && use_umma() && g_fuse.load() &&
-         umma_wprime_fusable(N, L->m, L->n, trans, L->b);
+         umma_wprime_fusable(N, padded(L->m, L->b), padded(L->n, L->b), trans, L->b);
 }
 
 // ---------------------------------------------------------------- layer plumbing
@@ -139,7 +156,8 @@ static poetx_status validate(const poetx_layer* L) {
   if (!L) return POETX_ERR_ARG;
   if (L->m <= 0 || L->n <= 0 || L->b <= 0) return POETX_ERR_ARG;
   if (L->order != 3) return POETX_ERR_UNSUPPORTED;
-  if (L->m % L->b || L->n % L->b) return POETX_ERR_SHAPE;
+  // a ragged side needs 16-byte rows at both widths
+  if ((L->m % L->b || L->n % L->b) && (L->b % 8 || L->m % 8 || L->n % 8)) return POETX_ERR_SHAPE;
   if (L->act == POETX_F32) {
     if (L->wdt != POETX_F32) return POETX_ERR_DTYPE;
     if (L->b < 2 || L->b > 1024 || L->m % 4 || L->n % 4) return POETX_ERR_SHAPE;
@@ -161,7 +179,8 @@ static Plan make_plan(const poetx_layer* L, long long N) {
   Plan p{};
   const size_t as = dtype_size(L->act);
   const size_t gs = L->act == POETX_F32 ? 4 : 2;
-  const size_t m = L->m, n = L->n, b = L->b;
+  // padded widths: every internal array has whole blocks
+  const size_t m = padded(L->m, L->b), n = padded(L->n, L->b), b = L->b;
   size_t o = 0;
   auto take = [&](size_t bytes) { size_t r = o; o += align_up(bytes, 256); return r; };
   // G_R and G_P (and Q_R^2, Q_P^2) are adjacent stacks so that one CNP launch covers both
@@ -181,8 +200,8 @@ static Plan make_plan(const poetx_layer* L, long long N) {
   p.f_zt = take((size_t)N * n * as);
   p.fwd_total = o;
 
-  p.splitsR = wgrad_splits(N, L->m / L->b, L->b);
-  p.splitsP = wgrad_splits(N, L->n / L->b, L->b);
+  p.splitsR = wgrad_splits(N, (int)(m / b), L->b);
+  p.splitsP = wgrad_splits(N, (int)(n / b), L->b);
   o = 0;
   p.b_cnp = take(cnp_bwd_scratch_bytes((int)((m + n) / b), (int)b));
   p.b_xt = L->variant == POETX_MEM ? take((size_t)N * m * as) : 0;
@@ -209,7 +228,7 @@ struct MergePlan {
 
 static MergePlan merge_plan(const poetx_layer* L) {
   MergePlan p{};
-  const size_t m = L->m, n = L->n, b = L->b;
+  const size_t m = padded(L->m, L->b), n = padded(L->n, L->b), b = L->b;
   size_t o = 0;
   auto take = [&](size_t bytes) { size_t r = o; o += align_up(bytes, 256); return r; };
   p.Qs = take((m + n) * b * 4);
@@ -267,9 +286,9 @@ extern "C" poetx_status poetx_merge_reinit(const poetx_layer* L, float* W0_new, 
   if (!aligned16(W0_new) || !aligned16(ws)) return POETX_ERR_ALIGN;
   const MergePlan p = merge_plan(L);
   if (ws_bytes < p.total) return POETX_ERR_WORKSPACE;
-  const int b = L->b, m = L->m, n = L->n;
+  const int b = L->b, m = padded(L->m, b), n = padded(L->n, b);  // padded widths
   // G_R (blocks [0, m/b)) and G_P (blocks [m/b, (m+n)/b)) in fp32
-  const CnpSides sides{{L->q_R, L->q_P}, {m / b, n / b}};
+  const CnpSides sides = layer_sides(L);
   float* G = at<float>(ws, p.G);
   POETX_TRY(cnp_forward_sides(sides, b, at<float>(ws, p.Qs), at<float>(ws, p.Q2), G, nullptr,
                               nullptr, stream));
@@ -305,8 +324,10 @@ extern "C" poetx_status poetx_merge_reinit(const poetx_layer* L, float* W0_new, 
   POETX_TRY(launch_simt_gemm(POETX_F32, POETX_F32, POETX_F32, g, stream));
   int32_t* inv_m = at<int32_t>(ws, p.inv_m);
   int32_t* inv_n = at<int32_t>(ws, p.inv_n);
-  POETX_TRY(launch_invert_perms(L->perm_m, m, inv_m, L->perm_n, n, inv_n, stream));
-  return launch_perm_rows(4, false, M, n, m, inv_m, W0_new, inv_n, nullptr, nullptr, stream);
+  POETX_TRY(launch_invert_perms(L->perm_m, L->m, inv_m, L->perm_n, L->n, inv_n, stream));
+  // the first L->n rows and L->m columns of the padded M hold the map
+  return launch_perm_rows(4, false, M, L->n, L->m, inv_m, W0_new, inv_n, nullptr, nullptr,
+                          stream, m, L->m);
 }
 
 extern "C" size_t poetx_layer_saved_bytes(const poetx_layer* L, int N) {
@@ -371,7 +392,8 @@ static poetx_status layer_fwd_impl(const poetx_layer* L, const void* x, int N, v
     return POETX_ERR_ALIGN;
   const Plan p = make_plan(L, N);
   if (ws_bytes < p.fwd_total) return POETX_ERR_WORKSPACE;
-  const int b = L->b, m = L->m, n = L->n;
+  // m, n: the features of x and y; mP, nP: the padded widths of every internal array
+  const int b = L->b, m = L->m, n = L->n, mP = padded(m, b), nP = padded(n, b);
   const poetx_dtype act = L->act;
   const bool f32 = act == POETX_F32;
   const size_t as = dtype_size(act);
@@ -384,26 +406,28 @@ static poetx_status layer_fwd_impl(const poetx_layer* L, const void* x, int N, v
   // and Q^2 kept for the backward.  (Running the x gather beside them on the side stream
   // was measured: the CNP kernels slowed by about what the gather saved, and the join cost
   // the programmatic overlap of the next launch; so S3 follows them.)
-  const CnpSides sides{{L->q_R, L->q_P}, {m / b, n / b}};
+  const CnpSides sides = layer_sides(L);
   POETX_TRY(cnp_forward_sides(sides, b, at<float>(saved, p.Qs), at<float>(saved, p.Q2R),
                               f32 ? at<float>(saved, p.GR) : nullptr,
                               f32 ? nullptr : at(saved, p.GR), nullptr, stream));
   if (N == 0) return POETX_OK;
   if (hk.x_ready) POETX_CUDA_TRY(cudaStreamWaitEvent(stream, hk.x_ready, 0));
-  POETX_TRY(launch_perm_rows(as, false, x, N, m, L->perm_m, xt, nullptr, nullptr, nullptr, stream));
-  POETX_TRY(blockdiag_impl(act, xt, N, m / b, b, at(saved, p.GR), 0, nullptr, nullptr, A, stream));
+  POETX_TRY(launch_perm_rows(as, false, x, N, m, L->perm_m, xt, nullptr, nullptr, nullptr, stream,
+                             m, mP));
+  POETX_TRY(blockdiag_impl(act, xt, N, mP / b, b, at(saved, p.GR), 0, nullptr, nullptr, A, stream));
   void* zt = at(ws, p.f_zt);
   if (fused_ok(L, N, 0)) {
     // S5 + S6 on the same tiles (mem does not keep B)
-    POETX_TRY(umma_wprime_fused(A, N, m, n, L->Wp, 0, at(saved, p.GP), b,
+    POETX_TRY(umma_wprime_fused(A, N, mP, nP, L->Wp, 0, at(saved, p.GP), b,
                                 L->variant == POETX_FAST ? B : nullptr, zt, stream));
   } else {
-    POETX_TRY(wprime_impl(act, L->wdt, A, N, m, n, L->Wp, L->w_scale, 0, B, stream));
-    POETX_TRY(blockdiag_impl(act, B, N, n / b, b, at(saved, p.GP), 0, nullptr, nullptr, zt, stream));
+    POETX_TRY(wprime_impl(act, L->wdt, A, N, mP, nP, L->Wp, L->w_scale, 0, B, stream));
+    POETX_TRY(blockdiag_impl(act, B, N, nP / b, b, at(saved, p.GP), 0, nullptr, nullptr, zt, stream));
   }
   // S7.  (Storing z~ through the permutation inside the product is supported, but its
   // 2-byte scattered stores are slower than this coalesced scatter pass.)
-  return launch_perm_rows(as, true, zt, N, n, L->perm_n, y, nullptr, nullptr, nullptr, stream);
+  return launch_perm_rows(as, true, zt, N, n, L->perm_n, y, nullptr, nullptr, nullptr, stream,
+                          nP, n);
 }
 
 extern "C" poetx_status poetx_layer_fwd(const poetx_layer* L, const void* x, int N, void* y,
@@ -424,7 +448,7 @@ static poetx_status layer_bwd_impl(const poetx_layer* L, const void* x, const vo
     return POETX_ERR_ALIGN;
   const Plan p = make_plan(L, N);
   if (ws_bytes < p.bwd_total) return POETX_ERR_WORKSPACE;
-  const int b = L->b, m = L->m, n = L->n;
+  const int b = L->b, m = L->m, n = L->n, mP = padded(m, b), nP = padded(n, b);
   const poetx_dtype act = L->act;
   const size_t as = dtype_size(act);
   prof_begin(stream);
@@ -440,33 +464,34 @@ static poetx_status layer_bwd_impl(const poetx_layer* L, const void* x, const vo
   if (N > 0) {
     if (!fast)  // mem: x~ is recomputed
       POETX_TRY(launch_perm_rows(as, false, x, N, m, L->perm_m, at(ws, p.b_xt), nullptr, nullptr,
-                                 nullptr, stream));
+                                 nullptr, stream, m, mP));
     if (hk.dy_ready) POETX_CUDA_TRY(cudaStreamWaitEvent(stream, hk.dy_ready, 0));
-    POETX_TRY(launch_perm_rows(as, false, dy, N, n, L->perm_n, dzt, nullptr, nullptr, nullptr, stream));
+    POETX_TRY(launch_perm_rows(as, false, dy, N, n, L->perm_n, dzt, nullptr, nullptr, nullptr,
+                               stream, n, nP));
   }
   const void* B;
   if (L->variant == POETX_MEM) {  // recompute B = (x~ blkdiag(G_R)) W'^T
     void* A = at(ws, p.b_A);
     void* Bw = at(ws, p.b_B);
-    POETX_TRY(blockdiag_impl(act, xt, N, m / b, b, GR, 0, nullptr, nullptr, A, stream));
-    POETX_TRY(wprime_impl(act, L->wdt, A, N, m, n, L->Wp, L->w_scale, 0, Bw, stream));
+    POETX_TRY(blockdiag_impl(act, xt, N, mP / b, b, GR, 0, nullptr, nullptr, A, stream));
+    POETX_TRY(wprime_impl(act, L->wdt, A, N, mP, nP, L->Wp, L->w_scale, 0, Bw, stream));
     B = Bw;
   } else {
     B = at(saved, p.Bsv);
   }
-  POETX_TRY(wgrad_impl(act, B, dzt, N, n / b, b, p.splitsP, dGP, stream));
+  POETX_TRY(wgrad_impl(act, B, dzt, N, nP / b, b, p.splitsP, dGP, stream));
   // int8 weight: dA = dB diag(s) W_q, the row scale is folded into dB's columns
-  POETX_TRY(blockdiag_impl(act, dzt, N, n / b, b, GP, 1,
+  POETX_TRY(blockdiag_impl(act, dzt, N, nP / b, b, GP, 1,
                            L->wdt == POETX_I8 ? L->w_scale : nullptr, nullptr, dB, stream));
   void* dxt = at(ws, p.b_dxt);
   if (fused_ok(L, N, 1)) {
     // S11 + the dx~ half of S12 on the same tiles
-    POETX_TRY(umma_wprime_fused(dB, N, m, n, L->Wp, 1, GR, b, dA, dxt, stream));
+    POETX_TRY(umma_wprime_fused(dB, N, mP, nP, L->Wp, 1, GR, b, dA, dxt, stream));
   } else {
-    POETX_TRY(wprime_impl(act, L->wdt, dB, N, m, n, L->Wp, L->w_scale, 1, dA, stream));
-    POETX_TRY(blockdiag_impl(act, dA, N, m / b, b, GR, 1, nullptr, nullptr, dxt, stream));
+    POETX_TRY(wprime_impl(act, L->wdt, dB, N, mP, nP, L->Wp, L->w_scale, 1, dA, stream));
+    POETX_TRY(blockdiag_impl(act, dA, N, mP / b, b, GR, 1, nullptr, nullptr, dxt, stream));
   }
-  poetx_status st = wgrad_impl(act, xt, dA, N, m / b, b, p.splitsR, dGR, stream);
+  poetx_status st = wgrad_impl(act, xt, dA, N, mP / b, b, p.splitsR, dGR, stream);
   // S13 beside S14 when it can: the dx scatter does not feed the CNP backward.  It is
   // forked after the G_R weight gradient (a whole-GPU kernel that it would slow down), and
   // not when a download waits for dx (dx_done): the co-resident scatter is slower than the
@@ -481,16 +506,18 @@ static poetx_status layer_bwd_impl(const poetx_layer* L, const void* x, const vo
   if (sc) {
     POETX_CUDA_TRY(cudaEventRecord(sc->fork, stream));
     POETX_CUDA_TRY(cudaStreamWaitEvent(sc->ss, sc->fork, 0));
-    const poetx_status g = launch_perm_rows_side(as, true, dxt, N, m, L->perm_m, dx, sc->ss);
+    const poetx_status g = launch_perm_rows_side(as, true, dxt, N, m, L->perm_m, dx, sc->ss,
+                                                 mP, m);
     POETX_CUDA_TRY(cudaEventRecord(sc->join, sc->ss));
     POETX_TRY(g);
   } else if (st == POETX_OK && N > 0) {
-    st = launch_perm_rows(as, true, dxt, N, m, L->perm_m, dx, nullptr, nullptr, nullptr, stream);
+    st = launch_perm_rows(as, true, dxt, N, m, L->perm_m, dx, nullptr, nullptr, nullptr, stream,
+                          mP, m);
     if (st == POETX_OK && hk.dx_done && cudaEventRecord(hk.dx_done, stream) != cudaSuccess)
       st = POETX_ERR_CUDA;
   }
   if (st == POETX_OK) {
-    const CnpSides sides{{L->q_R, L->q_P}, {m / b, n / b}};
+    const CnpSides sides = layer_sides(L);
     const float* const dGs[2] = {dGR, dGP};
     const int splits[2] = {p.splitsR, p.splitsP};
     float* const dqs[2] = {dq_R, dq_P};
@@ -532,8 +559,8 @@ static StepPlan step_plan(const poetx_layer* L, long long N) {
   sp.dy = take(N * n * as);
   sp.y = take(N * n * as);
   sp.dx = take(N * m * as);
-  sp.dqR = take(m / b * (b * (b - 1) / 2) * 4);
-  sp.dqP = take(n / b * (b * (b - 1) / 2) * 4);
+  sp.dqR = take((m + b - 1) / b * (b * (b - 1) / 2) * 4);
+  sp.dqP = take((n + b - 1) / b * (b * (b - 1) / 2) * 4);
   sp.saved = take(p.saved_total);
   sp.ws_bytes = p.fwd_total > p.bwd_total ? p.fwd_total : p.bwd_total;
   sp.ws = take(sp.ws_bytes);
@@ -581,7 +608,8 @@ extern "C" poetx_status poetx_layer_step_host(const poetx_layer* L, const void* 
   const size_t as = dtype_size(L->act);
   const size_t m = L->m, n = L->n, b = L->b;
   const size_t xb = (size_t)N * m * as, yb = (size_t)N * n * as;
-  const size_t qRb = m / b * (b * (b - 1) / 2) * 4, qPb = n / b * (b * (b - 1) / 2) * 4;
+  const size_t qRb = (m + b - 1) / b * (b * (b - 1) / 2) * 4;
+  const size_t qPb = (n + b - 1) / b * (b * (b - 1) / 2) * 4;
   // the copy stream starts after the caller's earlier work (which may still use `dev`)
   POETX_CUDA_TRY(cudaEventRecord(c.ev[EV_START], stream));
   POETX_CUDA_TRY(cudaStreamWaitEvent(c.cs, c.ev[EV_START], 0));

@@ -114,8 +114,8 @@ def layer_inputs(wl: Workload, layer: LayerShape, N: int | None = None,
     """All inputs of one layer of a workload, as float64 / int32 numpy arrays.
 
     x [N,m] and dy [N,n] ~ N(0,1) in the activation dtype; W0 [n,m] ~ N(0, 1/m) (fp32 when
-    the layer stores int8 weights: that is the pre-quantisation weight); q_R [m/b, b(b-1)/2]
-    and q_P [n/b, b(b-1)/2] ~ N(0, q_std^2) in fp32; perm_m [m], perm_n [n] uniform.
+    the layer stores int8 weights: that is the pre-quantisation weight); q_R [ceil(m/b),
+    b(b-1)/2] and q_P [ceil(n/b), b(b-1)/2] ~ N(0, q_std^2) in fp32; perm_m [m], perm_n [n] uniform.
     ``N`` overrides the token count (a token prefix of the same draw is NOT implied: a
     different N gives a different draw).
     """
@@ -128,8 +128,8 @@ def layer_inputs(wl: Workload, layer: LayerShape, N: int | None = None,
         "x": gaussian(s, tag + f"x{N}", (N, m), 1.0, wl.act),
         "dy": gaussian(s, tag + f"dy{N}", (N, n), 1.0, wl.act),
         "W0": gaussian(s, tag + "W0", (n, m), 1.0 / np.sqrt(m), wstore),
-        "q_R": gaussian(s, tag + "qR", (m // b, tri), wl.q_std * q_scale, "f32"),
-        "q_P": gaussian(s, tag + "qP", (n // b, tri), wl.q_std * q_scale, "f32"),
+        "q_R": gaussian(s, tag + "qR", (-(-m // b), tri), wl.q_std * q_scale, "f32"),
+        "q_P": gaussian(s, tag + "qP", (-(-n // b), tri), wl.q_std * q_scale, "f32"),
         "perm_m": permutation(s, tag + "pm", m),
         "perm_n": permutation(s, tag + "pn", n),
     }

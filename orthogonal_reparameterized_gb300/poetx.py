@@ -65,6 +65,7 @@ _SIGS = {
     "poetx_perm_gather": (_i, [_i, _vp, _i, _i, _vp, _vp, _vp]),
     "poetx_perm_scatter": (_i, [_i, _vp, _i, _i, _vp, _vp, _vp]),
     "poetx_merge_perm": (_i, [_vp, _vp, _i, _i, _i, _vp, _vp, _vp, _vp, _vp]),
+    "poetx_merge_perm_padded": (_i, [_vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp]),
     "poetx_quantize_rows_int8": (_i, [_vp, _i, _i, _vp, _vp, _vp]),
     "poetx_blockdiag_mm": (_i, [_i, _vp, _i, _i, _i, _vp, _i, _vp, _vp, _vp, _vp]),
     "poetx_blockdiag_wgrad": (_i, [_i, _vp, _vp, _i, _i, _i, _i, _vp, _vp]),
@@ -239,6 +240,16 @@ def poetx_merge_perm(W0, perm_n, perm_m, Wp, scale=None, scale_p=None, stream=No
     _check("poetx_merge_perm", lib().poetx_merge_perm(_p(W0), _p(scale), dtype_code(W0), n, m,
                                                       _p(perm_n), _p(perm_m), _p(Wp), _p(scale_p),
                                                       _stream(stream)))
+
+
+def poetx_merge_perm_padded(W0, perm_n, perm_m, Wp, scale=None, scale_p=None, stream=None):
+    """Wp [n_pad, m_pad] (its shape gives the padding) <- the merge of W0 [n, m], zero
+    elsewhere; scale_p [n_pad] likewise for int8."""
+    n, m = W0.shape
+    n_pad, m_pad = Wp.shape
+    _check("poetx_merge_perm_padded", lib().poetx_merge_perm_padded(
+        _p(W0), _p(scale), dtype_code(W0), n, m, n_pad, m_pad, _p(perm_n), _p(perm_m), _p(Wp),
+        _p(scale_p), _stream(stream)))
 
 
 def poetx_quantize_rows_int8(W, Wq, scale, stream=None):

@@ -76,7 +76,11 @@ def test_layer_sizes_host_logic(P):
         P.poetx_layer_workspace_bytes(L, N, 1)
     # invalid descriptors report 0 bytes
     assert P.poetx_layer_workspace_bytes(_desc(P, b=100), N, 0) == 0        # b not supported
-    assert P.poetx_layer_workspace_bytes(_desc(P, m=320, b=128), N, 0) == 0  # b does not divide m
+    # b does not divide m: a ragged last block, padded inside (m multiple of 8 needed)
+    rag = P.poetx_layer_workspace_bytes(_desc(P, m=320, b=128), N, 0)
+    assert rag >= N * (384 + 512) * 2                                     # A, z~ padded
+    assert P.poetx_layer_workspace_bytes(_desc(P, m=324, b=128), N, 0) == 0
+    assert P.poetx_layer_saved_bytes(_desc(P, m=320, b=128), N) >= N * (384 + 512) * 2
     assert P.poetx_layer_workspace_bytes(_desc(P, order=4), N, 0) == 0
     assert P.poetx_layer_workspace_bytes(_desc(P, wdt=P.I8), N, 0) == 0      # int8 needs mem
     assert P.poetx_layer_workspace_bytes(_desc(P, wdt=P.I8, variant=P.MEM), N, 0) > 0
@@ -168,3 +172,16 @@ def test_step_host_sizes_and_argument_errors(P):
                                      fake, 1 << 40, None) == 6
     assert lib.poetx_layer_step_host(ctypes.byref(L), *args[:2], -1, *args[2:], fake, 1 << 40,
                                      None) == 1
+
+
+def test_merge_perm_padded_argument_errors(P):
+    lib = P.lib()
+    fake = ctypes.c_void_p(4096)
+    f = lib.poetx_merge_perm_padded
+    assert f(fake, None, P.BF16, 8, 8, 4, 8, fake, fake, fake, None, None) == 1   # n_pad < n
+    assert f(fake, None, P.BF16, 8, 12, 8, 16, fake, fake, fake, None, None) == 2  # 24-byte rows
+    assert f(fake, None, P.BF16, 8, 8, 8, 8, fake, fake, ctypes.c_void_p(4100), None,
+             None) == 4                                                            # Wp unaligned
+    assert f(fake, fake, P.I8, 6, 16, 8, 16, fake, fake, fake, fake, None) == 2    # int8: n % 4
+    assert f(fake, None, P.I8, 8, 16, 8, 16, fake, fake, fake, fake, None) == 1    # no scale
+    assert f(fake, None, 9, 8, 8, 8, 8, fake, fake, fake, None, None) == 3         # dtype

@@ -85,6 +85,31 @@ def test_merge_perm_bit_exact(P, dtype, n, m):
         np.testing.assert_array_equal(host(sp), host(s)[pn])
 
 
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32, torch.int8])
+@pytest.mark.parametrize("n,m,n_pad,m_pad", [(200, 144, 256, 192), (72, 2048, 128, 2048),
+                                             (512, 48, 512, 64)])
+def test_merge_perm_padded_bit_exact(P, dtype, n, m, n_pad, m_pad):
+    """The merge into a zero-padded weight (ragged last blocks): the [n, m] corner is the
+    plain merge, every padding row, column and scale is 0 (the buffers start as garbage)."""
+    pn, pm = RNG.permutation(n), RNG.permutation(m)
+    if dtype == torch.int8:
+        W = torch.randint(-127, 128, (n, m), dtype=torch.int8, device=DEV)
+        s = torch.rand(n, device=DEV)
+        sp = torch.full((n_pad,), float("nan"), device=DEV)
+        Wp = torch.full((n_pad, m_pad), 5, dtype=torch.int8, device=DEV)
+    else:
+        W = torch.randn(n, m, device=DEV).to(dtype)
+        s = sp = None
+        Wp = torch.full((n_pad, m_pad), float("nan"), device=DEV).to(dtype)
+    P.poetx_merge_perm_padded(W, dev(pn, torch.int32), dev(pm, torch.int32), Wp, s, sp)
+    ref = np.zeros((n_pad, m_pad))
+    ref[:n, :m] = O.merge_perm(host(W), pn, pm)
+    np.testing.assert_array_equal(host(Wp), ref)
+    if s is not None:
+        np.testing.assert_array_equal(host(sp)[:n], host(s)[pn])
+        assert np.all(host(sp)[n:] == 0)
+
+
 @pytest.mark.parametrize("n,m", [(7, 33), (64, 4096), (13824, 5120)])
 def test_quantize_bit_exact(P, n, m):
     W = (RNG.standard_normal((n, m)) / np.sqrt(m)).astype(np.float32)

@@ -18,6 +18,8 @@ def run_layer(P, inp, b, act, wdt, variant, dy=None, q_zero=False, accumulate_in
     """Runs fwd + bwd through the C ABI; returns host arrays and the effective W0 that the
     oracle must use (the GPU quantiser's own output for int8 weights)."""
     m, n = inp["W0"].shape[1], inp["W0"].shape[0]
+    m_pad, n_pad = -(-m // b) * b, -(-n // b) * b
+    ragged = (m_pad, n_pad) != (m, n)
     adt = TDT[act]
     x = dev(inp["x"], adt)
     dyt = dev(inp["dy"] if dy is None else dy, adt)
@@ -31,15 +33,24 @@ def run_layer(P, inp, b, act, wdt, variant, dy=None, q_zero=False, accumulate_in
         Wq = torch.empty(n, m, dtype=torch.int8, device=DEV)
         s = torch.empty(n, device=DEV)
         P.poetx_quantize_rows_int8(W32, Wq, s)
-        Wp = torch.empty_like(Wq)
-        w_scale = torch.empty_like(s)
-        P.poetx_merge_perm(Wq, pn, pm, Wp, s, w_scale)
+        if ragged:
+            Wp = torch.full((n_pad, m_pad), 7, dtype=torch.int8, device=DEV)
+            w_scale = torch.full((n_pad,), float("nan"), device=DEV)
+            P.poetx_merge_perm_padded(Wq, pn, pm, Wp, s, w_scale)
+        else:
+            Wp = torch.empty_like(Wq)
+            w_scale = torch.empty_like(s)
+            P.poetx_merge_perm(Wq, pn, pm, Wp, s, w_scale)
         W_eff = O.dequantize_rows(host(Wq), host(s))
         wcode = P.I8
     else:
         W0 = dev(inp["W0"], TDT[wdt])
-        Wp = torch.empty_like(W0)
-        P.poetx_merge_perm(W0, pn, pm, Wp)
+        if ragged:  # padding filled with NaN first: it must be overwritten with zeros
+            Wp = torch.full((n_pad, m_pad), float("nan"), dtype=TDT[wdt], device=DEV)
+            P.poetx_merge_perm_padded(W0, pn, pm, Wp)
+        else:
+            Wp = torch.empty_like(W0)
+            P.poetx_merge_perm(W0, pn, pm, Wp)
         W_eff = inp["W0"]
         wcode = P.F32 if wdt == "f32" else P.BF16
     acode = P.F32 if act == "f32" else P.BF16
@@ -247,6 +258,7 @@ def _step_host(P, inp, b, act, wdt, variant, pinned=True):
     """poetx_layer_step_host with host tensors; the layer descriptor is built as run_layer
     builds it (same weights, permutations and q)."""
     m, n = inp["W0"].shape[1], inp["W0"].shape[0]
+    m_pad, n_pad = -(-m // b) * b, -(-n // b) * b
     adt = TDT[act]
     pm = dev(inp["perm_m"], torch.int32)
     pn = dev(inp["perm_n"], torch.int32)
@@ -257,14 +269,14 @@ def _step_host(P, inp, b, act, wdt, variant, pinned=True):
         Wq = torch.empty(n, m, dtype=torch.int8, device=DEV)
         s = torch.empty(n, device=DEV)
         P.poetx_quantize_rows_int8(dev(inp["W0"], torch.float32), Wq, s)
-        Wp = torch.empty_like(Wq)
-        w_scale = torch.empty_like(s)
-        P.poetx_merge_perm(Wq, pn, pm, Wp, s, w_scale)
+        Wp = torch.empty(n_pad, m_pad, dtype=torch.int8, device=DEV)
+        w_scale = torch.empty(n_pad, device=DEV)
+        P.poetx_merge_perm_padded(Wq, pn, pm, Wp, s, w_scale)
         wcode = P.I8
     else:
         W0 = dev(inp["W0"], TDT[wdt])
-        Wp = torch.empty_like(W0)
-        P.poetx_merge_perm(W0, pn, pm, Wp)
+        Wp = torch.empty(n_pad, m_pad, dtype=W0.dtype, device=DEV)
+        P.poetx_merge_perm_padded(W0, pn, pm, Wp)
         wcode = P.F32 if wdt == "f32" else P.BF16
     acode = P.F32 if act == "f32" else P.BF16
     L = P.make_layer(m, n, b, acode, wcode, P.FAST if variant == "fast" else P.MEM, pm, pn, Wp,
@@ -383,3 +395,47 @@ def test_overlapped_step_in_a_cuda_graph(P):
     got = {"y": host(y), "dx": host(dx), "dq_R": host(dqR), "dq_P": host(dqP)}
     for k in got:
         np.testing.assert_array_equal(got[k], ref[k], err_msg=k)
+
+
+@pytest.mark.parametrize("act,wdt,variant,shape", [
+    ("bf16", "bf16", "fast", (200, 328, 64, 150)),     # last blocks of 8 on both sides
+    ("bf16", "bf16", "mem", (200, 328, 64, 150)),
+    ("bf16", "bf16", "fast", (2000, 1000, 256, 300)),  # last blocks of 208 and 232
+    ("bf16", "bf16", "mem", (1016, 2040, 128, 260)),   # 120 and 120
+    ("bf16", "bf16", "fast", (512, 776, 256, 77)),     # m whole, n ragged (8)
+    ("bf16", "i8", "mem", (528, 776, 256, 150)),       # int8 rows: m % 16 == 0
+    ("f32", "f32", "fast", (200, 136, 32, 64)),        # fp32: last blocks of 8
+    ("f32", "f32", "mem", (104, 96, 64, 33)),
+])
+def test_layer_ragged_last_block(P, act, wdt, variant, shape):
+    """ceil(d/b) blocks with a ragged last one (padded inside the layer) against the oracle
+    written per block with its own size; the non-parameter entries of dq are exactly 0."""
+    m, n, b, N = shape
+    inp = inputs.small_layer_inputs(97 + b + m % 97, m, n, b, N, act=act, wdt=wdt)
+    got = run_layer(P, inp, b, act, wdt, variant)
+    ref = O.poetx_layer_ragged(inp["x"], inp["dy"], got["W_eff"], inp["perm_m"], inp["perm_n"],
+                               inp["q_R"], inp["q_P"], b)
+    check(got, ref, TOL_F32 if act == "f32" else TOL_BF16_LAYER)
+    for key, d in (("dq_R", m), ("dq_P", n)):
+        r = d - (-(-d // b) - 1) * b
+        if r < b:
+            last = got[key][-1]
+            mask = np.zeros(b * (b - 1) // 2, dtype=bool)
+            k = 0
+            for i in range(b):
+                for j in range(i + 1, b):
+                    mask[k] = j >= r
+                    k += 1
+            assert np.all(last[mask] == 0), key
+
+
+def test_layer_ragged_fast_mem_equal_and_step_host(P):
+    """fast and mem bit-identical on a ragged layer, and the host-buffer step too."""
+    m, n, b, N = 1016, 520, 128, 200
+    inp = inputs.small_layer_inputs(101, m, n, b, N, act="bf16", wdt="bf16")
+    a = run_layer(P, inp, b, "bf16", "bf16", "fast")
+    c = run_layer(P, inp, b, "bf16", "bf16", "mem")
+    h = _step_host(P, inp, b, "bf16", "bf16", "fast")
+    for k in ("y", "dx", "dq_R", "dq_P"):
+        np.testing.assert_array_equal(a[k], c[k], err_msg=k)
+        np.testing.assert_array_equal(a[k], h[k], err_msg=k)

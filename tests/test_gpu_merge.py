@@ -17,6 +17,7 @@ TDT = {"f32": torch.float32, "bf16": torch.bfloat16}
 
 def _layer_on_gpu(P, inp, b, act, wdt, variant="fast"):
     m, n = inp["W0"].shape[1], inp["W0"].shape[0]
+    m_pad, n_pad = -(-m // b) * b, -(-n // b) * b
     keep = {}
     pm = dev(inp["perm_m"], torch.int32)
     pn = dev(inp["perm_n"], torch.int32)
@@ -27,15 +28,15 @@ def _layer_on_gpu(P, inp, b, act, wdt, variant="fast"):
         Wq = torch.empty(n, m, dtype=torch.int8, device=DEV)
         s = torch.empty(n, device=DEV)
         P.poetx_quantize_rows_int8(dev(inp["W0"], torch.float32), Wq, s)
-        Wp = torch.empty_like(Wq)
-        w_scale = torch.empty_like(s)
-        P.poetx_merge_perm(Wq, pn, pm, Wp, s, w_scale)
+        Wp = torch.empty(n_pad, m_pad, dtype=torch.int8, device=DEV)
+        w_scale = torch.empty(n_pad, device=DEV)
+        P.poetx_merge_perm_padded(Wq, pn, pm, Wp, s, w_scale)
         W_eff = O.dequantize_rows(host(Wq), host(s))
         wcode = P.I8
     else:
         W0 = dev(inp["W0"], TDT[wdt])
-        Wp = torch.empty_like(W0)
-        P.poetx_merge_perm(W0, pn, pm, Wp)
+        Wp = torch.empty(n_pad, m_pad, dtype=W0.dtype, device=DEV)
+        P.poetx_merge_perm_padded(W0, pn, pm, Wp)
         W_eff = host(W0)
         wcode = P.F32 if wdt == "f32" else P.BF16
     acode = P.F32 if act == "f32" else P.BF16
@@ -130,3 +131,21 @@ def test_merge_reinit_argument_errors(P):
                                   ctypes.c_void_p(ws.data_ptr()), need - 1, None) == 5
     assert lib.poetx_merge_reinit(ctypes.byref(L), None, ctypes.c_void_p(ws.data_ptr()), need,
                                   None) == 1
+
+
+@pytest.mark.parametrize("m,n,b,act,wdt", [
+    (200, 136, 64, "bf16", "bf16"),     # last blocks of 8 on both sides
+    (1016, 520, 128, "bf16", "bf16"),
+    (528, 776, 256, "bf16", "i8"),      # int8 rows: m % 16 == 0
+    (104, 96, 32, "f32", "f32"),
+])
+def test_merge_reinit_ragged_matches_oracle(P, m, n, b, act, wdt):
+    """Ragged last blocks: W0_new is the ragged layer's map (its response to the identity,
+    the oracle written per block with its own size)."""
+    inp = inputs.small_layer_inputs(700 + m + b, m, n, b, 4, act=act, wdt=wdt)
+    variant = "mem" if wdt == "i8" else "fast"
+    L, keep, W_eff = _layer_on_gpu(P, inp, b, act, wdt, variant)
+    got = host(_merge(P, L, n, m))
+    ref = O.poetx_layer_ragged(np.eye(m), np.zeros((m, n)), W_eff, inp["perm_m"],
+                               inp["perm_n"], inp["q_R"], inp["q_P"], b)["y"].T
+    assert O.rel_fro(got, ref) <= TOL_F32
