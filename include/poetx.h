@@ -365,6 +365,21 @@ typedef struct poetx_adam {
 poetx_status poetx_adam_triu(float* q, const float* dq, float* m, float* v, long long count,
                              const poetx_adam* hp, cudaStream_t stream);
 
+/* poetx_layer_bwd followed by the optimizer step above on both sides, the update applied by
+ * the gradient-pack kernel as it writes each dq entry (one launch fewer; for single-replica
+ * training, where nothing is summed between the gradient and the update).  Updates
+ * L->q_R and L->q_P IN PLACE (the descriptor's const pointers are written: they must point
+ * to writable device memory), with m_R, v_R [ceil(m/b), b(b-1)/2] and m_P, v_P
+ * [ceil(n/b), b(b-1)/2] the fp32 Adam state (zero at step 1; device, 16-byte aligned).
+ * dq_R, dq_P are written as by poetx_layer_bwd (with accumulate != 0 the update uses the
+ * accumulated gradient).  The result equals poetx_layer_bwd + poetx_adam_triu bit for bit.
+ * Errors: those of poetx_layer_bwd and poetx_adam_triu's, before any launch. */
+poetx_status poetx_layer_bwd_adam(const poetx_layer* L, const void* x, const void* dy, int N,
+                                  const void* saved, void* dx, float* dq_R, float* dq_P,
+                                  int accumulate, const poetx_adam* hp, float* m_R, float* v_R,
+                                  float* m_P, float* v_P, void* ws, size_t ws_bytes,
+                                  cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -303,7 +303,8 @@ poetx_status cnp_forward(const float* q, int nblk, int b, float* Qs, float* Q2, 
 
 poetx_status cnp_backward_sides(const CnpSides& q, const float* Qin, const float* Q2in,
                                 const float* const dG[2], const int splits[2], int b,
-                                float* const dq[2], int accumulate, void* scratch, cudaStream_t s) {
+                                float* const dq[2], int accumulate, void* scratch, cudaStream_t s,
+                                const PackAdam* pa) {
   const int nblk = q.n[0] + q.n[1];
   if (nblk == 0) return POETX_OK;
   char* w = static_cast<char*>(scratch);
@@ -381,7 +382,7 @@ poetx_status cnp_backward_sides(const CnpSides& q, const float* Qin, const float
   r.out_f32 = Qbar;
   POETX_TRY(launch_cnp_gemm(r, nblk, ST_CNP_QBAR, s));
   return launch_triu_grad_pack2(Qbar, q.n[0], q.n[1], b, dq[0], dq[1], accumulate, s,
-                                q.last[0], q.last[1]);
+                                q.last[0], q.last[1], pa);
 }
 
 }  // namespace poetx

@@ -8,6 +8,7 @@
 // two permutations into W once per inner loop) and section 4 (upper-triangle storage).
 #include <mutex>
 
+#include "adam.cuh"
 #include "common.cuh"
 #include "kernels.h"
 
@@ -83,9 +84,12 @@ __global__ void triu_unpack_kernel(const float* __restrict__ q0, int n0, const f
 // block: the mirrored tile Qbar[J][I] is read with coalesced rows into shared memory and
 // read back transposed, so both reads of Qbar are coalesced; the writes of a row i of the
 // tile are consecutive entries of the packed triangle.
+// pa (nullable q): the optimizer update applied to each entry as its gradient is written
+// (single-replica training: nothing has to be summed between the pack and the update).
 __global__ void triu_grad_pack_kernel(const float* __restrict__ Qbar, int b, float* __restrict__ dq0,
                                       int n0, float* __restrict__ dq1, int accumulate, int r0,
-                                      int r1, unsigned long long* tr, size_t tr_cap) {
+                                      int r1, PackAdam pa, unsigned long long* tr,
+                                      size_t tr_cap) {
   if (threadIdx.x == 0 && threadIdx.y == 0) trace_stamp3(tr, tr_cap, 0);
   pdl_trigger();
   pdl_wait();
@@ -101,6 +105,8 @@ __global__ void triu_grad_pack_kernel(const float* __restrict__ Qbar, int b, flo
   const long long tri = (long long)b * (b - 1) / 2;
   const float* Qb = Qbar + (long long)blk * b * b;
   float* dqb = blk < n0 ? dq0 + blk * tri : dq1 + (blk - n0) * tri;
+  const int side = blk < n0 ? 0 : 1;
+  const long long off = (long long)(blk < n0 ? blk : blk - n0) * tri;  // this block's entries
   const int rv = block_valid(blk, n0, r0, r1, b);
   const int tx = threadIdx.x, ty = threadIdx.y;  // 32 x 8
   for (int r = ty; r < 32; r += 8) {  // tile[r][c] = Qbar[J*32 + r][I*32 + c]
@@ -112,8 +118,14 @@ __global__ void triu_grad_pack_kernel(const float* __restrict__ Qbar, int b, flo
     const int i = I * 32 + r, j = J * 32 + tx;
     if (i < j && j < b) {
       const float v = j < rv ? Qb[(long long)i * b + j] - tile[tx][r] : 0.f;
-      float* dst = dqb + tri_index(i, j, b);
-      *dst = accumulate ? *dst + v : v;
+      const long long k = tri_index(i, j, b);
+      float* dst = dqb + k;
+      const float g = accumulate ? *dst + v : v;
+      *dst = g;
+      if (pa.q[side]) {
+        const long long e = off + k;
+        adam_one(pa.q[side][e], g, pa.m[side][e], pa.v[side][e], pa.h);
+      }
     }
   }
   if (tr) {
@@ -141,14 +153,17 @@ poetx_status launch_triu_unpack(const float* q, int nblk, int b, float* Q, cudaS
 }
 
 poetx_status launch_triu_grad_pack2(const float* Qbar, int n0, int n1, int b, float* dq0, float* dq1,
-                                    int accumulate, cudaStream_t s, int r0, int r1) {
+                                    int accumulate, cudaStream_t s, int r0, int r1,
+                                    const PackAdam* pa) {
   if (n0 + n1 == 0 || b < 2) return POETX_OK;
   const int nt = (b + 31) / 32;
   dim3 grid(nt * (nt + 1) / 2, 1, n0 + n1);
   size_t tr_cap = 0;
   unsigned long long* tr = trace_buffer(&tr_cap);
+  PackAdam none{};
   POETX_CUDA_TRY(launch_pdl(triu_grad_pack_kernel, grid, dim3(32, 8), 0, s, Qbar, b, dq0, n0,
-                            dq1, accumulate, r0 > 0 ? r0 : b, r1 > 0 ? r1 : b, tr, tr_cap));
+                            dq1, accumulate, r0 > 0 ? r0 : b, r1 > 0 ? r1 : b, pa ? *pa : none,
+                            tr, tr_cap));
   POETX_CUDA_TRY(cudaGetLastError());
   after_launch(s, ST_TRIU_PACK);
   return POETX_OK;
@@ -235,7 +250,9 @@ __device__ __forceinline__ bool group_all(bool v, int g, int G) {
 
 constexpr int kPermWarps = 8;  // consumer warps; one more warp issues the row copies
 
-template <int E, bool SCATTER, typename IdxT>
+// PITCHED: rows of the source or the destination are wider than D (a padded layer side);
+// the common case keeps the plain row arithmetic.
+template <int E, bool SCATTER, typename IdxT, bool PITCHED>
 __global__ void __launch_bounds__((kPermWarps + 1) * 32) perm_rows_kernel(
     const uint8_t* __restrict__ X, long long N, int D, const int32_t* __restrict__ perm,
     uint8_t* __restrict__ Y, const int32_t* __restrict__ src_rows, const float* __restrict__ scale,
@@ -299,8 +316,8 @@ __global__ void __launch_bounds__((kPermWarps + 1) * 32) perm_rows_kernel(
           const long long r = first + gr + (long long)it * stride;
           const long long sr = src_rows ? (long long)__ldg(src_rows + r) : r;
           mbar_arrive_expect_tx(&full[slot], row_bytes);
-          bulk_load(ring + (size_t)slot * row_bytes, X + sr * src_pitch * E, row_bytes,
-                    &full[slot]);
+          bulk_load(ring + (size_t)slot * row_bytes,
+                    X + (PITCHED ? sr * src_pitch * E : sr * row_bytes), row_bytes, &full[slot]);
           issued[gr] = it + 1;
         }
         if (it == 0) trace_stamp(trace, trace_cap, 2);  // slot 2: first row of every group issued
@@ -330,7 +347,6 @@ __global__ void __launch_bounds__((kPermWarps + 1) * 32) perm_rows_kernel(
     if (threadIdx.x == 0) trace_stamp(trace, trace_cap, 3);  // slot 3: index staged
     const int nrows = rows_of(g);
     const int nvec = D / V;
-    const int nvec_dst = (int)(dst_pitch / V);
     const int gthreads = G * 32;
     int k = 0;
     uint32_t ph = 0;
@@ -341,7 +357,7 @@ __global__ void __launch_bounds__((kPermWarps + 1) * 32) perm_rows_kernel(
       if (threadIdx.x == 0 && it < 13) trace_stamp(trace, trace_cap, 4 + 2 * it);  // landed
       const long long r = first + g + (long long)it * stride;
       const T* row = reinterpret_cast<const T*>(ring + (size_t)slot * row_bytes);
-      uint4* out = reinterpret_cast<uint4*>(Y + r * dst_pitch * E);
+      uint4* out = reinterpret_cast<uint4*>(Y + (PITCHED ? r * dst_pitch * E : r * row_bytes));
 #pragma unroll 4
       for (int v = tig; v < nvec; v += gthreads) {
         const IdxVec<IdxT, V> ix = load_idx<IdxT, V>(idx + (size_t)v * V);
@@ -351,7 +367,9 @@ __global__ void __launch_bounds__((kPermWarps + 1) * 32) perm_rows_kernel(
         out[v] = pk.u;
       }
       // columns D .. dst_pitch - 1 of a padded destination row (ragged last block) are zero
-      for (int v = nvec + tig; v < nvec_dst; v += gthreads) out[v] = make_uint4(0, 0, 0, 0);
+      if constexpr (PITCHED)
+        for (int v = nvec + tig; v < (int)(dst_pitch / V); v += gthreads)
+          out[v] = make_uint4(0, 0, 0, 0);
       if (scale_out && tig == 0) scale_out[r] = scale[src_rows ? src_rows[r] : r];
       group_sync(g, G);  // every thread of the group is done with buffer k
       if (threadIdx.x == 0 && it < 13) trace_stamp(trace, trace_cap, 5 + 2 * it);  // row done
@@ -410,7 +428,7 @@ static bool perm_shape_side(size_t row_bytes, size_t idx_bytes, int* G, int* S, 
   return true;
 }
 
-template <int E, bool SCATTER, typename IdxT>
+template <int E, bool SCATTER, typename IdxT, bool PITCHED>
 static poetx_status launch_perm_rows_t(const void* X, long long N, int D, const int32_t* perm,
                                        void* Y, const int32_t* src_rows, const float* scale,
                                        float* scale_out, long long sp, long long dp, bool side,
@@ -421,7 +439,7 @@ static poetx_status launch_perm_rows_t(const void* X, long long N, int D, const 
   size_t smem = 0;
   if (!(side ? perm_shape_side : perm_shape)(row_bytes, idx_bytes, &G, &S, &smem))
     return POETX_ERR_SHAPE;
-  auto k = perm_rows_kernel<E, SCATTER, IdxT>;
+  auto k = perm_rows_kernel<E, SCATTER, IdxT, PITCHED>;
   static std::once_flag once;  // the opt-in limit is set once, to the largest size used
   static cudaError_t attr = cudaSuccess;
   std::call_once(once, [&] {
@@ -463,12 +481,16 @@ static poetx_status launch_perm_rows_e(bool scatter, const void* X, long long N,
                                        const int32_t* perm, void* Y, const int32_t* src_rows,
                                        const float* scale, float* scale_out, long long sp,
                                        long long dp, bool side, cudaStream_t s) {
+#define POETX_PERM_T(SC, IT, PI) \
+  launch_perm_rows_t<E, SC, IT, PI>(X, N, D, perm, Y, src_rows, scale, scale_out, sp, dp, side, s)
+  const bool pitched = sp != D || dp != D;
   if (D <= 65535) {
-    return scatter ? launch_perm_rows_t<E, true, uint16_t>(X, N, D, perm, Y, src_rows, scale, scale_out, sp, dp, side, s)
-                   : launch_perm_rows_t<E, false, uint16_t>(X, N, D, perm, Y, src_rows, scale, scale_out, sp, dp, side, s);
+    if (pitched) return scatter ? POETX_PERM_T(true, uint16_t, true) : POETX_PERM_T(false, uint16_t, true);
+    return scatter ? POETX_PERM_T(true, uint16_t, false) : POETX_PERM_T(false, uint16_t, false);
   }
-  return scatter ? launch_perm_rows_t<E, true, uint32_t>(X, N, D, perm, Y, src_rows, scale, scale_out, sp, dp, side, s)
-                 : launch_perm_rows_t<E, false, uint32_t>(X, N, D, perm, Y, src_rows, scale, scale_out, sp, dp, side, s);
+  if (pitched) return scatter ? POETX_PERM_T(true, uint32_t, true) : POETX_PERM_T(false, uint32_t, true);
+  return scatter ? POETX_PERM_T(true, uint32_t, false) : POETX_PERM_T(false, uint32_t, false);
+#undef POETX_PERM_T
 }
 
 // sp, dp: source and destination row pitches in elements (0: D).  The D permuted columns

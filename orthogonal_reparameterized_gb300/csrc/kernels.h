@@ -6,6 +6,7 @@
 #include <stdint.h>
 
 #include "../../include/poetx.h"
+#include "adam.cuh"
 
 namespace poetx {
 
@@ -16,8 +17,10 @@ poetx_status launch_triu_unpack(const float* q, int nblk, int b, float* Q, cudaS
 // block outside its r x r corner are zero in Q and get zero gradient.
 poetx_status launch_triu_unpack2(const float* q0, int n0, const float* q1, int n1, int b, float* Q,
                                  cudaStream_t s, int r0 = 0, int r1 = 0);
+// pa (nullable): the optimizer update applied as each dq entry is written.
 poetx_status launch_triu_grad_pack2(const float* Qbar, int n0, int n1, int b, float* dq0, float* dq1,
-                                    int accumulate, cudaStream_t s, int r0 = 0, int r1 = 0);
+                                    int accumulate, cudaStream_t s, int r0 = 0, int r1 = 0,
+                                    const PackAdam* pa = nullptr);
 poetx_status launch_triu_grad_pack(const float* Qbar, int nblk, int b, float* dq, int accumulate,
                                    cudaStream_t s);
 // Y[r][j] = X[src_rows ? src_rows[r] : r][perm[j]] (gather) or Y[r][perm[j]] = X[r][j]
@@ -85,10 +88,16 @@ poetx_status cnp_forward_sides(const CnpSides& q, int b, float* Qs, float* Q2, f
 // Backward CNP.  Q and Q2 may be the stacks kept from the forward, or NULL to recompute
 // them into the scratch; dG[side] is [splits[side], n[side], b, b]; dq[side] receives that
 // side's gradient.  scratch holds cnp_bwd_scratch_bytes(n[0] + n[1], b) bytes.
+// pa (nullable): the optimizer update of both sides applied by the gradient pack.
 poetx_status cnp_backward_sides(const CnpSides& q, const float* Q, const float* Q2,
                                 const float* const dG[2], const int splits[2], int b,
                                 float* const dq[2], int accumulate, void* scratch,
-                                cudaStream_t s);
+                                cudaStream_t s, const PackAdam* pa = nullptr);
+
+// ---- optim.cu
+// Adam hyperparameters for the kernels (bias corrections in fp64 on the host);
+// POETX_ERR_ARG for step < 1 or betas outside [0, 1).
+poetx_status adam_params(const poetx_adam* hp, AdamK* h);
 
 // ---- layer.cu: engine switch (tensor cores unless disabled by poetx_set_gemm_engine)
 bool use_tensor_cores();

@@ -439,7 +439,7 @@ extern "C" poetx_status poetx_layer_fwd(const poetx_layer* L, const void* x, int
 static poetx_status layer_bwd_impl(const poetx_layer* L, const void* x, const void* dy, int N,
                                    const void* saved, void* dx, float* dq_R, float* dq_P,
                                    int accumulate, void* ws, size_t ws_bytes, cudaStream_t stream,
-                                   const StepHooks& hk) {
+                                   const StepHooks& hk, const PackAdam* pa = nullptr) {
   POETX_TRY(validate(L));
   if (N < 0) return POETX_ERR_ARG;
   if (!saved || !ws || !dq_R || !dq_P || (N > 0 && (!x || !dy || !dx))) return POETX_ERR_ARG;
@@ -522,7 +522,7 @@ static poetx_status layer_bwd_impl(const poetx_layer* L, const void* x, const vo
     const int splits[2] = {p.splitsR, p.splitsP};
     float* const dqs[2] = {dq_R, dq_P};
     st = cnp_backward_sides(sides, at<float>(saved, p.Qs), at<float>(saved, p.Q2R), dGs, splits,
-                            b, dqs, accumulate, at(ws, p.b_cnp), stream);
+                            b, dqs, accumulate, at(ws, p.b_cnp), stream, pa);
   }
   if (sc && cudaStreamWaitEvent(stream, sc->join, 0) != cudaSuccess && st == POETX_OK)
     st = POETX_ERR_CUDA;
@@ -535,6 +535,29 @@ extern "C" poetx_status poetx_layer_bwd(const poetx_layer* L, const void* x, con
                                         cudaStream_t stream) {
   return layer_bwd_impl(L, x, dy, N, saved, dx, dq_R, dq_P, accumulate, ws, ws_bytes, stream,
                         StepHooks{});
+}
+
+extern "C" poetx_status poetx_layer_bwd_adam(const poetx_layer* L, const void* x, const void* dy,
+                                             int N, const void* saved, void* dx, float* dq_R,
+                                             float* dq_P, int accumulate, const poetx_adam* hp,
+                                             float* m_R, float* v_R, float* m_P, float* v_P,
+                                             void* ws, size_t ws_bytes, cudaStream_t stream) {
+  POETX_TRY(validate(L));
+  PackAdam pa{};
+  POETX_TRY(adam_params(hp, &pa.h));
+  if (!m_R || !v_R || !m_P || !v_P) return POETX_ERR_ARG;
+  if (!aligned16(m_R) || !aligned16(v_R) || !aligned16(m_P) || !aligned16(v_P))
+    return POETX_ERR_ALIGN;
+  // the optimizer writes the layer's parameters in place (nothing after the gradient pack
+  // reads them in this call; the CNP backward works from the unpacked Q of the forward)
+  pa.q[0] = const_cast<float*>(L->q_R);
+  pa.q[1] = const_cast<float*>(L->q_P);
+  pa.m[0] = m_R;
+  pa.v[0] = v_R;
+  pa.m[1] = m_P;
+  pa.v[1] = v_P;
+  return layer_bwd_impl(L, x, dy, N, saved, dx, dq_R, dq_P, accumulate, ws, ws_bytes, stream,
+                        StepHooks{}, &pa);
 }
 
 // ---------------------------------------------------------------- host-buffer step

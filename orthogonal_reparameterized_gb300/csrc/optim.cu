@@ -5,25 +5,27 @@
 // ("Practical guidance" 3) is the caller's, folded into lr.
 #include <cmath>
 
+#include "adam.cuh"
 #include "common.cuh"
 #include "kernels.h"
 
 namespace poetx {
 
-namespace {
-
-struct AdamK {
-  float lr, beta1, beta2, eps, wd;
-  float c1, c2;  // 1 / (1 - beta1^t), 1 / (1 - beta2^t), computed on the host in fp64
-};
-
-__device__ __forceinline__ void adam_one(float& q, float g, float& m, float& v, const AdamK& h) {
-  m = h.beta1 * m + (1.f - h.beta1) * g;
-  v = h.beta2 * v + (1.f - h.beta2) * g * g;
-  const float mh = m * h.c1;
-  const float vh = v * h.c2;
-  q = q - h.lr * (mh / (sqrtf(vh) + h.eps) + h.wd * q);
+poetx_status adam_params(const poetx_adam* hp, AdamK* h) {
+  if (!hp || hp->step < 1) return POETX_ERR_ARG;
+  if (!(hp->beta1 >= 0.f && hp->beta1 < 1.f && hp->beta2 >= 0.f && hp->beta2 < 1.f))
+    return POETX_ERR_ARG;
+  h->lr = hp->lr;
+  h->beta1 = hp->beta1;
+  h->beta2 = hp->beta2;
+  h->eps = hp->eps;
+  h->wd = hp->weight_decay;
+  h->c1 = (float)(1.0 / (1.0 - std::pow((double)hp->beta1, (double)hp->step)));
+  h->c2 = (float)(1.0 / (1.0 - std::pow((double)hp->beta2, (double)hp->step)));
+  return POETX_OK;
 }
+
+namespace {
 
 // Four parameters per thread (16-byte loads and stores), a scalar tail for count % 4.
 __global__ void __launch_bounds__(256) adam_kernel(float* __restrict__ q,
@@ -62,20 +64,12 @@ using namespace poetx;
 extern "C" poetx_status poetx_adam_triu(float* q, const float* dq, float* m, float* v,
                                         long long count, const poetx_adam* hp,
                                         cudaStream_t stream) {
-  if (count < 0 || !hp || hp->step < 1) return POETX_ERR_ARG;
+  if (count < 0) return POETX_ERR_ARG;
+  AdamK h;
+  POETX_TRY(adam_params(hp, &h));
   if (count == 0) return POETX_OK;
   if (!q || !dq || !m || !v) return POETX_ERR_ARG;
   if (!aligned16(q) || !aligned16(dq) || !aligned16(m) || !aligned16(v)) return POETX_ERR_ALIGN;
-  if (!(hp->beta1 >= 0.f && hp->beta1 < 1.f && hp->beta2 >= 0.f && hp->beta2 < 1.f))
-    return POETX_ERR_ARG;
-  AdamK h;
-  h.lr = hp->lr;
-  h.beta1 = hp->beta1;
-  h.beta2 = hp->beta2;
-  h.eps = hp->eps;
-  h.wd = hp->weight_decay;
-  h.c1 = (float)(1.0 / (1.0 - std::pow((double)hp->beta1, (double)hp->step)));
-  h.c2 = (float)(1.0 / (1.0 - std::pow((double)hp->beta2, (double)hp->step)));
   long long blocks = (count / 4 + 255) / 256;
   if (blocks < 1) blocks = 1;
   const long long cap = (long long)sm_count() * 8;

@@ -82,6 +82,9 @@ _SIGS = {
     "poetx_merge_reinit": (_i, [ctypes.POINTER(LayerDesc), _vp, _vp, _sz, _vp]),
     "poetx_adam_triu": (_i, [_vp, _vp, _vp, _vp, ctypes.c_longlong, ctypes.POINTER(AdamDesc),
                              _vp]),
+    "poetx_layer_bwd_adam": (_i, [ctypes.POINTER(LayerDesc), _vp, _vp, _i, _vp, _vp, _vp, _vp,
+                                  _i, ctypes.POINTER(AdamDesc), _vp, _vp, _vp, _vp, _vp, _sz,
+                                  _vp]),
 }
 
 _lib: Optional[ctypes.CDLL] = None
@@ -355,3 +358,17 @@ def poetx_timeout_site() -> int:
     """Site id of the first expired bounded wait reported by the last poetx_get_device_error
     (file id x 10000 + source line), 0 if none."""
     return lib().poetx_timeout_site()
+
+
+def poetx_layer_bwd_adam(L: LayerDesc, x, dy, saved, dx, dq_R, dq_P, ws, m_R, v_R, m_P, v_P,
+                         step: int, lr: float, beta1: float = 0.9, beta2: float = 0.999,
+                         eps: float = 1e-8, weight_decay: float = 0.0, accumulate=False,
+                         stream=None):
+    """poetx_layer_bwd, then Adam on the layer's q_R and q_P in place (fused into the
+    gradient pack)."""
+    hp = AdamDesc(lr, beta1, beta2, eps, weight_decay, step)
+    N = x.shape[0]
+    _check("poetx_layer_bwd_adam", lib().poetx_layer_bwd_adam(
+        ctypes.byref(L), _p(x), _p(dy), N, _p(saved), _p(dx), _p(dq_R), _p(dq_P),
+        int(bool(accumulate)), ctypes.byref(hp), _p(m_R), _p(v_R), _p(m_P), _p(v_P), _p(ws),
+        ws.numel(), _stream(stream)))

@@ -185,3 +185,22 @@ def test_merge_perm_padded_argument_errors(P):
     assert f(fake, fake, P.I8, 6, 16, 8, 16, fake, fake, fake, fake, None) == 2    # int8: n % 4
     assert f(fake, None, P.I8, 8, 16, 8, 16, fake, fake, fake, fake, None) == 1    # no scale
     assert f(fake, None, 9, 8, 8, 8, 8, fake, fake, fake, None, None) == 3         # dtype
+
+
+def test_layer_bwd_adam_argument_errors(P):
+    lib = P.lib()
+    fake = ctypes.c_void_p(4096)
+    L = _desc(P)
+    hp = P.AdamDesc(1e-3, 0.9, 0.999, 1e-8, 0.0, 0)           # step 0
+    args = (fake, fake, 4, fake, fake, fake, fake, 0)
+    assert lib.poetx_layer_bwd_adam(ctypes.byref(L), *args, ctypes.byref(hp), fake, fake, fake,
+                                    fake, fake, 1 << 30, None) == 1
+    hp.step = 1
+    assert lib.poetx_layer_bwd_adam(ctypes.byref(L), *args, ctypes.byref(hp), None, fake, fake,
+                                    fake, fake, 1 << 30, None) == 1
+    assert lib.poetx_layer_bwd_adam(ctypes.byref(L), *args, None, fake, fake, fake, fake, fake,
+                                    1 << 30, None) == 1
+    assert lib.poetx_layer_bwd_adam(ctypes.byref(_desc(P, order=2)), *args, ctypes.byref(hp),
+                                    fake, fake, fake, fake, fake, 1 << 30, None) == 6
+    assert lib.poetx_layer_bwd_adam(ctypes.byref(L), *args, ctypes.byref(hp), fake, fake, fake,
+                                    fake, fake, 16, None) == 5                 # workspace
