@@ -506,10 +506,8 @@ static poetx_status layer_bwd_impl(const poetx_layer* L, const void* x, const vo
   if (sc) {
     POETX_CUDA_TRY(cudaEventRecord(sc->fork, stream));
     POETX_CUDA_TRY(cudaStreamWaitEvent(sc->ss, sc->fork, 0));
-    const poetx_status g = launch_perm_rows_side(as, true, dxt, N, m, L->perm_m, dx, sc->ss,
-                                                 mP, m);
-    POETX_CUDA_TRY(cudaEventRecord(sc->join, sc->ss));
-    POETX_TRY(g);
+    st = launch_perm_rows_side(as, true, dxt, N, m, L->perm_m, dx, sc->ss, mP, m);
+    if (cudaEventRecord(sc->join, sc->ss) != cudaSuccess && st == POETX_OK) st = POETX_ERR_CUDA;
   } else if (st == POETX_OK && N > 0) {
     st = launch_perm_rows(as, true, dxt, N, m, L->perm_m, dx, nullptr, nullptr, nullptr, stream,
                           mP, m);
