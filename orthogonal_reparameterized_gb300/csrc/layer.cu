@@ -13,8 +13,11 @@
 // Backward (chain rule of the forward):  dz~ = dy[:, pi_n];  dG_P = B^T dz~ (per block);
 //   dB = dz~ blkdiag(G_P)^T;  dA = dB W';  dG_R = x~^T dA (per block);
 //   dx~ = dA blkdiag(G_R)^T;  dx[:, pi_m] = dx~;  dq = CNP backward of dG.
-// Host-side orchestration only: every step runs in this library's kernels on the caller's
-// stream; nothing is allocated.
+// Ragged last blocks (ceil(d/b) blocks per side) are computed with every internal array
+// padded to whole blocks (see `padded`).  Host-side orchestration only: every step runs in
+// this library's kernels, on the caller's stream except the overlapped dx scatter (a side
+// stream) and the host-buffer step's copies (a copy stream), both forked from and joined
+// back into the caller's stream; no device memory is allocated.
 #include <atomic>
 #include <mutex>
 
