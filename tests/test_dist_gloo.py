@@ -5,6 +5,7 @@ that a multi-GPU trainer would add (POET-X summary page, "Practice notes" §4: D
 import os
 
 import numpy as np
+import pytest
 import torch
 import torch.distributed as dist
 import torch.multiprocessing as mp
@@ -12,23 +13,28 @@ import torch.multiprocessing as mp
 import oracle as O
 
 
-def _layer():
+def _layer(ragged=False):
     r = np.random.default_rng(5)
-    m, n, b, N = 16, 8, 4, 10
+    m, n, b, N = (18, 10, 4, 10) if ragged else (16, 8, 4, 10)
     return dict(x=r.standard_normal((N, m)), dy=r.standard_normal((N, n)),
                 W0=r.standard_normal((n, m)) / 4, perm_m=r.permutation(m), perm_n=r.permutation(n),
-                q_R=r.standard_normal((m // b, b * (b - 1) // 2)) * 0.2,
-                q_P=r.standard_normal((n // b, b * (b - 1) // 2)) * 0.2, b=b)
+                q_R=r.standard_normal((-(-m // b), b * (b - 1) // 2)) * 0.2,
+                q_P=r.standard_normal((-(-n // b), b * (b - 1) // 2)) * 0.2, b=b)
 
 
-def _worker(rank, world, port, out):
+def _grads(L, rows, ragged):
+    f = O.poetx_layer_ragged if ragged else O.poetx_layer
+    return f(L["x"][rows], L["dy"][rows], L["W0"], L["perm_m"], L["perm_n"], L["q_R"],
+             L["q_P"], L["b"])
+
+
+def _worker(rank, world, port, out, ragged):
     os.environ["MASTER_ADDR"] = "127.0.0.1"
     os.environ["MASTER_PORT"] = str(port)
     dist.init_process_group("gloo", rank=rank, world_size=world)
-    L = _layer()
+    L = _layer(ragged)
     sl = np.array_split(np.arange(L["x"].shape[0]), world)[rank]
-    r = O.poetx_layer(L["x"][sl], L["dy"][sl], L["W0"], L["perm_m"], L["perm_n"], L["q_R"],
-                      L["q_P"], L["b"])
+    r = _grads(L, sl, ragged)
     g = torch.tensor(np.concatenate([r["dq_R"].ravel(), r["dq_P"].ravel()]))
     dist.all_reduce(g)
     if rank == 0:
@@ -37,22 +43,22 @@ def _worker(rank, world, port, out):
     dist.destroy_process_group()
 
 
-def test_gloo_allreduce_of_shard_gradients_equals_full_batch():
+@pytest.mark.parametrize("ragged", [False, True])
+def test_gloo_allreduce_of_shard_gradients_equals_full_batch(ragged):
     import socket
     with socket.socket() as s:
         s.bind(("127.0.0.1", 0))
         port = s.getsockname()[1]
     ctx = mp.get_context("spawn")
     q = ctx.Queue()
-    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q, ragged)) for r in range(2)]
     for p in procs:
         p.start()
     got = q.get(timeout=120)
     for p in procs:
         p.join(timeout=120)
         assert p.exitcode == 0
-    L = _layer()
-    full = O.poetx_layer(L["x"], L["dy"], L["W0"], L["perm_m"], L["perm_n"], L["q_R"], L["q_P"],
-                         L["b"])
+    L = _layer(ragged)
+    full = _grads(L, slice(None), ragged)
     ref = np.concatenate([full["dq_R"].ravel(), full["dq_P"].ravel()])
     np.testing.assert_allclose(got, ref, rtol=0, atol=1e-12)
