@@ -130,14 +130,14 @@ W = inp["W0"]
 if wl.wdt == "i8":
     Wq, s = O.quantize_rows_int8(W)
     W = O.dequantize_rows(Wq, s)
-O.poetx_layer(inp["x"][:8], inp["dy"][:8], W, inp["perm_m"], inp["perm_n"], inp["q_R"],
-              inp["q_P"], wl.b)
+# the per-block oracle when b does not divide a side (ragged last block)
+f = O.poetx_layer if layer.m %% wl.b == 0 and layer.n %% wl.b == 0 else O.poetx_layer_ragged
+f(inp["x"][:8], inp["dy"][:8], W, inp["perm_m"], inp["perm_n"], inp["q_R"], inp["q_P"], wl.b)
 times = []
 t_end = time.perf_counter() + %(budget)f
 while True:
     t0 = time.perf_counter()
-    O.poetx_layer(inp["x"], inp["dy"], W, inp["perm_m"], inp["perm_n"], inp["q_R"], inp["q_P"],
-                  wl.b)
+    f(inp["x"], inp["dy"], W, inp["perm_m"], inp["perm_n"], inp["q_R"], inp["q_P"], wl.b)
     times.append(time.perf_counter() - t0)
     if len(times) >= %(reps)d or time.perf_counter() > t_end:
         break
@@ -197,6 +197,21 @@ def reference_arm(args, rank, world):
 
 
 # ------------------------------------------------------------------ our arm
+def merged_weight(P, W0, pn, pm, b, scale=None):
+    """The layer's merged weight (and int8 scale), zero-padded to whole blocks of b when b
+    does not divide a side (a ragged last block)."""
+    import torch
+    n, m = W0.shape
+    n_pad, m_pad = -(-n // b) * b, -(-m // b) * b
+    Wp = torch.empty(n_pad, m_pad, dtype=W0.dtype, device=W0.device)
+    sc = None if scale is None else torch.empty(n_pad, device=W0.device)
+    if (n_pad, m_pad) == (n, m):
+        P.poetx_merge_perm(W0, pn, pm, Wp, scale, sc)
+    else:
+        P.poetx_merge_perm_padded(W0, pn, pm, Wp, scale, sc)
+    return Wp, sc
+
+
 def h2d_bytes_of(*ts):
     return sum(t.numel() * t.element_size() for t in ts)
 
@@ -251,14 +266,11 @@ def main():
         Wq = torch.empty(n, m, dtype=torch.int8, device=dev)
         s = torch.empty(n, device=dev)
         P.poetx_quantize_rows_int8(W32, Wq, s)
-        Wp = torch.empty_like(Wq)
-        w_scale = torch.empty_like(s)
-        P.poetx_merge_perm(Wq, pn, pm, Wp, s, w_scale)
+        Wp, w_scale = merged_weight(P, Wq, pn, pm, b, s)
         wcode = P.I8
     else:
         W0 = t(inp["W0"], bf)
-        Wp = torch.empty_like(W0)
-        P.poetx_merge_perm(W0, pn, pm, Wp)
+        Wp, _ = merged_weight(P, W0, pn, pm, b)
         wcode = P.BF16 if wl.wdt == "bf16" else P.F32
     acode = P.BF16 if wl.act == "bf16" else P.F32
     esz = 2 if wl.act == "bf16" else 4
@@ -417,8 +429,8 @@ def main():
 
     check_err("per-stage timing")
     # CNP blocks/s (standalone, both sides' blocks)
-    nblk = (m + n) // b
     qcat = torch.cat([qR, qP], 0).contiguous()
+    nblk = qcat.shape[0]  # ceil(m/b) + ceil(n/b)
     Gb = torch.empty(nblk, b, b, dtype=torch.bfloat16, device=dev)
     dG = torch.randn(1, nblk, b, b, device=dev)
     dq = torch.empty_like(qcat)
@@ -507,6 +519,31 @@ def main():
                           "frac_of_hbm": by / (us * 1e-6) / 1e9 / pk["hbm_gbs"],
                           "note": "per training step, not part of the timed layer step"}
     del oq, og, om, ov
+    # the backward followed by the optimizer on both sides, against the backward with the
+    # update applied by the gradient pack (poetx_layer_bwd_adam); on copies of q, so the
+    # benchmarked layer is left as it was
+    qRo, qPo = qR.clone(), qP.clone()
+    Lo = P.make_layer(m, n, b, acode, wcode, P.FAST if variant == "fast" else P.MEM, pm, pn,
+                      Wp, qRo, qPo, w_scale)
+    st = {k: torch.zeros_like(qRo if k[1] == "R" else qPo) for k in ("mR", "vR", "mP", "vP")}
+    Bo = main_b
+    P.poetx_layer_fwd(Lo, x, Bo["y"], Bo["saved"], Bo["wsf"])
+
+    def bwd_then_adam():
+        P.poetx_layer_bwd(Lo, x, dy, Bo["saved"], Bo["dx"], Bo["dqR"], Bo["dqP"], Bo["wsb"])
+        P.poetx_adam_triu(qRo, Bo["dqR"], st["mR"], st["vR"], 1, 1e-3)
+        P.poetx_adam_triu(qPo, Bo["dqP"], st["mP"], st["vP"], 1, 1e-3)
+
+    def bwd_adam():
+        P.poetx_layer_bwd_adam(Lo, x, dy, Bo["saved"], Bo["dx"], Bo["dqR"], Bo["dqP"], Bo["wsb"],
+                               st["mR"], st["vR"], st["mP"], st["vP"], 1, 1e-3)
+    t_sep = median_us(bwd_then_adam)
+    t_fused = median_us(bwd_adam)
+    setup["bwd_with_optimizer"] = {
+        "bwd_then_adam_us": t_sep, "bwd_adam_fused_us": t_fused,
+        "note": "eager, L2 flushed: poetx_layer_bwd + poetx_adam_triu on each side vs "
+                "poetx_layer_bwd_adam (the same bits; two launches fewer)"}
+    del qRo, qPo, st, Lo
 
     check_err("adam timing")
     # every layer of a multi-layer workload (on request): the metric of such a workload is
@@ -528,14 +565,11 @@ def main():
                 lWq = torch.empty(ly.n, ly.m, dtype=torch.int8, device=dev)
                 ls = torch.empty(ly.n, device=dev)
                 P.poetx_quantize_rows_int8(lW32, lWq, ls)
-                lWp = torch.empty_like(lWq)
-                lsc = torch.empty_like(ls)
-                P.poetx_merge_perm(lWq, lpn, lpm, lWp, ls, lsc)
+                lWp, lsc = merged_weight(P, lWq, lpn, lpm, b, ls)
                 del lW32
             else:
                 lW0 = t(li_inp["W0"], bf)
-                lWp = torch.empty_like(lW0)
-                P.poetx_merge_perm(lW0, lpn, lpm, lWp)
+                lWp, _ = merged_weight(P, lW0, lpn, lpm, b)
                 del lW0
             LL = P.make_layer(ly.m, ly.n, b, acode, wcode, P.FAST if variant == "fast" else P.MEM,
                               lpm, lpn, lWp, lqR, lqP, lsc)

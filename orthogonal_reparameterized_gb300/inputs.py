@@ -106,6 +106,10 @@ WORKLOADS: Dict[str, Workload] = {
                            0.02, ["fast", "mem"], 3),
     "llama13b_mlp_int8": _wl("llama13b_mlp_int8", [("up", 5120, 13824), ("down", 13824, 5120)],
                              512, 4096, "bf16", "i8", 0.02, ["mem"], 4),
+    # ragged last blocks (b does not divide the sides): 2000 = 7 x 256 + 208, computed padded
+    # to the 2048-wide layer
+    "ragged_2000_b256": _wl("ragged_2000_b256", [("lin", 2000, 2000)], 256, 4096, "bf16",
+                            "bf16", 0.02, ["fast", "mem"], 5),
 }
 
 
