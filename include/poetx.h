@@ -68,7 +68,8 @@ poetx_status poetx_get_device_error(cudaStream_t stream);
 
 /* Where the first expired bounded wait seen by poetx_get_device_error happened: a site id,
  * (source file id) x 10000 + (source line) of the waiting call (file ids: 1 the tensor-core
- * GEMM engine, 2 the CNP products, 3 the index kernels, 4 the self-test), or 0 if none was
+ * GEMM engine, 2 the CNP products, 3 the index kernels, 4 the self-test, 5 the fused
+ * backward block-diagonal product), or 0 if none was
  * recorded.  Host-only (no synchronisation); for diagnosis. */
 int poetx_timeout_site(void);
 
@@ -82,11 +83,16 @@ poetx_status poetx_selftest_timeout(unsigned int timeout_us, cudaStream_t stream
  * (fp32 accumulation, same rounding of the stored results).  Process-wide. */
 poetx_status poetx_set_gemm_engine(int engine);
 
-/* Diagnostic switch: with on = 1 (the default) the layer runs the W' contraction and the
- * block-diagonal product that follows it (forward: z~ = (A W'^T) blkdiag(G_P); backward:
- * dx~ = (dB W') blkdiag(G_R)^T) as one tensor-core kernel where the shape allows (bf16 W',
- * b = 64, 128 or 256, single-CTA tiles); on = 0 runs them as two kernels.  Same results up to
- * the order of fp32 accumulation.  Process-wide. */
+/* Diagnostic switch of the layer's fused kernels, a bit mask (default 3):
+ *   bit 0  the W' contraction and the block-diagonal product that follows it (forward:
+ *          z~ = (A W'^T) blkdiag(G_P); backward: dx~ = (dB W') blkdiag(G_R)^T) as one
+ *          tensor-core kernel where the shape allows (bf16 W', b = 64, 128 or 256,
+ *          single-CTA tiles);
+ *   bit 1  each backward block-diagonal product and its weight gradient (dB = dz~ G_P^T with
+ *          dG_P = B^T dz~; dx~ = dA G_R^T with dG_R = x~^T dA) as one kernel that reads the
+ *          upstream gradient once (bf16, b = 128 or 256).
+ * 0 runs every product as its own kernel.  Same results up to the order of fp32
+ * accumulation.  POETX_ERR_ARG outside 0..3.  Process-wide. */
 poetx_status poetx_set_fusion(int on);
 
 /* Overlap switch (default 1): poetx_layer_bwd runs the dx scatter beside the G_R weight
@@ -305,6 +311,49 @@ poetx_status poetx_layer_fwd(const poetx_layer* L, const void* x, int N, void* y
 poetx_status poetx_layer_bwd(const poetx_layer* L, const void* x, const void* dy, int N,
                              const void* saved, void* dx, float* dq_R, float* dq_P,
                              int accumulate, void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* ----------------------------------------------------------------------------------------
+ * Layer groups: the layers trained together (for example the seven linears of a transformer
+ * block) run their Cayley-Neumann parameterizations as one batch over all their blocks (the
+ * CNP of a block depends on that block's q only; POET-X summary page, "Core method" section
+ * 4), and their forward and backward chains (sections 1-5) layer by layer in between.  One
+ * training step of a group of `count` layers Ls[0..count-1]:
+ *   poetx_group_cnp_fwd                       G, Q and Q^2 of every block of every layer
+ *   poetx_group_layer_fwd(i), each layer      y_i from x_i, in whatever order the model needs
+ *   poetx_group_layer_bwd(i), each layer      dx_i from dy_i, and layer i's weight-gradient
+ *                                             partials (kept in ws)
+ *   poetx_group_cnp_bwd                       dq_R, dq_P of every layer
+ * Every layer of a group has the same b, act and order (POETX_ERR_SHAPE, POETX_ERR_DTYPE
+ * otherwise); wdt and variant may differ.  1 <= count <= POETX_GROUP_MAX_LAYERS.  N is the same
+ * for every call of a step.  The results equal those of poetx_layer_fwd / poetx_layer_bwd on
+ * each layer (up to the order of fp32 accumulation inside the CNP products).
+ *   saved  poetx_group_saved_bytes(Ls, count, N) bytes: the stacks of G, Q and Q^2 of every
+ *          block and, per layer, what its forward keeps (POETX_FAST: B and x~).
+ *   ws     poetx_group_workspace_bytes(Ls, count, N) bytes: the chains' scratch (one region,
+ *          shared by the layers, which run one after the other on the stream), every layer's
+ *          weight-gradient partials and the CNP backward's scratch.  The same ws must be
+ *          passed to every poetx_group_layer_bwd and the poetx_group_cnp_bwd of a step and not
+ *          be written in between; every layer's backward must come before the group's CNP
+ *          backward (a layer whose backward was not run in the step gets the gradient of
+ *          whatever partials ws holds).
+ * Errors: as for poetx_layer_fwd / poetx_layer_bwd; i outside [0, count) is POETX_ERR_ARG;
+ * 0 from the *_bytes calls means an invalid group. */
+#define POETX_GROUP_MAX_LAYERS 16
+size_t poetx_group_saved_bytes(const poetx_layer* Ls, int count, int N);
+size_t poetx_group_workspace_bytes(const poetx_layer* Ls, int count, int N);
+poetx_status poetx_group_cnp_fwd(const poetx_layer* Ls, int count, int N, void* saved,
+                                 cudaStream_t stream);
+poetx_status poetx_group_layer_fwd(const poetx_layer* Ls, int count, int i, const void* x, int N,
+                                   void* y, void* saved, void* ws, size_t ws_bytes,
+                                   cudaStream_t stream);
+poetx_status poetx_group_layer_bwd(const poetx_layer* Ls, int count, int i, const void* x,
+                                   const void* dy, int N, const void* saved, void* dx, void* ws,
+                                   size_t ws_bytes, cudaStream_t stream);
+/* dq_R, dq_P: HOST arrays of `count` device pointers, layer i's [ceil(m_i/b), b(b-1)/2] and
+ * [ceil(n_i/b), b(b-1)/2] fp32 gradients (accumulate != 0 adds to them). */
+poetx_status poetx_group_cnp_bwd(const poetx_layer* Ls, int count, int N, const void* saved,
+                                 float* const* dq_R, float* const* dq_P, int accumulate,
+                                 void* ws, size_t ws_bytes, cudaStream_t stream);
 
 /* One training step of the layer (forward, then backward from dy) with HOST buffers, the
  * transfers overlapped with the kernels (the input-centric chain, POET-X summary page, "Core

@@ -26,13 +26,4 @@ __device__ __forceinline__ void adam_one(float& q, float g, float& m, float& v, 
   q = __fsub_rn(q, __fmul_rn(h.lr, step));
 }
 
-// The update applied by the gradient pack of a layer's two sides (side 0: R, side 1: P):
-// q, m, v of each side, nullptr q = no update.
-struct PackAdam {
-  AdamK h;
-  float* q[2];
-  float* m[2];
-  float* v[2];
-};
-
 }  // namespace poetx

@@ -90,7 +90,8 @@ void prof_begin(cudaStream_t s) {
 static const char* kStageNames[ST_COUNT] = {
     "triu_unpack", "cnp_q2", "cnp_g", "cnp_sum_partials", "cnp_m1", "cnp_qbar", "triu_grad_pack",
     "perm_gather", "perm_scatter", "blockdiag_mm", "wprime_gemm", "blockdiag_wgrad",
-    "quantize_rows_int8", "merge_perm", "merge_reinit", "adam_triu", "wprime_blockdiag_fused"};
+    "quantize_rows_int8", "merge_perm", "merge_reinit", "adam_triu", "wprime_blockdiag_fused",
+    "blockdiag_bwd_fused"};
 
 // Waits on a shared-memory barrier that nothing arrives on, for at most limit_ns, then
 // records the timeout and returns.

@@ -142,19 +142,26 @@ poetx_status launch_cnp_gemm(const CnpGemm& g, int nblk, int stage, cudaStream_t
 Operand op1(const float* p, float c) { return Operand{p, c, nullptr, 0.f}; }
 Operand op2(const float* p, float c, const float* q, float d) { return Operand{p, c, q, d}; }
 
-// X[j] = sum_s dG_side[s][j'] in the order s = 0, 1, ..., S_side - 1 (j' = j for side 0,
-// j - n0 for side 1), and Xt[j] = X[j]^T, one 32 x 32 tile per CTA (transpose through
-// shared memory so that both stores are coalesced).
-__global__ void sum_partials_kernel(const float* __restrict__ dG0, int S0, int n0,
-                                    const float* __restrict__ dG1, int S1, int n1, int b,
+// X[j] = sum_s dG_k[s][j - start_k] in the order s = 0, 1, ..., splits_k - 1 for the side k
+// that owns block j, and Xt[j] = X[j]^T, one 32 x 32 tile per CTA (transpose through shared
+// memory so that both stores are coalesced).
+__device__ __forceinline__ int sum_side(const SideTable& t, int blk) {
+  int k = 0;
+  while (k + 1 < t.count && blk >= t.start[k + 1]) ++k;
+  return k;
+}
+
+__global__ void sum_partials_kernel(const __grid_constant__ SideTable st, int b,
                                     float* __restrict__ X, float* __restrict__ Xt) {
   pdl_trigger();
   pdl_wait();
   __shared__ float tile[32][33];
   const int j = blockIdx.z;
-  const float* src = j < n0 ? dG0 + (long long)j * b * b : dG1 + (long long)(j - n0) * b * b;
-  const int S = j < n0 ? S0 : S1;
-  const long long sstride = (long long)(j < n0 ? n0 : n1) * b * b;
+  const int k = sum_side(st, j);
+  const long long nk = st.start[k + 1] - st.start[k];
+  const float* src = st.src[k] + (long long)(j - st.start[k]) * b * b;
+  const int S = st.splits[k];
+  const long long sstride = nk * b * b;
   const int r0 = blockIdx.y * 32, c0 = blockIdx.x * 32;
   const long long base = (long long)j * b * b;
   for (int rr = threadIdx.y; rr < 32; rr += 8) {
@@ -183,11 +190,8 @@ __global__ void sum_partials_kernel(const float* __restrict__ dG0, int S0, int n
 constexpr int kSumR = 32, kSumC = 64, kSumChunk = 5;
 constexpr size_t kSumSmem = (size_t)(kSumChunk * kSumR * kSumC + kSumC * (kSumR + 1)) * 4;
 
-__global__ void __launch_bounds__(256) sum_partials_vec_kernel(const float* __restrict__ dG0,
-                                                                int S0, int n0,
-                                                                const float* __restrict__ dG1,
-                                                                int S1, int n1, int b,
-                                                                float* __restrict__ X,
+__global__ void __launch_bounds__(256) sum_partials_vec_kernel(const __grid_constant__ SideTable st,
+                                                                int b, float* __restrict__ X,
                                                                 float* __restrict__ Xt,
                                                                 unsigned long long* tr,
                                                                 size_t tr_cap) {
@@ -197,9 +201,10 @@ __global__ void __launch_bounds__(256) sum_partials_vec_kernel(const float* __re
   extern __shared__ __align__(16) float ssm[];
   float* T = ssm + kSumChunk * kSumR * kSumC;  // [kSumC][kSumR + 1] transposed tile
   const int j = blockIdx.z;
-  const float* src = j < n0 ? dG0 + (long long)j * b * b : dG1 + (long long)(j - n0) * b * b;
-  const int S = j < n0 ? S0 : S1;
-  const long long sstride = (long long)(j < n0 ? n0 : n1) * b * b;
+  const int k = sum_side(st, j);
+  const float* src = st.src[k] + (long long)(j - st.start[k]) * b * b;
+  const int S = st.splits[k];
+  const long long sstride = (long long)(st.start[k + 1] - st.start[k]) * b * b;
   const int r0 = blockIdx.y * kSumR, c0 = blockIdx.x * kSumC;
   const long long base = (long long)j * b * b;
   constexpr int G = kSumR * kSumC / 4;  // float4 groups of the tile (2 per thread)
@@ -260,15 +265,26 @@ size_t blk_bytes(int nblk, int b) { return align_up((size_t)nblk * b * b * sizeo
 
 }  // namespace
 
+SideTable CnpSides::table(int b) const {
+  SideTable t{};
+  t.count = count;
+  t.start[0] = 0;
+  for (int k = 0; k < count; ++k) {
+    t.start[k + 1] = t.start[k] + n[k];
+    t.valid[k] = last[k] > 0 ? last[k] : b;
+    t.src[k] = q[k];
+  }
+  return t;
+}
+
 size_t cnp_fwd_scratch_bytes(int nblk, int b) { return 2 * blk_bytes(nblk, b); }
 size_t cnp_bwd_scratch_bytes(int nblk, int b) { return 7 * blk_bytes(nblk, b); }
 
 poetx_status cnp_forward_sides(const CnpSides& q, int b, float* Qs, float* Q2, float* G_f32,
                                void* G_bf16, void* Gt_bf16, cudaStream_t s) {
-  const int nblk = q.n[0] + q.n[1];
+  const int nblk = q.total();
   if (nblk == 0) return POETX_OK;
-  POETX_TRY(launch_triu_unpack2(q.q[0], q.n[0], q.q[1], q.n[1], b, Qs, s, q.last[0],
-                                  q.last[1]));
+  POETX_TRY(launch_triu_unpack_sides(q.table(b), b, Qs, s));
   // Q2 = Q Q (symmetric); B^T = Q^T = -Q
   CnpGemm g{};
   g.b = b;
@@ -297,15 +313,15 @@ poetx_status cnp_forward_sides(const CnpSides& q, int b, float* Qs, float* Q2, f
 
 poetx_status cnp_forward(const float* q, int nblk, int b, float* Qs, float* Q2, float* G_f32,
                          void* G_bf16, void* Gt_bf16, cudaStream_t s) {
-  CnpSides sides{{q, nullptr}, {nblk, 0}};
+  CnpSides sides;
+  sides.add(q, nblk);
   return cnp_forward_sides(sides, b, Qs, Q2, G_f32, G_bf16, Gt_bf16, s);
 }
 
 poetx_status cnp_backward_sides(const CnpSides& q, const float* Qin, const float* Q2in,
-                                const float* const dG[2], const int splits[2], int b,
-                                float* const dq[2], int accumulate, void* scratch, cudaStream_t s,
-                                const PackAdam* pa) {
-  const int nblk = q.n[0] + q.n[1];
+                                const CnpGrads& gr, int b, int accumulate, void* scratch,
+                                cudaStream_t s, const PackAdam* pa) {
+  const int nblk = q.total();
   if (nblk == 0) return POETX_OK;
   char* w = static_cast<char*>(scratch);
   const size_t bb = blk_bytes(nblk, b);
@@ -317,9 +333,9 @@ poetx_status cnp_backward_sides(const CnpSides& q, const float* Qin, const float
   float* M1t = reinterpret_cast<float*>(w + 5 * bb);
   float* Qbar = reinterpret_cast<float*>(w + 6 * bb);
   const float* Qs = Qin;
+  SideTable t = q.table(b);
   if (!Qs) {
-    POETX_TRY(launch_triu_unpack2(q.q[0], q.n[0], q.q[1], q.n[1], b, Qw, s, q.last[0],
-                                  q.last[1]));
+    POETX_TRY(launch_triu_unpack_sides(t, b, Qw, s));
     Qs = Qw;
   }
   if (!Q2in) {
@@ -333,8 +349,16 @@ poetx_status cnp_backward_sides(const CnpSides& q, const float* Qin, const float
     POETX_TRY(launch_cnp_gemm(g, nblk, ST_CNP_Q2, s));
     Q2in = Q2;
   }
-  // X = sum of the partials (both sides, fixed order) and its transpose Xt
-  if (b % kSumC == 0 && aligned16(dG[0]) && (!dG[1] || aligned16(dG[1]))) {
+  // X = sum of the partials (every side, fixed order) and its transpose Xt
+  bool vec = b % kSumC == 0;
+  for (int k = 0; k < q.count; ++k) {
+    t.src[k] = gr.dG[k];
+    t.splits[k] = gr.splits[k];
+    t.dst[k] = gr.dq[k];
+    if (q.n[k] > 0 && (!gr.dG[k] || !gr.dq[k])) return POETX_ERR_ARG;
+    vec = vec && aligned16(gr.dG[k]);
+  }
+  if (vec) {
     static std::once_flag once;
     static cudaError_t attr = cudaSuccess;
     std::call_once(once, [] {
@@ -345,14 +369,13 @@ poetx_status cnp_backward_sides(const CnpSides& q, const float* Qin, const float
     dim3 grid(b / kSumC, b / kSumR, nblk);
     size_t tr_cap = 0;
     unsigned long long* tr = trace_buffer(&tr_cap);
-    POETX_CUDA_TRY(launch_pdl(sum_partials_vec_kernel, grid, dim3(256), kSumSmem, s, dG[0],
-                              splits[0], q.n[0], dG[1], splits[1], q.n[1], b, X, Xt, tr, tr_cap));
+    POETX_CUDA_TRY(launch_pdl(sum_partials_vec_kernel, grid, dim3(256), kSumSmem, s, t, b, X,
+                              Xt, tr, tr_cap));
     POETX_CUDA_TRY(cudaGetLastError());
     after_launch(s, ST_CNP_SUM);
   } else {
     dim3 grid(ceil_div(b, 32), ceil_div(b, 32), nblk);
-    POETX_CUDA_TRY(launch_pdl(sum_partials_kernel, grid, dim3(32, 8), 0, s, dG[0], splits[0],
-                              q.n[0], dG[1], splits[1], q.n[1], b, X, Xt));
+    POETX_CUDA_TRY(launch_pdl(sum_partials_kernel, grid, dim3(32, 8), 0, s, t, b, X, Xt));
     POETX_CUDA_TRY(cudaGetLastError());
     after_launch(s, ST_CNP_SUM);
   }
@@ -381,8 +404,7 @@ poetx_status cnp_backward_sides(const CnpSides& q, const float* Qin, const float
   r.e2 = 2.f;
   r.out_f32 = Qbar;
   POETX_TRY(launch_cnp_gemm(r, nblk, ST_CNP_QBAR, s));
-  return launch_triu_grad_pack2(Qbar, q.n[0], q.n[1], b, dq[0], dq[1], accumulate, s,
-                                q.last[0], q.last[1], pa);
+  return launch_triu_grad_pack_sides(Qbar, t, b, accumulate, s, pa);
 }
 
 }  // namespace poetx
@@ -420,9 +442,11 @@ extern "C" poetx_status poetx_cnp_bwd(const float* q, const float* dG, int split
   if (!q || !dG || !dq || !ws) return POETX_ERR_ARG;
   if (ws_bytes < cnp_bwd_scratch_bytes(nblk, b)) return POETX_ERR_WORKSPACE;
   if (!aligned16(ws) || !aligned16(dG)) return POETX_ERR_ALIGN;
-  CnpSides sides{{q, nullptr}, {nblk, 0}};
-  const float* const dGs[2] = {dG, nullptr};
-  const int sp[2] = {splits, 1};
-  float* const dqs[2] = {dq, nullptr};
-  return cnp_backward_sides(sides, nullptr, nullptr, dGs, sp, b, dqs, accumulate, ws, stream);
+  CnpSides sides;
+  sides.add(q, nblk);
+  CnpGrads g;
+  g.dG[0] = dG;
+  g.splits[0] = splits;
+  g.dq[0] = dq;
+  return cnp_backward_sides(sides, nullptr, nullptr, g, b, accumulate, ws, stream);
 }

@@ -24,20 +24,22 @@ __device__ __forceinline__ long long tri_index(int i, int j, int b) {
   return (long long)i * (b - 1) - (long long)i * (i - 1) / 2 + (j - i - 1);
 }
 
-// Blocks [0, n0) come from q0, blocks [n0, gridDim.z) from q1 (the R and P sides of a layer
-// are unpacked by one launch).  One CTA per 32 x 32 tile (I, J) with I <= J of a block: it
-// reads the packed entries of the tile's upper part (consecutive j are consecutive in q),
-// writes Q[I][J] and, through shared memory, the mirrored tile Q[J][I] = -Q[I][J]^T, both
-// with coalesced rows.
-// r0, r1: features of the last block of each side (b unless that block is ragged): the
-// entries of a ragged block outside its r x r corner are not parameters and are zero in Q.
-__device__ __forceinline__ int block_valid(int blk, int n0, int r0, int r1, int b) {
-  return blk == n0 - 1 ? r0 : (blk == (int)gridDim.z - 1 ? r1 : b);
+// The blocks of one launch come from the sides of a SideTable (the R and P sides of a layer,
+// or of every layer of a group): block blk belongs to the side whose [start, start + n)
+// range holds it.
+__device__ __forceinline__ int side_of(const SideTable& t, int blk) {
+  int k = 0;
+  while (k + 1 < t.count && blk >= t.start[k + 1]) ++k;
+  return k;
 }
 
-__global__ void triu_unpack_kernel(const float* __restrict__ q0, int n0, const float* __restrict__ q1,
-                                   int b, int r0, int r1, float* __restrict__ Q,
-                                   unsigned long long* tr, size_t tr_cap) {
+// One CTA per 32 x 32 tile (I, J) with I <= J of a block: it reads the packed entries of the
+// tile's upper part (consecutive j are consecutive in q), writes Q[I][J] and, through shared
+// memory, the mirrored tile Q[J][I] = -Q[I][J]^T, both with coalesced rows.  The entries of a
+// ragged last block (valid features r < b) outside its r x r corner are not parameters and
+// are zero in Q.
+__global__ void triu_unpack_kernel(const __grid_constant__ SideTable st, int b,
+                                   float* __restrict__ Q, unsigned long long* tr, size_t tr_cap) {
   if (threadIdx.x == 0 && threadIdx.y == 0) trace_stamp3(tr, tr_cap, 0);
   pdl_trigger();
   pdl_wait();
@@ -52,9 +54,11 @@ __global__ void triu_unpack_kernel(const float* __restrict__ q0, int n0, const f
   }
   const int J = I + t;
   const long long tri = (long long)b * (b - 1) / 2;
-  const float* qb = blk < n0 ? q0 + blk * tri : q1 + (blk - n0) * tri;
+  const int k = side_of(st, blk);
+  const int local = blk - st.start[k];
+  const float* qb = st.src[k] + local * tri;
   float* Qb = Q + (long long)blk * b * b;
-  const int rv = block_valid(blk, n0, r0, r1, b);
+  const int rv = blk == st.start[k + 1] - 1 ? st.valid[k] : b;
   const int tx = threadIdx.x, ty = threadIdx.y;  // 32 x 8
   for (int r = ty; r < 32; r += 8) {
     const int i = I * 32 + r, j = J * 32 + tx;
@@ -86,10 +90,10 @@ __global__ void triu_unpack_kernel(const float* __restrict__ q0, int n0, const f
 // tile are consecutive entries of the packed triangle.
 // pa (nullable q): the optimizer update applied to each entry as its gradient is written
 // (single-replica training: nothing has to be summed between the pack and the update).
-__global__ void triu_grad_pack_kernel(const float* __restrict__ Qbar, int b, float* __restrict__ dq0,
-                                      int n0, float* __restrict__ dq1, int accumulate, int r0,
-                                      int r1, PackAdam pa, unsigned long long* tr,
-                                      size_t tr_cap) {
+__global__ void triu_grad_pack_kernel(const float* __restrict__ Qbar, int b,
+                                      const __grid_constant__ SideTable st, int accumulate,
+                                      const __grid_constant__ PackAdam pa,
+                                      unsigned long long* tr, size_t tr_cap) {
   if (threadIdx.x == 0 && threadIdx.y == 0) trace_stamp3(tr, tr_cap, 0);
   pdl_trigger();
   pdl_wait();
@@ -104,10 +108,10 @@ __global__ void triu_grad_pack_kernel(const float* __restrict__ Qbar, int b, flo
   const int J = I + t;
   const long long tri = (long long)b * (b - 1) / 2;
   const float* Qb = Qbar + (long long)blk * b * b;
-  float* dqb = blk < n0 ? dq0 + blk * tri : dq1 + (blk - n0) * tri;
-  const int side = blk < n0 ? 0 : 1;
-  const long long off = (long long)(blk < n0 ? blk : blk - n0) * tri;  // this block's entries
-  const int rv = block_valid(blk, n0, r0, r1, b);
+  const int side = side_of(st, blk);
+  const long long off = (long long)(blk - st.start[side]) * tri;  // this block's entries
+  float* dqb = st.dst[side] + off;
+  const int rv = blk == st.start[side + 1] - 1 ? st.valid[side] : b;
   const int tx = threadIdx.x, ty = threadIdx.y;  // 32 x 8
   for (int r = ty; r < 32; r += 8) {  // tile[r][c] = Qbar[J*32 + r][I*32 + c]
     const int j = J * 32 + r, i = I * 32 + tx;
@@ -134,36 +138,40 @@ __global__ void triu_grad_pack_kernel(const float* __restrict__ Qbar, int b, flo
   }
 }
 
-poetx_status launch_triu_unpack2(const float* q0, int n0, const float* q1, int n1, int b, float* Q,
-                                 cudaStream_t s, int r0, int r1) {
-  if (n0 + n1 == 0) return POETX_OK;
+poetx_status launch_triu_unpack_sides(const SideTable& t, int b, float* Q, cudaStream_t s) {
+  const int total = t.start[t.count];
+  if (total == 0) return POETX_OK;
   const int nt = (b + 31) / 32;
-  dim3 grid(nt * (nt + 1) / 2, 1, n0 + n1);
+  dim3 grid(nt * (nt + 1) / 2, 1, total);
   size_t tr_cap = 0;
   unsigned long long* tr = trace_buffer(&tr_cap);
-  POETX_CUDA_TRY(launch_pdl(triu_unpack_kernel, grid, dim3(32, 8), 0, s, q0, n0, q1, b,
-                            r0 > 0 ? r0 : b, r1 > 0 ? r1 : b, Q, tr, tr_cap));
+  POETX_CUDA_TRY(launch_pdl(triu_unpack_kernel, grid, dim3(32, 8), 0, s, t, b, Q, tr, tr_cap));
   POETX_CUDA_TRY(cudaGetLastError());
   after_launch(s, ST_TRIU_UNPACK);
   return POETX_OK;
 }
 
 poetx_status launch_triu_unpack(const float* q, int nblk, int b, float* Q, cudaStream_t s) {
-  return launch_triu_unpack2(q, nblk, nullptr, 0, b, Q, s);
+  SideTable t{};
+  t.count = 1;
+  t.start[0] = 0;
+  t.start[1] = nblk;
+  t.valid[0] = b;
+  t.src[0] = q;
+  return launch_triu_unpack_sides(t, b, Q, s);
 }
 
-poetx_status launch_triu_grad_pack2(const float* Qbar, int n0, int n1, int b, float* dq0, float* dq1,
-                                    int accumulate, cudaStream_t s, int r0, int r1,
-                                    const PackAdam* pa) {
-  if (n0 + n1 == 0 || b < 2) return POETX_OK;
+poetx_status launch_triu_grad_pack_sides(const float* Qbar, const SideTable& t, int b,
+                                         int accumulate, cudaStream_t s, const PackAdam* pa) {
+  const int total = t.start[t.count];
+  if (total == 0 || b < 2) return POETX_OK;
   const int nt = (b + 31) / 32;
-  dim3 grid(nt * (nt + 1) / 2, 1, n0 + n1);
+  dim3 grid(nt * (nt + 1) / 2, 1, total);
   size_t tr_cap = 0;
   unsigned long long* tr = trace_buffer(&tr_cap);
   PackAdam none{};
-  POETX_CUDA_TRY(launch_pdl(triu_grad_pack_kernel, grid, dim3(32, 8), 0, s, Qbar, b, dq0, n0,
-                            dq1, accumulate, r0 > 0 ? r0 : b, r1 > 0 ? r1 : b, pa ? *pa : none,
-                            tr, tr_cap));
+  POETX_CUDA_TRY(launch_pdl(triu_grad_pack_kernel, grid, dim3(32, 8), 0, s, Qbar, b, t,
+                            accumulate, pa ? *pa : none, tr, tr_cap));
   POETX_CUDA_TRY(cudaGetLastError());
   after_launch(s, ST_TRIU_PACK);
   return POETX_OK;
@@ -171,7 +179,13 @@ poetx_status launch_triu_grad_pack2(const float* Qbar, int n0, int n1, int b, fl
 
 poetx_status launch_triu_grad_pack(const float* Qbar, int nblk, int b, float* dq, int accumulate,
                                    cudaStream_t s) {
-  return launch_triu_grad_pack2(Qbar, nblk, 0, b, dq, nullptr, accumulate, s);
+  SideTable t{};
+  t.count = 1;
+  t.start[0] = 0;
+  t.start[1] = nblk;
+  t.valid[0] = b;
+  t.dst[0] = dq;
+  return launch_triu_grad_pack_sides(Qbar, t, b, accumulate, s);
 }
 
 // ---------------------------------------------------------------- row permutations

@@ -1,6 +1,7 @@
 // Internal host-side launchers shared between the library's translation units.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -12,15 +13,38 @@ namespace poetx {
 
 // ---- index.cu
 poetx_status launch_triu_unpack(const float* q, int nblk, int b, float* Q, cudaStream_t s);
-// Two-sided: blocks [0, n0) from q0, [n0, n0 + n1) from q1.
-// r0, r1: features of the last block of side 0 / side 1 (0: b); entries of a ragged last
-// block outside its r x r corner are zero in Q and get zero gradient.
-poetx_status launch_triu_unpack2(const float* q0, int n0, const float* q1, int n1, int b, float* Q,
-                                 cudaStream_t s, int r0 = 0, int r1 = 0);
-// pa (nullable): the optimizer update applied as each dq entry is written.
-poetx_status launch_triu_grad_pack2(const float* Qbar, int n0, int n1, int b, float* dq0, float* dq1,
-                                    int accumulate, cudaStream_t s, int r0 = 0, int r1 = 0,
-                                    const PackAdam* pa = nullptr);
+// The blocks of one CNP call may come from several "sides" (the R and P factors of a layer,
+// or of every layer of a group): side k owns blocks [start[k], start[k] + n[k]) of one
+// contiguous [total, b, b] stack, sides in order.
+constexpr int kMaxSides = 32;
+
+// Per-side arguments of the unpack, partial-sum and gradient-pack kernels (a kernel
+// parameter: 1.2 KB).
+struct SideTable {
+  int count;
+  int start[kMaxSides + 1];    // first block of each side; start[count] = total blocks
+  int valid[kMaxSides];        // features of the side's last block (b when it is whole)
+  const float* src[kMaxSides];  // q of the side (unpack) or its dG partials (sum)
+  float* dst[kMaxSides];        // dq of the side (pack)
+  int splits[kMaxSides];        // dG partials of the side (sum)
+};
+
+// The optimizer update applied by the gradient pack, per side: q, m, v (nullptr q: none).
+struct PackAdam {
+  AdamK h;
+  float* q[kMaxSides];
+  float* m[kMaxSides];
+  float* v[kMaxSides];
+};
+
+// Q [total, b, b] = the unpacked skew blocks of every side's q (t.src); entries of a ragged
+// last block outside its r x r corner are zero in Q and get zero gradient.
+poetx_status launch_triu_unpack_sides(const SideTable& t, int b, float* Q, cudaStream_t s);
+// dq of every side (t.dst) (+)= Qbar_ij - Qbar_ji; pa (nullable): the optimizer update applied
+// as each dq entry is written.
+poetx_status launch_triu_grad_pack_sides(const float* Qbar, const SideTable& t, int b,
+                                         int accumulate, cudaStream_t s,
+                                         const PackAdam* pa = nullptr);
 poetx_status launch_triu_grad_pack(const float* Qbar, int nblk, int b, float* dq, int accumulate,
                                    cudaStream_t s);
 // Y[r][j] = X[src_rows ? src_rows[r] : r][perm[j]] (gather) or Y[r][perm[j]] = X[r][j]
@@ -70,13 +94,33 @@ poetx_status launch_simt_gemm(poetx_dtype ta, poetx_dtype tb, poetx_dtype tc, co
                               cudaStream_t s);
 
 // ---- cnp.cu
-// The blocks of one CNP call may come from two sides (the R and P factors of a layer):
-// blocks [0, n[0]) belong to side 0, [n[0], n[0] + n[1]) to side 1.  Every block array
-// (Q, Q^2, G, X, ...) is one contiguous [n[0] + n[1], b, b] stack.
 struct CnpSides {
-  const float* q[2];   // packed triangles of each side
-  int n[2];            // blocks of each side (n[1] may be 0)
-  int last[2] = {0, 0};  // features of each side's last block when ragged (0: b)
+  int count = 0;
+  const float* q[kMaxSides] = {};  // packed triangles of each side
+  int n[kMaxSides] = {};           // blocks of each side
+  int last[kMaxSides] = {};        // features of each side's last block when ragged (0: b)
+  int total() const {
+    int t = 0;
+    for (int k = 0; k < count; ++k) t += n[k];
+    return t;
+  }
+  // false when the table is full
+  bool add(const float* qk, int nk, int lastk = 0) {
+    if (count == kMaxSides) return false;
+    q[count] = qk;
+    n[count] = nk;
+    last[count] = lastk;
+    ++count;
+    return true;
+  }
+  // the unpack kernels' table: start, valid and src = q
+  SideTable table(int b) const;
+};
+// Per side: the dG partials [splits[k], n[k], b, b] and the dq output [n[k], b(b-1)/2].
+struct CnpGrads {
+  const float* dG[kMaxSides] = {};
+  int splits[kMaxSides] = {};
+  float* dq[kMaxSides] = {};
 };
 size_t cnp_fwd_scratch_bytes(int nblk, int b);
 size_t cnp_bwd_scratch_bytes(int nblk, int b);
@@ -86,12 +130,11 @@ poetx_status cnp_forward(const float* q, int nblk, int b, float* Qs, float* Q2, 
 poetx_status cnp_forward_sides(const CnpSides& q, int b, float* Qs, float* Q2, float* G_f32,
                                void* G_bf16, void* Gt_bf16, cudaStream_t s);
 // Backward CNP.  Q and Q2 may be the stacks kept from the forward, or NULL to recompute
-// them into the scratch; dG[side] is [splits[side], n[side], b, b]; dq[side] receives that
-// side's gradient.  scratch holds cnp_bwd_scratch_bytes(n[0] + n[1], b) bytes.
-// pa (nullable): the optimizer update of both sides applied by the gradient pack.
+// them into the scratch; g.dG[k] / g.splits[k] / g.dq[k] per side.  scratch holds
+// cnp_bwd_scratch_bytes(total blocks, b) bytes.  pa (nullable): the optimizer update of
+// every side applied by the gradient pack.
 poetx_status cnp_backward_sides(const CnpSides& q, const float* Q, const float* Q2,
-                                const float* const dG[2], const int splits[2], int b,
-                                float* const dq[2], int accumulate, void* scratch,
+                                const CnpGrads& g, int b, int accumulate, void* scratch,
                                 cudaStream_t s, const PackAdam* pa = nullptr);
 
 // ---- optim.cu
@@ -104,6 +147,11 @@ bool use_tensor_cores();
 
 // ---- umma_gemm.cu: tcgen05 / TMA tensor-core GEMMs (bf16 in, fp32 accumulate)
 bool umma_supported();
+enum TmaElem : int { TMA_U8 = 0, TMA_BF16 = 1, TMA_F32 = 2 };
+// Tensor map of a 2-D tensor [outer][inner] (row pitch in elements), box {box_inner,
+// box_outer}, 128-byte swizzle or none (cached per thread).
+bool encode_tma_2d(CUtensorMap* m, const void* ptr, TmaElem et, uint64_t inner, uint64_t outer,
+                   uint64_t pitch_elems, uint32_t box_inner, uint32_t box_outer, bool swizzle128);
 // Y = X . op(G) per block (bf16), op = identity (trans=0) or transpose; optional column
 // scale; optional output permutation (column c of the product is stored at out_perm[c]).
 poetx_status umma_blockdiag(const void* X, long long N, int nblk, int b, const void* G, int trans,
@@ -127,6 +175,14 @@ poetx_status umma_wprime_fused(const void* A, long long N, int m, int n, const v
 // scale already.
 poetx_status umma_wprime_i8(const void* A, long long N, int m, int n, const void* Wq,
                             const float* w_scale, int trans, void* C, cudaStream_t s);
+// ---- bdw.cu: the backward of a block-diagonal product in one pass over T (b = 128 or 256):
+// Y = T blkdiag(G)^T (column c times colscale[c] when given) and dG[s, j] = S_j^T T_j over
+// the token tiles of split s (fp32 partials [splits, nblk, b, b]).  bdw_splits: the split
+// count the layer uses with it.
+bool umma_bdw_ok(int b);
+int bdw_splits(long long N, int nblk, int b);
+poetx_status umma_bdw(const void* T, const void* S, long long N, int nblk, int b, const void* G,
+                      const float* colscale, void* Y, int splits, float* dG, cudaStream_t s);
 // dG[s, j] = X_j^T dY_j over the tokens of split s (fp32 partials).
 poetx_status umma_wgrad(const void* X, const void* dY, long long N, int nblk, int b, int splits,
                         float* dG, cudaStream_t s);

@@ -27,7 +27,9 @@
 namespace poetx {
 
 static std::atomic<int> g_engine{0};  // 0: tensor cores where supported, 1: CUDA cores only
-static std::atomic<int> g_fuse{1};    // W' contraction + following block product in one kernel
+// fusion switches: bit 0 the W' contraction + the block product after it in one kernel,
+// bit 1 the backward block product + its weight gradient in one kernel
+static std::atomic<int> g_fuse{3};
 static std::atomic<int> g_overlap{1};  // dx scatter beside the CNP backward (side stream)
 
 static bool use_umma() { return g_engine.load() == 0 && umma_supported(); }
@@ -130,18 +132,33 @@ poetx_status wprime_impl(poetx_dtype act, poetx_dtype wdt, const void* A, long l
 static int padded(int d, int b) { return (d + b - 1) / b * b; }
 static int last_block(int d, int b) { return d % b; }  // 0: the last block is whole
 
+// Appends the R side (m) and the P side (n) of a layer to a CNP side list.
+static bool add_layer_sides(CnpSides& sd, const poetx_layer* L) {
+  return sd.add(L->q_R, padded(L->m, L->b) / L->b, last_block(L->m, L->b)) &&
+         sd.add(L->q_P, padded(L->n, L->b) / L->b, last_block(L->n, L->b));
+}
+
 static CnpSides layer_sides(const poetx_layer* L) {
-  CnpSides sd{{L->q_R, L->q_P}, {padded(L->m, L->b) / L->b, padded(L->n, L->b) / L->b}};
-  sd.last[0] = last_block(L->m, L->b);
-  sd.last[1] = last_block(L->n, L->b);
+  CnpSides sd;
+  add_layer_sides(sd, L);
   return sd;
 }
 
 // The W' contraction and the block-diagonal product after it in one kernel (bf16 W', the
 // tensor-core engine, shapes the fused kernel takes).
 static bool fused_ok(const poetx_layer* L, long long N, int trans) {
-  return L->act == POETX_BF16 && L->wdt == POETX_BF16 && use_umma() && g_fuse.load() &&
+  return L->act == POETX_BF16 && L->wdt == POETX_BF16 && use_umma() && (g_fuse.load() & 1) &&
          umma_wprime_fusable(N, padded(L->m, L->b), padded(L->n, L->b), trans, L->b);
+}
+
+// The backward block product and its weight gradient in one kernel (bf16, b = 128 or 256):
+// on the P side always; on the R side unless the dx~ product is already fused into the
+// backward W' contraction.
+static bool bdw_ok(const poetx_layer* L) {
+  return L->act == POETX_BF16 && use_umma() && (g_fuse.load() & 2) && umma_bdw_ok(L->b);
+}
+static bool bdw_side_R(const poetx_layer* L, long long N) {
+  return bdw_ok(L) && !fused_ok(L, N, 1);
 }
 
 // ---------------------------------------------------------------- layer plumbing
@@ -150,8 +167,9 @@ struct Plan {
   size_t GR, GP, Q2R, Q2P, Qs, Bsv, Xsv, saved_total;
   // forward workspace
   size_t f_xt, f_A, f_B, f_zt, fwd_total;
-  // backward workspace
-  size_t b_cnp, b_xt, b_dzt, b_A, b_B, b_dB, b_dA, b_dxt, b_dGP, b_dGR, bwd_total;
+  // backward workspace: the chain's activations [0, bwd_chain), then the weight-gradient
+  // partials and the CNP backward's scratch
+  size_t b_xt, b_dzt, b_A, b_B, b_dB, b_dA, b_dxt, bwd_chain, b_dGP, b_dGR, b_cnp, bwd_total;
   int splitsR, splitsP;
 };
 
@@ -203,10 +221,15 @@ static Plan make_plan(const poetx_layer* L, long long N) {
   p.f_zt = take((size_t)N * n * as);
   p.fwd_total = o;
 
-  p.splitsR = wgrad_splits(N, (int)(m / b), L->b);
-  p.splitsP = wgrad_splits(N, (int)(n / b), L->b);
+  // token splits of the weight-gradient partials, from whichever kernel makes them; the
+  // partial buffers are sized for either, so a switch flipped between sizing and calling
+  // cannot overrun them
+  const int wsR = wgrad_splits(N, (int)(m / b), L->b), wsP = wgrad_splits(N, (int)(n / b), L->b);
+  const int fsR = bdw_splits(N, (int)(m / b), L->b), fsP = bdw_splits(N, (int)(n / b), L->b);
+  p.splitsR = bdw_side_R(L, N) ? fsR : wsR;
+  p.splitsP = bdw_ok(L) ? fsP : wsP;
+  const size_t maxR = (size_t)(wsR > fsR ? wsR : fsR), maxP = (size_t)(wsP > fsP ? wsP : fsP);
   o = 0;
-  p.b_cnp = take(cnp_bwd_scratch_bytes((int)((m + n) / b), (int)b));
   p.b_xt = L->variant == POETX_MEM ? take((size_t)N * m * as) : 0;
   p.b_dzt = take((size_t)N * n * as);
   p.b_A = L->variant == POETX_MEM ? take((size_t)N * m * as) : 0;
@@ -214,8 +237,10 @@ static Plan make_plan(const poetx_layer* L, long long N) {
   p.b_dB = take((size_t)N * n * as);
   p.b_dA = take((size_t)N * m * as);
   p.b_dxt = take((size_t)N * m * as);
-  p.b_dGP = take((size_t)p.splitsP * n * b * 4);
-  p.b_dGR = take((size_t)p.splitsR * m * b * 4);
+  p.bwd_chain = o;
+  p.b_dGP = take(maxP * n * b * 4);
+  p.b_dGR = take(maxR * m * b * 4);
+  p.b_cnp = take(cnp_bwd_scratch_bytes((int)((m + n) / b), (int)b));
   p.bwd_total = o;
   return p;
 }
@@ -260,7 +285,7 @@ static const T* at(const void* base, size_t off) {
 using namespace poetx;
 
 extern "C" poetx_status poetx_set_fusion(int on) {
-  if (on != 0 && on != 1) return POETX_ERR_ARG;
+  if (on < 0 || on > 3) return POETX_ERR_ARG;
   g_fuse.store(on);
   return POETX_OK;
 }
@@ -354,7 +379,10 @@ SideCtx g_side[64];    // per device
 
 // The device's side context, created on first use; nullptr when overlap is off or the
 // stream and events cannot be made (the calls then run everything on the caller's stream).
-static SideCtx* side_ctx() {
+// A stream capture that forks into the side stream keeps it in that capture until the
+// capture ends; a call on another stream in the meantime does not use it (its work would
+// land in that graph), and runs everything on its own stream instead.
+static SideCtx* side_ctx(cudaStream_t caller) {
   if (!g_overlap.load() || prof_enabled()) return nullptr;  // stage events need one stream
   int d = 0;
   if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= 64) return nullptr;
@@ -366,7 +394,23 @@ static SideCtx* side_ctx() {
     if (c.failed) cudaGetLastError();
     c.ready = !c.failed;
   }
-  return c.ready ? &c : nullptr;
+  if (!c.ready) return nullptr;
+  cudaStreamCaptureStatus side_st = cudaStreamCaptureStatusNone;
+  unsigned long long side_id = 0;
+  if (cudaStreamGetCaptureInfo(c.ss, &side_st, &side_id) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  if (side_st != cudaStreamCaptureStatusNone) {
+    cudaStreamCaptureStatus own_st = cudaStreamCaptureStatusNone;
+    unsigned long long own_id = 0;
+    if (cudaStreamGetCaptureInfo(caller, &own_st, &own_id) != cudaSuccess) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    if (own_st != cudaStreamCaptureStatusActive || own_id != side_id) return nullptr;
+  }
+  return &c;
 }
 
 extern "C" poetx_status poetx_set_overlap(int on) {
@@ -385,26 +429,71 @@ struct StepHooks {
   cudaEvent_t dx_done = nullptr;
 };
 
-static poetx_status layer_fwd_impl(const poetx_layer* L, const void* x, int N, void* y,
-                                   void* saved, void* ws, size_t ws_bytes, cudaStream_t stream,
-                                   const StepHooks& hk) {
+// The layer's G blocks and what its forward keeps for the backward (fast: B and x~).
+struct ChainSaved {
+  const void* GR;  // [mP/b, b, b], activation precision
+  const void* GP;  // [nP/b, b, b]
+  void* B;         // fast: B = A W'^T [N, nP]; mem: nullptr
+  void* xt;        // fast: x~ [N, mP]; mem: nullptr
+};
+
+static ChainSaved layer_chain_saved(const poetx_layer* L, const Plan& p, void* saved) {
+  const bool fast = L->variant == POETX_FAST;
+  return ChainSaved{at(saved, p.GR), at(saved, p.GP), fast ? at(saved, p.Bsv) : nullptr,
+                    fast ? at(saved, p.Xsv) : nullptr};
+}
+
+// S3-S7 from the G blocks: x~ = x[:, pi_m], A = x~ blkdiag(G_R), B = A W'^T,
+// z~ = B blkdiag(G_P), y[:, pi_n] = z~ (chain scratch at the Plan's forward offsets).
+static poetx_status chain_fwd(const poetx_layer* L, const Plan& p, const void* x, int N, void* y,
+                              const ChainSaved& cs, void* ws, cudaStream_t stream,
+                              const StepHooks& hk) {
+  if (N == 0) return POETX_OK;
+  // m, n: the features of x and y; mP, nP: the padded widths of every internal array
+  const int b = L->b, m = L->m, n = L->n, mP = padded(m, b), nP = padded(n, b);
+  const poetx_dtype act = L->act;
+  const size_t as = dtype_size(act);
+  // fast keeps x~ and B for the backward (what default autograd keeps), mem keeps neither
+  void* xt = cs.xt ? cs.xt : at(ws, p.f_xt);
+  void* A = at(ws, p.f_A);
+  void* B = cs.B ? cs.B : at(ws, p.f_B);
+  if (hk.x_ready) POETX_CUDA_TRY(cudaStreamWaitEvent(stream, hk.x_ready, 0));
+  POETX_TRY(launch_perm_rows(as, false, x, N, m, L->perm_m, xt, nullptr, nullptr, nullptr, stream,
+                             m, mP));
+  POETX_TRY(blockdiag_impl(act, xt, N, mP / b, b, cs.GR, 0, nullptr, nullptr, A, stream));
+  void* zt = at(ws, p.f_zt);
+  if (fused_ok(L, N, 0)) {
+    // S5 + S6 on the same tiles (mem does not keep B)
+    POETX_TRY(umma_wprime_fused(A, N, mP, nP, L->Wp, 0, cs.GP, b, cs.B, zt, stream));
+  } else {
+    POETX_TRY(wprime_impl(act, L->wdt, A, N, mP, nP, L->Wp, L->w_scale, 0, B, stream));
+    POETX_TRY(blockdiag_impl(act, B, N, nP / b, b, cs.GP, 0, nullptr, nullptr, zt, stream));
+  }
+  // S7.  (Storing z~ through the permutation inside the product is supported, but its
+  // 2-byte scattered stores are slower than this coalesced scatter pass.)
+  return launch_perm_rows(as, true, zt, N, n, L->perm_n, y, nullptr, nullptr, nullptr, stream,
+                          nP, n);
+}
+
+static poetx_status check_fwd_args(const poetx_layer* L, const void* x, int N, void* y,
+                                   void* saved, void* ws) {
   POETX_TRY(validate(L));
   if (N < 0) return POETX_ERR_ARG;
   if (!saved || !ws || (N > 0 && (!x || !y))) return POETX_ERR_ARG;
   if (!aligned16(saved) || !aligned16(ws) || (N > 0 && (!aligned16(x) || !aligned16(y))))
     return POETX_ERR_ALIGN;
+  return POETX_OK;
+}
+
+static poetx_status layer_fwd_impl(const poetx_layer* L, const void* x, int N, void* y,
+                                   void* saved, void* ws, size_t ws_bytes, cudaStream_t stream,
+                                   const StepHooks& hk) {
+  POETX_TRY(check_fwd_args(L, x, N, y, saved, ws));
   const Plan p = make_plan(L, N);
   if (ws_bytes < p.fwd_total) return POETX_ERR_WORKSPACE;
-  // m, n: the features of x and y; mP, nP: the padded widths of every internal array
-  const int b = L->b, m = L->m, n = L->n, mP = padded(m, b), nP = padded(n, b);
-  const poetx_dtype act = L->act;
-  const bool f32 = act == POETX_F32;
-  const size_t as = dtype_size(act);
+  const int b = L->b;
+  const bool f32 = L->act == POETX_F32;
   prof_begin(stream);
-  // fast keeps x~ and B for the backward (what default autograd keeps), mem keeps neither
-  void* xt = L->variant == POETX_FAST ? at(saved, p.Xsv) : at(ws, p.f_xt);
-  void* A = at(ws, p.f_A);
-  void* B = L->variant == POETX_FAST ? at(saved, p.Bsv) : at(ws, p.f_B);
   // S1-S2: both CNPs in one pass over the m/b + n/b blocks; G in the activation precision
   // and Q^2 kept for the backward.  (Running the x gather beside them on the side stream
   // was measured: the CNP kernels slowed by about what the gather saved, and the join cost
@@ -413,24 +502,7 @@ static poetx_status layer_fwd_impl(const poetx_layer* L, const void* x, int N, v
   POETX_TRY(cnp_forward_sides(sides, b, at<float>(saved, p.Qs), at<float>(saved, p.Q2R),
                               f32 ? at<float>(saved, p.GR) : nullptr,
                               f32 ? nullptr : at(saved, p.GR), nullptr, stream));
-  if (N == 0) return POETX_OK;
-  if (hk.x_ready) POETX_CUDA_TRY(cudaStreamWaitEvent(stream, hk.x_ready, 0));
-  POETX_TRY(launch_perm_rows(as, false, x, N, m, L->perm_m, xt, nullptr, nullptr, nullptr, stream,
-                             m, mP));
-  POETX_TRY(blockdiag_impl(act, xt, N, mP / b, b, at(saved, p.GR), 0, nullptr, nullptr, A, stream));
-  void* zt = at(ws, p.f_zt);
-  if (fused_ok(L, N, 0)) {
-    // S5 + S6 on the same tiles (mem does not keep B)
-    POETX_TRY(umma_wprime_fused(A, N, mP, nP, L->Wp, 0, at(saved, p.GP), b,
-                                L->variant == POETX_FAST ? B : nullptr, zt, stream));
-  } else {
-    POETX_TRY(wprime_impl(act, L->wdt, A, N, mP, nP, L->Wp, L->w_scale, 0, B, stream));
-    POETX_TRY(blockdiag_impl(act, B, N, nP / b, b, at(saved, p.GP), 0, nullptr, nullptr, zt, stream));
-  }
-  // S7.  (Storing z~ through the permutation inside the product is supported, but its
-  // 2-byte scattered stores are slower than this coalesced scatter pass.)
-  return launch_perm_rows(as, true, zt, N, n, L->perm_n, y, nullptr, nullptr, nullptr, stream,
-                          nP, n);
+  return chain_fwd(L, p, x, N, y, layer_chain_saved(L, p, saved), ws, stream, hk);
 }
 
 extern "C" poetx_status poetx_layer_fwd(const poetx_layer* L, const void* x, int N, void* y,
@@ -439,31 +511,23 @@ extern "C" poetx_status poetx_layer_fwd(const poetx_layer* L, const void* x, int
   return layer_fwd_impl(L, x, N, y, saved, ws, ws_bytes, stream, StepHooks{});
 }
 
-static poetx_status layer_bwd_impl(const poetx_layer* L, const void* x, const void* dy, int N,
-                                   const void* saved, void* dx, float* dq_R, float* dq_P,
-                                   int accumulate, void* ws, size_t ws_bytes, cudaStream_t stream,
-                                   const StepHooks& hk, const PackAdam* pa = nullptr) {
-  POETX_TRY(validate(L));
-  if (N < 0) return POETX_ERR_ARG;
-  if (!saved || !ws || !dq_R || !dq_P || (N > 0 && (!x || !dy || !dx))) return POETX_ERR_ARG;
-  if (!aligned16(saved) || !aligned16(ws) ||
-      (N > 0 && (!aligned16(x) || !aligned16(dy) || !aligned16(dx))))
-    return POETX_ERR_ALIGN;
-  const Plan p = make_plan(L, N);
-  if (ws_bytes < p.bwd_total) return POETX_ERR_WORKSPACE;
+// S8-S13 from the G blocks and what the forward kept: dz~ = dy[:, pi_n], the weight-gradient
+// partials dG_P [splitsP, nP/b, b, b] and dG_R [splitsR, mP/b, b, b], dx[:, pi_m] = dx~
+// (chain scratch at the Plan's backward offsets).  With `side` set, the dx scatter runs on the
+// side stream, forked here after the G_R weight gradient; the caller joins it (and holds the
+// side stream's lock).
+static poetx_status chain_bwd(const poetx_layer* L, const Plan& p, const void* x, const void* dy,
+                              int N, const ChainSaved& cs, void* dx, float* dGR, float* dGP,
+                              void* ws, cudaStream_t stream, const StepHooks& hk,
+                              SideCtx* side) {
   const int b = L->b, m = L->m, n = L->n, mP = padded(m, b), nP = padded(n, b);
   const poetx_dtype act = L->act;
   const size_t as = dtype_size(act);
-  prof_begin(stream);
   const bool fast = L->variant == POETX_FAST;
-  const void* xt = fast ? at(saved, p.Xsv) : at(ws, p.b_xt);
+  const void* xt = fast ? cs.xt : at(ws, p.b_xt);
   void* dzt = at(ws, p.b_dzt);
   void* dB = at(ws, p.b_dB);
   void* dA = at(ws, p.b_dA);
-  float* dGP = at<float>(ws, p.b_dGP);
-  float* dGR = at<float>(ws, p.b_dGR);
-  const void* GR = at(saved, p.GR);
-  const void* GP = at(saved, p.GP);
   if (N > 0) {
     if (!fast)  // mem: x~ is recomputed
       POETX_TRY(launch_perm_rows(as, false, x, N, m, L->perm_m, at(ws, p.b_xt), nullptr, nullptr,
@@ -473,57 +537,101 @@ static poetx_status layer_bwd_impl(const poetx_layer* L, const void* x, const vo
                                stream, n, nP));
   }
   const void* B;
-  if (L->variant == POETX_MEM) {  // recompute B = (x~ blkdiag(G_R)) W'^T
+  if (!fast) {  // recompute B = (x~ blkdiag(G_R)) W'^T
     void* A = at(ws, p.b_A);
     void* Bw = at(ws, p.b_B);
-    POETX_TRY(blockdiag_impl(act, xt, N, mP / b, b, GR, 0, nullptr, nullptr, A, stream));
+    POETX_TRY(blockdiag_impl(act, xt, N, mP / b, b, cs.GR, 0, nullptr, nullptr, A, stream));
     POETX_TRY(wprime_impl(act, L->wdt, A, N, mP, nP, L->Wp, L->w_scale, 0, Bw, stream));
     B = Bw;
   } else {
-    B = at(saved, p.Bsv);
+    B = cs.B;
   }
-  POETX_TRY(wgrad_impl(act, B, dzt, N, nP / b, b, p.splitsP, dGP, stream));
-  // int8 weight: dA = dB diag(s) W_q, the row scale is folded into dB's columns
-  POETX_TRY(blockdiag_impl(act, dzt, N, nP / b, b, GP, 1,
-                           L->wdt == POETX_I8 ? L->w_scale : nullptr, nullptr, dB, stream));
+  const float* colscale = L->wdt == POETX_I8 ? L->w_scale : nullptr;
+  if (bdw_ok(L)) {
+    // S10 in one pass over dz~: dB = dz~ blkdiag(G_P)^T and dG_P = B^T dz~ (int8 weight:
+    // dA = dB diag(s) W_q, the row scale folded into dB's columns)
+    POETX_TRY(umma_bdw(dzt, B, N, nP / b, b, cs.GP, colscale, dB, p.splitsP, dGP, stream));
+  } else {
+    POETX_TRY(wgrad_impl(act, B, dzt, N, nP / b, b, p.splitsP, dGP, stream));
+    POETX_TRY(blockdiag_impl(act, dzt, N, nP / b, b, cs.GP, 1, colscale, nullptr, dB, stream));
+  }
   void* dxt = at(ws, p.b_dxt);
   if (fused_ok(L, N, 1)) {
     // S11 + the dx~ half of S12 on the same tiles
-    POETX_TRY(umma_wprime_fused(dB, N, mP, nP, L->Wp, 1, GR, b, dA, dxt, stream));
+    POETX_TRY(umma_wprime_fused(dB, N, mP, nP, L->Wp, 1, cs.GR, b, dA, dxt, stream));
+    POETX_TRY(wgrad_impl(act, xt, dA, N, mP / b, b, p.splitsR, dGR, stream));
   } else {
     POETX_TRY(wprime_impl(act, L->wdt, dB, N, mP, nP, L->Wp, L->w_scale, 1, dA, stream));
-    POETX_TRY(blockdiag_impl(act, dA, N, mP / b, b, GR, 1, nullptr, nullptr, dxt, stream));
+    if (bdw_side_R(L, N)) {
+      // S12 in one pass over dA: dx~ = dA blkdiag(G_R)^T and dG_R = x~^T dA
+      POETX_TRY(umma_bdw(dA, xt, N, mP / b, b, cs.GR, nullptr, dxt, p.splitsR, dGR, stream));
+    } else {
+      POETX_TRY(blockdiag_impl(act, dA, N, mP / b, b, cs.GR, 1, nullptr, nullptr, dxt, stream));
+      POETX_TRY(wgrad_impl(act, xt, dA, N, mP / b, b, p.splitsR, dGR, stream));
+    }
   }
-  poetx_status st = wgrad_impl(act, xt, dA, N, mP / b, b, p.splitsR, dGR, stream);
+  if (N == 0) return POETX_OK;
+  if (side) {
+    POETX_CUDA_TRY(cudaEventRecord(side->fork, stream));
+    POETX_CUDA_TRY(cudaStreamWaitEvent(side->ss, side->fork, 0));
+    const poetx_status st = launch_perm_rows_side(as, true, dxt, N, m, L->perm_m, dx, side->ss, mP, m);
+    if (cudaEventRecord(side->join, side->ss) != cudaSuccess && st == POETX_OK) return POETX_ERR_CUDA;
+    return st;
+  }
+  POETX_TRY(launch_perm_rows(as, true, dxt, N, m, L->perm_m, dx, nullptr, nullptr, nullptr, stream,
+                             mP, m));
+  if (hk.dx_done) POETX_CUDA_TRY(cudaEventRecord(hk.dx_done, stream));
+  return POETX_OK;
+}
+
+static poetx_status check_bwd_args(const poetx_layer* L, const void* x, const void* dy, int N,
+                                   const void* saved, void* dx, const void* ws) {
+  POETX_TRY(validate(L));
+  if (N < 0) return POETX_ERR_ARG;
+  if (!saved || !ws || (N > 0 && (!x || !dy || !dx))) return POETX_ERR_ARG;
+  if (!aligned16(saved) || !aligned16(ws) ||
+      (N > 0 && (!aligned16(x) || !aligned16(dy) || !aligned16(dx))))
+    return POETX_ERR_ALIGN;
+  return POETX_OK;
+}
+
+static poetx_status layer_bwd_impl(const poetx_layer* L, const void* x, const void* dy, int N,
+                                   const void* saved, void* dx, float* dq_R, float* dq_P,
+                                   int accumulate, void* ws, size_t ws_bytes, cudaStream_t stream,
+                                   const StepHooks& hk, const PackAdam* pa = nullptr) {
+  POETX_TRY(check_bwd_args(L, x, dy, N, saved, dx, ws));
+  if (!dq_R || !dq_P) return POETX_ERR_ARG;
+  const Plan p = make_plan(L, N);
+  if (ws_bytes < p.bwd_total) return POETX_ERR_WORKSPACE;
+  const int b = L->b;
+  const size_t as = dtype_size(L->act);
+  prof_begin(stream);
+  float* dGP = at<float>(ws, p.b_dGP);
+  float* dGR = at<float>(ws, p.b_dGR);
   // S13 beside S14 when it can: the dx scatter does not feed the CNP backward.  It is
   // forked after the G_R weight gradient (a whole-GPU kernel that it would slow down), and
   // not when a download waits for dx (dx_done): the co-resident scatter is slower than the
   // whole-GPU one, and dx is then needed as early as possible.
   std::unique_lock<std::mutex> lk(g_side_mu, std::defer_lock);
   SideCtx* sc = nullptr;
-  if (st == POETX_OK && N > 0 && !hk.dx_done && perm_side_fits(as, m)) {
+  if (N > 0 && !hk.dx_done && perm_side_fits(as, L->m)) {
     lk.lock();
-    sc = side_ctx();
+    sc = side_ctx(stream);
     if (!sc) lk.unlock();
   }
-  if (sc) {
-    POETX_CUDA_TRY(cudaEventRecord(sc->fork, stream));
-    POETX_CUDA_TRY(cudaStreamWaitEvent(sc->ss, sc->fork, 0));
-    st = launch_perm_rows_side(as, true, dxt, N, m, L->perm_m, dx, sc->ss, mP, m);
-    if (cudaEventRecord(sc->join, sc->ss) != cudaSuccess && st == POETX_OK) st = POETX_ERR_CUDA;
-  } else if (st == POETX_OK && N > 0) {
-    st = launch_perm_rows(as, true, dxt, N, m, L->perm_m, dx, nullptr, nullptr, nullptr, stream,
-                          mP, m);
-    if (st == POETX_OK && hk.dx_done && cudaEventRecord(hk.dx_done, stream) != cudaSuccess)
-      st = POETX_ERR_CUDA;
-  }
+  poetx_status st = chain_bwd(L, p, x, dy, N, layer_chain_saved(L, p, const_cast<void*>(saved)),
+                              dx, dGR, dGP, ws, stream, hk, sc);
   if (st == POETX_OK) {
     const CnpSides sides = layer_sides(L);
-    const float* const dGs[2] = {dGR, dGP};
-    const int splits[2] = {p.splitsR, p.splitsP};
-    float* const dqs[2] = {dq_R, dq_P};
-    st = cnp_backward_sides(sides, at<float>(saved, p.Qs), at<float>(saved, p.Q2R), dGs, splits,
-                            b, dqs, accumulate, at(ws, p.b_cnp), stream, pa);
+    CnpGrads gr;
+    gr.dG[0] = dGR;
+    gr.dG[1] = dGP;
+    gr.splits[0] = p.splitsR;
+    gr.splits[1] = p.splitsP;
+    gr.dq[0] = dq_R;
+    gr.dq[1] = dq_P;
+    st = cnp_backward_sides(sides, at<float>(saved, p.Qs), at<float>(saved, p.Q2R), gr, b,
+                            accumulate, at(ws, p.b_cnp), stream, pa);
   }
   if (sc && cudaStreamWaitEvent(stream, sc->join, 0) != cudaSuccess && st == POETX_OK)
     st = POETX_ERR_CUDA;
@@ -559,6 +667,177 @@ extern "C" poetx_status poetx_layer_bwd_adam(const poetx_layer* L, const void* x
   pa.v[1] = v_P;
   return layer_bwd_impl(L, x, dy, N, saved, dx, dq_R, dq_P, accumulate, ws, ws_bytes, stream,
                         StepHooks{}, &pa);
+}
+
+// ---------------------------------------------------------------- layer groups
+// The layers of a group (e.g. the linears of a transformer block) share one stack of CNP
+// blocks: layer i's R blocks, then its P blocks, for i = 0, 1, ...  Its Q, Q^2 and G are
+// computed by one CNP forward over the whole stack and its dq by one CNP backward, so that
+// a block's few hundred small b x b products fill the GPU in a few launches instead of a
+// latency-bound wave per layer; each layer's forward and backward chain runs on its own
+// between them.  saved: the stacks, then per layer what its forward keeps (fast: B and x~).
+// ws: the chain scratch (one region shared by the layers, which run one after the other
+// on the caller's stream), every layer's weight-gradient partials (written by its backward
+// chain, read by the group's CNP backward) and the CNP backward's scratch.
+constexpr int kMaxGroup = kMaxSides / 2;
+static_assert(kMaxGroup == POETX_GROUP_MAX_LAYERS, "group size limit");
+
+struct GroupPlan {
+  int count = 0;
+  int blk0[kMaxGroup + 1] = {};  // first stack block of layer i (R side, then P side)
+  size_t G = 0, Qs = 0, Q2 = 0;
+  size_t Bsv[kMaxGroup] = {}, Xsv[kMaxGroup] = {};
+  size_t saved_total = 0;
+  size_t chain = 0, chain_bytes = 0;
+  size_t dGR[kMaxGroup] = {}, dGP[kMaxGroup] = {};
+  size_t cnp = 0, ws_total = 0;
+  Plan lp[kMaxGroup];
+};
+
+static poetx_status validate_group(const poetx_layer* Ls, int count) {
+  if (!Ls || count < 1 || count > kMaxGroup) return POETX_ERR_ARG;
+  for (int i = 0; i < count; ++i) {
+    POETX_TRY(validate(&Ls[i]));
+    if (Ls[i].b != Ls[0].b) return POETX_ERR_SHAPE;
+    if (Ls[i].act != Ls[0].act) return POETX_ERR_DTYPE;
+  }
+  return POETX_OK;
+}
+
+static GroupPlan group_plan(const poetx_layer* Ls, int count, long long N) {
+  GroupPlan g;
+  g.count = count;
+  const size_t b = Ls[0].b;
+  const size_t gs = Ls[0].act == POETX_F32 ? 4 : 2;
+  for (int i = 0; i < count; ++i) {
+    g.lp[i] = make_plan(&Ls[i], N);
+    g.blk0[i + 1] = g.blk0[i] + (padded(Ls[i].m, Ls[i].b) + padded(Ls[i].n, Ls[i].b)) / Ls[i].b;
+  }
+  const size_t nb = g.blk0[count];
+  size_t o = 0;
+  auto take = [&](size_t bytes) { size_t r = o; o += align_up(bytes, 256); return r; };
+  g.G = take(nb * b * b * gs);
+  g.Qs = take(nb * b * b * 4);
+  g.Q2 = take(nb * b * b * 4);
+  for (int i = 0; i < count; ++i) {
+    const bool fast = Ls[i].variant == POETX_FAST;
+    const size_t as = dtype_size(Ls[i].act);
+    const size_t m = padded(Ls[i].m, Ls[i].b), n = padded(Ls[i].n, Ls[i].b);
+    g.Bsv[i] = fast ? take((size_t)N * n * as) : 0;
+    g.Xsv[i] = fast ? take((size_t)N * m * as) : 0;
+  }
+  g.saved_total = o;
+  o = 0;
+  for (int i = 0; i < count; ++i) {
+    const size_t need = g.lp[i].fwd_total > g.lp[i].bwd_chain ? g.lp[i].fwd_total : g.lp[i].bwd_chain;
+    if (need > g.chain_bytes) g.chain_bytes = need;
+  }
+  g.chain = take(g.chain_bytes);
+  for (int i = 0; i < count; ++i) {
+    const size_t m = padded(Ls[i].m, Ls[i].b), n = padded(Ls[i].n, Ls[i].b);
+    g.dGR[i] = take((size_t)g.lp[i].splitsR * m * b * 4);
+    g.dGP[i] = take((size_t)g.lp[i].splitsP * n * b * 4);
+  }
+  g.cnp = take(cnp_bwd_scratch_bytes((int)nb, (int)b));
+  g.ws_total = o;
+  return g;
+}
+
+static CnpSides group_sides(const poetx_layer* Ls, int count) {
+  CnpSides sd;
+  for (int i = 0; i < count; ++i) add_layer_sides(sd, &Ls[i]);
+  return sd;
+}
+
+static ChainSaved group_chain_saved(const poetx_layer* Ls, const GroupPlan& g, int i,
+                                    const void* saved) {
+  const size_t b = Ls[0].b, gs = Ls[0].act == POETX_F32 ? 4 : 2;
+  const size_t r0 = (size_t)g.blk0[i], p0 = r0 + padded(Ls[i].m, Ls[i].b) / Ls[i].b;
+  void* sv = const_cast<void*>(saved);
+  const bool fast = Ls[i].variant == POETX_FAST;
+  return ChainSaved{at(sv, g.G + r0 * b * b * gs), at(sv, g.G + p0 * b * b * gs),
+                    fast ? at(sv, g.Bsv[i]) : nullptr, fast ? at(sv, g.Xsv[i]) : nullptr};
+}
+
+extern "C" size_t poetx_group_saved_bytes(const poetx_layer* Ls, int count, int N) {
+  if (validate_group(Ls, count) != POETX_OK || N < 0) return 0;
+  return group_plan(Ls, count, N).saved_total;
+}
+
+extern "C" size_t poetx_group_workspace_bytes(const poetx_layer* Ls, int count, int N) {
+  if (validate_group(Ls, count) != POETX_OK || N < 0) return 0;
+  return group_plan(Ls, count, N).ws_total;
+}
+
+extern "C" poetx_status poetx_group_cnp_fwd(const poetx_layer* Ls, int count, int N, void* saved,
+                                            cudaStream_t stream) {
+  POETX_TRY(validate_group(Ls, count));
+  if (N < 0 || !saved) return POETX_ERR_ARG;
+  if (!aligned16(saved)) return POETX_ERR_ALIGN;
+  const GroupPlan g = group_plan(Ls, count, N);
+  const bool f32 = Ls[0].act == POETX_F32;
+  prof_begin(stream);
+  return cnp_forward_sides(group_sides(Ls, count), Ls[0].b, at<float>(saved, g.Qs),
+                           at<float>(saved, g.Q2), f32 ? at<float>(saved, g.G) : nullptr,
+                           f32 ? nullptr : at(saved, g.G), nullptr, stream);
+}
+
+extern "C" poetx_status poetx_group_layer_fwd(const poetx_layer* Ls, int count, int i,
+                                              const void* x, int N, void* y, void* saved,
+                                              void* ws, size_t ws_bytes, cudaStream_t stream) {
+  POETX_TRY(validate_group(Ls, count));
+  if (i < 0 || i >= count) return POETX_ERR_ARG;
+  POETX_TRY(check_fwd_args(&Ls[i], x, N, y, saved, ws));
+  const GroupPlan g = group_plan(Ls, count, N);
+  if (ws_bytes < g.ws_total) return POETX_ERR_WORKSPACE;
+  prof_begin(stream);
+  return chain_fwd(&Ls[i], g.lp[i], x, N, y, group_chain_saved(Ls, g, i, saved),
+                   at(ws, g.chain), stream, StepHooks{});
+}
+
+extern "C" poetx_status poetx_group_layer_bwd(const poetx_layer* Ls, int count, int i,
+                                              const void* x, const void* dy, int N,
+                                              const void* saved, void* dx, void* ws,
+                                              size_t ws_bytes, cudaStream_t stream) {
+  POETX_TRY(validate_group(Ls, count));
+  if (i < 0 || i >= count) return POETX_ERR_ARG;
+  POETX_TRY(check_bwd_args(&Ls[i], x, dy, N, saved, dx, ws));
+  const GroupPlan g = group_plan(Ls, count, N);
+  if (ws_bytes < g.ws_total) return POETX_ERR_WORKSPACE;
+  prof_begin(stream);
+  // the dx scatter stays on the caller's stream: the next layer's chain follows it, not a
+  // CNP backward it could hide under
+  return chain_bwd(&Ls[i], g.lp[i], x, dy, N, group_chain_saved(Ls, g, i, saved), dx,
+                   at<float>(ws, g.dGR[i]), at<float>(ws, g.dGP[i]), at(ws, g.chain), stream,
+                   StepHooks{}, nullptr);
+}
+
+extern "C" poetx_status poetx_group_cnp_bwd(const poetx_layer* Ls, int count, int N,
+                                            const void* saved, float* const* dq_R,
+                                            float* const* dq_P, int accumulate, void* ws,
+                                            size_t ws_bytes, cudaStream_t stream) {
+  POETX_TRY(validate_group(Ls, count));
+  if (N < 0 || !saved || !ws || !dq_R || !dq_P) return POETX_ERR_ARG;
+  if (!aligned16(saved) || !aligned16(ws)) return POETX_ERR_ALIGN;
+  for (int i = 0; i < count; ++i) {
+    if (!dq_R[i] || !dq_P[i]) return POETX_ERR_ARG;
+    if (!aligned16(dq_R[i]) || !aligned16(dq_P[i])) return POETX_ERR_ALIGN;
+  }
+  const GroupPlan g = group_plan(Ls, count, N);
+  if (ws_bytes < g.ws_total) return POETX_ERR_WORKSPACE;
+  prof_begin(stream);
+  CnpGrads gr;
+  for (int i = 0; i < count; ++i) {
+    gr.dG[2 * i] = at<float>(ws, g.dGR[i]);
+    gr.splits[2 * i] = g.lp[i].splitsR;
+    gr.dq[2 * i] = dq_R[i];
+    gr.dG[2 * i + 1] = at<float>(ws, g.dGP[i]);
+    gr.splits[2 * i + 1] = g.lp[i].splitsP;
+    gr.dq[2 * i + 1] = dq_P[i];
+  }
+  return cnp_backward_sides(group_sides(Ls, count), at<float>(saved, g.Qs),
+                            at<float>(saved, g.Q2), gr, Ls[0].b, accumulate, at(ws, g.cnp),
+                            stream);
 }
 
 // ---------------------------------------------------------------- host-buffer step

@@ -63,28 +63,6 @@ struct UmmaParams {
 constexpr int BM = 128;
 constexpr int BK = 64;
 
-__host__ __device__ constexpr uint32_t make_idesc(int M, int N, bool a_mn, bool b_mn) {
-  return (1u << 4)                        // accumulator: f32
-         | (1u << 7)                      // A: bf16
-         | (1u << 10)                     // B: bf16
-         | ((a_mn ? 1u : 0u) << 15)       // A major: 0 = K, 1 = MN
-         | ((b_mn ? 1u : 0u) << 16)       // B major
-         | ((uint32_t)(N >> 3) << 17)     // N / 8
-         | ((uint32_t)(M >> 4) << 24);    // M / 16
-}
-
-// Shared-memory matrix descriptor: start address, leading / stride byte offsets (16-byte
-// units), descriptor version 1 (tcgen05), 128-byte swizzle.
-__device__ __forceinline__ uint64_t make_sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-  uint64_t d = 0;
-  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
-  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
-  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
-  d |= (uint64_t)1 << 46;
-  d |= (uint64_t)2 << 61;
-  return d;
-}
-
 // K-major tile: rows of 128 bytes (64 bf16 along K), 8-row groups 1024 bytes apart; the
 // k-th K=16 slice starts 32 bytes further.  MN-major tile: boxes of 64 K-rows x 64 MN
 // elements (8 KB) side by side along MN (LBO = 8 KB), 8 K-row groups 1024 bytes apart; the
@@ -931,16 +909,6 @@ struct I8Params {
   unsigned long long limit_ns;
 };
 
-__device__ __forceinline__ void umma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
-                                             uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
 __global__ void __launch_bounds__(I8_THREADS, 1)
     umma_i8_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                    const I8Params p) {
@@ -1197,47 +1165,10 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// 2-D bf16 tensor [outer][inner] with row pitch `pitch_elems`, box {box_inner, box_outer},
-// 128-byte swizzle, zero fill out of bounds.  Encoded maps are kept in a small per-thread
-// cache keyed by every argument, since training loops pass the same buffers every step.
 bool make_map_t(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer,
                 uint64_t pitch_elems, uint32_t box_inner, uint32_t box_outer, bool i8) {
-  struct Entry {
-    const void* ptr;
-    uint64_t inner, outer, pitch;
-    uint32_t bi, bo;
-    int dev, i8;
-    CUtensorMap map;
-  };
-  constexpr int kEntries = 64;
-  thread_local Entry cache[kEntries];
-  thread_local int next = 0;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  for (int i = 0; i < kEntries; ++i) {
-    const Entry& e = cache[i];
-    if (e.ptr == ptr && ptr && e.inner == inner && e.outer == outer && e.pitch == pitch_elems &&
-        e.bi == box_inner && e.bo == box_outer && e.dev == dev && e.i8 == (int)i8) {
-      *m = e.map;
-      return true;
-    }
-  }
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[2] = {inner, outer};
-  cuuint64_t strides[1] = {pitch_elems * (i8 ? 1 : 2)};
-  cuuint32_t box[2] = {box_inner, box_outer};
-  cuuint32_t es[2] = {1, 1};
-  if (fn(m, i8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
-         const_cast<void*>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-         i8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
-         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-    return false;
-  Entry& e = cache[next];
-  next = (next + 1) % kEntries;
-  e.ptr = ptr; e.inner = inner; e.outer = outer; e.pitch = pitch_elems;
-  e.bi = box_inner; e.bo = box_outer; e.dev = dev; e.i8 = (int)i8; e.map = *m;
-  return true;
+  return i8 ? encode_tma_2d(m, ptr, TMA_U8, inner, outer, pitch_elems, box_inner, box_outer, false)
+            : encode_tma_2d(m, ptr, TMA_BF16, inner, outer, pitch_elems, box_inner, box_outer, true);
 }
 
 // 2-D bf16 tensor [outer][inner] with row pitch `pitch_elems`, box {box_inner, box_outer},
@@ -1311,6 +1242,55 @@ UmmaParams base_params() {
 }
 
 }  // namespace
+
+// 2-D tensor [outer][inner] of element type et with row pitch `pitch_elems`, box {box_inner,
+// box_outer}, 128-byte swizzle or none, zero fill out of bounds.  Encoded maps are kept in a
+// small per-thread cache keyed by every argument, since training loops pass the same buffers
+// every step.
+bool encode_tma_2d(CUtensorMap* m, const void* ptr, TmaElem et, uint64_t inner, uint64_t outer,
+                   uint64_t pitch_elems, uint32_t box_inner, uint32_t box_outer, bool swizzle128) {
+  struct Entry {
+    const void* ptr;
+    uint64_t inner, outer, pitch;
+    uint32_t bi, bo;
+    int dev, et, sw;
+    CUtensorMap map;
+  };
+  constexpr int kEntries = 64;
+  thread_local Entry cache[kEntries];
+  thread_local int next = 0;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  for (int i = 0; i < kEntries; ++i) {
+    const Entry& e = cache[i];
+    if (e.ptr == ptr && ptr && e.inner == inner && e.outer == outer && e.pitch == pitch_elems &&
+        e.bi == box_inner && e.bo == box_outer && e.dev == dev && e.et == (int)et &&
+        e.sw == (int)swizzle128) {
+      *m = e.map;
+      return true;
+    }
+  }
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const uint64_t esz = et == TMA_U8 ? 1 : (et == TMA_BF16 ? 2 : 4);
+  const CUtensorMapDataType dt = et == TMA_U8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                 : (et == TMA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                   : CU_TENSOR_MAP_DATA_TYPE_FLOAT32);
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {pitch_elems * esz};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t es[2] = {1, 1};
+  if (fn(m, dt, 2, const_cast<void*>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+         swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  Entry& e = cache[next];
+  next = (next + 1) % kEntries;
+  e.ptr = ptr; e.inner = inner; e.outer = outer; e.pitch = pitch_elems;
+  e.bi = box_inner; e.bo = box_outer; e.dev = dev; e.et = (int)et; e.sw = (int)swizzle128;
+  e.map = *m;
+  return true;
+}
 
 bool umma_supported() {
   // sm_103 and a driver entry point for tensor maps; cached per device

@@ -2,7 +2,9 @@
 
 This module draws random arrays and rounds them to their storage dtype; it holds none of
 the method's arithmetic.  The fp64 oracle (through the tests and the CPU-baseline leg of
-the benchmark) and the CUDA path both consume exactly the arrays produced here.
+the benchmark) and the CUDA path both consume exactly the arrays produced here; the
+benchmark's timed full-size workloads draw the same distributions on the device instead
+(``device_layer_inputs``), where no oracle reads them.
 
 Generator: numpy's Philox4x32-10 counter-based bit generator (Salmon et al., SC'11),
 keyed by (seed, crc32(tensor name)) so that every tensor has its own sub-stream and the
@@ -45,10 +47,14 @@ def round_to(a: np.ndarray, dtype: str) -> np.ndarray:
     if dtype == "f32":
         return f32.astype(np.float64)
     if dtype == "bf16":
-        u = f32.view(np.uint32).astype(np.uint64)
-        # round-to-nearest-even on the 16 dropped mantissa bits (no NaN/Inf is ever drawn)
-        u = (u + 0x7FFF + ((u >> 16) & 1)) & 0xFFFF0000
-        return u.astype(np.uint32).view(np.float32).astype(np.float64)
+        # round-to-nearest-even on the 16 dropped mantissa bits, in 32-bit integers: the sum
+        # stays below 2^32 for every finite value (no NaN is ever drawn)
+        u = f32.view(np.uint32)
+        r = (u >> 16) & np.uint32(1)
+        r += np.uint32(0x7FFF)
+        r += u
+        r &= np.uint32(0xFFFF0000)
+        return r.view(np.float32).astype(np.float64)
     raise ValueError(f"unknown dtype {dtype}")
 
 
@@ -158,3 +164,44 @@ def dG_inputs(seed: int, splits: int, nblk: int, b: int, name: str = "dG") -> np
 
 def workload_names() -> List[str]:
     return list(WORKLOADS)
+
+
+def device_layer_inputs(wl: Workload, layer: LayerShape, device, N: int | None = None):
+    """The tensors of ``layer_inputs`` drawn on a CUDA device by torch's Philox generator,
+    for the benchmark's full-size workloads (numpy draws a Llama-8B block's ~1e9 values in
+    minutes).  Same names, shapes, distributions and storage dtypes, each tensor keyed by
+    (seed, crc32(name)) as above; the values differ from the numpy draw, so parity tests use
+    ``layer_inputs``.  Returns torch tensors on ``device``: x, dy in the activation dtype,
+    W0 (fp32 for an int8-stored weight), q_R, q_P fp32, perm_m, perm_n int32."""
+    import torch
+
+    N = wl.N if N is None else N
+    s, tag, b = wl.seed, f"{layer.name}/", wl.b
+    m, n = layer.m, layer.n
+    tdt = {"f32": torch.float32, "bf16": torch.bfloat16}
+    wstore = "f32" if wl.wdt == "i8" else wl.wdt
+    tri = b * (b - 1) // 2
+
+    def gen(name):
+        g = torch.Generator(device=device)
+        g.manual_seed(((int(s) & 0xFFFFFFFF) << 32) | zlib.crc32((tag + name).encode()))
+        return g
+
+    def gauss(name, shape, std, dt):
+        t = torch.randn(*shape, generator=gen(name), device=device, dtype=torch.float32)
+        if std != 1.0:
+            t.mul_(std)
+        return t.to(tdt[dt])
+
+    def perm(name, d):
+        return torch.randperm(d, generator=gen(name), device=device).to(torch.int32)
+
+    return {
+        "x": gauss(f"x{N}", (N, m), 1.0, wl.act),
+        "dy": gauss(f"dy{N}", (N, n), 1.0, wl.act),
+        "W0": gauss("W0", (n, m), 1.0 / float(np.sqrt(m)), wstore),
+        "q_R": gauss("qR", (-(-m // b), tri), wl.q_std, "f32"),
+        "q_P": gauss("qP", (-(-n // b), tri), wl.q_std, "f32"),
+        "perm_m": perm("pm", m),
+        "perm_n": perm("pn", n),
+    }

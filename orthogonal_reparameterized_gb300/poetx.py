@@ -85,6 +85,16 @@ _SIGS = {
     "poetx_layer_bwd_adam": (_i, [ctypes.POINTER(LayerDesc), _vp, _vp, _i, _vp, _vp, _vp, _vp,
                                   _i, ctypes.POINTER(AdamDesc), _vp, _vp, _vp, _vp, _vp, _sz,
                                   _vp]),
+    "poetx_group_saved_bytes": (_sz, [ctypes.POINTER(LayerDesc), _i, _i]),
+    "poetx_group_workspace_bytes": (_sz, [ctypes.POINTER(LayerDesc), _i, _i]),
+    "poetx_group_cnp_fwd": (_i, [ctypes.POINTER(LayerDesc), _i, _i, _vp, _vp]),
+    "poetx_group_layer_fwd": (_i, [ctypes.POINTER(LayerDesc), _i, _i, _vp, _i, _vp, _vp, _vp, _sz,
+                                   _vp]),
+    "poetx_group_layer_bwd": (_i, [ctypes.POINTER(LayerDesc), _i, _i, _vp, _vp, _i, _vp, _vp, _vp,
+                                   _sz, _vp]),
+    "poetx_group_cnp_bwd": (_i, [ctypes.POINTER(LayerDesc), _i, _i, _vp,
+                                 ctypes.POINTER(ctypes.c_void_p), ctypes.POINTER(ctypes.c_void_p),
+                                 _i, _vp, _sz, _vp]),
 }
 
 _lib: Optional[ctypes.CDLL] = None
@@ -141,8 +151,12 @@ def poetx_set_gemm_engine(engine: int):
     _check("poetx_set_gemm_engine", lib().poetx_set_gemm_engine(engine))
 
 
-def poetx_set_fusion(on: bool):
-    _check("poetx_set_fusion", lib().poetx_set_fusion(1 if on else 0))
+def poetx_set_fusion(on):
+    """True / False: every fused kernel on / off; an int: the library's bit mask (bit 0 the
+    W' contraction with the block product after it, bit 1 the backward block product with
+    its weight gradient)."""
+    mask = (3 if on else 0) if isinstance(on, bool) else int(on)
+    _check("poetx_set_fusion", lib().poetx_set_fusion(mask))
 
 
 def poetx_set_overlap(on: bool):
@@ -372,3 +386,53 @@ def poetx_layer_bwd_adam(L: LayerDesc, x, dy, saved, dx, dq_R, dq_P, ws, m_R, v_
         ctypes.byref(L), _p(x), _p(dy), N, _p(saved), _p(dx), _p(dq_R), _p(dq_P),
         int(bool(accumulate)), ctypes.byref(hp), _p(m_R), _p(v_R), _p(m_P), _p(v_P), _p(ws),
         ws.numel(), _stream(stream)))
+
+
+# ---------------------------------------------------------------- layer groups
+GROUP_MAX_LAYERS = 16
+
+
+def make_group(layers):
+    """A ctypes array of ``poetx_layer`` descriptors (the group); the tensors the descriptors
+    point to must outlive its use."""
+    arr = (LayerDesc * len(layers))(*layers)
+    return arr
+
+
+def poetx_group_saved_bytes(G, N: int) -> int:
+    return lib().poetx_group_saved_bytes(G, len(G), N)
+
+
+def poetx_group_workspace_bytes(G, N: int) -> int:
+    return lib().poetx_group_workspace_bytes(G, len(G), N)
+
+
+def poetx_group_cnp_fwd(G, N: int, saved, stream=None):
+    _check("poetx_group_cnp_fwd", lib().poetx_group_cnp_fwd(G, len(G), N, _p(saved),
+                                                            _stream(stream)))
+
+
+def poetx_group_layer_fwd(G, i: int, x, y, saved, ws, stream=None):
+    N = x.shape[0]
+    _check("poetx_group_layer_fwd", lib().poetx_group_layer_fwd(
+        G, len(G), i, _p(x), N, _p(y), _p(saved), _p(ws), ws.numel(), _stream(stream)))
+
+
+def poetx_group_layer_bwd(G, i: int, x, dy, saved, dx, ws, stream=None):
+    N = x.shape[0]
+    _check("poetx_group_layer_bwd", lib().poetx_group_layer_bwd(
+        G, len(G), i, _p(x), _p(dy), N, _p(saved), _p(dx), _p(ws), ws.numel(),
+        _stream(stream)))
+
+
+def poetx_group_cnp_bwd(G, N: int, saved, dq_R, dq_P, ws, accumulate=False, stream=None):
+    """dq_R, dq_P: one fp32 tensor per layer of the group."""
+    if len(dq_R) != len(G) or len(dq_P) != len(G):
+        raise ValueError("poetx_group_cnp_bwd: one dq_R and one dq_P per layer")
+    pr = (ctypes.c_void_p * len(G))(*[t.data_ptr() for t in dq_R])
+    pp = (ctypes.c_void_p * len(G))(*[t.data_ptr() for t in dq_P])
+    for t in list(dq_R) + list(dq_P):
+        _p(t)
+    _check("poetx_group_cnp_bwd", lib().poetx_group_cnp_bwd(
+        G, len(G), N, _p(saved), pr, pp, int(bool(accumulate)), _p(ws), ws.numel(),
+        _stream(stream)))

@@ -16,7 +16,8 @@ TDT = {"f32": torch.float32, "bf16": torch.bfloat16}
 
 def run_layer(P, inp, b, act, wdt, variant, dy=None, q_zero=False, accumulate_init=None):
     """Runs fwd + bwd through the C ABI; returns host arrays and the effective W0 that the
-    oracle must use (the GPU quantiser's own output for int8 weights)."""
+    oracle must use (for int8 weights, the oracle's own quantisation of W0 dequantised: the
+    library's quantiser is checked bit for bit against it on its own)."""
     m, n = inp["W0"].shape[1], inp["W0"].shape[0]
     m_pad, n_pad = -(-m // b) * b, -(-n // b) * b
     ragged = (m_pad, n_pad) != (m, n)
@@ -41,7 +42,7 @@ def run_layer(P, inp, b, act, wdt, variant, dy=None, q_zero=False, accumulate_in
             Wp = torch.empty_like(Wq)
             w_scale = torch.empty_like(s)
             P.poetx_merge_perm(Wq, pn, pm, Wp, s, w_scale)
-        W_eff = O.dequantize_rows(host(Wq), host(s))
+        W_eff = O.dequantize_rows(*O.quantize_rows_int8(inp["W0"]))
         wcode = P.I8
     else:
         W0 = dev(inp["W0"], TDT[wdt])

@@ -31,13 +31,13 @@ def _layer_on_gpu(P, inp, b, act, wdt, variant="fast"):
         Wp = torch.empty(n_pad, m_pad, dtype=torch.int8, device=DEV)
         w_scale = torch.empty(n_pad, device=DEV)
         P.poetx_merge_perm_padded(Wq, pn, pm, Wp, s, w_scale)
-        W_eff = O.dequantize_rows(host(Wq), host(s))
+        W_eff = O.dequantize_rows(*O.quantize_rows_int8(inp["W0"]))
         wcode = P.I8
     else:
         W0 = dev(inp["W0"], TDT[wdt])
         Wp = torch.empty(n_pad, m_pad, dtype=W0.dtype, device=DEV)
         P.poetx_merge_perm_padded(W0, pn, pm, Wp)
-        W_eff = host(W0)
+        W_eff = inp["W0"]
         wcode = P.F32 if wdt == "f32" else P.BF16
     acode = P.F32 if act == "f32" else P.BF16
     L = P.make_layer(m, n, b, acode, wcode, P.FAST if variant == "fast" else P.MEM, pm, pn, Wp,
