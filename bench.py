@@ -55,6 +55,9 @@ def parse():
                          "gradient only)")
     ap.add_argument("--overlap", default="on", choices=["on", "off"],
                     help="dx scatter on a side stream beside the CNP backward (library switch)")
+    ap.add_argument("--group", default="on", choices=["on", "off"],
+                    help="run the workload's layers as one layer group (one batched CNP "
+                         "forward and backward per step; default) or layer by layer")
     ap.add_argument("--tokens", type=int, default=None,
                     help="override the workload's token count (profiling cases)")
     ap.add_argument("--launches-only", action="store_true",
@@ -263,14 +266,17 @@ def hbm_sides(direction, variant, stage):
 
 class Rig:
     """Every tensor of one workload on the device: per layer the inputs (drawn on the device),
-    the merged weight, the descriptor, the saved state and the outputs; one forward and one
-    backward workspace shared by the layers (they run one after the other on one stream);
-    the parameters q, their gradients dq and the Adam state of all layers in flat buffers."""
+    the merged weight, the descriptor and the outputs; the parameters q, their gradients dq
+    and the Adam state of all layers in flat buffers.  With group=True (the default) the
+    layers form one layer group: one saved buffer and one workspace for the group, one CNP
+    forward and one CNP backward over every block of every layer per step.  Otherwise each
+    layer runs poetx_layer_fwd / poetx_layer_bwd with its own saved buffer and a shared
+    forward and backward workspace."""
 
-    def __init__(self, P, wl, variant, dev, N=None):
+    def __init__(self, P, wl, variant, dev, N=None, group=True):
         import torch
         from orthogonal_reparameterized_gb300 import dp, inputs
-        self.P, self.wl, self.variant, self.dev = P, wl, variant, dev
+        self.P, self.wl, self.variant, self.dev, self.group = P, wl, variant, dev, group
         self.N = N = wl.N if N is None else N
         self.bf = torch.bfloat16 if wl.act == "bf16" else torch.float32
         self.esz = 2 if wl.act == "bf16" else 4
@@ -307,32 +313,57 @@ class Rig:
                              Wp, self.q.view(f"{i}R"), self.q.view(f"{i}P"), w_scale)
             d = dict(shape=ly, L=L, x=inp["x"], dy=inp["dy"], pm=inp["perm_m"],
                      pn=inp["perm_n"], Wp=Wp, w_scale=w_scale,
-                     saved=P.workspace(P.poetx_layer_saved_bytes(L, N), dev),
                      y=torch.empty(N, ly.n, dtype=self.bf, device=dev),
                      dx=torch.empty(N, ly.m, dtype=self.bf, device=dev),
                      dqR=self.dq.view(f"{i}R"), dqP=self.dq.view(f"{i}P"))
-            wsf = max(wsf, P.poetx_layer_workspace_bytes(L, N, 0))
-            wsb = max(wsb, P.poetx_layer_workspace_bytes(L, N, 1))
+            if not group:
+                d["saved"] = P.workspace(P.poetx_layer_saved_bytes(L, N), dev)
+                wsf = max(wsf, P.poetx_layer_workspace_bytes(L, N, 0))
+                wsb = max(wsb, P.poetx_layer_workspace_bytes(L, N, 1))
             self.layers.append(d)
-        self.wsf = P.workspace(wsf, dev)
-        self.wsb = P.workspace(wsb, dev)
+        if group:
+            self.G = P.make_group([d["L"] for d in self.layers])
+            self.gsaved = P.workspace(P.poetx_group_saved_bytes(self.G, N), dev)
+            self.gws = P.workspace(P.poetx_group_workspace_bytes(self.G, N), dev)
+            self.dqR_list = [d["dqR"] for d in self.layers]
+            self.dqP_list = [d["dqP"] for d in self.layers]
+        else:
+            self.wsf = P.workspace(wsf, dev)
+            self.wsb = P.workspace(wsb, dev)
         self.adam_step = 1
 
-    def fwd(self, i):
-        d = self.layers[i]
-        self.P.poetx_layer_fwd(d["L"], d["x"], d["y"], d["saved"], self.wsf)
+    def calls(self):
+        """The step's library calls in order: (kind, layer index)."""
+        n = len(self.layers)
+        c = [("fwd", i) for i in range(n)] + [("bwd", i) for i in reversed(range(n))]
+        return ([("cnp_fwd", -1)] + c + [("cnp_bwd", -1)]) if self.group else c
 
-    def bwd(self, i):
-        d = self.layers[i]
-        self.P.poetx_layer_bwd(d["L"], d["x"], d["dy"], d["saved"], d["dx"], d["dqR"], d["dqP"],
-                               self.wsb)
+    def run(self, kind, i):
+        P = self.P
+        if kind == "cnp_fwd":
+            P.poetx_group_cnp_fwd(self.G, self.N, self.gsaved)
+        elif kind == "cnp_bwd":
+            P.poetx_group_cnp_bwd(self.G, self.N, self.gsaved, self.dqR_list, self.dqP_list,
+                                  self.gws)
+        elif kind == "fwd":
+            d = self.layers[i]
+            if self.group:
+                P.poetx_group_layer_fwd(self.G, i, d["x"], d["y"], self.gsaved, self.gws)
+            else:
+                P.poetx_layer_fwd(d["L"], d["x"], d["y"], d["saved"], self.wsf)
+        else:
+            d = self.layers[i]
+            if self.group:
+                P.poetx_group_layer_bwd(self.G, i, d["x"], d["dy"], self.gsaved, d["dx"], self.gws)
+            else:
+                P.poetx_layer_bwd(d["L"], d["x"], d["dy"], d["saved"], d["dx"], d["dqR"],
+                                  d["dqP"], self.wsb)
 
     def compute(self):
-        """Forward of every layer in order, backward in reverse order."""
-        for i in range(len(self.layers)):
-            self.fwd(i)
-        for i in reversed(range(len(self.layers))):
-            self.bwd(i)
+        """Forward of every layer in order, backward in reverse order (with the group: the
+        CNP forward of every block first, the CNP backward of every block last)."""
+        for kind, i in self.calls():
+            self.run(kind, i)
 
     def update(self):
         """Adam on every layer's packed triangles (one launch over the flat buffers)."""
@@ -436,7 +467,7 @@ def main():
     wl = inputs.WORKLOADS[args.workload]
     variant = args.variant or ("mem" if wl.wdt == "i8" else wl.variants[0])
     c_setup = P.poetx_launch_count()
-    rig = Rig(P, wl, variant, dev, N=args.tokens)
+    rig = Rig(P, wl, variant, dev, N=args.tokens, group=args.group == "on")
     N = rig.N
     if args.launches_only:
         c0 = P.poetx_launch_count()
@@ -498,11 +529,14 @@ def main():
         flush.zero_()
         torch.cuda.synchronize()
         P.poetx_profile_collect()
-        calls = [("fwd", i) for i in range(len(rig.layers))] + \
-                [("bwd", i) for i in reversed(range(len(rig.layers)))]
-        for direction, i in calls:
-            (rig.fwd if direction == "fwd" else rig.bwd)(i)
+        for direction, i in rig.calls():
+            rig.run(direction, i)
             recs = P.poetx_profile_collect()
+            if i < 0:  # the group's CNP calls
+                for name, t_ms in recs:
+                    stage_ms.setdefault(name, []).append(t_ms)
+                    cnp_layer_ms += t_ms
+                continue
             ly = rig.layers[i]["shape"]
             width = {"m": padded(ly.m, wl.b), "n": padded(ly.n, wl.b)}
             seen = {}
@@ -630,6 +664,7 @@ def main():
                        "layers": [{"name": ly.name, "m": ly.m, "n": ly.n} for ly in wl.layers],
                        "b": wl.b, "tokens_per_gpu": N, "variant": variant, "wdt": wl.wdt,
                        "fusion": args.fusion, "overlap": args.overlap == "on",
+                       "layer_group": args.group == "on",
                        "parallelism": (f"data parallel x{world}: token-sharded, one sum "
                                        f"all-reduce of dq per step") if world > 1 else
                                       "one GPU",

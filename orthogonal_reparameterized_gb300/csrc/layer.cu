@@ -170,6 +170,7 @@ struct Plan {
   // backward workspace: the chain's activations [0, bwd_chain), then the weight-gradient
   // partials and the CNP backward's scratch
   size_t b_xt, b_dzt, b_A, b_B, b_dB, b_dA, b_dxt, bwd_chain, b_dGP, b_dGR, b_cnp, bwd_total;
+  size_t dGR_bytes, dGP_bytes;  // partial buffers, sized for either weight-gradient kernel
   int splitsR, splitsP;
 };
 
@@ -238,8 +239,10 @@ static Plan make_plan(const poetx_layer* L, long long N) {
   p.b_dA = take((size_t)N * m * as);
   p.b_dxt = take((size_t)N * m * as);
   p.bwd_chain = o;
-  p.b_dGP = take(maxP * n * b * 4);
-  p.b_dGR = take(maxR * m * b * 4);
+  p.dGP_bytes = maxP * n * b * 4;
+  p.dGR_bytes = maxR * m * b * 4;
+  p.b_dGP = take(p.dGP_bytes);
+  p.b_dGR = take(p.dGR_bytes);
   p.b_cnp = take(cnp_bwd_scratch_bytes((int)((m + n) / b), (int)b));
   p.bwd_total = o;
   return p;
@@ -735,8 +738,8 @@ static GroupPlan group_plan(const poetx_layer* Ls, int count, long long N) {
   g.chain = take(g.chain_bytes);
   for (int i = 0; i < count; ++i) {
     const size_t m = padded(Ls[i].m, Ls[i].b), n = padded(Ls[i].n, Ls[i].b);
-    g.dGR[i] = take((size_t)g.lp[i].splitsR * m * b * 4);
-    g.dGP[i] = take((size_t)g.lp[i].splitsP * n * b * 4);
+    g.dGR[i] = take(g.lp[i].dGR_bytes);
+    g.dGP[i] = take(g.lp[i].dGP_bytes);
   }
   g.cnp = take(cnp_bwd_scratch_bytes((int)nb, (int)b));
   g.ws_total = o;
