@@ -295,6 +295,14 @@ typedef struct poetx_layer {
  * 0 if the descriptor is invalid. */
 size_t poetx_layer_workspace_bytes(const poetx_layer* L, int N, int phase);
 
+/* Which of the layer's products run on the CUDA cores instead of the tcgen05 tensor cores,
+ * as a bit mask: bit 0 the CNP products, bit 1 the block-diagonal products and their weight
+ * gradients, bit 2 the W' contraction; 0 when everything runs on the tensor cores.  bf16 and
+ * int8 layers take the tensor cores for every shape the descriptor accepts (on sm_103 with
+ * the default engine); fp32 layers run their layer products on the CUDA cores (1e-5
+ * accuracy), their CNP on the tensor cores.  -1 for an invalid descriptor.  Host-only. */
+int poetx_layer_cuda_core_steps(const poetx_layer* L, int N);
+
 /* Bytes the caller keeps from poetx_layer_fwd to poetx_layer_bwd ("saved"): the bf16 (or
  * fp32) blocks G_R, G_P and the fp32 Q_R, Q_P, Q_R^2, Q_P^2 (O((m+n) b), independent of N),
  * plus, for POETX_FAST only, what default autograd keeps: B = A W'^T ([N, n]) and the

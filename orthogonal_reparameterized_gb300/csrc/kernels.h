@@ -170,7 +170,7 @@ bool umma_wprime_fusable(long long N, int m, int n, int trans, int b);
 poetx_status umma_wprime_fused(const void* A, long long N, int m, int n, const void* W, int trans,
                                const void* G, int b, void* C1, void* C2, cudaStream_t s);
 // The same contraction with an int8 W, run transposed so that the widened weight is the
-// tensor-memory A operand (K and the output features must be multiples of 64 and 128); the
+// tensor-memory A operand (K and the output features must be multiples of 64); the
 // forward multiplies output column r by w_scale[r], the backward expects A to carry the
 // scale already.
 poetx_status umma_wprime_i8(const void* A, long long N, int m, int n, const void* Wq,

@@ -21,6 +21,7 @@
 #include <atomic>
 #include <mutex>
 
+#include "cnp_umma.h"
 #include "common.cuh"
 #include "kernels.h"
 
@@ -98,9 +99,10 @@ poetx_status wprime_impl(poetx_dtype act, poetx_dtype wdt, const void* A, long l
                          int n, const void* W, const float* w_scale, int trans, void* C,
                          cudaStream_t s) {
   if (N == 0) return POETX_OK;
-  if (act == POETX_BF16 && wdt == POETX_I8 && use_umma() && m % 256 == 0 && n % 256 == 0)
+  // tensor cores for every bf16 shape the layer has (padded widths are multiples of b >= 64)
+  if (act == POETX_BF16 && wdt == POETX_I8 && use_umma() && m % 64 == 0 && n % 64 == 0)
     return umma_wprime_i8(A, N, m, n, W, w_scale, trans, C, s);
-  if (act == POETX_BF16 && wdt == POETX_BF16 && use_umma() && m % 256 == 0 && n % 256 == 0)
+  if (act == POETX_BF16 && wdt == POETX_BF16 && use_umma() && m % 64 == 0 && n % 64 == 0)
     return umma_wprime(A, N, m, n, W, trans, C, s);
   SimtGemm g{};
   g.M = (int)N; g.batch = 1; g.A = A; g.B = W; g.C = C;
@@ -359,6 +361,16 @@ extern "C" poetx_status poetx_merge_reinit(const poetx_layer* L, float* W0_new, 
   // the first L->n rows and L->m columns of the padded M hold the map
   return launch_perm_rows(4, false, M, L->n, L->m, inv_m, W0_new, inv_n, nullptr, nullptr,
                           stream, m, L->m);
+}
+
+extern "C" int poetx_layer_cuda_core_steps(const poetx_layer* L, int N) {
+  if (validate(L) != POETX_OK || N < 0) return -1;
+  const int b = L->b, mP = padded(L->m, b), nP = padded(L->n, b);
+  int mask = 0;
+  if (!(use_tensor_cores() && cnp_umma_ok(b))) mask |= 1;
+  if (!(L->act == POETX_BF16 && use_umma() && b % 64 == 0 && b <= 512)) mask |= 2;
+  if (!(L->act == POETX_BF16 && use_umma() && mP % 64 == 0 && nP % 64 == 0)) mask |= 4;
+  return mask;
 }
 
 extern "C" size_t poetx_layer_saved_bytes(const poetx_layer* L, int N) {

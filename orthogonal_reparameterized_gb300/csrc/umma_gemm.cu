@@ -426,6 +426,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const long long row0 = c.out_row0 + q * 32;  // first output row of this warp
 #pragma unroll 1
       for (int c0 = cbeg; c0 < cbeg + WCOLS; c0 += EPC) {
+        // the contraction's last tile column may reach past the output width (a multiple of
+        // 64, so a pass is wholly inside or outside): nothing to store there
+        if (p.mode == MODE_PLAIN && c.out_col0 + c0 >= p.ldc) continue;
         // one or two 32-column TMEM loads, one wait
         uint32_t r[64];
         if (c.num_kb > 0) {
@@ -1121,7 +1124,7 @@ __global__ void __launch_bounds__(I8_THREADS, 1)
               __float2bfloat16_rn(__uint_as_float(r[j]) * sc);
         __syncwarp();
         const long long tok = t0 + c0 + lane;
-        if (tok < p.ntok) {
+        if (tok < p.ntok && f0 < p.nfeat) {  // (the last feature tile may be half full)
           const uint4* src = reinterpret_cast<const uint4*>(stg + lane * I8_STG_PITCH);
           uint4* dst = reinterpret_cast<uint4*>(p.C + tok * p.nfeat + f0);
 #pragma unroll
@@ -1372,21 +1375,21 @@ poetx_status umma_wprime(const void* A, long long N, int m, int n, const void* W
     if (!make_map(&tb, W, m, n, m, 64, pairs ? 128 : 256)) return POETX_ERR_CUDA;
     p.num_kb = m / 64;
     p.ldc = n;
-    if (pairs) return launch<256, 6, false, false, false, 0, 2>(ta, tb, p, tm2, n / 256, 1, s);
-    return launch<256, 4, false, false, false>(ta, tb, p, tm, n / 256, 1, s);
+    if (pairs) return launch<256, 6, false, false, false, 0, 2>(ta, tb, p, tm2, (n + 255) / 256, 1, s);
+    return launch<256, 4, false, false, false>(ta, tb, p, tm, (n + 255) / 256, 1, s);
   }
   // C[N,m] = A[N,n] W: B operand (output col c, K index r) = W[r][c], MN-major
   if (!make_map(&ta, A, n, N, n, 64, 128)) return POETX_ERR_CUDA;
   if (!make_map(&tb, W, m, n, m, 64, 64)) return POETX_ERR_CUDA;
   p.num_kb = n / 64;
   p.ldc = m;
-  if (pairs) return launch<256, 6, false, true, false, 0, 2>(ta, tb, p, tm2, m / 256, 1, s);
-  return launch<256, 4, false, true, false>(ta, tb, p, tm, m / 256, 1, s);
+  if (pairs) return launch<256, 6, false, true, false, 0, 2>(ta, tb, p, tm2, (m + 255) / 256, 1, s);
+  return launch<256, 4, false, true, false>(ta, tb, p, tm, (m + 255) / 256, 1, s);
 }
 
 bool umma_wprime_pairs(long long N, int m, int n, int trans) {
   const long long tm2 = ((N + BM - 1) / BM + 1) / 2;
-  return tm2 * ((trans ? m : n) / 256) >= sm_count();
+  return tm2 * (((trans ? m : n) + 255) / 256) >= sm_count();
 }
 
 bool umma_wprime_fusable(long long N, int m, int n, int trans, int b) {
@@ -1449,7 +1452,7 @@ poetx_status umma_wprime_i8(const void* A, long long N, int m, int n, const void
                             const float* w_scale, int trans, void* C, cudaStream_t s) {
   if (N == 0) return POETX_OK;
   const int K = trans ? n : m, F = trans ? m : n;  // contraction length, output features
-  if (K % 64 || F % 128) return POETX_ERR_SHAPE;
+  if (K % 64 || F % 64) return POETX_ERR_SHAPE;
   CUtensorMap tw, tx;
   if (!make_map(&tx, A, K, N, K, 64, I8N)) return POETX_ERR_CUDA;
   if (!trans) {
@@ -1458,7 +1461,7 @@ poetx_status umma_wprime_i8(const void* A, long long N, int m, int n, const void
     if (!make_map_t(&tw, Wq, m, n, m, 128, 64, true)) return POETX_ERR_CUDA;
   }
   I8Params p{};
-  p.tiles_f = F / BM;
+  p.tiles_f = (F + BM - 1) / BM;
   p.tiles_t = (int)((N + I8T - 1) / I8T);
   const long long tiles = (long long)p.tiles_f * p.tiles_t;
   if (tiles > 0x7fffffffLL) return POETX_ERR_SHAPE;

@@ -72,6 +72,7 @@ _SIGS = {
     "poetx_wprime_gemm": (_i, [_i, _i, _vp, _i, _i, _i, _vp, _vp, _i, _vp, _vp]),
     "poetx_layer_workspace_bytes": (_sz, [ctypes.POINTER(LayerDesc), _i, _i]),
     "poetx_layer_saved_bytes": (_sz, [ctypes.POINTER(LayerDesc), _i]),
+    "poetx_layer_cuda_core_steps": (_i, [ctypes.POINTER(LayerDesc), _i]),
     "poetx_layer_fwd": (_i, [ctypes.POINTER(LayerDesc), _vp, _i, _vp, _vp, _vp, _sz, _vp]),
     "poetx_layer_bwd": (_i, [ctypes.POINTER(LayerDesc), _vp, _vp, _i, _vp, _vp, _vp, _vp, _i,
                              _vp, _sz, _vp]),
@@ -310,6 +311,12 @@ def make_layer(m, n, b, act, wdt, variant, perm_m, perm_n, Wp, q_R, q_P, w_scale
 
 def poetx_layer_workspace_bytes(L: LayerDesc, N: int, phase: int) -> int:
     return lib().poetx_layer_workspace_bytes(ctypes.byref(L), N, phase)
+
+
+def poetx_layer_cuda_core_steps(L: LayerDesc, N: int) -> int:
+    """Bit mask of the layer's products on the CUDA cores (bit 0 CNP, bit 1 block-diagonal
+    products, bit 2 W' contraction); 0: all on the tensor cores; -1: invalid descriptor."""
+    return lib().poetx_layer_cuda_core_steps(ctypes.byref(L), N)
 
 
 def poetx_layer_saved_bytes(L: LayerDesc, N: int) -> int:

@@ -204,3 +204,28 @@ def test_layer_bwd_adam_argument_errors(P):
                                     fake, fake, fake, fake, fake, 1 << 30, None) == 6
     assert lib.poetx_layer_bwd_adam(ctypes.byref(L), *args, ctypes.byref(hp), fake, fake, fake,
                                     fake, fake, 16, None) == 5                 # workspace
+
+
+def test_engine_query_host_logic(P):
+    assert P.poetx_layer_cuda_core_steps(_desc(P, b=100), 64) == -1      # invalid descriptor
+    assert P.poetx_layer_cuda_core_steps(_desc(P), -1) == -1
+    # an fp32 layer runs its layer products on the CUDA cores by design
+    f32 = P.poetx_layer_cuda_core_steps(_desc(P, act=P.F32, wdt=P.F32, b=32), 64)
+    assert f32 >= 0 and f32 & 6 == 6
+    assert P.poetx_layer_cuda_core_steps(_desc(P), 64) >= 0
+
+
+def test_group_sizes_host_logic(P):
+    a, b = _desc(P), _desc(P, m=512, n=256)
+    G = P.make_group([a, b])
+    N = 100
+    sv = P.poetx_group_saved_bytes(G, N)
+    ws = P.poetx_group_workspace_bytes(G, N)
+    # the group keeps at least what the two layers keep, less N-independent duplication
+    assert sv >= P.poetx_layer_saved_bytes(a, N) + P.poetx_layer_saved_bytes(b, N) - 16 * 4096
+    assert ws > 0
+    assert P.poetx_group_saved_bytes(P.make_group([a, _desc(P, b=128)]), N) == 0  # mixed b
+    assert P.poetx_group_saved_bytes(P.make_group([a, _desc(P, act=P.F32, wdt=P.F32)]),
+                                     N) == 0                                 # mixed act
+    assert P.poetx_group_saved_bytes(P.make_group([a] * 17), N) == 0         # > 16 layers
+    assert P.poetx_group_saved_bytes(P.make_group([a] * 16), N) > 0

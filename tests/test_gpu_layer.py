@@ -440,3 +440,38 @@ def test_layer_ragged_fast_mem_equal_and_step_host(P):
     for k in ("y", "dx", "dq_R", "dq_P"):
         np.testing.assert_array_equal(a[k], c[k], err_msg=k)
         np.testing.assert_array_equal(a[k], h[k], err_msg=k)
+
+
+@pytest.mark.parametrize("m,n,b,wdt,variant", [(640, 384, 128, "bf16", "fast"),
+                                               (384, 640, 64, "bf16", "mem"),
+                                               (384, 320, 64, "i8", "mem")])
+def test_layer_widths_off_the_256_grid_take_tensor_cores(P, m, n, b, wdt, variant):
+    """Widths that are multiples of 64 but not of 256 (the W' tile): the contraction still
+    runs on the tensor cores (its last tile column is partly outside the output), which the
+    engine query reports, and the layer matches the oracle; with the CUDA-core engine the
+    query reports every product there and the result matches too."""
+    N = 300
+    inp = inputs.small_layer_inputs(880 + m + n, m, n, b, N, act="bf16", wdt=wdt)
+    fake = __import__("ctypes").c_void_p(4096)
+    desc = P.LayerDesc(m, n, b, 3, P.BF16, P.I8 if wdt == "i8" else P.BF16,
+                       P.FAST if variant == "fast" else P.MEM, fake, fake, fake,
+                       fake if wdt == "i8" else None, fake, fake)
+    assert P.poetx_layer_cuda_core_steps(desc, N) == 0
+    got = run_layer(P, inp, b, "bf16", wdt, variant)
+    check(got, oracle_for(inp, got, b), TOL_BF16_LAYER)
+    try:
+        P.poetx_set_gemm_engine(1)
+        assert P.poetx_layer_cuda_core_steps(desc, N) == 7
+        cc = run_layer(P, inp, b, "bf16", wdt, variant)
+    finally:
+        P.poetx_set_gemm_engine(0)
+    check(cc, oracle_for(inp, cc, b), TOL_BF16_LAYER)
+
+
+def test_layer_pair_tiles_with_partial_tile_columns(P):
+    """Enough tokens for the 2-CTA pair contraction, with widths (4160 = 65 x 64, 4224 = 66 x
+    64) whose last 256-wide tile column is partly outside the output, at b = 64; checked on
+    sampled tokens as the full-size cases are."""
+    wl = inputs.Workload("pairs_partial", (inputs.LayerShape("lin", 4160, 4224),), 64, 4096,
+                         "bf16", "bf16", 0.02, ("fast",), 4242)
+    _masked_full_size(P, wl, wl.layers[0], "fast")
