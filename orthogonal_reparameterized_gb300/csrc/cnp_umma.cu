@@ -15,7 +15,7 @@
 //               straight into tensor memory (where the MMA reads it), the B operand in place
 //               in shared memory (same swizzled offsets, so the layout is kept)
 //   warp 1      three tcgen05.mma kind::tf32 per K=8 step into the K block's accumulator
-//   warps 10..  promotion: add each K block's accumulator into the running sum (in TMEM)
+//   warps 10..  promotion: add each K block's accumulator into the running sum
 //   all warps   epilogue: out = sum + e1 E1 + e2 E2 + eI I through a shared-memory tile,
 //               stored as fp32 / fp32^T / bf16 / bf16^T with coalesced 16-byte accesses
 // Both operand tiles are K-major (kind::tf32 takes no MN-major operand): A tiles are rows of
@@ -141,17 +141,20 @@ __device__ __forceinline__ void combine_split(float4* x, float4* y, float c0, fl
 // (rows 32 (w % 4) .. +31, K columns 16 ((w - 2) / 4) .. +15) and writes hi and lo into
 // tensor memory; the B operand is formed and split in shared memory by all converters.
 // Promotion warp w adds each K block's accumulator of its lane quarter w % 4 (and column
-// slice) into the running sum, kept in TMEM as well so that it holds no accumulator registers.  TMEM columns: NACC
-// accumulators of BN, the running sum (BN), then STAGES A slots of 64 (hi 32 + lo 32).
+// slice) into the running sum, so that with two or more accumulators the MMAs of a K block
+// never wait for the promotion of the one before.  Tiles of 32 or 64 columns keep the sum in
+// registers (64 columns per thread); TMEM columns: NACC accumulators of BN, then STAGES A
+// slots of 64 (hi 32 + lo 32).  Tiles of 128 columns run 18 warps, which the SM's four
+// register partitions allow only 96 registers each, so they keep it in TMEM: 2 accumulators,
+// the sum, 2 A slots (released by the MMAs for the converters).
 constexpr int kConvWarps = 8;  // two per TMEM lane quarter
 // Tiles of 32 or 64 columns: 4 promotion warps, 4 TMEM accumulators, the epilogue-term tiles
 // prefetched into their own shared memory during the K loop.  Tiles of 128 columns (blocks of
 // 256 and up when 64-wide tiles would need more than one wave of CTAs): 8 promotion warps
-// (two per lane quarter, 64 columns each), one accumulator (the accumulators, the running sum
-// and the A slots must fit the 512 TMEM columns), epilogue-term tiles fetched into the idle
-// ring after the K loop.
+// (two per lane quarter, 64 columns each), two accumulators, epilogue-term tiles fetched into
+// the idle ring after the K loop.
 __host__ __device__ constexpr int prom_warps(int bn) { return bn >= 128 ? 8 : 4; }
-__host__ __device__ constexpr int cnp_nacc(int bn) { return bn >= 128 ? 1 : 4; }
+__host__ __device__ constexpr int cnp_nacc(int bn) { return bn >= 128 ? 2 : 4; }
 __host__ __device__ constexpr bool e_in_ring(int bn) { return bn >= 128; }
 __host__ __device__ constexpr int cnp_threads(int bn) {
   return 32 * (2 + kConvWarps + prom_warps(bn));
@@ -197,13 +200,15 @@ __global__ void __launch_bounds__(cnp_threads(BN), 1)
   constexpr uint32_t B_BYTES = BN * BK * 4;   // BN * 128 bytes per buffer
   constexpr uint32_t STAGE_BYTES = 2 * A_BYTES + 2 * B_BYTES;
   constexpr uint32_t RING_BYTES = cnp_ring_bytes<BN>();  // >= STAGES * STAGE_BYTES
-  constexpr uint32_t SUM_COL = NACC * BN;     // running sum
-  constexpr uint32_t A_COL = NACC * BN + BN;  // A slots: A_COL + 64 s (+32 for lo)
-  constexpr uint32_t TMEM_COLS = A_COL + 64 * STAGES <= 256 ? 256 : 512;
+  constexpr bool SUM_TMEM = BN >= 128;
+  constexpr int ASLOTS = SUM_TMEM ? 2 : STAGES;          // TMEM slots of the A operand
+  constexpr uint32_t SUM_COL = NACC * BN;                // running sum (SUM_TMEM)
+  constexpr uint32_t A_COL = NACC * BN + (SUM_TMEM ? BN : 0);  // A slots: + 64 j (+32: lo)
+  constexpr uint32_t TMEM_COLS = A_COL + 64 * ASLOTS <= 256 ? 256 : 512;
   constexpr int G4 = BN / 4;                  // float4 groups per tile row
   constexpr int LD = BN + 4;                  // staged tile pitch (16-byte rows)
   constexpr int TILE = BM * BN;               // floats of one epilogue-term tile
-  static_assert(A_COL + 64 * STAGES <= TMEM_COLS, "accumulators, sum and A slots fit TMEM");
+  static_assert(A_COL + 64 * ASLOTS <= TMEM_COLS, "accumulators, sum and A slots fit TMEM");
   static_assert(RING_BYTES >= (uint32_t)(BM * LD + (E_RING ? 2 * TILE : 0)) * 4,
                 "the staged tile (and the epilogue-term tiles) fit the ring");
   constexpr uint32_t IDESC = tf32_idesc(BM, BN);
@@ -219,7 +224,8 @@ __global__ void __launch_bounds__(cnp_threads(BN), 1)
   uint64_t* empty = conv + STAGES;
   uint64_t* tfull = empty + STAGES;   // [NACC] accumulator holds a finished K block
   uint64_t* tempty = tfull + NACC;    // [NACC] accumulator has been read back
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + NACC);
+  uint64_t* afree = tempty + NACC;    // [ASLOTS] A slot no longer read by MMAs (ASLOTS < STAGES)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(afree + ASLOTS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -250,6 +256,7 @@ __global__ void __launch_bounds__(cnp_threads(BN), 1)
       mbar_init(&tfull[a], 1);
       mbar_init(&tempty[a], kPromWarps);
     }
+    for (int j = 0; j < ASLOTS; ++j) mbar_init(&afree[j], 1);
     *abort_flag = 0;
     fence_mbar_init();
     for (int i = 0; i < p.nmaps; ++i) tma_prefetch_desc(&maps.m[i]);
@@ -312,7 +319,7 @@ __global__ void __launch_bounds__(cnp_threads(BN), 1)
       }
       tc_fence_after();
       const uint32_t d = tmem_base + (uint32_t)(a * BN);
-      const uint32_t a_hi = tmem_base + A_COL + 64u * (uint32_t)s;
+      const uint32_t a_hi = tmem_base + A_COL + 64u * (uint32_t)(kb % ASLOTS);
       const uint32_t a_lo = a_hi + 32;
       const uint32_t b_hi = smem_base + s * STAGE_BYTES + 2 * A_BYTES;
       const uint32_t b_lo = b_hi + B_BYTES;
@@ -325,6 +332,7 @@ __global__ void __launch_bounds__(cnp_threads(BN), 1)
       }
       umma_commit(&empty[s]);
       umma_commit(&tfull[a]);
+      if (ASLOTS < STAGES) umma_commit(&afree[kb % ASLOTS]);
       mma_last = kb;
     }
   } else if (warp >= 2 && warp < 2 + kConvWarps) {
@@ -336,7 +344,11 @@ __global__ void __launch_bounds__(cnp_threads(BN), 1)
     for (int kb = 0; kb < num_kb; ++kb) {
       const int s = kb % STAGES;
       const uint32_t ph = (kb / STAGES) & 1;
-      const bool ok = !*abort_flag && mbar_wait_bounded(&full[s], ph, p.err, p.limit_ns, kSite + __LINE__);
+      bool ok = !*abort_flag && mbar_wait_bounded(&full[s], ph, p.err, p.limit_ns, kSite + __LINE__);
+      // with fewer A slots than ring stages, the slot's previous K block must have been read
+      if (ASLOTS < STAGES && ok && kb >= ASLOTS)
+        ok = mbar_wait_bounded(&afree[kb % ASLOTS], (uint32_t)((kb / ASLOTS - 1) & 1), p.err,
+                               p.limit_ns, kSite + __LINE__);
       if (!__all_sync(0xffffffffu, ok)) {
         *abort_flag = 1;
         break;
@@ -368,7 +380,7 @@ __global__ void __launch_bounds__(cnp_threads(BN), 1)
           split_tf32(v.z, hi[4 * t + 2], lo[4 * t + 2]);
           split_tf32(v.w, hi[4 * t + 3], lo[4 * t + 3]);
         }
-        const uint32_t col = A_COL + 64u * (uint32_t)s + 16u * (uint32_t)ha;
+        const uint32_t col = A_COL + 64u * (uint32_t)(kb % ASLOTS) + 16u * (uint32_t)ha;
         tmem_st_32x32b_x16(a_lane + col, hi);
         tmem_st_32x32b_x16(a_lane + col + 32, lo);
       }
@@ -408,6 +420,7 @@ __global__ void __launch_bounds__(cnp_threads(BN), 1)
     };
     if (!E_RING) fetch_e();
     bool ok_all = true;
+    float sum[SUM_TMEM ? 1 : CW];  // (registers) this thread's row: columns h * CW .. + CW - 1
     for (int kb = 0; kb < num_kb; ++kb) {
       const int a = kb % NACC;
       const bool ok = !*abort_flag &&
@@ -418,28 +431,38 @@ __global__ void __launch_bounds__(cnp_threads(BN), 1)
         break;
       }
       tc_fence_after();
+      if constexpr (SUM_TMEM) {
 #pragma unroll
-      for (int c0 = 0; c0 < CW; c0 += 32) {  // two 16-column chunks per load round trip
-        uint32_t v[2][16], w[2][16];
+        for (int c0 = 0; c0 < CW; c0 += 32) {  // two 16-column chunks per load round trip
+          uint32_t v[2][16], w[2][16];
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          if (c0 + 16 * u >= CW) continue;
-          tmem_ld_32x32b_x16(lane_base + (uint32_t)(a * BN + c0 + 16 * u), v[u]);
-          if (kb > 0) tmem_ld_32x32b_x16(lane_base + (uint32_t)(SUM_COL + c0 + 16 * u), w[u]);
-        }
-        tmem_ld_wait();
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          if (c0 + 16 * u >= CW) continue;
-          if (kb > 0) {
-#pragma unroll
-            for (int t = 0; t < 16; ++t)
-              v[u][t] = __float_as_uint(__uint_as_float(w[u][t]) + __uint_as_float(v[u][t]));
+          for (int u = 0; u < 2; ++u) {
+            tmem_ld_32x32b_x16(lane_base + (uint32_t)(a * BN + c0 + 16 * u), v[u]);
+            if (kb > 0) tmem_ld_32x32b_x16(lane_base + (uint32_t)(SUM_COL + c0 + 16 * u), w[u]);
           }
-          tmem_st_32x32b_x16(lane_base + (uint32_t)(SUM_COL + c0 + 16 * u), v[u]);
+          tmem_ld_wait();
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            if (kb > 0) {
+#pragma unroll
+              for (int t = 0; t < 16; ++t)
+                v[u][t] = __float_as_uint(__uint_as_float(w[u][t]) + __uint_as_float(v[u][t]));
+            }
+            tmem_st_32x32b_x16(lane_base + (uint32_t)(SUM_COL + c0 + 16 * u), v[u]);
+          }
+        }
+        tmem_st_wait();
+      } else {
+#pragma unroll
+        for (int c0 = 0; c0 < CW; c0 += 16) {  // 16 columns per load: few live registers
+          uint32_t v[16];
+          tmem_ld_32x32b_x16(lane_base + (uint32_t)(a * BN + c0), v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int t = 0; t < 16; ++t)
+            sum[c0 + t] = kb == 0 ? __uint_as_float(v[t]) : sum[c0 + t] + __uint_as_float(v[t]);
         }
       }
-      tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty[a]);
@@ -448,17 +471,24 @@ __global__ void __launch_bounds__(cnp_threads(BN), 1)
     // every MMA has completed, so the ring is idle: the sum goes to a shared-memory tile
     if (E_RING && ok_all) fetch_e();
     if (ok_all && num_kb > 0) {
-      tc_fence_after();
+      if constexpr (SUM_TMEM) {
+        tc_fence_after();
 #pragma unroll
-      for (int c0 = 0; c0 < CW; c0 += 16) {
-        uint32_t v[16];
-        tmem_ld_32x32b_x16(lane_base + (uint32_t)(SUM_COL + c0), v);
-        tmem_ld_wait();
+        for (int c0 = 0; c0 < CW; c0 += 16) {
+          uint32_t v[16];
+          tmem_ld_32x32b_x16(lane_base + (uint32_t)(SUM_COL + c0), v);
+          tmem_ld_wait();
 #pragma unroll
-        for (int t = 0; t < 16; t += 4)
-          *reinterpret_cast<float4*>(tile + r * LD + h * CW + c0 + t) =
-              make_float4(__uint_as_float(v[t]), __uint_as_float(v[t + 1]),
-                          __uint_as_float(v[t + 2]), __uint_as_float(v[t + 3]));
+          for (int t = 0; t < 16; t += 4)
+            *reinterpret_cast<float4*>(tile + r * LD + h * CW + c0 + t) =
+                make_float4(__uint_as_float(v[t]), __uint_as_float(v[t + 1]),
+                            __uint_as_float(v[t + 2]), __uint_as_float(v[t + 3]));
+        }
+      } else {
+#pragma unroll
+        for (int c0 = 0; c0 < CW; c0 += 4)
+          *reinterpret_cast<float4*>(tile + r * LD + h * CW + c0) =
+              make_float4(sum[c0], sum[c0 + 1], sum[c0 + 2], sum[c0 + 3]);
       }
     }
     cp_async_wait_all();

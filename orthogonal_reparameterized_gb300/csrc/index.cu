@@ -287,9 +287,10 @@ __global__ void __launch_bounds__((kPermWarps + 1) * 32) perm_rows_kernel(
   // fit 32 bits (N < 2^31), so the loops below count in 32 bits and never divide
   const long long first = (long long)blockIdx.x * ngrp;
   const long long stride = (long long)gridDim.x * ngrp;
+  // (N < 2^31 rows: 32-bit division, a few instructions instead of a 64-bit subroutine)
   auto rows_of = [&](int gr) -> int {
     const long long f = first + gr;
-    return f < N ? (int)((N - 1 - f) / stride + 1) : 0;
+    return f < N ? (int)((uint32_t)(N - 1 - f) / (uint32_t)stride + 1) : 0;
   };
   if (threadIdx.x == 0) trace_stamp(trace, trace_cap, 0);  // slot 0: CTA start
   pdl_trigger();
@@ -515,6 +516,7 @@ static poetx_status perm_rows_any(size_t esize, bool scatter, const void* X, lon
                                   const float* scale, float* scale_out, long long sp,
                                   long long dp, bool side, cudaStream_t s) {
   if (N == 0 || D == 0) return POETX_OK;
+  if (N > 0x7fffffffLL) return POETX_ERR_SHAPE;  // rows are counted in 32 bits
   sp = sp ? sp : D;
   dp = dp ? dp : D;
   if (sp < D || dp < D) return POETX_ERR_ARG;
