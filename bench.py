@@ -58,6 +58,9 @@ def parse():
     ap.add_argument("--group", default="on", choices=["on", "off"],
                     help="run the workload's layers as one layer group (one batched CNP "
                          "forward and backward per step; default) or layer by layer")
+    ap.add_argument("--layers", default=None,
+                    help="comma-separated names of the workload's layers to keep (profiling "
+                         "cases, e.g. --layers gate)")
     ap.add_argument("--tokens", type=int, default=None,
                     help="override the workload's token count (profiling cases)")
     ap.add_argument("--launches-only", action="store_true",
@@ -465,6 +468,12 @@ def main():
 
     # ---------------------------------------------------------------- the headline workload
     wl = inputs.WORKLOADS[args.workload]
+    if args.layers:
+        import dataclasses
+        keep = args.layers.split(",")
+        wl = dataclasses.replace(wl, layers=tuple(l for l in wl.layers if l.name in keep))
+        if not wl.layers:
+            raise SystemExit(f"--layers {args.layers}: no such layer in {args.workload}")
     variant = args.variant or ("mem" if wl.wdt == "i8" else wl.variants[0])
     c_setup = P.poetx_launch_count()
     rig = Rig(P, wl, variant, dev, N=args.tokens, group=args.group == "on")

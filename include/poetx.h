@@ -166,8 +166,10 @@ poetx_status poetx_cnp_bwd(const float* q, const float* dG, int splits, int nblk
  * the same kernels, and takes the same arguments minus the workspace.
  *   Scratch: a fixed 16 MiB fp32 array in the library's device image; every GPU that loads
  *   the library holds it until the process exits.  The first call on a device looks up the
- *   array's device address (cudaGetSymbolAddress, with that device current); make that first
- *   call before any stream capture.  All calls on a device share the array and it keeps the
+ *   array's device address (cudaGetSymbolAddress, with that device current) and keeps it;
+ *   make that first call before any stream capture.  A cudaDeviceReset reloads the device
+ *   image, after which the kept address is stale: do not call this entry point again in a
+ *   process that has reset the device.  All calls on a device share the array and it keeps the
  *   last call's contents: calls that overlap on the GPU (on streams not ordered with each
  *   other) race and give wrong results, so order them.  Nothing in it needs to start at zero:
  *   every element read is first written by the same call.
