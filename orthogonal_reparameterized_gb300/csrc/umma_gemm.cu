@@ -131,8 +131,9 @@ template <int BN, int RES>
 constexpr int res_bytes() { return RES * BN * BK * 2; }
 
 // Columns the epilogue stages per pass: 64, or 32 when the operand ring leaves no room.
-template <int BN, int STAGES, bool OUT_F32, int RES, int CL = 1>
+template <int BN, int STAGES, bool OUT_F32, int RES, int CL = 1, bool TOUT = false>
 constexpr int epi_pass_cols() {
+  if (TOUT) return 64;  // dense 32 x 64 bf16 boxes (4 KB per warp)
   constexpr int ring = STAGES * stage_bytes<BN, RES, CL>() + res_bytes<BN, RES>();
   constexpr int esz = OUT_F32 ? 4 : 2;
   constexpr int wc = BN / (kEpiWarps / 4);
@@ -168,10 +169,17 @@ __device__ __forceinline__ uint32_t i8x2_to_bf16x2(uint32_t w, int lo) {
 // arrive on both CTAs' barriers; both CTAs' epilogue warps release an accumulator on the
 // even CTA's "empty" barrier; neither CTA exits before the other has drained what is aimed
 // at it.
-template <int BN, int STAGES, bool A_MN, bool B_MN, bool OUT_F32, int RES, int CL>
+//
+// TOUT (bf16 block-diagonal products): each epilogue warp converts its 32 rows x 64 columns
+// into a dense, 128-byte-swizzled shared-memory box (conflict-free: lane = row, 16-byte
+// chunk k at k ^ (row % 8)) that one lane stores by TMA through tmC, so the warp moves on to
+// the next accumulator while the copy drains; rows past the tensor's end are clipped by the
+// TMA unit.
+template <int BN, int STAGES, bool A_MN, bool B_MN, bool OUT_F32, int RES, int CL, bool TOUT>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     umma_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
-                     const __grid_constant__ CUtensorMap tmB, const UmmaParams p) {
+                     const __grid_constant__ CUtensorMap tmB,
+                     const __grid_constant__ CUtensorMap tmC, const UmmaParams p) {
   constexpr uint32_t A_BYTES = BM * BK * 2;
   constexpr uint32_t B_BYTES = BN * BK * 2;
   constexpr uint32_t STAGE_BYTES = stage_bytes<BN, RES, CL>();
@@ -184,8 +192,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   // per epilogue warp: 32 rows x 64 columns staging buffer (rows padded by 16 bytes), so
   // that the global stores cover whole row segments instead of 16 bytes of 32 rows each
   constexpr uint32_t ESZ = OUT_F32 ? 4 : 2;
-  constexpr int EPC = epi_pass_cols<BN, STAGES, OUT_F32, RES, CL>();  // columns per pass
-  constexpr uint32_t STG_PITCH = EPC * ESZ + 16;
+  constexpr int EPC = epi_pass_cols<BN, STAGES, OUT_F32, RES, CL, TOUT>();  // columns per pass
+  constexpr uint32_t STG_PITCH = TOUT ? 128 : EPC * ESZ + 16;
+  static_assert(!TOUT || (!OUT_F32 && CL == 1 && (BN / (kEpiWarps / 4)) % 64 == 0),
+                "TMA-stored epilogue: bf16 output, 64-column passes");
   uint8_t* resb = smem + STAGES * STAGE_BYTES;            // resident B panel (RES > 0)
   uint8_t* staging = resb + res_bytes<BN, RES>();         // EPIW buffers
   constexpr int EPIW = kEpiWarps;
@@ -458,13 +468,31 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             for (int i = 0; i < 64; ++i)
               if (i < ncol) v[i] *= __ldg(p.colscale + c.out_col0 + c0 + i);
           }
-          uint4* dst = reinterpret_cast<uint4*>(stg + lane * STG_PITCH);
+          if (TOUT) {
+            // the previous pass's box must have been read by its TMA store
+            if (lane == 0) bulk_wait_read<0>();
+            __syncwarp();
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            if (8 * i < ncol)
-              dst[i] = make_uint4(pack_bf16x2(v[8 * i], v[8 * i + 1]), pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
-                                  pack_bf16x2(v[8 * i + 4], v[8 * i + 5]), pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
+            for (int i = 0; i < 8; ++i)
+              *reinterpret_cast<uint4*>(stg + lane * 128 + ((i ^ (lane & 7)) << 4)) =
+                  make_uint4(pack_bf16x2(v[8 * i], v[8 * i + 1]), pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
+                             pack_bf16x2(v[8 * i + 4], v[8 * i + 5]), pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
+            fence_async_shared();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tmC, stg, (int)(c.out_col0 + c0), (int)row0);
+              bulk_commit();
+            }
+          } else {
+            uint4* dst = reinterpret_cast<uint4*>(stg + lane * STG_PITCH);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              if (8 * i < ncol)
+                dst[i] = make_uint4(pack_bf16x2(v[8 * i], v[8 * i + 1]), pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
+                                    pack_bf16x2(v[8 * i + 4], v[8 * i + 5]), pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
+          }
         }
+        if (TOUT) continue;  // stored by TMA above
         __syncwarp();
         // lanes cover whole row segments: (ncol * ESZ / 16) lanes per row
         const int per_row = ncol * (int)ESZ / 16;
@@ -505,6 +533,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
   }
   if (warp == 2 && lane == 0) trace_stamp(p.trace, p.trace_cap, 30);  // epilogue loop done
+  if (TOUT && warp >= 2 && lane == 0) bulk_wait_all();  // this warp's stores have landed
   tc_fence_before();
   if (CL > 1) cluster_sync();
   else __syncthreads();
@@ -1182,15 +1211,22 @@ bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, u
 }
 
 // CL = 2: tiles_m counts pairs of M tiles (see tile_coords).
-template <int BN, int STAGES, bool A_MN, bool B_MN, bool OUT_F32, int RES = 0, int CL = 1>
+// TOUT: the output is stored by TMA through tc (a bf16 [rows][columns] map with 32 x 64 boxes
+// and the 128-byte swizzle); otherwise tc is not read.
+template <int BN, int STAGES, bool A_MN, bool B_MN, bool OUT_F32, int RES = 0, int CL = 1,
+          bool TOUT = false>
 poetx_status launch(const CUtensorMap& ta, const CUtensorMap& tb, UmmaParams p, int tiles_m,
-                    int tiles_n, int tiles_z, cudaStream_t s) {
+                    int tiles_n, int tiles_z, cudaStream_t s, const CUtensorMap* tc = nullptr) {
   const int stage = p.mode == MODE_PLAIN ? ST_WPRIME : (p.mode == MODE_BLOCKDIAG ? ST_BLOCKDIAG : ST_WGRAD);
-  auto k = umma_gemm_kernel<BN, STAGES, A_MN, B_MN, OUT_F32, RES, CL>;
-  constexpr int smem = STAGES * stage_bytes<BN, RES, CL>() + res_bytes<BN, RES>() +
-                       kEpiWarps * 32 *
-                           (epi_pass_cols<BN, STAGES, OUT_F32, RES, CL>() * (OUT_F32 ? 4 : 2) + 16) +
+  auto k = umma_gemm_kernel<BN, STAGES, A_MN, B_MN, OUT_F32, RES, CL, TOUT>;
+  constexpr int stg_bytes =
+      TOUT ? kEpiWarps * 32 * 128
+           : kEpiWarps * 32 *
+                 (epi_pass_cols<BN, STAGES, OUT_F32, RES, CL>() * (OUT_F32 ? 4 : 2) + 16);
+  constexpr int smem = STAGES * stage_bytes<BN, RES, CL>() + res_bytes<BN, RES>() + stg_bytes +
                        1024 + 512;
+  if (TOUT && !tc) return POETX_ERR_ARG;
+  const CUtensorMap& tcm = TOUT ? *tc : tb;
   // CTAs per SM: bounded by TMEM (2 x BN columns each, 512 per SM) and shared memory.
   constexpr int by_tmem = 512 / (2 * BN);
   constexpr int by_smem = (int)((227 * 1024) / (smem + 1024));
@@ -1228,9 +1264,10 @@ poetx_status launch(const CUtensorMap& ta, const CUtensorMap& tb, UmmaParams p, 
   const long long want = CL > 1 ? max_clusters : (long long)sm_count() * per_sm;
   const int grid = CL * (int)(tiles < want ? tiles : want);
   if (CL > 1)
-    POETX_CUDA_TRY(launch_pdl_cluster(k, dim3(grid), dim3(kGemmThreads), smem, s, CL, ta, tb, p));
+    POETX_CUDA_TRY(launch_pdl_cluster(k, dim3(grid), dim3(kGemmThreads), smem, s, CL, ta, tb, tcm,
+                                      p));
   else
-    POETX_CUDA_TRY(launch_pdl(k, dim3(grid), dim3(kGemmThreads), smem, s, ta, tb, p));
+    POETX_CUDA_TRY(launch_pdl(k, dim3(grid), dim3(kGemmThreads), smem, s, ta, tb, tcm, p));
   POETX_CUDA_TRY(cudaGetLastError());
   after_launch(s, stage);
   return POETX_OK;
@@ -1336,7 +1373,24 @@ poetx_status umma_blockdiag(const void* X, long long N, int nblk, int b, const v
   p.bpre = static_cast<const uint8_t*>(G);
   p.bpre_bytes = (unsigned long long)nblk * b * b * 2;
   const int tm = (int)((N + BM - 1) / BM), tn = b / BN;
-  // resident G panel of b/64 K blocks; the ring carries only the activation tiles
+  // resident G panel of b/64 K blocks; the ring carries only the activation tiles; with
+  // 128-wide tiles and a plain output the epilogue stores by TMA
+  CUtensorMap tc;
+  if (BN == 128 && !out_perm) {
+    if (!make_map(&tc, Y, D, N, D, 64, 32)) return POETX_ERR_CUDA;
+    if (trans) {
+      switch (b) {
+        case 128: return launch<128, 10, false, false, false, 2, 1, true>(ta, tb, p, tm, tn, nblk, s, &tc);
+        case 256: return launch<128, 8, false, false, false, 4, 1, true>(ta, tb, p, tm, tn, nblk, s, &tc);
+        default: return launch<128, 4, false, false, false, 8, 1, true>(ta, tb, p, tm, tn, nblk, s, &tc);
+      }
+    }
+    switch (b) {
+      case 128: return launch<128, 10, false, true, false, 2, 1, true>(ta, tb, p, tm, tn, nblk, s, &tc);
+      case 256: return launch<128, 8, false, true, false, 4, 1, true>(ta, tb, p, tm, tn, nblk, s, &tc);
+      default: return launch<128, 4, false, true, false, 8, 1, true>(ta, tb, p, tm, tn, nblk, s, &tc);
+    }
+  }
   if (trans) {
     switch (b) {
       case 64: return launch<64, 10, false, false, false, 1>(ta, tb, p, tm, tn, nblk, s);

@@ -214,21 +214,22 @@ def test_layer_bf16_split_tiles_deterministic(P):
                                      (2048, 1024, 256, 1000)])
 @pytest.mark.parametrize("variant", ["fast", "mem"])
 def test_layer_fused_and_separate_products_agree(P, m, n, b, N, variant):
-    """The W' contraction fused with the block-diagonal product after it (one kernel) and
-    the two as separate kernels both match the oracle, and each other to within their
-    accumulation-order differences."""
+    """Every fusion mask (the W' contraction with the block-diagonal product after it as one
+    kernel, bit 0; each backward block product with its weight gradient as one kernel, bit 1)
+    matches the oracle, and the separate kernels to within accumulation-order differences."""
     inp = inputs.small_layer_inputs(61 + b, m, n, b, N, act="bf16", wdt="bf16")
+    got = {}
     try:
-        P.poetx_set_fusion(False)
-        sep = run_layer(P, inp, b, "bf16", "bf16", variant)
+        for mask in (0, 1, 2, 3):
+            P.poetx_set_fusion(mask)
+            got[mask] = run_layer(P, inp, b, "bf16", "bf16", variant)
     finally:
         P.poetx_set_fusion(True)
-    fus = run_layer(P, inp, b, "bf16", "bf16", variant)
-    ref = oracle_for(inp, fus, b)
-    check(sep, ref, TOL_BF16_LAYER)
-    check(fus, ref, TOL_BF16_LAYER)
-    for k in ("y", "dx", "dq_R", "dq_P"):
-        assert O.rel_fro(fus[k], sep[k]) <= 1e-2, k
+    ref = oracle_for(inp, got[3], b)
+    for mask, r in got.items():
+        check(r, ref, TOL_BF16_LAYER)
+        for k in ("y", "dx", "dq_R", "dq_P"):
+            assert O.rel_fro(r[k], got[0][k]) <= 1e-2, (mask, k)
 
 
 def _random_shapes(count, seed=2026):
