@@ -33,26 +33,35 @@ __device__ __forceinline__ int side_of(const SideTable& t, int blk) {
   return k;
 }
 
-// One CTA per 32 x 32 tile (I, J) with I <= J of a block: it reads the packed entries of the
-// tile's upper part (consecutive j are consecutive in q), writes Q[I][J] and, through shared
-// memory, the mirrored tile Q[J][I] = -Q[I][J]^T, both with coalesced rows.  The entries of a
-// ragged last block (valid features r < b) outside its r x r corner are not parameters and
-// are zero in Q.
+// Upper tiles per CTA of the unpack and the gradient pack: every thread issues the loads of all
+// of its CTA's tiles before the first store, so that enough bytes are in flight per SM for
+// these short, latency-bound passes.
+constexpr int kTriTiles = 4;
+
+// Linear upper-tile index t of a block -> (I, J), I <= J, of its nt x nt tiles of 32.
+__device__ __forceinline__ void upper_tile(int t, int nt, int& I, int& J) {
+  I = 0;
+  while (t >= nt - I) {
+    t -= nt - I;
+    ++I;
+  }
+  J = I + t;
+}
+
+// Each CTA takes kTriTiles 32 x 32 tiles (I, J), I <= J, of a block: per tile it reads the
+// packed entries of the tile's upper part (consecutive j are consecutive in q), writes Q[I][J]
+// and, through shared memory, the mirrored tile Q[J][I] = -Q[I][J]^T, both with coalesced
+// rows.  The entries of a ragged last block (valid features r < b) outside its r x r corner
+// are not parameters and are zero in Q.
 __global__ void triu_unpack_kernel(const __grid_constant__ SideTable st, int b,
                                    float* __restrict__ Q, unsigned long long* tr, size_t tr_cap) {
   if (threadIdx.x == 0 && threadIdx.y == 0) trace_stamp3(tr, tr_cap, 0);
   pdl_trigger();
   pdl_wait();
-  __shared__ float tile[32][33];
+  __shared__ float tile[kTriTiles][32][33];
   const int blk = blockIdx.z;
   const int nt = (b + 31) / 32;
-  // decode the linear upper-tile index blockIdx.x -> (I, J), I <= J
-  int t = blockIdx.x, I = 0;
-  while (t >= nt - I) {
-    t -= nt - I;
-    ++I;
-  }
-  const int J = I + t;
+  const int ntiles = nt * (nt + 1) / 2;
   const long long tri = (long long)b * (b - 1) / 2;
   const int k = side_of(st, blk);
   const int local = blk - st.start[k];
@@ -60,22 +69,44 @@ __global__ void triu_unpack_kernel(const __grid_constant__ SideTable st, int b,
   float* Qb = Q + (long long)blk * b * b;
   const int rv = blk == st.start[k + 1] - 1 ? st.valid[k] : b;
   const int tx = threadIdx.x, ty = threadIdx.y;  // 32 x 8
-  for (int r = ty; r < 32; r += 8) {
-    const int i = I * 32 + r, j = J * 32 + tx;
-    float v = 0.f;
-    if (i < b && j < b) {
-      if (i >= rv || j >= rv) v = 0.f;
-      else if (i < j) v = qb[tri_index(i, j, b)];
-      else if (i > j) v = -qb[tri_index(j, i, b)];
-      Qb[(long long)i * b + j] = v;
+  int I[kTriTiles], J[kTriTiles];
+  float v[kTriTiles][4];
+#pragma unroll
+  for (int u = 0; u < kTriTiles; ++u) {  // every load first
+    const int t = blockIdx.x * kTriTiles + u;
+    upper_tile(t < ntiles ? t : 0, nt, I[u], J[u]);
+    if (t >= ntiles) I[u] = -1;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int i = I[u] * 32 + ty + 8 * c, j = J[u] * 32 + tx;
+      float x = 0.f;
+      if (I[u] >= 0 && i < rv && j < rv) {
+        if (i < j) x = __ldg(qb + tri_index(i, j, b));
+        else if (i > j) x = -__ldg(qb + tri_index(j, i, b));
+      }
+      v[u][c] = x;
     }
-    tile[r][tx] = v;
   }
-  if (I != J) {  // the diagonal tile wrote both of its triangles already
-    __syncthreads();
-    for (int c = ty; c < 32; c += 8) {
-      const int i = J * 32 + c, j = I * 32 + tx;  // Q[i][j] = -Q[j][i]
-      if (i < b && j < b) Qb[(long long)i * b + j] = -tile[tx][c];
+#pragma unroll
+  for (int u = 0; u < kTriTiles; ++u) {
+    if (I[u] < 0) continue;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int r = ty + 8 * c;
+      const int i = I[u] * 32 + r, j = J[u] * 32 + tx;
+      if (i < b && j < b) Qb[(long long)i * b + j] = v[u][c];
+      tile[u][r][tx] = v[u][c];
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int u = 0; u < kTriTiles; ++u) {
+    if (I[u] < 0 || I[u] == J[u]) continue;  // a diagonal tile wrote both of its triangles
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int cc = ty + 8 * c;
+      const int i = J[u] * 32 + cc, j = I[u] * 32 + tx;  // Q[i][j] = -Q[j][i]
+      if (i < b && j < b) Qb[(long long)i * b + j] = -tile[u][tx][cc];
     }
   }
   if (tr) {
@@ -84,10 +115,10 @@ __global__ void triu_unpack_kernel(const __grid_constant__ SideTable st, int b,
   }
 }
 
-// dq_ij (+)= Qbar_ij - Qbar_ji for i < j.  One CTA per 32 x 32 tile (I, J), I <= J, of a
-// block: the mirrored tile Qbar[J][I] is read with coalesced rows into shared memory and
-// read back transposed, so both reads of Qbar are coalesced; the writes of a row i of the
-// tile are consecutive entries of the packed triangle.
+// dq_ij (+)= Qbar_ij - Qbar_ji for i < j.  Each CTA takes kTriTiles 32 x 32 tiles (I, J),
+// I <= J, of a block: the mirrored tile Qbar[J][I] is read with coalesced rows into shared
+// memory and read back transposed, so both reads of Qbar are coalesced; the writes of a row i
+// of the tile are consecutive entries of the packed triangle.
 // pa (nullable q): the optimizer update applied to each entry as its gradient is written
 // (single-replica training: nothing has to be summed between the pack and the update).
 __global__ void triu_grad_pack_kernel(const float* __restrict__ Qbar, int b,
@@ -97,15 +128,10 @@ __global__ void triu_grad_pack_kernel(const float* __restrict__ Qbar, int b,
   if (threadIdx.x == 0 && threadIdx.y == 0) trace_stamp3(tr, tr_cap, 0);
   pdl_trigger();
   pdl_wait();
-  __shared__ float tile[32][33];
+  __shared__ float tile[kTriTiles][32][33];
   const int blk = blockIdx.z;
   const int nt = (b + 31) / 32;
-  int t = blockIdx.x, I = 0;
-  while (t >= nt - I) {
-    t -= nt - I;
-    ++I;
-  }
-  const int J = I + t;
+  const int ntiles = nt * (nt + 1) / 2;
   const long long tri = (long long)b * (b - 1) / 2;
   const float* Qb = Qbar + (long long)blk * b * b;
   const int side = side_of(st, blk);
@@ -113,22 +139,42 @@ __global__ void triu_grad_pack_kernel(const float* __restrict__ Qbar, int b,
   float* dqb = st.dst[side] + off;
   const int rv = blk == st.start[side + 1] - 1 ? st.valid[side] : b;
   const int tx = threadIdx.x, ty = threadIdx.y;  // 32 x 8
-  for (int r = ty; r < 32; r += 8) {  // tile[r][c] = Qbar[J*32 + r][I*32 + c]
-    const int j = J * 32 + r, i = I * 32 + tx;
-    tile[r][tx] = (j < b && i < b) ? Qb[(long long)j * b + i] : 0.f;
+  int I[kTriTiles], J[kTriTiles];
+  float d[kTriTiles][4];
+#pragma unroll
+  for (int u = 0; u < kTriTiles; ++u) {  // every load first
+    const int t = blockIdx.x * kTriTiles + u;
+    upper_tile(t < ntiles ? t : 0, nt, I[u], J[u]);
+    if (t >= ntiles) I[u] = -1;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int r = ty + 8 * c;
+      // tile[u][r][tx] = Qbar[J*32 + r][I*32 + tx]; d = Qbar[I*32 + r][J*32 + tx]
+      const int jm = J[u] * 32 + r, im = I[u] * 32 + tx;
+      const int i = I[u] * 32 + r, j = J[u] * 32 + tx;
+      const bool live = I[u] >= 0;
+      tile[u][r][tx] = (live && jm < b && im < b) ? __ldg(Qb + (long long)jm * b + im) : 0.f;
+      d[u][c] = (live && i < j && j < b) ? __ldg(Qb + (long long)i * b + j) : 0.f;
+    }
   }
   __syncthreads();
-  for (int r = ty; r < 32; r += 8) {
-    const int i = I * 32 + r, j = J * 32 + tx;
-    if (i < j && j < b) {
-      const float v = j < rv ? Qb[(long long)i * b + j] - tile[tx][r] : 0.f;
-      const long long k = tri_index(i, j, b);
-      float* dst = dqb + k;
-      const float g = accumulate ? *dst + v : v;
-      *dst = g;
-      if (pa.q[side]) {
-        const long long e = off + k;
-        adam_one(pa.q[side][e], g, pa.m[side][e], pa.v[side][e], pa.h);
+#pragma unroll
+  for (int u = 0; u < kTriTiles; ++u) {
+    if (I[u] < 0) continue;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int r = ty + 8 * c;
+      const int i = I[u] * 32 + r, j = J[u] * 32 + tx;
+      if (i < j && j < b) {
+        const float v = j < rv ? d[u][c] - tile[u][tx][r] : 0.f;
+        const long long kk = tri_index(i, j, b);
+        float* dst = dqb + kk;
+        const float g = accumulate ? *dst + v : v;
+        *dst = g;
+        if (pa.q[side]) {
+          const long long e = off + kk;
+          adam_one(pa.q[side][e], g, pa.m[side][e], pa.v[side][e], pa.h);
+        }
       }
     }
   }
@@ -142,7 +188,7 @@ poetx_status launch_triu_unpack_sides(const SideTable& t, int b, float* Q, cudaS
   const int total = t.start[t.count];
   if (total == 0) return POETX_OK;
   const int nt = (b + 31) / 32;
-  dim3 grid(nt * (nt + 1) / 2, 1, total);
+  dim3 grid((nt * (nt + 1) / 2 + kTriTiles - 1) / kTriTiles, 1, total);
   size_t tr_cap = 0;
   unsigned long long* tr = trace_buffer(&tr_cap);
   POETX_CUDA_TRY(launch_pdl(triu_unpack_kernel, grid, dim3(32, 8), 0, s, t, b, Q, tr, tr_cap));
@@ -166,7 +212,7 @@ poetx_status launch_triu_grad_pack_sides(const float* Qbar, const SideTable& t, 
   const int total = t.start[t.count];
   if (total == 0 || b < 2) return POETX_OK;
   const int nt = (b + 31) / 32;
-  dim3 grid(nt * (nt + 1) / 2, 1, total);
+  dim3 grid((nt * (nt + 1) / 2 + kTriTiles - 1) / kTriTiles, 1, total);
   size_t tr_cap = 0;
   unsigned long long* tr = trace_buffer(&tr_cap);
   PackAdam none{};
