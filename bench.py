@@ -795,8 +795,12 @@ def setup_measure(P, torch, rig, flush, pk, dev):
     us = median_us(torch, flush, lambda: P.poetx_merge_reinit(d["L"], W0n, mws))
     fl = 2.0 * n * m * b * 2
     setup["merge_reinit"] = {"us": us, "flops": fl, "tflops_fp32": fl / (us * 1e-6) / 1e12,
-                             "note": "fp32 products + CNP + permutation inverse and gather; "
-                                     "once per many steps"}
+                             "engine": ("tensor cores, three-pass tf32"
+                                        if P.poetx_layer_cuda_core_steps(d["L"], 0) & 1 == 0
+                                        else "CUDA cores, fp32"),
+                             "note": "the two block-product passes over W' (fp32 accuracy) + "
+                                     "the CNP + permutation inverse and gather; once per many "
+                                     "steps"}
     del W0n, mws
     npar = rig.q.flat.numel()
     oq = torch.zeros(npar, device=dev)

@@ -298,8 +298,9 @@ typedef struct poetx_layer {
 size_t poetx_layer_workspace_bytes(const poetx_layer* L, int N, int phase);
 
 /* Which of the layer's products run on the CUDA cores instead of the tcgen05 tensor cores,
- * as a bit mask: bit 0 the CNP products, bit 1 the block-diagonal products and their weight
- * gradients, bit 2 the W' contraction; 0 when everything runs on the tensor cores.  bf16 and
+ * as a bit mask: bit 0 the CNP products (and poetx_merge_reinit's block products), bit 1
+ * the block-diagonal products and their weight gradients, bit 2 the W' contraction; 0 when
+ * everything runs on the tensor cores.  bf16 and
  * int8 layers take the tensor cores for every shape the descriptor accepts (on sm_103 with
  * the default engine); fp32 layers run their layer products on the CUDA cores (1e-5
  * accuracy), their CNP on the tensor cores.  -1 for an invalid descriptor.  Host-only. */
@@ -395,7 +396,9 @@ poetx_status poetx_layer_step_host(const poetx_layer* L, const void* x, const vo
  *   i.e.  W0_new[perm_n[r], perm_m[c]] = (blkdiag(G_P)^T W' blkdiag(G_R)^T)[r, c],
  * with G_R, G_P the CNP (order L->order) of the layer's current q_R, q_P and W' = L->Wp
  * (times L->w_scale per row for an int8 layer).  W0_new: [n, m] fp32, device, 16-byte
- * aligned, in the original (unpermuted) coordinates of W0.  fp32 arithmetic throughout.
+ * aligned, in the original (unpermuted) coordinates of W0.  fp32 accuracy throughout: the two
+ * block-product passes over W' run on the tensor cores with the CNP's three-pass tf32 split
+ * (b a multiple of 32; bit 0 of poetx_layer_cuda_core_steps clear), else on the CUDA cores.
  * The reinitialisation is then the caller's: set q_R and q_P to zero, draw new
  * permutations, and merge them into W0_new with poetx_merge_perm (an int8 layer first
  * re-quantises W0_new with poetx_quantize_rows_int8).  ws: at least

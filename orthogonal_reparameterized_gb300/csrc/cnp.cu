@@ -281,7 +281,7 @@ size_t cnp_fwd_scratch_bytes(int nblk, int b) { return 2 * blk_bytes(nblk, b); }
 size_t cnp_bwd_scratch_bytes(int nblk, int b) { return 7 * blk_bytes(nblk, b); }
 
 poetx_status cnp_forward_sides(const CnpSides& q, int b, float* Qs, float* Q2, float* G_f32,
-                               void* G_bf16, void* Gt_bf16, cudaStream_t s) {
+                               void* G_bf16, void* Gt_bf16, cudaStream_t s, float* Gt_f32) {
   const int nblk = q.total();
   if (nblk == 0) return POETX_OK;
   POETX_TRY(launch_triu_unpack_sides(q.table(b), b, Qs, s));
@@ -306,9 +306,26 @@ poetx_status cnp_forward_sides(const CnpSides& q, int b, float* Qs, float* Q2, f
   h.e2 = 2.f;
   h.eI = 1.f;
   h.out_f32 = G_f32;
+  h.out_f32_t = Gt_f32;
   h.out_bf16 = static_cast<__nv_bfloat16*>(G_bf16);
   h.out_bf16_t = static_cast<__nv_bfloat16*>(Gt_bf16);
   return launch_cnp_gemm(h, nblk, ST_CNP_G, s);
+}
+
+poetx_status matrix_blockmm_tc(const float* A, long long rows, int nblk, int b, const float* Bt,
+                               float* C, float* Ct, int stage, cudaStream_t s) {
+  if (nblk == 0 || rows == 0) return POETX_OK;
+  if (!(use_tensor_cores() && cnp_umma_ok(b))) return POETX_ERR_UNSUPPORTED;
+  CnpGemm g{};
+  g.b = b;
+  g.nseg = 1;
+  g.A[0] = op1(A, 1.f);
+  g.B[0] = op1(Bt, 1.f);
+  g.a_mat = A;
+  g.a_rows = rows;
+  g.out_f32 = C;
+  g.out_f32_t = Ct;
+  return launch_cnp_gemm(g, nblk, stage, s);
 }
 
 poetx_status cnp_forward(const float* q, int nblk, int b, float* Qs, float* Q2, float* G_f32,

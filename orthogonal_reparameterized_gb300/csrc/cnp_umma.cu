@@ -55,6 +55,12 @@ struct TOp {
 
 struct CnpUParams {
   int b;
+  // Geometry: batch entry j makes output rows 0 .. M-1 (M = b for a CNP product); its A tile
+  // (rows i0 .., K columns k0 ..) sits at coordinate (a_col_blk j + k0, a_row_blk j + i0) of
+  // the A map; output element (i, c) goes to out[j o_blk + i o_ld + c] and to
+  // out_t[j ot_blk + c ot_ld + i].
+  int M, a_row_blk, a_col_blk;
+  long long o_blk, o_ld, ot_blk, ot_ld;
   int nmaps;
   int nseg;
   int kb_per_seg;
@@ -244,7 +250,7 @@ __global__ void __launch_bounds__(cnp_threads(BN), 1)
   const int row0 = blk * b;  // first row of this block in the [nblk*b, b] views
   const long long base = (long long)blk * b * b;
   const int i0 = mt * BM, j0 = nt * BN;
-  const int rows = b - i0 < BM ? b - i0 : BM;  // valid rows of the tile; b % 32 == 0
+  const int rows = p.M - i0 < BM ? p.M - i0 : BM;  // valid rows of the tile; M % 32 == 0
 
   if (warp == 0 && lane == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -298,7 +304,8 @@ __global__ void __launch_bounds__(cnp_threads(BN), 1)
       uint8_t* st = smem + s * STAGE_BYTES;
       for (int i = 0; i < 2; ++i) {
         if (A.s[i].map >= 0)  // rows mt*128.. of A (one 32 x 128 box)
-          tma_load_2d(st + i * A_BYTES, &maps.m[A.s[i].map], &full[s], k0, row0 + i0);
+          tma_load_2d(st + i * A_BYTES, &maps.m[A.s[i].map], &full[s], p.a_col_blk * blk + k0,
+                      p.a_row_blk * blk + i0);
         if (B.s[i].map >= 0)  // rows nt*BN.. of B^T, columns k0..k0+31 (one 32 x BN box)
           tma_load_2d(st + 2 * A_BYTES + i * B_BYTES, &maps.m[B.s[i].map], &full[s], k0,
                       row0 + j0);
@@ -525,7 +532,7 @@ __global__ void __launch_bounds__(cnp_threads(BN), 1)
       if (i == j + 2) o.z += p.eI;
       if (i == j + 3) o.w += p.eI;
       *tp = o;
-      const long long idx = base + (long long)i * b + j;
+      const long long idx = blk * p.o_blk + (long long)i * p.o_ld + j;
       if (p.out_f32) *reinterpret_cast<float4*>(p.out_f32 + idx) = o;
       if (p.out_bf16)
         *reinterpret_cast<uint2*>(p.out_bf16 + idx) =
@@ -543,7 +550,7 @@ __global__ void __launch_bounds__(cnp_threads(BN), 1)
         const float o[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          const long long tidx = base + (long long)(j0 + c + k) * b + (i0 + rr);
+          const long long tidx = blk * p.ot_blk + (long long)(j0 + c + k) * p.ot_ld + (i0 + rr);
           if (p.out_f32_t) p.out_f32_t[tidx] = o[k];
           if (p.out_bf16_t) p.out_bf16_t[tidx] = __float2bfloat16_rn(o[k]);
         }
@@ -636,7 +643,7 @@ poetx_status launch_t(const CnpMaps& maps, const CnpUParams& p, int nblk, cudaSt
     attr = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   });
   POETX_CUDA_TRY(attr);
-  dim3 grid((p.b + BM - 1) / BM, p.b / BN, nblk);
+  dim3 grid((p.M + BM - 1) / BM, p.b / BN, nblk);
   POETX_CUDA_TRY(launch_pdl(k, grid, dim3(cnp_threads(BN)), smem, s, maps, p));
   POETX_CUDA_TRY(cudaGetLastError());
   return POETX_OK;
@@ -650,8 +657,12 @@ bool cnp_umma_ok(int b) {
 
 poetx_status cnp_umma_product(const CnpProduct& g, int nblk, cudaStream_t s) {
   if (nblk == 0) return POETX_OK;
+  const long long M = g.a_mat ? g.a_rows : g.b;
+  if (g.a_mat && (M <= 0 || M % 32 || M > 0x7fffffffLL || g.nseg != 1 || g.A[0].p1 != g.a_mat ||
+                  g.A[0].p2 || g.E1 || g.E2 || g.eI != 0.f || g.out_bf16 || g.out_bf16_t))
+    return POETX_ERR_ARG;
   // 128-wide tiles once 64-wide ones would take more than one wave of CTAs (one per SM)
-  const long long tiles64 = (long long)((g.b + BM - 1) / BM) * (g.b / 64) * nblk;
+  const long long tiles64 = (long long)((M + BM - 1) / BM) * (g.b / 64) * nblk;
   const int BN = (g.b % 128 == 0 && g.b >= 256 && tiles64 > sm_count()) ? 128
                  : (g.b % 64 == 0 ? 64 : 32);
   CnpMaps maps;
@@ -664,13 +675,33 @@ poetx_status cnp_umma_product(const CnpProduct& g, int nblk, cudaStream_t s) {
     for (int i = 0; i < nmaps; ++i)
       if (ptrs[i] == ptr && roles[i] == role) return i;
     if (nmaps == NMAPS) return -2;
-    if (!make_blk_map(&maps.m[nmaps], ptr, nblk, g.b, role == 0 ? BM : BN)) return -3;
+    if (role == 0 && g.a_mat && ptr == g.a_mat) {  // [a_rows, nblk b] matrix, 128-row boxes
+      const uint64_t cols = (uint64_t)nblk * g.b;
+      if (!encode_tma_2d(&maps.m[nmaps], ptr, TMA_F32, cols, (uint64_t)M, cols, 32, BM, true))
+        return -3;
+    } else if (!make_blk_map(&maps.m[nmaps], ptr, nblk, g.b, role == 0 ? BM : BN)) {
+      return -3;
+    }
     ptrs[nmaps] = ptr;
     roles[nmaps] = role;
     return nmaps++;
   };
   CnpUParams p{};
   p.b = g.b;
+  p.M = (int)M;
+  if (g.a_mat) {  // column block j of the matrix; outputs [M, nblk b] and its transpose
+    p.a_row_blk = 0;
+    p.a_col_blk = g.b;
+    p.o_blk = g.b;
+    p.o_ld = (long long)nblk * g.b;
+    p.ot_blk = (long long)g.b * M;
+    p.ot_ld = M;
+  } else {  // the [nblk, b, b] stacks
+    p.a_row_blk = g.b;
+    p.a_col_blk = 0;
+    p.o_blk = p.ot_blk = (long long)g.b * g.b;
+    p.o_ld = p.ot_ld = g.b;
+  }
   p.nseg = g.nseg;
   p.kb_per_seg = g.b / BK;
   for (int sg = 0; sg < g.nseg; ++sg) {

@@ -32,6 +32,13 @@ struct CnpProduct {
   float* out_f32_t;       // fp32 output transposed
   __nv_bfloat16* out_bf16;
   __nv_bfloat16* out_bf16_t;
+  // Block products over a matrix (tensor-core engine only): when a_mat is set, A[0] is
+  // op(a_mat, 1), a_mat an fp32 [a_rows, nblk b] matrix (a_rows a multiple of 32), and batch
+  // entry j computes C_j = a_mat[:, jb .. jb + b) . B_j ([a_rows, b]); out_f32 is then the
+  // [a_rows, nblk b] result and out_f32_t its [nblk b, a_rows] transpose.  One segment, no
+  // epilogue terms, fp32 outputs only.
+  const float* a_mat;
+  long long a_rows;
 };
 
 bool cnp_umma_ok(int b);

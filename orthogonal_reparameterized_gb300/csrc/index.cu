@@ -682,6 +682,34 @@ __global__ void __launch_bounds__(256) dequant_rows_kernel(const int8_t* __restr
   }
 }
 
+// W[i] = float(Wb[i]) for a bf16 array (count a multiple of 4: four values per thread).
+__global__ void __launch_bounds__(256) widen_bf16_kernel(const __nv_bfloat16* __restrict__ Wb,
+                                                         long long quads, float* __restrict__ W) {
+  pdl_trigger();
+  pdl_wait();
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < quads;
+       i += (long long)gridDim.x * blockDim.x) {
+    const uint2 u = reinterpret_cast<const uint2*>(Wb)[i];
+    reinterpret_cast<float4*>(W)[i] =
+        make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u),
+                    __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xFFFF0000u));
+  }
+}
+
+poetx_status launch_widen_bf16(const void* Wb, long long count, float* W, cudaStream_t s) {
+  if (count == 0) return POETX_OK;
+  if (count % 4) return POETX_ERR_SHAPE;
+  const long long quads = count / 4;
+  long long blocks = (quads + 255) / 256;
+  const long long cap = (long long)sm_count() * 8;
+  if (blocks > cap) blocks = cap;
+  POETX_CUDA_TRY(launch_pdl(widen_bf16_kernel, dim3((unsigned)blocks), dim3(256), 0, s,
+                            static_cast<const __nv_bfloat16*>(Wb), quads, W));
+  POETX_CUDA_TRY(cudaGetLastError());
+  after_launch(s, ST_MERGE_REINIT);
+  return POETX_OK;
+}
+
 poetx_status launch_dequant_rows(const int8_t* Wq, const float* scale, int n, int m, float* W,
                                  cudaStream_t s) {
   if (n == 0 || m == 0) return POETX_OK;

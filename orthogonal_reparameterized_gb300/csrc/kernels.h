@@ -65,6 +65,8 @@ poetx_status launch_quantize(const float* W, int n, int m, int8_t* Wq, float* sc
 // inv_a[perm_a[i]] = i (i < na) and inv_b[perm_b[k]] = k (k < nb), one launch.
 poetx_status launch_invert_perms(const int32_t* perm_a, int na, int32_t* inv_a,
                                  const int32_t* perm_b, int nb, int32_t* inv_b, cudaStream_t s);
+// W[i] = float(Wb[i]) over `count` bf16 values (a multiple of 4), exactly.
+poetx_status launch_widen_bf16(const void* Wb, long long count, float* W, cudaStream_t s);
 // W[r][c] = scale[r] * Wq[r][c] (fp32 out, m % 4 == 0).
 poetx_status launch_dequant_rows(const int8_t* Wq, const float* scale, int n, int m, float* W,
                                  cudaStream_t s);
@@ -128,7 +130,15 @@ size_t cnp_bwd_scratch_bytes(int nblk, int b);
 poetx_status cnp_forward(const float* q, int nblk, int b, float* Qs, float* Q2, float* G_f32,
                          void* G_bf16, void* Gt_bf16, cudaStream_t s);
 poetx_status cnp_forward_sides(const CnpSides& q, int b, float* Qs, float* Q2, float* G_f32,
-                               void* G_bf16, void* Gt_bf16, cudaStream_t s);
+                               void* G_bf16, void* Gt_bf16, cudaStream_t s,
+                               float* Gt_f32 = nullptr);
+// Block products over a matrix on the tensor cores (fp32 accuracy by the three-pass tf32
+// split): for every column block j of the fp32 [rows, nblk b] matrix A,
+//   C[:, jb .. jb + b) = A[:, jb .. jb + b) . B_j,  B_j^T = Bt[j] of a [nblk, b, b] stack;
+// C ([rows, nblk b]) and Ct (its [nblk b, rows] transpose) nullable.  rows a multiple of 32.
+// POETX_ERR_UNSUPPORTED where the tensor-core engine does not take b.
+poetx_status matrix_blockmm_tc(const float* A, long long rows, int nblk, int b, const float* Bt,
+                               float* C, float* Ct, int stage, cudaStream_t s);
 // Backward CNP.  Q and Q2 may be the stacks kept from the forward, or NULL to recompute
 // them into the scratch; g.dG[k] / g.splits[k] / g.dq[k] per side.  scratch holds
 // cnp_bwd_scratch_bytes(total blocks, b) bytes.  pa (nullable): the optimizer update of

@@ -256,8 +256,14 @@ static Plan make_plan(const poetx_layer* L, long long N) {
 // by one gather, W0_new[k, l] = M[inv_n[k], inv_m[l]].  fp32 throughout (CUDA cores): the
 // merge runs once per many steps and its error would stay in W0.
 struct MergePlan {
-  size_t Qs, Q2, G, Wf, T, M, inv_m, inv_n, total;
+  size_t Qs, Q2, G, Gt, Wf, T, M, inv_m, inv_n, total;
 };
+
+// Merge-then-reinitialize takes the tensor cores (three-pass tf32 products) where the CNP
+// engine takes the block size, else the CUDA cores.
+static bool merge_on_tensor_cores(const poetx_layer* L) {
+  return use_tensor_cores() && cnp_umma_ok(L->b);
+}
 
 static MergePlan merge_plan(const poetx_layer* L) {
   MergePlan p{};
@@ -267,7 +273,10 @@ static MergePlan merge_plan(const poetx_layer* L) {
   p.Qs = take((m + n) * b * 4);
   p.Q2 = take((m + n) * b * 4);
   p.G = take((m + n) * b * 4);
-  p.Wf = L->wdt == POETX_I8 ? take(n * m * 4) : 0;
+  const bool tc = merge_on_tensor_cores(L);
+  p.Gt = tc ? take((m + n) * b * 4) : 0;
+  // an fp32 copy of W' (int8: dequantised; bf16 for the tensor-core products)
+  p.Wf = (L->wdt == POETX_I8 || (tc && L->wdt == POETX_BF16)) ? take(n * m * 4) : 0;
   p.T = take(n * m * 4);
   p.M = take(n * m * 4);
   p.inv_m = take(m * 4);
@@ -322,39 +331,58 @@ extern "C" poetx_status poetx_merge_reinit(const poetx_layer* L, float* W0_new, 
   const int b = L->b, m = padded(L->m, b), n = padded(L->n, b);  // padded widths
   // G_R (blocks [0, m/b)) and G_P (blocks [m/b, (m+n)/b)) in fp32
   const CnpSides sides = layer_sides(L);
+  const bool tc = merge_on_tensor_cores(L);
   float* G = at<float>(ws, p.G);
+  float* Gt = tc ? at<float>(ws, p.Gt) : nullptr;
   POETX_TRY(cnp_forward_sides(sides, b, at<float>(ws, p.Qs), at<float>(ws, p.Q2), G, nullptr,
-                              nullptr, stream));
+                              nullptr, stream, Gt));
   const float* GR = G;
   const float* GP = G + (size_t)m * b;
-  const void* Wsrc = L->Wp;
-  poetx_dtype wt = L->wdt;
-  if (L->wdt == POETX_I8) {
-    POETX_TRY(launch_dequant_rows(static_cast<const int8_t*>(L->Wp), L->w_scale, n, m,
-                                  at<float>(ws, p.Wf), stream));
-    Wsrc = at<float>(ws, p.Wf);
-    wt = POETX_F32;
-  }
   float* T = at<float>(ws, p.T);
   float* M = at<float>(ws, p.M);
-  SimtGemm g{};
-  // T[:, jb:(j+1)b] = W'[:, jb:(j+1)b] G_R,j^T
-  g.M = n; g.N = b; g.K = b; g.batch = m / b;
-  g.A = Wsrc; g.sam = m; g.sak = 1; g.sab = b;
-  g.B = GR; g.sbk = 1; g.sbn = b; g.sbb = (long long)b * b;
-  g.C = T; g.scm = m; g.scn = 1; g.scb = b;
-  g.ksplit = 1; g.kchunk = b;
-  g.stage = ST_MERGE_REINIT;
-  POETX_TRY(launch_simt_gemm(wt, POETX_F32, POETX_F32, g, stream));
-  // M[jb:(j+1)b, :] = G_P,j^T T[jb:(j+1)b, :]
-  g = SimtGemm{};
-  g.M = b; g.N = m; g.K = b; g.batch = n / b;
-  g.A = GP; g.sam = 1; g.sak = b; g.sab = (long long)b * b;
-  g.B = T; g.sbk = m; g.sbn = 1; g.sbb = (long long)b * m;
-  g.C = M; g.scm = m; g.scn = 1; g.scb = (long long)b * m;
-  g.ksplit = 1; g.kchunk = b;
-  g.stage = ST_MERGE_REINIT;
-  POETX_TRY(launch_simt_gemm(POETX_F32, POETX_F32, POETX_F32, g, stream));
+  if (tc) {
+    // fp32 W' ([n, m]); T^T = (W' blkdiag(G_R)^T)^T ([m, n]); M = blkdiag(G_P)^T T ([n, m]),
+    // computed as M^T = T^T blkdiag(G_P) with its transposed output
+    const float* Wf = static_cast<const float*>(L->Wp);
+    if (L->wdt == POETX_I8) {
+      POETX_TRY(launch_dequant_rows(static_cast<const int8_t*>(L->Wp), L->w_scale, n, m,
+                                    at<float>(ws, p.Wf), stream));
+      Wf = at<float>(ws, p.Wf);
+    } else if (L->wdt == POETX_BF16) {
+      POETX_TRY(launch_widen_bf16(L->Wp, (long long)n * m, at<float>(ws, p.Wf), stream));
+      Wf = at<float>(ws, p.Wf);
+    }
+    POETX_TRY(matrix_blockmm_tc(Wf, n, m / b, b, GR, nullptr, T, ST_MERGE_REINIT, stream));
+    POETX_TRY(matrix_blockmm_tc(T, m, n / b, b, Gt + (size_t)m * b, nullptr, M, ST_MERGE_REINIT,
+                                stream));
+  } else {
+    const void* Wsrc = L->Wp;
+    poetx_dtype wt = L->wdt;
+    if (L->wdt == POETX_I8) {
+      POETX_TRY(launch_dequant_rows(static_cast<const int8_t*>(L->Wp), L->w_scale, n, m,
+                                    at<float>(ws, p.Wf), stream));
+      Wsrc = at<float>(ws, p.Wf);
+      wt = POETX_F32;
+    }
+    SimtGemm g{};
+    // T[:, jb:(j+1)b] = W'[:, jb:(j+1)b] G_R,j^T
+    g.M = n; g.N = b; g.K = b; g.batch = m / b;
+    g.A = Wsrc; g.sam = m; g.sak = 1; g.sab = b;
+    g.B = GR; g.sbk = 1; g.sbn = b; g.sbb = (long long)b * b;
+    g.C = T; g.scm = m; g.scn = 1; g.scb = b;
+    g.ksplit = 1; g.kchunk = b;
+    g.stage = ST_MERGE_REINIT;
+    POETX_TRY(launch_simt_gemm(wt, POETX_F32, POETX_F32, g, stream));
+    // M[jb:(j+1)b, :] = G_P,j^T T[jb:(j+1)b, :]
+    g = SimtGemm{};
+    g.M = b; g.N = m; g.K = b; g.batch = n / b;
+    g.A = GP; g.sam = 1; g.sak = b; g.sab = (long long)b * b;
+    g.B = T; g.sbk = m; g.sbn = 1; g.sbb = (long long)b * m;
+    g.C = M; g.scm = m; g.scn = 1; g.scb = (long long)b * m;
+    g.ksplit = 1; g.kchunk = b;
+    g.stage = ST_MERGE_REINIT;
+    POETX_TRY(launch_simt_gemm(POETX_F32, POETX_F32, POETX_F32, g, stream));
+  }
   int32_t* inv_m = at<int32_t>(ws, p.inv_m);
   int32_t* inv_n = at<int32_t>(ws, p.inv_n);
   POETX_TRY(launch_invert_perms(L->perm_m, L->m, inv_m, L->perm_n, L->n, inv_n, stream));
