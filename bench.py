@@ -816,10 +816,11 @@ def setup_measure(P, torch, rig, flush, pk, dev):
 
 
 def e2e_measure(P, torch, rig, args, world, dev, flush):
-    """End to end through the C ABI with pinned host buffers: every step, for each layer in
-    turn, one poetx_layer_step_host call (x and dy up, forward, backward, y, dx, dq_R and
-    dq_P down, the copies on the library's copy stream beside the kernels); then, the
-    gradients being in host memory, the exchange and the update run on the host copy."""
+    """End to end through the C ABI with pinned host buffers: every step, one
+    poetx_group_step_host call over the workload's layer group (every x and dy up, the
+    group's forward and backward, every y, dx, dq_R and dq_P down, the copies on the
+    library's upload and download streams beside the kernels), or with --group off one
+    poetx_layer_step_host call per layer."""
     from orthogonal_reparameterized_gb300 import dp
     hb = []
     dev_bytes = 16
@@ -830,12 +831,19 @@ def e2e_measure(P, torch, rig, args, world, dev, flush):
                        dqR=torch.empty(d["dqR"].shape).pin_memory(),
                        dqP=torch.empty(d["dqP"].shape).pin_memory()))
         dev_bytes = max(dev_bytes, P.poetx_layer_step_host_bytes(d["L"], rig.N))
+    if rig.group:
+        dev_bytes = P.poetx_group_step_host_bytes(rig.G, rig.N)
     step_dev = P.workspace(dev_bytes, dev)
     h2d = sum((h["x"].numel() + h["dy"].numel()) * rig.esz for h in hb)
     d2h = sum((h["y"].numel() + h["dx"].numel()) * rig.esz + (h["dqR"].numel() +
               h["dqP"].numel()) * 4 for h in hb)
 
     def step():
+        if rig.group:
+            P.poetx_group_step_host(rig.G, [h["x"] for h in hb], [h["dy"] for h in hb],
+                                    [h["y"] for h in hb], [h["dx"] for h in hb],
+                                    [h["dqR"] for h in hb], [h["dqP"] for h in hb], step_dev)
+            return
         for d, h in zip(rig.layers, hb):
             P.poetx_layer_step_host(d["L"], h["x"], h["dy"], h["y"], h["dx"], h["dqR"],
                                     h["dqP"], step_dev)
@@ -872,18 +880,40 @@ def e2e_measure(P, torch, rig, args, world, dev, flush):
             if i >= 3:
                 ts.append(c0.elapsed_time(c1))
         link[kind + "_gbs"] = round(nb / (statistics.median(ts) * 1e-3) / 1e9, 1)
-    del hbuf, dbuf
+    # both directions at once (an upload and a download on two streams)
+    hbuf2 = torch.empty(nb, dtype=torch.uint8).pin_memory()
+    dbuf2 = torch.empty(nb, dtype=torch.uint8, device=dev)
+    su, sd = torch.cuda.Stream(), torch.cuda.Stream()
+    ts = []
+    for i in range(8):
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        c0.record()
+        su.wait_stream(torch.cuda.current_stream())
+        sd.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(su):
+            dbuf.copy_(hbuf, non_blocking=True)
+        with torch.cuda.stream(sd):
+            hbuf2.copy_(dbuf2, non_blocking=True)
+        torch.cuda.current_stream().wait_stream(su)
+        torch.cuda.current_stream().wait_stream(sd)
+        c1.record()
+        torch.cuda.synchronize()
+        if i >= 3:
+            ts.append(c0.elapsed_time(c1))
+    link["both_directions_gbs"] = round(2 * nb / (statistics.median(ts) * 1e-3) / 1e9, 1)
+    del hbuf, dbuf, hbuf2, dbuf2
     t = statistics.mean(ms)
     return {"unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "ms_per_step": t,
             "link": {**link, "traffic_gbs": (h2d + d2h) / (t * 1e-3) / 1e9,
-                     "note": "one pinned copy of up to 1 GiB alone, each direction; the step "
-                             "moves h2d + d2h bytes"},
-            "note": "per step, one poetx_layer_step_host call per layer (pinned host buffers): "
-                    "x and dy up, forward, backward, y, dx, dq_R and dq_P down; the library's "
-                    "copy stream overlaps the uploads and downloads with the kernels; bound "
-                    "by the host link when the step's bytes / link rate exceed the kernels' "
-                    "time"}
+                     "note": "one pinned copy of up to 1 GiB alone in each direction, and one "
+                             "each way at once; the step moves h2d + d2h bytes"},
+            "note": ("per step, one poetx_group_step_host call over the layer group"
+                     if rig.group else "per step, one poetx_layer_step_host call per layer") +
+                    " (pinned host buffers): x and dy up, forward, backward, y, dx, dq_R and "
+                    "dq_P down; the library's upload and download streams overlap the copies "
+                    "with the kernels and with each other; bound by the host link when the "
+                    "step's bytes / link rate exceed the kernels' time"}
 
 
 def extra_measure(P, torch, wl, dev, flush, pk, graph_of, timed, steps=30):

@@ -377,16 +377,34 @@ poetx_status poetx_group_cnp_bwd(const poetx_layer* Ls, int count, int N, const 
  * under stream capture they fail (POETX_ERR_CUDA).  dev: device scratch of at least
  * poetx_layer_step_host_bytes(L, N) bytes (16-byte aligned; 0 for an invalid descriptor),
  * holding the device copies of the six arrays, the forward's saved state and the workspace;
- * the library allocates nothing.  The uploads and downloads of x, dy, y and dx run on a
- * copy stream the library creates once per device; the x upload overlaps the CNP forward,
- * dy's the forward chain, y's download the backward and dx's the CNP backward.  When the
- * call's work on `stream` completes, every output is in host memory (synchronise `stream`
- * before reading them).  Calls from several host threads are serialised while they enqueue.
+ * the library allocates nothing.  The uploads (x, dy) and the downloads (y, dx, dq) run on
+ * an upload and a download stream the library creates once per device, so that the two
+ * directions of the host link are used at once; the x upload overlaps the CNP forward, dy's
+ * the forward chain, y's download the backward and dx's the CNP backward.  When the call's
+ * work on `stream` completes, every output is in host memory (synchronise `stream` before
+ * reading them).  Calls from several host threads are serialised while they enqueue.
  * Errors: those of poetx_layer_fwd / poetx_layer_bwd, checked before any transfer. */
 size_t poetx_layer_step_host_bytes(const poetx_layer* L, int N);
 poetx_status poetx_layer_step_host(const poetx_layer* L, const void* x, const void* dy, int N,
                                    void* y, void* dx, float* dq_R, float* dq_P, void* dev,
                                    size_t dev_bytes, cudaStream_t stream);
+
+/* One training step of a layer group with HOST buffers (as poetx_group_cnp_fwd, every
+ * poetx_group_layer_fwd in order 0 .. count-1, every poetx_group_layer_bwd in reverse order
+ * and poetx_group_cnp_bwd with accumulate = 0): x[i] [N, m_i], dy[i] [N, n_i] are host
+ * inputs, y[i] [N, n_i], dx[i] [N, m_i], dq_R[i], dq_P[i] host outputs (HOST arrays of
+ * `count` host pointers each).  The uploads go in the order the kernels need them (every x,
+ * then every dy from the last layer to the first) and each output comes down as soon as it
+ * is written, beside the kernels, on the upload and download streams of
+ * poetx_layer_step_host.  dev: device scratch of at least poetx_group_step_host_bytes(Ls,
+ * count, N) bytes (16-byte aligned; 0 for an invalid group) holding every layer's device
+ * arrays, the group's saved state and its workspace.  Page-locked host buffers, completion
+ * and errors as for poetx_layer_step_host and the group calls. */
+size_t poetx_group_step_host_bytes(const poetx_layer* Ls, int count, int N);
+poetx_status poetx_group_step_host(const poetx_layer* Ls, int count, const void* const* x,
+                                   const void* const* dy, int N, void* const* y,
+                                   void* const* dx, float* const* dq_R, float* const* dq_P,
+                                   void* dev, size_t dev_bytes, cudaStream_t stream);
 
 /* Merge-then-reinitialize (POET skill page, Step 4 "Merge-Then-Reinitialize Optimization":
  * the current R W0 P is written back into W0 and the factors are reset to the identity).

@@ -884,10 +884,12 @@ extern "C" poetx_status poetx_group_cnp_bwd(const poetx_layer* Ls, int count, in
 }
 
 // ---------------------------------------------------------------- host-buffer step
-// One forward + backward with the caller's host buffers: the uploads and downloads run on a
-// copy stream of the library's own, beside the kernels on the caller's stream:
-//   copy stream   x up | dy up |           | y down (after the forward) | dx down |
-//   caller stream CNP fwd | (wait x) fwd chain | (wait dy) bwd chain | CNP bwd | dq down
+// One forward + backward with the caller's host buffers: the uploads and the downloads run
+// on two copy streams of the library's own (the host link carries both directions at once),
+// beside the kernels on the caller's stream:
+//   upload stream    x up | dy up |
+//   download stream               | y down (after the forward) | dx down | dq down
+//   caller stream    CNP fwd | (wait x) fwd chain | (wait dy) bwd chain | CNP bwd
 // so the CNP forward hides part of the x upload, the dy upload runs under the forward, the
 // y download under the backward and the dx download under the CNP backward.
 struct StepPlan {
@@ -915,15 +917,48 @@ static StepPlan step_plan(const poetx_layer* L, long long N) {
 }
 
 namespace {
-enum { EV_START, EV_X, EV_DY, EV_Y, EV_DX, EV_DONE, EV_COUNT };
+enum { EV_START, EV_X, EV_DY, EV_Y, EV_DX, EV_DQ, EV_UP, EV_DONE, EV_COUNT };
+// per layer of a group step: x uploaded, dy uploaded, y computed, dx computed
+enum { GEV_X, GEV_DY, GEV_Y, GEV_DX, GEV_COUNT };
 struct CopyCtx {
   bool ready = false;
-  cudaStream_t cs = nullptr;
+  cudaStream_t us = nullptr, ds = nullptr;  // uploads, downloads
   cudaEvent_t ev[EV_COUNT] = {};
+  cudaEvent_t gev[GEV_COUNT][POETX_GROUP_MAX_LAYERS] = {};
 };
 std::mutex g_step_mu;  // the events are reused: one step is enqueued at a time
 CopyCtx g_copy[64];    // per device
+
+// The device's copy streams and events, created on first use (under g_step_mu).
+poetx_status copy_ctx(CopyCtx** out) {
+  int d = 0;
+  POETX_CUDA_TRY(cudaGetDevice(&d));
+  if (d < 0 || d >= 64) return POETX_ERR_UNSUPPORTED;
+  CopyCtx& c = g_copy[d];
+  if (!c.ready) {
+    POETX_CUDA_TRY(cudaStreamCreateWithFlags(&c.us, cudaStreamNonBlocking));
+    POETX_CUDA_TRY(cudaStreamCreateWithFlags(&c.ds, cudaStreamNonBlocking));
+    for (int i = 0; i < EV_COUNT; ++i)
+      POETX_CUDA_TRY(cudaEventCreateWithFlags(&c.ev[i], cudaEventDisableTiming));
+    for (int k = 0; k < GEV_COUNT; ++k)
+      for (int i = 0; i < POETX_GROUP_MAX_LAYERS; ++i)
+        POETX_CUDA_TRY(cudaEventCreateWithFlags(&c.gev[k][i], cudaEventDisableTiming));
+    c.ready = true;
+  }
+  *out = &c;
+  return POETX_OK;
+}
 }  // namespace
+
+// The caller's stream waits for both copy streams (also after an error, so that nothing the
+// streams still do is left unordered with the caller's later work).
+static void join_copy_streams(CopyCtx& c, cudaStream_t stream, poetx_status& st) {
+  const cudaError_t e1 = cudaEventRecord(c.ev[EV_UP], c.us);
+  const cudaError_t e2 = cudaEventRecord(c.ev[EV_DONE], c.ds);
+  const cudaError_t e3 = e1 == cudaSuccess ? cudaStreamWaitEvent(stream, c.ev[EV_UP], 0) : e1;
+  const cudaError_t e4 = e2 == cudaSuccess ? cudaStreamWaitEvent(stream, c.ev[EV_DONE], 0) : e2;
+  if (st == POETX_OK && (e3 != cudaSuccess || e4 != cudaSuccess)) st = POETX_ERR_CUDA;
+}
 
 extern "C" size_t poetx_layer_step_host_bytes(const poetx_layer* L, int N) {
   if (validate(L) != POETX_OK || N < 0) return 0;
@@ -939,36 +974,30 @@ extern "C" poetx_status poetx_layer_step_host(const poetx_layer* L, const void* 
   if (!aligned16(dev)) return POETX_ERR_ALIGN;
   const StepPlan sp = step_plan(L, N);
   if (dev_bytes < sp.total) return POETX_ERR_WORKSPACE;
-  int d = 0;
-  POETX_CUDA_TRY(cudaGetDevice(&d));
-  if (d < 0 || d >= 64) return POETX_ERR_UNSUPPORTED;
   std::lock_guard<std::mutex> lk(g_step_mu);
-  CopyCtx& c = g_copy[d];
-  if (!c.ready) {
-    POETX_CUDA_TRY(cudaStreamCreateWithFlags(&c.cs, cudaStreamNonBlocking));
-    for (int i = 0; i < EV_COUNT; ++i)
-      POETX_CUDA_TRY(cudaEventCreateWithFlags(&c.ev[i], cudaEventDisableTiming));
-    c.ready = true;
-  }
+  CopyCtx* cp = nullptr;
+  POETX_TRY(copy_ctx(&cp));
+  CopyCtx& c = *cp;
   uint8_t* base = static_cast<uint8_t*>(dev);
   const size_t as = dtype_size(L->act);
   const size_t m = L->m, n = L->n, b = L->b;
   const size_t xb = (size_t)N * m * as, yb = (size_t)N * n * as;
   const size_t qRb = (m + b - 1) / b * (b * (b - 1) / 2) * 4;
   const size_t qPb = (n + b - 1) / b * (b * (b - 1) / 2) * 4;
-  // the copy stream starts after the caller's earlier work (which may still use `dev`)
+  // the copy streams start after the caller's earlier work (which may still use `dev`)
   POETX_CUDA_TRY(cudaEventRecord(c.ev[EV_START], stream));
-  POETX_CUDA_TRY(cudaStreamWaitEvent(c.cs, c.ev[EV_START], 0));
+  POETX_CUDA_TRY(cudaStreamWaitEvent(c.us, c.ev[EV_START], 0));
+  POETX_CUDA_TRY(cudaStreamWaitEvent(c.ds, c.ev[EV_START], 0));
   StepHooks fh, bh;
   poetx_status st = POETX_OK;
   auto cuda = [&](cudaError_t e) {
     if (st == POETX_OK && e != cudaSuccess) st = POETX_ERR_CUDA;
   };
   if (N > 0) {
-    cuda(cudaMemcpyAsync(base + sp.x, x, xb, cudaMemcpyHostToDevice, c.cs));
-    cuda(cudaEventRecord(c.ev[EV_X], c.cs));
-    cuda(cudaMemcpyAsync(base + sp.dy, dy, yb, cudaMemcpyHostToDevice, c.cs));
-    cuda(cudaEventRecord(c.ev[EV_DY], c.cs));
+    cuda(cudaMemcpyAsync(base + sp.x, x, xb, cudaMemcpyHostToDevice, c.us));
+    cuda(cudaEventRecord(c.ev[EV_X], c.us));
+    cuda(cudaMemcpyAsync(base + sp.dy, dy, yb, cudaMemcpyHostToDevice, c.us));
+    cuda(cudaEventRecord(c.ev[EV_DY], c.us));
     fh.x_ready = c.ev[EV_X];
     bh.dy_ready = c.ev[EV_DY];
     bh.dx_done = c.ev[EV_DX];
@@ -978,8 +1007,8 @@ extern "C" poetx_status poetx_layer_step_host(const poetx_layer* L, const void* 
                         sp.ws_bytes, stream, fh);
   if (st == POETX_OK && N > 0) {
     cuda(cudaEventRecord(c.ev[EV_Y], stream));
-    cuda(cudaStreamWaitEvent(c.cs, c.ev[EV_Y], 0));
-    cuda(cudaMemcpyAsync(y, base + sp.y, yb, cudaMemcpyDeviceToHost, c.cs));
+    cuda(cudaStreamWaitEvent(c.ds, c.ev[EV_Y], 0));
+    cuda(cudaMemcpyAsync(y, base + sp.y, yb, cudaMemcpyDeviceToHost, c.ds));
   }
   if (st == POETX_OK)
     st = layer_bwd_impl(L, base + sp.x, base + sp.dy, N, base + sp.saved, base + sp.dx,
@@ -987,17 +1016,157 @@ extern "C" poetx_status poetx_layer_step_host(const poetx_layer* L, const void* 
                         reinterpret_cast<float*>(base + sp.dqP), 0, base + sp.ws, sp.ws_bytes,
                         stream, bh);
   if (st == POETX_OK && N > 0) {
-    cuda(cudaStreamWaitEvent(c.cs, c.ev[EV_DX], 0));
-    cuda(cudaMemcpyAsync(dx, base + sp.dx, xb, cudaMemcpyDeviceToHost, c.cs));
+    cuda(cudaStreamWaitEvent(c.ds, c.ev[EV_DX], 0));
+    cuda(cudaMemcpyAsync(dx, base + sp.dx, xb, cudaMemcpyDeviceToHost, c.ds));
   }
   if (st == POETX_OK) {
-    cuda(cudaMemcpyAsync(dq_R, base + sp.dqR, qRb, cudaMemcpyDeviceToHost, stream));
-    cuda(cudaMemcpyAsync(dq_P, base + sp.dqP, qPb, cudaMemcpyDeviceToHost, stream));
+    cuda(cudaEventRecord(c.ev[EV_DQ], stream));
+    cuda(cudaStreamWaitEvent(c.ds, c.ev[EV_DQ], 0));
+    cuda(cudaMemcpyAsync(dq_R, base + sp.dqR, qRb, cudaMemcpyDeviceToHost, c.ds));
+    cuda(cudaMemcpyAsync(dq_P, base + sp.dqP, qPb, cudaMemcpyDeviceToHost, c.ds));
   }
-  // the caller's stream is done with the step only when the copy stream is
-  const cudaError_t e1 = cudaEventRecord(c.ev[EV_DONE], c.cs);
-  const cudaError_t e2 = e1 == cudaSuccess ? cudaStreamWaitEvent(stream, c.ev[EV_DONE], 0) : e1;
-  cuda(e2);
+  // the caller's stream is done with the step only when both copy streams are
+  join_copy_streams(c, stream, st);
+  return st;
+}
+
+// ---------------------------------------------------------------- host-buffer group step
+// One training step of a layer group with host buffers: every layer's x and dy go up on the
+// upload stream in the order the kernels need them (x_0 .. x_{c-1}, then dy_{c-1} .. dy_0),
+// every y comes down as soon as its forward chain has written it, every dx as soon as its
+// backward chain has, and the dq of every layer after the group's CNP backward, on the
+// download stream; the kernels run on the caller's stream between them, each chain waiting
+// only for its own inputs.
+struct GroupStepPlan {
+  size_t x[kMaxGroup], dy[kMaxGroup], y[kMaxGroup], dx[kMaxGroup], dqR[kMaxGroup],
+      dqP[kMaxGroup];
+  size_t saved, ws, ws_bytes, total;
+};
+
+static GroupStepPlan group_step_plan(const poetx_layer* Ls, int count, long long N) {
+  GroupStepPlan sp{};
+  size_t o = 0;
+  auto take = [&](size_t bytes) { size_t r = o; o += align_up(bytes, 256); return r; };
+  for (int i = 0; i < count; ++i) {
+    const size_t as = dtype_size(Ls[i].act), m = Ls[i].m, n = Ls[i].n, b = Ls[i].b;
+    sp.x[i] = take(N * m * as);
+    sp.dy[i] = take(N * n * as);
+    sp.y[i] = take(N * n * as);
+    sp.dx[i] = take(N * m * as);
+    sp.dqR[i] = take((m + b - 1) / b * (b * (b - 1) / 2) * 4);
+    sp.dqP[i] = take((n + b - 1) / b * (b * (b - 1) / 2) * 4);
+  }
+  const GroupPlan g = group_plan(Ls, count, N);
+  sp.saved = take(g.saved_total);
+  sp.ws_bytes = g.ws_total;
+  sp.ws = take(sp.ws_bytes);
+  sp.total = o;
+  return sp;
+}
+
+extern "C" size_t poetx_group_step_host_bytes(const poetx_layer* Ls, int count, int N) {
+  if (validate_group(Ls, count) != POETX_OK || N < 0) return 0;
+  return group_step_plan(Ls, count, N).total;
+}
+
+extern "C" poetx_status poetx_group_step_host(const poetx_layer* Ls, int count,
+                                              const void* const* x, const void* const* dy, int N,
+                                              void* const* y, void* const* dx,
+                                              float* const* dq_R, float* const* dq_P, void* dev,
+                                              size_t dev_bytes, cudaStream_t stream) {
+  POETX_TRY(validate_group(Ls, count));
+  if (N < 0 || !dev || !dq_R || !dq_P) return POETX_ERR_ARG;
+  if (N > 0 && (!x || !dy || !y || !dx)) return POETX_ERR_ARG;
+  for (int i = 0; i < count; ++i) {
+    if (!dq_R[i] || !dq_P[i]) return POETX_ERR_ARG;
+    if (N > 0 && (!x[i] || !dy[i] || !y[i] || !dx[i])) return POETX_ERR_ARG;
+  }
+  if (!aligned16(dev)) return POETX_ERR_ALIGN;
+  const GroupStepPlan sp = group_step_plan(Ls, count, N);
+  if (dev_bytes < sp.total) return POETX_ERR_WORKSPACE;
+  const GroupPlan g = group_plan(Ls, count, N);
+  std::lock_guard<std::mutex> lk(g_step_mu);
+  CopyCtx* cp = nullptr;
+  POETX_TRY(copy_ctx(&cp));
+  CopyCtx& c = *cp;
+  uint8_t* base = static_cast<uint8_t*>(dev);
+  void* saved = base + sp.saved;
+  void* ws = base + sp.ws;
+  POETX_CUDA_TRY(cudaEventRecord(c.ev[EV_START], stream));
+  POETX_CUDA_TRY(cudaStreamWaitEvent(c.us, c.ev[EV_START], 0));
+  POETX_CUDA_TRY(cudaStreamWaitEvent(c.ds, c.ev[EV_START], 0));
+  poetx_status st = POETX_OK;
+  auto cuda = [&](cudaError_t e) {
+    if (st == POETX_OK && e != cudaSuccess) st = POETX_ERR_CUDA;
+  };
+  auto abytes = [&](int i, bool in) {
+    return (size_t)N * (in ? Ls[i].m : Ls[i].n) * dtype_size(Ls[i].act);
+  };
+  if (N > 0) {
+    for (int i = 0; i < count; ++i) {
+      cuda(cudaMemcpyAsync(base + sp.x[i], x[i], abytes(i, true), cudaMemcpyHostToDevice, c.us));
+      cuda(cudaEventRecord(c.gev[GEV_X][i], c.us));
+    }
+    for (int i = count - 1; i >= 0; --i) {
+      cuda(cudaMemcpyAsync(base + sp.dy[i], dy[i], abytes(i, false), cudaMemcpyHostToDevice,
+                           c.us));
+      cuda(cudaEventRecord(c.gev[GEV_DY][i], c.us));
+    }
+  }
+  const bool f32 = Ls[0].act == POETX_F32;
+  if (st == POETX_OK) {
+    prof_begin(stream);
+    st = cnp_forward_sides(group_sides(Ls, count), Ls[0].b, at<float>(saved, g.Qs),
+                           at<float>(saved, g.Q2), f32 ? at<float>(saved, g.G) : nullptr,
+                           f32 ? nullptr : at(saved, g.G), nullptr, stream);
+  }
+  for (int i = 0; i < count && st == POETX_OK && N > 0; ++i) {
+    StepHooks h;
+    h.x_ready = c.gev[GEV_X][i];
+    st = chain_fwd(&Ls[i], g.lp[i], base + sp.x[i], N, base + sp.y[i],
+                   group_chain_saved(Ls, g, i, saved), at(ws, g.chain), stream, h);
+    if (st != POETX_OK) break;
+    cuda(cudaEventRecord(c.gev[GEV_Y][i], stream));
+    cuda(cudaStreamWaitEvent(c.ds, c.gev[GEV_Y][i], 0));
+    cuda(cudaMemcpyAsync(y[i], base + sp.y[i], abytes(i, false), cudaMemcpyDeviceToHost, c.ds));
+  }
+  for (int i = count - 1; i >= 0 && st == POETX_OK; --i) {
+    StepHooks h;
+    h.dy_ready = N > 0 ? c.gev[GEV_DY][i] : nullptr;
+    h.dx_done = N > 0 ? c.gev[GEV_DX][i] : nullptr;
+    st = chain_bwd(&Ls[i], g.lp[i], base + sp.x[i], base + sp.dy[i], N,
+                   group_chain_saved(Ls, g, i, saved), base + sp.dx[i],
+                   at<float>(ws, g.dGR[i]), at<float>(ws, g.dGP[i]), at(ws, g.chain), stream, h,
+                   nullptr);
+    if (st != POETX_OK || N == 0) continue;
+    cuda(cudaStreamWaitEvent(c.ds, c.gev[GEV_DX][i], 0));
+    cuda(cudaMemcpyAsync(dx[i], base + sp.dx[i], abytes(i, true), cudaMemcpyDeviceToHost, c.ds));
+  }
+  if (st == POETX_OK) {
+    CnpGrads gr;
+    for (int i = 0; i < count; ++i) {
+      gr.dG[2 * i] = at<float>(ws, g.dGR[i]);
+      gr.splits[2 * i] = g.lp[i].splitsR;
+      gr.dq[2 * i] = reinterpret_cast<float*>(base + sp.dqR[i]);
+      gr.dG[2 * i + 1] = at<float>(ws, g.dGP[i]);
+      gr.splits[2 * i + 1] = g.lp[i].splitsP;
+      gr.dq[2 * i + 1] = reinterpret_cast<float*>(base + sp.dqP[i]);
+    }
+    st = cnp_backward_sides(group_sides(Ls, count), at<float>(saved, g.Qs),
+                            at<float>(saved, g.Q2), gr, Ls[0].b, 0, at(ws, g.cnp), stream);
+  }
+  if (st == POETX_OK) {
+    cuda(cudaEventRecord(c.ev[EV_DQ], stream));
+    cuda(cudaStreamWaitEvent(c.ds, c.ev[EV_DQ], 0));
+    for (int i = 0; i < count; ++i) {
+      const size_t b = Ls[i].b, tri = b * (b - 1) / 2;
+      cuda(cudaMemcpyAsync(dq_R[i], base + sp.dqR[i], (Ls[i].m + b - 1) / b * tri * 4,
+                           cudaMemcpyDeviceToHost, c.ds));
+      cuda(cudaMemcpyAsync(dq_P[i], base + sp.dqP[i], (Ls[i].n + b - 1) / b * tri * 4,
+                           cudaMemcpyDeviceToHost, c.ds));
+    }
+  }
+  join_copy_streams(c, stream, st);
   return st;
 }
 

@@ -96,6 +96,10 @@ _SIGS = {
     "poetx_group_cnp_bwd": (_i, [ctypes.POINTER(LayerDesc), _i, _i, _vp,
                                  ctypes.POINTER(ctypes.c_void_p), ctypes.POINTER(ctypes.c_void_p),
                                  _i, _vp, _sz, _vp]),
+    "poetx_group_step_host_bytes": (_sz, [ctypes.POINTER(LayerDesc), _i, _i]),
+    "poetx_group_step_host": (_i, [ctypes.POINTER(LayerDesc), _i] +
+                              [ctypes.POINTER(ctypes.c_void_p)] * 2 + [_i] +
+                              [ctypes.POINTER(ctypes.c_void_p)] * 4 + [_vp, _sz, _vp]),
 }
 
 _lib: Optional[ctypes.CDLL] = None
@@ -443,3 +447,27 @@ def poetx_group_cnp_bwd(G, N: int, saved, dq_R, dq_P, ws, accumulate=False, stre
     _check("poetx_group_cnp_bwd", lib().poetx_group_cnp_bwd(
         G, len(G), N, _p(saved), pr, pp, int(bool(accumulate)), _p(ws), ws.numel(),
         _stream(stream)))
+
+
+def poetx_group_step_host_bytes(G, N: int) -> int:
+    return lib().poetx_group_step_host_bytes(G, len(G), N)
+
+
+def poetx_group_step_host(G, xs, dys, ys, dxs, dq_R, dq_P, dev, stream=None):
+    """One training step of the group with host (CPU, preferably pinned) tensors: xs, dys in,
+    ys, dxs, dq_R, dq_P out (one per layer); dev: device scratch of
+    poetx_group_step_host_bytes(G, N) bytes.  The outputs are valid once `stream` has been
+    synchronised."""
+    k = len(G)
+    lists = (xs, dys, ys, dxs, dq_R, dq_P)
+    if any(len(t) != k for t in lists):
+        raise ValueError("poetx_group_step_host: one tensor per layer in every list")
+    for ts in lists:
+        for t in ts:
+            if t.is_cuda or not t.is_contiguous():
+                raise ValueError("poetx_group_step_host takes contiguous host tensors")
+    N = xs[0].shape[0]
+    arr = lambda ts: (ctypes.c_void_p * k)(*[t.data_ptr() for t in ts])
+    _check("poetx_group_step_host", lib().poetx_group_step_host(
+        G, k, arr(xs), arr(dys), N, arr(ys), arr(dxs), arr(dq_R), arr(dq_P), _p(dev),
+        dev.numel() * dev.element_size(), _stream(stream)))

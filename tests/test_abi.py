@@ -229,3 +229,17 @@ def test_group_sizes_host_logic(P):
                                      N) == 0                                 # mixed act
     assert P.poetx_group_saved_bytes(P.make_group([a] * 17), N) == 0         # > 16 layers
     assert P.poetx_group_saved_bytes(P.make_group([a] * 16), N) > 0
+
+
+def test_group_step_host_sizes_host_logic(P):
+    a, b = _desc(P), _desc(P, m=512, n=256)
+    G = P.make_group([a, b])
+    N = 100
+    host = P.poetx_group_step_host_bytes(G, N)
+    # every layer's x, dy, y, dx and dq on the device, plus the group's saved state and workspace
+    arrays = 0
+    for d in (a, b):
+        arrays += 2 * N * (d.m + d.n) * 2 + (d.m // d.b + d.n // d.b) * (d.b * (d.b - 1) // 2) * 4
+    assert host >= arrays + P.poetx_group_saved_bytes(G, N) + P.poetx_group_workspace_bytes(G, N)
+    assert P.poetx_group_step_host_bytes(P.make_group([a, _desc(P, b=128)]), N) == 0
+    assert P.poetx_group_step_host_bytes(G, -1) == 0

@@ -169,3 +169,40 @@ def test_group_argument_errors(P):
     other = _build(P, [(256, 256, "bf16", "fast")], 64, "bf16", 8, seed=6)
     mixed = P.make_group([layers[0]["L"], other[0]["L"]])  # two block sizes
     assert P.poetx_group_saved_bytes(mixed, 8) == 0
+
+
+@pytest.mark.parametrize("name", ["mixed_b128", "ragged_b128"])
+def test_group_step_host_equals_device_calls(P, name):
+    """The host-buffer group step (uploads and downloads beside the kernels) gives the same
+    bits as the device group calls, and N = 0 gives zero gradients."""
+    spec, b, N = GROUPS[name]
+    layers = _build(P, spec, b, "bf16", N, seed=700 + b)
+    ref = _run_group(P, layers, N, "bf16")
+    G = P.make_group([d["L"] for d in layers])
+    pin = lambda t: t.detach().cpu().contiguous().pin_memory()
+    xs = [pin(d["x"]) for d in layers]
+    dys = [pin(d["dy"]) for d in layers]
+    ys = [torch.empty(N, d["n"], dtype=torch.bfloat16).pin_memory() for d in layers]
+    dxs = [torch.empty(N, d["m"], dtype=torch.bfloat16).pin_memory() for d in layers]
+    dqR = [torch.full(tuple(d["qR"].shape), float("nan")).pin_memory() for d in layers]
+    dqP = [torch.full(tuple(d["qP"].shape), float("nan")).pin_memory() for d in layers]
+    dev = P.workspace(P.poetx_group_step_host_bytes(G, N), DEV)
+    for _ in range(2):  # a repeated step gives the same bits
+        P.poetx_group_step_host(G, xs, dys, ys, dxs, dqR, dqP, dev)
+        torch.cuda.synchronize()
+        assert P.poetx_get_device_error() == 0
+        for i in range(len(layers)):
+            np.testing.assert_array_equal(ys[i].float().numpy(), ref[i]["y"], err_msg=f"y {i}")
+            np.testing.assert_array_equal(dxs[i].float().numpy(), ref[i]["dx"], err_msg=f"dx {i}")
+            np.testing.assert_array_equal(dqR[i].numpy(), ref[i]["dq_R"], err_msg=f"dq_R {i}")
+            np.testing.assert_array_equal(dqP[i].numpy(), ref[i]["dq_P"], err_msg=f"dq_P {i}")
+    empty = _build(P, spec, b, "bf16", 0, seed=701)
+    G0 = P.make_group([d["L"] for d in empty])
+    z = lambda shape, dt=torch.bfloat16: torch.empty(shape, dtype=dt).pin_memory()
+    dqR0 = [torch.full(tuple(d["qR"].shape), float("nan")).pin_memory() for d in empty]
+    dqP0 = [torch.full(tuple(d["qP"].shape), float("nan")).pin_memory() for d in empty]
+    P.poetx_group_step_host(G0, [z((0, d["m"])) for d in empty], [z((0, d["n"])) for d in empty],
+                            [z((0, d["n"])) for d in empty], [z((0, d["m"])) for d in empty],
+                            dqR0, dqP0, P.workspace(P.poetx_group_step_host_bytes(G0, 0), DEV))
+    torch.cuda.synchronize()
+    assert all(not np.any(t.numpy()) for t in dqR0 + dqP0)
