@@ -1353,7 +1353,9 @@ poetx_status umma_blockdiag(const void* X, long long N, int nblk, int b, const v
                             cudaStream_t s) {
   if (N == 0 || nblk == 0) return POETX_OK;
   const int D = nblk * b;
-  const int BN = b < 128 ? b : 128;  // narrow tiles, deep ring: this product is HBM bound
+  // b = 256 with a plain output: 256-wide tiles (each activation tile read once, the whole
+  // G block resident); otherwise at most 128 wide with a deeper ring
+  const int BN = b < 128 ? b : (b == 256 && !out_perm ? 256 : 128);
   CUtensorMap ta, tb;
   if (!make_map(&ta, X, D, N, D, 64, 128)) return POETX_ERR_CUDA;
   if (trans) {
@@ -1374,20 +1376,20 @@ poetx_status umma_blockdiag(const void* X, long long N, int nblk, int b, const v
   p.bpre_bytes = (unsigned long long)nblk * b * b * 2;
   const int tm = (int)((N + BM - 1) / BM), tn = b / BN;
   // resident G panel of b/64 K blocks; the ring carries only the activation tiles; with
-  // 128-wide tiles and a plain output the epilogue stores by TMA
+  // tiles of 128 columns or more and a plain output the epilogue stores by TMA
   CUtensorMap tc;
-  if (BN == 128 && !out_perm) {
+  if (BN >= 128 && !out_perm) {
     if (!make_map(&tc, Y, D, N, D, 64, 32)) return POETX_ERR_CUDA;
     if (trans) {
       switch (b) {
         case 128: return launch<128, 10, false, false, false, 2, 1, true>(ta, tb, p, tm, tn, nblk, s, &tc);
-        case 256: return launch<128, 8, false, false, false, 4, 1, true>(ta, tb, p, tm, tn, nblk, s, &tc);
+        case 256: return launch<256, 4, false, false, false, 4, 1, true>(ta, tb, p, tm, tn, nblk, s, &tc);
         default: return launch<128, 4, false, false, false, 8, 1, true>(ta, tb, p, tm, tn, nblk, s, &tc);
       }
     }
     switch (b) {
       case 128: return launch<128, 10, false, true, false, 2, 1, true>(ta, tb, p, tm, tn, nblk, s, &tc);
-      case 256: return launch<128, 8, false, true, false, 4, 1, true>(ta, tb, p, tm, tn, nblk, s, &tc);
+      case 256: return launch<256, 4, false, true, false, 4, 1, true>(ta, tb, p, tm, tn, nblk, s, &tc);
       default: return launch<128, 4, false, true, false, 8, 1, true>(ta, tb, p, tm, tn, nblk, s, &tc);
     }
   }
