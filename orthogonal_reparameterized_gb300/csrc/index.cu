@@ -453,7 +453,20 @@ __global__ void __launch_bounds__((kPermWarps + 1) * 32) perm_rows_kernel(
 // even that fits.  (Measured on 2048-wide bf16 rows: two-warp groups match one-warp groups at
 // 4096 rows and stream ~10 % faster from 8192 rows up; wider groups are slower.)
 static bool perm_shape(size_t row_bytes, size_t idx_bytes, int* G, int* S, size_t* smem) {
-  const size_t budget2 = 110 * 1024, budget1 = 220 * 1024;
+  const size_t budget3 = 74 * 1024, budget2 = 110 * 1024, budget1 = 220 * 1024;
+  // three CTAs per SM (more consumer warps to cover the shared-memory read latency) while
+  // two-warp groups still get two rows in flight each
+  {
+    const size_t ngrp = kPermWarps / 2;
+    if (idx_bytes + ngrp * 2 * (row_bytes + 16) <= budget3) {
+      int s = (int)((budget3 - idx_bytes) / (ngrp * (row_bytes + 16)));
+      s = s > 8 ? 8 : s;
+      *G = 2;
+      *S = s;
+      *smem = idx_bytes + ngrp * s * (row_bytes + 16);
+      return true;
+    }
+  }
   for (int g = 2; g <= kPermWarps; g *= 2) {
     const size_t ngrp = kPermWarps / g;
     if (idx_bytes + ngrp * 2 * (row_bytes + 16) <= budget2) {
@@ -515,7 +528,7 @@ static poetx_status launch_perm_rows_t(const void* X, long long N, int D, const 
   const int ngrp = kPermWarps / G;
   size_t tr_cap = 0;
   unsigned long long* tr = trace_buffer(&tr_cap);
-  const int per_sm = side ? 1 : (smem <= 110 * 1024 ? 2 : 1);
+  const int per_sm = side ? 1 : (smem <= 74 * 1024 ? 3 : (smem <= 110 * 1024 ? 2 : 1));
   const long long want = (long long)sm_count() * per_sm;
   const long long need = (N + ngrp - 1) / ngrp;
   const int grid = (int)(need < want ? need : want);
