@@ -9,7 +9,9 @@
 //   block weight gradients     dG_j = X_j^T dY_j over a token range (S10, S12)
 //
 // Persistent CTAs walk the 128 x BN output tiles (tile t = blockIdx.x, + gridDim.x, ...; the
-// M index varies fastest so that concurrent CTAs share the B operand in L2).  Warp 0 issues
+// M index varies fastest so that concurrent CTAs share the B operand in L2; the W'
+// contraction walks bands of 2048 tokens that way, so that the concurrent CTAs also share a
+// few A row stripes).  Warp 0 issues
 // the TMA loads into a STAGES-deep ring, one thread of warp 1 issues the MMAs (4 x K=16 per
 // 64-wide K block) into one of two TMEM accumulators (alternate tiles), and warps 2-9 read
 // the other accumulator back (tcgen05.ld 32x32b: warp w reads lanes 32*(w%4)..+31 = output
@@ -41,6 +43,7 @@ struct UmmaParams {
   int mode;
   int tiles_m, tiles_n, num_tiles;  // tile t: mt = t % tiles_m, nt = (t / tiles_m) % tiles_n,
                                     // z = t / (tiles_m * tiles_n) (block, or block*splits+split)
+  int band_m;    // PLAIN: M tiles per band of the grouped raster (0: plain M-fastest order)
   int M;         // valid output rows of the whole problem (tokens, or b for WGRAD)
   int num_kb;    // 64-wide K blocks per CTA (PLAIN, BLOCKDIAG)
   int b;         // block size (BLOCKDIAG, WGRAD)
@@ -85,10 +88,25 @@ struct TileCoords {
 template <int BN, bool B_MN, int CL>
 __device__ __forceinline__ TileCoords tile_coords(const UmmaParams& p, int t, int crank) {
   TileCoords c;
-  const int mt = CL > 1 ? CL * (t % p.tiles_m) + crank : t % p.tiles_m;
-  const int rest = t / p.tiles_m;
-  const int nt = rest % p.tiles_n;
-  const int z = rest / p.tiles_n;
+  int mi, nt, z;
+  if (p.mode == MODE_PLAIN && p.band_m > 0 && p.band_m < p.tiles_m) {
+    // grouped raster: bands of band_m M tiles, each band's tiles M-fastest across all N
+    // columns, so the tiles in flight at once share a few A row stripes and a few W' stripes
+    // (both re-read from L2 instead of DRAM)
+    const int per_band = p.band_m * p.tiles_n;
+    const int band = t / per_band, r = t % per_band;
+    const int m0 = band * p.band_m;
+    const int gm = p.tiles_m - m0 < p.band_m ? p.tiles_m - m0 : p.band_m;
+    mi = m0 + r % gm;
+    nt = r / gm;
+    z = 0;
+  } else {
+    mi = t % p.tiles_m;
+    const int rest = t / p.tiles_m;
+    nt = rest % p.tiles_n;
+    z = rest / p.tiles_n;
+  }
+  const int mt = CL > 1 ? CL * mi + crank : mi;
   c.num_kb = p.num_kb;
   c.out_row0 = (long long)mt * BM;
   c.out_col0 = (long long)nt * BN;
@@ -1425,6 +1443,8 @@ poetx_status umma_wprime(const void* A, long long N, int m, int n, const void* W
   // number of tile rounds and the single-CTA 128 x 256 tiles start faster.
   const int tm2 = (tm + 1) / 2;
   const bool pairs = umma_wprime_pairs(N, m, n, trans);
+  // grouped raster over bands of 2048 tokens (8 pairs of M tiles, or 16 single ones)
+  p.band_m = pairs ? 8 : 16;
   if (!trans) {  // C[N,n] = A[N,m] W^T
     if (!make_map(&ta, A, m, N, m, 64, 128)) return POETX_ERR_CUDA;
     // (pairs: each CTA loads half of a 256-row W' tile)
