@@ -61,6 +61,7 @@ def _merge(P, L, n, m):
     (1024, 512, 256, "bf16", "bf16"),
     (512, 768, 128, "bf16", "i8"),       # int8 W': the dequantised weight is merged
     (2048, 2048, 256, "bf16", "bf16"),   # the Llama-1B-shaped layer
+    (1024, 1536, 512, "bf16", "bf16"),   # b = 512
 ])
 def test_merge_reinit_matches_oracle(P, m, n, b, act, wdt):
     inp = inputs.small_layer_inputs(500 + m + b, m, n, b, 4, act=act, wdt=wdt)
