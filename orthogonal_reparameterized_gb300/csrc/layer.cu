@@ -16,8 +16,8 @@
 // Ragged last blocks (ceil(d/b) blocks per side) are computed with every internal array
 // padded to whole blocks (see `padded`).  Host-side orchestration only: every step runs in
 // this library's kernels, on the caller's stream except the overlapped dx scatter (a side
-// stream) and the host-buffer step's copies (a copy stream), both forked from and joined
-// back into the caller's stream; no device memory is allocated.
+// stream) and the host-buffer steps' copies (an upload and a download stream), all forked
+// from and joined back into the caller's stream; no device memory is allocated.
 #include <atomic>
 #include <mutex>
 
