@@ -309,11 +309,30 @@ __device__ __forceinline__ bool group_all(bool v, int g, int G) {
 }
 
 constexpr int kPermWarps = 8;  // consumer warps; one more warp issues the row copies
+constexpr int kIdxRound = 4;   // 16-byte index loads in flight per consumer thread
+
+// Stores the four gather indices perm[i0 .. i0 + 3] = v into the staged index (gather: idx[i]
+// = perm[i]; scatter, the inverse: idx[perm[i]] = i).
+template <bool SCATTER, typename IdxT>
+__device__ __forceinline__ void stage_idx4(IdxT* idx, int i0, int4 v) {
+  if (SCATTER) {
+    idx[v.x] = (IdxT)i0;
+    idx[v.y] = (IdxT)(i0 + 1);
+    idx[v.z] = (IdxT)(i0 + 2);
+    idx[v.w] = (IdxT)(i0 + 3);
+  } else if (sizeof(IdxT) == 2) {
+    *reinterpret_cast<uint2*>(idx + i0) =
+        make_uint2(((uint32_t)v.y << 16) | ((uint32_t)v.x & 0xFFFFu),
+                   ((uint32_t)v.w << 16) | ((uint32_t)v.z & 0xFFFFu));
+  } else {
+    *reinterpret_cast<int4*>(idx + i0) = v;
+  }
+}
 
 // PITCHED: rows of the source or the destination are wider than D (a padded layer side);
 // the common case keeps the plain row arithmetic.
 template <int E, bool SCATTER, typename IdxT, bool PITCHED>
-__global__ void __launch_bounds__((kPermWarps + 1) * 32) perm_rows_kernel(
+__global__ void __launch_bounds__((kPermWarps + 1) * 32, 3) perm_rows_kernel(
     const uint8_t* __restrict__ X, long long N, int D, const int32_t* __restrict__ perm,
     uint8_t* __restrict__ Y, const int32_t* __restrict__ src_rows, const float* __restrict__ scale,
     float* __restrict__ scale_out, long long src_pitch, long long dst_pitch, int G, int S,
@@ -328,6 +347,7 @@ __global__ void __launch_bounds__((kPermWarps + 1) * 32) perm_rows_kernel(
   uint8_t* ring = smem_raw + idx_bytes;  // [ngrp][S] rows
   uint64_t* full = reinterpret_cast<uint64_t*>(ring + (size_t)ngrp * S * row_bytes);
   uint64_t* empty = full + ngrp * S;
+  uint64_t* idx_go = empty + ngrp * S;  // every consumer warp's first index loads are issued
   const int warp = threadIdx.x >> 5;
   // group gr of this CTA owns rows first + gr + it * stride, it < rows_of(gr); rows per group
   // fit 32 bits (N < 2^31), so the loops below count in 32 bits and never divide
@@ -345,12 +365,17 @@ __global__ void __launch_bounds__((kPermWarps + 1) * 32) perm_rows_kernel(
       mbar_init(&full[k], 1);
       mbar_init(&empty[k], 1);
     }
+    mbar_init(idx_go, kPermWarps);
     fence_mbar_init();
   }
   __syncthreads();
   pdl_wait();
   if (threadIdx.x == 0) trace_stamp(trace, trace_cap, 1);  // slot 1: predecessor done
 
+  // The index is read with every consumer thread's first round of loads in flight at once,
+  // and those loads are issued before the row copies, so that the index (needed before any
+  // row can be permuted) does not queue behind the rows in the memory system.
+  const bool idx_vec = ((reinterpret_cast<uintptr_t>(perm) & 15u) == 0) && (D & 3) == 0;
   if (warp == kPermWarps) {
     // producer: one thread streams every group's rows, round robin over the groups so the
     // first rows of all groups land first; a slot is refilled once its group released it
@@ -363,7 +388,7 @@ __global__ void __launch_bounds__((kPermWarps + 1) * 32) perm_rows_kernel(
         issued[gr] = 0;
         most = nr[gr] > most ? nr[gr] : most;
       }
-      bool ok = true;
+      bool ok = mbar_wait_bounded(idx_go, 0, err, limit_ns, kSite + __LINE__);
       int k = 0, round = 0;
       for (int it = 0; ok && it < most; ++it) {
 #pragma unroll
@@ -399,11 +424,52 @@ __global__ void __launch_bounds__((kPermWarps + 1) * 32) perm_rows_kernel(
     // consumers: stage the index, then each group of G warps permutes its own rows
     const int g = warp / G;
     const int tig = threadIdx.x - g * G * 32;
-    for (int i = threadIdx.x; i < D; i += kPermWarps * 32) {
-      const int pi = __ldg(perm + i);
-      if (SCATTER) idx[pi] = (IdxT)i;
-      else idx[i] = (IdxT)pi;
+    constexpr int kStride = kPermWarps * 32;
+    // rounds of loads: the trip count is the same for every thread (so warps stay converged
+    // for the barriers below), the bounds are per element
+    auto first_round_issued = [&](int r0) {
+      if (r0 == 0) {
+        __syncwarp();
+        if ((threadIdx.x & 31) == 0) mbar_arrive(idx_go);
+      }
+    };
+    if (idx_vec) {
+      const int nv = D >> 2;
+      const int4* p4 = reinterpret_cast<const int4*>(perm);
+      for (int r0 = 0; r0 == 0 || r0 < nv; r0 += kStride * kIdxRound) {
+        int4 v[kIdxRound];
+#pragma unroll
+        for (int u = 0; u < kIdxRound; ++u) {
+          const int j = r0 + u * kStride + (int)threadIdx.x;
+          if (j < nv) v[u] = __ldg(p4 + j);
+        }
+        first_round_issued(r0);
+#pragma unroll
+        for (int u = 0; u < kIdxRound; ++u) {
+          const int j = r0 + u * kStride + (int)threadIdx.x;
+          if (j < nv) stage_idx4<SCATTER, IdxT>(idx, 4 * j, v[u]);
+        }
+      }
+    } else {
+      for (int r0 = 0; r0 == 0 || r0 < D; r0 += kStride * 4 * kIdxRound) {
+        int v[4 * kIdxRound];
+#pragma unroll
+        for (int u = 0; u < 4 * kIdxRound; ++u) {
+          const int i = r0 + u * kStride + (int)threadIdx.x;
+          if (i < D) v[u] = __ldg(perm + i);
+        }
+        first_round_issued(r0);
+#pragma unroll
+        for (int u = 0; u < 4 * kIdxRound; ++u) {
+          const int i = r0 + u * kStride + (int)threadIdx.x;
+          if (i < D) {
+            if (SCATTER) idx[v[u]] = (IdxT)i;
+            else idx[i] = (IdxT)v[u];
+          }
+        }
+      }
     }
+    __syncwarp();
     asm volatile("bar.sync %0, %1;" ::"r"(kPermWarps + 1), "r"(kPermWarps * 32) : "memory");
     if (threadIdx.x == 0) trace_stamp(trace, trace_cap, 3);  // slot 3: index staged
     const int nrows = rows_of(g);
@@ -511,7 +577,8 @@ static poetx_status launch_perm_rows_t(const void* X, long long N, int D, const 
   const size_t idx_bytes = ((size_t)D * sizeof(IdxT) + 127) & ~(size_t)127;
   int G = 0, S = 0;
   size_t smem = 0;
-  if (!(side ? perm_shape_side : perm_shape)(row_bytes, idx_bytes, &G, &S, &smem))
+  // (the index, and 16 bytes for the barrier that starts the row copies)
+  if (!(side ? perm_shape_side : perm_shape)(row_bytes, idx_bytes + 16, &G, &S, &smem))
     return POETX_ERR_SHAPE;
   auto k = perm_rows_kernel<E, SCATTER, IdxT, PITCHED>;
   static std::once_flag once;  // the opt-in limit is set once, to the largest size used
@@ -600,7 +667,8 @@ bool perm_side_fits(size_t esize, int D) {
   const size_t idx = ((size_t)D * (D <= 65535 ? 2 : 4) + 127) & ~(size_t)127;
   int G = 0, S = 0;
   size_t smem = 0;
-  return ((size_t)D * esize) % 16 == 0 && perm_shape_side((size_t)D * esize, idx, &G, &S, &smem);
+  return ((size_t)D * esize) % 16 == 0 &&
+         perm_shape_side((size_t)D * esize, idx + 16, &G, &S, &smem);
 }
 
 poetx_status launch_perm_rows_side(size_t esize, bool scatter, const void* X, long long N, int D,
