@@ -165,11 +165,10 @@ poetx_status poetx_cnp_bwd(const float* q, const float* dG, int splits, int nblk
  * set-up.  No counterpart in the paper: it computes exactly what poetx_cnp_fwd computes, with
  * the same kernels, and takes the same arguments minus the workspace.
  *   Scratch: a fixed 16 MiB fp32 array in the library's device image; every GPU that loads
- *   the library holds it until the process exits.  The first call on a device looks up the
- *   array's device address (cudaGetSymbolAddress, with that device current) and keeps it;
- *   make that first call before any stream capture.  A cudaDeviceReset reloads the device
- *   image, after which the kept address is stale: do not call this entry point again in a
- *   process that has reset the device.  All calls on a device share the array and it keeps the
+ *   the library holds it until the process exits.  Every call looks up the array's device
+ *   address in the current context (cudaGetSymbolAddress), so a cudaDeviceReset, which loads
+ *   the device image again, is followed; make the first call on a device before any stream
+ *   capture (it may load the image).  All calls on a device share the array and it keeps the
  *   last call's contents: calls that overlap on the GPU (on streams not ordered with each
  *   other) race and give wrong results, so order them.  Nothing in it needs to start at zero:
  *   every element read is first written by the same call.

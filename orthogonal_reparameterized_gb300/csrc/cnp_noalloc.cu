@@ -10,9 +10,8 @@
 //
 // The array is module-scope device memory: every GPU that loads the library holds it until
 // the process exits, and every call on a device shares it.  Its host-side name is only a
-// stand-in for the device address, so the address is looked up once per device with
-// cudaGetSymbolAddress (the first call on a device does it, with that device current).
-#include <mutex>
+// stand-in for the device address, so each call looks the address up with
+// cudaGetSymbolAddress in the current context.
 
 #include "common.cuh"
 #include "kernels.h"
@@ -23,20 +22,16 @@ namespace {
 // Q and Q^2 of up to POETX_CNP_NOALLOC_MAX_ELEMS elements each (nblk * b * b), fp32.
 static __device__ __align__(256) float g_cnp_scratch[2 * POETX_CNP_NOALLOC_MAX_ELEMS];
 
-std::mutex g_mu;
-float* g_scratch_ptr[64];
-
-// Device address of g_cnp_scratch for the current device (nullptr on failure).
+// Device address of g_cnp_scratch in the current context (nullptr on failure).  Looked up on
+// every call, not cached: after a device reset the module is loaded again and the array may
+// sit at another address.
 float* scratch_for_current_device() {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  std::lock_guard<std::mutex> lk(g_mu);
-  if (!g_scratch_ptr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_cnp_scratch) != cudaSuccess || !p) return nullptr;
-    g_scratch_ptr[dev] = static_cast<float*>(p);
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_cnp_scratch) != cudaSuccess || !p) {
+    cudaGetLastError();
+    return nullptr;
   }
-  return g_scratch_ptr[dev];
+  return static_cast<float*>(p);
 }
 
 }  // namespace
