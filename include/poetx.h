@@ -190,7 +190,9 @@ poetx_status poetx_triu_grad_pack(const float* Qbar, int nblk, int b, float* dq,
  * ------------------------------------------------------------------------------------- */
 
 /* Y[t, i] = X[t, perm[i]] for t < N, i < D.  dt: POETX_F32, POETX_BF16 or POETX_I8.
- * X and Y must not overlap.  D * sizeof(dt) must be a multiple of 16. */
+ * X and Y must not overlap.  D * sizeof(dt) must be a multiple of 16, and the staged index
+ * (2 bytes per column) with one row must fit an SM's shared memory: D <= 37528 (fp32),
+ * 56304 (bf16), 65520 (int8); wider rows return POETX_ERR_SHAPE before any launch. */
 poetx_status poetx_perm_gather(poetx_dtype dt, const void* X, int N, int D,
                                const int32_t* perm, void* Y, cudaStream_t stream);
 

@@ -625,12 +625,10 @@ static poetx_status launch_perm_rows_e(bool scatter, const void* X, long long N,
 #define POETX_PERM_T(SC, IT, PI) \
   launch_perm_rows_t<E, SC, IT, PI>(X, N, D, perm, Y, src_rows, scale, scale_out, sp, dp, side, s)
   const bool pitched = sp != D || dp != D;
-  if (D <= 65535) {
-    if (pitched) return scatter ? POETX_PERM_T(true, uint16_t, true) : POETX_PERM_T(false, uint16_t, true);
-    return scatter ? POETX_PERM_T(true, uint16_t, false) : POETX_PERM_T(false, uint16_t, false);
-  }
-  if (pitched) return scatter ? POETX_PERM_T(true, uint32_t, true) : POETX_PERM_T(false, uint32_t, true);
-  return scatter ? POETX_PERM_T(true, uint32_t, false) : POETX_PERM_T(false, uint32_t, false);
+  // (a 16-bit index covers every width whose index and one row fit an SM's shared memory)
+  if (D > 65535) return POETX_ERR_SHAPE;
+  if (pitched) return scatter ? POETX_PERM_T(true, uint16_t, true) : POETX_PERM_T(false, uint16_t, true);
+  return scatter ? POETX_PERM_T(true, uint16_t, false) : POETX_PERM_T(false, uint16_t, false);
 #undef POETX_PERM_T
 }
 
@@ -664,7 +662,8 @@ poetx_status launch_perm_rows(size_t esize, bool scatter, const void* X, long lo
 }
 
 bool perm_side_fits(size_t esize, int D) {
-  const size_t idx = ((size_t)D * (D <= 65535 ? 2 : 4) + 127) & ~(size_t)127;
+  if (D > 65535) return false;
+  const size_t idx = ((size_t)D * 2 + 127) & ~(size_t)127;
   int G = 0, S = 0;
   size_t smem = 0;
   return ((size_t)D * esize) % 16 == 0 &&

@@ -62,6 +62,48 @@ def test_perm_gather_scatter_bit_exact(P, dtype, N, D):
         np.testing.assert_array_equal(host(Z), host(X), err_msg=name)
 
 
+def _rand_rows(dtype, N, D):
+    if dtype == torch.int8:
+        return torch.randint(-128, 127, (N, D), dtype=torch.int8, device=DEV)
+    return torch.randn(N, D, device=DEV).to(dtype)
+
+
+# the widest rows each element type takes: the staged 2-byte index and one row fill the
+# shared memory of an SM; one 16-byte vector wider is refused on the host, before any launch
+@pytest.mark.parametrize("dtype,D", [(torch.float32, 37528), (torch.bfloat16, 56304),
+                                     (torch.int8, 65520)])
+def test_perm_widest_rows(P, dtype, D):
+    X = _rand_rows(dtype, 3, D)
+    p = RNG.permutation(D)
+    pt = dev(p, torch.int32)
+    Y = torch.empty_like(X)
+    P.poetx_perm_gather(X, pt, Y)
+    np.testing.assert_array_equal(host(Y), O.perm_gather(host(X), p))
+    Z = torch.empty_like(X)
+    P.poetx_perm_scatter(Y, pt, Z)
+    np.testing.assert_array_equal(host(Z), host(X))
+    wide = D + 16 // X.element_size()
+    Xw = _rand_rows(dtype, 3, wide)
+    with pytest.raises(Exception):
+        P.poetx_perm_gather(Xw, dev(np.arange(wide), torch.int32), torch.empty_like(Xw))
+
+
+def test_perm_index_not_16_byte_aligned(P):
+    """An index starting 4 bytes past a 16-byte boundary is staged one element at a time."""
+    N, D = 64, 4096
+    p = RNG.permutation(D)
+    buf = dev(np.r_[0, p], torch.int32)
+    pt = buf[1:]
+    assert pt.data_ptr() % 16 == 4
+    X = _rand_rows(torch.bfloat16, N, D)
+    Y = torch.empty_like(X)
+    P.poetx_perm_gather(X, pt, Y)
+    np.testing.assert_array_equal(host(Y), O.perm_gather(host(X), p))
+    Z = torch.empty_like(X)
+    P.poetx_perm_scatter(X, pt, Z)
+    np.testing.assert_array_equal(host(Z), O.perm_scatter(host(X), p))
+
+
 def test_perm_empty(P):
     X = torch.empty(0, 64, dtype=torch.bfloat16, device=DEV)
     P.poetx_perm_gather(X, dev(np.arange(64), torch.int32), torch.empty_like(X))
