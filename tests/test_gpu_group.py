@@ -106,6 +106,9 @@ GROUPS = {
                      (264, 256, "bf16", "fast")], 128, 97),
     "block_b256": ([(512, 512, "bf16", "fast")] * 2 + [(512, 1024, "bf16", "fast"),
                                                       (1024, 512, "bf16", "fast")], 256, 300),
+    # a ragged bf16 first layer and an int8 layer, 700 tokens
+    "mixed_ragged_b128": ([(200, 264, "bf16", "fast"), (256, 512, "bf16", "mem"),
+                    (384, 256, "i8", "mem")], 128, 700),
 }
 
 
@@ -171,7 +174,7 @@ def test_group_argument_errors(P):
     assert P.poetx_group_saved_bytes(mixed, 8) == 0
 
 
-@pytest.mark.parametrize("name", ["mixed_b128", "ragged_b128"])
+@pytest.mark.parametrize("name", ["mixed_b128", "ragged_b128", "block_b256", "mixed_ragged_b128"])
 def test_group_step_host_equals_device_calls(P, name):
     """The host-buffer group step (uploads and downloads beside the kernels) gives the same
     bits as the device group calls, and N = 0 gives zero gradients."""
