@@ -236,13 +236,14 @@ poetx_status launch_triu_grad_pack(const float* Qbar, int nblk, int b, float* dq
 
 // ---------------------------------------------------------------- row permutations
 // Every row is permuted on its own: out[i] = row[idx[i]], with idx = perm for a gather and
-// its inverse (idx[perm[i]] = i) for a scatter, staged once per CTA in shared memory.  The
-// CTA's eight warps form 8/G independent groups of G warps (G = 1 when rows are short): a
-// group owns the rows r = group, + groups in the grid, ..., streams them into its own ring of
-// S row buffers by one-dimensional TMA bulk copies (S rows ahead) and writes 16-byte vectors
-// of each output row, so loads and stores are fully coalesced and no barrier wider than the
-// group ever stalls the other groups.  `src_rows` (nullable) remaps the source row (the
-// merge W'[r, :] = W0[perm_n[r], perm_m]).  Waits are bounded; on expiry the kernel records
+// its inverse (idx[perm[i]] = i) for a scatter, staged once per CTA in shared memory as
+// 16-bit entries.  The CTA's eight consumer warps form 8/G independent groups of G >= 2 warps
+// (wider groups for longer rows): a group owns the rows r = group, + groups in the grid, ...,
+// which a ninth (producer) warp streams into the group's own ring of S row buffers by
+// one-dimensional TMA bulk copies (S rows ahead); the group writes 16-byte vectors of each
+// output row, so loads and stores are fully coalesced and no barrier wider than the group
+// ever stalls the other groups.  `src_rows` (nullable) remaps the source row (the merge
+// W'[r, :] = W0[perm_n[r], perm_m]).  Waits are bounded; on expiry the kernel records
 // POETX_ERR_TIMEOUT, drains the copies it issued and returns.
 template <int E>
 struct VecT;
