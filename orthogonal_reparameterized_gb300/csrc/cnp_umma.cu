@@ -78,6 +78,11 @@ struct CnpUParams {
   size_t trace_cap;
   int* err;
   unsigned long long limit_ns;
+  // 1: the product is symmetric (b a multiple of 128): only the tiles whose 128-column block
+  // is on or right of their 128-row block run (blockIdx.x enumerates them row by row), and
+  // each one right of the diagonal also writes its transpose into out_f32, so every element
+  // below a diagonal 128 x 128 block is the copy of its mirror whatever the tile width
+  int sym;
 };
 
 __host__ __device__ constexpr uint32_t tf32_idesc(int M, int N) {
@@ -235,7 +240,20 @@ __global__ void __launch_bounds__(cnp_threads(BN), 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int mt = blockIdx.x, nt = blockIdx.y, blk = blockIdx.z;
+  const int blk = blockIdx.z;
+  constexpr int R = BM / BN;  // tiles per 128-column block
+  int mt = blockIdx.x, nt = blockIdx.y;
+  if (p.sym) {  // row mt holds the tiles nt = R mt .. b / BN - 1
+    const int MT = p.b / BM, NT = p.b / BN;
+    int idx = blockIdx.x;
+    mt = 0;
+    while (mt < MT - 1 && idx >= NT - mt * R) {
+      idx -= NT - mt * R;
+      ++mt;
+    }
+    nt = mt * R + idx;
+  }
+  const bool mirror_tile = p.sym && nt / R != mt;
   const unsigned long long lin = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
   auto stamp = [&](int slot) {
     if (p.trace) {
@@ -539,7 +557,7 @@ __global__ void __launch_bounds__(cnp_threads(BN), 1)
             make_uint2(pack_bf16x2(o.x, o.y), pack_bf16x2(o.z, o.w));
     }
   }
-  if (p.out_f32_t || p.out_bf16_t) {
+  if (p.out_f32_t || p.out_bf16_t || mirror_tile) {
     __syncthreads();
     if (live) {
       // transposed outputs: consecutive threads take consecutive rows (rows % 32 == 0), so
@@ -552,6 +570,8 @@ __global__ void __launch_bounds__(cnp_threads(BN), 1)
         for (int k = 0; k < 4; ++k) {
           const long long tidx = blk * p.ot_blk + (long long)(j0 + c + k) * p.ot_ld + (i0 + rr);
           if (p.out_f32_t) p.out_f32_t[tidx] = o[k];
+          if (mirror_tile)  // the symmetric partner tile
+            p.out_f32[blk * p.o_blk + (long long)(j0 + c + k) * p.o_ld + (i0 + rr)] = o[k];
           if (p.out_bf16_t) p.out_bf16_t[tidx] = __float2bfloat16_rn(o[k]);
         }
       }
@@ -643,7 +663,9 @@ poetx_status launch_t(const CnpMaps& maps, const CnpUParams& p, int nblk, cudaSt
     attr = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   });
   POETX_CUDA_TRY(attr);
-  dim3 grid((p.M + BM - 1) / BM, p.b / BN, nblk);
+  const int MT = p.b / BM, NT = p.b / BN;
+  dim3 grid(p.sym ? MT * NT - (BM / BN) * MT * (MT - 1) / 2 : (p.M + BM - 1) / BM,
+            p.sym ? 1 : p.b / BN, nblk);
   POETX_CUDA_TRY(launch_pdl(k, grid, dim3(cnp_threads(BN)), smem, s, maps, p));
   POETX_CUDA_TRY(cudaGetLastError());
   return POETX_OK;
@@ -726,6 +748,8 @@ poetx_status cnp_umma_product(const CnpProduct& g, int nblk, cudaStream_t s) {
   p.limit_ns = kWaitLimitNs;
   p.trace = trace_buffer(&p.trace_cap);
   p.nmaps = nmaps;
+  p.sym = g.mirror && g.b % BM == 0 && !g.a_mat && g.out_f32 && !g.out_f32_t && !g.out_bf16 &&
+          !g.out_bf16_t;
   if (BN == 128) return launch_t<128>(maps, p, nblk, s);
   if (BN == 64) return launch_t<64>(maps, p, nblk, s);
   return launch_t<32>(maps, p, nblk, s);
