@@ -9,7 +9,8 @@
 // Each CNP product (POET-X summary page, "Core method" section 4, eq. 9 and its gradient)
 // is C_j = sum_seg opA_seg(j) . opB_seg(j) + epilogue, for every block j, where each operand
 // is a linear combination of at most two b x b fp32 arrays (Q, Q^2, X, M1).  One CTA makes
-// one 128 x BN output tile of one block:
+// one 128 x BN output tile of one block (of a symmetric product such as Q^2, only the tiles on
+// and right of each diagonal 128 x 128 block, the ones right of it also storing their mirror):
 //   warp 0      TMA: the raw fp32 tiles of every source array of the current K block
 //   warps 2-9   form v = c0*src0 + c1*src1 and split it into hi(v), lo(v): the A operand
 //               straight into tensor memory (where the MMA reads it), the B operand in place
