@@ -9,8 +9,10 @@
 //
 // One work unit is (block j, token split s, half h of the block's 128-wide column halves,
 // b = 128 or 256).  Its CTA streams the split's token tiles:
-//   warp 0      TMA: per tile, the b/64 sub-tiles [128 tokens x 64 features] of T into an
-//               8-deep ring and the half's two S sub-tiles into one of two S slots
+//   warp 0      TMA: per tile, the b/64 sub-tiles [128 tokens x 64 features] of T as one 3-D
+//               box into one of the 8 / (b/64) slots of a 128 KB ring, and the half's two S
+//               sub-tiles as one box into one of two S slots (a single thread issuing tiled
+//               copies moves ~50 GB/s into its SM with 16 KB boxes, ~75 with 64 KB boxes)
 //   warp 1      MMA issuer, per tile:
 //                 dG_h (+)= S_h^T T        M = 128 (S features), N = b, K = 128 tokens;
 //                                          both operands MN-major straight from the tiles
@@ -40,7 +42,7 @@ constexpr int kSite = 5 * 10000;
 namespace {
 
 constexpr int BDW_TOK = 128;                          // tokens per tile
-constexpr int BDW_T_STAGES = 8;                       // T ring (a multiple of b / 64)
+constexpr int BDW_T_STAGES = 8;                       // T ring in sub-tiles (a multiple of b / 64)
 constexpr uint32_t BDW_SUB = 128 * 64 * 2;            // one sub-tile: 16 KB
 constexpr uint32_t BDW_S_SLOT = 2 * BDW_SUB;          // the half's 128 features of S
 constexpr int BDW_EPIW = 8;
@@ -52,6 +54,16 @@ constexpr uint32_t BDW_BAR_OFF = BDW_STG_OFF + BDW_EPIW * BDW_STG;
 constexpr int BDW_SMEM = BDW_BAR_OFF + 256 + 1024;    // + barriers + alignment slack
 static_assert(BDW_SMEM <= 227 * 1024, "fused block-diagonal backward: shared memory");
 constexpr uint32_t G_COL = 0, Y_COL = 128, DG_COL = 256;
+
+// Load a 3-D box into this CTA's shared memory, completing on `bar`.
+__device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* map, uint64_t* bar,
+                                            int c0, int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
 
 struct BdwParams {
   int b, halves, nblk, splits, chunk_tiles, ntiles, num_units;
@@ -87,8 +99,8 @@ __global__ void __launch_bounds__(BDW_THREADS, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + BDW_BAR_OFF);
-  uint64_t* tfull = bars;                   // [8] T sub-tile landed
-  uint64_t* tempty = bars + 8;              // [8] T sub-tile read by its MMAs
+  uint64_t* tfull = bars;                   // [8 / TS] T tile slot landed
+  uint64_t* tempty = bars + 8;              // [8 / TS] T tile slot read by its MMAs
   uint64_t* sfull = bars + 16;              // [2]
   uint64_t* sempty = bars + 18;             // [2]
   uint64_t* yfull = bars + 20;              // Y accumulator holds a tile
@@ -103,6 +115,7 @@ __global__ void __launch_bounds__(BDW_THREADS, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int TS = p.b / 64;  // T sub-tiles per token tile
+  const int NSLOT = BDW_T_STAGES / TS;  // T tile slots
   if (threadIdx.x == 0) trace_stamp(p.trace, p.trace_cap, 0);
   pdl_trigger();
   if (warp == 0 && lane == 0) {
@@ -149,41 +162,30 @@ __global__ void __launch_bounds__(BDW_THREADS, 1)
       for (int i = 0; i < w.nt; ++i, ++gt) {
         const int row = (w.t0 + i) * BDW_TOK;
         const int slot = (int)(gt & 1);
+        const int ts = (int)(gt % NSLOT);
         if (*abort_flag ||
             !mbar_wait_bounded(&sempty[slot], (uint32_t)(((gt >> 1) & 1) ^ 1), p.err, p.limit_ns,
-                               kSite + __LINE__)) {
+                               kSite + __LINE__) ||
+            !mbar_wait_bounded(&tempty[ts], (uint32_t)(((gt / NSLOT) & 1) ^ 1), p.err,
+                               p.limit_ns, kSite + __LINE__)) {
           *abort_flag = 1;
           ok = false;
           break;
         }
         if (gt == 0) trace_stamp(p.trace, p.trace_cap, 2);  // slot 2: first load issued
+        // S: the half's 128 features (2 groups of 64); T: the block's b / 64 groups
         mbar_arrive_expect_tx(&sfull[slot], BDW_S_SLOT);
-        uint8_t* sd = smem + BDW_S_OFF + slot * BDW_S_SLOT;
-        const int scol = w.j * p.b + w.h * 128;
-        tma_load_2d(sd, &tmS, &sfull[slot], scol, row);
-        tma_load_2d(sd + BDW_SUB, &tmS, &sfull[slot], scol + 64, row);
-        for (int v = 0; v < TS; ++v) {
-          const long long q = gt * TS + v;
-          const int st = (int)(q % BDW_T_STAGES);
-          if (*abort_flag ||
-              !mbar_wait_bounded(&tempty[st], (uint32_t)(((q / BDW_T_STAGES) & 1) ^ 1), p.err,
-                                 p.limit_ns, kSite + __LINE__)) {
-            *abort_flag = 1;
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(&tfull[st], BDW_SUB);
-          tma_load_2d(smem + st * BDW_SUB, &tmT, &tfull[st], w.j * p.b + 64 * v, row);
-        }
-        if (!ok) break;
+        tma_load_3d(smem + BDW_S_OFF + slot * BDW_S_SLOT, &tmS, &sfull[slot], 0, row,
+                    w.j * TS + 2 * w.h);
+        mbar_arrive_expect_tx(&tfull[ts], (uint32_t)TS * BDW_SUB);
+        tma_load_3d(smem + (size_t)ts * TS * BDW_SUB, &tmT, &tfull[ts], 0, row, w.j * TS);
       }
     }
     // Loads still landing (only after an abort) must complete before the CTA exits: wait for
-    // the last load issued into every stage and slot.
-    const long long nq = gt * TS;
-    for (long long q = nq - 1; q >= 0 && q >= nq - BDW_T_STAGES; --q)
-      mbar_wait_bounded(&tfull[q % BDW_T_STAGES], (uint32_t)((q / BDW_T_STAGES) & 1), p.err,
-                        p.limit_ns, kSite + __LINE__);
+    // the last load issued into every slot.
+    for (long long g = gt - 1; g >= 0 && g >= gt - NSLOT; --g)
+      mbar_wait_bounded(&tfull[g % NSLOT], (uint32_t)((g / NSLOT) & 1), p.err, p.limit_ns,
+                        kSite + __LINE__);
     for (long long g = gt - 1; g >= 0 && g >= gt - 2; --g)
       mbar_wait_bounded(&sfull[g & 1], (uint32_t)((g >> 1) & 1), p.err, p.limit_ns,
                         kSite + __LINE__);
@@ -208,11 +210,8 @@ __global__ void __launch_bounds__(BDW_THREADS, 1)
         const int slot = (int)(gt & 1);
         bool got = !*abort_flag && mbar_wait_bounded(&sfull[slot], (uint32_t)((gt >> 1) & 1),
                                                      p.err, p.limit_ns, kSite + __LINE__);
-        for (int v = 0; v < TS && got; ++v) {
-          const long long q = gt * TS + v;
-          got = mbar_wait_bounded(&tfull[q % BDW_T_STAGES], (uint32_t)((q / BDW_T_STAGES) & 1),
-                                  p.err, p.limit_ns, kSite + __LINE__);
-        }
+        got = got && mbar_wait_bounded(&tfull[gt % NSLOT], (uint32_t)((gt / NSLOT) & 1), p.err,
+                                       p.limit_ns, kSite + __LINE__);
         if (!got) {
           *abort_flag = 1;
           ok = false;
@@ -244,7 +243,7 @@ __global__ void __launch_bounds__(BDW_THREADS, 1)
             umma_bf16_ta(tmem_base + Y_COL, tmem_base + G_COL + 32 * v + 8 * kk,
                          make_sdesc(tb + v * BDW_SUB + kk * 32, 16, 1024), idesc_y,
                          (v | kk) != 0);
-        for (int v = 0; v < TS; ++v) umma_commit(&tempty[(gt * TS + v) % BDW_T_STAGES]);
+        umma_commit(&tempty[gt % NSLOT]);
         umma_commit(&sempty[slot]);
         umma_commit(yfull);
       }
@@ -397,6 +396,36 @@ __global__ void __launch_bounds__(BDW_THREADS, 1)
 
 bool umma_bdw_ok(int b) { return (b == 128 || b == 256) && umma_supported(); }
 
+typedef CUresult (*EncodeTiledFn3)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// A bf16 [N, D] row-major tensor as the 3-D view {64 features, N tokens, D / 64 feature groups}
+// (strides: the row pitch, 128 bytes), boxes of 64 features x 128 tokens x `groups` groups with
+// 128-byte swizzle: a box lands as `groups` consecutive [128 x 64] sub-tiles of 16 KB.
+static bool encode_groups_3d(CUtensorMap* m, const void* ptr, long long N, long long D,
+                             int groups) {
+  static EncodeTiledFn3 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn3>(f);
+  });
+  if (!fn || D % 64) return false;
+  cuuint64_t dims[3] = {64, (cuuint64_t)N, (cuuint64_t)(D / 64)};
+  cuuint64_t strides[2] = {(cuuint64_t)D * 2, 128};
+  cuuint32_t box[3] = {64, (cuuint32_t)BDW_TOK, (cuuint32_t)groups};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int bdw_splits(long long N, int nblk, int b) {
   // the split count that puts the fewest token tiles on the busiest SM (ties: fewer splits,
   // i.e. fewer partials for the CNP backward to sum)
@@ -429,8 +458,7 @@ poetx_status umma_bdw(const void* T, const void* S, long long N, int nblk, int b
   }
   const long long D = (long long)nblk * b;
   CUtensorMap tT, tS, tY, tD;
-  if (!encode_tma_2d(&tT, T, TMA_BF16, D, N, D, 64, BDW_TOK, true) ||
-      !encode_tma_2d(&tS, S, TMA_BF16, D, N, D, 64, BDW_TOK, true) ||
+  if (!encode_groups_3d(&tT, T, N, D, b / 64) || !encode_groups_3d(&tS, S, N, D, 2) ||
       !encode_tma_2d(&tY, Y, TMA_BF16, D, N, D, 32, 32, false) ||
       !encode_tma_2d(&tD, dG, TMA_F32, b, (uint64_t)splits * nblk * b, b, 32, 32, true))
     return POETX_ERR_CUDA;
